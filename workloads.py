@@ -1,0 +1,141 @@
+"""Seeded synthetic inputs for decode-phase attention.
+
+This module only draws numbers: it holds no step of the attention method.
+The test suite and the benchmark use it to feed the same bytes to the CUDA
+library and to the CPU oracle (the oracle receives copies of the exact
+fp16/bf16 tensors the GPU reads; neither side regenerates them).
+
+Layout of one batch (the library's and the oracle's layout):
+  q   [batch, hq, d]
+  k,v request b occupies a [hkv, L_b, d] slab at element offset hkv*cu[b]*d,
+      L_b = cu[b+1] - cu[b]; with equal lengths this is [batch, hkv, L, d].
+  cu  int32 [batch+1], cu[0] = 0, the running sum of the context lengths.
+
+The named workloads are the decode shapes the LeanAttention evaluation
+sweeps (context length, batch, head count, head dim, ragged batches and
+grouped-query heads); the pages' own model runs and 500-sample sweep need
+trained weights and are replaced by these i.i.d. N(0, 1) inputs.
+"""
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+
+@dataclass
+class Workload:
+    name: str
+    batch: int
+    hq: int
+    hkv: int
+    d: int
+    dtype: str  # "f16" or "bf16"
+    lengths: list = field(default_factory=list)
+    grid: int = 0  # 0: the library's default (one persistent CTA per SM)
+    outlier_frac: float = 0.0  # fraction of key rows multiplied by outlier_scale
+    outlier_scale: float = 8.0
+    description: str = ""
+
+    @property
+    def scale(self):
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def cu(self):
+        return np.concatenate([[0], np.cumsum(self.lengths)]).astype(np.int32)
+
+    @property
+    def total_tokens(self):
+        return int(sum(self.lengths))
+
+    def kv_bytes(self):
+        """Bytes of K plus V the attention must read once."""
+        return 2 * self.hkv * self.d * 2 * self.total_tokens
+
+
+def _seed(*parts):
+    """A 63-bit seed from integer parts (splitmix-style mixing, plain integers)."""
+    x = 0x9E3779B97F4A7C15
+    for p in parts:
+        x = (x ^ (int(p) & 0xFFFFFFFFFFFFFFFF)) * 0xBF58476D1CE4E5B9 & 0xFFFFFFFFFFFFFFFF
+        x ^= x >> 31
+    return x & 0x7FFFFFFFFFFFFFFF
+
+
+def ragged_lengths(n, lo, hi, seed, log_uniform):
+    rng = np.random.default_rng(_seed(seed, 0x1E9, n, lo, hi, int(log_uniform)))
+    if log_uniform:
+        x = np.exp(rng.uniform(math.log(lo), math.log(hi), size=n))
+        return [int(min(hi, max(lo, math.floor(v)))) for v in x]
+    return [int(v) for v in rng.integers(lo, hi + 1, size=n)]
+
+
+def named(name, seed=0):
+    """The benchmark and parity workloads, by name."""
+    if name == "tiny":
+        return Workload(name, 1, 4, 4, 64, "f16", [1024], grid=3,
+                        description="tiny exact check: batch 1, 4/4 heads, d 64, ctx 1024, "
+                                    "fp16, grid forced to 3 CTAs")
+    if name == "uniform":
+        return Workload(name, 8, 32, 32, 128, "bf16", [8192] * 8,
+                        description="uniform decode batch: batch 8, 32/32 heads, d 128, "
+                                    "ctx 8192 per request, bf16")
+    if name.startswith("long"):
+        ctx = {"long64k": 65536, "long256k": 262144, "long512k": 524288}[name]
+        return Workload(name, 1, 32, 32, 128, "f16", [ctx],
+                        description=f"long context: batch 1, 32/32 heads, d 128, ctx {ctx}, fp16")
+    if name == "ragged":
+        lens = ragged_lengths(16, 1024, 131072, seed, log_uniform=True)
+        return Workload(name, 16, 32, 32, 128, "bf16", lens,
+                        description="ragged batch: 16 requests, 32/32 heads, d 128, ctx "
+                                    "log-uniform in [1024, 131072], bf16")
+    if name == "gqa":
+        lens = ragged_lengths(8, 16384, 65536, seed, log_uniform=False)
+        return Workload(name, 8, 64, 8, 64, "bf16", lens, outlier_frac=0.01,
+                        description="GQA small-head: batch 8, 64 query over 8 kv heads, d 64, "
+                                    "ctx uniform in [16384, 65536], bf16, 1% of keys x8")
+    raise KeyError(name)
+
+
+NAMES = ["tiny", "uniform", "long64k", "long256k", "long512k", "ragged", "gqa"]
+
+
+def make_inputs(w, seed=0, device="cpu"):
+    """Draw q, k, v for a workload; returns (q, k, v, cu_host_np).
+
+    Each (request, kv head) slab of K and V is drawn from its own generator
+    seeded by (seed, slab, tensor), N(0, 1) in float32, then rounded to the
+    workload's dtype (round to nearest even). For the grouped-query workload
+    a seeded 1% of key rows is multiplied by 8 before rounding (a power of
+    two, so the rounding is unchanged).
+    """
+    import torch
+
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[w.dtype]
+    dev = torch.device(device)
+    cu = w.cu
+    gen = torch.Generator(device=dev)
+
+    gen.manual_seed(_seed(seed, 0xA11, 0))
+    q = torch.randn(w.batch, w.hq, w.d, generator=gen, device=dev, dtype=torch.float32).to(tdt)
+    n_kv = w.hkv * w.total_tokens * w.d
+    k = torch.empty(n_kv, dtype=tdt, device=dev)
+    v = torch.empty(n_kv, dtype=tdt, device=dev)
+    for b in range(w.batch):
+        L = int(cu[b + 1] - cu[b])
+        for h in range(w.hkv):
+            off = (w.hkv * int(cu[b]) + h * L) * w.d
+            for which, dst in ((1, k), (2, v)):
+                gen.manual_seed(_seed(seed, b, h, which))
+                x = torch.randn(L, w.d, generator=gen, device=dev, dtype=torch.float32)
+                if which == 1 and w.outlier_frac > 0:
+                    gen.manual_seed(_seed(seed, b, h, 3))
+                    rows = torch.rand(L, generator=gen, device=dev) < w.outlier_frac
+                    x[rows] *= w.outlier_scale
+                dst[off:off + L * w.d] = x.reshape(-1).to(tdt)
+    return q, k, v, cu
+
+
+def custom(batch, hq, hkv, d, dtype, lengths, grid=0, name="custom"):
+    return Workload(name, batch, hq, hkv, d, dtype, list(lengths), grid=grid,
+                    description=f"{name}: batch {batch}, {hq}/{hkv} heads, d {d}, {dtype}")
