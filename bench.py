@@ -1,0 +1,402 @@
+"""Benchmark: LeanAttention stream-K decode attention on GB300.
+
+One step is one decode-attention call over one batch: the LeanTile loop,
+the partial exchange, the host-CTA reduction and the normalisation, all in
+one launch of the library's kernel (the schedule is planned once for the
+batch, outside the timed region; its host time is reported as plan_us).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--kernel lean|naive|fixed_split] [--impl ours|reference]
+
+value = K+V bytes read / kernel time, summed over ranks (GB/s); the kernel
+time is taken with CUDA events on the launching stream, L2 flushed (a
+256 MiB write) before every timed call. e2e = the same metric with the
+inputs copied from pinned host memory and the output copied back inside
+every timed step. --impl reference times the float64 CPU oracle instead.
+Under torchrun every rank runs an independent replica (the path has no
+cross-GPU exchange) and the slowest rank's time is reported.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention µs/call and KV-read GB/s as % of GB300 HBM peak, 1 GPU"
+FLUSH_BYTES = 256 << 20
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="uniform")
+    ap.add_argument("--kernel", default="lean", choices=["lean", "naive", "fixed_split"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--grid", type=int, default=0, help="stream-K grid; 0 = one CTA per SM")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_phase_attention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it is for this kernel source."""
+    path = os.path.join(ROOT, "profiles", f"lean_decode_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not src or not tr or src.group(1) != kernel_source_digest():
+        return None
+    return int(tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return None
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.06]
+        used = inside if inside else rows
+        if not used:
+            return None
+        mhz = sorted(float(p[2]) for _, p in used if p[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, p in used:
+            for n, val in zip(names, p[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": mhz[len(mhz) // 2] if mhz else None,
+                "sm_max_mhz": float(used[0][1][3]) if used[0][1][3].replace(".", "").isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(used),
+                "in_timed_region": bool(inside)}
+
+
+def algorithmic_bytes(w, grid, kernel):
+    """Bytes a launch must move: K+V once, q, out, and the partial records."""
+    kv = w.kv_bytes()
+    q = w.batch * w.hq * w.d * 2
+    out = w.batch * w.hq * w.d * 4
+    grp = w.hq // w.hkv
+    rec = grp * (w.d + 2) * 4
+    ws = 2 * grid * rec if kernel != "naive" else 0  # written once, read once
+    return kv, kv + q + out + ws
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    import workloads
+
+    w = workloads.named(args.workload, seed=args.seed)
+    q, k, v, cu = workloads.make_inputs(w, seed=args.seed, device="cpu")
+    code = {"f16": oracle.F16, "bf16": oracle.BF16}[w.dtype]
+    cores = os.cpu_count() or 1
+    nrows = w.batch * w.hq
+    grp = w.hq // w.hkv
+    row_bytes = np.array([2 * (cu[r // w.hq + 1] - cu[r // w.hq]) * w.d * 2 / grp for r in range(nrows)])
+    per_step = cores
+    qn, kn, vn = (t.view(torch.int16).numpy().view(np.uint16) for t in (q, k, v))
+    pos = 0
+
+    def step():
+        nonlocal pos
+        rows = np.array([(pos + i) % nrows for i in range(per_step)], dtype=np.int64)
+        pos = (pos + per_step) % nrows
+        oracle.attend(qn, kn, vn, cu, w.hq, w.hkv, w.d, w.scale, code, rows=rows, threads=cores)
+        return float(row_bytes[rows].sum())
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    total = 0.0
+    for _ in range(args.steps):
+        total += step()
+    dt = time.perf_counter() - t0
+    gbs = total / dt / 1e9
+    sample = (f"{per_step} (request, head) rows per step, cycling over the {nrows} rows of the "
+              f"workload; float64 two-pass softmax over the exact {w.dtype} inputs")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.description, "seed": args.seed},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, q, k, v, cu, seconds):
+    import numpy as np
+    import torch
+
+    import oracle
+
+    code = {"f16": oracle.F16, "bf16": oracle.BF16}[w.dtype]
+    cores = os.cpu_count() or 1
+    qn, kn, vn = (t.view(torch.int16).numpy().view(np.uint16) for t in (q, k, v))
+    nrows = w.batch * w.hq
+    grp = w.hq // w.hkv
+    row_bytes = np.array([2 * (cu[r // w.hq + 1] - cu[r // w.hq]) * w.d * 2 / grp for r in range(nrows)])
+    # rows in chunks of one per core until the time budget is spent (at least one chunk)
+    t0 = time.perf_counter()
+    done, pos = 0.0, 0
+    while True:
+        rows = np.array([(pos + i) % nrows for i in range(cores)], dtype=np.int64)
+        pos = (pos + cores) % nrows
+        oracle.attend(qn, kn, vn, cu, w.hq, w.hkv, w.d, w.scale, code, rows=rows, threads=cores)
+        done += float(row_bytes[rows].sum())
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{int(round(done / w.kv_bytes() * nrows))} of the workload's {nrows} "
+                      f"(request, head) rows in {dt:.1f} s, one row per core at a time"}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import decode_phase_attention_gb300 as la
+    import workloads
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workloads.named(args.workload, seed=args.seed)
+    q, k, v, cu = workloads.make_inputs(w, seed=args.seed, device=dev)
+    grid = args.grid if args.grid > 0 else (w.grid if args.workload == "tiny" else 0)
+    t_plan = time.perf_counter()
+    if args.kernel == "lean":
+        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev)
+    elif args.kernel == "naive":
+        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, device=dev, fixed_splits=1)
+    else:
+        per_sm, sms = la.la_device_capacity(w.d, w.hq // w.hkv)
+        splits = -(-sms // (w.batch * w.hkv))
+        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, device=dev, fixed_splits=max(1, splits))
+    plan_us = (time.perf_counter() - t_plan) * 1e6
+    G = dec.sched.grid
+    launches_per_call = 2 if (args.kernel == "fixed_split" and dec.sched.grid > w.batch * w.hkv) else 1
+    stream = torch.cuda.current_stream(dev)
+    out = torch.empty(w.batch, w.hq, w.d, dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def call():
+        dec(q, k, v, w.scale, out=out, stream=stream)
+
+    # warm-up (also uploads the schedule)
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(dev)
+    st = dec.status()
+    if st != la.LA_OK:
+        raise RuntimeError(f"kernel reported: {la.status_string(st)}")
+
+    sampler = ClockSampler(local_rank)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.2)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    wall1 = time.time()
+    sampler.stop()
+    times_ms = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))
+    mean_ms = sum(times_ms) / len(times_ms)
+    if world > 1:
+        t = torch.tensor([mean_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    st = dec.status()
+    if st != la.LA_OK:
+        raise RuntimeError(f"kernel reported: {la.status_string(st)}")
+
+    kv_bytes, algo_bytes = algorithmic_bytes(w, G, args.kernel)
+    value = world * kv_bytes / (mean_ms * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        n_e2e = max(1, min(args.e2e_steps, args.steps))
+        for _ in range(2):
+            q.copy_(qh, non_blocking=True), k.copy_(kh, non_blocking=True), v.copy_(vh, non_blocking=True)
+            call()
+            outh.copy_(out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            q.copy_(qh, non_blocking=True)
+            k.copy_(kh, non_blocking=True)
+            v.copy_(vh, non_blocking=True)
+            call()
+            outh.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = (q.numel() + k.numel() + v.numel()) * q.element_size()
+        e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "us_per_call": round(e2e_ms * 1e3, 2), "steps": n_e2e,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * out.element_size()}
+
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    achieved = algo_bytes / (mean_ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(w, q.cpu(), k.cpu(), v.cpu(), cu, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean_ms, 6),
+        "us_per_call": round(mean_ms * 1e3, 3),
+        "kv_read_frac_of_measured_hbm": round(kv_bytes / (mean_ms * 1e-3) / 1e9 / peak, 4),
+        "kv_read_frac_of_8tbs_nominal": round(kv_bytes / (mean_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.description, "kernel": args.kernel, "grid": G,
+                   "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
+                   "total_context_tokens": w.total_tokens, "kv_bytes": kv_bytes,
+                   "l2": "flushed (256 MiB write) before every timed call; K+V also exceed L2",
+                   "plan_us": round(plan_us, 1), "seed": args.seed,
+                   "p10_us": round(times_ms[len(times_ms) // 10] * 1e3, 2),
+                   "p90_us": round(times_ms[(9 * len(times_ms)) // 10] * 1e3, 2)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": "measured hbm_gbs (copy, burst)" if peaks else "fallback 6.8 TB/s",
+                     "traffic": profiled_traffic(args.workload) if args.kernel == "lean" else None,
+                     "algorithmic_bytes_per_launch": algo_bytes},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * launches_per_call,
+        "clocks": sampler.summary(wall0, wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

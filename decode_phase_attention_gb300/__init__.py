@@ -1,0 +1,231 @@
+"""Python binding of the LeanAttention decode library (liblean_attn.so).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library behind the C ABI of include/lean_attn.h, under the same names
+(la_plan, la_plan_fixed, la_workspace_size, la_workspace_init, la_decode,
+la_get_status, la_schedule_export, ...). PyTorch supplies device memory and
+streams. There is no CPU fallback: if the shared library is missing the
+import fails.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblean_attn.so")
+
+LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
+LA_F16, LA_BF16 = 0, 1
+SEG_WHOLE, SEG_NONHOST, SEG_HOST, SEG_PARTIAL = range(4)
+EXPORTED = ["la_plan", "la_plan_fixed", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
+            "la_decode", "la_get_status", "la_schedule_export_size", "la_schedule_export",
+            "la_schedule_set_debug", "la_device_capacity", "la_schedule_destroy",
+            "la_status_string"]
+
+
+class LeanAttentionError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    c_int, c_size, vp, c_float, c_ll = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float, ctypes.c_longlong
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    sig = {
+        "la_plan": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
+        "la_plan_fixed": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
+        "la_schedule_grid": (c_int, [vp]),
+        "la_workspace_size": (c_size, [vp]),
+        "la_workspace_init": (c_int, [vp, c_size, vp]),
+        "la_decode": (c_int, [vp, vp, vp, c_int, vp, vp, vp, vp, c_float, vp]),
+        "la_get_status": (c_int, [vp, vp]),
+        "la_schedule_export_size": (c_size, [vp]),
+        "la_schedule_export": (c_int, [vp, vp, c_size]),
+        "la_schedule_set_debug": (c_int, [vp, c_int, c_ll]),
+        "la_device_capacity": (c_int, [c_int, c_int, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
+        "la_schedule_destroy": (None, [vp]),
+        "la_status_string": (ctypes.c_char_p, [c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def status_string(status):
+    return _lib.la_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status != LA_OK:
+        raise LeanAttentionError(status, what)
+
+
+class Schedule:
+    """Owns an la_schedule; destroyed with the object."""
+
+    def __init__(self, handle, batch, hq, hkv, d, cu):
+        self._h = handle
+        self.batch, self.hq, self.hkv, self.d = batch, hq, hkv, d
+        self.cu = cu
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def grid(self):
+        return _lib.la_schedule_grid(self._h)
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h and _lib is not None:
+            _lib.la_schedule_destroy(h)
+
+
+def _cu_array(cu_seqlens_k):
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens_k, dtype=np.int64))
+    if cu.ndim != 1 or cu.size < 2:
+        raise ValueError("cu_seqlens_k must be 1-D with batch + 1 entries")
+    if cu.min() < 0 or cu.max() > np.iinfo(np.int32).max:
+        raise ValueError("cu_seqlens_k out of int32 range")
+    return np.ascontiguousarray(cu, dtype=np.int32)
+
+
+def la_plan(batch, hq, hkv, d, cu_seqlens_k, num_sms=0):
+    """Stream-K tile planner; num_sms <= 0 uses one CTA per SM of the current device."""
+    cu = _cu_array(cu_seqlens_k)
+    if cu.size != batch + 1:
+        raise ValueError("cu_seqlens_k must have batch + 1 entries")
+    h = ctypes.c_void_p()
+    _check(_lib.la_plan(batch, hq, hkv, d, cu.ctypes.data_as(ctypes.c_void_p), int(num_sms),
+                        ctypes.byref(h)), "la_plan")
+    return Schedule(h.value, batch, hq, hkv, d, cu)
+
+
+def la_plan_fixed(batch, hq, hkv, d, cu_seqlens_k, splits):
+    """Fixed-partition baselines: splits == 1 one CTA per unit, > 1 FlashDecoding-style split."""
+    cu = _cu_array(cu_seqlens_k)
+    if cu.size != batch + 1:
+        raise ValueError("cu_seqlens_k must have batch + 1 entries")
+    h = ctypes.c_void_p()
+    _check(_lib.la_plan_fixed(batch, hq, hkv, d, cu.ctypes.data_as(ctypes.c_void_p), int(splits),
+                              ctypes.byref(h)), "la_plan_fixed")
+    return Schedule(h.value, batch, hq, hkv, d, cu)
+
+
+def la_workspace_size(sched):
+    return int(_lib.la_workspace_size(sched.handle))
+
+
+def la_schedule_export(sched):
+    n = int(_lib.la_schedule_export_size(sched.handle))
+    buf = np.zeros(n, dtype=np.int32)
+    _check(_lib.la_schedule_export(sched.handle, buf.ctypes.data_as(ctypes.c_void_p), n),
+           "la_schedule_export")
+    return buf.tolist()
+
+
+def la_schedule_set_debug(sched, skip_signal_cta=-1, spin_timeout_ns=2_000_000_000):
+    _check(_lib.la_schedule_set_debug(sched.handle, int(skip_signal_cta), int(spin_timeout_ns)),
+           "la_schedule_set_debug")
+
+
+def la_device_capacity(d, grp):
+    per_sm, sms = ctypes.c_int(), ctypes.c_int()
+    _check(_lib.la_device_capacity(d, grp, ctypes.byref(per_sm), ctypes.byref(sms)),
+           "la_device_capacity")
+    return per_sm.value, sms.value
+
+
+# ---------------------------------------------------------------- torch side
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def new_workspace(sched, device=None):
+    """A zeroed device workspace (uint8 tensor, 256-byte aligned) for a schedule."""
+    import torch
+    n = la_workspace_size(sched)
+    ws = torch.zeros(n + 256, dtype=torch.uint8, device=device or "cuda")
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def la_workspace_init(workspace, stream=None):
+    _check(_lib.la_workspace_init(ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                                  _stream_handle(stream)), "la_workspace_init")
+
+
+def la_decode(q, k, v, cu_seqlens_k, sched, workspace, out, scale, stream=None):
+    """Enqueue one decode-attention call (shapes as in include/lean_attn.h)."""
+    import torch
+    if not (q.is_cuda and k.is_cuda and v.is_cuda and out.is_cuda and cu_seqlens_k.is_cuda
+            and workspace.is_cuda):
+        raise ValueError("la_decode takes device tensors")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k and v must share one dtype")
+    dt = {torch.float16: LA_F16, torch.bfloat16: LA_BF16}.get(q.dtype)
+    if dt is None:
+        raise ValueError("q, k, v must be float16 or bfloat16")
+    if out.dtype != torch.float32 or cu_seqlens_k.dtype != torch.int32:
+        raise ValueError("out must be float32 and cu_seqlens_k int32")
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("cu_seqlens_k", cu_seqlens_k)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    b, hq, hkv, d = sched.batch, sched.hq, sched.hkv, sched.d
+    kv_elems = int(sched.cu[-1]) * hkv * d
+    if q.numel() != b * hq * d or out.numel() != b * hq * d:
+        raise ValueError("q / out do not match the schedule's [batch, hq, d]")
+    if k.numel() < kv_elems or v.numel() < kv_elems:
+        raise ValueError("k / v are smaller than the schedule's contexts")
+    if cu_seqlens_k.numel() != b + 1:
+        raise ValueError("cu_seqlens_k does not match the schedule's batch")
+    if workspace.numel() * workspace.element_size() < la_workspace_size(sched):
+        raise ValueError("workspace smaller than la_workspace_size")
+    _check(_lib.la_decode(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                          ctypes.c_void_p(v.data_ptr()), dt,
+                          ctypes.c_void_p(cu_seqlens_k.data_ptr()), sched.handle,
+                          ctypes.c_void_p(workspace.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                          float(scale), _stream_handle(stream)), "la_decode")
+    return out
+
+
+def la_get_status(workspace, stream=None):
+    return int(_lib.la_get_status(ctypes.c_void_p(workspace.data_ptr()), _stream_handle(stream)))
+
+
+class LeanDecoder:
+    """Convenience holder: a schedule, its workspace and the device offsets."""
+
+    def __init__(self, batch, hq, hkv, d, cu_seqlens_k, num_sms=0, device="cuda", fixed_splits=None):
+        import torch
+        if fixed_splits is None:
+            self.sched = la_plan(batch, hq, hkv, d, cu_seqlens_k, num_sms)
+        else:
+            self.sched = la_plan_fixed(batch, hq, hkv, d, cu_seqlens_k, fixed_splits)
+        self.workspace = new_workspace(self.sched, device)
+        self.cu_dev = torch.as_tensor(self.sched.cu, dtype=torch.int32, device=device)
+        self.batch, self.hq, self.hkv, self.d = batch, hq, hkv, d
+
+    def __call__(self, q, k, v, scale, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(self.batch, self.hq, self.d, dtype=torch.float32, device=q.device)
+        return la_decode(q, k, v, self.cu_dev, self.sched, self.workspace, out, scale, stream)
+
+    def status(self, stream=None):
+        return la_get_status(self.workspace, stream)

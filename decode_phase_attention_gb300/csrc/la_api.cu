@@ -1,0 +1,437 @@
+// la_api.cu -- the C ABI of lean_attn.h: host tile planner, schedule
+// upload, argument checks and kernel launches.
+//
+// Planner rules (xllm-io paper review of LeanAttention):
+//   "3.3 LeanTile"              T = 256 tokens at d = 64, 128 at d = 128
+//   "3.4 stream-K decomposition" tiles of all units on one line, split
+//                               evenly over G CTAs, crossing unit boundaries
+//   "3.5 execution flow"        I_G = I / G per CTA; host and finishing CTA
+//                               per output tile; non-host CTAs hand their
+//                               partial to the host through global memory
+//   "4.3 work distribution"     fixed partitions (FlashAttention-2,
+//                               FlashDecoding) for the baselines
+// The planner walks CTA ranges arithmetically in O(G + units).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "la_internal.h"
+#include "lean_attn.h"
+
+struct la_schedule {
+  int batch = 0, hq = 0, hkv = 0, d = 0, grp = 0, T = 0;
+  int kind = 0;    // 0 stream-K, 1 fixed
+  int splits = 0;  // fixed partitions only
+  int G = 0, U = 0;
+  int64_t I = 0;
+  std::vector<int32_t> cu, cta_iter, unit_iter, cta_seg, segs, unit_host, unit_fin;
+  // debug hooks
+  int skip_signal = -1;
+  long long spin_ns = 2000000000LL;
+  // device copy: [cu (batch+1)] [cta_seg (G+1)] [segs] [unit_host (U)] [unit_fin (U)]
+  std::mutex mu;
+  int device = -1;
+  int32_t* dev = nullptr;
+  size_t off_cu = 0, off_cta_seg = 0, off_segs = 0, off_host = 0, off_fin = 0;
+};
+
+namespace {
+
+constexpr int kMaxGrid = 1 << 20;
+
+int lean_tile(int d) { return d == 64 ? 256 : (d == 128 ? 128 : 0); }
+
+la_status check_shape(int batch, int hq, int hkv, int d, const int32_t* cu) {
+  if (batch <= 0 || hq <= 0 || hkv <= 0 || cu == nullptr) return LA_ERR_INVALID;
+  if (hq % hkv != 0) return LA_ERR_INVALID;
+  if (cu[0] != 0) return LA_ERR_INVALID;
+  for (int b = 0; b < batch; ++b)
+    if (cu[b + 1] <= cu[b]) return LA_ERR_INVALID;  // every context holds >= 1 token
+  if (d <= 0) return LA_ERR_INVALID;
+  if (d != 64 && d != 128) return LA_ERR_UNSUPPORTED;
+  const int grp = hq / hkv;
+  if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return LA_ERR_UNSUPPORTED;
+  // element offsets are formed in 64 bits, tile indices in 32 bits
+  if ((int64_t)hkv * cu[batch] > (int64_t)INT32_MAX * 64) return LA_ERR_UNSUPPORTED;
+  return LA_OK;
+}
+
+// Units (b, kv head) in request-major order and their tile prefix sums.
+bool build_units(la_schedule* s) {
+  s->U = s->batch * s->hkv;
+  s->unit_iter.assign((size_t)s->U + 1, 0);
+  int64_t acc = 0;
+  for (int b = 0; b < s->batch; ++b) {
+    const int64_t L = (int64_t)s->cu[b + 1] - s->cu[b];
+    const int64_t tiles = (L + s->T - 1) / s->T;
+    for (int h = 0; h < s->hkv; ++h) {
+      s->unit_iter[(size_t)b * s->hkv + h] = (int32_t)acc;
+      acc += tiles;
+      if (acc > INT32_MAX) return false;
+    }
+  }
+  s->unit_iter[s->U] = (int32_t)acc;
+  s->I = acc;
+  return true;
+}
+
+void add_seg(la_schedule* s, int unit, int t0, int t1, int kind, int peer) {
+  s->segs.insert(s->segs.end(), {unit, t0, t1, kind, peer});
+}
+
+// CTA of global iteration i under the even split of I over G.
+int cta_of(int64_t i, int64_t I, int G) {
+  const int64_t q = I / G, r = I % G;
+  if (q == 0 || i < r * (q + 1)) return (int)(i / (q + 1));
+  return (int)(r + (i - r * (q + 1)) / q);
+}
+
+la_status plan_lean(la_schedule* s) {
+  const int G = s->G;
+  const int64_t I = s->I, q = I / G, r = I % G;
+  s->cta_iter.resize((size_t)G + 1);
+  for (int g = 0; g <= G; ++g) s->cta_iter[g] = (int32_t)(g * q + std::min<int64_t>(g, r));
+  s->unit_host.resize(s->U);
+  s->unit_fin.resize(s->U);
+  for (int u = 0; u < s->U; ++u) {
+    s->unit_host[u] = cta_of(s->unit_iter[u], I, G);
+    s->unit_fin[u] = cta_of((int64_t)s->unit_iter[u + 1] - 1, I, G);
+  }
+  s->cta_seg.assign((size_t)G + 1, 0);
+  s->segs.clear();
+  int u = 0;
+  for (int g = 0; g < G; ++g) {
+    s->cta_seg[g] = (int32_t)(s->segs.size() / la::kSegWords);
+    int64_t i = s->cta_iter[g];
+    const int64_t e = s->cta_iter[g + 1];
+    while (i < e) {
+      while (s->unit_iter[u + 1] <= i) ++u;
+      const int64_t ub = s->unit_iter[u], ue = s->unit_iter[u + 1];
+      const int64_t j = std::min(e, ue);
+      const int t0 = (int)(i - ub), t1 = (int)(j - ub);
+      if (i == ub && j == ue)
+        add_seg(s, u, t0, t1, la::kWhole, -1);
+      else if (i == ub)
+        add_seg(s, u, t0, t1, la::kHost, s->unit_fin[u]);
+      else
+        add_seg(s, u, t0, t1, la::kNonHost, -1);
+      i = j;
+    }
+  }
+  s->cta_seg[G] = (int32_t)(s->segs.size() / la::kSegWords);
+  return LA_OK;
+}
+
+la_status plan_fixed(la_schedule* s) {
+  s->cta_iter.assign(1, 0);
+  s->cta_seg.assign(1, 0);
+  s->segs.clear();
+  s->unit_host.resize(s->U);
+  s->unit_fin.resize(s->U);
+  int g = 0;
+  for (int u = 0; u < s->U; ++u) {
+    const int64_t n = (int64_t)s->unit_iter[u + 1] - s->unit_iter[u];
+    const int64_t k = std::min<int64_t>(s->splits, n);
+    s->unit_host[u] = g;
+    for (int64_t p = 0; p < k; ++p) {
+      const int t0 = (int)(p * n / k), t1 = (int)((p + 1) * n / k);
+      add_seg(s, u, t0, t1, k == 1 ? la::kWhole : la::kPartial, -1);
+      s->cta_iter.push_back(s->cta_iter.back() + (t1 - t0));
+      s->cta_seg.push_back((int32_t)(s->segs.size() / la::kSegWords));
+      if (++g > kMaxGrid) return LA_ERR_UNSUPPORTED;
+    }
+    s->unit_fin[u] = g - 1;
+  }
+  s->G = g;
+  return LA_OK;
+}
+
+la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, int kind, int grid_or_splits,
+                        la_schedule** out) {
+  if (out == nullptr) return LA_ERR_INVALID;
+  *out = nullptr;
+  const la_status st = check_shape(batch, hq, hkv, d, cu);
+  if (st != LA_OK) return st;
+  la_schedule* s = new (std::nothrow) la_schedule();
+  if (s == nullptr) return LA_ERR_INVALID;
+  s->batch = batch;
+  s->hq = hq;
+  s->hkv = hkv;
+  s->d = d;
+  s->grp = hq / hkv;
+  s->T = lean_tile(d);
+  s->kind = kind;
+  s->cu.assign(cu, cu + batch + 1);
+  if (!build_units(s)) {
+    delete s;
+    return LA_ERR_UNSUPPORTED;
+  }
+  la_status r;
+  if (kind == 0) {
+    s->G = grid_or_splits;
+    r = plan_lean(s);
+  } else {
+    s->splits = grid_or_splits;
+    r = plan_fixed(s);
+  }
+  if (r != LA_OK) {
+    delete s;
+    return r;
+  }
+  *out = s;
+  return LA_OK;
+}
+
+// CTAs per SM of the decode kernel, cached per (device, d, grp).
+la_status capacity(int d, int grp, int* per_sm) {
+  static std::mutex mu;
+  static int cache[64][2][4];
+  static bool init = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
+  const int di = d == 64 ? 0 : 1;
+  const int gi = grp == 1 ? 0 : grp == 2 ? 1 : grp == 4 ? 2 : 3;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (auto& a : cache)
+      for (auto& b : a)
+        for (int& c : b) c = -1;
+    init = true;
+  }
+  if (dev < 64 && cache[dev][di][gi] >= 0) {
+    *per_sm = cache[dev][di][gi];
+    return LA_OK;
+  }
+  cudaError_t e = d == 64 ? la::decode_capacity_d64(grp, per_sm) : la::decode_capacity_d128(grp, per_sm);
+  if (e != cudaSuccess) return LA_ERR_CUDA;
+  if (dev < 64) cache[dev][di][gi] = *per_sm;
+  return LA_OK;
+}
+
+la_status device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return LA_ERR_CUDA;
+  return LA_OK;
+}
+
+// Upload the schedule tables to the current device once.
+la_status ensure_uploaded(la_schedule* s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(s->mu);
+  if (s->dev != nullptr) return s->device == dev ? LA_OK : LA_ERR_INVALID;
+  std::vector<int32_t> buf;
+  s->off_cu = buf.size();
+  buf.insert(buf.end(), s->cu.begin(), s->cu.end());
+  s->off_cta_seg = buf.size();
+  buf.insert(buf.end(), s->cta_seg.begin(), s->cta_seg.end());
+  s->off_segs = buf.size();
+  buf.insert(buf.end(), s->segs.begin(), s->segs.end());
+  s->off_host = buf.size();
+  buf.insert(buf.end(), s->unit_host.begin(), s->unit_host.end());
+  s->off_fin = buf.size();
+  buf.insert(buf.end(), s->unit_fin.begin(), s->unit_fin.end());
+  int32_t* d = nullptr;
+  if (cudaMalloc(&d, buf.size() * sizeof(int32_t)) != cudaSuccess) return LA_ERR_CUDA;
+  if (cudaMemcpy(d, buf.data(), buf.size() * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(d);
+    return LA_ERR_CUDA;
+  }
+  s->dev = d;
+  s->device = dev;
+  return LA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int num_sms,
+                  la_schedule** out) {
+  if (out != nullptr) *out = nullptr;
+  int G = num_sms;
+  if (G <= 0) {
+    const la_status st = check_shape(batch, hq, hkv, d, cu_seqlens_k);
+    if (st != LA_OK) return st;
+    int sms = 0, per_sm = 0;
+    la_status e = device_sms(&sms);
+    if (e != LA_OK) return e;
+    e = capacity(d, hq / hkv, &per_sm);
+    if (e != LA_OK) return e;
+    G = sms * std::max(1, per_sm);
+  }
+  if (G > kMaxGrid) return LA_ERR_INVALID;
+  return make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out);
+}
+
+la_status la_plan_fixed(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int splits,
+                        la_schedule** out) {
+  if (out != nullptr) *out = nullptr;
+  if (splits <= 0) return LA_ERR_INVALID;
+  return make_schedule(batch, hq, hkv, d, cu_seqlens_k, 1, splits, out);
+}
+
+int la_schedule_grid(const la_schedule* s) { return s ? s->G : -1; }
+
+size_t la_workspace_size(const la_schedule* s) {
+  if (s == nullptr) return 0;
+  return la::workspace_bytes(s->G, s->d, s->grp);
+}
+
+la_status la_workspace_init(void* workspace, size_t bytes, la_stream_t stream) {
+  if (workspace == nullptr || bytes < la::kHeaderBytes) return LA_ERR_WORKSPACE;
+  return cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt, const int32_t* cu_seqlens_k_dev,
+                    const la_schedule* sc, void* workspace, float* out, float scale, la_stream_t stream) {
+  if (sc == nullptr || q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
+      cu_seqlens_k_dev == nullptr)
+    return LA_ERR_INVALID;
+  if (dt != LA_F16 && dt != LA_BF16) return LA_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(cu_seqlens_k_dev, 4))
+    return LA_ERR_INVALID;
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return LA_ERR_INVALID;
+  if (workspace == nullptr || !aligned(workspace, 256)) return LA_ERR_WORKSPACE;
+  la_schedule* s = const_cast<la_schedule*>(sc);
+  if (s->kind == 0) {
+    // Host CTAs wait for later CTAs inside the launch: all G must be resident at once.
+    int sms = 0, per_sm = 0;
+    la_status e = device_sms(&sms);
+    if (e != LA_OK) return e;
+    e = capacity(s->d, s->grp, &per_sm);
+    if (e != LA_OK) return e;
+    if ((int64_t)s->G > (int64_t)sms * per_sm) return LA_ERR_INVALID;
+  }
+  la_status e = ensure_uploaded(s);
+  if (e != LA_OK) return e;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  la::KParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.cu = cu_seqlens_k_dev;
+  p.sched_cu = s->dev + s->off_cu;
+  p.cta_seg = s->dev + s->off_cta_seg;
+  p.segs = s->dev + s->off_segs;
+  p.out = out;
+  p.hdr = reinterpret_cast<uint32_t*>(ws);
+  p.flags = reinterpret_cast<uint32_t*>(ws + la::kHeaderBytes);
+  p.recs = reinterpret_cast<float*>(ws + la::kHeaderBytes + la::flags_bytes(s->G));
+  p.G = s->G;
+  p.batch = s->batch;
+  p.hq = s->hq;
+  p.hkv = s->hkv;
+  p.qscale = scale * 1.4426950408889634f;  // log2(e): scores in base-2 units
+  p.spin_ns = s->spin_ns;
+  p.skip_signal = s->skip_signal;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int dtype = dt == LA_BF16 ? 1 : 0;
+  cudaError_t ce = s->d == 64 ? la::launch_decode_d64(s->grp, dtype, p, st)
+                              : la::launch_decode_d128(s->grp, dtype, p, st);
+  if (ce != cudaSuccess) return LA_ERR_CUDA;
+  if (s->kind == 1 && s->splits > 1) {
+    la::CParams c;
+    c.unit_host = s->dev + s->off_host;
+    c.unit_fin = s->dev + s->off_fin;
+    c.recs = p.recs;
+    c.out = out;
+    c.U = s->U;
+    c.hq = s->hq;
+    c.hkv = s->hkv;
+    ce = s->d == 64 ? la::launch_combine_d64(s->grp, c, st) : la::launch_combine_d128(s->grp, c, st);
+    if (ce != cudaSuccess) return LA_ERR_CUDA;
+  }
+  return LA_OK;
+}
+
+la_status la_get_status(void* workspace, la_stream_t stream) {
+  if (workspace == nullptr) return LA_ERR_WORKSPACE;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LA_ERR_CUDA;
+  uint32_t hdr[8] = {0};
+  if (cudaMemcpy(hdr, workspace, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess) return LA_ERR_CUDA;
+  const uint32_t code = hdr[la::kStatus];
+  if (code != 0) {
+    uint32_t zero[3] = {0, 0, 0};
+    if (cudaMemcpy(static_cast<uint32_t*>(workspace) + la::kStatus, zero, sizeof(zero), cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+      return LA_ERR_CUDA;
+  }
+  switch (code) {
+    case 0: return LA_OK;
+    case LA_ERR_INVALID: return LA_ERR_INVALID;
+    case LA_ERR_TIMEOUT: return LA_ERR_TIMEOUT;
+    default: return LA_ERR_CUDA;
+  }
+}
+
+size_t la_schedule_export_size(const la_schedule* s) {
+  if (s == nullptr) return 0;
+  return 8 + (size_t)(s->G + 1) * 2 + (size_t)(s->U + 1) + s->segs.size() + (size_t)s->U * 2;
+}
+
+la_status la_schedule_export(const la_schedule* s, int32_t* buf, size_t n) {
+  if (s == nullptr || buf == nullptr || n < la_schedule_export_size(s)) return LA_ERR_INVALID;
+  size_t w = 0;
+  const int32_t head[8] = {0x4C41, s->G, s->U, (int32_t)s->I, s->T,
+                           (int32_t)(s->segs.size() / la::kSegWords), s->kind, s->splits};
+  for (int32_t x : head) buf[w++] = x;
+  for (int32_t x : s->cta_iter) buf[w++] = x;
+  for (int32_t x : s->unit_iter) buf[w++] = x;
+  for (int32_t x : s->cta_seg) buf[w++] = x;
+  for (int32_t x : s->segs) buf[w++] = x;
+  for (int32_t x : s->unit_host) buf[w++] = x;
+  for (int32_t x : s->unit_fin) buf[w++] = x;
+  return LA_OK;
+}
+
+la_status la_schedule_set_debug(la_schedule* s, int skip_signal_cta, long long spin_timeout_ns) {
+  if (s == nullptr || spin_timeout_ns <= 0) return LA_ERR_INVALID;
+  s->skip_signal = skip_signal_cta;
+  s->spin_ns = spin_timeout_ns;
+  return LA_OK;
+}
+
+la_status la_device_capacity(int d, int grp, int* ctas_per_sm, int* num_sms) {
+  if (ctas_per_sm == nullptr || num_sms == nullptr) return LA_ERR_INVALID;
+  if (d != 64 && d != 128) return LA_ERR_UNSUPPORTED;
+  if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return LA_ERR_UNSUPPORTED;
+  la_status e = device_sms(num_sms);
+  if (e != LA_OK) return e;
+  return capacity(d, grp, ctas_per_sm);
+}
+
+void la_schedule_destroy(la_schedule* s) {
+  if (s == nullptr) return;
+  if (s->dev != nullptr) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != s->device) cudaSetDevice(s->device);
+    cudaFree(s->dev);
+    if (cur >= 0 && cur != s->device) cudaSetDevice(cur);
+  }
+  delete s;
+}
+
+const char* la_status_string(la_status st) {
+  switch (st) {
+    case LA_OK: return "ok";
+    case LA_ERR_INVALID: return "invalid argument";
+    case LA_ERR_UNSUPPORTED: return "unsupported shape";
+    case LA_ERR_CUDA: return "CUDA error";
+    case LA_ERR_TIMEOUT: return "a bounded wait inside the kernel ran out";
+    case LA_ERR_WORKSPACE: return "bad workspace";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

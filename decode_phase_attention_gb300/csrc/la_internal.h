@@ -1,0 +1,69 @@
+// la_internal.h -- what the C ABI layer and the kernels share: kernel
+// parameters, the workspace layout and the launch entry points.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace la {
+
+// Kinds of segment (match LA_SEG_* in lean_attn.h).
+enum SegKind : int32_t { kWhole = 0, kNonHost = 1, kHost = 2, kPartial = 3 };
+
+// One segment of a CTA's work, as stored in the device schedule.
+constexpr int kSegWords = 5;  // unit, tile_begin, tile_end, kind, peer
+
+// Workspace: a 256-byte header, G ready flags (padded to 256 bytes), then G
+// partial records of grp * (d + 2) floats: per query head [m, l, O[d]].
+constexpr size_t kHeaderBytes = 256;
+enum HeaderWord { kEpoch = 0, kDone = 1, kStatus = 2, kInfoCta = 3, kInfoPeer = 4 };
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline size_t flags_bytes(int G) { return align_up(sizeof(uint32_t) * (size_t)G, 256); }
+inline size_t record_floats(int d, int grp) { return (size_t)grp * (size_t)(d + 2); }
+inline size_t workspace_bytes(int G, int d, int grp) {
+  return kHeaderBytes + flags_bytes(G) + sizeof(float) * record_floats(d, grp) * (size_t)G;
+}
+
+struct KParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* cu;        // device cu_seqlens_k from the caller
+  const int32_t* sched_cu;  // the schedule's own copy (batch + 1)
+  const int32_t* cta_seg;   // [G + 1]
+  const int32_t* segs;      // [nseg * kSegWords]
+  float* out;
+  uint32_t* hdr;
+  uint32_t* flags;
+  float* recs;
+  int G;
+  int batch;
+  int hq;
+  int hkv;
+  float qscale;             // scale * log2(e): scores are kept in base-2 units
+  long long spin_ns;        // limit of every wait inside the kernel
+  int skip_signal;          // test hook: this CTA never sets its flag (-1: none)
+};
+
+struct CParams {            // fixed-split merge launch
+  const int32_t* unit_host; // [U]
+  const int32_t* unit_fin;  // [U]
+  const float* recs;
+  float* out;
+  int U;
+  int hq;
+  int hkv;
+};
+
+// Launches (defined in la_kernels_d64.cu / la_kernels_d128.cu). dtype: 0 fp16, 1 bf16.
+cudaError_t launch_decode_d64(int grp, int dtype, const KParams& p, cudaStream_t st);
+cudaError_t launch_decode_d128(int grp, int dtype, const KParams& p, cudaStream_t st);
+cudaError_t launch_combine_d64(int grp, const CParams& p, cudaStream_t st);
+cudaError_t launch_combine_d128(int grp, const CParams& p, cudaStream_t st);
+// CTAs of the decode kernel one SM holds at once (cudaOccupancy...).
+cudaError_t decode_capacity_d64(int grp, int* per_sm);
+cudaError_t decode_capacity_d128(int grp, int* per_sm);
+
+}  // namespace la

@@ -1,0 +1,656 @@
+// la_kernel.cuh -- the stream-K LeanAttention decode kernel for sm_103a.
+//
+// One launch computes every output of a decode-attention call (xllm-io
+// paper review of LeanAttention, "3.5 execution flow" and "4.4 single
+// kernel fusion"). CTA g walks the segments the host planner gave it:
+//   kWhole    a whole (request, kv head) unit: LeanTile loop, normalise, store
+//   kNonHost  the leading piece of a unit hosted by a lower CTA: LeanTile
+//             loop, write the partial (m, l, O) to the workspace, release a
+//             ready flag
+//   kHost     the trailing piece of a unit: LeanTile loop, then for every
+//             later CTA of the unit wait on its flag and merge its partial
+//             with the rescaling reduction f ("3.2", part 2), normalise, store
+//   kPartial  fixed-split baseline piece: write the partial, no flag
+//
+// Warp roles (288 threads, one CTA per SM):
+//   warp 8, lane 0: producer. Streams the K and V rows of each LeanTile of
+//                   every segment, in order, from HBM into a 3-stage
+//                   shared-memory ring with 1-D bulk async copies
+//                   (cp.async.bulk, completion counted in bytes on an
+//                   mbarrier). A tile's K rows (and V rows) are contiguous
+//                   in the [hkv, L, d] slab, so one copy moves all of them.
+//   warps 0-7:      consumers. Each takes T/8 consecutive tokens of the
+//                   tile; d/8 lanes share one token (8 elements = 16 bytes
+//                   per lane, so a warp reads whole rows without bank
+//                   conflicts). Scores q.k are reduced across those lanes
+//                   with shuffles, the running max / sum are updated online
+//                   ("3.3 LeanTile": online softmax statistics m, l, then
+//                   O_acc = P V + diag(rescale) O_acc), and P.V accumulates
+//                   in fp32 registers.
+// At the end of a segment the lane groups of a warp merge by shuffles and
+// the 8 warps merge through shared memory, both with f.
+//
+// Scores are kept in base-2 units: q is pre-multiplied by scale*log2(e) so
+// exp(s - m) becomes ex2(s2 - m2); m in the workspace records is in the
+// same units (the records are internal to this kernel).
+//
+// Every wait is bounded (globaltimer). A wait that runs out records
+// LA_ERR_TIMEOUT in the workspace header, raises a CTA-wide abort flag that
+// makes every other wait return at once, the producer waits (bounded) for
+// its copies still in flight, and the affected outputs are written as NaN.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "la_internal.h"
+
+namespace la {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint32_t kStatusInvalid = 1;  // LA_ERR_INVALID
+constexpr uint32_t kStatusTimeout = 4;  // LA_ERR_TIMEOUT
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// 1-D bulk copy global -> shared, completion signalled on `bar` in bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {  // 2^x; ex2(-inf) = 0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------ element types
+template <typename E>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+  // bf16 is the upper half of an fp32: widening is a shift / mask.
+  __device__ static __forceinline__ void to_f32(const uint4& x, float f[8]) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+template <>
+struct Elem<__half> {
+  __device__ static __forceinline__ void to_f32(const uint4& x, float f[8]) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      float2 t = __half22float2(h);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+};
+
+// ------------------------------------------------------------ configuration
+template <int D, int GRP>
+struct Cfg {
+  static constexpr int T = (D == 64) ? 256 : 128;  // LeanTile ("3.3 LeanTile" table)
+  static constexpr int NCW = 8;                     // consumer warps
+  static constexpr int NCT = NCW * 32;              // consumer threads
+  static constexpr int NTHREADS = NCT + 32;         // + producer warp
+  static constexpr int LPT = D / 8;                 // lanes per token
+  static constexpr int TPS = 32 / LPT;              // tokens per warp step
+  static constexpr int TPW = T / NCW;               // tokens per warp per tile
+  static constexpr int STEPS = TPW / TPS;
+  static constexpr int CH = (GRP <= 2) ? STEPS : (GRP == 4 ? 4 : 2);  // steps per softmax update
+  static constexpr int STAGES = 3;
+  static constexpr int TILE_ELEMS = T * D;
+  static constexpr size_t KV_BYTES = (size_t)STAGES * 2 * TILE_ELEMS * 2;
+  static constexpr int REC = D + 2;                 // [m, l, O[d]]
+  static constexpr size_t MERGE_BYTES = (size_t)NCW * GRP * REC * 4;
+  static constexpr size_t BAR_BYTES = 2 * STAGES * 8 + 16;
+  static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES;
+  static constexpr int ITEMS = (GRP * D + NCT - 1) / NCT;  // (head, dim) outputs per consumer thread
+  static_assert(STEPS % CH == 0, "chunking");
+  static_assert(TPW % TPS == 0, "tokens per warp");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+};
+
+// Record the first error of the launch in the workspace header.
+__device__ __forceinline__ void record_error(uint32_t* hdr, uint32_t code, int cta, int peer) {
+  if (atomicCAS(&hdr[kStatus], 0u, code) == 0u) {
+    hdr[kInfoCta] = (uint32_t)cta;
+    hdr[kInfoPeer] = (uint32_t)peer;
+  }
+}
+
+// Bounded wait on an mbarrier phase. Returns false if the abort flag is up
+// or the limit ran out (the caller records the error).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if ((long long)(global_ns() - t0) > limit_ns) return false;
+    }
+  }
+}
+
+// The schedule was planned with host offsets; the kernel reads the device
+// copy the caller passes. They must agree before any address is formed.
+__device__ __forceinline__ bool unit_offsets_ok(const KParams& p, int b) {
+  return p.cu[b] == p.sched_cu[b] && p.cu[b + 1] == p.sched_cu[b + 1];
+}
+
+// ------------------------------------------------------------------ producer
+template <int D, int GRP, typename E>
+__device__ __forceinline__ void produce(const KParams& p, int g, E* kv, uint64_t* full, uint64_t* empty,
+                                        volatile int* abort_flag) {
+  using C = Cfg<D, GRP>;
+  const uint64_t pol = l2_evict_first_policy();
+  const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
+  int stage = 0;
+  uint32_t phase = 1;  // a fresh barrier counts its previous (odd) phase as complete
+  long long issued = 0;
+  bool aborted = false;
+  for (int si = s_begin; si < s_end && !aborted; ++si) {
+    const int* sg = p.segs + (size_t)si * kSegWords;
+    const int unit = sg[0], t0 = sg[1], t1 = sg[2];
+    const int b = unit / p.hkv, kvh = unit % p.hkv;
+    if (!unit_offsets_ok(p, b)) continue;  // consumers skip the same segment
+    const long long L = (long long)p.cu[b + 1] - p.cu[b];
+    const long long base = ((long long)p.hkv * p.cu[b] + (long long)kvh * L) * D;
+    const E* kb = static_cast<const E*>(p.k) + base;
+    const E* vb = static_cast<const E*>(p.v) + base;
+    for (int t = t0; t < t1; ++t) {
+      const long long rem = L - (long long)t * C::T;
+      const int ntok = rem < C::T ? (int)rem : C::T;
+      if (!mbar_wait_bounded(&empty[stage], phase, abort_flag, p.spin_ns)) {
+        record_error(p.hdr, kStatusTimeout, g, -1);
+        *abort_flag = 1;
+        aborted = true;
+        break;
+      }
+      const uint32_t bytes = (uint32_t)ntok * D * 2u;
+      mbar_arrive_expect_tx(&full[stage], 2u * bytes);
+      E* ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
+      bulk_g2s(ks, kb + (long long)t * C::T * D, bytes, &full[stage], pol);
+      bulk_g2s(ks + C::TILE_ELEMS, vb + (long long)t * C::T * D, bytes, &full[stage], pol);
+      ++issued;
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (aborted) {
+    // Do not leave the CTA while copies into its shared memory are in flight:
+    // wait (bounded) for the latest fill of every stage that was used.
+    for (int s = 0; s < C::STAGES; ++s) {
+      const long long fills = issued / C::STAGES + (s < issued % C::STAGES ? 1 : 0);
+      if (fills == 0) continue;
+      const uint32_t parity = (uint32_t)((fills - 1) & 1);
+      volatile int no_abort = 0;
+      mbar_wait_bounded(&full[s], parity, &no_abort, p.spin_ns);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ consumers
+template <int D, int GRP, typename E>
+__device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, uint64_t* full,
+                                        uint64_t* empty, float* mrg, volatile int* abort_flag,
+                                        uint32_t epoch) {
+  using C = Cfg<D, GRP>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gl = lane % C::LPT;  // which 8-element chunk of the row
+  const int ts = lane / C::LPT;  // which token of the warp step
+  const int c0 = gl * 8;
+  const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
+  const uint32_t ready = epoch + 1u;
+  int stage = 0;
+  uint32_t phase = 0;
+
+  for (int si = s_begin; si < s_end; ++si) {
+    const int* sg = p.segs + (size_t)si * kSegWords;
+    const int unit = sg[0], t0 = sg[1], t1 = sg[2], kind = sg[3], peer = sg[4];
+    const int b = unit / p.hkv, kvh = unit % p.hkv;
+    const bool ok = unit_offsets_ok(p, b);
+    if (!ok && tid == 0) record_error(p.hdr, kStatusInvalid, g, unit);
+    const long long L = ok ? (long long)p.cu[b + 1] - p.cu[b] : 0;
+
+    // q rows of the GRP query heads that read this kv head, pre-scaled.
+    float qf[GRP][8];
+#pragma unroll
+    for (int j = 0; j < GRP; ++j) {
+      const int h = kvh * GRP + j;
+      const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) +
+                                                        ((size_t)b * p.hq + h) * D + c0);
+      Elem<E>::to_f32(raw, qf[j]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qf[j][e] *= p.qscale;
+    }
+    float m[GRP], l[GRP], o[GRP][8];
+#pragma unroll
+    for (int j = 0; j < GRP; ++j) {
+      m[j] = -INFINITY;
+      l[j] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[j][e] = 0.f;
+    }
+
+    // ---- the LeanTile loop
+    const int n_tiles = ok ? t1 - t0 : 0;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int t = t0 + it;
+      const long long rem = L - (long long)t * C::T;
+      const int ntok = rem < C::T ? (int)rem : C::T;
+      bool have = mbar_wait_bounded(&full[stage], phase, abort_flag, p.spin_ns);
+      have = __all_sync(kFull, have);
+      if (!have) {
+        if (lane == 0) {
+          if (!*abort_flag) record_error(p.hdr, kStatusTimeout, g, -1);
+          *abort_flag = 1;
+        }
+      } else {
+        const E* Ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
+        const E* Vs = Ks + C::TILE_ELEMS;
+        const int wtok = warp * C::TPW;
+#pragma unroll
+        for (int c = 0; c < C::STEPS; c += C::CH) {
+          float s[C::CH][GRP];
+#pragma unroll
+          for (int st = 0; st < C::CH; ++st) {
+            const int tok = wtok + (c + st) * C::TPS + ts;
+            const uint4 raw = *reinterpret_cast<const uint4*>(Ks + tok * D + c0);
+            float kf[8];
+            Elem<E>::to_f32(raw, kf);
+#pragma unroll
+            for (int j = 0; j < GRP; ++j) {
+              float a0 = qf[j][0] * kf[0], a1 = qf[j][1] * kf[1];
+#pragma unroll
+              for (int e = 2; e < 8; e += 2) {
+                a0 = fmaf(qf[j][e], kf[e], a0);
+                a1 = fmaf(qf[j][e + 1], kf[e + 1], a1);
+              }
+              s[st][j] = a0 + a1;
+            }
+          }
+#pragma unroll
+          for (int st = 0; st < C::CH; ++st)
+#pragma unroll
+            for (int j = 0; j < GRP; ++j)
+#pragma unroll
+              for (int off = C::LPT / 2; off >= 1; off >>= 1)
+                s[st][j] += __shfl_xor_sync(kFull, s[st][j], off);
+#pragma unroll
+          for (int st = 0; st < C::CH; ++st) {
+            const int tok = wtok + (c + st) * C::TPS + ts;
+            if (tok >= ntok) {
+#pragma unroll
+              for (int j = 0; j < GRP; ++j) s[st][j] = -INFINITY;
+            }
+          }
+          // online softmax: new max, rescale, exponentiate
+#pragma unroll
+          for (int j = 0; j < GRP; ++j) {
+            float mx = s[0][j];
+#pragma unroll
+            for (int st = 1; st < C::CH; ++st) mx = fmaxf(mx, s[st][j]);
+            const float mn = fmaxf(m[j], mx);
+            if (mn == -INFINITY) {
+#pragma unroll
+              for (int st = 0; st < C::CH; ++st) s[st][j] = 0.f;
+              continue;
+            }
+            const float alpha = ex2(m[j] - mn);
+            m[j] = mn;
+            l[j] *= alpha;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[j][e] *= alpha;
+#pragma unroll
+            for (int st = 0; st < C::CH; ++st) {
+              const float pj = ex2(s[st][j] - mn);
+              s[st][j] = pj;
+              l[j] += pj;
+            }
+          }
+          // P.V
+#pragma unroll
+          for (int st = 0; st < C::CH; ++st) {
+            const int tok = wtok + (c + st) * C::TPS + ts;
+            if (tok < ntok) {
+              const uint4 raw = *reinterpret_cast<const uint4*>(Vs + tok * D + c0);
+              float vf[8];
+              Elem<E>::to_f32(raw, vf);
+#pragma unroll
+              for (int j = 0; j < GRP; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[j][e] = fmaf(s[st][j], vf[e], o[j][e]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+
+    // ---- merge the token slots of the warp (lanes with equal gl) with f
+#pragma unroll
+    for (int off = C::LPT; off < 32; off <<= 1) {
+#pragma unroll
+      for (int j = 0; j < GRP; ++j) {
+        const float mo = __shfl_xor_sync(kFull, m[j], off);
+        const float lo = __shfl_xor_sync(kFull, l[j], off);
+        const float mn = fmaxf(m[j], mo);
+        const float a = (m[j] == -INFINITY) ? 0.f : ex2(m[j] - mn);
+        const float bw = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
+        l[j] = a * l[j] + bw * lo;
+        m[j] = mn;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float oo = __shfl_xor_sync(kFull, o[j][e], off);
+          o[j][e] = a * o[j][e] + bw * oo;
+        }
+      }
+    }
+    float* wrec = mrg + (size_t)warp * GRP * C::REC;
+    if (ts == 0) {
+#pragma unroll
+      for (int j = 0; j < GRP; ++j) {
+        float* r = wrec + j * C::REC;
+        if (gl == 0) {
+          r[0] = m[j];
+          r[1] = l[j];
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r[2 + c0 + e] = o[j][e];
+      }
+    }
+    consumer_sync(C::NCT);
+
+    // ---- merge the 8 warps with f: thread -> (head j, dim c) items
+    float M[C::ITEMS], Lsum[C::ITEMS], O[C::ITEMS];
+#pragma unroll
+    for (int i = 0; i < C::ITEMS; ++i) {
+      const int idx = tid + i * C::NCT;
+      M[i] = -INFINITY;
+      Lsum[i] = 0.f;
+      O[i] = 0.f;
+      if (idx < GRP * D) {
+        const int j = idx / D, cc = idx % D;
+        float mm = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::NCW; ++w) mm = fmaxf(mm, mrg[(w * GRP + j) * C::REC]);
+        if (mm != -INFINITY) {
+          float ls = 0.f, os = 0.f;
+#pragma unroll
+          for (int w = 0; w < C::NCW; ++w) {
+            const float* r = mrg + (w * GRP + j) * C::REC;
+            const float wt = (r[0] == -INFINITY) ? 0.f : ex2(r[0] - mm);
+            ls = fmaf(wt, r[1], ls);
+            os = fmaf(wt, r[2 + cc], os);
+          }
+          M[i] = mm;
+          Lsum[i] = ls;
+          O[i] = os;
+        }
+      }
+    }
+    const bool poisoned = (*abort_flag != 0) || !ok;
+
+    if (kind == kNonHost || kind == kPartial) {
+      float* rec = p.recs + (size_t)g * GRP * C::REC;
+#pragma unroll
+      for (int i = 0; i < C::ITEMS; ++i) {
+        const int idx = tid + i * C::NCT;
+        if (idx < GRP * D) {
+          const int j = idx / D, cc = idx % D;
+          float* r = rec + j * C::REC;
+          r[2 + cc] = O[i];
+          if (cc == 0) {
+            r[0] = poisoned ? __int_as_float(0x7fc00000) : M[i];
+            r[1] = Lsum[i];
+          }
+        }
+      }
+      __threadfence();
+      consumer_sync(C::NCT);
+      if (kind == kNonHost && tid == 0 && g != p.skip_signal) st_release_gpu(&p.flags[g], ready);
+    } else {
+      bool fail = poisoned;
+      if (kind == kHost) {
+        volatile int* bcast = abort_flag + 1;
+        for (int g2 = g + 1; g2 <= peer; ++g2) {
+          if (tid == 0) {
+            bool got = false;
+            if (!*abort_flag) {
+              const uint64_t tstart = global_ns();
+              for (uint32_t it = 0;; ++it) {
+                if (ld_acquire_gpu(&p.flags[g2]) == ready) {
+                  got = true;
+                  break;
+                }
+                if (*abort_flag) break;
+                if ((it & 15u) == 15u) {
+                  if ((long long)(global_ns() - tstart) > p.spin_ns) {
+                    record_error(p.hdr, kStatusTimeout, g, g2);
+                    *abort_flag = 1;
+                    break;
+                  }
+                  __nanosleep(100);
+                }
+              }
+            }
+            *bcast = got ? 1 : 0;
+          }
+          consumer_sync(C::NCT);
+          const bool got = *bcast != 0;
+          consumer_sync(C::NCT);  // everyone has read bcast before thread 0 rewrites it
+          if (!got) {
+            fail = true;
+            break;
+          }
+          const float* rec = p.recs + (size_t)g2 * GRP * C::REC;
+#pragma unroll
+          for (int i = 0; i < C::ITEMS; ++i) {
+            const int idx = tid + i * C::NCT;
+            if (idx < GRP * D) {
+              const int j = idx / D, cc = idx % D;
+              const float* r = rec + j * C::REC;
+              const float m2 = __ldcg(r), l2 = __ldcg(r + 1), o2 = __ldcg(r + 2 + cc);
+              const float mn = fmaxf(M[i], m2);
+              if (mn == -INFINITY) continue;
+              const float a = (M[i] == -INFINITY) ? 0.f : ex2(M[i] - mn);
+              const float bw = (m2 == -INFINITY) ? 0.f : ex2(m2 - mn);
+              Lsum[i] = a * Lsum[i] + bw * l2;
+              O[i] = a * O[i] + bw * o2;
+              M[i] = mn;  // a NaN m2 (poisoned partial) propagates here
+            }
+          }
+        }
+      }
+      // normalise and store: O = Obar / l
+#pragma unroll
+      for (int i = 0; i < C::ITEMS; ++i) {
+        const int idx = tid + i * C::NCT;
+        if (idx < GRP * D) {
+          const int j = idx / D, cc = idx % D;
+          const float val = fail ? __int_as_float(0x7fc00000) : O[i] / Lsum[i];
+          p.out[((size_t)b * p.hq + (size_t)kvh * GRP + j) * D + cc] = val;
+        }
+      }
+    }
+    consumer_sync(C::NCT);  // the merge area is rewritten by the next segment
+  }
+}
+
+// -------------------------------------------------------------------- kernel
+template <int D, int GRP, typename E>
+__global__ void __launch_bounds__(Cfg<D, GRP>::NTHREADS, 1) lean_decode_kernel(const KParams p) {
+  using C = Cfg<D, GRP>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  E* kv = reinterpret_cast<E*>(smem);
+  float* mrg = reinterpret_cast<float*>(smem + C::KV_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::KV_BYTES + C::MERGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  volatile int* flags_smem = reinterpret_cast<volatile int*>(empty + C::STAGES);  // [0] abort, [1] bcast
+
+  const int tid = threadIdx.x;
+  const int g = blockIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::NCW);
+    }
+    flags_smem[0] = 0;
+    flags_smem[1] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr[kEpoch]);
+
+  if ((tid >> 5) == C::NCW) {
+    if ((tid & 31) == 0) produce<D, GRP, E>(p, g, kv, full, empty, flags_smem);
+    __syncwarp();
+  } else {
+    consume<D, GRP, E>(p, g, kv, full, empty, mrg, flags_smem, epoch);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // The last CTA to finish advances the epoch, so the next launch's ready
+    // flags can never be confused with this one's.
+    __threadfence();
+    const uint32_t prev = atomicAdd(&p.hdr[kDone], 1u);
+    if (prev == (uint32_t)p.G - 1u) {
+      p.hdr[kDone] = 0u;
+      __threadfence();
+      p.hdr[kEpoch] = epoch + 1u;
+    }
+  }
+}
+
+// Fixed-split baseline: merge the pieces of every unit with f (one block per
+// (unit, query head of the group), one thread per dimension).
+template <int D, int GRP>
+__global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
+  constexpr int REC = D + 2;
+  const int row = blockIdx.x;  // unit * GRP + j
+  const int unit = row / GRP, j = row % GRP;
+  const int c = threadIdx.x;
+  const int h0 = p.unit_host[unit], h1 = p.unit_fin[unit];
+  if (h0 == h1) return;  // a whole unit was written by the decode kernel
+  float M = -INFINITY, Ls = 0.f, O = 0.f;
+  for (int s = h0; s <= h1; ++s) {
+    const float* r = p.recs + ((size_t)s * GRP + j) * REC;
+    const float m2 = r[0], l2 = r[1], o2 = r[2 + c];
+    const float mn = fmaxf(M, m2);
+    if (mn == -INFINITY) continue;
+    const float a = (M == -INFINITY) ? 0.f : ex2(M - mn);
+    const float bw = (m2 == -INFINITY) ? 0.f : ex2(m2 - mn);
+    Ls = a * Ls + bw * l2;
+    O = a * O + bw * o2;
+    M = mn;
+  }
+  const int b = unit / p.hkv, kvh = unit % p.hkv;
+  p.out[((size_t)b * p.hq + (size_t)kvh * GRP + j) * D + c] = O / Ls;
+}
+
+// ------------------------------------------------------------- host launchers
+template <int D, int GRP, typename E>
+cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
+  using C = Cfg<D, GRP>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(lean_decode_kernel<D, GRP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  if (p.G <= 0) return cudaSuccess;
+  lean_decode_kernel<D, GRP, E><<<p.G, C::NTHREADS, C::SMEM, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int GRP>
+cudaError_t capacity_t(int* per_sm) {
+  using C = Cfg<D, GRP>;
+  cudaError_t e = cudaFuncSetAttribute(lean_decode_kernel<D, GRP, __nv_bfloat16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lean_decode_kernel<D, GRP, __nv_bfloat16>,
+                                                       C::NTHREADS, C::SMEM);
+}
+
+template <int D, int GRP>
+cudaError_t launch_combine_t(const CParams& p, cudaStream_t st) {
+  if (p.U <= 0) return cudaSuccess;
+  lean_combine_kernel<D, GRP><<<p.U * GRP, D, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace la

@@ -1,0 +1,195 @@
+/*
+ * lean_attn.h -- C ABI of the LeanAttention decode-phase attention library
+ * (stream-K decode attention for one GPU, sm_103a).
+ *
+ * The operation (xllm-io paper review of LeanAttention, "3.1 standard
+ * attention", decode phase with one query token): for every request b and
+ * query head h,
+ *     s_t   = scale * q[b,h,:] . K[b, h/grp, t, :]      t < L_b
+ *     out[b,h,:] = sum_t softmax(s)_t V[b, h/grp, t, :]
+ * with grp = hq / hkv query heads sharing one kv head.
+ *
+ * How it is computed (same review, "3.3 LeanTile" to "3.5 execution flow",
+ * and "3.2 softmax rescaling as a reduction"): the context of every
+ * (request, kv head) unit is cut into LeanTiles (256 tokens at d = 64, 128
+ * tokens at d = 128); all tiles are laid out on one line and split evenly
+ * over G CTAs, which may cross head and request boundaries; each CTA
+ * produces partial results (m, l, unscaled O) that the unit's host CTA
+ * merges with the rescaling reduction f and normalises, all in one launch.
+ *
+ * Data layout (device memory, row-major, no padding):
+ *   q    [batch, hq, d]                         fp16 or bf16
+ *   k, v request b is a contiguous [hkv, L_b, d] slab starting at element
+ *        hkv * cu[b] * d; token t of kv head h sits at element
+ *        (hkv * cu[b] + h * L_b + t) * d.  With equal lengths this is the
+ *        [batch, heads, seq_len, head_dim] layout the review's "7.4
+ *        limitations" names.                    fp16 or bf16 (same as q)
+ *   cu_seqlens_k  int32 [batch + 1], cu[0] = 0, cu[b+1] - cu[b] = L_b >= 1
+ *   out  [batch, hq, d]                         fp32
+ *
+ * Threading and ownership: the caller owns every buffer and the stream.
+ * A schedule is owned by the library until la_schedule_destroy; it keeps a
+ * device copy of its tables, uploaded on its first la_decode (that call
+ * allocates device memory and synchronises, so make it before any stream
+ * capture). A schedule may be used from one thread at a time.
+ *
+ * Errors: every entry point returns an la_status and never throws. Argument,
+ * shape and support problems are reported before anything is launched.
+ * la_decode is asynchronous; a failure detected inside the kernel (a
+ * bounded wait that ran out, a cu_seqlens_k that disagrees with the
+ * schedule) is recorded in the workspace and returned by la_get_status.
+ */
+#ifndef LEAN_ATTN_H
+#define LEAN_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* la_stream_t;
+
+typedef struct la_schedule la_schedule;
+
+typedef enum {
+  LA_OK = 0,
+  LA_ERR_INVALID = 1,     /* bad argument, shape, pointer or alignment */
+  LA_ERR_UNSUPPORTED = 2, /* a valid shape this build does not implement */
+  LA_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+  LA_ERR_TIMEOUT = 4,     /* a bounded wait inside the kernel ran out */
+  LA_ERR_WORKSPACE = 5    /* workspace missing, too small or misaligned */
+} la_status;
+
+typedef enum { LA_F16 = 0, LA_BF16 = 1 } la_dtype;
+
+/* Kinds of work a CTA does on one unit, as exported by la_schedule_export. */
+enum {
+  LA_SEG_WHOLE = 0,   /* the CTA covers the whole unit: normalise, write out */
+  LA_SEG_NONHOST = 1, /* a later piece: write (m, l, O) to the workspace, set a ready flag */
+  LA_SEG_HOST = 2,    /* the first piece: wait for the later pieces, merge with f, write out */
+  LA_SEG_PARTIAL = 3  /* fixed-split piece: write (m, l, O); a second launch merges */
+};
+
+/*
+ * la_plan -- the stream-K tile planner ("3.4 stream-K style decomposition"
+ * and "3.5 execution flow" of the xllm-io review).
+ *
+ *   batch, hq, hkv, d  shape; d in {64, 128}; hq % hkv == 0 and
+ *                      hq / hkv in {1, 2, 4, 8}
+ *   cu_seqlens_k       HOST pointer to batch + 1 int32 offsets (read, not kept)
+ *   num_sms            grid size G; <= 0 picks one persistent CTA per SM of
+ *                      the current device (the kernel runs one CTA per SM).
+ *                      A G larger than the device can hold at once is
+ *                      rejected by la_decode, because host CTAs wait for
+ *                      later CTAs inside the launch.
+ *   out                receives the new schedule
+ *
+ * Rules: tiles(b) = ceil(L_b / T), T = 256 (d = 64) or 128 (d = 128);
+ * units (b, kv head) in request-major order; I = total tiles; CTA g takes
+ * floor(I/G) iterations plus one if g < I mod G, in order; the host of a
+ * unit is the CTA holding its first tile, the finisher the one holding its
+ * last. Pure host code when num_sms > 0. Returns LA_ERR_INVALID for bad
+ * shapes or lengths, LA_ERR_UNSUPPORTED for d or group sizes not built.
+ */
+la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int num_sms,
+                  la_schedule** out);
+
+/*
+ * la_plan_fixed -- fixed partitions used as baselines (the review's "2.2"
+ * and "2.3" on FlashAttention-2 and FlashDecoding, and "4.3" on their
+ * relation to the stream-K mapping). Every unit is cut into
+ * min(splits, tiles) even pieces, one CTA each. splits == 1: one CTA per
+ * (request, kv head), no reduction. splits > 1: every piece writes its
+ * partial result and a second kernel merges them (two launches per call).
+ * No CTA waits on another, so G is not limited by co-residency.
+ */
+la_status la_plan_fixed(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k,
+                        int splits, la_schedule** out);
+
+/* Grid size G of a schedule (CTAs per launch), or -1 for NULL. */
+int la_schedule_grid(const la_schedule* s);
+
+/*
+ * Bytes of device workspace la_decode needs for this schedule: a header, G
+ * ready flags and G partial records of grp * (d + 2) floats ("7.4
+ * limitations": a small amount of global memory for sharing partial
+ * results). Zero it once (la_workspace_init) before its first use; after
+ * that it needs no clearing between calls. One workspace must not be used
+ * by two launches that can run at the same time.
+ */
+size_t la_workspace_size(const la_schedule* s);
+
+/* Zero a workspace on a stream (cudaMemsetAsync). */
+la_status la_workspace_init(void* workspace, size_t bytes, la_stream_t stream);
+
+/*
+ * la_decode -- one decode-attention call, enqueued on `stream`.
+ *
+ *   q, k, v           device pointers, layout above, 16-byte aligned
+ *   dt                element type of q, k and v
+ *   cu_seqlens_k_dev  DEVICE copy of the offsets the schedule was planned
+ *                     with; the kernel checks it against the schedule and
+ *                     reports LA_ERR_INVALID through la_get_status if they
+ *                     differ (the affected outputs are NaN)
+ *   s                 schedule from la_plan or la_plan_fixed
+ *   workspace         device memory of la_workspace_size(s) bytes,
+ *                     256-byte aligned, zeroed once before first use
+ *   out               device fp32 [batch, hq, d], 16-byte aligned
+ *   scale             multiplies every score before the softmax (1/sqrt(d)
+ *                     in the review's formula)
+ *
+ * One kernel launch for stream-K schedules (plus one merge launch for
+ * fixed splits > 1). Does not synchronise, except on a schedule's first
+ * use (upload of its tables). Returns LA_ERR_INVALID / LA_ERR_WORKSPACE
+ * for bad arguments, LA_ERR_CUDA if a launch fails.
+ */
+la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt,
+                    const int32_t* cu_seqlens_k_dev, const la_schedule* s, void* workspace,
+                    float* out, float scale, la_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the first error a kernel
+ * recorded in `workspace` since the last call (LA_OK if none). Meant for
+ * tests and error handling, not for the hot loop.
+ */
+la_status la_get_status(void* workspace, la_stream_t stream);
+
+/*
+ * Planner parity: the schedule as int32 words,
+ *   [0x4C41, G, U, I, T, nseg, kind (0 stream-K, 1 fixed), splits]
+ *   cta_iter[G+1]  first global tile iteration of every CTA (+ total)
+ *   unit_iter[U+1] first global tile iteration of every unit (+ total)
+ *   cta_seg[G+1]   first segment of every CTA (+ total)
+ *   segs[nseg*5]   (unit, tile_begin, tile_end, LA_SEG_* kind, peer): peer
+ *                  is the finishing CTA for LA_SEG_HOST, else -1
+ *   unit_host[U], unit_fin[U]
+ * la_schedule_export_size gives the word count; la_schedule_export fails
+ * with LA_ERR_INVALID if n is smaller.
+ */
+size_t la_schedule_export_size(const la_schedule* s);
+la_status la_schedule_export(const la_schedule* s, int32_t* buf, size_t n);
+
+/*
+ * Test hooks for failure detection (no GPU fault is ever needed):
+ *   skip_signal_cta  CTA whose ready flag is never set (-1: none), so its
+ *                    host's bounded wait runs out and reports LA_ERR_TIMEOUT
+ *   spin_timeout_ns  limit of every wait inside the kernel (default 2 s)
+ */
+la_status la_schedule_set_debug(la_schedule* s, int skip_signal_cta, long long spin_timeout_ns);
+
+/* Most CTAs of the stream-K kernel one SM of the current device holds for
+ * head dim d and group size grp, and the SM count. */
+la_status la_device_capacity(int d, int grp, int* ctas_per_sm, int* num_sms);
+
+void la_schedule_destroy(la_schedule* s);
+
+const char* la_status_string(la_status st);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LEAN_ATTN_H */

@@ -1,0 +1,137 @@
+"""CPU checks of the C ABI: the library loads, exports every declared
+symbol, plans exactly like the reference planner, and rejects bad arguments
+before it touches a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import decode_phase_attention_gb300 as la
+from oracle import plan as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "lean_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(la.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(la.EXPORTED) == names
+
+
+def cu_of(lengths):
+    return [0] + np.cumsum(lengths).tolist()
+
+
+def shapes():
+    r = np.random.default_rng(123)
+    out = [(1, 4, 4, 64, [1024], 3), (8, 32, 32, 128, [8192] * 8, 148), (8, 32, 32, 128, [8192] * 8, 152),
+           (1, 32, 32, 128, [65536], 152), (2, 8, 8, 64, [300, 5000], 7)]
+    for _ in range(60):
+        batch = int(r.integers(1, 6))
+        hkv = int(r.integers(1, 5))
+        grp = int(r.choice([1, 2, 4, 8]))
+        d = int(r.choice([64, 128]))
+        lengths = r.integers(1, 3000, size=batch).tolist()
+        out.append((batch, hkv * grp, hkv, d, lengths, int(r.integers(1, 200))))
+    return out
+
+
+@pytest.mark.parametrize("shape", shapes())
+def test_planner_matches_reference_planner_exactly(shape):
+    batch, hq, hkv, d, lengths, G = shape
+    s = la.la_plan(batch, hq, hkv, d, cu_of(lengths), G)
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(batch, hq, hkv, d, cu_of(lengths), G))
+    assert s.grid == G
+
+
+def test_planner_matches_on_the_ragged_and_gqa_workloads():
+    import workloads
+    for name in ("ragged", "gqa", "long512k"):
+        w = workloads.named(name)
+        for G in (148, 152, 304):
+            s = la.la_plan(w.batch, w.hq, w.hkv, w.d, w.cu, G)
+            assert la.la_schedule_export(s) == P.export(P.plan_lean(w.batch, w.hq, w.hkv, w.d, w.cu.tolist(), G))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 16])
+def test_fixed_planner_matches_reference(splits):
+    lengths = [1000, 17, 4096, 129, 8000]
+    s = la.la_plan_fixed(5, 8, 2, 128, cu_of(lengths), splits)
+    assert la.la_schedule_export(s) == P.export(P.plan_fixed(5, 8, 2, 128, cu_of(lengths), splits))
+
+
+@pytest.mark.parametrize("args,status", [
+    ((1, 6, 4, 64, [0, 10], 4), la.LA_ERR_INVALID),             # hq not a multiple of hkv
+    ((2, 4, 4, 64, [0, 10, 10], 4), la.LA_ERR_INVALID),         # empty context
+    ((1, 4, 4, 64, [1, 10], 4), la.LA_ERR_INVALID),             # cu[0] != 0
+    ((1, 4, 4, 96, [0, 10], 4), la.LA_ERR_UNSUPPORTED),         # no LeanTile for d = 96
+    ((1, 64, 4, 64, [0, 10], 4), la.LA_ERR_UNSUPPORTED),        # group of 16 not built
+])
+def test_plan_rejects_bad_shapes(args, status):
+    with pytest.raises(la.LeanAttentionError) as e:
+        la.la_plan(*args)
+    assert e.value.status == status
+
+
+def test_plan_rejects_empty_batch_and_null_offsets_through_the_c_abi():
+    h = ctypes.c_void_p()
+    cu = np.array([0], np.int32)
+    assert la._lib.la_plan(0, 4, 4, 64, cu.ctypes.data_as(ctypes.c_void_p), 4, ctypes.byref(h)) == la.LA_ERR_INVALID
+    assert la._lib.la_plan(1, 4, 4, 64, None, 4, ctypes.byref(h)) == la.LA_ERR_INVALID
+    assert la._lib.la_plan(1, 4, 4, 64, cu.ctypes.data_as(ctypes.c_void_p), 4, None) == la.LA_ERR_INVALID
+    assert la._lib.la_plan_fixed(1, 4, 4, 64, cu.ctypes.data_as(ctypes.c_void_p), 0, ctypes.byref(h)) == la.LA_ERR_INVALID
+    assert not h.value
+
+
+def test_decode_rejects_bad_pointers_before_any_launch():
+    s = la.la_plan(1, 4, 4, 64, [0, 1024], 3)
+    lib = la._lib
+    vp = ctypes.c_void_p
+    good = vp(0x10000)  # never dereferenced: validation fails first
+    odd = vp(0x10008)
+    ws = vp(0x20000)
+    # null inputs
+    assert lib.la_decode(None, good, good, 0, good, s.handle, ws, good, 0.125, None) == la.LA_ERR_INVALID
+    # misaligned k (bulk copies need 16-byte alignment)
+    assert lib.la_decode(good, odd, good, 0, good, s.handle, ws, good, 0.125, None) == la.LA_ERR_INVALID
+    # bad dtype
+    assert lib.la_decode(good, good, good, 7, good, s.handle, ws, good, 0.125, None) == la.LA_ERR_INVALID
+    # NaN scale
+    assert lib.la_decode(good, good, good, 0, good, s.handle, ws, good, float("nan"), None) == la.LA_ERR_INVALID
+    # missing / misaligned workspace
+    assert lib.la_decode(good, good, good, 0, good, s.handle, None, good, 0.125, None) == la.LA_ERR_WORKSPACE
+    assert lib.la_decode(good, good, good, 0, good, s.handle, vp(0x20010), good, 0.125, None) == la.LA_ERR_WORKSPACE
+    # no schedule
+    assert lib.la_decode(good, good, good, 0, good, None, ws, good, 0.125, None) == la.LA_ERR_INVALID
+
+
+def test_workspace_size_formula():
+    s = la.la_plan(1, 4, 4, 64, [0, 1024], 3)
+    # header 256 + flags (3 words padded to 256) + 3 records of 1 x (64 + 2) floats
+    assert la.la_workspace_size(s) == 256 + 256 + 3 * 66 * 4
+    g = la.la_plan(2, 16, 2, 128, [0, 100, 300], 5)
+    assert la.la_workspace_size(g) == 256 + 256 + 5 * 8 * 130 * 4
+
+
+def test_export_size_and_short_buffer():
+    s = la.la_plan(1, 4, 4, 64, [0, 1024], 3)
+    n = la._lib.la_schedule_export_size(s.handle)
+    buf = (ctypes.c_int32 * n)()
+    assert la._lib.la_schedule_export(s.handle, buf, n - 1) == la.LA_ERR_INVALID
+    assert la._lib.la_schedule_export(s.handle, buf, n) == la.LA_OK
+
+
+def test_status_strings():
+    for code in range(6):
+        assert la.status_string(code)

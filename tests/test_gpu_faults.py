@@ -1,0 +1,59 @@
+"""Failure detection on the GPU without faulting it: a bounded wait that is
+made to run out (a ready flag that is never set), and device offsets that
+disagree with the schedule. Both must come back as a status the host reads,
+with the GPU context still usable afterwards."""
+import numpy as np
+import pytest
+import torch
+
+import decode_phase_attention_gb300 as la
+import workloads
+from _parity import compare, reference
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def test_missing_ready_flag_times_out_and_poisons_only_that_unit():
+    w = workloads.custom(1, 4, 4, 64, "f16", [4096])  # 16 tiles per head, I = 64
+    q, k, v, _ = workloads.make_inputs(w, seed=4, device="cuda")
+    ref = reference(w, q, k, v)
+    dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, w.cu, num_sms=5)
+    exp = la.la_schedule_export(dec.sched)
+    G, U, nseg = exp[1], exp[2], exp[5]
+    base = 8 + 2 * (G + 1) + (U + 1)
+    segs = [exp[base + 5 * i: base + 5 * i + 5] for i in range(nseg)]
+    host = next(s for s in segs if s[3] == la.SEG_HOST)
+    unit, fin = host[0], host[4]
+    la.la_schedule_set_debug(dec.sched, skip_signal_cta=fin, spin_timeout_ns=50_000_000)
+    out = dec(q, k, v, w.scale)
+    assert dec.status() == la.LA_ERR_TIMEOUT
+    got = out.cpu().double().numpy().reshape(ref.shape)
+    bad = np.isnan(got).any(axis=1)
+    assert bad[unit] and bad.sum() == 1  # kv head == query head here
+    compare(np.delete(got, unit, axis=0), np.delete(ref, unit, axis=0))
+    # the context and the workspace stay usable
+    la.la_schedule_set_debug(dec.sched, skip_signal_cta=-1, spin_timeout_ns=2_000_000_000)
+    out = dec(q, k, v, w.scale)
+    assert dec.status() == la.LA_OK
+    compare(out.cpu(), ref)
+
+
+def test_device_offsets_that_disagree_with_the_schedule_are_reported():
+    w = workloads.custom(2, 4, 2, 128, "bf16", [1000, 3000])
+    q, k, v, _ = workloads.make_inputs(w, seed=6, device="cuda")
+    dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, w.cu, num_sms=4)
+    wrong = torch.tensor([0, 3000, 4000], dtype=torch.int32, device="cuda")  # same total, other split
+    out = torch.empty(w.batch, w.hq, w.d, device="cuda")
+    la.la_decode(q, k, v, wrong, dec.sched, dec.workspace, out, w.scale)
+    assert dec.status() == la.LA_ERR_INVALID
+    assert torch.isnan(out).all()
+    out = dec(q, k, v, w.scale)
+    assert dec.status() == la.LA_OK
+    compare(out.cpu(), reference(w, q, k, v))

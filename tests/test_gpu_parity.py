@@ -1,0 +1,132 @@
+"""GPU parity: the CUDA library against the float64 oracle on the same
+seeded bytes, through the C ABI (tolerances: max-abs 2e-3, rel-L2 1e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import decode_phase_attention_gb300 as la
+import workloads
+from _parity import compare, reference, run_lean
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def capacity(d, grp):
+    per_sm, sms = la.la_device_capacity(d, grp)
+    return per_sm * sms
+
+
+def test_tiny_exact_check_three_ctas_cross_head_boundaries():
+    w = workloads.named("tiny")
+    q, k, v, _ = workloads.make_inputs(w, seed=0, device="cuda")
+    out, dec = run_lean(w, q, k, v, num_sms=3)
+    compare(out.cpu(), reference(w, q, k, v))
+    exp = la.la_schedule_export(dec.sched)
+    assert exp[1] == 3 and exp[3] == 16  # G = 3, I = 16 LeanTiles
+
+
+SMALL = []
+for d in (64, 128):
+    for grp in (1, 2, 4, 8):
+        for dt in ("f16", "bf16"):
+            SMALL.append((d, grp, dt))
+
+
+@pytest.mark.parametrize("d,grp,dt", SMALL)
+@pytest.mark.parametrize("grid", [1, 2, 7, 0])
+def test_small_shapes_ragged_tails(d, grp, dt, grid):
+    lengths = [1, 255, 257, 1000, 128, 129]
+    hkv = 2
+    w = workloads.custom(len(lengths), hkv * grp, hkv, d, dt, lengths)
+    q, k, v, _ = workloads.make_inputs(w, seed=d + grp, device="cuda")
+    out, _ = run_lean(w, q, k, v, num_sms=grid)
+    compare(out.cpu(), reference(w, q, k, v))
+
+
+def test_grid_sweep_up_to_device_capacity():
+    w = workloads.custom(3, 8, 4, 128, "bf16", [700, 3000, 129])
+    q, k, v, _ = workloads.make_inputs(w, seed=5, device="cuda")
+    ref = reference(w, q, k, v)
+    cap = capacity(128, 2)
+    for G in list(range(1, 40)) + [cap // 2, cap - 1, cap]:
+        out, _ = run_lean(w, q, k, v, num_sms=G)
+        compare(out.cpu(), ref)
+
+
+def test_grid_beyond_residency_is_rejected():
+    w = workloads.custom(1, 4, 4, 64, "f16", [4096])
+    cap = capacity(64, 1)
+    s = la.la_plan(1, 4, 4, 64, w.cu, cap + 1)
+    q, k, v, _ = workloads.make_inputs(w, device="cuda")
+    ws = la.new_workspace(s)
+    out = torch.empty(1, 4, 64, device="cuda")
+    cu = torch.as_tensor(w.cu, device="cuda")
+    with pytest.raises(la.LeanAttentionError) as e:
+        la.la_decode(q, k, v, cu, s, ws, out, w.scale)
+    assert e.value.status == la.LA_ERR_INVALID
+
+
+def test_zero_query_gives_the_mean_of_v():
+    w = workloads.custom(2, 8, 8, 128, "bf16", [5000, 777])
+    q, k, v, _ = workloads.make_inputs(w, seed=1, device="cuda")
+    q.zero_()
+    out, _ = run_lean(w, q, k, v)
+    for b in range(w.batch):
+        L, off0 = w.lengths[b], int(w.cu[b]) * w.hkv * w.d
+        slab = v[off0:off0 + w.hkv * L * w.d].double().reshape(w.hkv, L, w.d)
+        np.testing.assert_allclose(out[b].double().cpu().numpy(), slab.mean(dim=1).cpu().numpy(),
+                                   atol=2e-3, rtol=0)
+
+
+def test_one_hot_scores_select_one_value_row():
+    w = workloads.custom(1, 4, 4, 64, "f16", [3000])
+    q, k, v, _ = workloads.make_inputs(w, seed=2, device="cuda")
+    j = 2345
+    kk = k.view(w.hkv, 3000, w.d)
+    q.copy_((kk[:, j, :].float() * 4.0).to(q.dtype).view(1, w.hkv, w.d))
+    out, _ = run_lean(w, q, k, v, scale=1.0)
+    vv = v.view(w.hkv, 3000, w.d)[:, j, :].float()
+    torch.testing.assert_close(out[0], vv, atol=2e-3, rtol=0)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 16])
+def test_fixed_partition_baselines(splits):
+    w = workloads.custom(4, 16, 4, 128, "bf16", [10000, 300, 4097, 128])
+    q, k, v, _ = workloads.make_inputs(w, seed=9, device="cuda")
+    out, _ = run_lean(w, q, k, v, fixed_splits=splits)
+    compare(out.cpu(), reference(w, q, k, v))
+
+
+def test_repeated_calls_and_two_schedules_sharing_one_workspace():
+    w = workloads.custom(2, 8, 8, 64, "f16", [3000, 5000])
+    q, k, v, _ = workloads.make_inputs(w, seed=3, device="cuda")
+    ref = reference(w, q, k, v)
+    s1 = la.la_plan(w.batch, w.hq, w.hkv, w.d, w.cu, 13)
+    s2 = la.la_plan(w.batch, w.hq, w.hkv, w.d, w.cu, 29)
+    ws = la.new_workspace(s2)  # the larger of the two
+    assert ws.numel() >= la.la_workspace_size(s1)
+    cu = torch.as_tensor(w.cu, device="cuda")
+    out = torch.empty(w.batch, w.hq, w.d, device="cuda")
+    for i in range(12):
+        out.fill_(float("nan"))
+        la.la_decode(q, k, v, cu, s1 if i % 3 else s2, ws, out, w.scale)
+        compare(out.cpu(), ref)
+    assert la.la_get_status(ws) == la.LA_OK
+
+
+# ---- the named workloads, in the launch configuration the benchmark times
+@pytest.mark.parametrize("name", ["uniform", "long64k", "long256k", "long512k", "ragged", "gqa"])
+def test_named_workloads_full_output(name):
+    w = workloads.named(name)
+    q, k, v, _ = workloads.make_inputs(w, seed=0, device="cuda")
+    out, dec = run_lean(w, q, k, v)
+    compare(out.cpu(), reference(w, q, k, v))
+    del q, k, v
+    torch.cuda.empty_cache()
