@@ -19,7 +19,7 @@ LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_W
 LA_F16, LA_BF16 = 0, 1
 SEG_WHOLE, SEG_NONHOST, SEG_HOST, SEG_PARTIAL = range(4)
 EXPORTED = ["la_plan", "la_plan_fixed", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
-            "la_decode", "la_get_status", "la_schedule_export_size", "la_schedule_export",
+            "la_decode", "la_decode_static", "la_get_status", "la_schedule_export_size", "la_schedule_export",
             "la_schedule_set_debug", "la_device_capacity", "la_schedule_destroy",
             "la_status_string"]
 
@@ -44,6 +44,7 @@ def _load():
         "la_workspace_size": (c_size, [vp]),
         "la_workspace_init": (c_int, [vp, c_size, vp]),
         "la_decode": (c_int, [vp, vp, vp, c_int, vp, vp, vp, vp, c_float, vp]),
+        "la_decode_static": (c_int, [vp, vp, vp, c_int, vp, vp, vp, c_float, vp]),
         "la_get_status": (c_int, [vp, vp]),
         "la_schedule_export_size": (c_size, [vp]),
         "la_schedule_export": (c_int, [vp, vp, c_size]),
@@ -201,6 +202,38 @@ def la_decode(q, k, v, cu_seqlens_k, sched, workspace, out, scale, stream=None):
                           ctypes.c_void_p(cu_seqlens_k.data_ptr()), sched.handle,
                           ctypes.c_void_p(workspace.data_ptr()), ctypes.c_void_p(out.data_ptr()),
                           float(scale), _stream_handle(stream)), "la_decode")
+    return out
+
+
+def la_decode_static(q, k, v, cu_seqlens_k, sched, out, scale, stream=None):
+    """la_decode without a workspace or any device allocation.
+
+    For callers that cannot allocate device memory (a plugin without access
+    to its host program's allocator, or a serving loop whose HBM is all
+    reserved up front). The scratch lives in a fixed 4 MiB array inside the
+    library that every call shares: do not let two calls overlap on the
+    GPU. In-kernel failures show up as NaN outputs (there is no status word).
+    """
+    import torch
+    if not (q.is_cuda and k.is_cuda and v.is_cuda and out.is_cuda and cu_seqlens_k.is_cuda):
+        raise ValueError("la_decode_static takes device tensors")
+    dt = {torch.float16: LA_F16, torch.bfloat16: LA_BF16}.get(q.dtype)
+    if dt is None or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, float16 or bfloat16")
+    if out.dtype != torch.float32 or cu_seqlens_k.dtype != torch.int32:
+        raise ValueError("out must be float32 and cu_seqlens_k int32")
+    b, hq, hkv, d = sched.batch, sched.hq, sched.hkv, sched.d
+    kv_elems = int(sched.cu[-1]) * hkv * d
+    if not all(t.is_contiguous() for t in (q, k, v, out, cu_seqlens_k)):
+        raise ValueError("tensors must be contiguous")
+    if (q.numel() != b * hq * d or out.numel() != b * hq * d or k.numel() < kv_elems
+            or v.numel() < kv_elems or cu_seqlens_k.numel() != b + 1):
+        raise ValueError("tensor sizes do not match the schedule")
+    _check(_lib.la_decode_static(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                                 ctypes.c_void_p(v.data_ptr()), dt,
+                                 ctypes.c_void_p(cu_seqlens_k.data_ptr()), sched.handle,
+                                 ctypes.c_void_p(out.data_ptr()), float(scale),
+                                 _stream_handle(stream)), "la_decode_static")
     return out
 
 

@@ -21,24 +21,8 @@
 #include <vector>
 
 #include "la_internal.h"
+#include "la_schedule.h"
 #include "lean_attn.h"
-
-struct la_schedule {
-  int batch = 0, hq = 0, hkv = 0, d = 0, grp = 0, T = 0;
-  int kind = 0;    // 0 stream-K, 1 fixed
-  int splits = 0;  // fixed partitions only
-  int G = 0, U = 0;
-  int64_t I = 0;
-  std::vector<int32_t> cu, cta_iter, unit_iter, cta_seg, segs, unit_host, unit_fin;
-  // debug hooks
-  int skip_signal = -1;
-  long long spin_ns = 2000000000LL;
-  // device copy: [cu (batch+1)] [cta_seg (G+1)] [segs] [unit_host (U)] [unit_fin (U)]
-  std::mutex mu;
-  int device = -1;
-  int32_t* dev = nullptr;
-  size_t off_cu = 0, off_cta_seg = 0, off_segs = 0, off_host = 0, off_fin = 0;
-};
 
 namespace {
 

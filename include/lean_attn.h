@@ -151,6 +151,37 @@ la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt,
                     float* out, float scale, la_stream_t stream);
 
 /*
+ * la_decode_static -- la_decode without a workspace and without any device
+ * allocation. The paper has no counterpart: this is a library convenience.
+ *
+ * Some callers cannot allocate device memory: a plugin loaded into a host
+ * program whose allocator it cannot reach, or a serving loop that reserves
+ * all of HBM for its KV cache up front and must not call cudaMalloc (which
+ * can synchronise the device) while it decodes. This call keeps the
+ * kernel's scratch (ready flags, partial records and the schedule's
+ * tables) in one fixed 4 MiB array of device memory built into the
+ * library; every GPU that loads the library holds that array until the
+ * process exits. Arguments are those of la_decode minus the workspace.
+ *
+ *   - A schedule whose scratch does not fit in 4 MiB is rejected with
+ *     LA_ERR_WORKSPACE before anything is enqueued (about 7,000 CTA records
+ *     at d = 128 without query-head grouping; use la_decode for more).
+ *   - The first call on a device looks up the array's address on that
+ *     device (cudaGetSymbolAddress) with the device current; make that
+ *     first call before any stream capture.
+ *   - Each call clears the flags and copies the schedule's tables from
+ *     host memory into the array on `stream`, then launches the same
+ *     kernel(s) as la_decode. All calls share the one array, which keeps
+ *     the previous call's contents: calls that can overlap on the GPU (on
+ *     different streams, or from several threads) race, so serialise them.
+ *   - There is no status word to read back: a failure detected inside the
+ *     kernel shows up as NaN outputs.
+ */
+la_status la_decode_static(const void* q, const void* k, const void* v, la_dtype dt,
+                           const int32_t* cu_seqlens_k_dev, const la_schedule* s, float* out,
+                           float scale, la_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the first error a kernel
  * recorded in `workspace` since the last call (LA_OK if none). Meant for
  * tests and error handling, not for the hot loop.
