@@ -11,6 +11,7 @@
 //   "4.3 work distribution"     fixed partitions (FlashAttention-2,
 //                               FlashDecoding) for the baselines
 // The planner walks CTA ranges arithmetically in O(G + units).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -236,6 +237,46 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 }  // namespace
 
+namespace la {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda), looked up once.
+cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, int T, int elem_type,
+                           CUtensorMap* mk, CUtensorMap* mv) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static std::mutex mu;
+  static Encode fn = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (fn == nullptr) {
+      void* ptr = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || ptr == nullptr)
+        return cudaErrorNotSupported;
+      fn = reinterpret_cast<Encode>(ptr);
+    }
+  }
+  if (rows <= 0 || rows > (1LL << 31) - 1) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)T};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = (CUtensorMapDataType)elem_type;
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = fn(i == 0 ? mk : mv, dt, 2, const_cast<void*>(i == 0 ? k : v), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace la
+
 extern "C" {
 
 la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int num_sms,
@@ -311,6 +352,7 @@ la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt, co
   p.hdr = reinterpret_cast<uint32_t*>(ws);
   p.flags = reinterpret_cast<uint32_t*>(ws + la::kHeaderBytes);
   p.recs = reinterpret_cast<float*>(ws + la::kHeaderBytes + la::flags_bytes(s->G));
+  p.kv_rows = (long long)s->hkv * s->cu[s->batch];
   p.G = s->G;
   p.batch = s->batch;
   p.hq = s->hq;

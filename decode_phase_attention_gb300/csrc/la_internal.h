@@ -38,6 +38,7 @@ struct KParams {
   uint32_t* hdr;
   uint32_t* flags;
   float* recs;
+  long long kv_rows;        // hkv * total tokens: rows of K (and V) seen as [rows, d]
   int G;
   int batch;
   int hq;

@@ -15,22 +15,30 @@
 // Warp roles (288 threads, one CTA per SM):
 //   warp 8, lane 0: producer. Streams the K and V rows of each LeanTile of
 //                   every segment, in order, from HBM into a 3-stage
-//                   shared-memory ring with 1-D bulk async copies
-//                   (cp.async.bulk, completion counted in bytes on an
-//                   mbarrier). A tile's K rows (and V rows) are contiguous
-//                   in the [hkv, L, d] slab, so one copy moves all of them.
-//   warps 0-7:      consumers. Each takes T/8 consecutive tokens of the
-//                   tile; d/8 lanes share one token (8 elements = 16 bytes
-//                   per lane, so a warp reads whole rows without bank
-//                   conflicts). Scores q.k are reduced across those lanes
-//                   with shuffles, the running max / sum are updated online
-//                   ("3.3 LeanTile": online softmax statistics m, l, then
-//                   O_acc = P V + diag(rescale) O_acc), and P.V accumulates
-//                   in fp32 registers.
-// At the end of a segment the lane groups of a warp merge by shuffles and
-// the 8 warps merge through shared memory, both with f.
+//                   shared-memory ring (completion counted in bytes on one
+//                   mbarrier per stage).
+//   warps 0-7:      consumers. Each takes T/8 consecutive tokens of the tile
+//                   and keeps online-softmax statistics m, l and the
+//                   unnormalised output in fp32 ("3.3 LeanTile": S_f = Q K^T,
+//                   update m and l, O_acc = P V + diag(rescale) O_acc).
+// Two tile paths:
+//   CUDA cores (query-head group 1 or 2, about 1-2 flop per K/V byte): a
+//     tile's K rows (and V rows) are one contiguous run of the [hkv, L, d]
+//     slab, moved by a 1-D bulk copy (cp.async.bulk). d/8 lanes share one
+//     token (16 bytes each, whole rows per warp, no bank conflicts); q.k is
+//     reduced across them with shuffles, P.V accumulates in registers.
+//   tensor cores (group 4 or 8, up to 8 flop per byte, which would saturate
+//     the fp32 pipes): tiles arrive by 2-D TMA (cp.async.bulk.tensor) with
+//     128-byte swizzle, so ldmatrix reads are conflict-free. With the query
+//     heads of the group as the N = 8 side of an m16n8k16 MMA, S = K q^T
+//     (tokens x heads) and O^T = V^T P (dims x heads) need no padding rows;
+//     P moves from the accumulator layout to the operand layout with
+//     movmatrix, and is split into a bf16/fp16 high and low part so that
+//     the P.V product keeps fp32-level accuracy.
+// At the end of a segment the lanes of a warp and then the 8 warps merge
+// with f (the warps through shared memory).
 //
-// Scores are kept in base-2 units: q is pre-multiplied by scale*log2(e) so
+// Scores are kept in base-2 units: scale*log2(e) multiplies q.k so that
 // exp(s - m) becomes ex2(s2 - m2); m in the workspace records is in the
 // same units (the records are internal to this kernel).
 //
@@ -40,9 +48,11 @@
 // its copies still in flight, and the affected outputs are written as NaN.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "la_internal.h"
 
@@ -89,6 +99,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// 2-D tiled TMA load of box (x, y) of tensor map `tmap` into shared memory.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tmap, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -115,6 +137,21 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x; ex2(-inf) = 0
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ void ldsm_x4(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
 
 // ------------------------------------------------------------ element types
 template <typename E>
@@ -130,6 +167,22 @@ struct Elem<__nv_bfloat16> {
       f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
   }
+  // Pack (lo, hi) into a bf16x2 register, round to nearest even.
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ float2 unpack(uint32_t x) {
+    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+  }
+  __device__ static __forceinline__ void mma(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 };
 template <>
 struct Elem<__half> {
@@ -143,30 +196,52 @@ struct Elem<__half> {
       f[2 * i + 1] = t.y;
     }
   }
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static __forceinline__ float2 unpack(uint32_t x) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&x));
+  }
+  __device__ static __forceinline__ void mma(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 };
 
 // ------------------------------------------------------------ configuration
 template <int D, int GRP>
 struct Cfg {
   static constexpr int T = (D == 64) ? 256 : 128;  // LeanTile ("3.3 LeanTile" table)
+  static constexpr bool TC = (GRP >= 4);            // tensor-core tile path
   static constexpr int NCW = 8;                     // consumer warps
   static constexpr int NCT = NCW * 32;              // consumer threads
   static constexpr int NTHREADS = NCT + 32;         // + producer warp
+  static constexpr int TPW = T / NCW;               // tokens per warp per tile
+  // CUDA-core path
   static constexpr int LPT = D / 8;                 // lanes per token
   static constexpr int TPS = 32 / LPT;              // tokens per warp step
-  static constexpr int TPW = T / NCW;               // tokens per warp per tile
   static constexpr int STEPS = TPW / TPS;
   static constexpr int CH = (GRP <= 2) ? STEPS : (GRP == 4 ? 4 : 2);  // steps per softmax update
+  // tensor-core path
+  static constexpr int MT = TPW / 16;               // 16-token MMA tiles per warp
+  static constexpr int KS = D / 16;                 // 16-wide k steps over the head dim
+  static constexpr int NB = D / 64;                 // 64-column (128-byte) swizzled blocks
   static constexpr int STAGES = 3;
   static constexpr int TILE_ELEMS = T * D;
   static constexpr size_t KV_BYTES = (size_t)STAGES * 2 * TILE_ELEMS * 2;
   static constexpr int REC = D + 2;                 // [m, l, O[d]]
   static constexpr size_t MERGE_BYTES = (size_t)NCW * GRP * REC * 4;
   static constexpr size_t BAR_BYTES = 2 * STAGES * 8 + 16;
-  static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES;
+  static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES + (TC ? 1024 : 0);
   static constexpr int ITEMS = (GRP * D + NCT - 1) / NCT;  // (head, dim) outputs per consumer thread
   static_assert(STEPS % CH == 0, "chunking");
   static_assert(TPW % TPS == 0, "tokens per warp");
+  static_assert(!TC || (TPW % 16 == 0 && GRP <= 8), "tensor-core tile shape");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
@@ -201,10 +276,14 @@ __device__ __forceinline__ bool unit_offsets_ok(const KParams& p, int b) {
 
 // ------------------------------------------------------------------ producer
 template <int D, int GRP, typename E>
-__device__ __forceinline__ void produce(const KParams& p, int g, E* kv, uint64_t* full, uint64_t* empty,
-                                        volatile int* abort_flag) {
+__device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, int g,
+                                        E* kv, uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
   using C = Cfg<D, GRP>;
   const uint64_t pol = l2_evict_first_policy();
+  if (C::TC) {
+    prefetch_tmap(tmk);
+    prefetch_tmap(tmv);
+  }
   const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
   int stage = 0;
   uint32_t phase = 1;  // a fresh barrier counts its previous (odd) phase as complete
@@ -216,9 +295,7 @@ __device__ __forceinline__ void produce(const KParams& p, int g, E* kv, uint64_t
     const int b = unit / p.hkv, kvh = unit % p.hkv;
     if (!unit_offsets_ok(p, b)) continue;  // consumers skip the same segment
     const long long L = (long long)p.cu[b + 1] - p.cu[b];
-    const long long base = ((long long)p.hkv * p.cu[b] + (long long)kvh * L) * D;
-    const E* kb = static_cast<const E*>(p.k) + base;
-    const E* vb = static_cast<const E*>(p.v) + base;
+    const long long row0 = (long long)p.hkv * p.cu[b] + (long long)kvh * L;  // first row of the slab
     for (int t = t0; t < t1; ++t) {
       const long long rem = L - (long long)t * C::T;
       const int ntok = rem < C::T ? (int)rem : C::T;
@@ -228,11 +305,25 @@ __device__ __forceinline__ void produce(const KParams& p, int g, E* kv, uint64_t
         aborted = true;
         break;
       }
-      const uint32_t bytes = (uint32_t)ntok * D * 2u;
-      mbar_arrive_expect_tx(&full[stage], 2u * bytes);
       E* ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
-      bulk_g2s(ks, kb + (long long)t * C::T * D, bytes, &full[stage], pol);
-      bulk_g2s(ks + C::TILE_ELEMS, vb + (long long)t * C::T * D, bytes, &full[stage], pol);
+      if (C::TC) {
+        // Whole boxes of T rows: rows past the slab are the next slab's (or
+        // zero fill past the tensor) and are masked by the consumers.
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * C::TILE_ELEMS * 2));
+        const int y = (int)(row0 + (long long)t * C::T);
+#pragma unroll
+        for (int bk = 0; bk < C::NB; ++bk) {
+          tma_load_2d(ks + bk * C::T * 64, tmk, bk * 64, y, &full[stage], pol);
+          tma_load_2d(ks + C::TILE_ELEMS + bk * C::T * 64, tmv, bk * 64, y, &full[stage], pol);
+        }
+      } else {
+        const uint32_t bytes = (uint32_t)ntok * D * 2u;
+        mbar_arrive_expect_tx(&full[stage], 2u * bytes);
+        const E* src_k = static_cast<const E*>(p.k) + (row0 + (long long)t * C::T) * D;
+        const E* src_v = static_cast<const E*>(p.v) + (row0 + (long long)t * C::T) * D;
+        bulk_g2s(ks, src_k, bytes, &full[stage], pol);
+        bulk_g2s(ks + C::TILE_ELEMS, src_v, bytes, &full[stage], pol);
+      }
       ++issued;
       if (++stage == C::STAGES) {
         stage = 0;
@@ -253,16 +344,336 @@ __device__ __forceinline__ void produce(const KParams& p, int g, E* kv, uint64_t
   }
 }
 
-// ------------------------------------------------------------------ consumers
+// Wait for the next stage; false (for the whole warp) if it never came.
+template <int D, int GRP>
+__device__ __forceinline__ bool wait_tile(const KParams& p, int g, uint64_t* full, int stage, uint32_t phase,
+                                          volatile int* abort_flag, int lane) {
+  bool have = mbar_wait_bounded(&full[stage], phase, abort_flag, p.spin_ns);
+  have = __all_sync(kFull, have);
+  if (!have && lane == 0) {
+    if (!*abort_flag) record_error(p.hdr, kStatusTimeout, g, -1);
+    *abort_flag = 1;
+  }
+  return have;
+}
+
+// ----------------------------------------------- CUDA-core tile path (grp 1, 2)
+// Runs the segment's tiles and leaves this warp's (m, l, O) for every head
+// of the group in its slot of the merge area.
 template <int D, int GRP, typename E>
-__device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, uint64_t* full,
-                                        uint64_t* empty, float* mrg, volatile int* abort_flag,
-                                        uint32_t epoch) {
+__device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, int kvh, long long L, int t0,
+                                                int n_tiles, const E* kv, uint64_t* full, uint64_t* empty,
+                                                int& stage, uint32_t& phase, volatile int* abort_flag,
+                                                float* wrec) {
   using C = Cfg<D, GRP>;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gl = lane % C::LPT;  // which 8-element chunk of the row
   const int ts = lane / C::LPT;  // which token of the warp step
   const int c0 = gl * 8;
+
+  float qf[GRP][8];
+#pragma unroll
+  for (int j = 0; j < GRP; ++j) {
+    const int h = kvh * GRP + j;
+    const uint4 raw =
+        *reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) + ((size_t)b * p.hq + h) * D + c0);
+    Elem<E>::to_f32(raw, qf[j]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qf[j][e] *= p.qscale;
+  }
+  float m[GRP], l[GRP], o[GRP][8];
+#pragma unroll
+  for (int j = 0; j < GRP; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[j][e] = 0.f;
+  }
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const long long rem = L - (long long)(t0 + it) * C::T;
+    const int ntok = rem < C::T ? (int)rem : C::T;
+    if (wait_tile<D, GRP>(p, g, full, stage, phase, abort_flag, lane)) {
+      const E* Ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
+      const E* Vs = Ks + C::TILE_ELEMS;
+      const int wtok = warp * C::TPW;
+#pragma unroll
+      for (int c = 0; c < C::STEPS; c += C::CH) {
+        float s[C::CH][GRP];
+#pragma unroll
+        for (int st = 0; st < C::CH; ++st) {
+          const int tok = wtok + (c + st) * C::TPS + ts;
+          const uint4 raw = *reinterpret_cast<const uint4*>(Ks + tok * D + c0);
+          float kf[8];
+          Elem<E>::to_f32(raw, kf);
+#pragma unroll
+          for (int j = 0; j < GRP; ++j) {
+            float a0 = qf[j][0] * kf[0], a1 = qf[j][1] * kf[1];
+#pragma unroll
+            for (int e = 2; e < 8; e += 2) {
+              a0 = fmaf(qf[j][e], kf[e], a0);
+              a1 = fmaf(qf[j][e + 1], kf[e + 1], a1);
+            }
+            s[st][j] = a0 + a1;
+          }
+        }
+#pragma unroll
+        for (int st = 0; st < C::CH; ++st)
+#pragma unroll
+          for (int j = 0; j < GRP; ++j)
+#pragma unroll
+            for (int off = C::LPT / 2; off >= 1; off >>= 1) s[st][j] += __shfl_xor_sync(kFull, s[st][j], off);
+#pragma unroll
+        for (int st = 0; st < C::CH; ++st) {
+          const int tok = wtok + (c + st) * C::TPS + ts;
+          if (tok >= ntok) {
+#pragma unroll
+            for (int j = 0; j < GRP; ++j) s[st][j] = -INFINITY;
+          }
+        }
+        // online softmax: new max, rescale, exponentiate
+#pragma unroll
+        for (int j = 0; j < GRP; ++j) {
+          float mx = s[0][j];
+#pragma unroll
+          for (int st = 1; st < C::CH; ++st) mx = fmaxf(mx, s[st][j]);
+          const float mn = fmaxf(m[j], mx);
+          if (mn == -INFINITY) {
+#pragma unroll
+            for (int st = 0; st < C::CH; ++st) s[st][j] = 0.f;
+            continue;
+          }
+          const float alpha = ex2(m[j] - mn);
+          m[j] = mn;
+          l[j] *= alpha;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[j][e] *= alpha;
+#pragma unroll
+          for (int st = 0; st < C::CH; ++st) {
+            const float pj = ex2(s[st][j] - mn);
+            s[st][j] = pj;
+            l[j] += pj;
+          }
+        }
+        // P.V
+#pragma unroll
+        for (int st = 0; st < C::CH; ++st) {
+          const int tok = wtok + (c + st) * C::TPS + ts;
+          if (tok < ntok) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(Vs + tok * D + c0);
+            float vf[8];
+            Elem<E>::to_f32(raw, vf);
+#pragma unroll
+            for (int j = 0; j < GRP; ++j)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[j][e] = fmaf(s[st][j], vf[e], o[j][e]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == C::STAGES) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+
+  // merge the token slots of the warp (lanes with equal gl) with f
+#pragma unroll
+  for (int off = C::LPT; off < 32; off <<= 1) {
+#pragma unroll
+    for (int j = 0; j < GRP; ++j) {
+      const float mo = __shfl_xor_sync(kFull, m[j], off);
+      const float lo = __shfl_xor_sync(kFull, l[j], off);
+      const float mn = fmaxf(m[j], mo);
+      const float a = (m[j] == -INFINITY) ? 0.f : ex2(m[j] - mn);
+      const float bw = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
+      l[j] = a * l[j] + bw * lo;
+      m[j] = mn;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float oo = __shfl_xor_sync(kFull, o[j][e], off);
+        o[j][e] = a * o[j][e] + bw * oo;
+      }
+    }
+  }
+  if (ts == 0) {
+#pragma unroll
+    for (int j = 0; j < GRP; ++j) {
+      float* r = wrec + j * C::REC;
+      if (gl == 0) {
+        r[0] = m[j];
+        r[1] = l[j];
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[2 + c0 + e] = o[j][e];
+    }
+  }
+}
+
+// -------------------------------------------- tensor-core tile path (grp 4, 8)
+// Swizzled shared-memory address (128-byte swizzle: 16-byte chunk c of row r
+// sits at chunk c ^ (r mod 8)) of row `row`, chunk `c` of 64-column block bk.
+template <int D, int GRP>
+__device__ __forceinline__ uint32_t swz(uint32_t tile_base, int bk, int row, int c) {
+  using C = Cfg<D, GRP>;
+  return tile_base + (uint32_t)(bk * C::T * 128 + row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+template <int D, int GRP, typename E>
+__device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, int kvh, long long L, int t0,
+                                                int n_tiles, const E* kv, uint64_t* full, uint64_t* empty,
+                                                int& stage, uint32_t& phase, volatile int* abort_flag,
+                                                float* wrec) {
+  using C = Cfg<D, GRP>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gq = lane >> 2;  // fragment row group
+  const int tq = lane & 3;   // fragment column pair
+  // B operand of S = K q^T: q^T (16 dims x 8 heads), raw q bits; heads past
+  // the group are zero columns that are never written out.
+  uint32_t qb[C::KS][2];
+  {
+    const bool live = gq < GRP;
+    const uint32_t* qrow =
+        reinterpret_cast<const uint32_t*>(static_cast<const E*>(p.q) + ((size_t)b * p.hq + kvh * GRP + (live ? gq : 0)) * D);
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ++ks) {
+      qb[ks][0] = live ? qrow[(ks * 16 + 2 * tq) / 2] : 0u;
+      qb[ks][1] = live ? qrow[(ks * 16 + 2 * tq + 8) / 2] : 0u;
+    }
+  }
+  // State for heads 2tq and 2tq+1: m (uniform over the 8 row groups), the
+  // thread's share of l, and O^T fragments (dims x heads).
+  float m[2] = {-INFINITY, -INFINITY};
+  float l[2] = {0.f, 0.f};
+  float o[C::KS][4];
+#pragma unroll
+  for (int dm = 0; dm < C::KS; ++dm)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[dm][i] = 0.f;
+
+  const uint32_t kv_base = smem_u32(kv);
+  for (int it = 0; it < n_tiles; ++it) {
+    const long long rem = L - (long long)(t0 + it) * C::T;
+    const int ntok = rem < C::T ? (int)rem : C::T;
+    if (wait_tile<D, GRP>(p, g, full, stage, phase, abort_flag, lane)) {
+      const uint32_t kb = kv_base + (uint32_t)(stage * 2 * C::TILE_ELEMS * 2);
+      const uint32_t vb = kb + (uint32_t)(C::TILE_ELEMS * 2);
+      const int wtok = warp * C::TPW;
+      // S = K q^T for the warp's TPW tokens: MT tiles of 16 tokens x 8 heads
+      float s[C::MT][4];
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[mt][i] = 0.f;
+        const int row = wtok + mt * 16 + (lane & 15);
+#pragma unroll
+        for (int ks = 0; ks < C::KS; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(a, swz<D, GRP>(kb, ks >> 2, row, (ks & 3) * 2 + (lane >> 4)));
+          Elem<E>::mma(s[mt], a, qb[ks][0], qb[ks][1]);
+        }
+      }
+      // scale to base-2 units, mask tokens past the context
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = wtok + mt * 16 + gq + ((i & 2) ? 8 : 0);
+          s[mt][i] = (tok < ntok) ? s[mt][i] * p.qscale : -INFINITY;
+          mx[i & 1] = fmaxf(mx[i & 1], s[mt][i]);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 4));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 8));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 16));
+      }
+      float mn[2], alpha[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mn[h] = fmaxf(m[h], mx[h]);
+        alpha[h] = (m[h] == -INFINITY) ? 0.f : ex2(m[h] - mn[h]);
+        if (mn[h] == -INFINITY) alpha[h] = 1.f;  // nothing seen yet
+        m[h] = mn[h];
+        l[h] *= alpha[h];
+      }
+#pragma unroll
+      for (int dm = 0; dm < C::KS; ++dm) {
+        o[dm][0] *= alpha[0];
+        o[dm][1] *= alpha[1];
+        o[dm][2] *= alpha[0];
+        o[dm][3] *= alpha[1];
+      }
+      // P = 2^(s - m), split into high and low 16-bit parts; O^T += V^T P
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt) {
+        float pv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float mi = mn[i & 1];
+          pv[i] = (mi == -INFINITY) ? 0.f : ex2(s[mt][i] - mi);
+          l[i & 1] += pv[i];
+        }
+        const uint32_t h01 = Elem<E>::pack(pv[0], pv[1]);
+        const uint32_t h23 = Elem<E>::pack(pv[2], pv[3]);
+        const float2 f01 = Elem<E>::unpack(h01), f23 = Elem<E>::unpack(h23);
+        const uint32_t l01 = Elem<E>::pack(pv[0] - f01.x, pv[1] - f01.y);
+        const uint32_t l23 = Elem<E>::pack(pv[2] - f23.x, pv[3] - f23.y);
+        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+        const int vrow = wtok + mt * 16 + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+        for (int dm = 0; dm < C::KS; ++dm) {
+          uint32_t a[4];
+          ldsm_x4_trans(a, swz<D, GRP>(vb, dm >> 2, vrow, (dm & 3) * 2 + ((lane >> 3) & 1)));
+          Elem<E>::mma(o[dm], a, bh0, bh1);
+          Elem<E>::mma(o[dm], a, bl0, bl1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == C::STAGES) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+
+  // l: sum the shares of the 8 row groups (m is already common to them)
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    l[h] += __shfl_xor_sync(kFull, l[h], 4);
+    l[h] += __shfl_xor_sync(kFull, l[h], 8);
+    l[h] += __shfl_xor_sync(kFull, l[h], 16);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int head = 2 * tq + h;
+    if (head < GRP) {
+      float* r = wrec + head * C::REC;
+      if (gq == 0) {
+        r[0] = m[h];
+        r[1] = l[h];
+      }
+#pragma unroll
+      for (int dm = 0; dm < C::KS; ++dm) {
+        r[2 + dm * 16 + gq] = o[dm][h];
+        r[2 + dm * 16 + gq + 8] = o[dm][2 + h];
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ consumers
+template <int D, int GRP, typename E>
+__device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, uint64_t* full, uint64_t* empty,
+                                        float* mrg, volatile int* abort_flag, uint32_t epoch) {
+  using C = Cfg<D, GRP>;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
   const uint32_t ready = epoch + 1u;
   int stage = 0;
@@ -275,159 +686,14 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
     const bool ok = unit_offsets_ok(p, b);
     if (!ok && tid == 0) record_error(p.hdr, kStatusInvalid, g, unit);
     const long long L = ok ? (long long)p.cu[b + 1] - p.cu[b] : 0;
-
-    // q rows of the GRP query heads that read this kv head, pre-scaled.
-    float qf[GRP][8];
-#pragma unroll
-    for (int j = 0; j < GRP; ++j) {
-      const int h = kvh * GRP + j;
-      const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) +
-                                                        ((size_t)b * p.hq + h) * D + c0);
-      Elem<E>::to_f32(raw, qf[j]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qf[j][e] *= p.qscale;
-    }
-    float m[GRP], l[GRP], o[GRP][8];
-#pragma unroll
-    for (int j = 0; j < GRP; ++j) {
-      m[j] = -INFINITY;
-      l[j] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[j][e] = 0.f;
-    }
-
-    // ---- the LeanTile loop
     const int n_tiles = ok ? t1 - t0 : 0;
-    for (int it = 0; it < n_tiles; ++it) {
-      const int t = t0 + it;
-      const long long rem = L - (long long)t * C::T;
-      const int ntok = rem < C::T ? (int)rem : C::T;
-      bool have = mbar_wait_bounded(&full[stage], phase, abort_flag, p.spin_ns);
-      have = __all_sync(kFull, have);
-      if (!have) {
-        if (lane == 0) {
-          if (!*abort_flag) record_error(p.hdr, kStatusTimeout, g, -1);
-          *abort_flag = 1;
-        }
-      } else {
-        const E* Ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
-        const E* Vs = Ks + C::TILE_ELEMS;
-        const int wtok = warp * C::TPW;
-#pragma unroll
-        for (int c = 0; c < C::STEPS; c += C::CH) {
-          float s[C::CH][GRP];
-#pragma unroll
-          for (int st = 0; st < C::CH; ++st) {
-            const int tok = wtok + (c + st) * C::TPS + ts;
-            const uint4 raw = *reinterpret_cast<const uint4*>(Ks + tok * D + c0);
-            float kf[8];
-            Elem<E>::to_f32(raw, kf);
-#pragma unroll
-            for (int j = 0; j < GRP; ++j) {
-              float a0 = qf[j][0] * kf[0], a1 = qf[j][1] * kf[1];
-#pragma unroll
-              for (int e = 2; e < 8; e += 2) {
-                a0 = fmaf(qf[j][e], kf[e], a0);
-                a1 = fmaf(qf[j][e + 1], kf[e + 1], a1);
-              }
-              s[st][j] = a0 + a1;
-            }
-          }
-#pragma unroll
-          for (int st = 0; st < C::CH; ++st)
-#pragma unroll
-            for (int j = 0; j < GRP; ++j)
-#pragma unroll
-              for (int off = C::LPT / 2; off >= 1; off >>= 1)
-                s[st][j] += __shfl_xor_sync(kFull, s[st][j], off);
-#pragma unroll
-          for (int st = 0; st < C::CH; ++st) {
-            const int tok = wtok + (c + st) * C::TPS + ts;
-            if (tok >= ntok) {
-#pragma unroll
-              for (int j = 0; j < GRP; ++j) s[st][j] = -INFINITY;
-            }
-          }
-          // online softmax: new max, rescale, exponentiate
-#pragma unroll
-          for (int j = 0; j < GRP; ++j) {
-            float mx = s[0][j];
-#pragma unroll
-            for (int st = 1; st < C::CH; ++st) mx = fmaxf(mx, s[st][j]);
-            const float mn = fmaxf(m[j], mx);
-            if (mn == -INFINITY) {
-#pragma unroll
-              for (int st = 0; st < C::CH; ++st) s[st][j] = 0.f;
-              continue;
-            }
-            const float alpha = ex2(m[j] - mn);
-            m[j] = mn;
-            l[j] *= alpha;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[j][e] *= alpha;
-#pragma unroll
-            for (int st = 0; st < C::CH; ++st) {
-              const float pj = ex2(s[st][j] - mn);
-              s[st][j] = pj;
-              l[j] += pj;
-            }
-          }
-          // P.V
-#pragma unroll
-          for (int st = 0; st < C::CH; ++st) {
-            const int tok = wtok + (c + st) * C::TPS + ts;
-            if (tok < ntok) {
-              const uint4 raw = *reinterpret_cast<const uint4*>(Vs + tok * D + c0);
-              float vf[8];
-              Elem<E>::to_f32(raw, vf);
-#pragma unroll
-              for (int j = 0; j < GRP; ++j)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[j][e] = fmaf(s[st][j], vf[e], o[j][e]);
-            }
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == C::STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
 
-    // ---- merge the token slots of the warp (lanes with equal gl) with f
-#pragma unroll
-    for (int off = C::LPT; off < 32; off <<= 1) {
-#pragma unroll
-      for (int j = 0; j < GRP; ++j) {
-        const float mo = __shfl_xor_sync(kFull, m[j], off);
-        const float lo = __shfl_xor_sync(kFull, l[j], off);
-        const float mn = fmaxf(m[j], mo);
-        const float a = (m[j] == -INFINITY) ? 0.f : ex2(m[j] - mn);
-        const float bw = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
-        l[j] = a * l[j] + bw * lo;
-        m[j] = mn;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float oo = __shfl_xor_sync(kFull, o[j][e], off);
-          o[j][e] = a * o[j][e] + bw * oo;
-        }
-      }
-    }
+    // ---- the LeanTile loop; leaves this warp's (m, l, O) in the merge area
     float* wrec = mrg + (size_t)warp * GRP * C::REC;
-    if (ts == 0) {
-#pragma unroll
-      for (int j = 0; j < GRP; ++j) {
-        float* r = wrec + j * C::REC;
-        if (gl == 0) {
-          r[0] = m[j];
-          r[1] = l[j];
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) r[2 + c0 + e] = o[j][e];
-      }
-    }
+    if constexpr (C::TC)
+      warp_segment_tc<D, GRP, E>(p, g, b, kvh, L, t0, n_tiles, kv, full, empty, stage, phase, abort_flag, wrec);
+    else
+      warp_segment_cc<D, GRP, E>(p, g, b, kvh, L, t0, n_tiles, kv, full, empty, stage, phase, abort_flag, wrec);
     consumer_sync(C::NCT);
 
     // ---- merge the 8 warps with f: thread -> (head j, dim c) items
@@ -526,7 +792,7 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
               const float bw = (m2 == -INFINITY) ? 0.f : ex2(m2 - mn);
               Lsum[i] = a * Lsum[i] + bw * l2;
               O[i] = a * O[i] + bw * o2;
-              M[i] = mn;  // a NaN m2 (poisoned partial) propagates here
+              M[i] = mn;  // a NaN m2 (poisoned partial) propagates through bw
             }
           }
         }
@@ -548,9 +814,15 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
 
 // -------------------------------------------------------------------- kernel
 template <int D, int GRP, typename E>
-__global__ void __launch_bounds__(Cfg<D, GRP>::NTHREADS, 1) lean_decode_kernel(const KParams p) {
+__global__ void __launch_bounds__(Cfg<D, GRP>::NTHREADS, 1)
+    lean_decode_kernel(const KParams p, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv) {
   using C = Cfg<D, GRP>;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the 128-byte swizzle of TMA tiles needs 1024-byte aligned destinations
+  unsigned char* smem = C::TC ? reinterpret_cast<unsigned char*>(
+                                    (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))
+                              : smem_raw;
   E* kv = reinterpret_cast<E*>(smem);
   float* mrg = reinterpret_cast<float*>(smem + C::KV_BYTES);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::KV_BYTES + C::MERGE_BYTES);
@@ -572,7 +844,7 @@ __global__ void __launch_bounds__(Cfg<D, GRP>::NTHREADS, 1) lean_decode_kernel(c
   const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr[kEpoch]);
 
   if ((tid >> 5) == C::NCW) {
-    if ((tid & 31) == 0) produce<D, GRP, E>(p, g, kv, full, empty, flags_smem);
+    if ((tid & 31) == 0) produce<D, GRP, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
     __syncwarp();
   } else {
     consume<D, GRP, E>(p, g, kv, full, empty, mrg, flags_smem, epoch);
@@ -618,6 +890,11 @@ __global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
 }
 
 // ------------------------------------------------------------- host launchers
+// Tensor maps of K and V seen as one [rows = hkv * total tokens, D] matrix,
+// boxes of 64 columns x T rows with 128-byte swizzle.
+cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, int T, int elem_type,
+                           CUtensorMap* mk, CUtensorMap* mv);
+
 template <int D, int GRP, typename E>
 cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
   using C = Cfg<D, GRP>;
@@ -632,7 +909,15 @@ cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
     configured_device = dev;
   }
   if (p.G <= 0) return cudaSuccess;
-  lean_decode_kernel<D, GRP, E><<<p.G, C::NTHREADS, C::SMEM, st>>>(p);
+  CUtensorMap mk, mv;
+  if (C::TC) {
+    e = encode_kv_maps(p.k, p.v, p.kv_rows, D, C::T, (int)Elem<E>::kTmaType, &mk, &mv);
+    if (e != cudaSuccess) return e;
+  } else {
+    memset(&mk, 0, sizeof(mk));
+    memset(&mv, 0, sizeof(mv));
+  }
+  lean_decode_kernel<D, GRP, E><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
   return cudaGetLastError();
 }
 

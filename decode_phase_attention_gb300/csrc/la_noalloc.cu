@@ -121,6 +121,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   p.hdr = reinterpret_cast<uint32_t*>(base);
   p.flags = reinterpret_cast<uint32_t*>(base + L.flags);
   p.recs = reinterpret_cast<float*>(base + L.recs);
+  p.kv_rows = (long long)s->hkv * s->cu[s->batch];
   p.G = s->G;
   p.batch = s->batch;
   p.hq = s->hq;
