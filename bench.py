@@ -147,6 +147,26 @@ class ClockSampler:
                 "in_timed_region": bool(inside)}
 
 
+def summarize_trace(tr):
+    """Per-CTA timeline of one call: balance of busy time and host-CTA waits (microseconds)."""
+    import numpy as np
+    t0 = tr[:, 1].min()
+    busy = (tr[:, 3] - tr[:, 1]) / 1e3
+    end = (tr[:, 5] - t0) / 1e3
+    first = (tr[:, 2] - tr[:, 1]) / 1e3
+    wait = tr[:, 4] / 1e3
+    active = tr[:, 6] > 0
+
+    def stats(x):
+        x = x[active]
+        return {"min": round(float(x.min()), 2), "mean": round(float(x.mean()), 2),
+                "max": round(float(x.max()), 2)}
+    return {"ctas": int(active.sum()), "tile_loop_us": stats(busy), "end_us": stats(end),
+            "first_tile_latency_us": stats(first), "host_wait_us": stats(wait),
+            "tiles_per_cta": stats(tr[:, 6].astype(float)),
+            "launch_skew_us": round(float((tr[active, 1].max() - t0) / 1e3), 2)}
+
+
 def algorithmic_bytes(w, grid, kernel):
     """Bytes a launch must move: K+V once, q, out, and the partial records."""
     kv = w.kv_bytes()
@@ -319,6 +339,14 @@ def run_ours(args, rank, world, local_rank):
     if st != la.LA_OK:
         raise RuntimeError(f"kernel reported: {la.status_string(st)}")
 
+    # one extra traced call (outside the timed region): per-CTA balance and host waits
+    trace = torch.zeros(G * la.TRACE_WORDS, dtype=torch.int64, device=dev)
+    la.la_schedule_set_trace(dec.sched, trace)
+    call()
+    torch.cuda.synchronize(dev)
+    la.la_schedule_set_trace(dec.sched, None)
+    cta_trace = summarize_trace(trace.view(G, la.TRACE_WORDS).cpu().numpy())
+
     kv_bytes, algo_bytes = algorithmic_bytes(w, G, args.kernel)
     value = world * kv_bytes / (mean_ms * 1e-3) / 1e9
 
@@ -387,6 +415,7 @@ def run_ours(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": algo_bytes},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "cta_trace": cta_trace,
         "gpu_launches": args.steps * launches_per_call,
         "clocks": sampler.summary(wall0, wall1),
     }

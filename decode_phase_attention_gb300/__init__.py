@@ -20,7 +20,7 @@ LA_F16, LA_BF16 = 0, 1
 SEG_WHOLE, SEG_NONHOST, SEG_HOST, SEG_PARTIAL = range(4)
 EXPORTED = ["la_plan", "la_plan_fixed", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
             "la_decode", "la_decode_static", "la_get_status", "la_schedule_export_size", "la_schedule_export",
-            "la_schedule_set_debug", "la_device_capacity", "la_schedule_destroy",
+            "la_schedule_set_debug", "la_schedule_set_trace", "la_device_capacity", "la_schedule_destroy",
             "la_status_string"]
 
 
@@ -49,6 +49,7 @@ def _load():
         "la_schedule_export_size": (c_size, [vp]),
         "la_schedule_export": (c_int, [vp, vp, c_size]),
         "la_schedule_set_debug": (c_int, [vp, c_int, c_ll]),
+        "la_schedule_set_trace": (c_int, [vp, vp]),
         "la_device_capacity": (c_int, [c_int, c_int, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
         "la_schedule_destroy": (None, [vp]),
         "la_status_string": (ctypes.c_char_p, [c_int]),
@@ -140,6 +141,18 @@ def la_schedule_export(sched):
 def la_schedule_set_debug(sched, skip_signal_cta=-1, spin_timeout_ns=2_000_000_000):
     _check(_lib.la_schedule_set_debug(sched.handle, int(skip_signal_cta), int(spin_timeout_ns)),
            "la_schedule_set_debug")
+
+
+def la_schedule_set_trace(sched, trace=None):
+    """Record a per-CTA timeline into `trace` (int64 device tensor of grid*8 words); None stops."""
+    if trace is not None and trace.numel() * trace.element_size() < sched.grid * 8 * 8:
+        raise ValueError("trace buffer smaller than grid * 8 words")
+    ptr = None if trace is None else ctypes.c_void_p(trace.data_ptr())
+    _check(_lib.la_schedule_set_trace(sched.handle, ptr), "la_schedule_set_trace")
+
+
+TRACE_WORDS = 8
+TRACE_FIELDS = ["sm", "start", "first_tile", "tiles_done", "wait_ns", "end", "tiles", "segments"]
 
 
 def la_device_capacity(d, grp):

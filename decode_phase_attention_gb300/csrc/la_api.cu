@@ -136,6 +136,23 @@ la_status plan_fixed(la_schedule* s) {
   return LA_OK;
 }
 
+// Device segment records: the planner's words plus L and the slab's first row.
+void build_dev_segs(la_schedule* s) {
+  const size_t n = s->segs.size() / la::kSegWords;
+  s->dev_segs.assign(n * la::kDevSegWords, 0);
+  for (size_t i = 0; i < n; ++i) {
+    const int32_t* sg = &s->segs[i * la::kSegWords];
+    int32_t* dv = &s->dev_segs[i * la::kDevSegWords];
+    const int b = sg[0] / s->hkv, kvh = sg[0] % s->hkv;
+    const int64_t L = (int64_t)s->cu[b + 1] - s->cu[b];
+    const int64_t row0 = (int64_t)s->hkv * s->cu[b] + (int64_t)kvh * L;
+    for (int w = 0; w < la::kSegWords; ++w) dv[w] = sg[w];
+    dv[5] = (int32_t)L;
+    dv[6] = (int32_t)(uint32_t)(row0 & 0xffffffffLL);
+    dv[7] = (int32_t)(row0 >> 32);
+  }
+}
+
 la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, int kind, int grid_or_splits,
                         la_schedule** out) {
   if (out == nullptr) return LA_ERR_INVALID;
@@ -168,6 +185,7 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
     delete s;
     return r;
   }
+  build_dev_segs(s);
   *out = s;
   return LA_OK;
 }
@@ -216,8 +234,9 @@ la_status ensure_uploaded(la_schedule* s) {
   buf.insert(buf.end(), s->cu.begin(), s->cu.end());
   s->off_cta_seg = buf.size();
   buf.insert(buf.end(), s->cta_seg.begin(), s->cta_seg.end());
+  while (buf.size() % 4 != 0) buf.push_back(0);  // segment records are read as 16-byte vectors
   s->off_segs = buf.size();
-  buf.insert(buf.end(), s->segs.begin(), s->segs.end());
+  buf.insert(buf.end(), s->dev_segs.begin(), s->dev_segs.end());
   s->off_host = buf.size();
   buf.insert(buf.end(), s->unit_host.begin(), s->unit_host.end());
   s->off_fin = buf.size();
@@ -360,6 +379,7 @@ la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt, co
   p.qscale = scale * 1.4426950408889634f;  // log2(e): scores in base-2 units
   p.spin_ns = s->spin_ns;
   p.skip_signal = s->skip_signal;
+  p.trace = s->trace;
   cudaStream_t st = (cudaStream_t)stream;
   const int dtype = dt == LA_BF16 ? 1 : 0;
   cudaError_t ce = s->d == 64 ? la::launch_decode_d64(s->grp, dtype, p, st)
@@ -424,6 +444,13 @@ la_status la_schedule_set_debug(la_schedule* s, int skip_signal_cta, long long s
   if (s == nullptr || spin_timeout_ns <= 0) return LA_ERR_INVALID;
   s->skip_signal = skip_signal_cta;
   s->spin_ns = spin_timeout_ns;
+  return LA_OK;
+}
+
+la_status la_schedule_set_trace(la_schedule* s, void* trace_dev) {
+  if (s == nullptr) return LA_ERR_INVALID;
+  if (trace_dev != nullptr && (reinterpret_cast<uintptr_t>(trace_dev) % 8) != 0) return LA_ERR_INVALID;
+  s->trace = static_cast<unsigned long long*>(trace_dev);
   return LA_OK;
 }
 

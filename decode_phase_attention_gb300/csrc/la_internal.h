@@ -11,8 +11,12 @@ namespace la {
 // Kinds of segment (match LA_SEG_* in lean_attn.h).
 enum SegKind : int32_t { kWhole = 0, kNonHost = 1, kHost = 2, kPartial = 3 };
 
-// One segment of a CTA's work, as stored in the device schedule.
-constexpr int kSegWords = 5;  // unit, tile_begin, tile_end, kind, peer
+// One segment of a CTA's work: the planner's 5 words (unit, tile_begin,
+// tile_end, kind, peer) as exported, and the 8-word device record that adds
+// the request's context length and the slab's first K/V row (64-bit), so the
+// producer can issue its first copy after two dependent loads.
+constexpr int kSegWords = 5;
+constexpr int kDevSegWords = 8;  // unit, t0, t1, kind, peer, L, row0 low, row0 high
 
 // Workspace: a 256-byte header, G ready flags (padded to 256 bytes), then G
 // partial records of grp * (d + 2) floats: per query head [m, l, O[d]].
@@ -46,6 +50,20 @@ struct KParams {
   float qscale;             // scale * log2(e): scores are kept in base-2 units
   long long spin_ns;        // limit of every wait inside the kernel
   int skip_signal;          // test hook: this CTA never sets its flag (-1: none)
+  unsigned long long* trace;  // optional per-CTA timeline (kTraceWords each), or null
+};
+
+// Per-CTA trace record (globaltimer ns): written when KParams::trace is set.
+constexpr int kTraceWords = 8;
+enum TraceWord {
+  kTrSm = 0,         // SM the CTA ran on
+  kTrStart = 1,      // kernel entry
+  kTrFirstTile = 2,  // first tile landed in shared memory
+  kTrTilesDone = 3,  // last tile of the last segment consumed
+  kTrWaitNs = 4,     // total time the host CTA spent waiting for ready flags
+  kTrEnd = 5,        // all outputs / partials written
+  kTrTiles = 6,      // LeanTiles processed
+  kTrSegs = 7        // segments processed
 };
 
 struct CParams {            // fixed-split merge launch

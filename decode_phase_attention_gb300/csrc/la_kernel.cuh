@@ -290,12 +290,13 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
   long long issued = 0;
   bool aborted = false;
   for (int si = s_begin; si < s_end && !aborted; ++si) {
-    const int* sg = p.segs + (size_t)si * kSegWords;
-    const int unit = sg[0], t0 = sg[1], t1 = sg[2];
-    const int b = unit / p.hkv, kvh = unit % p.hkv;
-    if (!unit_offsets_ok(p, b)) continue;  // consumers skip the same segment
-    const long long L = (long long)p.cu[b + 1] - p.cu[b];
-    const long long row0 = (long long)p.hkv * p.cu[b] + (long long)kvh * L;  // first row of the slab
+    // the schedule's own offsets: every copy stays inside the K/V extent the
+    // schedule was planned for, whatever the caller's device offsets hold
+    const int4 w0 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords);
+    const int4 w1 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 4);
+    const int t0 = w0.y, t1 = w0.z;
+    const long long L = w1.y;
+    const long long row0 = (long long)(((unsigned long long)(unsigned)w1.w << 32) | (unsigned)w1.z);
     for (int t = t0; t < t1; ++t) {
       const long long rem = L - (long long)t * C::T;
       const int ntok = rem < C::T ? (int)rem : C::T;
@@ -354,6 +355,11 @@ __device__ __forceinline__ bool wait_tile(const KParams& p, int g, uint64_t* ful
     if (!*abort_flag) record_error(p.hdr, kStatusTimeout, g, -1);
     *abort_flag = 1;
   }
+  if (p.trace != nullptr && threadIdx.x == 0) {
+    unsigned long long* tr = p.trace + (size_t)g * kTraceWords;
+    if (tr[kTrFirstTile] == 0ull) tr[kTrFirstTile] = global_ns();
+    tr[kTrTiles] += 1ull;
+  }
   return have;
 }
 
@@ -362,7 +368,7 @@ __device__ __forceinline__ bool wait_tile(const KParams& p, int g, uint64_t* ful
 // of the group in its slot of the merge area.
 template <int D, int GRP, typename E>
 __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, int kvh, long long L, int t0,
-                                                int n_tiles, const E* kv, uint64_t* full, uint64_t* empty,
+                                                int n_tiles, bool ok, const E* kv, uint64_t* full, uint64_t* empty,
                                                 int& stage, uint32_t& phase, volatile int* abort_flag,
                                                 float* wrec) {
   using C = Cfg<D, GRP>;
@@ -393,7 +399,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
   for (int it = 0; it < n_tiles; ++it) {
     const long long rem = L - (long long)(t0 + it) * C::T;
     const int ntok = rem < C::T ? (int)rem : C::T;
-    if (wait_tile<D, GRP>(p, g, full, stage, phase, abort_flag, lane)) {
+    if (wait_tile<D, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
       const E* Ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
       const E* Vs = Ks + C::TILE_ELEMS;
       const int wtok = warp * C::TPW;
@@ -523,7 +529,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile_base, int bk, int row, int
 
 template <int D, int GRP, typename E>
 __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, int kvh, long long L, int t0,
-                                                int n_tiles, const E* kv, uint64_t* full, uint64_t* empty,
+                                                int n_tiles, bool ok, const E* kv, uint64_t* full, uint64_t* empty,
                                                 int& stage, uint32_t& phase, volatile int* abort_flag,
                                                 float* wrec) {
   using C = Cfg<D, GRP>;
@@ -557,7 +563,7 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
   for (int it = 0; it < n_tiles; ++it) {
     const long long rem = L - (long long)(t0 + it) * C::T;
     const int ntok = rem < C::T ? (int)rem : C::T;
-    if (wait_tile<D, GRP>(p, g, full, stage, phase, abort_flag, lane)) {
+    if (wait_tile<D, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
       const uint32_t kb = kv_base + (uint32_t)(stage * 2 * C::TILE_ELEMS * 2);
       const uint32_t vb = kb + (uint32_t)(C::TILE_ELEMS * 2);
       const int wtok = warp * C::TPW;
@@ -680,20 +686,31 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
   uint32_t phase = 0;
 
   for (int si = s_begin; si < s_end; ++si) {
-    const int* sg = p.segs + (size_t)si * kSegWords;
-    const int unit = sg[0], t0 = sg[1], t1 = sg[2], kind = sg[3], peer = sg[4];
+    const int4 w0 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords);
+    const int4 w1 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 4);
+    const int unit = w0.x, t0 = w0.y, t1 = w0.z, kind = w0.w, peer = w1.x;
     const int b = unit / p.hkv, kvh = unit % p.hkv;
+    // Device offsets that disagree with the schedule: the tiles are still
+    // taken from the ring (the producer streams them) but not used, and the
+    // unit's outputs are NaN.
     const bool ok = unit_offsets_ok(p, b);
     if (!ok && tid == 0) record_error(p.hdr, kStatusInvalid, g, unit);
-    const long long L = ok ? (long long)p.cu[b + 1] - p.cu[b] : 0;
-    const int n_tiles = ok ? t1 - t0 : 0;
+    const long long L = w1.y;
+    const int n_tiles = t1 - t0;
 
     // ---- the LeanTile loop; leaves this warp's (m, l, O) in the merge area
     float* wrec = mrg + (size_t)warp * GRP * C::REC;
     if constexpr (C::TC)
-      warp_segment_tc<D, GRP, E>(p, g, b, kvh, L, t0, n_tiles, kv, full, empty, stage, phase, abort_flag, wrec);
+      warp_segment_tc<D, GRP, E>(p, g, b, kvh, L, t0, n_tiles, ok, kv, full, empty, stage, phase, abort_flag,
+                                 wrec);
     else
-      warp_segment_cc<D, GRP, E>(p, g, b, kvh, L, t0, n_tiles, kv, full, empty, stage, phase, abort_flag, wrec);
+      warp_segment_cc<D, GRP, E>(p, g, b, kvh, L, t0, n_tiles, ok, kv, full, empty, stage, phase, abort_flag,
+                                 wrec);
+    if (p.trace != nullptr && tid == 0) {
+      unsigned long long* tr = p.trace + (size_t)g * kTraceWords;
+      tr[kTrTilesDone] = global_ns();
+      tr[kTrSegs] += 1ull;
+    }
     consumer_sync(C::NCT);
 
     // ---- merge the 8 warps with f: thread -> (head j, dim c) items
@@ -751,8 +768,9 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
         for (int g2 = g + 1; g2 <= peer; ++g2) {
           if (tid == 0) {
             bool got = false;
+            const uint64_t tstart_all = global_ns();
             if (!*abort_flag) {
-              const uint64_t tstart = global_ns();
+              const uint64_t tstart = tstart_all;
               for (uint32_t it = 0;; ++it) {
                 if (ld_acquire_gpu(&p.flags[g2]) == ready) {
                   got = true;
@@ -770,6 +788,8 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
               }
             }
             *bcast = got ? 1 : 0;
+            if (p.trace != nullptr && !*abort_flag)
+              p.trace[(size_t)g * kTraceWords + kTrWaitNs] += global_ns() - tstart_all;
           }
           consumer_sync(C::NCT);
           const bool got = *bcast != 0;
@@ -832,6 +852,14 @@ __global__ void __launch_bounds__(Cfg<D, GRP>::NTHREADS, 1)
   const int tid = threadIdx.x;
   const int g = blockIdx.x;
   if (tid == 0) {
+    if (p.trace != nullptr) {
+      unsigned long long* tr = p.trace + (size_t)g * kTraceWords;
+      uint32_t sm;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+      tr[kTrSm] = sm;
+      tr[kTrStart] = global_ns();
+      for (int w = 2; w < kTraceWords; ++w) tr[w] = 0ull;
+    }
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C::NCW);
@@ -851,6 +879,7 @@ __global__ void __launch_bounds__(Cfg<D, GRP>::NTHREADS, 1)
   }
   __syncthreads();
   if (tid == 0) {
+    if (p.trace != nullptr) p.trace[(size_t)g * kTraceWords + kTrEnd] = global_ns();
     // The last CTA to finish advances the epoch, so the next launch's ready
     // flags can never be confused with this one's.
     __threadfence();

@@ -57,7 +57,7 @@ Layout layout_of(const la_schedule* s) {
   };
   L.cu = table(s->cu.size());
   L.cta_seg = table(s->cta_seg.size());
-  L.segs = table(s->segs.size());
+  L.segs = table(s->dev_segs.size());
   L.host = table(s->unit_host.size());
   L.fin = table(s->unit_fin.size());
   L.total = off;
@@ -105,7 +105,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   // (epoch, done counter, status) and the ready flags, then copy the tables.
   if (cudaMemsetAsync(base, 0, L.recs, st) != cudaSuccess) return LA_ERR_CUDA;
   if (put(base, L.cu, s->cu, st) != cudaSuccess || put(base, L.cta_seg, s->cta_seg, st) != cudaSuccess ||
-      put(base, L.segs, s->segs, st) != cudaSuccess || put(base, L.host, s->unit_host, st) != cudaSuccess ||
+      put(base, L.segs, s->dev_segs, st) != cudaSuccess || put(base, L.host, s->unit_host, st) != cudaSuccess ||
       put(base, L.fin, s->unit_fin, st) != cudaSuccess)
     return LA_ERR_CUDA;
 
@@ -129,6 +129,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   p.qscale = scale * 1.4426950408889634f;
   p.spin_ns = s->spin_ns;
   p.skip_signal = s->skip_signal;
+  p.trace = s->trace;
   const int dtype = dt == LA_BF16 ? 1 : 0;
   cudaError_t ce = s->d == 64 ? la::launch_decode_d64(s->grp, dtype, p, st)
                               : la::launch_decode_d128(s->grp, dtype, p, st);

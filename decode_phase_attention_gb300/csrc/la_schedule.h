@@ -14,9 +14,11 @@ struct la_schedule {
   int G = 0, U = 0;
   int64_t I = 0;
   std::vector<int32_t> cu, cta_iter, unit_iter, cta_seg, segs, unit_host, unit_fin;
+  std::vector<int32_t> dev_segs;  // device records (kDevSegWords per segment)
   // debug hooks
   int skip_signal = -1;
   long long spin_ns = 2000000000LL;
+  unsigned long long* trace = nullptr;  // device buffer of G * 8 words, or null
   // device copy: [cu (batch+1)] [cta_seg (G+1)] [segs] [unit_host (U)] [unit_fin (U)]
   std::mutex mu;
   int device = -1;

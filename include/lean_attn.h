@@ -211,6 +211,18 @@ la_status la_schedule_export(const la_schedule* s, int32_t* buf, size_t n);
  */
 la_status la_schedule_set_debug(la_schedule* s, int skip_signal_cta, long long spin_timeout_ns);
 
+/*
+ * Optional per-CTA timeline, to measure the balance of work across SMs and
+ * how long host CTAs wait for partial results (the talk's "temporal skew").
+ * trace_dev: device buffer of la_schedule_grid(s) * 8 uint64 words (8-byte
+ * aligned), or NULL to stop tracing. Per CTA, in globaltimer nanoseconds
+ * unless noted: [0] SM id, [1] kernel entry, [2] first tile landed,
+ * [3] last tile consumed, [4] total host wait (ns), [5] end,
+ * [6] tiles processed, [7] segments processed. The buffer is written by
+ * every later la_decode with this schedule until tracing is turned off.
+ */
+la_status la_schedule_set_trace(la_schedule* s, void* trace_dev);
+
 /* Most CTAs of the stream-K kernel one SM of the current device holds for
  * head dim d and group size grp, and the SM count. */
 la_status la_device_capacity(int d, int grp, int* ctas_per_sm, int* num_sms);

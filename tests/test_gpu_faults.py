@@ -57,3 +57,24 @@ def test_device_offsets_that_disagree_with_the_schedule_are_reported():
     out = dec(q, k, v, w.scale)
     assert dec.status() == la.LA_OK
     compare(out.cpu(), reference(w, q, k, v))
+
+
+def test_trace_records_the_planned_work_of_every_cta():
+    w = workloads.custom(3, 16, 2, 64, "bf16", [5000, 300, 12000])
+    q, k, v, _ = workloads.make_inputs(w, seed=8, device="cuda")
+    dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, w.cu, num_sms=23)
+    G = dec.sched.grid
+    trace = torch.zeros(G * la.TRACE_WORDS, dtype=torch.int64, device="cuda")
+    la.la_schedule_set_trace(dec.sched, trace)
+    out = dec(q, k, v, w.scale)
+    assert dec.status() == la.LA_OK
+    la.la_schedule_set_trace(dec.sched, None)
+    compare(out.cpu(), reference(w, q, k, v))
+    tr = trace.view(G, la.TRACE_WORDS).cpu().numpy()
+    exp = la.la_schedule_export(dec.sched)
+    cta_iter = np.array(exp[8:8 + G + 1])
+    cta_seg = np.array(exp[8 + G + 1 + w.batch * w.hkv + 1:][:G + 1])
+    assert np.array_equal(tr[:, 6], np.diff(cta_iter))  # tiles per CTA as planned
+    assert np.array_equal(tr[:, 7], np.diff(cta_seg))   # segments per CTA as planned
+    assert np.all(tr[:, 1] <= tr[:, 2]) and np.all(tr[:, 2] <= tr[:, 3]) and np.all(tr[:, 3] <= tr[:, 5])
+    assert np.all(tr[:, 4] >= 0) and np.all(tr[:, 4] <= tr[:, 5] - tr[:, 1])

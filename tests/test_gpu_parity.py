@@ -130,3 +130,17 @@ def test_named_workloads_full_output(name):
     compare(out.cpu(), reference(w, q, k, v))
     del q, k, v
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("lengths,hq,hkv,d,dt,grid", [
+    ([1] * 7, 8, 8, 128, "bf16", 0),          # single-token contexts: every tile is a 1-token tail
+    ([300], 1, 1, 64, "f16", 152),            # one head, 2 tiles, 150 idle CTAs
+    ([5, 700, 1], 16, 2, 128, "bf16", 3),     # group 8 at d 128 on a 3-CTA grid
+    ([256 * 9], 2, 2, 64, "bf16", 9),         # exact tile multiples, one tile per CTA
+    ([128 * 40 + 1], 8, 1, 128, "f16", 40),   # MQA (one kv head, group 8)
+])
+def test_degenerate_shapes(lengths, hq, hkv, d, dt, grid):
+    w = workloads.custom(len(lengths), hq, hkv, d, dt, lengths)
+    q, k, v, _ = workloads.make_inputs(w, seed=17, device="cuda")
+    out, _ = run_lean(w, q, k, v, num_sms=grid)
+    compare(out.cpu(), reference(w, q, k, v))
