@@ -44,12 +44,9 @@ def build(force=False):
     return _LIB
 
 
-def _load():
-    global _lib
-    if _lib is not None:
-        return _lib
-    build()
-    lib = ctypes.CDLL(_LIB)
+def _open(path):
+    """Load an oracle library file and declare its C signatures."""
+    lib = ctypes.CDLL(path)
     vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_double
     lib.oracle_half_to_double.restype = dbl
     lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
@@ -65,8 +62,15 @@ def _load():
     lib.oracle_partial.argtypes = [i32, i32, vp, vp, vp, i64, i64, dbl, vp]
     lib.oracle_attend.restype = i32
     lib.oracle_attend.argtypes = [i32, i32, i32, i32, vp, i32, vp, vp, vp, dbl, i64, vp, vp, i32]
-    _lib = lib
     return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _open(_LIB)
+    return _lib
 
 
 def _ptr(a):
