@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="uniform")
-    ap.add_argument("--kernel", default="lean", choices=["lean", "naive", "fixed_split"])
+    ap.add_argument("--kernel", default="lean", choices=["lean", "naive", "fixed_split", "auto"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--grid", type=int, default=0, help="stream-K grid; 0 = one CTA per SM")
     ap.add_argument("--seed", type=int, default=0)
@@ -167,15 +167,17 @@ def summarize_trace(tr):
             "launch_skew_us": round(float((tr[active, 1].max() - t0) / 1e3), 2)}
 
 
-def algorithmic_bytes(w, grid, kernel):
-    """Bytes a launch must move: K+V once, q, out, and the partial records."""
+def algorithmic_bytes(w, export):
+    """Bytes a call must move: K+V once, q, out, and every partial record
+    written once and read once (one per non-host or fixed-split piece)."""
     kv = w.kv_bytes()
     q = w.batch * w.hq * w.d * 2
     out = w.batch * w.hq * w.d * 4
-    grp = w.hq // w.hkv
-    rec = grp * (w.d + 2) * 4
-    ws = 2 * grid * rec if kernel != "naive" else 0  # written once, read once
-    return kv, kv + q + out + ws
+    G, U, nseg = export[1], export[2], export[5]
+    base = 8 + 2 * (G + 1) + (U + 1)
+    pieces = sum(1 for i in range(nseg) if export[base + 5 * i + 3] in (1, 3))
+    rec = (w.hq // w.hkv) * (w.d + 2) * 4
+    return kv, kv + q + out + 2 * pieces * rec
 
 
 # ------------------------------------------------------------------ reference arm
@@ -280,12 +282,14 @@ def run_ours(args, rank, world, local_rank):
         dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev)
     elif args.kernel == "naive":
         dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, device=dev, fixed_splits=1)
+    elif args.kernel == "auto":
+        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, auto=True)
     else:
         per_sm, sms = la.la_device_capacity(w.d, w.hq // w.hkv)
         splits = -(-sms // (w.batch * w.hkv))
         dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, device=dev, fixed_splits=max(1, splits))
     G = dec.sched.grid
-    launches_per_call = 2 if (args.kernel == "fixed_split" and dec.sched.grid > w.batch * w.hkv) else 1
+    launches_per_call = 2 if (dec.kind == "fixed_split" and dec.sched.grid > w.batch * w.hkv) else 1
     stream = torch.cuda.current_stream(dev)
     out = torch.empty(w.batch, w.hq, w.d, dtype=torch.float32, device=dev)
     # K+V well above L2 (129 MB) cannot be served from L2 by the next call; smaller
@@ -347,7 +351,7 @@ def run_ours(args, rank, world, local_rank):
     la.la_schedule_set_trace(dec.sched, None)
     cta_trace = summarize_trace(trace.view(G, la.TRACE_WORDS).cpu().numpy())
 
-    kv_bytes, algo_bytes = algorithmic_bytes(w, G, args.kernel)
+    kv_bytes, algo_bytes = algorithmic_bytes(w, la.la_schedule_export(dec.sched))
     value = world * kv_bytes / (mean_ms * 1e-3) / 1e9
 
     e2e = None
@@ -399,7 +403,8 @@ def run_ours(args, rank, world, local_rank):
         "kv_read_frac_of_8tbs_nominal": round(kv_bytes / (mean_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.description, "kernel": args.kernel, "grid": G,
+        "config": {"workload": w.description, "kernel": args.kernel, "schedule": dec.kind,
+                   "predicted_us": dec.predicted_us, "grid": G,
                    "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
                    "total_context_tokens": w.total_tokens, "kv_bytes": kv_bytes,
                    "l2": ("flushed (256 MiB write) before every timed call" if use_flush else

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "liblean_attn.so")
 LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
 LA_F16, LA_BF16 = 0, 1
 SEG_WHOLE, SEG_NONHOST, SEG_HOST, SEG_PARTIAL = range(4)
-EXPORTED = ["la_plan", "la_plan_fixed", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
+EXPORTED = ["la_plan", "la_plan_fixed", "la_plan_auto", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
             "la_decode", "la_decode_static", "la_get_status", "la_schedule_export_size", "la_schedule_export",
             "la_schedule_set_debug", "la_schedule_set_trace", "la_device_capacity", "la_schedule_destroy",
             "la_status_string"]
@@ -40,6 +40,7 @@ def _load():
     sig = {
         "la_plan": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
         "la_plan_fixed": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
+        "la_plan_auto": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp, ctypes.POINTER(ctypes.c_double)]),
         "la_schedule_grid": (c_int, [vp]),
         "la_workspace_size": (c_size, [vp]),
         "la_workspace_init": (c_int, [vp, c_size, vp]),
@@ -124,6 +125,25 @@ def la_plan_fixed(batch, hq, hkv, d, cu_seqlens_k, splits):
     _check(_lib.la_plan_fixed(batch, hq, hkv, d, cu.ctypes.data_as(ctypes.c_void_p), int(splits),
                               ctypes.byref(h)), "la_plan_fixed")
     return Schedule(h.value, batch, hq, hkv, d, cu)
+
+
+def la_plan_auto(batch, hq, hkv, d, cu_seqlens_k, num_sms=0):
+    """Pick stream-K, one-CTA-per-unit or fixed split by predicted time.
+
+    Returns (schedule, kind, predicted_us) where kind is "lean", "naive" or
+    "fixed_split" and predicted_us the three predictions in that order.
+    """
+    cu = _cu_array(cu_seqlens_k)
+    if cu.size != batch + 1:
+        raise ValueError("cu_seqlens_k must have batch + 1 entries")
+    h = ctypes.c_void_p()
+    pred = (ctypes.c_double * 3)()
+    _check(_lib.la_plan_auto(batch, hq, hkv, d, cu.ctypes.data_as(ctypes.c_void_p), int(num_sms),
+                             ctypes.byref(h), pred), "la_plan_auto")
+    sched = Schedule(h.value, batch, hq, hkv, d, cu)
+    head = la_schedule_export(sched)[:8]
+    kind = "lean" if head[6] == 0 else ("naive" if head[7] == 1 else "fixed_split")
+    return sched, kind, list(pred)
 
 
 def la_workspace_size(sched):
@@ -257,12 +277,17 @@ def la_get_status(workspace, stream=None):
 class LeanDecoder:
     """Convenience holder: a schedule, its workspace and the device offsets."""
 
-    def __init__(self, batch, hq, hkv, d, cu_seqlens_k, num_sms=0, device="cuda", fixed_splits=None):
+    def __init__(self, batch, hq, hkv, d, cu_seqlens_k, num_sms=0, device="cuda", fixed_splits=None,
+                 auto=False):
         import torch
-        if fixed_splits is None:
-            self.sched = la_plan(batch, hq, hkv, d, cu_seqlens_k, num_sms)
+        self.predicted_us = None
+        if auto:
+            self.sched, self.kind, self.predicted_us = la_plan_auto(batch, hq, hkv, d, cu_seqlens_k, num_sms)
+        elif fixed_splits is None:
+            self.sched, self.kind = la_plan(batch, hq, hkv, d, cu_seqlens_k, num_sms), "lean"
         else:
             self.sched = la_plan_fixed(batch, hq, hkv, d, cu_seqlens_k, fixed_splits)
+            self.kind = "naive" if fixed_splits == 1 else "fixed_split"
         self.workspace = new_workspace(self.sched, device)
         self.cu_dev = torch.as_tensor(self.sched.cu, dtype=torch.int32, device=device)
         self.batch, self.hq, self.hkv, self.d = batch, hq, hkv, d

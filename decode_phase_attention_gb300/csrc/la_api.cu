@@ -254,6 +254,61 @@ la_status ensure_uploaded(la_schedule* s) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// ---- shape-driven choice among the three partitions ----------------------
+// Time model (seconds) of a launch whose CTAs each stream a fixed number of
+// bytes: CTAs are dispatched in order onto `slots` SMs as SMs free up (the
+// hardware's in-order block dispatch); while n CTAs run, each streams at
+// min(per_sm, total / n) bytes/s. Jobs finish in order of their cumulative
+// progress, so a heap of finish thresholds gives the makespan.
+double simulate_dispatch(const std::vector<double>& job_bytes, int slots, double per_sm, double total) {
+  if (job_bytes.empty()) return 0.0;
+  std::vector<double> heap;  // min-heap of progress thresholds of running jobs
+  auto cmp = [](double a, double b) { return a > b; };
+  size_t next = 0;
+  double progress = 0.0, t = 0.0;
+  while (next < job_bytes.size() && (int)heap.size() < slots) {
+    heap.push_back(progress + job_bytes[next++]);
+    std::push_heap(heap.begin(), heap.end(), cmp);
+  }
+  while (!heap.empty()) {
+    const double rate = std::min(per_sm, total / (double)heap.size());
+    std::pop_heap(heap.begin(), heap.end(), cmp);
+    const double thr = heap.back();
+    heap.pop_back();
+    t += (thr - progress) / rate;
+    progress = thr;
+    if (next < job_bytes.size()) {
+      heap.push_back(progress + job_bytes[next++]);
+      std::push_heap(heap.begin(), heap.end(), cmp);
+    }
+  }
+  return t;
+}
+
+// Bytes of K+V of tiles [t0, t1) of unit u.
+double piece_bytes(const la_schedule* s, int u, int t0, int t1) {
+  const int b = u / s->hkv;
+  const int64_t L = (int64_t)s->cu[b + 1] - s->cu[b];
+  const int64_t tok = std::min<int64_t>((int64_t)t1 * s->T, L) - (int64_t)t0 * s->T;
+  return (double)tok * s->d * 2.0 * 2.0;
+}
+
+// Predicted time of a schedule: per-CTA byte totals through the dispatch model
+// plus launch overheads (one launch, or two for fixed splits > 1).
+double predict_seconds(const la_schedule* s, int slots) {
+  constexpr double kPerSm = 70e9, kTotal = 7.3e12;  // measured on GB300 (one active SM / all SMs)
+  constexpr double kLaunch = 8e-6, kMergeLaunch = 4e-6;
+  std::vector<double> jobs((size_t)s->G, 0.0);
+  for (int g = 0; g < s->G; ++g)
+    for (int i = s->cta_seg[g]; i < s->cta_seg[g + 1]; ++i) {
+      const int32_t* sg = &s->segs[(size_t)i * la::kSegWords];
+      jobs[g] += piece_bytes(s, sg[0], sg[1], sg[2]);
+    }
+  double t = simulate_dispatch(jobs, slots, kPerSm, kTotal) + kLaunch;
+  if (s->kind == 1 && s->splits > 1) t += kMergeLaunch;
+  return t;
+}
+
 }  // namespace
 
 namespace la {
@@ -321,6 +376,46 @@ la_status la_plan_fixed(int batch, int hq, int hkv, int d, const int32_t* cu_seq
   if (out != nullptr) *out = nullptr;
   if (splits <= 0) return LA_ERR_INVALID;
   return make_schedule(batch, hq, hkv, d, cu_seqlens_k, 1, splits, out);
+}
+
+la_status la_plan_auto(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int num_sms,
+                       la_schedule** out, double* predicted_us) {
+  if (out != nullptr) *out = nullptr;
+  if (out == nullptr) return LA_ERR_INVALID;
+  la_status st = check_shape(batch, hq, hkv, d, cu_seqlens_k);
+  if (st != LA_OK) return st;
+  int slots = num_sms;
+  if (slots <= 0) {
+    int sms = 0, per_sm = 0;
+    st = device_sms(&sms);
+    if (st != LA_OK) return st;
+    st = capacity(d, hq / hkv, &per_sm);
+    if (st != LA_OK) return st;
+    slots = sms * std::max(1, per_sm);
+  }
+  la_schedule* cand[3] = {nullptr, nullptr, nullptr};
+  st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, slots, &cand[0]);  // stream-K over every SM
+  if (st == LA_OK) st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 1, 1, &cand[1]);  // one CTA per unit
+  if (st == LA_OK) {
+    const int units = batch * hkv;
+    const int k = std::max(2, (slots + units - 1) / units);  // fixed split that fills the SMs
+    st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 1, k, &cand[2]);
+  }
+  if (st != LA_OK) {
+    for (la_schedule* c : cand) delete c;
+    return st;
+  }
+  int best = 0;
+  double t[3];
+  for (int i = 0; i < 3; ++i) {
+    t[i] = predict_seconds(cand[i], slots);
+    if (predicted_us != nullptr) predicted_us[i] = t[i] * 1e6;
+    if (t[i] < t[best]) best = i;
+  }
+  for (int i = 0; i < 3; ++i)
+    if (i != best) delete cand[i];
+  *out = cand[best];
+  return LA_OK;
 }
 
 int la_schedule_grid(const la_schedule* s) { return s ? s->G : -1; }

@@ -109,6 +109,26 @@ la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k
 la_status la_plan_fixed(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k,
                         int splits, la_schedule** out);
 
+/*
+ * la_plan_auto -- shape-driven choice among the three partitions (the
+ * Silicon & Systems digest's "a useful control policy": a runtime picks a
+ * FlashAttention-style, fixed-split or stream-K schedule from the shape;
+ * the xllm-io review's "4.3" shows the first two are special cases).
+ *
+ * Builds the stream-K schedule over num_sms CTAs (<= 0: one per SM of the
+ * current device), the one-CTA-per-unit partition and the fixed split into
+ * max(2, ceil(SMs / units)) pieces, predicts each one's time and returns
+ * the fastest. Time model: CTAs dispatched in order onto the SMs as they
+ * free up, each running CTA streaming its K+V bytes at min(70 GB/s,
+ * 7.3 TB/s / running CTAs) — rates measured on GB300 — plus 8 us per
+ * launch and 4 us for the second (merge) launch of a fixed split.
+ * predicted_us: NULL, or 3 doubles receiving the predictions (stream-K,
+ * one per unit, fixed split). The returned schedule is used like any
+ * other; la_schedule_export tells which kind it is (word 6, word 7).
+ */
+la_status la_plan_auto(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int num_sms,
+                       la_schedule** out, double* predicted_us);
+
 /* Grid size G of a schedule (CTAs per launch), or -1 for NULL. */
 int la_schedule_grid(const la_schedule* s);
 

@@ -135,3 +135,29 @@ def test_export_size_and_short_buffer():
 def test_status_strings():
     for code in range(6):
         assert la.status_string(code)
+
+
+@pytest.mark.parametrize("shape", shapes()[:25])
+def test_auto_plan_is_exactly_one_of_the_explicit_partitions(shape):
+    batch, hq, hkv, d, lengths, _ = shape
+    cu = cu_of(lengths)
+    s, kind, pred = la.la_plan_auto(batch, hq, hkv, d, cu, 152)
+    assert len(pred) == 3 and all(p > 0 for p in pred)
+    units = batch * hkv
+    explicit = {"lean": P.plan_lean(batch, hq, hkv, d, cu, 152),
+                "naive": P.plan_fixed(batch, hq, hkv, d, cu, 1),
+                "fixed_split": P.plan_fixed(batch, hq, hkv, d, cu, max(2, -(-152 // units)))}
+    assert la.la_schedule_export(s) == P.export(explicit[kind])
+    idx = ["lean", "naive", "fixed_split"].index(kind)
+    assert pred[idx] == min(pred)
+
+
+def test_auto_plan_prefers_stream_k_when_heads_cannot_fill_the_gpu():
+    s, kind, pred = la.la_plan_auto(1, 32, 32, 128, [0, 524288], 152)
+    assert kind == "lean" and pred[1] > 3 * pred[0] and pred[2] > 1.4 * pred[0]
+
+
+def test_auto_plan_time_model_is_even_when_units_fill_the_gpu():
+    # 2048 one-tile units on 152 SMs: the partitions stream the same bytes at full rate
+    s, kind, pred = la.la_plan_auto(64, 32, 32, 128, cu_of([128] * 64), 152)
+    assert abs(pred[0] - pred[1]) / pred[1] < 0.05

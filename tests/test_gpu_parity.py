@@ -144,3 +144,15 @@ def test_degenerate_shapes(lengths, hq, hkv, d, dt, grid):
     q, k, v, _ = workloads.make_inputs(w, seed=17, device="cuda")
     out, _ = run_lean(w, q, k, v, num_sms=grid)
     compare(out.cpu(), reference(w, q, k, v))
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "gqa"])
+def test_auto_selected_schedule_matches_the_oracle(name):
+    w = workloads.named(name)
+    q, k, v, _ = workloads.make_inputs(w, seed=2, device="cuda")
+    s, kind, pred = la.la_plan_auto(w.batch, w.hq, w.hkv, w.d, w.cu)
+    ws = la.new_workspace(s)
+    out = torch.empty(w.batch, w.hq, w.d, device="cuda")
+    la.la_decode(q, k, v, torch.as_tensor(w.cu, device="cuda"), s, ws, out, w.scale)
+    assert la.la_get_status(ws) == la.LA_OK
+    compare(out.cpu(), reference(w, q, k, v))
