@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--kernel", default="lean", choices=["lean", "naive", "fixed_split", "auto"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--grid", type=int, default=0, help="stream-K grid; 0 = one CTA per SM")
+    ap.add_argument("--tile", type=int, default=0, help="LeanTile tokens; 0 = the head dim's default")
+    ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -167,12 +169,12 @@ def summarize_trace(tr):
             "launch_skew_us": round(float((tr[active, 1].max() - t0) / 1e3), 2)}
 
 
-def algorithmic_bytes(w, export):
+def algorithmic_bytes(w, export, out_bytes=4):
     """Bytes a call must move: K+V once, q, out, and every partial record
     written once and read once (one per non-host or fixed-split piece)."""
     kv = w.kv_bytes()
     q = w.batch * w.hq * w.d * 2
-    out = w.batch * w.hq * w.d * 4
+    out = w.batch * w.hq * w.d * out_bytes
     G, U, nseg = export[1], export[2], export[5]
     base = 8 + 2 * (G + 1) + (U + 1)
     pieces = sum(1 for i in range(nseg) if export[base + 5 * i + 3] in (1, 3))
@@ -275,11 +277,12 @@ def run_ours(args, rank, world, local_rank):
     plan_times = []
     for _ in range(21):
         t0 = time.perf_counter()
-        la.la_plan(w.batch, w.hq, w.hkv, w.d, cu, grid if grid > 0 else 0)
+        la.la_plan(w.batch, w.hq, w.hkv, w.d, cu, grid if grid > 0 else 0, args.tile)
         plan_times.append((time.perf_counter() - t0) * 1e6)
     plan_us = sorted(plan_times)[len(plan_times) // 2]
+    out_torch = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[args.out_dtype]
     if args.kernel == "lean":
-        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev)
+        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, tile_tokens=args.tile)
     elif args.kernel == "naive":
         dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, device=dev, fixed_splits=1)
     elif args.kernel == "auto":
@@ -291,7 +294,7 @@ def run_ours(args, rank, world, local_rank):
     G = dec.sched.grid
     launches_per_call = 2 if (dec.kind == "fixed_split" and dec.sched.grid > w.batch * w.hkv) else 1
     stream = torch.cuda.current_stream(dev)
-    out = torch.empty(w.batch, w.hq, w.d, dtype=torch.float32, device=dev)
+    out = torch.empty(w.batch, w.hq, w.d, dtype=out_torch, device=dev)
     # K+V well above L2 (129 MB) cannot be served from L2 by the next call; smaller
     # inputs get a 256 MiB write between calls to flush L2.
     use_flush = args.flush or w.kv_bytes() < L2_BYTES * 4
@@ -351,7 +354,7 @@ def run_ours(args, rank, world, local_rank):
     la.la_schedule_set_trace(dec.sched, None)
     cta_trace = summarize_trace(trace.view(G, la.TRACE_WORDS).cpu().numpy())
 
-    kv_bytes, algo_bytes = algorithmic_bytes(w, la.la_schedule_export(dec.sched))
+    kv_bytes, algo_bytes = algorithmic_bytes(w, la.la_schedule_export(dec.sched), out.element_size())
     value = world * kv_bytes / (mean_ms * 1e-3) / 1e9
 
     e2e = None
@@ -404,6 +407,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.description, "kernel": args.kernel, "schedule": dec.kind,
+                   "tile_tokens": la.la_schedule_export(dec.sched)[4], "out_dtype": args.out_dtype,
                    "predicted_us": dec.predicted_us, "grid": G,
                    "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
                    "total_context_tokens": w.total_tokens, "kv_bytes": kv_bytes,

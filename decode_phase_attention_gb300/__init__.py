@@ -17,8 +17,11 @@ LIB_PATH = os.path.join(_PKG, "liblean_attn.so")
 
 LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_WORKSPACE = range(6)
 LA_F16, LA_BF16 = 0, 1
+LA_OUT_F32, LA_OUT_F16, LA_OUT_BF16 = 0, 1, 2
+HEAD_DIMS = (64, 80, 96, 128, 256)
+TILE_SIZES = {64: (256, 128), 80: (128,), 96: (128,), 128: (128, 64), 256: (64,)}  # first = default
 SEG_WHOLE, SEG_NONHOST, SEG_HOST, SEG_PARTIAL = range(4)
-EXPORTED = ["la_plan", "la_plan_fixed", "la_plan_auto", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
+EXPORTED = ["la_plan", "la_plan_ex", "la_plan_fixed", "la_plan_auto", "la_decode_ex", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
             "la_decode", "la_decode_static", "la_get_status", "la_schedule_export_size", "la_schedule_export",
             "la_schedule_set_debug", "la_schedule_set_trace", "la_device_capacity", "la_schedule_destroy",
             "la_status_string"]
@@ -39,6 +42,8 @@ def _load():
     pp = ctypes.POINTER(ctypes.c_void_p)
     sig = {
         "la_plan": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
+        "la_plan_ex": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, c_int, pp]),
+        "la_decode_ex": (c_int, [vp, vp, vp, c_int, vp, vp, vp, vp, c_int, c_float, vp]),
         "la_plan_fixed": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
         "la_plan_auto": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp, ctypes.POINTER(ctypes.c_double)]),
         "la_schedule_grid": (c_int, [vp]),
@@ -105,14 +110,22 @@ def _cu_array(cu_seqlens_k):
     return np.ascontiguousarray(cu, dtype=np.int32)
 
 
-def la_plan(batch, hq, hkv, d, cu_seqlens_k, num_sms=0):
-    """Stream-K tile planner; num_sms <= 0 uses one CTA per SM of the current device."""
+def la_plan(batch, hq, hkv, d, cu_seqlens_k, num_sms=0, tile_tokens=0):
+    """Stream-K tile planner; num_sms <= 0 uses one CTA per SM of the current device.
+
+    tile_tokens 0 picks the LeanTile of the head dim (la_plan), else la_plan_ex
+    with that LeanTile size.
+    """
     cu = _cu_array(cu_seqlens_k)
     if cu.size != batch + 1:
         raise ValueError("cu_seqlens_k must have batch + 1 entries")
     h = ctypes.c_void_p()
-    _check(_lib.la_plan(batch, hq, hkv, d, cu.ctypes.data_as(ctypes.c_void_p), int(num_sms),
-                        ctypes.byref(h)), "la_plan")
+    cup = cu.ctypes.data_as(ctypes.c_void_p)
+    if tile_tokens:
+        _check(_lib.la_plan_ex(batch, hq, hkv, d, cup, int(num_sms), int(tile_tokens), ctypes.byref(h)),
+               "la_plan_ex")
+    else:
+        _check(_lib.la_plan(batch, hq, hkv, d, cup, int(num_sms), ctypes.byref(h)), "la_plan")
     return Schedule(h.value, batch, hq, hkv, d, cu)
 
 
@@ -215,8 +228,9 @@ def la_decode(q, k, v, cu_seqlens_k, sched, workspace, out, scale, stream=None):
     dt = {torch.float16: LA_F16, torch.bfloat16: LA_BF16}.get(q.dtype)
     if dt is None:
         raise ValueError("q, k, v must be float16 or bfloat16")
-    if out.dtype != torch.float32 or cu_seqlens_k.dtype != torch.int32:
-        raise ValueError("out must be float32 and cu_seqlens_k int32")
+    out_dt = {torch.float32: LA_OUT_F32, torch.float16: LA_OUT_F16, torch.bfloat16: LA_OUT_BF16}.get(out.dtype)
+    if out_dt is None or cu_seqlens_k.dtype != torch.int32:
+        raise ValueError("out must be float32, float16 or bfloat16 and cu_seqlens_k int32")
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("cu_seqlens_k", cu_seqlens_k)):
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
@@ -230,11 +244,13 @@ def la_decode(q, k, v, cu_seqlens_k, sched, workspace, out, scale, stream=None):
         raise ValueError("cu_seqlens_k does not match the schedule's batch")
     if workspace.numel() * workspace.element_size() < la_workspace_size(sched):
         raise ValueError("workspace smaller than la_workspace_size")
-    _check(_lib.la_decode(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
-                          ctypes.c_void_p(v.data_ptr()), dt,
-                          ctypes.c_void_p(cu_seqlens_k.data_ptr()), sched.handle,
-                          ctypes.c_void_p(workspace.data_ptr()), ctypes.c_void_p(out.data_ptr()),
-                          float(scale), _stream_handle(stream)), "la_decode")
+    args = (ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()), dt,
+            ctypes.c_void_p(cu_seqlens_k.data_ptr()), sched.handle, ctypes.c_void_p(workspace.data_ptr()),
+            ctypes.c_void_p(out.data_ptr()))
+    if out_dt == LA_OUT_F32:
+        _check(_lib.la_decode(*args, float(scale), _stream_handle(stream)), "la_decode")
+    else:
+        _check(_lib.la_decode_ex(*args, out_dt, float(scale), _stream_handle(stream)), "la_decode_ex")
     return out
 
 
@@ -278,13 +294,15 @@ class LeanDecoder:
     """Convenience holder: a schedule, its workspace and the device offsets."""
 
     def __init__(self, batch, hq, hkv, d, cu_seqlens_k, num_sms=0, device="cuda", fixed_splits=None,
-                 auto=False):
+                 auto=False, tile_tokens=0, out_dtype=None):
         import torch
         self.predicted_us = None
+        self.out_dtype = out_dtype or torch.float32
         if auto:
             self.sched, self.kind, self.predicted_us = la_plan_auto(batch, hq, hkv, d, cu_seqlens_k, num_sms)
         elif fixed_splits is None:
-            self.sched, self.kind = la_plan(batch, hq, hkv, d, cu_seqlens_k, num_sms), "lean"
+            self.sched = la_plan(batch, hq, hkv, d, cu_seqlens_k, num_sms, tile_tokens)
+            self.kind = "lean"
         else:
             self.sched = la_plan_fixed(batch, hq, hkv, d, cu_seqlens_k, fixed_splits)
             self.kind = "naive" if fixed_splits == 1 else "fixed_split"
@@ -295,7 +313,7 @@ class LeanDecoder:
     def __call__(self, q, k, v, scale, out=None, stream=None):
         import torch
         if out is None:
-            out = torch.empty(self.batch, self.hq, self.d, dtype=torch.float32, device=q.device)
+            out = torch.empty(self.batch, self.hq, self.d, dtype=self.out_dtype, device=q.device)
         return la_decode(q, k, v, self.cu_dev, self.sched, self.workspace, out, scale, stream)
 
     def status(self, stream=None):

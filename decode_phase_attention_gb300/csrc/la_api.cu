@@ -3,6 +3,8 @@
 //
 // Planner rules (xllm-io paper review of LeanAttention):
 //   "3.3 LeanTile"              T = 256 tokens at d = 64, 128 at d = 128
+//                               (other head dims: the tile that keeps a
+//                               stage near 64 KiB of K+V, see default_tile)
 //   "3.4 stream-K decomposition" tiles of all units on one line, split
 //                               evenly over G CTAs, crossing unit boundaries
 //   "3.5 execution flow"        I_G = I / G per CTA; host and finishing CTA
@@ -15,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <map>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -29,8 +32,6 @@ namespace {
 
 constexpr int kMaxGrid = 1 << 20;
 
-int lean_tile(int d) { return d == 64 ? 256 : (d == 128 ? 128 : 0); }
-
 la_status check_shape(int batch, int hq, int hkv, int d, const int32_t* cu) {
   if (batch <= 0 || hq <= 0 || hkv <= 0 || cu == nullptr) return LA_ERR_INVALID;
   if (hq % hkv != 0) return LA_ERR_INVALID;
@@ -38,7 +39,7 @@ la_status check_shape(int batch, int hq, int hkv, int d, const int32_t* cu) {
   for (int b = 0; b < batch; ++b)
     if (cu[b + 1] <= cu[b]) return LA_ERR_INVALID;  // every context holds >= 1 token
   if (d <= 0) return LA_ERR_INVALID;
-  if (d != 64 && d != 128) return LA_ERR_UNSUPPORTED;
+  if (la::default_tile(d) == 0) return LA_ERR_UNSUPPORTED;
   const int grp = hq / hkv;
   if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return LA_ERR_UNSUPPORTED;
   // element offsets are formed in 64 bits, tile indices in 32 bits
@@ -154,11 +155,14 @@ void build_dev_segs(la_schedule* s) {
 }
 
 la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, int kind, int grid_or_splits,
-                        la_schedule** out) {
+                        la_schedule** out, int tile = 0) {
   if (out == nullptr) return LA_ERR_INVALID;
   *out = nullptr;
   const la_status st = check_shape(batch, hq, hkv, d, cu);
   if (st != LA_OK) return st;
+  if (tile == 0) tile = la::default_tile(d);
+  if (tile < 0) return LA_ERR_INVALID;
+  if (!la::tile_supported(d, tile)) return LA_ERR_UNSUPPORTED;
   la_schedule* s = new (std::nothrow) la_schedule();
   if (s == nullptr) return LA_ERR_INVALID;
   s->batch = batch;
@@ -166,7 +170,7 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   s->hkv = hkv;
   s->d = d;
   s->grp = hq / hkv;
-  s->T = lean_tile(d);
+  s->T = tile;
   s->kind = kind;
   s->cu.assign(cu, cu + batch + 1);
   if (!build_units(s)) {
@@ -190,29 +194,23 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   return LA_OK;
 }
 
-// CTAs per SM of the decode kernel, cached per (device, d, grp).
-la_status capacity(int d, int grp, int* per_sm) {
+// CTAs per SM of the decode kernel, cached per (device, d, T, grp).
+la_status capacity(int d, int T, int grp, int* per_sm) {
   static std::mutex mu;
-  static int cache[64][2][4];
-  static bool init = false;
+  static std::map<long long, int> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
-  const int di = d == 64 ? 0 : 1;
-  const int gi = grp == 1 ? 0 : grp == 2 ? 1 : grp == 4 ? 2 : 3;
+  const long long key = (((long long)dev * 1024 + d) * 1024 + T) * 16 + grp;
   std::lock_guard<std::mutex> lock(mu);
-  if (!init) {
-    for (auto& a : cache)
-      for (auto& b : a)
-        for (int& c : b) c = -1;
-    init = true;
-  }
-  if (dev < 64 && cache[dev][di][gi] >= 0) {
-    *per_sm = cache[dev][di][gi];
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *per_sm = it->second;
     return LA_OK;
   }
-  cudaError_t e = d == 64 ? la::decode_capacity_d64(grp, per_sm) : la::decode_capacity_d128(grp, per_sm);
+  cudaError_t e = la::decode_capacity(d, T, grp, per_sm);
+  if (e == cudaErrorInvalidValue) return LA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return LA_ERR_CUDA;
-  if (dev < 64) cache[dev][di][gi] = *per_sm;
+  cache[key] = *per_sm;
   return LA_OK;
 }
 
@@ -315,7 +313,62 @@ namespace la {
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // against libcuda), looked up once.
-cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, int T, int elem_type,
+int default_tile(int d) {
+  switch (d) {
+    case 64: return 256;   // the review's LeanTile table
+    case 128: return 128;  // the review's LeanTile table
+    case 80: return 128;   // 40 KiB of K+V per tile
+    case 96: return 128;   // 48 KiB
+    case 256: return 64;   // 64 KiB, like the table's two sizes
+    default: return 0;
+  }
+}
+
+bool tile_supported(int d, int T) {
+  switch (d) {
+    case 64: return T == 256 || T == 128;
+    case 128: return T == 128 || T == 64;
+    case 80:
+    case 96: return T == 128;
+    case 256: return T == 64;
+    default: return false;
+  }
+}
+
+cudaError_t launch_decode(int d, int T, int grp, int dtype, const KParams& p, cudaStream_t st) {
+  switch (d) {
+    case 64: return launch_decode_d64(T, grp, dtype, p, st);
+    case 80: return launch_decode_d80(T, grp, dtype, p, st);
+    case 96: return launch_decode_d96(T, grp, dtype, p, st);
+    case 128: return launch_decode_d128(T, grp, dtype, p, st);
+    case 256: return launch_decode_d256(T, grp, dtype, p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st) {
+  switch (d) {
+    case 64: return launch_combine_d64(grp, p, st);
+    case 80: return launch_combine_d80(grp, p, st);
+    case 96: return launch_combine_d96(grp, p, st);
+    case 128: return launch_combine_d128(grp, p, st);
+    case 256: return launch_combine_d256(grp, p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t decode_capacity(int d, int T, int grp, int* per_sm) {
+  switch (d) {
+    case 64: return decode_capacity_d64(T, grp, per_sm);
+    case 80: return decode_capacity_d80(T, grp, per_sm);
+    case 96: return decode_capacity_d96(T, grp, per_sm);
+    case 128: return decode_capacity_d128(T, grp, per_sm);
+    case 256: return decode_capacity_d256(T, grp, per_sm);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, int T, int W, int elem_type,
                            CUtensorMap* mk, CUtensorMap* mv) {
   using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -337,12 +390,14 @@ cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, 
   if (rows <= 0 || rows > (1LL << 31) - 1) return cudaErrorInvalidValue;
   const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)T};
+  const cuuint32_t box[2] = {(cuuint32_t)W, (cuuint32_t)T};
+  const CUtensorMapSwizzle swz = W == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                          : (W == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = (CUtensorMapDataType)elem_type;
   for (int i = 0; i < 2; ++i) {
     CUresult r = fn(i == 0 ? mk : mv, dt, 2, const_cast<void*>(i == 0 ? k : v), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
@@ -353,22 +408,30 @@ cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, 
 
 extern "C" {
 
-la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int num_sms,
-                  la_schedule** out) {
+la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int num_sms,
+                     int tile_tokens, la_schedule** out) {
   if (out != nullptr) *out = nullptr;
   int G = num_sms;
   if (G <= 0) {
     const la_status st = check_shape(batch, hq, hkv, d, cu_seqlens_k);
     if (st != LA_OK) return st;
+    const int T = tile_tokens == 0 ? la::default_tile(d) : tile_tokens;
+    if (T <= 0) return LA_ERR_INVALID;
+    if (!la::tile_supported(d, T)) return LA_ERR_UNSUPPORTED;
     int sms = 0, per_sm = 0;
     la_status e = device_sms(&sms);
     if (e != LA_OK) return e;
-    e = capacity(d, hq / hkv, &per_sm);
+    e = capacity(d, T, hq / hkv, &per_sm);
     if (e != LA_OK) return e;
     G = sms * std::max(1, per_sm);
   }
   if (G > kMaxGrid) return LA_ERR_INVALID;
-  return make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out);
+  return make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out, tile_tokens);
+}
+
+la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int num_sms,
+                  la_schedule** out) {
+  return la_plan_ex(batch, hq, hkv, d, cu_seqlens_k, num_sms, 0, out);
 }
 
 la_status la_plan_fixed(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int splits,
@@ -389,7 +452,7 @@ la_status la_plan_auto(int batch, int hq, int hkv, int d, const int32_t* cu_seql
     int sms = 0, per_sm = 0;
     st = device_sms(&sms);
     if (st != LA_OK) return st;
-    st = capacity(d, hq / hkv, &per_sm);
+    st = capacity(d, la::default_tile(d), hq / hkv, &per_sm);
     if (st != LA_OK) return st;
     slots = sms * std::max(1, per_sm);
   }
@@ -430,8 +493,11 @@ la_status la_workspace_init(void* workspace, size_t bytes, la_stream_t stream) {
   return cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
-la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt, const int32_t* cu_seqlens_k_dev,
-                    const la_schedule* sc, void* workspace, float* out, float scale, la_stream_t stream) {
+la_status la_decode_ex(const void* q, const void* k, const void* v, la_dtype dt, const int32_t* cu_seqlens_k_dev,
+                       const la_schedule* sc, void* workspace, void* out, la_dtype_out out_dt, float scale,
+                       la_stream_t stream) {
+  if (out_dt != LA_OUT_F32 && out_dt != LA_OUT_F16 && out_dt != LA_OUT_BF16) return LA_ERR_INVALID;
+  const int out_dtype = (int)out_dt;
   if (sc == nullptr || q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
       cu_seqlens_k_dev == nullptr)
     return LA_ERR_INVALID;
@@ -446,7 +512,7 @@ la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt, co
     int sms = 0, per_sm = 0;
     la_status e = device_sms(&sms);
     if (e != LA_OK) return e;
-    e = capacity(s->d, s->grp, &per_sm);
+    e = capacity(s->d, s->T, s->grp, &per_sm);
     if (e != LA_OK) return e;
     if ((int64_t)s->G > (int64_t)sms * per_sm) return LA_ERR_INVALID;
   }
@@ -475,10 +541,10 @@ la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt, co
   p.spin_ns = s->spin_ns;
   p.skip_signal = s->skip_signal;
   p.trace = s->trace;
+  p.out_dtype = out_dtype;
   cudaStream_t st = (cudaStream_t)stream;
   const int dtype = dt == LA_BF16 ? 1 : 0;
-  cudaError_t ce = s->d == 64 ? la::launch_decode_d64(s->grp, dtype, p, st)
-                              : la::launch_decode_d128(s->grp, dtype, p, st);
+  cudaError_t ce = la::launch_decode(s->d, s->T, s->grp, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {
     la::CParams c;
@@ -489,10 +555,16 @@ la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt, co
     c.U = s->U;
     c.hq = s->hq;
     c.hkv = s->hkv;
-    ce = s->d == 64 ? la::launch_combine_d64(s->grp, c, st) : la::launch_combine_d128(s->grp, c, st);
+    c.out_dtype = out_dtype;
+    ce = la::launch_combine(s->d, s->grp, c, st);
     if (ce != cudaSuccess) return LA_ERR_CUDA;
   }
   return LA_OK;
+}
+
+la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt, const int32_t* cu_seqlens_k_dev,
+                    const la_schedule* s, void* workspace, float* out, float scale, la_stream_t stream) {
+  return la_decode_ex(q, k, v, dt, cu_seqlens_k_dev, s, workspace, out, LA_OUT_F32, scale, stream);
 }
 
 la_status la_get_status(void* workspace, la_stream_t stream) {
@@ -551,11 +623,11 @@ la_status la_schedule_set_trace(la_schedule* s, void* trace_dev) {
 
 la_status la_device_capacity(int d, int grp, int* ctas_per_sm, int* num_sms) {
   if (ctas_per_sm == nullptr || num_sms == nullptr) return LA_ERR_INVALID;
-  if (d != 64 && d != 128) return LA_ERR_UNSUPPORTED;
+  if (la::default_tile(d) == 0) return LA_ERR_UNSUPPORTED;
   if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return LA_ERR_UNSUPPORTED;
   la_status e = device_sms(num_sms);
   if (e != LA_OK) return e;
-  return capacity(d, grp, ctas_per_sm);
+  return capacity(d, la::default_tile(d), grp, ctas_per_sm);
 }
 
 void la_schedule_destroy(la_schedule* s) {

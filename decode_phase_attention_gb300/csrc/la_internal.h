@@ -38,7 +38,7 @@ struct KParams {
   const int32_t* sched_cu;  // the schedule's own copy (batch + 1)
   const int32_t* cta_seg;   // [G + 1]
   const int32_t* segs;      // [nseg * kSegWords]
-  float* out;
+  void* out;                // fp32, fp16 or bf16 per out_dtype
   uint32_t* hdr;
   uint32_t* flags;
   float* recs;
@@ -51,6 +51,7 @@ struct KParams {
   long long spin_ns;        // limit of every wait inside the kernel
   int skip_signal;          // test hook: this CTA never sets its flag (-1: none)
   unsigned long long* trace;  // optional per-CTA timeline (kTraceWords each), or null
+  int out_dtype = 0;          // 0 fp32, 1 fp16, 2 bf16
 };
 
 // Per-CTA trace record (globaltimer ns): written when KParams::trace is set.
@@ -70,19 +71,32 @@ struct CParams {            // fixed-split merge launch
   const int32_t* unit_host; // [U]
   const int32_t* unit_fin;  // [U]
   const float* recs;
-  float* out;
+  void* out;
   int U;
   int hq;
   int hkv;
+  int out_dtype = 0;        // 0 fp32, 1 fp16, 2 bf16
 };
 
-// Launches (defined in la_kernels_d64.cu / la_kernels_d128.cu). dtype: 0 fp16, 1 bf16.
-cudaError_t launch_decode_d64(int grp, int dtype, const KParams& p, cudaStream_t st);
-cudaError_t launch_decode_d128(int grp, int dtype, const KParams& p, cudaStream_t st);
-cudaError_t launch_combine_d64(int grp, const CParams& p, cudaStream_t st);
-cudaError_t launch_combine_d128(int grp, const CParams& p, cudaStream_t st);
+// LeanTile sizes: the default per head dim, and whether (d, T) is built.
+int default_tile(int d);
+bool tile_supported(int d, int T);
+
+// Launches (la_kernels_d<d>.cu, one file per head dim). dtype: 0 fp16, 1 bf16.
+// cudaErrorInvalidValue for a (d, T, grp) that is not built.
+cudaError_t launch_decode(int d, int T, int grp, int dtype, const KParams& p, cudaStream_t st);
+cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st);
 // CTAs of the decode kernel one SM holds at once (cudaOccupancy...).
-cudaError_t decode_capacity_d64(int grp, int* per_sm);
-cudaError_t decode_capacity_d128(int grp, int* per_sm);
+cudaError_t decode_capacity(int d, int T, int grp, int* per_sm);
+#define LA_DECLARE_HEAD_DIM(D)                                                           \
+  cudaError_t launch_decode_d##D(int T, int grp, int dtype, const KParams& p, cudaStream_t st); \
+  cudaError_t launch_combine_d##D(int grp, const CParams& p, cudaStream_t st);           \
+  cudaError_t decode_capacity_d##D(int T, int grp, int* per_sm);
+LA_DECLARE_HEAD_DIM(64)
+LA_DECLARE_HEAD_DIM(80)
+LA_DECLARE_HEAD_DIM(96)
+LA_DECLARE_HEAD_DIM(128)
+LA_DECLARE_HEAD_DIM(256)
+#undef LA_DECLARE_HEAD_DIM
 
 }  // namespace la

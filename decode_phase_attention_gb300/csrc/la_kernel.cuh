@@ -214,36 +214,55 @@ struct Elem<__half> {
 };
 
 // ------------------------------------------------------------ configuration
-template <int D, int GRP>
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
+
+template <int D, int T_, int GRP>
 struct Cfg {
-  static constexpr int T = (D == 64) ? 256 : 128;  // LeanTile ("3.3 LeanTile" table)
+  static constexpr int T = T_;                      // LeanTile tokens
   static constexpr bool TC = (GRP >= 4);            // tensor-core tile path
-  static constexpr int NCW = 8;                     // consumer warps
+  // consumer warps: 8, or fewer when an MMA tile of 16 tokens per warp needs it
+  static constexpr int NCW = TC ? cmin(8, T / 16) : 8;
   static constexpr int NCT = NCW * 32;              // consumer threads
   static constexpr int NTHREADS = NCT + 32;         // + producer warp
   static constexpr int TPW = T / NCW;               // tokens per warp per tile
-  // CUDA-core path
-  static constexpr int LPT = D / 8;                 // lanes per token
+  // CUDA-core path: d/8 active lanes per token (16 bytes each), rounded up
+  // to a power-of-two lane group; the spare lanes of a group idle.
+  static constexpr int ACT = D / 8;
+  static constexpr int LPT = ACT <= 8 ? 8 : (ACT <= 16 ? 16 : 32);
   static constexpr int TPS = 32 / LPT;              // tokens per warp step
   static constexpr int STEPS = TPW / TPS;
-  static constexpr int CH = (GRP <= 2) ? STEPS : (GRP == 4 ? 4 : 2);  // steps per softmax update
-  // tensor-core path
+  static constexpr int CH = (GRP <= 2) ? cmin(STEPS, 8) : (GRP == 4 ? cmin(STEPS, 4) : cmin(STEPS, 2));
+  // tensor-core path: TMA boxes of W columns (W*2-byte rows, swizzled)
+  static constexpr int W = (D % 64 == 0) ? 64 : ((D % 32 == 0) ? 32 : 16);
+  static constexpr int RB = W * 2;                  // box row bytes: 128, 64 or 32
+  static constexpr int NB = D / W;                  // boxes per tile per tensor
   static constexpr int MT = TPW / 16;               // 16-token MMA tiles per warp
-  static constexpr int KS = D / 16;                 // 16-wide k steps over the head dim
-  static constexpr int NB = D / 64;                 // 64-column (128-byte) swizzled blocks
-  static constexpr int STAGES = 3;
+  static constexpr int KS = D / 16;                 // 16-wide steps over the head dim
   static constexpr int TILE_ELEMS = T * D;
-  static constexpr size_t KV_BYTES = (size_t)STAGES * 2 * TILE_ELEMS * 2;
+  static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
+  static constexpr int STAGES = cmax(2, cmin(4, 196608 / STAGE_BYTES));
+  static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
   static constexpr int REC = D + 2;                 // [m, l, O[d]]
   static constexpr size_t MERGE_BYTES = (size_t)NCW * GRP * REC * 4;
   static constexpr size_t BAR_BYTES = 2 * STAGES * 8 + 16;
   static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES + (TC ? 1024 : 0);
   static constexpr int ITEMS = (GRP * D + NCT - 1) / NCT;  // (head, dim) outputs per consumer thread
-  static_assert(STEPS % CH == 0, "chunking");
-  static_assert(TPW % TPS == 0, "tokens per warp");
+  static_assert(D % 16 == 0 && T % 16 == 0, "tile shape");
+  static_assert(STEPS % CH == 0 && TPW % TPS == 0, "CUDA-core tile shape");
   static_assert(!TC || (TPW % 16 == 0 && GRP <= 8), "tensor-core tile shape");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
+
+// Output element store (fp32, fp16 or bf16, chosen per call).
+__device__ __forceinline__ void store_out(void* out, size_t idx, float v, int out_dtype) {
+  if (out_dtype == 0)
+    static_cast<float*>(out)[idx] = v;
+  else if (out_dtype == 1)
+    static_cast<__half*>(out)[idx] = __float2half_rn(v);
+  else
+    static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+}
 
 // Record the first error of the launch in the workspace header.
 __device__ __forceinline__ void record_error(uint32_t* hdr, uint32_t code, int cta, int peer) {
@@ -275,10 +294,10 @@ __device__ __forceinline__ bool unit_offsets_ok(const KParams& p, int b) {
 }
 
 // ------------------------------------------------------------------ producer
-template <int D, int GRP, typename E>
+template <int D, int T, int GRP, typename E>
 __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, int g,
                                         E* kv, uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
-  using C = Cfg<D, GRP>;
+  using C = Cfg<D, T, GRP>;
   const uint64_t pol = l2_evict_first_policy();
   if (C::TC) {
     prefetch_tmap(tmk);
@@ -314,8 +333,8 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
         const int y = (int)(row0 + (long long)t * C::T);
 #pragma unroll
         for (int bk = 0; bk < C::NB; ++bk) {
-          tma_load_2d(ks + bk * C::T * 64, tmk, bk * 64, y, &full[stage], pol);
-          tma_load_2d(ks + C::TILE_ELEMS + bk * C::T * 64, tmv, bk * 64, y, &full[stage], pol);
+          tma_load_2d(ks + bk * C::T * C::W, tmk, bk * C::W, y, &full[stage], pol);
+          tma_load_2d(ks + C::TILE_ELEMS + bk * C::T * C::W, tmv, bk * C::W, y, &full[stage], pol);
         }
       } else {
         const uint32_t bytes = (uint32_t)ntok * D * 2u;
@@ -346,7 +365,7 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
 }
 
 // Wait for the next stage; false (for the whole warp) if it never came.
-template <int D, int GRP>
+template <int D, int T, int GRP>
 __device__ __forceinline__ bool wait_tile(const KParams& p, int g, uint64_t* full, int stage, uint32_t phase,
                                           volatile int* abort_flag, int lane) {
   bool have = mbar_wait_bounded(&full[stage], phase, abort_flag, p.spin_ns);
@@ -366,23 +385,26 @@ __device__ __forceinline__ bool wait_tile(const KParams& p, int g, uint64_t* ful
 // ----------------------------------------------- CUDA-core tile path (grp 1, 2)
 // Runs the segment's tiles and leaves this warp's (m, l, O) for every head
 // of the group in its slot of the merge area.
-template <int D, int GRP, typename E>
+template <int D, int T, int GRP, typename E>
 __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, int kvh, long long L, int t0,
                                                 int n_tiles, bool ok, const E* kv, uint64_t* full, uint64_t* empty,
                                                 int& stage, uint32_t& phase, volatile int* abort_flag,
                                                 float* wrec) {
-  using C = Cfg<D, GRP>;
+  using C = Cfg<D, T, GRP>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int gl = lane % C::LPT;  // which 8-element chunk of the row
-  const int ts = lane / C::LPT;  // which token of the warp step
-  const int c0 = gl * 8;
+  const int gl = lane % C::LPT;   // which 8-element chunk of the row
+  const int ts = lane / C::LPT;   // which token of the warp step
+  const bool act = gl < C::ACT;   // spare lanes of a group (d = 80, 96) idle
+  const int c0 = act ? gl * 8 : 0;
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
 
   float qf[GRP][8];
 #pragma unroll
   for (int j = 0; j < GRP; ++j) {
     const int h = kvh * GRP + j;
     const uint4 raw =
-        *reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) + ((size_t)b * p.hq + h) * D + c0);
+        act ? *reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) + ((size_t)b * p.hq + h) * D + c0)
+            : zero4;
     Elem<E>::to_f32(raw, qf[j]);
 #pragma unroll
     for (int e = 0; e < 8; ++e) qf[j][e] *= p.qscale;
@@ -399,7 +421,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
   for (int it = 0; it < n_tiles; ++it) {
     const long long rem = L - (long long)(t0 + it) * C::T;
     const int ntok = rem < C::T ? (int)rem : C::T;
-    if (wait_tile<D, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
+    if (wait_tile<D, T, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
       const E* Ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
       const E* Vs = Ks + C::TILE_ELEMS;
       const int wtok = warp * C::TPW;
@@ -409,7 +431,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
 #pragma unroll
         for (int st = 0; st < C::CH; ++st) {
           const int tok = wtok + (c + st) * C::TPS + ts;
-          const uint4 raw = *reinterpret_cast<const uint4*>(Ks + tok * D + c0);
+          const uint4 raw = act ? *reinterpret_cast<const uint4*>(Ks + tok * D + c0) : zero4;
           float kf[8];
           Elem<E>::to_f32(raw, kf);
 #pragma unroll
@@ -465,7 +487,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
 #pragma unroll
         for (int st = 0; st < C::CH; ++st) {
           const int tok = wtok + (c + st) * C::TPS + ts;
-          if (tok < ntok) {
+          if (tok < ntok && act) {
             const uint4 raw = *reinterpret_cast<const uint4*>(Vs + tok * D + c0);
             float vf[8];
             Elem<E>::to_f32(raw, vf);
@@ -504,7 +526,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
       }
     }
   }
-  if (ts == 0) {
+  if (ts == 0 && act) {
 #pragma unroll
     for (int j = 0; j < GRP; ++j) {
       float* r = wrec + j * C::REC;
@@ -521,18 +543,19 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
 // -------------------------------------------- tensor-core tile path (grp 4, 8)
 // Swizzled shared-memory address (128-byte swizzle: 16-byte chunk c of row r
 // sits at chunk c ^ (r mod 8)) of row `row`, chunk `c` of 64-column block bk.
-template <int D, int GRP>
+template <int D, int T, int GRP>
 __device__ __forceinline__ uint32_t swz(uint32_t tile_base, int bk, int row, int c) {
-  using C = Cfg<D, GRP>;
-  return tile_base + (uint32_t)(bk * C::T * 128 + row * 128 + ((c ^ (row & 7)) << 4));
+  using C = Cfg<D, T, GRP>;
+  return tile_base + (uint32_t)(bk * C::T * C::RB + row * C::RB +
+                                ((c ^ ((row * C::RB >> 7) & (C::RB / 16 - 1))) << 4));
 }
 
-template <int D, int GRP, typename E>
+template <int D, int T, int GRP, typename E>
 __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, int kvh, long long L, int t0,
                                                 int n_tiles, bool ok, const E* kv, uint64_t* full, uint64_t* empty,
                                                 int& stage, uint32_t& phase, volatile int* abort_flag,
                                                 float* wrec) {
-  using C = Cfg<D, GRP>;
+  using C = Cfg<D, T, GRP>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gq = lane >> 2;  // fragment row group
   const int tq = lane & 3;   // fragment column pair
@@ -563,7 +586,7 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
   for (int it = 0; it < n_tiles; ++it) {
     const long long rem = L - (long long)(t0 + it) * C::T;
     const int ntok = rem < C::T ? (int)rem : C::T;
-    if (wait_tile<D, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
+    if (wait_tile<D, T, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
       const uint32_t kb = kv_base + (uint32_t)(stage * 2 * C::TILE_ELEMS * 2);
       const uint32_t vb = kb + (uint32_t)(C::TILE_ELEMS * 2);
       const int wtok = warp * C::TPW;
@@ -577,7 +600,7 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
           uint32_t a[4];
-          ldsm_x4(a, swz<D, GRP>(kb, ks >> 2, row, (ks & 3) * 2 + (lane >> 4)));
+          ldsm_x4(a, swz<D, T, GRP>(kb, ks * 16 / C::W, row, (ks * 16 % C::W) / 8 + (lane >> 4)));
           Elem<E>::mma(s[mt], a, qb[ks][0], qb[ks][1]);
         }
       }
@@ -635,7 +658,7 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
 #pragma unroll
         for (int dm = 0; dm < C::KS; ++dm) {
           uint32_t a[4];
-          ldsm_x4_trans(a, swz<D, GRP>(vb, dm >> 2, vrow, (dm & 3) * 2 + ((lane >> 3) & 1)));
+          ldsm_x4_trans(a, swz<D, T, GRP>(vb, dm * 16 / C::W, vrow, (dm * 16 % C::W) / 8 + ((lane >> 3) & 1)));
           Elem<E>::mma(o[dm], a, bh0, bh1);
           Elem<E>::mma(o[dm], a, bl0, bl1);
         }
@@ -675,10 +698,10 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
 }
 
 // ------------------------------------------------------------------ consumers
-template <int D, int GRP, typename E>
+template <int D, int T, int GRP, typename E>
 __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, uint64_t* full, uint64_t* empty,
                                         float* mrg, volatile int* abort_flag, uint32_t epoch) {
-  using C = Cfg<D, GRP>;
+  using C = Cfg<D, T, GRP>;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
   const uint32_t ready = epoch + 1u;
@@ -701,10 +724,10 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
     // ---- the LeanTile loop; leaves this warp's (m, l, O) in the merge area
     float* wrec = mrg + (size_t)warp * GRP * C::REC;
     if constexpr (C::TC)
-      warp_segment_tc<D, GRP, E>(p, g, b, kvh, L, t0, n_tiles, ok, kv, full, empty, stage, phase, abort_flag,
+      warp_segment_tc<D, T, GRP, E>(p, g, b, kvh, L, t0, n_tiles, ok, kv, full, empty, stage, phase, abort_flag,
                                  wrec);
     else
-      warp_segment_cc<D, GRP, E>(p, g, b, kvh, L, t0, n_tiles, ok, kv, full, empty, stage, phase, abort_flag,
+      warp_segment_cc<D, T, GRP, E>(p, g, b, kvh, L, t0, n_tiles, ok, kv, full, empty, stage, phase, abort_flag,
                                  wrec);
     if (p.trace != nullptr && tid == 0) {
       unsigned long long* tr = p.trace + (size_t)g * kTraceWords;
@@ -824,7 +847,7 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
         if (idx < GRP * D) {
           const int j = idx / D, cc = idx % D;
           const float val = fail ? __int_as_float(0x7fc00000) : O[i] / Lsum[i];
-          p.out[((size_t)b * p.hq + (size_t)kvh * GRP + j) * D + cc] = val;
+          store_out(p.out, ((size_t)b * p.hq + (size_t)kvh * GRP + j) * D + cc, val, p.out_dtype);
         }
       }
     }
@@ -833,11 +856,11 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
 }
 
 // -------------------------------------------------------------------- kernel
-template <int D, int GRP, typename E>
-__global__ void __launch_bounds__(Cfg<D, GRP>::NTHREADS, 1)
+template <int D, int T, int GRP, typename E>
+__global__ void __launch_bounds__(Cfg<D, T, GRP>::NTHREADS, 1)
     lean_decode_kernel(const KParams p, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv) {
-  using C = Cfg<D, GRP>;
+  using C = Cfg<D, T, GRP>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the 128-byte swizzle of TMA tiles needs 1024-byte aligned destinations
   unsigned char* smem = C::TC ? reinterpret_cast<unsigned char*>(
@@ -872,10 +895,10 @@ __global__ void __launch_bounds__(Cfg<D, GRP>::NTHREADS, 1)
   const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr[kEpoch]);
 
   if ((tid >> 5) == C::NCW) {
-    if ((tid & 31) == 0) produce<D, GRP, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
+    if ((tid & 31) == 0) produce<D, T, GRP, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
     __syncwarp();
   } else {
-    consume<D, GRP, E>(p, g, kv, full, empty, mrg, flags_smem, epoch);
+    consume<D, T, GRP, E>(p, g, kv, full, empty, mrg, flags_smem, epoch);
   }
   __syncthreads();
   if (tid == 0) {
@@ -915,24 +938,24 @@ __global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
     M = mn;
   }
   const int b = unit / p.hkv, kvh = unit % p.hkv;
-  p.out[((size_t)b * p.hq + (size_t)kvh * GRP + j) * D + c] = O / Ls;
+  store_out(p.out, ((size_t)b * p.hq + (size_t)kvh * GRP + j) * D + c, O / Ls, p.out_dtype);
 }
 
 // ------------------------------------------------------------- host launchers
 // Tensor maps of K and V seen as one [rows = hkv * total tokens, D] matrix,
-// boxes of 64 columns x T rows with 128-byte swizzle.
-cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, int T, int elem_type,
+// boxes of W columns x T rows, swizzled over W * 2 bytes (32, 64 or 128).
+cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, int T, int W, int elem_type,
                            CUtensorMap* mk, CUtensorMap* mv);
 
-template <int D, int GRP, typename E>
+template <int D, int T, int GRP, typename E>
 cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
-  using C = Cfg<D, GRP>;
+  using C = Cfg<D, T, GRP>;
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(lean_decode_kernel<D, GRP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(lean_decode_kernel<D, T, GRP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM);
     if (e != cudaSuccess) return e;
     configured_device = dev;
@@ -940,23 +963,23 @@ cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
   if (p.G <= 0) return cudaSuccess;
   CUtensorMap mk, mv;
   if (C::TC) {
-    e = encode_kv_maps(p.k, p.v, p.kv_rows, D, C::T, (int)Elem<E>::kTmaType, &mk, &mv);
+    e = encode_kv_maps(p.k, p.v, p.kv_rows, D, C::T, C::W, (int)Elem<E>::kTmaType, &mk, &mv);
     if (e != cudaSuccess) return e;
   } else {
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
   }
-  lean_decode_kernel<D, GRP, E><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
+  lean_decode_kernel<D, T, GRP, E><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
   return cudaGetLastError();
 }
 
-template <int D, int GRP>
+template <int D, int T, int GRP>
 cudaError_t capacity_t(int* per_sm) {
-  using C = Cfg<D, GRP>;
-  cudaError_t e = cudaFuncSetAttribute(lean_decode_kernel<D, GRP, __nv_bfloat16>,
+  using C = Cfg<D, T, GRP>;
+  cudaError_t e = cudaFuncSetAttribute(lean_decode_kernel<D, T, GRP, __nv_bfloat16>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lean_decode_kernel<D, GRP, __nv_bfloat16>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lean_decode_kernel<D, T, GRP, __nv_bfloat16>,
                                                        C::NTHREADS, C::SMEM);
 }
 

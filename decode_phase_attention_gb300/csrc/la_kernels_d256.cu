@@ -1,0 +1,41 @@
+// la_kernels_d256.cu -- instances of the decode kernels for head dim 256
+// (LeanTile sizes 64 tokens), query-head groups 1, 2, 4 and 8, fp16 and bf16.
+#include "la_kernel.cuh"
+
+namespace la {
+
+cudaError_t launch_decode_d256(int T, int grp, int dtype, const KParams& p, cudaStream_t st) {
+  if (T == 64 && grp == 1)
+    return dtype ? launch_decode_t<256, 64, 1, __nv_bfloat16>(p, st)
+                 : launch_decode_t<256, 64, 1, __half>(p, st);
+  if (T == 64 && grp == 2)
+    return dtype ? launch_decode_t<256, 64, 2, __nv_bfloat16>(p, st)
+                 : launch_decode_t<256, 64, 2, __half>(p, st);
+  if (T == 64 && grp == 4)
+    return dtype ? launch_decode_t<256, 64, 4, __nv_bfloat16>(p, st)
+                 : launch_decode_t<256, 64, 4, __half>(p, st);
+  if (T == 64 && grp == 8)
+    return dtype ? launch_decode_t<256, 64, 8, __nv_bfloat16>(p, st)
+                 : launch_decode_t<256, 64, 8, __half>(p, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine_d256(int grp, const CParams& p, cudaStream_t st) {
+  switch (grp) {
+    case 1: return launch_combine_t<256, 1>(p, st);
+    case 2: return launch_combine_t<256, 2>(p, st);
+    case 4: return launch_combine_t<256, 4>(p, st);
+    case 8: return launch_combine_t<256, 8>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t decode_capacity_d256(int T, int grp, int* per_sm) {
+  if (T == 64 && grp == 1) return capacity_t<256, 64, 1>(per_sm);
+  if (T == 64 && grp == 2) return capacity_t<256, 64, 2>(per_sm);
+  if (T == 64 && grp == 4) return capacity_t<256, 64, 4>(per_sm);
+  if (T == 64 && grp == 8) return capacity_t<256, 64, 8>(per_sm);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace la

@@ -1,0 +1,41 @@
+// la_kernels_d96.cu -- instances of the decode kernels for head dim 96
+// (LeanTile sizes 128 tokens), query-head groups 1, 2, 4 and 8, fp16 and bf16.
+#include "la_kernel.cuh"
+
+namespace la {
+
+cudaError_t launch_decode_d96(int T, int grp, int dtype, const KParams& p, cudaStream_t st) {
+  if (T == 128 && grp == 1)
+    return dtype ? launch_decode_t<96, 128, 1, __nv_bfloat16>(p, st)
+                 : launch_decode_t<96, 128, 1, __half>(p, st);
+  if (T == 128 && grp == 2)
+    return dtype ? launch_decode_t<96, 128, 2, __nv_bfloat16>(p, st)
+                 : launch_decode_t<96, 128, 2, __half>(p, st);
+  if (T == 128 && grp == 4)
+    return dtype ? launch_decode_t<96, 128, 4, __nv_bfloat16>(p, st)
+                 : launch_decode_t<96, 128, 4, __half>(p, st);
+  if (T == 128 && grp == 8)
+    return dtype ? launch_decode_t<96, 128, 8, __nv_bfloat16>(p, st)
+                 : launch_decode_t<96, 128, 8, __half>(p, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine_d96(int grp, const CParams& p, cudaStream_t st) {
+  switch (grp) {
+    case 1: return launch_combine_t<96, 1>(p, st);
+    case 2: return launch_combine_t<96, 2>(p, st);
+    case 4: return launch_combine_t<96, 4>(p, st);
+    case 8: return launch_combine_t<96, 8>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t decode_capacity_d96(int T, int grp, int* per_sm) {
+  if (T == 128 && grp == 1) return capacity_t<96, 128, 1>(per_sm);
+  if (T == 128 && grp == 2) return capacity_t<96, 128, 2>(per_sm);
+  if (T == 128 && grp == 4) return capacity_t<96, 128, 4>(per_sm);
+  if (T == 128 && grp == 8) return capacity_t<96, 128, 8>(per_sm);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace la

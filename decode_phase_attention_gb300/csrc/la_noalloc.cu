@@ -89,8 +89,9 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
 
   if (s->kind == 0) {  // host CTAs wait on later CTAs: all of the grid must be resident
     int per_sm = 0, sms = 0;
-    const la_status e = la_device_capacity(s->d, s->grp, &per_sm, &sms);
+    la_status e = la_device_capacity(s->d, s->grp, &per_sm, &sms);
     if (e != LA_OK) return e;
+    if (la::decode_capacity(s->d, s->T, s->grp, &per_sm) != cudaSuccess) return LA_ERR_CUDA;
     if ((long long)s->G > (long long)per_sm * sms) return LA_ERR_INVALID;
   }
   int dev = 0;
@@ -131,8 +132,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   p.skip_signal = s->skip_signal;
   p.trace = s->trace;
   const int dtype = dt == LA_BF16 ? 1 : 0;
-  cudaError_t ce = s->d == 64 ? la::launch_decode_d64(s->grp, dtype, p, st)
-                              : la::launch_decode_d128(s->grp, dtype, p, st);
+  cudaError_t ce = la::launch_decode(s->d, s->T, s->grp, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {
     la::CParams c;
@@ -143,7 +143,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
     c.U = s->U;
     c.hq = s->hq;
     c.hkv = s->hkv;
-    ce = s->d == 64 ? la::launch_combine_d64(s->grp, c, st) : la::launch_combine_d128(s->grp, c, st);
+    ce = la::launch_combine(s->d, s->grp, c, st);
     if (ce != cudaSuccess) return LA_ERR_CUDA;
   }
   return LA_OK;

@@ -65,6 +65,9 @@ typedef enum {
 
 typedef enum { LA_F16 = 0, LA_BF16 = 1 } la_dtype;
 
+/* Element type of the output of la_decode_ex. */
+typedef enum { LA_OUT_F32 = 0, LA_OUT_F16 = 1, LA_OUT_BF16 = 2 } la_dtype_out;
+
 /* Kinds of work a CTA does on one unit, as exported by la_schedule_export. */
 enum {
   LA_SEG_WHOLE = 0,   /* the CTA covers the whole unit: normalise, write out */
@@ -77,7 +80,7 @@ enum {
  * la_plan -- the stream-K tile planner ("3.4 stream-K style decomposition"
  * and "3.5 execution flow" of the xllm-io review).
  *
- *   batch, hq, hkv, d  shape; d in {64, 128}; hq % hkv == 0 and
+ *   batch, hq, hkv, d  shape; d in {64, 80, 96, 128, 256}; hq % hkv == 0 and
  *                      hq / hkv in {1, 2, 4, 8}
  *   cu_seqlens_k       HOST pointer to batch + 1 int32 offsets (read, not kept)
  *   num_sms            grid size G; <= 0 picks one persistent CTA per SM of
@@ -87,7 +90,8 @@ enum {
  *                      later CTAs inside the launch.
  *   out                receives the new schedule
  *
- * Rules: tiles(b) = ceil(L_b / T), T = 256 (d = 64) or 128 (d = 128);
+ * Rules: tiles(b) = ceil(L_b / T), T = 256 (d = 64) or 128 (d = 128),
+ * for other head dims the default of la_plan_ex;
  * units (b, kv head) in request-major order; I = total tiles; CTA g takes
  * floor(I/G) iterations plus one if g < I mod G, in order; the host of a
  * unit is the CTA holding its first tile, the finisher the one holding its
@@ -96,6 +100,24 @@ enum {
  */
 la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int num_sms,
                   la_schedule** out);
+
+/*
+ * la_plan_ex -- la_plan with more head dims and a chosen LeanTile size (the
+ * review's "7.4 limitations": the best LeanTile depends on the hardware and
+ * the configuration, so it is a parameter).
+ *
+ *   d            64, 80, 96, 128 or 256
+ *   tile_tokens  0 for the default of d, else one of the built sizes:
+ *                d = 64: 256 (default) or 128;  d = 128: 128 (default) or 64;
+ *                d = 80, 96: 128;  d = 256: 64.
+ *                The table gives 256 and 128 tokens for d = 64 and 128
+ *                (64 KiB of K+V per tile); the other defaults keep a tile
+ *                near that size (40, 48 and 64 KiB).
+ * Other arguments and rules as la_plan. LA_ERR_UNSUPPORTED for a (d, T)
+ * that is not built.
+ */
+la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int num_sms,
+                     int tile_tokens, la_schedule** out);
 
 /*
  * la_plan_fixed -- fixed partitions used as baselines (the review's "2.2"
@@ -169,6 +191,16 @@ la_status la_workspace_init(void* workspace, size_t bytes, la_stream_t stream);
 la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt,
                     const int32_t* cu_seqlens_k_dev, const la_schedule* s, void* workspace,
                     float* out, float scale, la_stream_t stream);
+
+/*
+ * la_decode_ex -- la_decode with a choice of output element type: out is
+ * [batch, hq, d] of fp32 (LA_OUT_F32, what la_decode writes), fp16 or bf16
+ * (rounded to nearest even from the fp32 result); 16-byte aligned.
+ * LA_ERR_INVALID for an unknown out_dt; otherwise as la_decode.
+ */
+la_status la_decode_ex(const void* q, const void* k, const void* v, la_dtype dt,
+                       const int32_t* cu_seqlens_k_dev, const la_schedule* s, void* workspace,
+                       void* out, la_dtype_out out_dt, float scale, la_stream_t stream);
 
 /*
  * la_decode_static -- la_decode without a workspace and without any device

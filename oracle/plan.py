@@ -44,8 +44,10 @@ def lean_tile(d):
     return table[d]
 
 
-def _units(batch, hkv, d, cu):
-    T = lean_tile(d)
+def _units(batch, hkv, d, cu, T=None):
+    T = lean_tile(d) if T is None else T
+    if T <= 0:
+        raise ValueError("tile size must be positive")
     tiles = []
     for b in range(batch):
         L = cu[b + 1] - cu[b]
@@ -106,11 +108,11 @@ def _segments_from_owner(owner, unit_iter, G, kind_rule):
     return segs, cta_seg, unit_host, unit_fin
 
 
-def plan_lean(batch, hq, hkv, d, cu, G):
-    """Stream-K schedule over G CTAs."""
+def plan_lean(batch, hq, hkv, d, cu, G, T=None):
+    """Stream-K schedule over G CTAs (T: LeanTile tokens, default from the table)."""
     if hq % hkv != 0 or G <= 0:
         raise ValueError("bad shape")
-    T, tiles = _units(batch, hkv, d, cu)
+    T, tiles = _units(batch, hkv, d, cu, T)
     unit_iter = [0]
     for n in tiles:
         unit_iter.append(unit_iter[-1] + n)
@@ -132,7 +134,7 @@ def plan_lean(batch, hq, hkv, d, cu, G):
                 unit_fin=unit_fin)
 
 
-def plan_fixed(batch, hq, hkv, d, cu, splits):
+def plan_fixed(batch, hq, hkv, d, cu, splits, T=None):
     """Fixed partition: every unit cut into min(splits, tiles) even pieces, one CTA each.
 
     splits == 1 is the FlashAttention-2 decode partition (one CTA per unit);
@@ -141,7 +143,7 @@ def plan_fixed(batch, hq, hkv, d, cu, splits):
     """
     if hq % hkv != 0 or splits <= 0:
         raise ValueError("bad shape")
-    T, tiles = _units(batch, hkv, d, cu)
+    T, tiles = _units(batch, hkv, d, cu, T)
     unit_iter = [0]
     for n in tiles:
         unit_iter.append(unit_iter[-1] + n)

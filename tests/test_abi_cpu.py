@@ -75,7 +75,7 @@ def test_fixed_planner_matches_reference(splits):
     ((1, 6, 4, 64, [0, 10], 4), la.LA_ERR_INVALID),             # hq not a multiple of hkv
     ((2, 4, 4, 64, [0, 10, 10], 4), la.LA_ERR_INVALID),         # empty context
     ((1, 4, 4, 64, [1, 10], 4), la.LA_ERR_INVALID),             # cu[0] != 0
-    ((1, 4, 4, 96, [0, 10], 4), la.LA_ERR_UNSUPPORTED),         # no LeanTile for d = 96
+    ((1, 4, 4, 112, [0, 10], 4), la.LA_ERR_UNSUPPORTED),        # head dim not built
     ((1, 64, 4, 64, [0, 10], 4), la.LA_ERR_UNSUPPORTED),        # group of 16 not built
 ])
 def test_plan_rejects_bad_shapes(args, status):
@@ -161,3 +161,35 @@ def test_auto_plan_time_model_is_even_when_units_fill_the_gpu():
     # 2048 one-tile units on 152 SMs: the partitions stream the same bytes at full rate
     s, kind, pred = la.la_plan_auto(64, 32, 32, 128, cu_of([128] * 64), 152)
     assert abs(pred[0] - pred[1]) / pred[1] < 0.05
+
+
+@pytest.mark.parametrize("d", la.HEAD_DIMS)
+def test_planner_parity_for_every_head_dim_and_tile_size(d):
+    r = np.random.default_rng(d)
+    for T in la.TILE_SIZES[d]:
+        for _ in range(6):
+            batch = int(r.integers(1, 5))
+            hkv = int(r.integers(1, 4))
+            grp = int(r.choice([1, 2, 4, 8]))
+            lengths = r.integers(1, 3000, size=batch).tolist()
+            G = int(r.integers(1, 160))
+            s = la.la_plan(batch, hkv * grp, hkv, d, cu_of(lengths), G, tile_tokens=T)
+            assert la.la_schedule_export(s)[4] == T
+            assert la.la_schedule_export(s) == P.export(P.plan_lean(batch, hkv * grp, hkv, d, cu_of(lengths), G, T))
+    # the default tile of every head dim
+    s = la.la_plan(1, 2, 2, d, [0, 1000], 7)
+    assert la.la_schedule_export(s)[4] == la.TILE_SIZES[d][0]
+
+
+@pytest.mark.parametrize("d,T", [(64, 64), (64, 512), (128, 256), (80, 64), (256, 128), (96, 256)])
+def test_tile_sizes_that_are_not_built_are_rejected(d, T):
+    with pytest.raises(la.LeanAttentionError) as e:
+        la.la_plan(1, 2, 2, d, [0, 1000], 7, tile_tokens=T)
+    assert e.value.status == la.LA_ERR_UNSUPPORTED
+
+
+def test_decode_ex_rejects_an_unknown_output_type():
+    s = la.la_plan(1, 4, 4, 64, [0, 1024], 3)
+    p = ctypes.c_void_p(0x10000)
+    assert la._lib.la_decode_ex(p, p, p, 0, p, s.handle, ctypes.c_void_p(0x20000), p, 7, 0.125, None) \
+        == la.LA_ERR_INVALID

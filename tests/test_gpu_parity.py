@@ -156,3 +156,69 @@ def test_auto_selected_schedule_matches_the_oracle(name):
     la.la_decode(q, k, v, torch.as_tensor(w.cu, device="cuda"), s, ws, out, w.scale)
     assert la.la_get_status(ws) == la.LA_OK
     compare(out.cpu(), reference(w, q, k, v))
+
+
+# ---- head dims beyond the LeanTile table, tile sizes, 16-bit outputs
+NEW_DIMS = [(d, grp, dt) for d in (80, 96, 256) for grp in (1, 2, 4, 8) for dt in ("f16", "bf16")]
+
+
+@pytest.mark.parametrize("d,grp,dt", NEW_DIMS)
+@pytest.mark.parametrize("grid", [3, 0])
+def test_more_head_dims_ragged_tails(d, grp, dt, grid):
+    lengths = [1, 63, 65, 1000, 128, 129]
+    hkv = 2
+    w = workloads.custom(len(lengths), hkv * grp, hkv, d, dt, lengths)
+    q, k, v, _ = workloads.make_inputs(w, seed=d * 3 + grp, device="cuda")
+    out, _ = run_lean(w, q, k, v, num_sms=grid)
+    compare(out.cpu(), reference(w, q, k, v))
+
+
+@pytest.mark.parametrize("d,T", [(64, 128), (128, 64)])
+@pytest.mark.parametrize("grp", [1, 2, 4, 8])
+def test_alternative_tile_sizes(d, T, grp):
+    lengths = [5000, 1, 200, 3000]
+    w = workloads.custom(len(lengths), 2 * grp, 2, d, "bf16", lengths)
+    q, k, v, _ = workloads.make_inputs(w, seed=T + grp, device="cuda")
+    dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, w.cu, num_sms=0, tile_tokens=T)
+    assert la.la_schedule_export(dec.sched)[4] == T
+    out = dec(q, k, v, w.scale)
+    assert dec.status() == la.LA_OK
+    compare(out.cpu(), reference(w, q, k, v))
+
+
+@pytest.mark.parametrize("out_dt", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("d,grp", [(128, 1), (64, 8), (96, 4)])
+def test_16_bit_outputs_are_the_fp32_result_rounded(out_dt, d, grp):
+    w = workloads.custom(3, 2 * grp, 2, d, "bf16", [3000, 17, 9000])
+    q, k, v, _ = workloads.make_inputs(w, seed=21, device="cuda")
+    dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, w.cu)
+    out32 = dec(q, k, v, w.scale)
+    out16 = torch.empty(w.batch, w.hq, w.d, dtype=out_dt, device="cuda")
+    dec(q, k, v, w.scale, out=out16)
+    assert dec.status() == la.LA_OK
+    assert torch.equal(out16, out32.to(out_dt))  # round to nearest even of the same fp32 values
+    ref = reference(w, q, k, v)
+    got = out16.double().cpu().numpy().reshape(ref.shape)
+    mant = 10 if out_dt == torch.float16 else 7
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - mant)
+    assert np.all(np.abs(got - ref) <= 2e-3 + ulp)
+
+
+@pytest.mark.parametrize("splits", [1, 4])
+def test_fixed_split_with_16_bit_output(splits):
+    w = workloads.custom(2, 8, 8, 80, "f16", [2000, 700])
+    q, k, v, _ = workloads.make_inputs(w, seed=23, device="cuda")
+    dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, w.cu, fixed_splits=splits)
+    out32 = dec(q, k, v, w.scale)
+    out16 = torch.empty(w.batch, w.hq, w.d, dtype=torch.bfloat16, device="cuda")
+    dec(q, k, v, w.scale, out=out16)
+    assert torch.equal(out16, out32.to(torch.bfloat16))
+    compare(out32.cpu(), reference(w, q, k, v))
+
+
+@pytest.mark.parametrize("name", ["hd80", "hd96", "hd256", "hd128gqa"])
+def test_head_dim_workloads_full_output(name):
+    w = workloads.named(name)
+    q, k, v, _ = workloads.make_inputs(w, seed=0, device="cuda")
+    out, _ = run_lean(w, q, k, v)
+    compare(out.cpu(), reference(w, q, k, v))

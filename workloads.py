@@ -94,10 +94,19 @@ def named(name, seed=0):
         return Workload(name, 8, 64, 8, 64, "bf16", lens, outlier_frac=0.01,
                         description="GQA small-head: batch 8, 64 query over 8 kv heads, d 64, "
                                     "ctx uniform in [16384, 65536], bf16, 1% of keys x8")
+    if name in ("hd80", "hd96", "hd256"):
+        d = int(name[2:])
+        heads = 16 if d == 256 else 32
+        return Workload(name, 4, heads, heads, d, "bf16", [32768] * 4,
+                        description=f"head dim {d}: batch 4, {heads}/{heads} heads, d {d}, ctx 32768, bf16")
+    if name == "hd128gqa":
+        return Workload(name, 4, 32, 4, 128, "bf16", [32768] * 4,
+                        description="GQA d 128: batch 4, 32 query over 4 kv heads, d 128, ctx 32768, bf16")
     raise KeyError(name)
 
 
 NAMES = ["tiny", "uniform", "long64k", "long256k", "long512k", "ragged", "gqa"]
+EXTRA_NAMES = ["hd80", "hd96", "hd256", "hd128gqa"]
 
 
 def make_inputs(w, seed=0, device="cpu"):
