@@ -787,55 +787,61 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
     } else {
       bool fail = poisoned;
       if (kind == kHost) {
-        volatile int* bcast = abort_flag + 1;
-        for (int g2 = g + 1; g2 <= peer; ++g2) {
-          if (tid == 0) {
-            bool got = false;
-            const uint64_t tstart_all = global_ns();
-            if (!*abort_flag) {
-              const uint64_t tstart = tstart_all;
-              for (uint32_t it = 0;; ++it) {
-                if (ld_acquire_gpu(&p.flags[g2]) == ready) {
-                  got = true;
-                  break;
-                }
-                if (*abort_flag) break;
-                if ((it & 15u) == 15u) {
-                  if ((long long)(global_ns() - tstart) > p.spin_ns) {
-                    record_error(p.hdr, kStatusTimeout, g, g2);
-                    *abort_flag = 1;
-                    break;
-                  }
-                  __nanosleep(100);
-                }
+        // Wait for every later CTA of the unit at once: consumer thread i
+        // spins (bounded) on the ready flags of peers i, i + NCT, ...
+        const int npeer = peer - g;
+        const uint64_t twait = global_ns();
+        for (int i = tid; i < npeer; i += C::NCT) {
+          const int g2 = g + 1 + i;
+          const uint64_t tstart = global_ns();
+          for (uint32_t it = 0; !*abort_flag; ++it) {
+            if (ld_acquire_gpu(&p.flags[g2]) == ready) break;
+            if ((it & 15u) == 15u) {
+              if ((long long)(global_ns() - tstart) > p.spin_ns) {
+                record_error(p.hdr, kStatusTimeout, g, g2);
+                *abort_flag = 1;
+                break;
               }
+              __nanosleep(100);
             }
-            *bcast = got ? 1 : 0;
-            if (p.trace != nullptr && !*abort_flag)
-              p.trace[(size_t)g * kTraceWords + kTrWaitNs] += global_ns() - tstart_all;
           }
-          consumer_sync(C::NCT);
-          const bool got = *bcast != 0;
-          consumer_sync(C::NCT);  // everyone has read bcast before thread 0 rewrites it
-          if (!got) {
-            fail = true;
-            break;
-          }
-          const float* rec = p.recs + (size_t)g2 * GRP * C::REC;
+        }
+        consumer_sync(C::NCT);  // every flag seen (or the abort raised) before any record is read
+        if (p.trace != nullptr && tid == 0)
+          p.trace[(size_t)g * kTraceWords + kTrWaitNs] += global_ns() - twait;
+        if (*abort_flag) {
+          fail = true;
+        } else {
+          // merge the peers' partials with f, loading four records at a time
 #pragma unroll
           for (int i = 0; i < C::ITEMS; ++i) {
             const int idx = tid + i * C::NCT;
-            if (idx < GRP * D) {
-              const int j = idx / D, cc = idx % D;
-              const float* r = rec + j * C::REC;
-              const float m2 = __ldcg(r), l2 = __ldcg(r + 1), o2 = __ldcg(r + 2 + cc);
-              const float mn = fmaxf(M[i], m2);
-              if (mn == -INFINITY) continue;
-              const float a = (M[i] == -INFINITY) ? 0.f : ex2(M[i] - mn);
-              const float bw = (m2 == -INFINITY) ? 0.f : ex2(m2 - mn);
-              Lsum[i] = a * Lsum[i] + bw * l2;
-              O[i] = a * O[i] + bw * o2;
-              M[i] = mn;  // a NaN m2 (poisoned partial) propagates through bw
+            if (idx >= GRP * D) continue;
+            const int j = idx / D, cc = idx % D;
+            for (int p0 = 0; p0 < npeer; p0 += 4) {
+              float m2[4], l2[4], o2[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                m2[u] = -INFINITY;
+                l2[u] = 0.f;
+                o2[u] = 0.f;
+                if (p0 + u < npeer) {
+                  const float* r = p.recs + ((size_t)(g + 1 + p0 + u) * GRP + j) * C::REC;
+                  m2[u] = __ldcg(r);
+                  l2[u] = __ldcg(r + 1);
+                  o2[u] = __ldcg(r + 2 + cc);
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float mn = fmaxf(M[i], m2[u]);
+                if (mn == -INFINITY) continue;
+                const float a = (M[i] == -INFINITY) ? 0.f : ex2(M[i] - mn);
+                const float bw = (m2[u] == -INFINITY) ? 0.f : ex2(m2[u] - mn);
+                Lsum[i] = a * Lsum[i] + bw * l2[u];
+                O[i] = a * O[i] + bw * o2[u];
+                M[i] = mn;  // a NaN m2 (poisoned partial) propagates through bw
+              }
             }
           }
         }
@@ -870,7 +876,7 @@ __global__ void __launch_bounds__(Cfg<D, T, GRP>::NTHREADS, 1)
   float* mrg = reinterpret_cast<float*>(smem + C::KV_BYTES);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::KV_BYTES + C::MERGE_BYTES);
   uint64_t* empty = full + C::STAGES;
-  volatile int* flags_smem = reinterpret_cast<volatile int*>(empty + C::STAGES);  // [0] abort, [1] bcast
+  volatile int* flags_smem = reinterpret_cast<volatile int*>(empty + C::STAGES);  // [0] abort, [1] spare
 
   const int tid = threadIdx.x;
   const int g = blockIdx.x;
