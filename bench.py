@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--grid", type=int, default=0, help="stream-K grid; 0 = one CTA per SM")
     ap.add_argument("--tile", type=int, default=0, help="LeanTile tokens; 0 = the head dim's default")
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"])
+    ap.add_argument("--kv-layout", default="slab", choices=["slab", "token_major", "paged"])
+    ap.add_argument("--page-size", type=int, default=64)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -300,8 +302,23 @@ def run_ours(args, rank, world, local_rank):
     use_flush = args.flush or w.kv_bytes() < L2_BYTES * 4
     flush = torch.empty(FLUSH_BYTES if use_flush else 1, dtype=torch.uint8, device=dev)
 
-    def call():
-        dec(q, k, v, w.scale, out=out, stream=stream)
+    if args.kv_layout == "slab":
+        def call():
+            dec(q, k, v, w.scale, out=out, stream=stream)
+    else:
+        if args.kv_layout == "token_major":
+            kc, vc = workloads.to_token_major(w, k, v)
+            table, npages = None, 0
+        else:
+            kc, vc, table, npages = workloads.to_paged(w, k, v, args.page_size, seed=args.seed)
+            table = table.to(dev)
+        del k, v
+        k, v = kc, vc  # the e2e leg copies these caches
+        cu_dev = torch.as_tensor(cu, dtype=torch.int32, device=dev)
+
+        def call():
+            la.la_decode_kv(q, kc, vc, cu_dev, dec.sched, dec.workspace, out, w.scale, layout=args.kv_layout,
+                            block_table=table, page_size=args.page_size, num_pages=npages, stream=stream)
 
     # warm-up (also uploads the schedule)
     for _ in range(max(3, args.warmup)):
@@ -408,6 +425,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.description, "kernel": args.kernel, "schedule": dec.kind,
                    "tile_tokens": la.la_schedule_export(dec.sched)[4], "out_dtype": args.out_dtype,
+                   "kv_layout": args.kv_layout + (f" (page {args.page_size})" if args.kv_layout == "paged" else ""),
                    "predicted_us": dec.predicted_us, "grid": G,
                    "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
                    "total_context_tokens": w.total_tokens, "kv_bytes": kv_bytes,

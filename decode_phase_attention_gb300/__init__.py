@@ -21,7 +21,14 @@ LA_OUT_F32, LA_OUT_F16, LA_OUT_BF16 = 0, 1, 2
 HEAD_DIMS = (64, 80, 96, 128, 256)
 TILE_SIZES = {64: (256, 128), 80: (128,), 96: (128,), 128: (128, 64), 256: (64,)}  # first = default
 SEG_WHOLE, SEG_NONHOST, SEG_HOST, SEG_PARTIAL = range(4)
-EXPORTED = ["la_plan", "la_plan_ex", "la_plan_fixed", "la_plan_auto", "la_decode_ex", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
+KV_SLAB, KV_TOKEN_MAJOR, KV_PAGED = range(3)
+
+
+class KvDesc(ctypes.Structure):
+    """la_kv_desc: layout of the K/V caches."""
+    _fields_ = [("layout", ctypes.c_int), ("block_table", ctypes.c_void_p), ("max_blocks", ctypes.c_int),
+                ("page_size", ctypes.c_int), ("num_pages", ctypes.c_longlong)]
+EXPORTED = ["la_plan", "la_plan_ex", "la_plan_fixed", "la_plan_auto", "la_decode_ex", "la_decode_kv", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
             "la_decode", "la_decode_static", "la_get_status", "la_schedule_export_size", "la_schedule_export",
             "la_schedule_set_debug", "la_schedule_set_trace", "la_device_capacity", "la_schedule_destroy",
             "la_status_string"]
@@ -44,6 +51,7 @@ def _load():
         "la_plan": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
         "la_plan_ex": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, c_int, pp]),
         "la_decode_ex": (c_int, [vp, vp, vp, c_int, vp, vp, vp, vp, c_int, c_float, vp]),
+        "la_decode_kv": (c_int, [vp, vp, vp, c_int, vp, ctypes.POINTER(KvDesc), vp, vp, vp, c_int, c_float, vp]),
         "la_plan_fixed": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
         "la_plan_auto": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp, ctypes.POINTER(ctypes.c_double)]),
         "la_schedule_grid": (c_int, [vp]),
@@ -283,6 +291,48 @@ def la_decode_static(q, k, v, cu_seqlens_k, sched, out, scale, stream=None):
                                  ctypes.c_void_p(cu_seqlens_k.data_ptr()), sched.handle,
                                  ctypes.c_void_p(out.data_ptr()), float(scale),
                                  _stream_handle(stream)), "la_decode_static")
+    return out
+
+
+def la_decode_kv(q, k_cache, v_cache, cu_seqlens_k, sched, workspace, out, scale, layout="token_major",
+                 block_table=None, page_size=0, num_pages=0, stream=None):
+    """Decode attention over a token-major ([tokens, hkv, d]) or paged
+    ([pages, page_size, hkv, d] + block table) K/V cache."""
+    import torch
+    code = {"slab": KV_SLAB, "token_major": KV_TOKEN_MAJOR, "paged": KV_PAGED}[layout]
+    if not (q.is_cuda and k_cache.is_cuda and v_cache.is_cuda and out.is_cuda and cu_seqlens_k.is_cuda
+            and workspace.is_cuda):
+        raise ValueError("la_decode_kv takes device tensors")
+    dt = {torch.float16: LA_F16, torch.bfloat16: LA_BF16}.get(q.dtype)
+    if dt is None or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise ValueError("q and the caches must share one dtype, float16 or bfloat16")
+    out_dt = {torch.float32: LA_OUT_F32, torch.float16: LA_OUT_F16, torch.bfloat16: LA_OUT_BF16}.get(out.dtype)
+    if out_dt is None or cu_seqlens_k.dtype != torch.int32:
+        raise ValueError("out must be float32, float16 or bfloat16 and cu_seqlens_k int32")
+    b, hq, hkv, d = sched.batch, sched.hq, sched.hkv, sched.d
+    if q.numel() != b * hq * d or out.numel() != b * hq * d or cu_seqlens_k.numel() != b + 1:
+        raise ValueError("q / out / cu_seqlens_k do not match the schedule")
+    desc = KvDesc(code, None, 0, 0, 0)
+    if code == KV_PAGED:
+        if block_table is None or not block_table.is_cuda or block_table.dtype != torch.int32 \
+                or block_table.dim() != 2 or block_table.shape[0] != b or not block_table.is_contiguous():
+            raise ValueError("paged layout needs a contiguous int32 device block table [batch, max_blocks]")
+        need = int(num_pages) * int(page_size) * hkv * d
+        desc = KvDesc(code, block_table.data_ptr(), block_table.shape[1], int(page_size), int(num_pages))
+    else:
+        need = int(sched.cu[-1]) * hkv * d
+    if k_cache.numel() < need or v_cache.numel() < need:
+        raise ValueError("caches are smaller than the layout implies")
+    for t in (q, k_cache, v_cache, out, cu_seqlens_k):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if workspace.numel() * workspace.element_size() < la_workspace_size(sched):
+        raise ValueError("workspace smaller than la_workspace_size")
+    _check(_lib.la_decode_kv(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_cache.data_ptr()),
+                             ctypes.c_void_p(v_cache.data_ptr()), dt, ctypes.c_void_p(cu_seqlens_k.data_ptr()),
+                             ctypes.byref(desc), sched.handle, ctypes.c_void_p(workspace.data_ptr()),
+                             ctypes.c_void_p(out.data_ptr()), out_dt, float(scale), _stream_handle(stream)),
+           "la_decode_kv")
     return out
 
 

@@ -151,6 +151,10 @@ void build_dev_segs(la_schedule* s) {
     dv[5] = (int32_t)L;
     dv[6] = (int32_t)(uint32_t)(row0 & 0xffffffffLL);
     dv[7] = (int32_t)(row0 >> 32);
+    dv[8] = s->cu[b];
+    dv[9] = b;
+    dv[10] = kvh;
+    dv[11] = 0;
   }
 }
 
@@ -404,6 +408,35 @@ cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, 
   return cudaSuccess;
 }
 
+cudaError_t encode_kv_maps_3d(const void* k, const void* v, long long rows, int hkv, int d, int bw, int box_rows,
+                              bool swizzle, int elem_type, CUtensorMap* mk, CUtensorMap* mv) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || ptr == nullptr)
+    return cudaErrorNotSupported;
+  Encode fn = reinterpret_cast<Encode>(ptr);
+  if (rows <= 0 || rows > (1LL << 31) - 1) return cudaErrorInvalidValue;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hkv * d * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)bw, 1, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swizzle)
+    swz = bw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : (bw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+  for (int i = 0; i < 2; ++i) {
+    CUresult r = fn(i == 0 ? mk : mv, (CUtensorMapDataType)elem_type, 3, const_cast<void*>(i == 0 ? k : v), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace la
 
 extern "C" {
@@ -493,11 +526,43 @@ la_status la_workspace_init(void* workspace, size_t bytes, la_stream_t stream) {
   return cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
-la_status la_decode_ex(const void* q, const void* k, const void* v, la_dtype dt, const int32_t* cu_seqlens_k_dev,
-                       const la_schedule* sc, void* workspace, void* out, la_dtype_out out_dt, float scale,
-                       la_stream_t stream) {
+la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt, const int32_t* cu_seqlens_k_dev,
+                       const la_kv_desc* kv, const la_schedule* sc, void* workspace, void* out,
+                       la_dtype_out out_dt, float scale, la_stream_t stream) {
   if (out_dt != LA_OUT_F32 && out_dt != LA_OUT_F16 && out_dt != LA_OUT_BF16) return LA_ERR_INVALID;
   const int out_dtype = (int)out_dt;
+  if (kv == nullptr || sc == nullptr) return LA_ERR_INVALID;
+  int kv_layout = la::kKvSlab, box_rows = 0, page_size = 0, bt_stride = 0;
+  long long kv_rows = 0;
+  if (kv->layout == LA_KV_TOKEN_MAJOR) {
+    kv_layout = la::kKvTokenMajor;
+    box_rows = sc->T;
+    kv_rows = sc->cu[sc->batch];
+  } else if (kv->layout == LA_KV_PAGED) {
+    kv_layout = la::kKvPaged;
+    page_size = kv->page_size;
+    if (page_size < 16 || (page_size & (page_size - 1)) != 0 || kv->block_table == nullptr ||
+        kv->num_pages <= 0 || !aligned(kv->block_table, 4))
+      return LA_ERR_INVALID;
+    if (kv->num_pages * (long long)page_size > (1LL << 31) - 1) return LA_ERR_UNSUPPORTED;
+    int64_t need = 0;  // block-table entries the longest request uses
+    for (int b = 0; b < sc->batch; ++b)
+      need = std::max<int64_t>(need, ((int64_t)sc->cu[b + 1] - sc->cu[b] + page_size - 1) / page_size);
+    if (kv->max_blocks < need) return LA_ERR_INVALID;
+    bt_stride = kv->max_blocks;
+    box_rows = std::min(sc->T, page_size);
+    kv_rows = kv->num_pages * (long long)page_size;
+  } else if (kv->layout != LA_KV_SLAB) {
+    return LA_ERR_INVALID;
+  }
+  if (kv_layout != la::kKvSlab) {
+    // TMA destinations: 1024-byte aligned pieces when swizzled (tensor-core
+    // path), 128-byte aligned rows otherwise.
+    const bool tc = sc->grp >= 4;
+    const int w = sc->d % 64 == 0 ? 64 : (sc->d % 32 == 0 ? 32 : 16);
+    const long long piece = tc ? (long long)box_rows * w * 2 : (long long)box_rows * sc->d * 2;
+    if (piece % (tc ? 1024 : 128) != 0) return LA_ERR_UNSUPPORTED;
+  }
   if (sc == nullptr || q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
       cu_seqlens_k_dev == nullptr)
     return LA_ERR_INVALID;
@@ -542,6 +607,14 @@ la_status la_decode_ex(const void* q, const void* k, const void* v, la_dtype dt,
   p.skip_signal = s->skip_signal;
   p.trace = s->trace;
   p.out_dtype = out_dtype;
+  p.kv_layout = kv_layout;
+  if (kv_layout != la::kKvSlab) {
+    p.kv_rows = kv_rows;
+    p.box_rows = box_rows;
+    p.page_size = page_size;
+    p.bt_stride = bt_stride;
+    p.block_table = kv->block_table;
+  }
   cudaStream_t st = (cudaStream_t)stream;
   const int dtype = dt == LA_BF16 ? 1 : 0;
   cudaError_t ce = la::launch_decode(s->d, s->T, s->grp, dtype, p, st);
@@ -560,6 +633,13 @@ la_status la_decode_ex(const void* q, const void* k, const void* v, la_dtype dt,
     if (ce != cudaSuccess) return LA_ERR_CUDA;
   }
   return LA_OK;
+}
+
+la_status la_decode_ex(const void* q, const void* k, const void* v, la_dtype dt, const int32_t* cu_seqlens_k_dev,
+                       const la_schedule* s, void* workspace, void* out, la_dtype_out out_dt, float scale,
+                       la_stream_t stream) {
+  const la_kv_desc slab = {LA_KV_SLAB, nullptr, 0, 0, 0};
+  return la_decode_kv(q, k, v, dt, cu_seqlens_k_dev, &slab, s, workspace, out, out_dt, scale, stream);
 }
 
 la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt, const int32_t* cu_seqlens_k_dev,

@@ -16,7 +16,15 @@ enum SegKind : int32_t { kWhole = 0, kNonHost = 1, kHost = 2, kPartial = 3 };
 // the request's context length and the slab's first K/V row (64-bit), so the
 // producer can issue its first copy after two dependent loads.
 constexpr int kSegWords = 5;
-constexpr int kDevSegWords = 8;  // unit, t0, t1, kind, peer, L, row0 low, row0 high
+// unit, t0, t1, kind, peer, L, row0 low, row0 high, cu[b], b, kv head, 0
+constexpr int kDevSegWords = 12;
+
+// Where the K/V rows of a (request, kv head, token) live.
+enum KvLayout : int {
+  kKvSlab = 0,        // request b: [hkv, L_b, d] slab at row hkv*cu[b] (1-D bulk copies / 2-D TMA)
+  kKvTokenMajor = 1,  // [total tokens, hkv, d], token t of request b at row cu[b] + t (3-D TMA)
+  kKvPaged = 2        // [pages, page_size, hkv, d] with a block table per request (3-D TMA)
+};
 
 // Workspace: a 256-byte header, G ready flags (padded to 256 bytes), then G
 // partial records of grp * (d + 2) floats: per query head [m, l, O[d]].
@@ -52,6 +60,11 @@ struct KParams {
   int skip_signal;          // test hook: this CTA never sets its flag (-1: none)
   unsigned long long* trace;  // optional per-CTA timeline (kTraceWords each), or null
   int out_dtype = 0;          // 0 fp32, 1 fp16, 2 bf16
+  int kv_layout = kKvSlab;
+  const int32_t* block_table = nullptr;  // paged: [batch, bt_stride] page ids
+  int bt_stride = 0;
+  int page_size = 0;                     // paged: tokens per page
+  int box_rows = 0;                      // 3-D TMA: token rows per load (T, or the page size if smaller)
 };
 
 // Per-CTA trace record (globaltimer ns): written when KParams::trace is set.

@@ -108,6 +108,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tmap, 
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// 3-D tiled TMA load of box (x, y, z) of tensor map `tmap` into shared memory.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tmap, int x, int y, int z, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -246,7 +255,7 @@ struct Cfg {
   static constexpr int REC = D + 2;                 // [m, l, O[d]]
   static constexpr size_t MERGE_BYTES = (size_t)NCW * GRP * REC * 4;
   static constexpr size_t BAR_BYTES = 2 * STAGES * 8 + 16;
-  static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES + (TC ? 1024 : 0);
+  static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
   static constexpr int ITEMS = (GRP * D + NCT - 1) / NCT;  // (head, dim) outputs per consumer thread
   static_assert(D % 16 == 0 && T % 16 == 0, "tile shape");
   static_assert(STEPS % CH == 0 && TPW % TPS == 0, "CUDA-core tile shape");
@@ -297,9 +306,16 @@ __device__ __forceinline__ bool unit_offsets_ok(const KParams& p, int b) {
 template <int D, int T, int GRP, typename E>
 __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, int g,
                                         E* kv, uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
+  // Run by the whole producer warp. Lane 0 posts byte counts and issues the
+  // slab-layout copies; for token-major and paged caches lane i issues the
+  // load of the i-th piece of a tile (a tile spans up to T / 16 pages), so
+  // small pages do not serialise on one thread.
   using C = Cfg<D, T, GRP>;
+  const int lane = threadIdx.x & 31;
+  const bool leader = lane == 0;
   const uint64_t pol = l2_evict_first_policy();
-  if (C::TC) {
+  const bool tma3 = p.kv_layout != kKvSlab;
+  if (leader && (C::TC || tma3)) {
     prefetch_tmap(tmk);
     prefetch_tmap(tmv);
   }
@@ -313,36 +329,76 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
     // schedule was planned for, whatever the caller's device offsets hold
     const int4 w0 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords);
     const int4 w1 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 4);
+    const int4 w2 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 8);
     const int t0 = w0.y, t1 = w0.z;
     const long long L = w1.y;
     const long long row0 = (long long)(((unsigned long long)(unsigned)w1.w << 32) | (unsigned)w1.z);
+    const int cu_b = w2.x, b = w2.y, kvh = w2.z;
     for (int t = t0; t < t1; ++t) {
       const long long rem = L - (long long)t * C::T;
       const int ntok = rem < C::T ? (int)rem : C::T;
-      if (!mbar_wait_bounded(&empty[stage], phase, abort_flag, p.spin_ns)) {
-        record_error(p.hdr, kStatusTimeout, g, -1);
-        *abort_flag = 1;
+      const int br = tma3 ? p.box_rows : C::T;
+      const int nload = (ntok + br - 1) / br;  // pieces that start inside the context
+      // this lane's piece: its first token row in the cache (read before the
+      // wait, so a page id's latency overlaps it)
+      int row = 0;
+      if (tma3 && lane < nload) {
+        const int tok = t * C::T + lane * br;
+        if (p.kv_layout == kKvTokenMajor) {
+          row = cu_b + tok;
+        } else {
+          const int page = p.block_table[(size_t)b * p.bt_stride + tok / p.page_size];
+          row = page * p.page_size + tok % p.page_size;
+        }
+      }
+      bool free_slot = mbar_wait_bounded(&empty[stage], phase, abort_flag, p.spin_ns);
+      free_slot = __all_sync(kFull, free_slot);
+      if (!free_slot) {
+        if (leader) {
+          record_error(p.hdr, kStatusTimeout, g, -1);
+          *abort_flag = 1;
+        }
         aborted = true;
         break;
       }
       E* ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
-      if (C::TC) {
-        // Whole boxes of T rows: rows past the slab are the next slab's (or
-        // zero fill past the tensor) and are masked by the consumers.
-        mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * C::TILE_ELEMS * 2));
-        const int y = (int)(row0 + (long long)t * C::T);
+      if (tma3) {
+        // Token-major or paged cache, seen as [rows, hkv, d]: box_rows token
+        // rows of one kv head per load; the consumers mask the tail tokens.
+        if (leader) mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * nload * br * D * 2));
+        __syncwarp();
+        if (lane < nload) {
+          if (C::TC) {
 #pragma unroll
-        for (int bk = 0; bk < C::NB; ++bk) {
-          tma_load_2d(ks + bk * C::T * C::W, tmk, bk * C::W, y, &full[stage], pol);
-          tma_load_2d(ks + C::TILE_ELEMS + bk * C::T * C::W, tmv, bk * C::W, y, &full[stage], pol);
+            for (int bk = 0; bk < C::NB; ++bk) {
+              tma_load_3d(ks + bk * C::T * C::W + lane * br * C::W, tmk, bk * C::W, kvh, row, &full[stage], pol);
+              tma_load_3d(ks + C::TILE_ELEMS + bk * C::T * C::W + lane * br * C::W, tmv, bk * C::W, kvh, row,
+                          &full[stage], pol);
+            }
+          } else {
+            tma_load_3d(ks + lane * br * D, tmk, 0, kvh, row, &full[stage], pol);
+            tma_load_3d(ks + C::TILE_ELEMS + lane * br * D, tmv, 0, kvh, row, &full[stage], pol);
+          }
         }
-      } else {
-        const uint32_t bytes = (uint32_t)ntok * D * 2u;
-        mbar_arrive_expect_tx(&full[stage], 2u * bytes);
-        const E* src_k = static_cast<const E*>(p.k) + (row0 + (long long)t * C::T) * D;
-        const E* src_v = static_cast<const E*>(p.v) + (row0 + (long long)t * C::T) * D;
-        bulk_g2s(ks, src_k, bytes, &full[stage], pol);
-        bulk_g2s(ks + C::TILE_ELEMS, src_v, bytes, &full[stage], pol);
+      } else if (leader) {
+        if (C::TC) {
+          // Whole boxes of T rows: rows past the slab are the next slab's (or
+          // zero fill past the tensor) and are masked by the consumers.
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * C::TILE_ELEMS * 2));
+          const int y = (int)(row0 + (long long)t * C::T);
+#pragma unroll
+          for (int bk = 0; bk < C::NB; ++bk) {
+            tma_load_2d(ks + bk * C::T * C::W, tmk, bk * C::W, y, &full[stage], pol);
+            tma_load_2d(ks + C::TILE_ELEMS + bk * C::T * C::W, tmv, bk * C::W, y, &full[stage], pol);
+          }
+        } else {
+          const uint32_t bytes = (uint32_t)ntok * D * 2u;
+          mbar_arrive_expect_tx(&full[stage], 2u * bytes);
+          const E* src_k = static_cast<const E*>(p.k) + (row0 + (long long)t * C::T) * D;
+          const E* src_v = static_cast<const E*>(p.v) + (row0 + (long long)t * C::T) * D;
+          bulk_g2s(ks, src_k, bytes, &full[stage], pol);
+          bulk_g2s(ks + C::TILE_ELEMS, src_v, bytes, &full[stage], pol);
+        }
       }
       ++issued;
       if (++stage == C::STAGES) {
@@ -351,7 +407,7 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
       }
     }
   }
-  if (aborted) {
+  if (aborted && leader) {
     // Do not leave the CTA while copies into its shared memory are in flight:
     // wait (bounded) for the latest fill of every stage that was used.
     for (int s = 0; s < C::STAGES; ++s) {
@@ -362,6 +418,7 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
       mbar_wait_bounded(&full[s], parity, &no_abort, p.spin_ns);
     }
   }
+  __syncwarp();
 }
 
 // Wait for the next stage; false (for the whole warp) if it never came.
@@ -637,6 +694,21 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
         o[dm][2] *= alpha[0];
         o[dm][3] *= alpha[1];
       }
+      // Rows past the context may hold anything (another request's tokens,
+      // an unused page slot): their P is zero, but 0 * NaN is not, so the
+      // warp clears its own V rows there before the P.V product.
+      if (ntok < C::T && wtok + C::TPW > ntok) {
+        constexpr int CHUNKS = C::RB / 16;  // 16-byte chunks per row and box
+        for (int idx = lane; idx < C::TPW * C::NB * CHUNKS; idx += 32) {
+          const int row = wtok + idx / (C::NB * CHUNKS);
+          const int rest = idx % (C::NB * CHUNKS);
+          if (row >= ntok) {
+            const uint32_t a = vb + (uint32_t)((rest / CHUNKS) * C::T * C::RB + row * C::RB + (rest % CHUNKS) * 16);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+          }
+        }
+        __syncwarp();
+      }
       // P = 2^(s - m), split into high and low 16-bit parts; O^T += V^T P
 #pragma unroll
       for (int mt = 0; mt < C::MT; ++mt) {
@@ -868,10 +940,9 @@ __global__ void __launch_bounds__(Cfg<D, T, GRP>::NTHREADS, 1)
                        const __grid_constant__ CUtensorMap tmv) {
   using C = Cfg<D, T, GRP>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // the 128-byte swizzle of TMA tiles needs 1024-byte aligned destinations
-  unsigned char* smem = C::TC ? reinterpret_cast<unsigned char*>(
-                                    (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))
-                              : smem_raw;
+  // swizzled TMA tiles need 1024-byte aligned destinations, plain ones 128
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   E* kv = reinterpret_cast<E*>(smem);
   float* mrg = reinterpret_cast<float*>(smem + C::KV_BYTES);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::KV_BYTES + C::MERGE_BYTES);
@@ -901,8 +972,7 @@ __global__ void __launch_bounds__(Cfg<D, T, GRP>::NTHREADS, 1)
   const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr[kEpoch]);
 
   if ((tid >> 5) == C::NCW) {
-    if ((tid & 31) == 0) produce<D, T, GRP, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
-    __syncwarp();
+    produce<D, T, GRP, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
   } else {
     consume<D, T, GRP, E>(p, g, kv, full, empty, mrg, flags_smem, epoch);
   }
@@ -952,6 +1022,11 @@ __global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
 // boxes of W columns x T rows, swizzled over W * 2 bytes (32, 64 or 128).
 cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, int T, int W, int elem_type,
                            CUtensorMap* mk, CUtensorMap* mv);
+// Tensor maps of a token-major or paged cache seen as [rows, hkv, d]: boxes
+// of bw columns x 1 head x box_rows rows; swizzled over bw * 2 bytes when
+// swizzle is set (tensor-core path), plain rows otherwise.
+cudaError_t encode_kv_maps_3d(const void* k, const void* v, long long rows, int hkv, int d, int bw, int box_rows,
+                              bool swizzle, int elem_type, CUtensorMap* mk, CUtensorMap* mv);
 
 template <int D, int T, int GRP, typename E>
 cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
@@ -968,7 +1043,11 @@ cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
   }
   if (p.G <= 0) return cudaSuccess;
   CUtensorMap mk, mv;
-  if (C::TC) {
+  if (p.kv_layout != kKvSlab) {
+    e = encode_kv_maps_3d(p.k, p.v, p.kv_rows, p.hkv, D, C::TC ? C::W : D, p.box_rows, C::TC,
+                          (int)Elem<E>::kTmaType, &mk, &mv);
+    if (e != cudaSuccess) return e;
+  } else if (C::TC) {
     e = encode_kv_maps(p.k, p.v, p.kv_rows, D, C::T, C::W, (int)Elem<E>::kTmaType, &mk, &mv);
     if (e != cudaSuccess) return e;
   } else {

@@ -203,6 +203,43 @@ la_status la_decode_ex(const void* q, const void* k, const void* v, la_dtype dt,
                        void* out, la_dtype_out out_dt, float scale, la_stream_t stream);
 
 /*
+ * K/V cache layouts for la_decode_kv (the review's "7.4 limitations" notes
+ * that the method asks for a [batch, heads, seq_len, head_dim] layout;
+ * serving stacks keep a token-major or paged cache instead).
+ *   LA_KV_SLAB         request b is a [hkv, L_b, d] slab at element
+ *                      hkv*cu[b]*d (the layout of la_decode)
+ *   LA_KV_TOKEN_MAJOR  [total tokens, hkv, d]: token t of request b, kv
+ *                      head h at element ((cu[b] + t)*hkv + h)*d
+ *   LA_KV_PAGED        [num_pages, page_size, hkv, d]: token t of request b
+ *                      sits in page block_table[b*max_blocks + t/page_size]
+ *                      at slot t % page_size
+ * Both non-slab layouts are read with 3-D TMA loads; page ids outside
+ * [0, num_pages) read as zeros, never out of bounds.
+ */
+typedef enum { LA_KV_SLAB = 0, LA_KV_TOKEN_MAJOR = 1, LA_KV_PAGED = 2 } la_kv_layout;
+
+typedef struct {
+  la_kv_layout layout;
+  const int32_t* block_table; /* paged: DEVICE int32 [batch, max_blocks] page ids */
+  int max_blocks;             /* paged: row stride of block_table, >= ceil(max L_b / page_size) */
+  int page_size;              /* paged: tokens per page, a power of two >= 16 */
+  long long num_pages;        /* paged: pages in each of the K and V caches */
+} la_kv_desc;
+
+/*
+ * la_decode_kv -- la_decode_ex on a cache in any of the layouts above
+ * (k and v point at the caches; cu_seqlens_k_dev still gives the context
+ * lengths). LA_ERR_INVALID for a bad descriptor (page size not a power of
+ * two >= 16, too few block-table columns, NULL table); LA_ERR_UNSUPPORTED
+ * when a page is too small for the tensor-core path's swizzled pieces
+ * (d = 80 with groups 4/8 needs page_size >= 32) or the cache has more than
+ * 2^31 - 1 token rows.
+ */
+la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
+                       const int32_t* cu_seqlens_k_dev, const la_kv_desc* kv, const la_schedule* s,
+                       void* workspace, void* out, la_dtype_out out_dt, float scale, la_stream_t stream);
+
+/*
  * la_decode_static -- la_decode without a workspace and without any device
  * allocation. The paper has no counterpart: this is a library convenience.
  *

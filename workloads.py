@@ -148,3 +148,53 @@ def make_inputs(w, seed=0, device="cpu"):
 def custom(batch, hq, hkv, d, dtype, lengths, grid=0, name="custom"):
     return Workload(name, batch, hq, hkv, d, dtype, list(lengths), grid=grid,
                     description=f"{name}: batch {batch}, {hq}/{hkv} heads, d {d}, {dtype}")
+
+
+def to_token_major(w, k, v):
+    """Re-lay slab-layout K and V as [total tokens, hkv, d] (same values)."""
+    out = []
+    for x in (k, v):
+        y = x.new_empty(w.total_tokens * w.hkv * w.d)
+        cu = w.cu
+        for b in range(w.batch):
+            L = int(cu[b + 1] - cu[b])
+            slab = x[w.hkv * int(cu[b]) * w.d: w.hkv * int(cu[b + 1]) * w.d].view(w.hkv, L, w.d)
+            y[int(cu[b]) * w.hkv * w.d: int(cu[b + 1]) * w.hkv * w.d] = slab.transpose(0, 1).reshape(-1)
+        out.append(y)
+    return out[0], out[1]
+
+
+def to_paged(w, k, v, page_size, seed=0, spare_pages=3, fill=float("nan")):
+    """Re-lay slab-layout K and V as a paged cache [pages, page_size, hkv, d].
+
+    Pages are handed out in a seeded random order; unused slots of the last
+    page of each request, the spare pages and the unused block-table
+    entries (-1) hold junk (NaN by default) so that reading them shows up.
+    Returns (k_cache, v_cache, block_table [batch, max_blocks] int32, num_pages).
+    """
+    import torch
+
+    cu = w.cu
+    blocks = [-(-int(cu[b + 1] - cu[b]) // page_size) for b in range(w.batch)]
+    num_pages = sum(blocks) + spare_pages
+    max_blocks = max(blocks) + 1
+    rng = np.random.default_rng(_seed(seed, 0xB10C, page_size))
+    perm = rng.permutation(num_pages)
+    table = np.full((w.batch, max_blocks), -1, dtype=np.int32)
+    nxt = 0
+    for b in range(w.batch):
+        for i in range(blocks[b]):
+            table[b, i] = perm[nxt]
+            nxt += 1
+    caches = []
+    for x in (k, v):
+        c = x.new_full((num_pages, page_size, w.hkv, w.d), fill)
+        for b in range(w.batch):
+            L = int(cu[b + 1] - cu[b])
+            slab = x[w.hkv * int(cu[b]) * w.d: w.hkv * int(cu[b + 1]) * w.d].view(w.hkv, L, w.d)
+            tok_major = slab.transpose(0, 1)  # [L, hkv, d]
+            for i in range(blocks[b]):
+                t0, t1 = i * page_size, min(L, (i + 1) * page_size)
+                c[int(table[b, i]), : t1 - t0] = tok_major[t0:t1]
+        caches.append(c.reshape(-1))
+    return caches[0], caches[1], torch.as_tensor(table), num_pages
