@@ -175,12 +175,13 @@ def algorithmic_bytes(w, export, out_bytes=4):
     """Bytes a call must move: K+V once, q, out, and every partial record
     written once and read once (one per non-host or fixed-split piece)."""
     kv = w.kv_bytes()
-    q = w.batch * w.hq * w.d * 2
-    out = w.batch * w.hq * w.d * out_bytes
+    q = w.batch * w.nq * w.hq * w.d * 2
+    out = w.batch * w.nq * w.hq * w.d * out_bytes
     G, U, nseg = export[1], export[2], export[5]
     base = 8 + 2 * (G + 1) + (U + 1)
     pieces = sum(1 for i in range(nseg) if export[base + 5 * i + 3] in (1, 3))
-    rec = (w.hq // w.hkv) * (w.d + 2) * 4
+    rows = (w.hq // w.hkv) * w.nq
+    rec = (1 if rows <= 1 else 2 if rows <= 2 else 4 if rows <= 4 else 8) * (w.d + 2) * 4
     return kv, kv + q + out + 2 * pieces * rec
 
 
@@ -283,7 +284,9 @@ def run_ours(args, rank, world, local_rank):
         plan_times.append((time.perf_counter() - t0) * 1e6)
     plan_us = sorted(plan_times)[len(plan_times) // 2]
     out_torch = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[args.out_dtype]
-    if args.kernel == "lean":
+    if w.nq > 1:
+        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, nq=w.nq)
+    elif args.kernel == "lean":
         dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, tile_tokens=args.tile)
     elif args.kernel == "naive":
         dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, device=dev, fixed_splits=1)
@@ -296,7 +299,7 @@ def run_ours(args, rank, world, local_rank):
     G = dec.sched.grid
     launches_per_call = 2 if (dec.kind == "fixed_split" and dec.sched.grid > w.batch * w.hkv) else 1
     stream = torch.cuda.current_stream(dev)
-    out = torch.empty(w.batch, w.hq, w.d, dtype=out_torch, device=dev)
+    out = torch.empty(*q.shape, dtype=out_torch, device=dev)
     # K+V well above L2 (129 MB) cannot be served from L2 by the next call; smaller
     # inputs get a 256 MiB write between calls to flush L2.
     use_flush = args.flush or w.kv_bytes() < L2_BYTES * 4

@@ -28,7 +28,7 @@ class KvDesc(ctypes.Structure):
     """la_kv_desc: layout of the K/V caches."""
     _fields_ = [("layout", ctypes.c_int), ("block_table", ctypes.c_void_p), ("max_blocks", ctypes.c_int),
                 ("page_size", ctypes.c_int), ("num_pages", ctypes.c_longlong)]
-EXPORTED = ["la_plan", "la_plan_ex", "la_plan_fixed", "la_plan_auto", "la_decode_ex", "la_decode_kv", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
+EXPORTED = ["la_plan", "la_plan_ex", "la_plan_spec", "la_plan_fixed", "la_plan_auto", "la_decode_ex", "la_decode_kv", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
             "la_decode", "la_decode_static", "la_get_status", "la_schedule_export_size", "la_schedule_export",
             "la_schedule_set_debug", "la_schedule_set_trace", "la_device_capacity", "la_schedule_destroy",
             "la_status_string"]
@@ -50,6 +50,7 @@ def _load():
     sig = {
         "la_plan": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
         "la_plan_ex": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, c_int, pp]),
+        "la_plan_spec": (c_int, [c_int, c_int, c_int, c_int, c_int, vp, c_int, pp]),
         "la_decode_ex": (c_int, [vp, vp, vp, c_int, vp, vp, vp, vp, c_int, c_float, vp]),
         "la_decode_kv": (c_int, [vp, vp, vp, c_int, vp, ctypes.POINTER(KvDesc), vp, vp, vp, c_int, c_float, vp]),
         "la_plan_fixed": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
@@ -90,10 +91,11 @@ def _check(status, what):
 class Schedule:
     """Owns an la_schedule; destroyed with the object."""
 
-    def __init__(self, handle, batch, hq, hkv, d, cu):
+    def __init__(self, handle, batch, hq, hkv, d, cu, nq=1):
         self._h = handle
         self.batch, self.hq, self.hkv, self.d = batch, hq, hkv, d
         self.cu = cu
+        self.nq = nq
 
     @property
     def handle(self):
@@ -135,6 +137,18 @@ def la_plan(batch, hq, hkv, d, cu_seqlens_k, num_sms=0, tile_tokens=0):
     else:
         _check(_lib.la_plan(batch, hq, hkv, d, cup, int(num_sms), ctypes.byref(h)), "la_plan")
     return Schedule(h.value, batch, hq, hkv, d, cu)
+
+
+def la_plan_spec(batch, hq, hkv, d, nq, cu_seqlens_k, num_sms=0):
+    """Stream-K schedule for nq query tokens per request (the last nq tokens of each
+    context, causal among themselves); q and out are then [batch, nq, hq, d]."""
+    cu = _cu_array(cu_seqlens_k)
+    if cu.size != batch + 1:
+        raise ValueError("cu_seqlens_k must have batch + 1 entries")
+    h = ctypes.c_void_p()
+    _check(_lib.la_plan_spec(batch, hq, hkv, d, int(nq), cu.ctypes.data_as(ctypes.c_void_p), int(num_sms),
+                             ctypes.byref(h)), "la_plan_spec")
+    return Schedule(h.value, batch, hq, hkv, d, cu, nq=int(nq))
 
 
 def la_plan_fixed(batch, hq, hkv, d, cu_seqlens_k, splits):
@@ -244,8 +258,8 @@ def la_decode(q, k, v, cu_seqlens_k, sched, workspace, out, scale, stream=None):
             raise ValueError(f"{name} must be contiguous")
     b, hq, hkv, d = sched.batch, sched.hq, sched.hkv, sched.d
     kv_elems = int(sched.cu[-1]) * hkv * d
-    if q.numel() != b * hq * d or out.numel() != b * hq * d:
-        raise ValueError("q / out do not match the schedule's [batch, hq, d]")
+    if q.numel() != b * sched.nq * hq * d or out.numel() != b * sched.nq * hq * d:
+        raise ValueError("q / out do not match the schedule's [batch, nq, hq, d]")
     if k.numel() < kv_elems or v.numel() < kv_elems:
         raise ValueError("k / v are smaller than the schedule's contexts")
     if cu_seqlens_k.numel() != b + 1:
@@ -283,7 +297,7 @@ def la_decode_static(q, k, v, cu_seqlens_k, sched, out, scale, stream=None):
     kv_elems = int(sched.cu[-1]) * hkv * d
     if not all(t.is_contiguous() for t in (q, k, v, out, cu_seqlens_k)):
         raise ValueError("tensors must be contiguous")
-    if (q.numel() != b * hq * d or out.numel() != b * hq * d or k.numel() < kv_elems
+    if (q.numel() != b * sched.nq * hq * d or out.numel() != b * sched.nq * hq * d or k.numel() < kv_elems
             or v.numel() < kv_elems or cu_seqlens_k.numel() != b + 1):
         raise ValueError("tensor sizes do not match the schedule")
     _check(_lib.la_decode_static(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
@@ -310,7 +324,8 @@ def la_decode_kv(q, k_cache, v_cache, cu_seqlens_k, sched, workspace, out, scale
     if out_dt is None or cu_seqlens_k.dtype != torch.int32:
         raise ValueError("out must be float32, float16 or bfloat16 and cu_seqlens_k int32")
     b, hq, hkv, d = sched.batch, sched.hq, sched.hkv, sched.d
-    if q.numel() != b * hq * d or out.numel() != b * hq * d or cu_seqlens_k.numel() != b + 1:
+    if q.numel() != b * sched.nq * hq * d or out.numel() != b * sched.nq * hq * d \
+            or cu_seqlens_k.numel() != b + 1:
         raise ValueError("q / out / cu_seqlens_k do not match the schedule")
     desc = KvDesc(code, None, 0, 0, 0)
     if code == KV_PAGED:
@@ -344,11 +359,14 @@ class LeanDecoder:
     """Convenience holder: a schedule, its workspace and the device offsets."""
 
     def __init__(self, batch, hq, hkv, d, cu_seqlens_k, num_sms=0, device="cuda", fixed_splits=None,
-                 auto=False, tile_tokens=0, out_dtype=None):
+                 auto=False, tile_tokens=0, out_dtype=None, nq=1):
         import torch
         self.predicted_us = None
         self.out_dtype = out_dtype or torch.float32
-        if auto:
+        self.nq = nq
+        if nq > 1:
+            self.sched, self.kind = la_plan_spec(batch, hq, hkv, d, nq, cu_seqlens_k, num_sms), "lean"
+        elif auto:
             self.sched, self.kind, self.predicted_us = la_plan_auto(batch, hq, hkv, d, cu_seqlens_k, num_sms)
         elif fixed_splits is None:
             self.sched = la_plan(batch, hq, hkv, d, cu_seqlens_k, num_sms, tile_tokens)
@@ -363,7 +381,8 @@ class LeanDecoder:
     def __call__(self, q, k, v, scale, out=None, stream=None):
         import torch
         if out is None:
-            out = torch.empty(self.batch, self.hq, self.d, dtype=self.out_dtype, device=q.device)
+            shape = (self.batch, self.hq, self.d) if self.nq == 1 else (self.batch, self.nq, self.hq, self.d)
+            out = torch.empty(*shape, dtype=self.out_dtype, device=q.device)
         return la_decode(q, k, v, self.cu_dev, self.sched, self.workspace, out, scale, stream)
 
     def status(self, stream=None):

@@ -174,6 +174,8 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   s->hkv = hkv;
   s->d = d;
   s->grp = hq / hkv;
+  s->nq = 1;
+  s->R = s->grp;
   s->T = tile;
   s->kind = kind;
   s->cu.assign(cu, cu + batch + 1);
@@ -467,6 +469,34 @@ la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k
   return la_plan_ex(batch, hq, hkv, d, cu_seqlens_k, num_sms, 0, out);
 }
 
+la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t* cu_seqlens_k, int num_sms,
+                       la_schedule** out) {
+  if (out != nullptr) *out = nullptr;
+  la_status st = check_shape(batch, hq, hkv, d, cu_seqlens_k);
+  if (st != LA_OK) return st;
+  if (nq < 1) return LA_ERR_INVALID;
+  const int rows = (hq / hkv) * nq;
+  if (rows > 8) return LA_ERR_UNSUPPORTED;
+  for (int b = 0; b < batch; ++b)
+    if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
+  const int R = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  int G = num_sms;
+  if (G <= 0) {
+    int sms = 0, per_sm = 0;
+    st = device_sms(&sms);
+    if (st != LA_OK) return st;
+    st = capacity(d, la::default_tile(d), R, &per_sm);
+    if (st != LA_OK) return st;
+    G = sms * std::max(1, per_sm);
+  }
+  if (G > kMaxGrid) return LA_ERR_INVALID;
+  st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out);
+  if (st != LA_OK) return st;
+  (*out)->nq = nq;
+  (*out)->R = R;
+  return LA_OK;
+}
+
 la_status la_plan_fixed(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int splits,
                         la_schedule** out) {
   if (out != nullptr) *out = nullptr;
@@ -518,7 +548,7 @@ int la_schedule_grid(const la_schedule* s) { return s ? s->G : -1; }
 
 size_t la_workspace_size(const la_schedule* s) {
   if (s == nullptr) return 0;
-  return la::workspace_bytes(s->G, s->d, s->grp);
+  return la::workspace_bytes(s->G, s->d, s->R);
 }
 
 la_status la_workspace_init(void* workspace, size_t bytes, la_stream_t stream) {
@@ -558,7 +588,7 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
   if (kv_layout != la::kKvSlab) {
     // TMA destinations: 1024-byte aligned pieces when swizzled (tensor-core
     // path), 128-byte aligned rows otherwise.
-    const bool tc = sc->grp >= 4;
+    const bool tc = sc->R >= 4;
     const int w = sc->d % 64 == 0 ? 64 : (sc->d % 32 == 0 ? 32 : 16);
     const long long piece = tc ? (long long)box_rows * w * 2 : (long long)box_rows * sc->d * 2;
     if (piece % (tc ? 1024 : 128) != 0) return LA_ERR_UNSUPPORTED;
@@ -577,7 +607,7 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
     int sms = 0, per_sm = 0;
     la_status e = device_sms(&sms);
     if (e != LA_OK) return e;
-    e = capacity(s->d, s->T, s->grp, &per_sm);
+    e = capacity(s->d, s->T, s->R, &per_sm);
     if (e != LA_OK) return e;
     if ((int64_t)s->G > (int64_t)sms * per_sm) return LA_ERR_INVALID;
   }
@@ -617,7 +647,10 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
   }
   cudaStream_t st = (cudaStream_t)stream;
   const int dtype = dt == LA_BF16 ? 1 : 0;
-  cudaError_t ce = la::launch_decode(s->d, s->T, s->grp, dtype, p, st);
+  p.grp = s->grp;
+  p.nq = s->nq;
+  p.rows = s->grp * s->nq;
+  cudaError_t ce = la::launch_decode(s->d, s->T, s->R, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {
     la::CParams c;
@@ -629,7 +662,10 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
     c.hq = s->hq;
     c.hkv = s->hkv;
     c.out_dtype = out_dtype;
-    ce = la::launch_combine(s->d, s->grp, c, st);
+    c.grp = s->grp;
+    c.nq = s->nq;
+    c.rows = s->grp * s->nq;
+    ce = la::launch_combine(s->d, s->R, c, st);
     if (ce != cudaSuccess) return LA_ERR_CUDA;
   }
   return LA_OK;

@@ -60,6 +60,11 @@ struct KParams {
   int skip_signal;          // test hook: this CTA never sets its flag (-1: none)
   unsigned long long* trace;  // optional per-CTA timeline (kTraceWords each), or null
   int out_dtype = 0;          // 0 fp32, 1 fp16, 2 bf16
+  // Query rows of a unit: rows = grp * nq (<= the instance's row count);
+  // row r is query token r / grp of the request and head kvh * grp + r % grp.
+  int grp = 1;                // query heads per kv head
+  int nq = 1;                 // query tokens per request (speculative decoding: > 1)
+  int rows = 1;               // grp * nq
   int kv_layout = kKvSlab;
   const int32_t* block_table = nullptr;  // paged: [batch, bt_stride] page ids
   int bt_stride = 0;
@@ -89,6 +94,9 @@ struct CParams {            // fixed-split merge launch
   int hq;
   int hkv;
   int out_dtype = 0;        // 0 fp32, 1 fp16, 2 bf16
+  int grp = 1;              // query heads per kv head
+  int nq = 1;               // query tokens per request
+  int rows = 1;             // grp * nq
 };
 
 // LeanTile sizes: the default per head dim, and whether (d, T) is built.

@@ -273,6 +273,20 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, int ou
     static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
 }
 
+// Element offset / D of query row r of unit (b, kvh) in q and out
+// ([batch, nq, hq, d]): query token r / grp, head kvh * grp + r % grp.
+template <typename P>
+__device__ __forceinline__ size_t row_index(const P& p, int b, int kvh, int r) {
+  return ((size_t)b * p.nq + r / p.grp) * p.hq + (size_t)kvh * p.grp + r % p.grp;
+}
+
+// Tokens of tile t (0-based inside the request) that row r may attend to:
+// query token i of nq sits at position L - nq + i and sees keys up to it.
+__device__ __forceinline__ int row_visible(const KParams& p, long long L, int t, int T, int r) {
+  const long long lim = L - (p.nq - 1 - r / p.grp) - (long long)t * T;
+  return lim < 0 ? 0 : (lim > T ? T : (int)lim);
+}
+
 // Record the first error of the launch in the workspace header.
 __device__ __forceinline__ void record_error(uint32_t* hdr, uint32_t code, int cta, int peer) {
   if (atomicCAS(&hdr[kStatus], 0u, code) == 0u) {
@@ -458,9 +472,8 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
   float qf[GRP][8];
 #pragma unroll
   for (int j = 0; j < GRP; ++j) {
-    const int h = kvh * GRP + j;
     const uint4 raw =
-        act ? *reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) + ((size_t)b * p.hq + h) * D + c0)
+        act ? *reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) + row_index(p, b, kvh, j) * D + c0)
             : zero4;
     Elem<E>::to_f32(raw, qf[j]);
 #pragma unroll
@@ -478,6 +491,9 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
   for (int it = 0; it < n_tiles; ++it) {
     const long long rem = L - (long long)(t0 + it) * C::T;
     const int ntok = rem < C::T ? (int)rem : C::T;
+    int vis[GRP];  // tokens of this tile each row may attend to
+#pragma unroll
+    for (int j = 0; j < GRP; ++j) vis[j] = row_visible(p, L, t0 + it, C::T, j);
     if (wait_tile<D, T, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
       const E* Ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
       const E* Vs = Ks + C::TILE_ELEMS;
@@ -511,10 +527,9 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
 #pragma unroll
         for (int st = 0; st < C::CH; ++st) {
           const int tok = wtok + (c + st) * C::TPS + ts;
-          if (tok >= ntok) {
 #pragma unroll
-            for (int j = 0; j < GRP; ++j) s[st][j] = -INFINITY;
-          }
+          for (int j = 0; j < GRP; ++j)
+            if (tok >= vis[j]) s[st][j] = -INFINITY;
         }
         // online softmax: new max, rescale, exponentiate
 #pragma unroll
@@ -620,9 +635,9 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
   // the group are zero columns that are never written out.
   uint32_t qb[C::KS][2];
   {
-    const bool live = gq < GRP;
+    const bool live = gq < p.rows;
     const uint32_t* qrow =
-        reinterpret_cast<const uint32_t*>(static_cast<const E*>(p.q) + ((size_t)b * p.hq + kvh * GRP + (live ? gq : 0)) * D);
+        reinterpret_cast<const uint32_t*>(static_cast<const E*>(p.q) + row_index(p, b, kvh, live ? gq : 0) * D);
 #pragma unroll
     for (int ks = 0; ks < C::KS; ++ks) {
       qb[ks][0] = live ? qrow[(ks * 16 + 2 * tq) / 2] : 0u;
@@ -661,14 +676,16 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
           Elem<E>::mma(s[mt], a, qb[ks][0], qb[ks][1]);
         }
       }
-      // scale to base-2 units, mask tokens past the context
+      // scale to base-2 units, mask tokens each row may not see
+      const int vis0 = row_visible(p, L, t0 + it, C::T, 2 * tq);
+      const int vis1 = row_visible(p, L, t0 + it, C::T, 2 * tq + 1);
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int tok = wtok + mt * 16 + gq + ((i & 2) ? 8 : 0);
-          s[mt][i] = (tok < ntok) ? s[mt][i] * p.qscale : -INFINITY;
+          s[mt][i] = (tok < ((i & 1) ? vis1 : vis0)) ? s[mt][i] * p.qscale : -INFINITY;
           mx[i & 1] = fmaxf(mx[i & 1], s[mt][i]);
         }
       }
@@ -754,7 +771,7 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int head = 2 * tq + h;
-    if (head < GRP) {
+    if (head < p.rows) {
       float* r = wrec + head * C::REC;
       if (gq == 0) {
         r[0] = m[h];
@@ -816,7 +833,7 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
       M[i] = -INFINITY;
       Lsum[i] = 0.f;
       O[i] = 0.f;
-      if (idx < GRP * D) {
+      if (idx < p.rows * D) {
         const int j = idx / D, cc = idx % D;
         float mm = -INFINITY;
 #pragma unroll
@@ -843,7 +860,7 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
 #pragma unroll
       for (int i = 0; i < C::ITEMS; ++i) {
         const int idx = tid + i * C::NCT;
-        if (idx < GRP * D) {
+        if (idx < p.rows * D) {
           const int j = idx / D, cc = idx % D;
           float* r = rec + j * C::REC;
           r[2 + cc] = O[i];
@@ -888,7 +905,7 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
 #pragma unroll
           for (int i = 0; i < C::ITEMS; ++i) {
             const int idx = tid + i * C::NCT;
-            if (idx >= GRP * D) continue;
+            if (idx >= p.rows * D) continue;
             const int j = idx / D, cc = idx % D;
             for (int p0 = 0; p0 < npeer; p0 += 4) {
               float m2[4], l2[4], o2[4];
@@ -922,10 +939,10 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
 #pragma unroll
       for (int i = 0; i < C::ITEMS; ++i) {
         const int idx = tid + i * C::NCT;
-        if (idx < GRP * D) {
+        if (idx < p.rows * D) {
           const int j = idx / D, cc = idx % D;
           const float val = fail ? __int_as_float(0x7fc00000) : O[i] / Lsum[i];
-          store_out(p.out, ((size_t)b * p.hq + (size_t)kvh * GRP + j) * D + cc, val, p.out_dtype);
+          store_out(p.out, row_index(p, b, kvh, j) * D + cc, val, p.out_dtype);
         }
       }
     }
@@ -999,6 +1016,7 @@ __global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
   const int row = blockIdx.x;  // unit * GRP + j
   const int unit = row / GRP, j = row % GRP;
   const int c = threadIdx.x;
+  if (j >= p.rows) return;
   const int h0 = p.unit_host[unit], h1 = p.unit_fin[unit];
   if (h0 == h1) return;  // a whole unit was written by the decode kernel
   float M = -INFINITY, Ls = 0.f, O = 0.f;
@@ -1014,7 +1032,7 @@ __global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
     M = mn;
   }
   const int b = unit / p.hkv, kvh = unit % p.hkv;
-  store_out(p.out, ((size_t)b * p.hq + (size_t)kvh * GRP + j) * D + c, O / Ls, p.out_dtype);
+  store_out(p.out, row_index(p, b, kvh, j) * D + c, O / Ls, p.out_dtype);
 }
 
 // ------------------------------------------------------------- host launchers

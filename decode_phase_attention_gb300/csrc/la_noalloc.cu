@@ -49,7 +49,7 @@ Layout layout_of(const la_schedule* s) {
   L.flags = off;
   off += la::flags_bytes(s->G);
   L.recs = off;
-  off = la::align_up(off + sizeof(float) * la::record_floats(s->d, s->grp) * (size_t)s->G, 256);
+  off = la::align_up(off + sizeof(float) * la::record_floats(s->d, s->R) * (size_t)s->G, 256);
   auto table = [&off](size_t words) {
     const size_t at = off;
     off = la::align_up(off + words * sizeof(int32_t), 16);
@@ -91,7 +91,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
     int per_sm = 0, sms = 0;
     la_status e = la_device_capacity(s->d, s->grp, &per_sm, &sms);
     if (e != LA_OK) return e;
-    if (la::decode_capacity(s->d, s->T, s->grp, &per_sm) != cudaSuccess) return LA_ERR_CUDA;
+    if (la::decode_capacity(s->d, s->T, s->R, &per_sm) != cudaSuccess) return LA_ERR_CUDA;
     if ((long long)s->G > (long long)per_sm * sms) return LA_ERR_INVALID;
   }
   int dev = 0;
@@ -132,7 +132,10 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   p.skip_signal = s->skip_signal;
   p.trace = s->trace;
   const int dtype = dt == LA_BF16 ? 1 : 0;
-  cudaError_t ce = la::launch_decode(s->d, s->T, s->grp, dtype, p, st);
+  p.grp = s->grp;
+  p.nq = s->nq;
+  p.rows = s->grp * s->nq;
+  cudaError_t ce = la::launch_decode(s->d, s->T, s->R, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {
     la::CParams c;
@@ -143,7 +146,10 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
     c.U = s->U;
     c.hq = s->hq;
     c.hkv = s->hkv;
-    ce = la::launch_combine(s->d, s->grp, c, st);
+    c.grp = s->grp;
+    c.nq = s->nq;
+    c.rows = s->grp * s->nq;
+    ce = la::launch_combine(s->d, s->R, c, st);
     if (ce != cudaSuccess) return LA_ERR_CUDA;
   }
   return LA_OK;

@@ -120,6 +120,23 @@ la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlen
                      int tile_tokens, la_schedule** out);
 
 /*
+ * la_plan_spec -- stream-K schedule for nq query tokens per request, as in
+ * speculative-decoding verification (the review's "7.4" lists combining
+ * the method with speculative decoding as future work).
+ *
+ * The nq query tokens of request b are the last nq tokens of its context:
+ * query i (0 <= i < nq) sits at position L_b - nq + i and attends to keys
+ * 0 .. L_b - nq + i (a causal mask inside the last tile). With such a
+ * schedule la_decode / la_decode_ex / la_decode_kv / la_decode_static read
+ * q as [batch, nq, hq, d] and write out as [batch, nq, hq, d]. The tiles and
+ * their split are those of la_plan (K/V are read once per kv head for all
+ * grp * nq query rows). Requires grp * nq <= 8 (LA_ERR_UNSUPPORTED) and
+ * L_b >= nq for every request (LA_ERR_INVALID); nq = 1 is la_plan.
+ */
+la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t* cu_seqlens_k, int num_sms,
+                       la_schedule** out);
+
+/*
  * la_plan_fixed -- fixed partitions used as baselines (the review's "2.2"
  * and "2.3" on FlashAttention-2 and FlashDecoding, and "4.3" on their
  * relation to the stream-K mapping). Every unit is cut into

@@ -62,6 +62,8 @@ def _open(path):
     lib.oracle_partial.argtypes = [i32, i32, vp, vp, vp, i64, i64, dbl, vp]
     lib.oracle_attend.restype = i32
     lib.oracle_attend.argtypes = [i32, i32, i32, i32, vp, i32, vp, vp, vp, dbl, i64, vp, vp, i32]
+    lib.oracle_attend_spec.restype = i32
+    lib.oracle_attend_spec.argtypes = [i32, i32, i32, i32, i32, vp, i32, vp, vp, vp, dbl, i64, vp, vp, i32]
     return lib
 
 
@@ -121,30 +123,31 @@ def bf16_to_double(bits):
     return out
 
 
-def attend(q, k, v, cu, hq, hkv, d, scale, dtype, rows=None, threads=None):
-    """Decode attention for every (request, query head) row, or the listed rows.
+def attend(q, k, v, cu, hq, hkv, d, scale, dtype, rows=None, threads=None, nq=1):
+    """Decode attention for every (request, query token, query head) row, or the listed rows.
 
-    q: [batch, hq, d]; k, v: per request b a [hkv, L_b, d] slab at element
+    q: [batch, nq, hq, d]; k, v: per request b a [hkv, L_b, d] slab at element
     offset hkv*cu[b]*d (L_b = cu[b+1]-cu[b]); query head h reads kv head
-    h // (hq // hkv). Returns float64 [nrows, d] (rows are b*hq + h).
+    h // (hq // hkv); with nq > 1 query i of request b sees keys
+    0 .. L_b - nq + i. Returns float64 [nrows, d] (rows are (b*nq + i)*hq + h).
     """
     lib = _load()
     cu = np.ascontiguousarray(cu, dtype=np.int32)
     batch = cu.size - 1
     qa, ka, va = _as_input(q, dtype), _as_input(k, dtype), _as_input(v, dtype)
     need_kv = int(cu[-1]) * hkv * d
-    if qa.size < batch * hq * d or ka.size < need_kv or va.size < need_kv:
+    if qa.size < batch * nq * hq * d or ka.size < need_kv or va.size < need_kv:
         raise ValueError("input arrays are smaller than the shape implies")
     if rows is None:
-        nrows, rows_ptr = batch * hq, None
+        nrows, rows_ptr = batch * nq * hq, None
     else:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         nrows, rows_ptr = rows.size, _ptr(rows)
     out = np.zeros((nrows, d), dtype=np.float64)
     if threads is None:
         threads = os.cpu_count() or 1
-    rc = lib.oracle_attend(batch, hq, hkv, d, _ptr(cu), dtype, _ptr(qa), _ptr(ka), _ptr(va),
-                           float(scale), nrows, rows_ptr, _ptr(out), int(threads))
+    rc = lib.oracle_attend_spec(batch, int(nq), hq, hkv, d, _ptr(cu), dtype, _ptr(qa), _ptr(ka), _ptr(va),
+                                float(scale), nrows, rows_ptr, _ptr(out), int(threads))
     if rc != 0:
         raise ValueError("oracle_attend rejected its arguments")
     return out

@@ -172,14 +172,17 @@ int oracle_partial(int d, int dtype, const void* q, const void* k, const void* v
 
 /*
  * Layout of the batched inputs (decode phase, ragged batch):
- *   q   [batch, hq, d]
+ *   q   [batch, nq, hq, d]  (nq = 1: one query token per request)
  *   k,v per request b: a [hkv, L_b, d] slab at element offset hkv*cu[b]*d,
  *       L_b = cu[b+1] - cu[b]; token t of kv head h at (hkv*cu[b] + h*L_b + t)*d.
  *   query head h reads kv head h / (hq/hkv).
- *   out [nrows, d] for the requested rows (row index r = b*hq + h).
+ *   With nq > 1 (verification of speculative tokens) the queries are the
+ *   last nq tokens of the context: query i sits at position L_b - nq + i and
+ *   sees keys 0 .. L_b - nq + i (causal).
+ *   out [nrows, d] for the requested rows (row index r = (b*nq + i)*hq + h).
  */
 typedef struct {
-  int batch, hq, hkv, d, dtype;
+  int batch, nq, hq, hkv, d, dtype;
   const int32_t* cu;
   const void *q, *k, *v;
   double scale;
@@ -200,10 +203,11 @@ static void* attend_worker(void* arg) {
   }
   for (long i = j->tid; i < j->nrows; i += j->nthreads) {
     long r = j->rows ? (long)j->rows[i] : i;
-    long b = r / j->hq, h = r % j->hq, kvh = h / grp;
+    long h = r % j->hq, bq = r / j->hq, b = bq / j->nq, qi = bq % j->nq, kvh = h / grp;
     long L = (long)j->cu[b + 1] - (long)j->cu[b];
     long kv_off = ((long)j->hkv * j->cu[b] + kvh * L) * (long)j->d;
-    if (partial_row(j->d, j->dtype, j->q, r * (long)j->d, j->k, j->v, kv_off, 0, L, j->scale,
+    long visible = L - (j->nq - 1 - qi); /* keys 0 .. L - nq + qi */
+    if (partial_row(j->d, j->dtype, j->q, r * (long)j->d, j->k, j->v, kv_off, 0, visible, j->scale,
                     &tri[0], &tri[1], tri + 2) != 0) {
       j->status = -1;
       break;
@@ -219,22 +223,22 @@ static void* attend_worker(void* arg) {
  * batch*hq rows in order). Returns 0, or -1 on bad arguments or allocation
  * failure.
  */
-int oracle_attend(int batch, int hq, int hkv, int d, const int32_t* cu, int dtype, const void* q,
-                  const void* k, const void* v, double scale, long nrows, const int64_t* rows,
-                  double* out, int nthreads) {
-  if (batch <= 0 || hq <= 0 || hkv <= 0 || d <= 0 || hq % hkv != 0) return -1;
+int oracle_attend_spec(int batch, int nq, int hq, int hkv, int d, const int32_t* cu, int dtype,
+                       const void* q, const void* k, const void* v, double scale, long nrows,
+                       const int64_t* rows, double* out, int nthreads) {
+  if (batch <= 0 || nq <= 0 || hq <= 0 || hkv <= 0 || d <= 0 || hq % hkv != 0) return -1;
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 256) nthreads = 256;
   for (long i = 0; i < nrows; ++i) {
     long r = rows ? (long)rows[i] : i;
-    if (r < 0 || r >= (long)batch * hq) return -1;
+    if (r < 0 || r >= (long)batch * nq * hq) return -1;
   }
   for (int b = 0; b < batch; ++b)
-    if (cu[b + 1] < cu[b]) return -1;
+    if (cu[b + 1] - cu[b] < nq) return -1; /* the query tokens are part of the context */
   job_t jobs[256];
   pthread_t th[256];
   for (int t = 0; t < nthreads; ++t) {
-    job_t j = {batch, hq, hkv, d, dtype, cu, q, k, v, scale, nrows, rows, out, nthreads, t, 0};
+    job_t j = {batch, nq, hq, hkv, d, dtype, cu, q, k, v, scale, nrows, rows, out, nthreads, t, 0};
     jobs[t] = j;
   }
   if (nthreads == 1) {
@@ -252,4 +256,13 @@ int oracle_attend(int batch, int hq, int hkv, int d, const int32_t* cu, int dtyp
   for (int t = 0; t < nthreads; ++t)
     if (jobs[t].status != 0) return -1;
   return 0;
+}
+
+/* Decode attention with one query token per request: the definition of
+   "3.1 standard attention" with N_q = 1. */
+int oracle_attend(int batch, int hq, int hkv, int d, const int32_t* cu, int dtype, const void* q,
+                  const void* k, const void* v, double scale, long nrows, const int64_t* rows,
+                  double* out, int nthreads) {
+  return oracle_attend_spec(batch, 1, hq, hkv, d, cu, dtype, q, k, v, scale, nrows, rows, out,
+                            nthreads);
 }

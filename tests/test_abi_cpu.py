@@ -193,3 +193,23 @@ def test_decode_ex_rejects_an_unknown_output_type():
     p = ctypes.c_void_p(0x10000)
     assert la._lib.la_decode_ex(p, p, p, 0, p, s.handle, ctypes.c_void_p(0x20000), p, 7, 0.125, None) \
         == la.LA_ERR_INVALID
+
+
+def test_spec_schedule_matches_the_decode_plan_and_sizes_its_records():
+    lengths = [300, 17, 1000]
+    s = la.la_plan_spec(3, 4, 2, 128, 3, cu_of(lengths), 11)
+    assert s.nq == 3
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(3, 4, 2, 128, cu_of(lengths), 11))
+    # grp 2 x nq 3 = 6 query rows per unit: records of 8 rows (the instance's row count)
+    assert la.la_workspace_size(s) == 256 + 256 + 11 * 8 * 130 * 4
+
+
+@pytest.mark.parametrize("hq,hkv,nq,lengths,status", [
+    (8, 2, 3, [100, 200], la.LA_ERR_UNSUPPORTED),   # 4 x 3 = 12 query rows per unit
+    (4, 4, 5, [100, 4], la.LA_ERR_INVALID),          # a context shorter than its query tokens
+    (4, 4, 0, [100, 200], la.LA_ERR_INVALID),
+])
+def test_spec_schedule_rejections(hq, hkv, nq, lengths, status):
+    with pytest.raises(la.LeanAttentionError) as e:
+        la.la_plan_spec(len(lengths), hq, hkv, 64, nq, cu_of(lengths), 7)
+    assert e.value.status == status

@@ -284,3 +284,49 @@ def test_f_identity_element():
     assert empty[0] == -np.inf and empty[1] == 0 and not np.any(empty[2:])
     np.testing.assert_array_equal(oracle.merge_f(x, empty), x)
     np.testing.assert_array_equal(oracle.merge_f(empty, x), x)
+
+
+# --- several query tokens per request (speculative-decoding verification) -----
+
+def test_each_query_token_sees_exactly_its_causal_prefix():
+    r = rng(15)
+    lens, nq, hq, hkv, d = [9, 4, 30], 4, 4, 2, 8
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    K = r.normal(size=hkv * cu[-1] * d)
+    V = r.normal(size=hkv * cu[-1] * d)
+    q = r.normal(size=(len(lens), nq, hq, d))
+    out = oracle.attend(q, K, V, cu, hq, hkv, d, 0.3, oracle.F64, nq=nq, threads=3)
+    for b, L in enumerate(lens):
+        slab_k = K[hkv * cu[b] * d:hkv * cu[b + 1] * d].reshape(hkv, L, d)
+        slab_v = V[hkv * cu[b] * d:hkv * cu[b + 1] * d].reshape(hkv, L, d)
+        for i in range(nq):
+            vis = L - nq + i + 1  # keys 0 .. L - nq + i
+            for h in range(hq):
+                kv = h // (hq // hkv)
+                want = oracle.attend_row(q[b, i, h], slab_k[kv, :vis], slab_v[kv, :vis], 0.3)
+                np.testing.assert_array_equal(out[(b * nq + i) * hq + h], want)
+
+
+def test_keys_after_a_query_token_do_not_change_it():
+    r = rng(16)
+    L, nq, d = 20, 3, 16
+    cu = np.array([0, L], np.int32)
+    K, V = r.normal(size=L * d), r.normal(size=L * d)
+    q = r.normal(size=(1, nq, 1, d))
+    base = oracle.attend(q, K, V, cu, 1, 1, d, 0.25, oracle.F64, nq=nq, threads=1)
+    K2, V2 = K.copy(), V.copy()
+    K2[(L - 1) * d:] += 5.0  # the last key: visible to the last query only
+    V2[(L - 1) * d:] -= 3.0
+    moved = oracle.attend(q, K2, V2, cu, 1, 1, d, 0.25, oracle.F64, nq=nq, threads=1)
+    np.testing.assert_array_equal(moved[:nq - 1], base[:nq - 1])
+    assert not np.allclose(moved[nq - 1], base[nq - 1])
+
+
+def test_one_query_token_is_ordinary_decode():
+    r = rng(17)
+    cu = np.array([0, 50, 51], np.int32)
+    K, V = r.normal(size=2 * 51 * 8), r.normal(size=2 * 51 * 8)
+    q = r.normal(size=(2, 4, 8))
+    a = oracle.attend(q, K, V, cu, 4, 2, 8, 0.5, oracle.F64)
+    b = oracle.attend(q.reshape(2, 1, 4, 8), K, V, cu, 4, 2, 8, 0.5, oracle.F64, nq=1)
+    np.testing.assert_array_equal(a, b)

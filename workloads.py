@@ -35,6 +35,7 @@ class Workload:
     outlier_frac: float = 0.0  # fraction of key rows multiplied by outlier_scale
     outlier_scale: float = 8.0
     description: str = ""
+    nq: int = 1  # query tokens per request (the last nq tokens of the context)
 
     @property
     def scale(self):
@@ -99,6 +100,11 @@ def named(name, seed=0):
         heads = 16 if d == 256 else 32
         return Workload(name, 4, heads, heads, d, "bf16", [32768] * 4,
                         description=f"head dim {d}: batch 4, {heads}/{heads} heads, d {d}, ctx 32768, bf16")
+    if name.startswith("spec"):
+        # speculative-decoding verification: 4 draft tokens per request
+        return Workload(name, 8, 32, 32, 128, "bf16", [8192] * 8, nq=4,
+                        description="speculative verification: batch 8, 4 query tokens per request, "
+                                    "32/32 heads, d 128, ctx 8192, bf16, causal among the 4")
     if name == "hd128gqa":
         return Workload(name, 4, 32, 4, 128, "bf16", [32768] * 4,
                         description="GQA d 128: batch 4, 32 query over 4 kv heads, d 128, ctx 32768, bf16")
@@ -106,7 +112,7 @@ def named(name, seed=0):
 
 
 NAMES = ["tiny", "uniform", "long64k", "long256k", "long512k", "ragged", "gqa"]
-EXTRA_NAMES = ["hd80", "hd96", "hd256", "hd128gqa"]
+EXTRA_NAMES = ["hd80", "hd96", "hd256", "hd128gqa", "spec4"]
 
 
 def make_inputs(w, seed=0, device="cpu"):
@@ -126,7 +132,8 @@ def make_inputs(w, seed=0, device="cpu"):
     gen = torch.Generator(device=dev)
 
     gen.manual_seed(_seed(seed, 0xA11, 0))
-    q = torch.randn(w.batch, w.hq, w.d, generator=gen, device=dev, dtype=torch.float32).to(tdt)
+    qshape = (w.batch, w.hq, w.d) if w.nq == 1 else (w.batch, w.nq, w.hq, w.d)
+    q = torch.randn(*qshape, generator=gen, device=dev, dtype=torch.float32).to(tdt)
     n_kv = w.hkv * w.total_tokens * w.d
     k = torch.empty(n_kv, dtype=tdt, device=dev)
     v = torch.empty(n_kv, dtype=tdt, device=dev)
@@ -145,9 +152,9 @@ def make_inputs(w, seed=0, device="cpu"):
     return q, k, v, cu
 
 
-def custom(batch, hq, hkv, d, dtype, lengths, grid=0, name="custom"):
-    return Workload(name, batch, hq, hkv, d, dtype, list(lengths), grid=grid,
-                    description=f"{name}: batch {batch}, {hq}/{hkv} heads, d {d}, {dtype}")
+def custom(batch, hq, hkv, d, dtype, lengths, grid=0, name="custom", nq=1):
+    return Workload(name, batch, hq, hkv, d, dtype, list(lengths), grid=grid, nq=nq,
+                    description=f"{name}: batch {batch}, {hq}/{hkv} heads, d {d}, {dtype}, nq {nq}")
 
 
 def to_token_major(w, k, v):
