@@ -152,6 +152,17 @@ class ClockSampler:
                 "in_timed_region": bool(inside)}
 
 
+def max_over_ranks(x, device=None):
+    """The slowest rank's value (every rank runs an independent replica)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def summarize_trace(tr):
     """Per-CTA timeline of one call: balance of busy time and host-CTA waits (microseconds)."""
     import numpy as np
@@ -379,10 +390,7 @@ def run_ours(args, rank, world, local_rank):
         e.record(stream)
     torch.cuda.synchronize(dev)
     times_ms = sorted(a.elapsed_time(e) for a, e in sp)
-    if world > 1:
-        t = torch.tensor([mean_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms = max_over_ranks(mean_ms, dev)
     st = dec.status()
     if st != la.LA_OK:
         raise RuntimeError(f"kernel reported: {la.status_string(st)}")
@@ -421,10 +429,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dev)
         h2d = (q.numel() + k.numel() + v.numel()) * q.element_size()
         e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
                "us_per_call": round(e2e_ms * 1e3, 2), "steps": n_e2e,

@@ -317,8 +317,6 @@ double predict_seconds(const la_schedule* s, int slots) {
 
 namespace la {
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against libcuda), looked up once.
 int default_tile(int d) {
   switch (d) {
     case 64: return 256;   // the review's LeanTile table
@@ -374,25 +372,30 @@ cudaError_t decode_capacity(int d, int T, int grp, int* per_sm) {
   }
 }
 
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, looked up once.
+EncodeTiled encode_fn() {
+  static std::mutex mu;
+  static EncodeTiled fn = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  }
+  return fn;
+}
+
 cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, int T, int W, int elem_type,
                            CUtensorMap* mk, CUtensorMap* mv) {
-  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-  static std::mutex mu;
-  static Encode fn = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (fn == nullptr) {
-      void* ptr = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-              cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || ptr == nullptr)
-        return cudaErrorNotSupported;
-      fn = reinterpret_cast<Encode>(ptr);
-    }
-  }
+  const EncodeTiled fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
   if (rows <= 0 || rows > (1LL << 31) - 1) return cudaErrorInvalidValue;
   const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
@@ -412,16 +415,8 @@ cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, 
 
 cudaError_t encode_kv_maps_3d(const void* k, const void* v, long long rows, int hkv, int d, int bw, int box_rows,
                               bool swizzle, int elem_type, CUtensorMap* mk, CUtensorMap* mv) {
-  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-  void* ptr = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-          cudaSuccess ||
-      q != cudaDriverEntryPointSuccess || ptr == nullptr)
-    return cudaErrorNotSupported;
-  Encode fn = reinterpret_cast<Encode>(ptr);
+  const EncodeTiled fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
   if (rows <= 0 || rows > (1LL << 31) - 1) return cudaErrorInvalidValue;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hkv * d * 2};
