@@ -297,18 +297,26 @@ double piece_bytes(const la_schedule* s, int u, int t0, int t1) {
   return (double)tok * s->d * 2.0 * 2.0;
 }
 
-// Predicted time of a schedule: per-CTA byte totals through the dispatch model
-// plus launch overheads (one launch, or two for fixed splits > 1).
+// Predicted time of a schedule: per-CTA byte totals through the dispatch model,
+// a start-up latency for every CTA an SM runs in turn (its first tile must
+// arrive before it computes), the host CTAs' merge when units are split
+// within the launch, and launch overheads (two launches for fixed splits > 1).
+// Constants measured on GB300: one SM streams up to 70 GB/s, all SMs 7.3 TB/s;
+// 3 us from CTA start to its first tile; 2.5 us for a host CTA's merge.
 double predict_seconds(const la_schedule* s, int slots) {
-  constexpr double kPerSm = 70e9, kTotal = 7.3e12;  // measured on GB300 (one active SM / all SMs)
-  constexpr double kLaunch = 8e-6, kMergeLaunch = 4e-6;
+  constexpr double kPerSm = 70e9, kTotal = 7.3e12;
+  constexpr double kLaunch = 8e-6, kMergeLaunch = 4e-6, kStartup = 3e-6, kHostMerge = 2.5e-6;
   std::vector<double> jobs((size_t)s->G, 0.0);
+  bool split = false;
   for (int g = 0; g < s->G; ++g)
     for (int i = s->cta_seg[g]; i < s->cta_seg[g + 1]; ++i) {
       const int32_t* sg = &s->segs[(size_t)i * la::kSegWords];
       jobs[g] += piece_bytes(s, sg[0], sg[1], sg[2]);
+      split = split || sg[3] == la::kHost;
     }
-  double t = simulate_dispatch(jobs, slots, kPerSm, kTotal) + kLaunch;
+  const int rounds = (s->G + slots - 1) / std::max(1, slots);  // CTAs one SM runs in turn
+  double t = simulate_dispatch(jobs, slots, kPerSm, kTotal) + kLaunch + kStartup * rounds;
+  if (split) t += kHostMerge;
   if (s->kind == 1 && s->splits > 1) t += kMergeLaunch;
   return t;
 }

@@ -28,9 +28,12 @@ def _rank(rank, world, port, out):
 
 def test_max_over_two_gloo_ranks():
     port = _free_port()
-    out = mp.Manager().dict()
-    mp.start_processes(_rank, args=(2, port, out), nprocs=2, join=True, start_method="spawn")
-    assert dict(out) == {0: 15.0, 1: 15.0}
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as manager:
+        out = manager.dict()
+        mp.start_processes(_rank, args=(2, port, out), nprocs=2, join=True, start_method="spawn")
+        result = dict(out)
+    assert result == {0: 15.0, 1: 15.0}
 
 
 def test_single_process_is_unchanged():

@@ -100,6 +100,12 @@ def named(name, seed=0):
         heads = 16 if d == 256 else 32
         return Workload(name, 4, heads, heads, d, "bf16", [32768] * 4,
                         description=f"head dim {d}: batch 4, {heads}/{heads} heads, d {d}, ctx 32768, bf16")
+    if name.startswith("mha_"):
+        # sweep shapes, e.g. mha_h56_b1_c65536_d64: batch b, h/h heads, d, equal contexts, fp16
+        parts = dict((p[0], int(p[1:])) for p in name.split("_")[1:])
+        h, b, c, d = parts["h"], parts["b"], parts["c"], parts["d"]
+        return Workload(name, b, h, h, d, "f16", [c] * b,
+                        description=f"sweep: batch {b}, {h}/{h} heads, d {d}, ctx {c}, fp16")
     if name.startswith("spec"):
         # speculative-decoding verification: 4 draft tokens per request
         return Workload(name, 8, 32, 32, 128, "bf16", [8192] * 8, nq=4,
