@@ -68,11 +68,13 @@ def measured_peaks():
 
 
 def kernel_source_digest():
+    """Digest of the device-code sources (kernel template, its parameters and instances)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_phase_attention_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        h.update(f.encode())
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        if f == "la_kernel.cuh" or f == "la_internal.h" or f.startswith("la_kernels_"):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 

@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <map>
 #include <cstdint>
 #include <cstring>
@@ -261,10 +262,11 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // ---- shape-driven choice among the three partitions ----------------------
 // Time model (seconds) of a launch whose CTAs each stream a fixed number of
 // bytes: CTAs are dispatched in order onto `slots` SMs as SMs free up (the
-// hardware's in-order block dispatch); while n CTAs run, each streams at
-// min(per_sm, total / n) bytes/s. Jobs finish in order of their cumulative
-// progress, so a heap of finish thresholds gives the makespan.
-double simulate_dispatch(const std::vector<double>& job_bytes, int slots, double per_sm, double total) {
+// hardware's in-order block dispatch); while n CTAs run, together they read
+// R(n) = r_max * (1 - exp(-n / n0)) bytes/s, shared equally. Jobs finish in
+// order of their cumulative progress, so a heap of finish thresholds gives
+// the makespan.
+double simulate_dispatch(const std::vector<double>& job_bytes, int slots, double r_max, double n0) {
   if (job_bytes.empty()) return 0.0;
   std::vector<double> heap;  // min-heap of progress thresholds of running jobs
   auto cmp = [](double a, double b) { return a > b; };
@@ -275,7 +277,8 @@ double simulate_dispatch(const std::vector<double>& job_bytes, int slots, double
     std::push_heap(heap.begin(), heap.end(), cmp);
   }
   while (!heap.empty()) {
-    const double rate = std::min(per_sm, total / (double)heap.size());
+    const double n = (double)heap.size();
+    const double rate = r_max * (1.0 - std::exp(-n / n0)) / n;
     std::pop_heap(heap.begin(), heap.end(), cmp);
     const double thr = heap.back();
     heap.pop_back();
@@ -301,10 +304,11 @@ double piece_bytes(const la_schedule* s, int u, int t0, int t1) {
 // a start-up latency for every CTA an SM runs in turn (its first tile must
 // arrive before it computes), the host CTAs' merge when units are split
 // within the launch, and launch overheads (two launches for fixed splits > 1).
-// Constants measured on GB300: one SM streams up to 70 GB/s, all SMs 7.3 TB/s;
+// Constants fitted to GB300 measurements: aggregate read rate with n busy SMs
+// 7.5 TB/s * (1 - exp(-n / 60)) (3.1 TB/s at 32, 6.6 at 128, 6.9 at 152);
 // 3 us from CTA start to its first tile; 2.5 us for a host CTA's merge.
 double predict_seconds(const la_schedule* s, int slots) {
-  constexpr double kPerSm = 70e9, kTotal = 7.3e12;
+  constexpr double kRateMax = 7.5e12, kRateN0 = 60.0;
   constexpr double kLaunch = 8e-6, kMergeLaunch = 4e-6, kStartup = 3e-6, kHostMerge = 2.5e-6;
   std::vector<double> jobs((size_t)s->G, 0.0);
   bool split = false;
@@ -315,7 +319,7 @@ double predict_seconds(const la_schedule* s, int slots) {
       split = split || sg[3] == la::kHost;
     }
   const int rounds = (s->G + slots - 1) / std::max(1, slots);  // CTAs one SM runs in turn
-  double t = simulate_dispatch(jobs, slots, kPerSm, kTotal) + kLaunch + kStartup * rounds;
+  double t = simulate_dispatch(jobs, slots, kRateMax, kRateN0) + kLaunch + kStartup * rounds;
   if (split) t += kHostMerge;
   if (s->kind == 1 && s->splits > 1) t += kMergeLaunch;
   return t;

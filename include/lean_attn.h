@@ -158,9 +158,10 @@ la_status la_plan_fixed(int batch, int hq, int hkv, int d, const int32_t* cu_seq
  * current device), the one-CTA-per-unit partition and the fixed split into
  * max(2, ceil(SMs / units)) pieces, predicts each one's time and returns
  * the fastest. Time model: CTAs dispatched in order onto the SMs as they
- * free up, each running CTA streaming its K+V bytes at min(70 GB/s,
- * 7.3 TB/s / running CTAs) — rates measured on GB300 — plus 8 us per
- * launch and 4 us for the second (merge) launch of a fixed split.
+ * free up; n running CTAs read 7.5 TB/s * (1 - exp(-n / 60)) together
+ * (fitted to GB300 measurements); 3 us of start-up per CTA an SM runs in
+ * turn, 2.5 us for host CTAs' merges, 8 us per launch and 4 us for the
+ * second (merge) launch of a fixed split.
  * predicted_us: NULL, or 3 doubles receiving the predictions (stream-K,
  * one per unit, fixed split). The returned schedule is used like any
  * other; la_schedule_export tells which kind it is (word 6, word 7).

