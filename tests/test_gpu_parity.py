@@ -222,3 +222,16 @@ def test_head_dim_workloads_full_output(name):
     q, k, v, _ = workloads.make_inputs(w, seed=0, device="cuda")
     out, _ = run_lean(w, q, k, v)
     compare(out.cpu(), reference(w, q, k, v))
+
+
+def test_offsets_beyond_two_to_the_31_elements():
+    # 1M-token context, 32 heads, d 128: K alone is 2^32 elements (8.6 GB), so every
+    # slab offset past the first half needs 64-bit arithmetic; rows sampled for the oracle
+    w = workloads.custom(1, 32, 32, 128, "bf16", [1 << 20])
+    q, k, v, _ = workloads.make_inputs(w, seed=29, device="cuda")
+    out, _ = run_lean(w, q, k, v)
+    rows = np.array([0, 13, 31], np.int64)
+    ref = reference(w, q, k, v, rows=rows)
+    compare(out.view(32, 128)[rows].cpu(), ref)
+    del q, k, v
+    torch.cuda.empty_cache()

@@ -48,7 +48,7 @@ def test_schedule_too_large_for_the_fixed_array_is_rejected_before_any_launch():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("case", ["tiny", "ragged_gqa", "fixed_split"])
+@pytest.mark.parametrize("case", ["tiny", "ragged_gqa", "fixed_split", "three_query_tokens"])
 def test_static_scratch_matches_la_decode_on_two_calls_in_a_row(case):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -59,18 +59,21 @@ def test_static_scratch_matches_la_decode_on_two_calls_in_a_row(case):
     elif case == "ragged_gqa":
         w = workloads.custom(5, 32, 4, 64, "bf16", [3000, 17, 20000, 257, 9000])
         make = lambda: la.la_plan(w.batch, w.hq, w.hkv, w.d, w.cu, 0)  # noqa: E731
-    else:
+    elif case == "fixed_split":
         w = workloads.custom(3, 8, 8, 128, "f16", [5000, 300, 12000])
         make = lambda: la.la_plan_fixed(w.batch, w.hq, w.hkv, w.d, w.cu, 6)  # noqa: E731
+    else:
+        w = workloads.custom(3, 4, 2, 128, "bf16", [700, 3, 4000], nq=3)
+        make = lambda: la.la_plan_spec(w.batch, w.hq, w.hkv, w.d, 3, w.cu)  # noqa: E731
     q, k, v, _ = workloads.make_inputs(w, seed=11, device="cuda")
     cu = torch.as_tensor(w.cu, dtype=torch.int32, device="cuda")
     sched = make()
-    ref = torch.empty(w.batch, w.hq, w.d, device="cuda")
+    ref = torch.empty(*q.shape, device="cuda")
     ws = la.new_workspace(sched)
     la.la_decode(q, k, v, cu, sched, ws, ref, w.scale)
     assert la.la_get_status(ws) == la.LA_OK
     for _ in range(2):
-        out = torch.full((w.batch, w.hq, w.d), float("nan"), device="cuda")
+        out = torch.full(tuple(q.shape), float("nan"), device="cuda")
         assert _static_call(q, k, v, cu, sched, out, w.scale) == la.LA_OK
         torch.cuda.synchronize()
         _close(out, ref)
