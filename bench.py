@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"])
     ap.add_argument("--kv-layout", default="slab", choices=["slab", "token_major", "paged"])
     ap.add_argument("--page-size", type=int, default=64)
+    ap.add_argument("--heads-per-unit", type=int, default=0,
+                    help="token-major / paged caches: kv heads per unit (0 = la_plan_kv's choice)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -194,8 +196,8 @@ def algorithmic_bytes(w, export, out_bytes=4):
     G, U, nseg = export[1], export[2], export[5]
     base = 8 + 2 * (G + 1) + (U + 1)
     pieces = sum(1 for i in range(nseg) if export[base + 5 * i + 3] in (1, 3))
-    rows = (w.hq // w.hkv) * w.nq
-    rec = (1 if rows <= 1 else 2 if rows <= 2 else 4 if rows <= 4 else 8) * (w.d + 2) * 4
+    rows = (w.hq // w.hkv) * w.nq * (w.batch * w.hkv // U)  # query rows of a unit (all its kv heads)
+    rec = rows * (w.d + 2) * 4
     return kv, kv + q + out + 2 * pieces * rec
 
 
@@ -298,7 +300,10 @@ def run_ours(args, rank, world, local_rank):
         plan_times.append((time.perf_counter() - t0) * 1e6)
     plan_us = sorted(plan_times)[len(plan_times) // 2]
     out_torch = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[args.out_dtype]
-    if w.nq > 1:
+    if args.kv_layout != "slab" and args.kernel == "lean":
+        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, nq=w.nq,
+                             tile_tokens=args.tile, heads_per_unit=args.heads_per_unit)
+    elif w.nq > 1:
         dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, nq=w.nq)
     elif args.kernel == "lean":
         dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, tile_tokens=args.tile)
@@ -463,6 +468,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.description, "kernel": args.kernel, "schedule": dec.kind,
                    "tile_tokens": la.la_schedule_export(dec.sched)[4], "out_dtype": args.out_dtype,
+                   "kv_heads_per_unit": dec.sched.heads_per_unit,
                    "kv_layout": args.kv_layout + (f" (page {args.page_size})" if args.kv_layout == "paged" else ""),
                    "predicted_us": dec.predicted_us, "grid": G,
                    "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,

@@ -28,7 +28,7 @@ class KvDesc(ctypes.Structure):
     """la_kv_desc: layout of the K/V caches."""
     _fields_ = [("layout", ctypes.c_int), ("block_table", ctypes.c_void_p), ("max_blocks", ctypes.c_int),
                 ("page_size", ctypes.c_int), ("num_pages", ctypes.c_longlong)]
-EXPORTED = ["la_plan", "la_plan_ex", "la_plan_spec", "la_plan_fixed", "la_plan_auto", "la_decode_ex", "la_decode_kv", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
+EXPORTED = ["la_plan", "la_plan_ex", "la_plan_spec", "la_plan_kv", "la_plan_fixed", "la_plan_auto", "la_decode_ex", "la_decode_kv", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
             "la_decode", "la_decode_static", "la_get_status", "la_schedule_export_size", "la_schedule_export",
             "la_schedule_set_debug", "la_schedule_set_trace", "la_device_capacity", "la_schedule_destroy",
             "la_status_string"]
@@ -51,6 +51,7 @@ def _load():
         "la_plan": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
         "la_plan_ex": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, c_int, pp]),
         "la_plan_spec": (c_int, [c_int, c_int, c_int, c_int, c_int, vp, c_int, pp]),
+        "la_plan_kv": (c_int, [c_int, c_int, c_int, c_int, c_int, vp, c_int, c_int, c_int, pp]),
         "la_decode_ex": (c_int, [vp, vp, vp, c_int, vp, vp, vp, vp, c_int, c_float, vp]),
         "la_decode_kv": (c_int, [vp, vp, vp, c_int, vp, ctypes.POINTER(KvDesc), vp, vp, vp, c_int, c_float, vp]),
         "la_plan_fixed": (c_int, [c_int, c_int, c_int, c_int, vp, c_int, pp]),
@@ -96,6 +97,8 @@ class Schedule:
         self.batch, self.hq, self.hkv, self.d = batch, hq, hkv, d
         self.cu = cu
         self.nq = nq
+        head = la_schedule_export(self)[:3]
+        self.heads_per_unit = batch * hkv // head[2]  # kv heads of one unit (U = batch * hkv / that)
 
     @property
     def handle(self):
@@ -148,6 +151,19 @@ def la_plan_spec(batch, hq, hkv, d, nq, cu_seqlens_k, num_sms=0):
     h = ctypes.c_void_p()
     _check(_lib.la_plan_spec(batch, hq, hkv, d, int(nq), cu.ctypes.data_as(ctypes.c_void_p), int(num_sms),
                              ctypes.byref(h)), "la_plan_spec")
+    return Schedule(h.value, batch, hq, hkv, d, cu, nq=int(nq))
+
+
+def la_plan_kv(batch, hq, hkv, d, cu_seqlens_k, nq=1, heads_per_unit=0, tile_tokens=0, num_sms=0):
+    """Stream-K schedule for token-major / paged caches: units of heads_per_unit
+    kv heads (0: two when d is 64, 80 or 96 and hkv is even), tile_tokens tokens
+    of each head per tile (0: the default), nq query tokens per request."""
+    cu = _cu_array(cu_seqlens_k)
+    if cu.size != batch + 1:
+        raise ValueError("cu_seqlens_k must have batch + 1 entries")
+    h = ctypes.c_void_p()
+    _check(_lib.la_plan_kv(batch, hq, hkv, d, int(nq), cu.ctypes.data_as(ctypes.c_void_p), int(heads_per_unit),
+                           int(tile_tokens), int(num_sms), ctypes.byref(h)), "la_plan_kv")
     return Schedule(h.value, batch, hq, hkv, d, cu, nq=int(nq))
 
 
@@ -359,12 +375,16 @@ class LeanDecoder:
     """Convenience holder: a schedule, its workspace and the device offsets."""
 
     def __init__(self, batch, hq, hkv, d, cu_seqlens_k, num_sms=0, device="cuda", fixed_splits=None,
-                 auto=False, tile_tokens=0, out_dtype=None, nq=1):
+                 auto=False, tile_tokens=0, out_dtype=None, nq=1, heads_per_unit=None):
+        """heads_per_unit not None: plan with la_plan_kv (token-major / paged caches, 0 = its default)."""
         import torch
         self.predicted_us = None
         self.out_dtype = out_dtype or torch.float32
         self.nq = nq
-        if nq > 1:
+        if heads_per_unit is not None:
+            self.sched = la_plan_kv(batch, hq, hkv, d, cu_seqlens_k, nq, heads_per_unit, tile_tokens, num_sms)
+            self.kind = "lean"
+        elif nq > 1:
             self.sched, self.kind = la_plan_spec(batch, hq, hkv, d, nq, cu_seqlens_k, num_sms), "lean"
         elif auto:
             self.sched, self.kind, self.predicted_us = la_plan_auto(batch, hq, hkv, d, cu_seqlens_k, num_sms)

@@ -48,16 +48,18 @@ la_status check_shape(int batch, int hq, int hkv, int d, const int32_t* cu) {
   return LA_OK;
 }
 
-// Units (b, kv head) in request-major order and their tile prefix sums.
+// Units (b, kv head group of hp heads) in request-major order and their tile
+// prefix sums.
 bool build_units(la_schedule* s) {
-  s->U = s->batch * s->hkv;
+  const int groups = s->hkv / s->hp;
+  s->U = s->batch * groups;
   s->unit_iter.assign((size_t)s->U + 1, 0);
   int64_t acc = 0;
   for (int b = 0; b < s->batch; ++b) {
     const int64_t L = (int64_t)s->cu[b + 1] - s->cu[b];
     const int64_t tiles = (L + s->T - 1) / s->T;
-    for (int h = 0; h < s->hkv; ++h) {
-      s->unit_iter[(size_t)b * s->hkv + h] = (int32_t)acc;
+    for (int h = 0; h < groups; ++h) {
+      s->unit_iter[(size_t)b * groups + h] = (int32_t)acc;
       acc += tiles;
       if (acc > INT32_MAX) return false;
     }
@@ -145,7 +147,8 @@ void build_dev_segs(la_schedule* s) {
   for (size_t i = 0; i < n; ++i) {
     const int32_t* sg = &s->segs[i * la::kSegWords];
     int32_t* dv = &s->dev_segs[i * la::kDevSegWords];
-    const int b = sg[0] / s->hkv, kvh = sg[0] % s->hkv;
+    const int groups = s->hkv / s->hp;
+    const int b = sg[0] / groups, kvh = (sg[0] % groups) * s->hp;  // first kv head of the unit
     const int64_t L = (int64_t)s->cu[b + 1] - s->cu[b];
     const int64_t row0 = (int64_t)s->hkv * s->cu[b] + (int64_t)kvh * L;
     for (int w = 0; w < la::kSegWords; ++w) dv[w] = sg[w];
@@ -160,14 +163,15 @@ void build_dev_segs(la_schedule* s) {
 }
 
 la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, int kind, int grid_or_splits,
-                        la_schedule** out, int tile = 0) {
+                        la_schedule** out, int tile = 0, int hp = 1) {
   if (out == nullptr) return LA_ERR_INVALID;
   *out = nullptr;
   const la_status st = check_shape(batch, hq, hkv, d, cu);
   if (st != LA_OK) return st;
-  if (tile == 0) tile = la::default_tile(d);
+  if (hp < 1 || hkv % hp != 0) return LA_ERR_INVALID;
+  if (tile == 0) tile = la::default_tile(d) / hp;
   if (tile < 0) return LA_ERR_INVALID;
-  if (!la::tile_supported(d, tile)) return LA_ERR_UNSUPPORTED;
+  if (!la::tile_supported(d, tile, hp)) return LA_ERR_UNSUPPORTED;
   la_schedule* s = new (std::nothrow) la_schedule();
   if (s == nullptr) return LA_ERR_INVALID;
   s->batch = batch;
@@ -177,6 +181,7 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   s->grp = hq / hkv;
   s->nq = 1;
   s->R = s->grp;
+  s->hp = hp;
   s->T = tile;
   s->kind = kind;
   s->cu.assign(cu, cu + batch + 1);
@@ -201,20 +206,20 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   return LA_OK;
 }
 
-// CTAs per SM of the decode kernel, cached per (device, d, T, grp).
-la_status capacity(int d, int T, int grp, int* per_sm) {
+// CTAs per SM of the decode kernel, cached per (device, d, T, grp, hp).
+la_status capacity(int d, int T, int grp, int* per_sm, int hp = 1) {
   static std::mutex mu;
   static std::map<long long, int> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
-  const long long key = (((long long)dev * 1024 + d) * 1024 + T) * 16 + grp;
+  const long long key = ((((long long)dev * 1024 + d) * 1024 + T) * 16 + grp) * 4 + hp;
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it != cache.end()) {
     *per_sm = it->second;
     return LA_OK;
   }
-  cudaError_t e = la::decode_capacity(d, T, grp, per_sm);
+  cudaError_t e = la::decode_capacity(d, T, grp, hp, per_sm);
   if (e == cudaErrorInvalidValue) return LA_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return LA_ERR_CUDA;
   cache[key] = *per_sm;
@@ -294,10 +299,10 @@ double simulate_dispatch(const std::vector<double>& job_bytes, int slots, double
 
 // Bytes of K+V of tiles [t0, t1) of unit u.
 double piece_bytes(const la_schedule* s, int u, int t0, int t1) {
-  const int b = u / s->hkv;
+  const int b = u / (s->hkv / s->hp);
   const int64_t L = (int64_t)s->cu[b + 1] - s->cu[b];
   const int64_t tok = std::min<int64_t>((int64_t)t1 * s->T, L) - (int64_t)t0 * s->T;
-  return (double)tok * s->d * 2.0 * 2.0;
+  return (double)tok * s->hp * s->d * 2.0 * 2.0;
 }
 
 // Predicted time of a schedule: per-CTA byte totals through the dispatch model,
@@ -340,7 +345,9 @@ int default_tile(int d) {
   }
 }
 
-bool tile_supported(int d, int T) {
+bool tile_supported(int d, int T, int hp) {
+  if (hp == 2) return (d == 64 && T == 128) || ((d == 80 || d == 96) && T == 64);
+  if (hp != 1) return false;
   switch (d) {
     case 64: return T == 256 || T == 128;
     case 128: return T == 128 || T == 64;
@@ -351,7 +358,16 @@ bool tile_supported(int d, int T) {
   }
 }
 
-cudaError_t launch_decode(int d, int T, int grp, int dtype, const KParams& p, cudaStream_t st) {
+cudaError_t launch_decode(int d, int T, int grp, int hp, int dtype, const KParams& p, cudaStream_t st) {
+  if (hp == 2) {
+    switch (d) {
+      case 64: return launch_decode_d64_hp2(T, grp, dtype, p, st);
+      case 80: return launch_decode_d80_hp2(T, grp, dtype, p, st);
+      case 96: return launch_decode_d96_hp2(T, grp, dtype, p, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (hp != 1) return cudaErrorInvalidValue;
   switch (d) {
     case 64: return launch_decode_d64(T, grp, dtype, p, st);
     case 80: return launch_decode_d80(T, grp, dtype, p, st);
@@ -373,7 +389,16 @@ cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st) {
   }
 }
 
-cudaError_t decode_capacity(int d, int T, int grp, int* per_sm) {
+cudaError_t decode_capacity(int d, int T, int grp, int hp, int* per_sm) {
+  if (hp == 2) {
+    switch (d) {
+      case 64: return decode_capacity_d64_hp2(T, grp, per_sm);
+      case 80: return decode_capacity_d80_hp2(T, grp, per_sm);
+      case 96: return decode_capacity_d96_hp2(T, grp, per_sm);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (hp != 1) return cudaErrorInvalidValue;
   switch (d) {
     case 64: return decode_capacity_d64(T, grp, per_sm);
     case 80: return decode_capacity_d80(T, grp, per_sm);
@@ -425,14 +450,15 @@ cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, 
   return cudaSuccess;
 }
 
-cudaError_t encode_kv_maps_3d(const void* k, const void* v, long long rows, int hkv, int d, int bw, int box_rows,
-                              bool swizzle, int elem_type, CUtensorMap* mk, CUtensorMap* mv) {
+cudaError_t encode_kv_maps_3d(const void* k, const void* v, long long rows, int hkv, int d, int bw, int hp,
+                              int box_rows, bool swizzle, int elem_type, CUtensorMap* mk, CUtensorMap* mv) {
   const EncodeTiled fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
   if (rows <= 0 || rows > (1LL << 31) - 1) return cudaErrorInvalidValue;
+  if (hp < 1 || hkv % hp != 0) return cudaErrorInvalidValue;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)rows};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hkv * d * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)bw, 1, (cuuint32_t)box_rows};
+  const cuuint32_t box[3] = {(cuuint32_t)bw, (cuuint32_t)hp, (cuuint32_t)box_rows};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE;
   if (swizzle)
@@ -504,6 +530,40 @@ la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t*
   return LA_OK;
 }
 
+la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* cu_seqlens_k, int heads_per_unit,
+                     int tile_tokens, int num_sms, la_schedule** out) {
+  if (out != nullptr) *out = nullptr;
+  if (out == nullptr) return LA_ERR_INVALID;
+  la_status st = check_shape(batch, hq, hkv, d, cu_seqlens_k);
+  if (st != LA_OK) return st;
+  if (nq < 1 || tile_tokens < 0) return LA_ERR_INVALID;
+  int hp = heads_per_unit;
+  if (hp == 0) hp = ((d == 64 || d == 80 || d == 96) && hkv % 2 == 0) ? 2 : 1;
+  if ((hp != 1 && hp != 2) || hkv % hp != 0) return LA_ERR_INVALID;
+  const int rows = (hq / hkv) * nq;
+  if (rows > 8) return LA_ERR_UNSUPPORTED;
+  for (int b = 0; b < batch; ++b)
+    if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
+  const int R = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  const int T = tile_tokens == 0 ? la::default_tile(d) / hp : tile_tokens;
+  if (!la::tile_supported(d, T, hp)) return LA_ERR_UNSUPPORTED;
+  int G = num_sms;
+  if (G <= 0) {
+    int sms = 0, per_sm = 0;
+    st = device_sms(&sms);
+    if (st != LA_OK) return st;
+    st = capacity(d, T, R, &per_sm, hp);
+    if (st != LA_OK) return st;
+    G = sms * std::max(1, per_sm);
+  }
+  if (G > kMaxGrid) return LA_ERR_INVALID;
+  st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out, T, hp);
+  if (st != LA_OK) return st;
+  (*out)->nq = nq;
+  (*out)->R = R;
+  return LA_OK;
+}
+
 la_status la_plan_fixed(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int splits,
                         la_schedule** out) {
   if (out != nullptr) *out = nullptr;
@@ -555,7 +615,7 @@ int la_schedule_grid(const la_schedule* s) { return s ? s->G : -1; }
 
 size_t la_workspace_size(const la_schedule* s) {
   if (s == nullptr) return 0;
-  return la::workspace_bytes(s->G, s->d, s->R);
+  return la::workspace_bytes(s->G, s->d, s->R * s->hp);
 }
 
 la_status la_workspace_init(void* workspace, size_t bytes, la_stream_t stream) {
@@ -592,12 +652,13 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
   } else if (kv->layout != LA_KV_SLAB) {
     return LA_ERR_INVALID;
   }
+  if (kv_layout == la::kKvSlab && sc->hp != 1) return LA_ERR_UNSUPPORTED;  // units of several heads: caches only
   if (kv_layout != la::kKvSlab) {
     // TMA destinations: 1024-byte aligned pieces when swizzled (tensor-core
     // path), 128-byte aligned rows otherwise.
     const bool tc = sc->R >= 4;
     const int w = sc->d % 64 == 0 ? 64 : (sc->d % 32 == 0 ? 32 : 16);
-    const long long piece = tc ? (long long)box_rows * w * 2 : (long long)box_rows * sc->d * 2;
+    const long long piece = (tc ? (long long)box_rows * w * 2 : (long long)box_rows * sc->d * 2) * sc->hp;
     if (piece % (tc ? 1024 : 128) != 0) return LA_ERR_UNSUPPORTED;
   }
   if (sc == nullptr || q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
@@ -614,7 +675,7 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
     int sms = 0, per_sm = 0;
     la_status e = device_sms(&sms);
     if (e != LA_OK) return e;
-    e = capacity(s->d, s->T, s->R, &per_sm);
+    e = capacity(s->d, s->T, s->R, &per_sm, s->hp);
     if (e != LA_OK) return e;
     if ((int64_t)s->G > (int64_t)sms * per_sm) return LA_ERR_INVALID;
   }
@@ -657,7 +718,7 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
   p.grp = s->grp;
   p.nq = s->nq;
   p.rows = s->grp * s->nq;
-  cudaError_t ce = la::launch_decode(s->d, s->T, s->R, dtype, p, st);
+  cudaError_t ce = la::launch_decode(s->d, s->T, s->R, s->hp, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {
     la::CParams c;

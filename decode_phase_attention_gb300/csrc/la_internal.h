@@ -16,7 +16,7 @@ enum SegKind : int32_t { kWhole = 0, kNonHost = 1, kHost = 2, kPartial = 3 };
 // the request's context length and the slab's first K/V row (64-bit), so the
 // producer can issue its first copy after two dependent loads.
 constexpr int kSegWords = 5;
-// unit, t0, t1, kind, peer, L, row0 low, row0 high, cu[b], b, kv head, 0
+// unit, t0, t1, kind, peer, L, row0 low, row0 high, cu[b], b, first kv head of the unit, 0
 constexpr int kDevSegWords = 12;
 
 // Where the K/V rows of a (request, kv head, token) live.
@@ -27,15 +27,16 @@ enum KvLayout : int {
 };
 
 // Workspace: a 256-byte header, G ready flags (padded to 256 bytes), then G
-// partial records of grp * (d + 2) floats: per query head [m, l, O[d]].
+// partial records of rows * (d + 2) floats: per query row [m, l, O[d]]
+// (rows = the instance's rows per kv head x kv heads per unit).
 constexpr size_t kHeaderBytes = 256;
 enum HeaderWord { kEpoch = 0, kDone = 1, kStatus = 2, kInfoCta = 3, kInfoPeer = 4 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline size_t flags_bytes(int G) { return align_up(sizeof(uint32_t) * (size_t)G, 256); }
-inline size_t record_floats(int d, int grp) { return (size_t)grp * (size_t)(d + 2); }
-inline size_t workspace_bytes(int G, int d, int grp) {
-  return kHeaderBytes + flags_bytes(G) + sizeof(float) * record_floats(d, grp) * (size_t)G;
+inline size_t record_floats(int d, int rows) { return (size_t)rows * (size_t)(d + 2); }
+inline size_t workspace_bytes(int G, int d, int rows) {
+  return kHeaderBytes + flags_bytes(G) + sizeof(float) * record_floats(d, rows) * (size_t)G;
 }
 
 struct KParams {
@@ -99,16 +100,18 @@ struct CParams {            // fixed-split merge launch
   int rows = 1;             // grp * nq
 };
 
-// LeanTile sizes: the default per head dim, and whether (d, T) is built.
+// LeanTile sizes: the default per head dim, and whether (d, T) is built for
+// units of hp kv heads (T tokens of each head per tile).
 int default_tile(int d);
-bool tile_supported(int d, int T);
+bool tile_supported(int d, int T, int hp = 1);
 
-// Launches (la_kernels_d<d>.cu, one file per head dim). dtype: 0 fp16, 1 bf16.
-// cudaErrorInvalidValue for a (d, T, grp) that is not built.
-cudaError_t launch_decode(int d, int T, int grp, int dtype, const KParams& p, cudaStream_t st);
+// Launches (la_kernels_d<d>.cu, one file per head dim; la_kernels_d<d>_hp2.cu
+// for units of two kv heads). dtype: 0 fp16, 1 bf16.
+// cudaErrorInvalidValue for a (d, T, grp, hp) that is not built.
+cudaError_t launch_decode(int d, int T, int grp, int hp, int dtype, const KParams& p, cudaStream_t st);
 cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st);
 // CTAs of the decode kernel one SM holds at once (cudaOccupancy...).
-cudaError_t decode_capacity(int d, int T, int grp, int* per_sm);
+cudaError_t decode_capacity(int d, int T, int grp, int hp, int* per_sm);
 #define LA_DECLARE_HEAD_DIM(D)                                                           \
   cudaError_t launch_decode_d##D(int T, int grp, int dtype, const KParams& p, cudaStream_t st); \
   cudaError_t launch_combine_d##D(int grp, const CParams& p, cudaStream_t st);           \
@@ -119,5 +122,12 @@ LA_DECLARE_HEAD_DIM(96)
 LA_DECLARE_HEAD_DIM(128)
 LA_DECLARE_HEAD_DIM(256)
 #undef LA_DECLARE_HEAD_DIM
+#define LA_DECLARE_HEAD_DIM_HP2(D)                                                            \
+  cudaError_t launch_decode_d##D##_hp2(int T, int grp, int dtype, const KParams& p, cudaStream_t st); \
+  cudaError_t decode_capacity_d##D##_hp2(int T, int grp, int* per_sm);
+LA_DECLARE_HEAD_DIM_HP2(64)
+LA_DECLARE_HEAD_DIM_HP2(80)
+LA_DECLARE_HEAD_DIM_HP2(96)
+#undef LA_DECLARE_HEAD_DIM_HP2
 
 }  // namespace la

@@ -226,15 +226,17 @@ struct Elem<__half> {
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
-template <int D, int T_, int GRP>
+template <int D, int T_, int GRP, int HP = 1>
 struct Cfg {
-  static constexpr int T = T_;                      // LeanTile tokens
+  static constexpr int T = T_;                      // LeanTile tokens (of each kv head of the unit)
+  static constexpr int ROWS = T * HP;               // K (and V) rows of a tile: T tokens x HP kv heads
   static constexpr bool TC = (GRP >= 4);            // tensor-core tile path
   // consumer warps: 8, or fewer when an MMA tile of 16 tokens per warp needs it
-  static constexpr int NCW = TC ? cmin(8, T / 16) : 8;
+  static constexpr int NCW = TC ? cmin(8, ROWS / 16) : 8;
   static constexpr int NCT = NCW * 32;              // consumer threads
   static constexpr int NTHREADS = NCT + 32;         // + producer warp
-  static constexpr int TPW = T / NCW;               // tokens per warp per tile
+  static constexpr int WPH = NCW / HP;              // consumer warps per kv head of the unit
+  static constexpr int TPW = T / WPH;               // tokens per warp per tile
   // CUDA-core path: d/8 active lanes per token (16 bytes each), rounded up
   // to a power-of-two lane group; the spare lanes of a group idle.
   static constexpr int ACT = D / 8;
@@ -248,7 +250,7 @@ struct Cfg {
   static constexpr int NB = D / W;                  // boxes per tile per tensor
   static constexpr int MT = TPW / 16;               // 16-token MMA tiles per warp
   static constexpr int KS = D / 16;                 // 16-wide steps over the head dim
-  static constexpr int TILE_ELEMS = T * D;
+  static constexpr int TILE_ELEMS = ROWS * D;
   static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
   static constexpr int STAGES = cmax(2, cmin(4, 196608 / STAGE_BYTES));
   static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
@@ -256,8 +258,10 @@ struct Cfg {
   static constexpr size_t MERGE_BYTES = (size_t)NCW * GRP * REC * 4;
   static constexpr size_t BAR_BYTES = 2 * STAGES * 8 + 16;
   static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
-  static constexpr int ITEMS = (GRP * D + NCT - 1) / NCT;  // (head, dim) outputs per consumer thread
+  static constexpr int ITEMS = (HP * GRP * D + NCT - 1) / NCT;  // (row, dim) outputs per consumer thread
+  static constexpr int PB = cmax(1, 16 / ITEMS);     // peer records per batch of host-merge loads
   static_assert(D % 16 == 0 && T % 16 == 0, "tile shape");
+  static_assert((HP == 1 || HP == 2) && NCW % HP == 0 && T % WPH == 0, "kv heads per unit");
   static_assert(STEPS % CH == 0 && TPW % TPS == 0, "CUDA-core tile shape");
   static_assert(!TC || (TPW % 16 == 0 && GRP <= 8), "tensor-core tile shape");
   static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -317,14 +321,17 @@ __device__ __forceinline__ bool unit_offsets_ok(const KParams& p, int b) {
 }
 
 // ------------------------------------------------------------------ producer
-template <int D, int T, int GRP, typename E>
+template <int D, int T, int GRP, typename E, int HP>
 __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, int g,
                                         E* kv, uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
   // Run by the whole producer warp. Lane 0 posts byte counts and issues the
   // slab-layout copies; for token-major and paged caches lane i issues the
   // load of the i-th piece of a tile (a tile spans up to T / 16 pages), so
-  // small pages do not serialise on one thread.
-  using C = Cfg<D, T, GRP>;
+  // small pages do not serialise on one thread. A unit of HP > 1 kv heads
+  // (token-major and paged caches only) loads the HP heads of each token
+  // row together: HP * d contiguous elements per row, kept interleaved in
+  // shared memory (tile row = token * HP + head).
+  using C = Cfg<D, T, GRP, HP>;
   const int lane = threadIdx.x & 31;
   const bool leader = lane == 0;
   const uint64_t pol = l2_evict_first_policy();
@@ -378,23 +385,24 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
       E* ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
       if (tma3) {
         // Token-major or paged cache, seen as [rows, hkv, d]: box_rows token
-        // rows of one kv head per load; the consumers mask the tail tokens.
-        if (leader) mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * nload * br * D * 2));
+        // rows of the unit's HP kv heads per load; the consumers mask the
+        // tail tokens.
+        if (leader) mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * nload * br * HP * D * 2));
         __syncwarp();
         if (lane < nload) {
           if (C::TC) {
 #pragma unroll
             for (int bk = 0; bk < C::NB; ++bk) {
-              tma_load_3d(ks + bk * C::T * C::W + lane * br * C::W, tmk, bk * C::W, kvh, row, &full[stage], pol);
-              tma_load_3d(ks + C::TILE_ELEMS + bk * C::T * C::W + lane * br * C::W, tmv, bk * C::W, kvh, row,
-                          &full[stage], pol);
+              const int off = bk * C::ROWS * C::W + lane * br * HP * C::W;
+              tma_load_3d(ks + off, tmk, bk * C::W, kvh, row, &full[stage], pol);
+              tma_load_3d(ks + C::TILE_ELEMS + off, tmv, bk * C::W, kvh, row, &full[stage], pol);
             }
           } else {
-            tma_load_3d(ks + lane * br * D, tmk, 0, kvh, row, &full[stage], pol);
-            tma_load_3d(ks + C::TILE_ELEMS + lane * br * D, tmv, 0, kvh, row, &full[stage], pol);
+            tma_load_3d(ks + lane * br * HP * D, tmk, 0, kvh, row, &full[stage], pol);
+            tma_load_3d(ks + C::TILE_ELEMS + lane * br * HP * D, tmv, 0, kvh, row, &full[stage], pol);
           }
         }
-      } else if (leader) {
+      } else if (HP == 1 && leader) {  // slab layout: the host accepts only HP = 1
         if (C::TC) {
           // Whole boxes of T rows: rows past the slab are the next slab's (or
           // zero fill past the tensor) and are masked by the consumers.
@@ -456,13 +464,15 @@ __device__ __forceinline__ bool wait_tile(const KParams& p, int g, uint64_t* ful
 // ----------------------------------------------- CUDA-core tile path (grp 1, 2)
 // Runs the segment's tiles and leaves this warp's (m, l, O) for every head
 // of the group in its slot of the merge area.
-template <int D, int T, int GRP, typename E>
-__device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, int kvh, long long L, int t0,
+template <int D, int T, int GRP, typename E, int HP>
+__device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, int kvh0, long long L, int t0,
                                                 int n_tiles, bool ok, const E* kv, uint64_t* full, uint64_t* empty,
                                                 int& stage, uint32_t& phase, volatile int* abort_flag,
                                                 float* wrec) {
-  using C = Cfg<D, T, GRP>;
+  using C = Cfg<D, T, GRP, HP>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hh = warp / C::WPH;   // kv head of the unit this warp works on
+  const int kvh = kvh0 + hh;
   const int gl = lane % C::LPT;   // which 8-element chunk of the row
   const int ts = lane / C::LPT;   // which token of the warp step
   const bool act = gl < C::ACT;   // spare lanes of a group (d = 80, 96) idle
@@ -497,14 +507,14 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
     if (wait_tile<D, T, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
       const E* Ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
       const E* Vs = Ks + C::TILE_ELEMS;
-      const int wtok = warp * C::TPW;
+      const int wtok = (warp % C::WPH) * C::TPW;
 #pragma unroll
       for (int c = 0; c < C::STEPS; c += C::CH) {
         float s[C::CH][GRP];
 #pragma unroll
         for (int st = 0; st < C::CH; ++st) {
           const int tok = wtok + (c + st) * C::TPS + ts;
-          const uint4 raw = act ? *reinterpret_cast<const uint4*>(Ks + tok * D + c0) : zero4;
+          const uint4 raw = act ? *reinterpret_cast<const uint4*>(Ks + (tok * HP + hh) * D + c0) : zero4;
           float kf[8];
           Elem<E>::to_f32(raw, kf);
 #pragma unroll
@@ -560,7 +570,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
         for (int st = 0; st < C::CH; ++st) {
           const int tok = wtok + (c + st) * C::TPS + ts;
           if (tok < ntok && act) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(Vs + tok * D + c0);
+            const uint4 raw = *reinterpret_cast<const uint4*>(Vs + (tok * HP + hh) * D + c0);
             float vf[8];
             Elem<E>::to_f32(raw, vf);
 #pragma unroll
@@ -615,20 +625,22 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
 // -------------------------------------------- tensor-core tile path (grp 4, 8)
 // Swizzled shared-memory address (128-byte swizzle: 16-byte chunk c of row r
 // sits at chunk c ^ (r mod 8)) of row `row`, chunk `c` of 64-column block bk.
-template <int D, int T, int GRP>
+template <int D, int T, int GRP, int HP>
 __device__ __forceinline__ uint32_t swz(uint32_t tile_base, int bk, int row, int c) {
-  using C = Cfg<D, T, GRP>;
-  return tile_base + (uint32_t)(bk * C::T * C::RB + row * C::RB +
+  using C = Cfg<D, T, GRP, HP>;
+  return tile_base + (uint32_t)(bk * C::ROWS * C::RB + row * C::RB +
                                 ((c ^ ((row * C::RB >> 7) & (C::RB / 16 - 1))) << 4));
 }
 
-template <int D, int T, int GRP, typename E>
-__device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, int kvh, long long L, int t0,
+template <int D, int T, int GRP, typename E, int HP>
+__device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, int kvh0, long long L, int t0,
                                                 int n_tiles, bool ok, const E* kv, uint64_t* full, uint64_t* empty,
                                                 int& stage, uint32_t& phase, volatile int* abort_flag,
                                                 float* wrec) {
-  using C = Cfg<D, T, GRP>;
+  using C = Cfg<D, T, GRP, HP>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hh = warp / C::WPH;   // kv head of the unit this warp works on
+  const int kvh = kvh0 + hh;
   const int gq = lane >> 2;  // fragment row group
   const int tq = lane & 3;   // fragment column pair
   // B operand of S = K q^T: q^T (16 dims x 8 heads), raw q bits; heads past
@@ -661,18 +673,18 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
     if (wait_tile<D, T, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
       const uint32_t kb = kv_base + (uint32_t)(stage * 2 * C::TILE_ELEMS * 2);
       const uint32_t vb = kb + (uint32_t)(C::TILE_ELEMS * 2);
-      const int wtok = warp * C::TPW;
+      const int wtok = (warp % C::WPH) * C::TPW;
       // S = K q^T for the warp's TPW tokens: MT tiles of 16 tokens x 8 heads
       float s[C::MT][4];
 #pragma unroll
       for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) s[mt][i] = 0.f;
-        const int row = wtok + mt * 16 + (lane & 15);
+        const int row = (wtok + mt * 16 + (lane & 15)) * HP + hh;
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
           uint32_t a[4];
-          ldsm_x4(a, swz<D, T, GRP>(kb, ks * 16 / C::W, row, (ks * 16 % C::W) / 8 + (lane >> 4)));
+          ldsm_x4(a, swz<D, T, GRP, HP>(kb, ks * 16 / C::W, row, (ks * 16 % C::W) / 8 + (lane >> 4)));
           Elem<E>::mma(s[mt], a, qb[ks][0], qb[ks][1]);
         }
       }
@@ -717,10 +729,11 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
       if (ntok < C::T && wtok + C::TPW > ntok) {
         constexpr int CHUNKS = C::RB / 16;  // 16-byte chunks per row and box
         for (int idx = lane; idx < C::TPW * C::NB * CHUNKS; idx += 32) {
-          const int row = wtok + idx / (C::NB * CHUNKS);
+          const int tok = wtok + idx / (C::NB * CHUNKS);
           const int rest = idx % (C::NB * CHUNKS);
-          if (row >= ntok) {
-            const uint32_t a = vb + (uint32_t)((rest / CHUNKS) * C::T * C::RB + row * C::RB + (rest % CHUNKS) * 16);
+          if (tok >= ntok) {
+            const uint32_t a = vb + (uint32_t)((rest / CHUNKS) * C::ROWS * C::RB + (tok * HP + hh) * C::RB +
+                                               (rest % CHUNKS) * 16);
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
           }
         }
@@ -743,11 +756,11 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
         const uint32_t l23 = Elem<E>::pack(pv[2] - f23.x, pv[3] - f23.y);
         const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
         const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-        const int vrow = wtok + mt * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int vrow = (wtok + mt * 16 + (lane & 7) + ((lane >> 4) << 3)) * HP + hh;
 #pragma unroll
         for (int dm = 0; dm < C::KS; ++dm) {
           uint32_t a[4];
-          ldsm_x4_trans(a, swz<D, T, GRP>(vb, dm * 16 / C::W, vrow, (dm * 16 % C::W) / 8 + ((lane >> 3) & 1)));
+          ldsm_x4_trans(a, swz<D, T, GRP, HP>(vb, dm * 16 / C::W, vrow, (dm * 16 % C::W) / 8 + ((lane >> 3) & 1)));
           Elem<E>::mma(o[dm], a, bh0, bh1);
           Elem<E>::mma(o[dm], a, bl0, bl1);
         }
@@ -787,21 +800,23 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
 }
 
 // ------------------------------------------------------------------ consumers
-template <int D, int T, int GRP, typename E>
+template <int D, int T, int GRP, typename E, int HP>
 __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, uint64_t* full, uint64_t* empty,
                                         float* mrg, volatile int* abort_flag, uint32_t epoch) {
-  using C = Cfg<D, T, GRP>;
+  using C = Cfg<D, T, GRP, HP>;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
   const uint32_t ready = epoch + 1u;
+  const int nitems = HP * p.rows * D;  // outputs of a unit: (kv head of the unit, row, dim)
   int stage = 0;
   uint32_t phase = 0;
 
   for (int si = s_begin; si < s_end; ++si) {
     const int4 w0 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords);
     const int4 w1 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 4);
+    const int4 w2 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 8);
     const int unit = w0.x, t0 = w0.y, t1 = w0.z, kind = w0.w, peer = w1.x;
-    const int b = unit / p.hkv, kvh = unit % p.hkv;
+    const int b = w2.y, kvh0 = w2.z;  // request, first kv head of the unit
     // Device offsets that disagree with the schedule: the tiles are still
     // taken from the ring (the producer streams them) but not used, and the
     // unit's outputs are NaN.
@@ -813,11 +828,11 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
     // ---- the LeanTile loop; leaves this warp's (m, l, O) in the merge area
     float* wrec = mrg + (size_t)warp * GRP * C::REC;
     if constexpr (C::TC)
-      warp_segment_tc<D, T, GRP, E>(p, g, b, kvh, L, t0, n_tiles, ok, kv, full, empty, stage, phase, abort_flag,
-                                 wrec);
+      warp_segment_tc<D, T, GRP, E, HP>(p, g, b, kvh0, L, t0, n_tiles, ok, kv, full, empty, stage, phase,
+                                        abort_flag, wrec);
     else
-      warp_segment_cc<D, T, GRP, E>(p, g, b, kvh, L, t0, n_tiles, ok, kv, full, empty, stage, phase, abort_flag,
-                                 wrec);
+      warp_segment_cc<D, T, GRP, E, HP>(p, g, b, kvh0, L, t0, n_tiles, ok, kv, full, empty, stage, phase,
+                                        abort_flag, wrec);
     if (p.trace != nullptr && tid == 0) {
       unsigned long long* tr = p.trace + (size_t)g * kTraceWords;
       tr[kTrTilesDone] = global_ns();
@@ -825,7 +840,8 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
     }
     consumer_sync(C::NCT);
 
-    // ---- merge the 8 warps with f: thread -> (head j, dim c) items
+    // ---- merge the warps of each kv head with f: thread -> (head, row, dim)
+    // items; a record row is hh * GRP + j
     float M[C::ITEMS], Lsum[C::ITEMS], O[C::ITEMS];
 #pragma unroll
     for (int i = 0; i < C::ITEMS; ++i) {
@@ -833,16 +849,18 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
       M[i] = -INFINITY;
       Lsum[i] = 0.f;
       O[i] = 0.f;
-      if (idx < p.rows * D) {
-        const int j = idx / D, cc = idx % D;
+      if (idx < nitems) {
+        const int hr = idx / D, cc = idx % D;
+        const int hh = hr / p.rows, j = hr % p.rows;
+        const float* base = mrg + ((size_t)hh * C::WPH * GRP + j) * C::REC;
         float mm = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < C::NCW; ++w) mm = fmaxf(mm, mrg[(w * GRP + j) * C::REC]);
+        for (int w = 0; w < C::WPH; ++w) mm = fmaxf(mm, base[w * GRP * C::REC]);
         if (mm != -INFINITY) {
           float ls = 0.f, os = 0.f;
 #pragma unroll
-          for (int w = 0; w < C::NCW; ++w) {
-            const float* r = mrg + (w * GRP + j) * C::REC;
+          for (int w = 0; w < C::WPH; ++w) {
+            const float* r = base + w * GRP * C::REC;
             const float wt = (r[0] == -INFINITY) ? 0.f : ex2(r[0] - mm);
             ls = fmaf(wt, r[1], ls);
             os = fmaf(wt, r[2 + cc], os);
@@ -856,13 +874,13 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
     const bool poisoned = (*abort_flag != 0) || !ok;
 
     if (kind == kNonHost || kind == kPartial) {
-      float* rec = p.recs + (size_t)g * GRP * C::REC;
+      float* rec = p.recs + (size_t)g * HP * GRP * C::REC;
 #pragma unroll
       for (int i = 0; i < C::ITEMS; ++i) {
         const int idx = tid + i * C::NCT;
-        if (idx < p.rows * D) {
-          const int j = idx / D, cc = idx % D;
-          float* r = rec + j * C::REC;
+        if (idx < nitems) {
+          const int hr = idx / D, cc = idx % D;
+          float* r = rec + ((hr / p.rows) * GRP + hr % p.rows) * C::REC;
           r[2 + cc] = O[i];
           if (cc == 0) {
             r[0] = poisoned ? __int_as_float(0x7fc00000) : M[i];
@@ -901,34 +919,39 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
         if (*abort_flag) {
           fail = true;
         } else {
-          // merge the peers' partials with f, loading four records at a time
+          // merge the peers' partials with f: the loads of PB peers for all of
+          // this thread's outputs are issued before any of them is used, so a
+          // batch costs one L2 round trip
+          for (int p0 = 0; p0 < npeer; p0 += C::PB) {
+            float m2[C::ITEMS][C::PB], l2[C::ITEMS][C::PB], o2[C::ITEMS][C::PB];
 #pragma unroll
-          for (int i = 0; i < C::ITEMS; ++i) {
-            const int idx = tid + i * C::NCT;
-            if (idx >= p.rows * D) continue;
-            const int j = idx / D, cc = idx % D;
-            for (int p0 = 0; p0 < npeer; p0 += 4) {
-              float m2[4], l2[4], o2[4];
+            for (int i = 0; i < C::ITEMS; ++i) {
+              const int idx = tid + i * C::NCT;
+              const int hr = idx / D, cc = idx % D;
+              const int rr = (hr / p.rows) * GRP + hr % p.rows;
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                m2[u] = -INFINITY;
-                l2[u] = 0.f;
-                o2[u] = 0.f;
-                if (p0 + u < npeer) {
-                  const float* r = p.recs + ((size_t)(g + 1 + p0 + u) * GRP + j) * C::REC;
-                  m2[u] = __ldcg(r);
-                  l2[u] = __ldcg(r + 1);
-                  o2[u] = __ldcg(r + 2 + cc);
+              for (int u = 0; u < C::PB; ++u) {
+                m2[i][u] = -INFINITY;
+                l2[i][u] = 0.f;
+                o2[i][u] = 0.f;
+                if (idx < nitems && p0 + u < npeer) {
+                  const float* r = p.recs + ((size_t)(g + 1 + p0 + u) * HP * GRP + rr) * C::REC;
+                  m2[i][u] = __ldcg(r);
+                  l2[i][u] = __ldcg(r + 1);
+                  o2[i][u] = __ldcg(r + 2 + cc);
                 }
               }
+            }
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float mn = fmaxf(M[i], m2[u]);
+            for (int i = 0; i < C::ITEMS; ++i) {
+#pragma unroll
+              for (int u = 0; u < C::PB; ++u) {
+                const float mn = fmaxf(M[i], m2[i][u]);
                 if (mn == -INFINITY) continue;
                 const float a = (M[i] == -INFINITY) ? 0.f : ex2(M[i] - mn);
-                const float bw = (m2[u] == -INFINITY) ? 0.f : ex2(m2[u] - mn);
-                Lsum[i] = a * Lsum[i] + bw * l2[u];
-                O[i] = a * O[i] + bw * o2[u];
+                const float bw = (m2[i][u] == -INFINITY) ? 0.f : ex2(m2[i][u] - mn);
+                Lsum[i] = a * Lsum[i] + bw * l2[i][u];
+                O[i] = a * O[i] + bw * o2[i][u];
                 M[i] = mn;  // a NaN m2 (poisoned partial) propagates through bw
               }
             }
@@ -939,10 +962,10 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
 #pragma unroll
       for (int i = 0; i < C::ITEMS; ++i) {
         const int idx = tid + i * C::NCT;
-        if (idx < p.rows * D) {
-          const int j = idx / D, cc = idx % D;
+        if (idx < nitems) {
+          const int hr = idx / D, cc = idx % D;
           const float val = fail ? __int_as_float(0x7fc00000) : O[i] / Lsum[i];
-          store_out(p.out, row_index(p, b, kvh, j) * D + cc, val, p.out_dtype);
+          store_out(p.out, row_index(p, b, kvh0 + hr / p.rows, hr % p.rows) * D + cc, val, p.out_dtype);
         }
       }
     }
@@ -951,11 +974,11 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
 }
 
 // -------------------------------------------------------------------- kernel
-template <int D, int T, int GRP, typename E>
-__global__ void __launch_bounds__(Cfg<D, T, GRP>::NTHREADS, 1)
+template <int D, int T, int GRP, typename E, int HP>
+__global__ void __launch_bounds__(Cfg<D, T, GRP, HP>::NTHREADS, 1)
     lean_decode_kernel(const KParams p, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv) {
-  using C = Cfg<D, T, GRP>;
+  using C = Cfg<D, T, GRP, HP>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // swizzled TMA tiles need 1024-byte aligned destinations, plain ones 128
   unsigned char* smem =
@@ -989,9 +1012,9 @@ __global__ void __launch_bounds__(Cfg<D, T, GRP>::NTHREADS, 1)
   const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr[kEpoch]);
 
   if ((tid >> 5) == C::NCW) {
-    produce<D, T, GRP, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
+    produce<D, T, GRP, E, HP>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
   } else {
-    consume<D, T, GRP, E>(p, g, kv, full, empty, mrg, flags_smem, epoch);
+    consume<D, T, GRP, E, HP>(p, g, kv, full, empty, mrg, flags_smem, epoch);
   }
   __syncthreads();
   if (tid == 0) {
@@ -1041,20 +1064,20 @@ __global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
 cudaError_t encode_kv_maps(const void* k, const void* v, long long rows, int d, int T, int W, int elem_type,
                            CUtensorMap* mk, CUtensorMap* mv);
 // Tensor maps of a token-major or paged cache seen as [rows, hkv, d]: boxes
-// of bw columns x 1 head x box_rows rows; swizzled over bw * 2 bytes when
+// of bw columns x hp heads x box_rows rows; swizzled over bw * 2 bytes when
 // swizzle is set (tensor-core path), plain rows otherwise.
-cudaError_t encode_kv_maps_3d(const void* k, const void* v, long long rows, int hkv, int d, int bw, int box_rows,
-                              bool swizzle, int elem_type, CUtensorMap* mk, CUtensorMap* mv);
+cudaError_t encode_kv_maps_3d(const void* k, const void* v, long long rows, int hkv, int d, int bw, int hp,
+                              int box_rows, bool swizzle, int elem_type, CUtensorMap* mk, CUtensorMap* mv);
 
-template <int D, int T, int GRP, typename E>
+template <int D, int T, int GRP, typename E, int HP = 1>
 cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
-  using C = Cfg<D, T, GRP>;
+  using C = Cfg<D, T, GRP, HP>;
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(lean_decode_kernel<D, T, GRP, E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(lean_decode_kernel<D, T, GRP, E, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM);
     if (e != cudaSuccess) return e;
     configured_device = dev;
@@ -1062,9 +1085,11 @@ cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
   if (p.G <= 0) return cudaSuccess;
   CUtensorMap mk, mv;
   if (p.kv_layout != kKvSlab) {
-    e = encode_kv_maps_3d(p.k, p.v, p.kv_rows, p.hkv, D, C::TC ? C::W : D, p.box_rows, C::TC,
+    e = encode_kv_maps_3d(p.k, p.v, p.kv_rows, p.hkv, D, C::TC ? C::W : D, HP, p.box_rows, C::TC,
                           (int)Elem<E>::kTmaType, &mk, &mv);
     if (e != cudaSuccess) return e;
+  } else if (HP != 1) {
+    return cudaErrorInvalidValue;  // units of several kv heads read token-major or paged caches only
   } else if (C::TC) {
     e = encode_kv_maps(p.k, p.v, p.kv_rows, D, C::T, C::W, (int)Elem<E>::kTmaType, &mk, &mv);
     if (e != cudaSuccess) return e;
@@ -1072,17 +1097,17 @@ cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
   }
-  lean_decode_kernel<D, T, GRP, E><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
+  lean_decode_kernel<D, T, GRP, E, HP><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
   return cudaGetLastError();
 }
 
-template <int D, int T, int GRP>
+template <int D, int T, int GRP, int HP = 1>
 cudaError_t capacity_t(int* per_sm) {
-  using C = Cfg<D, T, GRP>;
-  cudaError_t e = cudaFuncSetAttribute(lean_decode_kernel<D, T, GRP, __nv_bfloat16>,
+  using C = Cfg<D, T, GRP, HP>;
+  cudaError_t e = cudaFuncSetAttribute(lean_decode_kernel<D, T, GRP, __nv_bfloat16, HP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lean_decode_kernel<D, T, GRP, __nv_bfloat16>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lean_decode_kernel<D, T, GRP, __nv_bfloat16, HP>,
                                                        C::NTHREADS, C::SMEM);
 }
 

@@ -84,6 +84,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
     return LA_ERR_INVALID;
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return LA_ERR_INVALID;
   const la_schedule* s = sc;
+  if (s->hp != 1) return LA_ERR_UNSUPPORTED;  // units of several kv heads read token-major or paged caches
   const Layout L = layout_of(s);
   if (L.total > kStaticScratchBytes) return LA_ERR_WORKSPACE;  // schedule too large for the fixed array
 
@@ -91,7 +92,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
     int per_sm = 0, sms = 0;
     la_status e = la_device_capacity(s->d, s->grp, &per_sm, &sms);
     if (e != LA_OK) return e;
-    if (la::decode_capacity(s->d, s->T, s->R, &per_sm) != cudaSuccess) return LA_ERR_CUDA;
+    if (la::decode_capacity(s->d, s->T, s->R, 1, &per_sm) != cudaSuccess) return LA_ERR_CUDA;
     if ((long long)s->G > (long long)per_sm * sms) return LA_ERR_INVALID;
   }
   int dev = 0;
@@ -135,7 +136,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   p.grp = s->grp;
   p.nq = s->nq;
   p.rows = s->grp * s->nq;
-  cudaError_t ce = la::launch_decode(s->d, s->T, s->R, dtype, p, st);
+  cudaError_t ce = la::launch_decode(s->d, s->T, s->R, 1, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {
     la::CParams c;

@@ -258,6 +258,37 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
                        void* workspace, void* out, la_dtype_out out_dt, float scale, la_stream_t stream);
 
 /*
+ * la_plan_kv -- stream-K schedule for a token-major or paged cache whose
+ * rows of one kv head are short (d * 2 bytes < 256, i.e. d = 64, 80, 96).
+ * The paper has no counterpart: its units are single (request, head) pairs
+ * over a [batch, heads, seq_len, head_dim] layout. In a token-major or paged
+ * cache the d elements of one kv head are only 128-192 contiguous bytes of
+ * each token row; read one head at a time they stream at about 0.65 of the
+ * copy rate on GB300. A unit of two kv heads reads both heads of every token
+ * row together (256-384 contiguous bytes).
+ *
+ *   nq              query tokens per request, as la_plan_spec (1: decode)
+ *   heads_per_unit  kv heads of one unit: 1, 2, or 0 to pick 2 when
+ *                   d in {64, 80, 96} and hkv is even, else 1
+ *   tile_tokens     tokens of each head per tile; 0 picks the default:
+ *                   la_plan_ex's for 1 head per unit, half of it for 2
+ *                   (d = 64: 128; d = 80, 96: 64), so a tile still holds the
+ *                   same bytes. Two heads per unit are built for these
+ *                   defaults only.
+ *   num_sms, out    as la_plan
+ * Units are (request, group of heads_per_unit consecutive kv heads) in
+ * request-major order, tiles(b) = ceil(L_b / tile_tokens), and the split
+ * rules are la_plan's with hkv / heads_per_unit heads. A schedule with two
+ * heads per unit runs with la_decode_kv on LA_KV_TOKEN_MAJOR or
+ * LA_KV_PAGED caches only (la_decode, la_decode_ex, la_decode_static and
+ * the slab layout return LA_ERR_UNSUPPORTED). Its la_schedule_export
+ * counts units of two heads. LA_ERR_INVALID when heads_per_unit does not
+ * divide hkv or is not 0, 1 or 2; otherwise the errors of la_plan_spec.
+ */
+la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* cu_seqlens_k,
+                     int heads_per_unit, int tile_tokens, int num_sms, la_schedule** out);
+
+/*
  * la_decode_static -- la_decode without a workspace and without any device
  * allocation. The paper has no counterpart: this is a library convenience.
  *

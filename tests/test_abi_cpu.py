@@ -221,3 +221,69 @@ def test_spec_schedule_rejections(hq, hkv, nq, lengths, status):
     with pytest.raises(la.LeanAttentionError) as e:
         la.la_plan_spec(len(lengths), hq, hkv, 64, nq, cu_of(lengths), 7)
     assert e.value.status == status
+
+
+# ---- la_plan_kv: units of two kv heads for token-major / paged caches
+@pytest.mark.parametrize("d", [64, 80, 96])
+def test_two_head_units_are_the_reference_plan_over_head_pairs(d):
+    """A unit of two kv heads is the reference planner's unit over hkv / 2
+    heads with half the tokens per tile (the tile keeps its bytes)."""
+    r = np.random.default_rng(100 + d)
+    T = la.TILE_SIZES[d][0] // 2
+    for _ in range(8):
+        batch = int(r.integers(1, 5))
+        hkv = 2 * int(r.integers(1, 5))
+        grp = int(r.choice([1, 2, 4, 8]))
+        lengths = r.integers(1, 3000, size=batch).tolist()
+        G = int(r.integers(1, 160))
+        s = la.la_plan_kv(batch, hkv * grp, hkv, d, cu_of(lengths), num_sms=G)
+        assert s.heads_per_unit == 2
+        exp = la.la_schedule_export(s)
+        assert exp[2] == batch * hkv // 2 and exp[4] == T
+        assert exp == P.export(P.plan_lean(batch, (hkv // 2) * grp, hkv // 2, d, cu_of(lengths), G, T))
+
+
+def test_plan_kv_picks_one_head_where_rows_are_long_or_heads_odd():
+    assert la.la_plan_kv(1, 8, 8, 128, [0, 1000], num_sms=7).heads_per_unit == 1
+    assert la.la_plan_kv(1, 3, 3, 64, [0, 1000], num_sms=7).heads_per_unit == 1
+    assert la.la_plan_kv(1, 8, 1, 64, [0, 1000], num_sms=7).heads_per_unit == 1
+    s = la.la_plan_kv(2, 8, 8, 64, [0, 1000, 1500], heads_per_unit=1, num_sms=7)
+    assert la.la_schedule_export(s) == la.la_schedule_export(la.la_plan(2, 8, 8, 64, [0, 1000, 1500], 7))
+    # one head per unit with nq > 1 is la_plan_spec's schedule
+    s = la.la_plan_kv(2, 8, 4, 128, [0, 100, 150], nq=3, num_sms=5)
+    assert s.nq == 3 and s.heads_per_unit == 1
+    assert la.la_schedule_export(s) == la.la_schedule_export(la.la_plan_spec(2, 8, 4, 128, 3, [0, 100, 150], 5))
+
+
+def test_two_head_records_hold_both_heads():
+    # d 64, grp 4, nq 2: 8 query rows per kv head, two kv heads per unit
+    s = la.la_plan_kv(2, 16, 4, 64, [0, 300, 700], nq=2, num_sms=9)
+    assert s.heads_per_unit == 2
+    assert la.la_workspace_size(s) == 256 + 256 + 9 * 2 * 8 * 66 * 4
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(hkv=3, hq=6, heads_per_unit=2), la.LA_ERR_INVALID),     # two does not divide three kv heads
+    (dict(hkv=4, hq=8, heads_per_unit=3), la.LA_ERR_INVALID),
+    (dict(hkv=4, hq=8, heads_per_unit=2, d=128), la.LA_ERR_UNSUPPORTED),   # rows already 256 bytes: not built
+    (dict(hkv=4, hq=8, heads_per_unit=2, tile_tokens=256), la.LA_ERR_UNSUPPORTED),
+    (dict(hkv=4, hq=8, tile_tokens=-1), la.LA_ERR_INVALID),
+    (dict(hkv=2, hq=16, nq=2), la.LA_ERR_UNSUPPORTED),            # 8 x 2 query rows per kv head
+])
+def test_plan_kv_rejections(kw, status):
+    args = dict(batch=2, hq=8, hkv=4, d=64, cu=[0, 100, 300], nq=1, heads_per_unit=0, tile_tokens=0)
+    args.update(kw)
+    with pytest.raises(la.LeanAttentionError) as e:
+        la.la_plan_kv(args["batch"], args["hq"], args["hkv"], args["d"], args["cu"], nq=args["nq"],
+                      heads_per_unit=args["heads_per_unit"], tile_tokens=args["tile_tokens"], num_sms=7)
+    assert e.value.status == status
+
+
+def test_two_head_schedules_are_refused_for_the_slab_layout():
+    s = la.la_plan_kv(1, 4, 4, 64, [0, 1024], num_sms=3)
+    assert s.heads_per_unit == 2
+    p = ctypes.c_void_p(0x10000)
+    ws = ctypes.c_void_p(0x20000)
+    assert la._lib.la_decode(p, p, p, 0, p, s.handle, ws, p, ctypes.c_float(0.125), None) == la.LA_ERR_UNSUPPORTED
+    assert la._lib.la_decode_static(p, p, p, 0, p, s.handle, p, ctypes.c_float(0.125), None) \
+        == la.LA_ERR_UNSUPPORTED
