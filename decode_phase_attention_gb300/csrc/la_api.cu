@@ -346,7 +346,13 @@ int default_tile(int d) {
 }
 
 bool tile_supported(int d, int T, int hp) {
-  if (hp == 2) return (d == 64 && T == 128) || ((d == 80 || d == 96) && T == 64);
+  // units of several kv heads: the default tile of the head dim divided over
+  // the heads (the tile keeps its bytes)
+  if (hp > 1) {
+    const bool built = (d == 64 && hp == 2) || (d == 80 && (hp == 2 || hp == 8)) ||
+                       (d == 96 && (hp == 2 || hp == 4));
+    return built && T * hp == default_tile(d);
+  }
   if (hp != 1) return false;
   switch (d) {
     case 64: return T == 256 || T == 128;
@@ -359,13 +365,13 @@ bool tile_supported(int d, int T, int hp) {
 }
 
 cudaError_t launch_decode(int d, int T, int grp, int hp, int dtype, const KParams& p, cudaStream_t st) {
-  if (hp == 2) {
-    switch (d) {
-      case 64: return launch_decode_d64_hp2(T, grp, dtype, p, st);
-      case 80: return launch_decode_d80_hp2(T, grp, dtype, p, st);
-      case 96: return launch_decode_d96_hp2(T, grp, dtype, p, st);
-      default: return cudaErrorInvalidValue;
-    }
+  switch (d * 16 + hp) {
+    case 64 * 16 + 2: return launch_decode_d64_hp2(T, grp, dtype, p, st);
+    case 80 * 16 + 2: return launch_decode_d80_hp2(T, grp, dtype, p, st);
+    case 80 * 16 + 8: return launch_decode_d80_hp8(T, grp, dtype, p, st);
+    case 96 * 16 + 2: return launch_decode_d96_hp2(T, grp, dtype, p, st);
+    case 96 * 16 + 4: return launch_decode_d96_hp4(T, grp, dtype, p, st);
+    default: break;
   }
   if (hp != 1) return cudaErrorInvalidValue;
   switch (d) {
@@ -390,13 +396,13 @@ cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st) {
 }
 
 cudaError_t decode_capacity(int d, int T, int grp, int hp, int* per_sm) {
-  if (hp == 2) {
-    switch (d) {
-      case 64: return decode_capacity_d64_hp2(T, grp, per_sm);
-      case 80: return decode_capacity_d80_hp2(T, grp, per_sm);
-      case 96: return decode_capacity_d96_hp2(T, grp, per_sm);
-      default: return cudaErrorInvalidValue;
-    }
+  switch (d * 16 + hp) {
+    case 64 * 16 + 2: return decode_capacity_d64_hp2(T, grp, per_sm);
+    case 80 * 16 + 2: return decode_capacity_d80_hp2(T, grp, per_sm);
+    case 80 * 16 + 8: return decode_capacity_d80_hp8(T, grp, per_sm);
+    case 96 * 16 + 2: return decode_capacity_d96_hp2(T, grp, per_sm);
+    case 96 * 16 + 4: return decode_capacity_d96_hp4(T, grp, per_sm);
+    default: break;
   }
   if (hp != 1) return cudaErrorInvalidValue;
   switch (d) {
@@ -538,8 +544,17 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
   if (st != LA_OK) return st;
   if (nq < 1 || tile_tokens < 0) return LA_ERR_INVALID;
   int hp = heads_per_unit;
-  if (hp == 0) hp = ((d == 64 || d == 80 || d == 96) && hkv % 2 == 0) ? 2 : 1;
-  if ((hp != 1 && hp != 2) || hkv % hp != 0) return LA_ERR_INVALID;
+  if (hp == 0) {
+    // the fewest kv heads whose rows together make whole 256-byte pieces
+    // (d = 64: 2, 96: 4, 80: 8), else the most of those that divide hkv
+    hp = 1;
+    for (int h = 8; h >= 2; h /= 2)
+      if ((h * d * 2) % 256 == 0 && hkv % h == 0 && la::tile_supported(d, la::default_tile(d) / h, h)) hp = h;
+    if (hp == 1)
+      for (int h = 8; h >= 2 && hp == 1; h /= 2)
+        if (hkv % h == 0 && la::tile_supported(d, la::default_tile(d) / h, h)) hp = h;
+  }
+  if ((hp != 1 && hp != 2 && hp != 4 && hp != 8) || hkv % hp != 0) return LA_ERR_INVALID;
   const int rows = (hq / hkv) * nq;
   if (rows > 8) return LA_ERR_UNSUPPORTED;
   for (int b = 0; b < batch; ++b)

@@ -105,8 +105,8 @@ struct CParams {            // fixed-split merge launch
 int default_tile(int d);
 bool tile_supported(int d, int T, int hp = 1);
 
-// Launches (la_kernels_d<d>.cu, one file per head dim; la_kernels_d<d>_hp2.cu
-// for units of two kv heads). dtype: 0 fp16, 1 bf16.
+// Launches (la_kernels_d<d>.cu, one file per head dim; la_kernels_d<d>_hp<h>.cu
+// for units of h kv heads). dtype: 0 fp16, 1 bf16.
 // cudaErrorInvalidValue for a (d, T, grp, hp) that is not built.
 cudaError_t launch_decode(int d, int T, int grp, int hp, int dtype, const KParams& p, cudaStream_t st);
 cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st);
@@ -122,12 +122,14 @@ LA_DECLARE_HEAD_DIM(96)
 LA_DECLARE_HEAD_DIM(128)
 LA_DECLARE_HEAD_DIM(256)
 #undef LA_DECLARE_HEAD_DIM
-#define LA_DECLARE_HEAD_DIM_HP2(D)                                                            \
-  cudaError_t launch_decode_d##D##_hp2(int T, int grp, int dtype, const KParams& p, cudaStream_t st); \
-  cudaError_t decode_capacity_d##D##_hp2(int T, int grp, int* per_sm);
-LA_DECLARE_HEAD_DIM_HP2(64)
-LA_DECLARE_HEAD_DIM_HP2(80)
-LA_DECLARE_HEAD_DIM_HP2(96)
-#undef LA_DECLARE_HEAD_DIM_HP2
+#define LA_DECLARE_HEAD_DIM_HP(D, H)                                                            \
+  cudaError_t launch_decode_d##D##_hp##H(int T, int grp, int dtype, const KParams& p, cudaStream_t st); \
+  cudaError_t decode_capacity_d##D##_hp##H(int T, int grp, int* per_sm);
+LA_DECLARE_HEAD_DIM_HP(64, 2)
+LA_DECLARE_HEAD_DIM_HP(80, 2)
+LA_DECLARE_HEAD_DIM_HP(80, 8)
+LA_DECLARE_HEAD_DIM_HP(96, 2)
+LA_DECLARE_HEAD_DIM_HP(96, 4)
+#undef LA_DECLARE_HEAD_DIM_HP
 
 }  // namespace la

@@ -38,6 +38,12 @@
 // At the end of a segment the lanes of a warp and then the 8 warps merge
 // with f (the warps through shared memory).
 //
+// Units of HP > 1 kv heads (token-major and paged caches with short rows):
+// a tile holds T tokens of each of the unit's HP heads, loaded as the cache
+// stores them (tile row = token * HP + head, so each load reads HP * d
+// contiguous elements per token); the warps split into HP groups of NCW / HP,
+// one group per head, and merge within their group.
+//
 // Scores are kept in base-2 units: scale*log2(e) multiplies q.k so that
 // exp(s - m) becomes ex2(s2 - m2); m in the workspace records is in the
 // same units (the records are internal to this kernel).
@@ -261,7 +267,7 @@ struct Cfg {
   static constexpr int ITEMS = (HP * GRP * D + NCT - 1) / NCT;  // (row, dim) outputs per consumer thread
   static constexpr int PB = cmax(1, 16 / ITEMS);     // peer records per batch of host-merge loads
   static_assert(D % 16 == 0 && T % 16 == 0, "tile shape");
-  static_assert((HP == 1 || HP == 2) && NCW % HP == 0 && T % WPH == 0, "kv heads per unit");
+  static_assert((HP == 1 || HP == 2 || HP == 4 || HP == 8) && NCW % HP == 0 && T % WPH == 0, "kv heads per unit");
   static_assert(STEPS % CH == 0 && TPW % TPS == 0, "CUDA-core tile shape");
   static_assert(!TC || (TPW % 16 == 0 && GRP <= 8), "tensor-core tile shape");
   static_assert(SMEM <= 232448, "shared memory per CTA");

@@ -1,5 +1,5 @@
 // la_kernels_d80_hp2.cu -- instances of the decode kernel for head dim 80 with
-// units of two kv heads (token-major and paged caches: 320-byte pieces per token
+// units of 2 kv heads (token-major and paged caches: 320-byte pieces per token
 // row instead of 160), 64 tokens of each head per tile, query-head groups 1, 2, 4
 // and 8, fp16 and bf16.
 #include "la_kernel.cuh"

@@ -1,0 +1,33 @@
+// la_kernels_d96_hp4.cu -- instances of the decode kernel for head dim 96 with
+// units of 4 kv heads (token-major and paged caches: 768-byte pieces per token
+// row instead of 192), 32 tokens of each head per tile, query-head groups 1, 2, 4
+// and 8, fp16 and bf16.
+#include "la_kernel.cuh"
+
+namespace la {
+
+cudaError_t launch_decode_d96_hp4(int T, int grp, int dtype, const KParams& p, cudaStream_t st) {
+  if (T == 32 && grp == 1)
+    return dtype ? launch_decode_t<96, 32, 1, __nv_bfloat16, 4>(p, st)
+                 : launch_decode_t<96, 32, 1, __half, 4>(p, st);
+  if (T == 32 && grp == 2)
+    return dtype ? launch_decode_t<96, 32, 2, __nv_bfloat16, 4>(p, st)
+                 : launch_decode_t<96, 32, 2, __half, 4>(p, st);
+  if (T == 32 && grp == 4)
+    return dtype ? launch_decode_t<96, 32, 4, __nv_bfloat16, 4>(p, st)
+                 : launch_decode_t<96, 32, 4, __half, 4>(p, st);
+  if (T == 32 && grp == 8)
+    return dtype ? launch_decode_t<96, 32, 8, __nv_bfloat16, 4>(p, st)
+                 : launch_decode_t<96, 32, 8, __half, 4>(p, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t decode_capacity_d96_hp4(int T, int grp, int* per_sm) {
+  if (T == 32 && grp == 1) return capacity_t<96, 32, 1, 4>(per_sm);
+  if (T == 32 && grp == 2) return capacity_t<96, 32, 2, 4>(per_sm);
+  if (T == 32 && grp == 4) return capacity_t<96, 32, 4, 4>(per_sm);
+  if (T == 32 && grp == 8) return capacity_t<96, 32, 8, 4>(per_sm);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace la

@@ -263,27 +263,31 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
  * The paper has no counterpart: its units are single (request, head) pairs
  * over a [batch, heads, seq_len, head_dim] layout. In a token-major or paged
  * cache the d elements of one kv head are only 128-192 contiguous bytes of
- * each token row; read one head at a time they stream at about 0.65 of the
- * copy rate on GB300. A unit of two kv heads reads both heads of every token
- * row together (256-384 contiguous bytes).
+ * each token row; read one head at a time they stream at 0.5-0.85 of the
+ * copy rate on GB300. A unit of several kv heads reads those heads of every
+ * token row together, in whole 256-byte multiples where it can (d = 64: two
+ * heads, 256 bytes; d = 96: four, 768 bytes; d = 80: eight, 1280 bytes).
  *
  *   nq              query tokens per request, as la_plan_spec (1: decode)
- *   heads_per_unit  kv heads of one unit: 1, 2, or 0 to pick 2 when
- *                   d in {64, 80, 96} and hkv is even, else 1
+ *   heads_per_unit  kv heads of one unit. Built: 1 (any d); d = 64: 2;
+ *                   d = 80: 2, 8; d = 96: 2, 4. 0 picks the fewest heads
+ *                   whose rows make whole 256-byte pieces if that count
+ *                   divides hkv, else the most built count that divides
+ *                   hkv, else 1 (always 1 for d = 128, 256).
  *   tile_tokens     tokens of each head per tile; 0 picks the default:
- *                   la_plan_ex's for 1 head per unit, half of it for 2
- *                   (d = 64: 128; d = 80, 96: 64), so a tile still holds the
- *                   same bytes. Two heads per unit are built for these
- *                   defaults only.
+ *                   la_plan_ex's divided by heads_per_unit, so a tile still
+ *                   holds the same bytes (only these defaults are built for
+ *                   more than one head per unit).
  *   num_sms, out    as la_plan
  * Units are (request, group of heads_per_unit consecutive kv heads) in
  * request-major order, tiles(b) = ceil(L_b / tile_tokens), and the split
- * rules are la_plan's with hkv / heads_per_unit heads. A schedule with two
- * heads per unit runs with la_decode_kv on LA_KV_TOKEN_MAJOR or
+ * rules are la_plan's over hkv / heads_per_unit heads. A schedule with more
+ * than one head per unit runs with la_decode_kv on LA_KV_TOKEN_MAJOR or
  * LA_KV_PAGED caches only (la_decode, la_decode_ex, la_decode_static and
- * the slab layout return LA_ERR_UNSUPPORTED). Its la_schedule_export
- * counts units of two heads. LA_ERR_INVALID when heads_per_unit does not
- * divide hkv or is not 0, 1 or 2; otherwise the errors of la_plan_spec.
+ * the slab layout return LA_ERR_UNSUPPORTED); its la_schedule_export
+ * counts units of heads_per_unit heads. LA_ERR_INVALID when heads_per_unit
+ * is not 0, 1, 2, 4 or 8 or does not divide hkv; LA_ERR_UNSUPPORTED for a
+ * count or tile that is not built; otherwise the errors of la_plan_spec.
  */
 la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* cu_seqlens_k,
                      int heads_per_unit, int tile_tokens, int num_sms, la_schedule** out);

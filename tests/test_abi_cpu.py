@@ -224,23 +224,36 @@ def test_spec_schedule_rejections(hq, hkv, nq, lengths, status):
 
 
 # ---- la_plan_kv: units of two kv heads for token-major / paged caches
-@pytest.mark.parametrize("d", [64, 80, 96])
-def test_two_head_units_are_the_reference_plan_over_head_pairs(d):
-    """A unit of two kv heads is the reference planner's unit over hkv / 2
-    heads with half the tokens per tile (the tile keeps its bytes)."""
-    r = np.random.default_rng(100 + d)
-    T = la.TILE_SIZES[d][0] // 2
+MULTI_HEAD = [(64, 2), (80, 2), (80, 8), (96, 2), (96, 4)]
+
+
+@pytest.mark.parametrize("d,hp", MULTI_HEAD)
+def test_multi_head_units_are_the_reference_plan_over_head_groups(d, hp):
+    """A unit of hp kv heads is the reference planner's unit over hkv / hp
+    heads with 1/hp of the tokens per tile (the tile keeps its bytes)."""
+    r = np.random.default_rng(100 + d + hp)
+    T = la.TILE_SIZES[d][0] // hp
     for _ in range(8):
         batch = int(r.integers(1, 5))
-        hkv = 2 * int(r.integers(1, 5))
+        hkv = hp * int(r.integers(1, 4))
         grp = int(r.choice([1, 2, 4, 8]))
         lengths = r.integers(1, 3000, size=batch).tolist()
         G = int(r.integers(1, 160))
-        s = la.la_plan_kv(batch, hkv * grp, hkv, d, cu_of(lengths), num_sms=G)
-        assert s.heads_per_unit == 2
+        s = la.la_plan_kv(batch, hkv * grp, hkv, d, cu_of(lengths), heads_per_unit=hp, num_sms=G)
+        assert s.heads_per_unit == hp
         exp = la.la_schedule_export(s)
-        assert exp[2] == batch * hkv // 2 and exp[4] == T
-        assert exp == P.export(P.plan_lean(batch, (hkv // 2) * grp, hkv // 2, d, cu_of(lengths), G, T))
+        assert exp[2] == batch * hkv // hp and exp[4] == T
+        assert exp == P.export(P.plan_lean(batch, (hkv // hp) * grp, hkv // hp, d, cu_of(lengths), G, T))
+
+
+@pytest.mark.parametrize("d,hkv,hp", [(64, 32, 2), (64, 1, 1), (80, 32, 8), (80, 4, 2), (80, 12, 2), (96, 8, 4),
+                                       (96, 6, 2), (96, 3, 1), (128, 8, 1), (256, 4, 1)])
+def test_plan_kv_default_heads_per_unit(d, hkv, hp):
+    """The default: the fewest kv heads whose rows make whole 256-byte pieces
+    (d 64: 2, d 96: 4, d 80: 8); if that does not divide hkv, the most built
+    count that does."""
+    s = la.la_plan_kv(2, hkv, hkv, d, [0, 1000, 3000], num_sms=7)
+    assert s.heads_per_unit == hp
 
 
 def test_plan_kv_picks_one_head_where_rows_are_long_or_heads_odd():
@@ -265,6 +278,10 @@ def test_two_head_records_hold_both_heads():
 @pytest.mark.parametrize("kw,status", [
     (dict(hkv=3, hq=6, heads_per_unit=2), la.LA_ERR_INVALID),     # two does not divide three kv heads
     (dict(hkv=4, hq=8, heads_per_unit=3), la.LA_ERR_INVALID),
+    (dict(hkv=4, hq=8, heads_per_unit=8), la.LA_ERR_INVALID),     # eight does not divide four kv heads
+    (dict(hkv=16, hq=16, heads_per_unit=16), la.LA_ERR_INVALID),
+    (dict(hkv=8, hq=8, heads_per_unit=8), la.LA_ERR_UNSUPPORTED),  # d 64 with 8 heads per unit: not built
+    (dict(hkv=8, hq=8, heads_per_unit=4), la.LA_ERR_UNSUPPORTED),  # nor with 4 (no faster than 2)
     (dict(hkv=4, hq=8, heads_per_unit=2, d=128), la.LA_ERR_UNSUPPORTED),   # rows already 256 bytes: not built
     (dict(hkv=4, hq=8, heads_per_unit=2, tile_tokens=256), la.LA_ERR_UNSUPPORTED),
     (dict(hkv=4, hq=8, tile_tokens=-1), la.LA_ERR_INVALID),

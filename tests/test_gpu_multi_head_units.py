@@ -1,4 +1,4 @@
-"""GPU parity for units of two kv heads (la_plan_kv) on token-major and
+"""GPU parity for units of several kv heads (la_plan_kv) on token-major and
 paged caches: every output row against the float64 oracle, which gathers K
 and V from the same caches by plain per-token indexing. Paged caches put
 their pages in a seeded random order and fill unused slots with NaN."""
@@ -49,23 +49,27 @@ def run(w, q, kc, vc, layout, grid=0, table=None, P=0, npages=0, out_dtype=torch
     return out, s
 
 
-CASES = [(d, grp, dt) for d in (64, 80, 96) for grp, dt in ((1, "f16"), (2, "bf16"), (4, "bf16"), (8, "f16"))]
+MULTI_HEAD = [(64, 2), (80, 2), (80, 8), (96, 2), (96, 4)]
+CASES = [(d, hp, grp, dt) for d, hp in MULTI_HEAD
+         for grp, dt in ((1, "f16"), (2, "bf16"), (4, "bf16"), (8, "f16"))]
 
 
-@pytest.mark.parametrize("d,grp,dt", CASES)
+@pytest.mark.parametrize("d,hp,grp,dt", CASES)
 @pytest.mark.parametrize("layout,P", [("token_major", 0), ("paged", 16), ("paged", 64), ("paged", 256)])
-def test_two_head_units(d, grp, dt, layout, P):
-    # ragged lengths: a 1-token request, tails inside a page and across tiles
-    w = workloads.custom(4, 4 * grp, 4, d, dt, [1, 700, 129, 3000])
-    q, k, v, _ = workloads.make_inputs(w, seed=d + grp + P, device="cuda")
+def test_multi_head_units(d, hp, grp, dt, layout, P):
+    # ragged lengths: a 1-token request, tails inside a page and across tiles;
+    # two units per request
+    hkv = 2 * hp
+    w = workloads.custom(4, hkv * grp, hkv, d, dt, [1, 700, 129, 3000])
+    q, k, v, _ = workloads.make_inputs(w, seed=d + hp + grp + P, device="cuda")
     kc, vc, table, npages, gather = caches(w, k, v, layout, P)
-    out, s = run(w, q, kc, vc, layout, grid=7, table=table, P=P, npages=npages)
-    assert s.heads_per_unit == 2
+    out, s = run(w, q, kc, vc, layout, grid=7, table=table, P=P, npages=npages, heads_per_unit=hp)
+    assert s.heads_per_unit == hp
     compare(out.cpu(), oracle_from_cache(w, q, kc, vc, gather))
 
 
 @pytest.mark.parametrize("grid", [0, 1, 2, 5, 33, 150, 304])
-def test_two_head_units_over_grid_sizes(grid):
+def test_multi_head_units_over_grid_sizes(grid):
     w = workloads.custom(3, 48, 6, 64, "bf16", [2000, 37, 900])
     q, k, v, _ = workloads.make_inputs(w, seed=grid, device="cuda")
     kc, vc, table, npages, gather = caches(w, k, v, "paged", 32)
@@ -76,15 +80,16 @@ def test_two_head_units_over_grid_sizes(grid):
     compare(out.cpu(), oracle_from_cache(w, q, kc, vc, gather))
 
 
-@pytest.mark.parametrize("d,grp,nq", [(64, 1, 3), (64, 2, 4), (64, 4, 2), (80, 1, 8), (96, 2, 2)])
+@pytest.mark.parametrize("d,hp,grp,nq", [(64, 2, 1, 3), (64, 2, 2, 4), (64, 2, 4, 2), (80, 2, 1, 8), (80, 8, 2, 3),
+                                         (96, 2, 2, 2), (96, 4, 1, 5)])
 @pytest.mark.parametrize("layout,P", [("token_major", 0), ("paged", 16)])
-def test_two_head_units_with_several_query_tokens(d, grp, nq, layout, P):
+def test_multi_head_units_with_several_query_tokens(d, hp, grp, nq, layout, P):
     lengths = [nq, 130, 257, 1000, 64 * 7 + 3]
-    w = workloads.custom(len(lengths), 2 * grp, 2, d, "bf16", lengths, nq=nq)
+    w = workloads.custom(len(lengths), hp * grp, hp, d, "bf16", lengths, nq=nq)
     q, k, v, _ = workloads.make_inputs(w, seed=d * nq + grp, device="cuda")
     kc, vc, table, npages, gather = caches(w, k, v, layout, P)
-    out, s = run(w, q, kc, vc, layout, grid=5, table=table, P=P, npages=npages)
-    assert s.heads_per_unit == 2 and out.shape == (w.batch, nq, w.hq, w.d)
+    out, s = run(w, q, kc, vc, layout, grid=5, table=table, P=P, npages=npages, heads_per_unit=hp)
+    assert s.heads_per_unit == hp and out.shape == (w.batch, nq, w.hq, w.d)
     compare(out.cpu(), oracle_from_cache(w, q, kc, vc, gather))
 
 
@@ -102,15 +107,15 @@ def test_one_and_two_head_units_agree_and_16_bit_outputs_round_the_fp32_result()
     assert torch.equal(b16, two.to(torch.bfloat16))
 
 
-@pytest.mark.parametrize("name", ["gqa", "mha_h32_b8_c8192_d64"])
+@pytest.mark.parametrize("name,hp", [("gqa", 2), ("mha_h32_b8_c8192_d64", 2), ("hd80", 8), ("hd96", 4)])
 @pytest.mark.parametrize("layout,P", [("token_major", 0), ("paged", 16)])
-def test_named_workloads_with_two_head_units(name, layout, P):
+def test_named_workloads_with_multi_head_units(name, hp, layout, P):
     w = workloads.named(name)
     q, k, v, _ = workloads.make_inputs(w, seed=0, device="cuda")
     kc, vc, table, npages, gather = caches(w, k, v, layout, P)
     del k, v
     out, s = run(w, q, kc, vc, layout, table=table, P=P, npages=npages)
-    assert s.heads_per_unit == 2
+    assert s.heads_per_unit == hp  # the default choice
     compare(out.cpu(), oracle_from_cache(w, q, kc, vc, gather))
 
 
