@@ -80,9 +80,15 @@ def kernel_source_digest():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
+def profile_name(workload, kv_layout="slab", page_size=0):
+    """Name of the committed ncu summary of the stream-K kernel on a workload and cache layout."""
+    suffix = "" if kv_layout == "slab" else ("_token_major" if kv_layout == "token_major" else f"_paged{page_size}")
+    return f"lean_decode_kernel_{workload}{suffix}"
+
+
+def profiled_traffic(name):
     """DRAM bytes per launch from the committed ncu summary, if it is for this kernel source."""
-    path = os.path.join(ROOT, "profiles", f"lean_decode_kernel_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{name}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -296,7 +302,10 @@ def run_ours(args, rank, world, local_rank):
     plan_times = []
     for _ in range(21):
         t0 = time.perf_counter()
-        la.la_plan(w.batch, w.hq, w.hkv, w.d, cu, grid if grid > 0 else 0, args.tile)
+        if args.kv_layout != "slab" and args.kernel == "lean":
+            la.la_plan_kv(w.batch, w.hq, w.hkv, w.d, cu, w.nq, args.heads_per_unit, args.tile, grid)
+        else:
+            la.la_plan(w.batch, w.hq, w.hkv, w.d, cu, grid if grid > 0 else 0, args.tile)
         plan_times.append((time.perf_counter() - t0) * 1e6)
     plan_us = sorted(plan_times)[len(plan_times) // 2]
     out_torch = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[args.out_dtype]
@@ -476,7 +485,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": ("flushed before every timed call (256 MiB write, then 256 MiB read so no "
                           "dirty line is written back inside the call)" if use_flush else
                           f"no flush: K+V ({kv_bytes / 1e9:.2f} GB) exceed 4x the 129 MB L2"),
-                   "plan_us": round(plan_us, 1), "plan_note": "median host time of la_plan, outside the timed region",
+                   "plan_us": round(plan_us, 1), "plan_note": "median host time of the planner call, outside the timed region",
                    "seed": args.seed,
                    "timing": ("CUDA events around the K back-to-back calls" if not use_flush else
                               "CUDA events around each call, after a 256 MiB L2 flush"),
@@ -485,7 +494,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": "measured hbm_gbs (copy, burst)" if peaks else "fallback 6.8 TB/s",
-                     "traffic": profiled_traffic(args.workload) if args.kernel == "lean" else None,
+                     "traffic": (profiled_traffic(profile_name(args.workload, args.kv_layout, args.page_size))
+                                 if args.kernel == "lean" and args.heads_per_unit == 0 else None),
                      "algorithmic_bytes_per_launch": algo_bytes},
         "cpu_baseline": cpu,
         "e2e": e2e,
