@@ -265,7 +265,7 @@ struct Cfg {
   static constexpr size_t BAR_BYTES = 2 * STAGES * 8 + 16;
   static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
   static constexpr int ITEMS = (HP * GRP * D + NCT - 1) / NCT;  // (row, dim) outputs per consumer thread
-  static constexpr int PB = cmax(1, 16 / ITEMS);     // peer records per batch of host-merge loads
+  static constexpr int PB = cmax(1, cmin(4, 16 / ITEMS));  // peer records per batch of host-merge loads
   static_assert(D % 16 == 0 && T % 16 == 0, "tile shape");
   static_assert((HP == 1 || HP == 2 || HP == 4 || HP == 8) && NCW % HP == 0 && T % WPH == 0, "kv heads per unit");
   static_assert(STEPS % CH == 0 && TPW % TPS == 0, "CUDA-core tile shape");
@@ -477,7 +477,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
                                                 float* wrec) {
   using C = Cfg<D, T, GRP, HP>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int hh = warp / C::WPH;   // kv head of the unit this warp works on
+  const int hh = HP == 1 ? 0 : warp / C::WPH;  // kv head of the unit this warp works on
   const int kvh = kvh0 + hh;
   const int gl = lane % C::LPT;   // which 8-element chunk of the row
   const int ts = lane / C::LPT;   // which token of the warp step
@@ -513,7 +513,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
     if (wait_tile<D, T, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
       const E* Ks = kv + (size_t)stage * 2 * C::TILE_ELEMS;
       const E* Vs = Ks + C::TILE_ELEMS;
-      const int wtok = (warp % C::WPH) * C::TPW;
+      const int wtok = (HP == 1 ? warp : warp % C::WPH) * C::TPW;
 #pragma unroll
       for (int c = 0; c < C::STEPS; c += C::CH) {
         float s[C::CH][GRP];
@@ -645,7 +645,7 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
                                                 float* wrec) {
   using C = Cfg<D, T, GRP, HP>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int hh = warp / C::WPH;   // kv head of the unit this warp works on
+  const int hh = HP == 1 ? 0 : warp / C::WPH;  // kv head of the unit this warp works on
   const int kvh = kvh0 + hh;
   const int gq = lane >> 2;  // fragment row group
   const int tq = lane & 3;   // fragment column pair
@@ -679,7 +679,7 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
     if (wait_tile<D, T, GRP>(p, g, full, stage, phase, abort_flag, lane) && ok) {
       const uint32_t kb = kv_base + (uint32_t)(stage * 2 * C::TILE_ELEMS * 2);
       const uint32_t vb = kb + (uint32_t)(C::TILE_ELEMS * 2);
-      const int wtok = (warp % C::WPH) * C::TPW;
+      const int wtok = (HP == 1 ? warp : warp % C::WPH) * C::TPW;
       // S = K q^T for the warp's TPW tokens: MT tiles of 16 tokens x 8 heads
       float s[C::MT][4];
 #pragma unroll
@@ -813,16 +813,18 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
   const int tid = threadIdx.x, warp = tid >> 5;
   const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
   const uint32_t ready = epoch + 1u;
-  const int nitems = HP * p.rows * D;  // outputs of a unit: (kv head of the unit, row, dim)
+  // Outputs of a unit: item idx -> record row rr = idx / D = hh * GRP + j
+  // (kv head hh of the unit, query row j, live when j < rows) and dim idx % D.
+  constexpr int kItems = HP * GRP * D;
   int stage = 0;
   uint32_t phase = 0;
 
   for (int si = s_begin; si < s_end; ++si) {
     const int4 w0 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords);
     const int4 w1 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 4);
-    const int4 w2 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 8);
     const int unit = w0.x, t0 = w0.y, t1 = w0.z, kind = w0.w, peer = w1.x;
-    const int b = w2.y, kvh0 = w2.z;  // request, first kv head of the unit
+    const int groups = p.hkv / HP;  // units per request
+    const int b = unit / groups, kvh0 = (unit % groups) * HP;  // request, first kv head of the unit
     // Device offsets that disagree with the schedule: the tiles are still
     // taken from the ring (the producer streams them) but not used, and the
     // unit's outputs are NaN.
@@ -846,18 +848,16 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
     }
     consumer_sync(C::NCT);
 
-    // ---- merge the warps of each kv head with f: thread -> (head, row, dim)
-    // items; a record row is hh * GRP + j
+    // ---- merge the warps of each kv head with f: thread -> (head, row, dim) items
     float M[C::ITEMS], Lsum[C::ITEMS], O[C::ITEMS];
 #pragma unroll
     for (int i = 0; i < C::ITEMS; ++i) {
       const int idx = tid + i * C::NCT;
+      const int rr = idx / D, cc = idx % D, hh = rr / GRP, j = rr % GRP;
       M[i] = -INFINITY;
       Lsum[i] = 0.f;
       O[i] = 0.f;
-      if (idx < nitems) {
-        const int hr = idx / D, cc = idx % D;
-        const int hh = hr / p.rows, j = hr % p.rows;
+      if (idx < kItems && j < p.rows) {
         const float* base = mrg + ((size_t)hh * C::WPH * GRP + j) * C::REC;
         float mm = -INFINITY;
 #pragma unroll
@@ -884,9 +884,9 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
 #pragma unroll
       for (int i = 0; i < C::ITEMS; ++i) {
         const int idx = tid + i * C::NCT;
-        if (idx < nitems) {
-          const int hr = idx / D, cc = idx % D;
-          float* r = rec + ((hr / p.rows) * GRP + hr % p.rows) * C::REC;
+        const int rr = idx / D, cc = idx % D;
+        if (idx < kItems && rr % GRP < p.rows) {
+          float* r = rec + rr * C::REC;
           r[2 + cc] = O[i];
           if (cc == 0) {
             r[0] = poisoned ? __int_as_float(0x7fc00000) : M[i];
@@ -933,14 +933,13 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
 #pragma unroll
             for (int i = 0; i < C::ITEMS; ++i) {
               const int idx = tid + i * C::NCT;
-              const int hr = idx / D, cc = idx % D;
-              const int rr = (hr / p.rows) * GRP + hr % p.rows;
+              const int rr = idx / D, cc = idx % D;
 #pragma unroll
               for (int u = 0; u < C::PB; ++u) {
                 m2[i][u] = -INFINITY;
                 l2[i][u] = 0.f;
                 o2[i][u] = 0.f;
-                if (idx < nitems && p0 + u < npeer) {
+                if (idx < kItems && rr % GRP < p.rows && p0 + u < npeer) {
                   const float* r = p.recs + ((size_t)(g + 1 + p0 + u) * HP * GRP + rr) * C::REC;
                   m2[i][u] = __ldcg(r);
                   l2[i][u] = __ldcg(r + 1);
@@ -968,10 +967,10 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
 #pragma unroll
       for (int i = 0; i < C::ITEMS; ++i) {
         const int idx = tid + i * C::NCT;
-        if (idx < nitems) {
-          const int hr = idx / D, cc = idx % D;
+        const int rr = idx / D, cc = idx % D;
+        if (idx < kItems && rr % GRP < p.rows) {
           const float val = fail ? __int_as_float(0x7fc00000) : O[i] / Lsum[i];
-          store_out(p.out, row_index(p, b, kvh0 + hr / p.rows, hr % p.rows) * D + cc, val, p.out_dtype);
+          store_out(p.out, row_index(p, b, kvh0 + rr / GRP, rr % GRP) * D + cc, val, p.out_dtype);
         }
       }
     }
