@@ -27,14 +27,17 @@ enum KvLayout : int {
 };
 
 // Workspace: a 256-byte header, G ready flags (padded to 256 bytes), then G
-// partial records of rows * (d + 2) floats: per query row [m, l, O[d]]
-// (rows = the instance's rows per kv head x kv heads per unit).
+// partial records of rows * (d + 2) floats, per query row [m, l, O[d]]
+// (rows = the instance's rows per kv head x kv heads per unit), each record
+// padded to a multiple of 4 floats so that records can be moved as 16-byte
+// vectors.
 constexpr size_t kHeaderBytes = 256;
 enum HeaderWord { kEpoch = 0, kDone = 1, kStatus = 2, kInfoCta = 3, kInfoPeer = 4 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline size_t flags_bytes(int G) { return align_up(sizeof(uint32_t) * (size_t)G, 256); }
-inline size_t record_floats(int d, int rows) { return (size_t)rows * (size_t)(d + 2); }
+__host__ __device__ constexpr int record_stride(int d, int rows) { return (rows * (d + 2) + 3) / 4 * 4; }
+inline size_t record_floats(int d, int rows) { return (size_t)record_stride(d, rows); }
 inline size_t workspace_bytes(int G, int d, int rows) {
   return kHeaderBytes + flags_bytes(G) + sizeof(float) * record_floats(d, rows) * (size_t)G;
 }

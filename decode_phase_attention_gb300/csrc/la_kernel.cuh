@@ -261,11 +261,13 @@ struct Cfg {
   static constexpr int STAGES = cmax(2, cmin(4, 196608 / STAGE_BYTES));
   static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
   static constexpr int REC = D + 2;                 // [m, l, O[d]]
+  static constexpr int RS = record_stride(D, HP * GRP);  // floats per CTA record in the workspace
   static constexpr size_t MERGE_BYTES = (size_t)NCW * GRP * REC * 4;
   static constexpr size_t BAR_BYTES = 2 * STAGES * 8 + 16;
   static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
   static constexpr int ITEMS = (HP * GRP * D + NCT - 1) / NCT;  // (row, dim) outputs per consumer thread
   static constexpr int PB = cmax(1, cmin(4, 16 / ITEMS));  // peer records per batch of host-merge loads
+  static constexpr int STAGE_RECS = (int)(KV_BYTES / (RS * 4));  // peer records the idle ring can hold
   static_assert(D % 16 == 0 && T % 16 == 0, "tile shape");
   static_assert((HP == 1 || HP == 2 || HP == 4 || HP == 8) && NCW % HP == 0 && T % WPH == 0, "kv heads per unit");
   static_assert(STEPS % CH == 0 && TPW % TPS == 0, "CUDA-core tile shape");
@@ -806,8 +808,21 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
 }
 
 // ------------------------------------------------------------------ consumers
+// The rescaling reduction f of one output element: (M, Ls, O) <- f((M, Ls, O),
+// (m2, l2, o2)) in base-2 units; (-inf, 0, 0) is the identity and a NaN m2
+// (a poisoned partial) propagates through its weight.
+__device__ __forceinline__ void merge_f(float& M, float& Ls, float& O, float m2, float l2, float o2) {
+  const float mn = fmaxf(M, m2);
+  if (mn == -INFINITY) return;
+  const float a = (M == -INFINITY) ? 0.f : ex2(M - mn);
+  const float bw = (m2 == -INFINITY) ? 0.f : ex2(m2 - mn);
+  Ls = a * Ls + bw * l2;
+  O = a * O + bw * o2;
+  M = mn;
+}
+
 template <int D, int T, int GRP, typename E, int HP>
-__device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, uint64_t* full, uint64_t* empty,
+__device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t* full, uint64_t* empty,
                                         float* mrg, volatile int* abort_flag, uint32_t epoch) {
   using C = Cfg<D, T, GRP, HP>;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -880,7 +895,7 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
     const bool poisoned = (*abort_flag != 0) || !ok;
 
     if (kind == kNonHost || kind == kPartial) {
-      float* rec = p.recs + (size_t)g * HP * GRP * C::REC;
+      float* rec = p.recs + (size_t)g * C::RS;
 #pragma unroll
       for (int i = 0; i < C::ITEMS; ++i) {
         const int idx = tid + i * C::NCT;
@@ -925,10 +940,59 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
         if (*abort_flag) {
           fail = true;
         } else {
-          // merge the peers' partials with f: the loads of PB peers for all of
-          // this thread's outputs are issued before any of them is used, so a
-          // batch costs one L2 round trip
-          for (int p0 = 0; p0 < npeer; p0 += C::PB) {
+          int p0 = 0;
+          if (si == s_end - 1 && npeer > C::PB) {
+            // Many peers, and the CTA's last segment: every tile has been
+            // consumed and the producer issues no more copies, so the ring is
+            // idle. Stage the records of the first peers there with one
+            // cooperative round of 16-byte L2 loads (the records of
+            // consecutive CTAs are contiguous), then apply f to all of them
+            // at once: the maximum m over the partials, then the weighted
+            // sums of l and O (f is associative, so k partials reduce in one
+            // step).
+            const int ns = npeer < C::STAGE_RECS ? npeer : C::STAGE_RECS;
+            float4* stg = reinterpret_cast<float4*>(kv);
+            const float4* src = reinterpret_cast<const float4*>(p.recs + (size_t)(g + 1) * C::RS);
+            const int n4 = ns * (C::RS / 4);
+            for (int i0 = tid; i0 < n4; i0 += 8 * C::NCT) {
+              float4 buf[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                if (i0 + u * C::NCT < n4) buf[u] = __ldcg(src + i0 + u * C::NCT);
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                if (i0 + u * C::NCT < n4) stg[i0 + u * C::NCT] = buf[u];
+            }
+            consumer_sync(C::NCT);
+            const float* st = reinterpret_cast<const float*>(kv);
+#pragma unroll
+            for (int i = 0; i < C::ITEMS; ++i) {
+              const int idx = tid + i * C::NCT;
+              const int rr = idx / D, cc = idx % D;
+              if (!(idx < kItems && rr % GRP < p.rows)) continue;
+              float mm = M[i];
+#pragma unroll 4
+              for (int u = 0; u < ns; ++u) mm = fmaxf(mm, st[u * C::RS + rr * C::REC]);
+              if (mm == -INFINITY) continue;
+              const float a = (M[i] == -INFINITY) ? 0.f : ex2(M[i] - mm);
+              float ls = a * Lsum[i], os = a * O[i];
+#pragma unroll 4
+              for (int u = 0; u < ns; ++u) {
+                const float* r = st + u * C::RS + rr * C::REC;
+                const float w = (r[0] == -INFINITY) ? 0.f : ex2(r[0] - mm);  // NaN m (poisoned) propagates
+                ls = fmaf(w, r[1], ls);
+                os = fmaf(w, r[2 + cc], os);
+              }
+              M[i] = mm;
+              Lsum[i] = ls;
+              O[i] = os;
+            }
+            p0 = ns;
+          }
+          // Few peers (or peers beyond the staged ones): the loads of PB
+          // peers for all of this thread's outputs are issued before any of
+          // them is used, so a batch costs one L2 round trip.
+          for (; p0 < npeer; p0 += C::PB) {
             float m2[C::ITEMS][C::PB], l2[C::ITEMS][C::PB], o2[C::ITEMS][C::PB];
 #pragma unroll
             for (int i = 0; i < C::ITEMS; ++i) {
@@ -940,7 +1004,7 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
                 l2[i][u] = 0.f;
                 o2[i][u] = 0.f;
                 if (idx < kItems && rr % GRP < p.rows && p0 + u < npeer) {
-                  const float* r = p.recs + ((size_t)(g + 1 + p0 + u) * HP * GRP + rr) * C::REC;
+                  const float* r = p.recs + (size_t)(g + 1 + p0 + u) * C::RS + rr * C::REC;
                   m2[i][u] = __ldcg(r);
                   l2[i][u] = __ldcg(r + 1);
                   o2[i][u] = __ldcg(r + 2 + cc);
@@ -948,18 +1012,9 @@ __device__ __forceinline__ void consume(const KParams& p, int g, const E* kv, ui
               }
             }
 #pragma unroll
-            for (int i = 0; i < C::ITEMS; ++i) {
+            for (int i = 0; i < C::ITEMS; ++i)
 #pragma unroll
-              for (int u = 0; u < C::PB; ++u) {
-                const float mn = fmaxf(M[i], m2[i][u]);
-                if (mn == -INFINITY) continue;
-                const float a = (M[i] == -INFINITY) ? 0.f : ex2(M[i] - mn);
-                const float bw = (m2[i][u] == -INFINITY) ? 0.f : ex2(m2[i][u] - mn);
-                Lsum[i] = a * Lsum[i] + bw * l2[i][u];
-                O[i] = a * O[i] + bw * o2[i][u];
-                M[i] = mn;  // a NaN m2 (poisoned partial) propagates through bw
-              }
-            }
+              for (int u = 0; u < C::PB; ++u) merge_f(M[i], Lsum[i], O[i], m2[i][u], l2[i][u], o2[i][u]);
           }
         }
       }
@@ -1049,7 +1104,7 @@ __global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
   if (h0 == h1) return;  // a whole unit was written by the decode kernel
   float M = -INFINITY, Ls = 0.f, O = 0.f;
   for (int s = h0; s <= h1; ++s) {
-    const float* r = p.recs + ((size_t)s * GRP + j) * REC;
+    const float* r = p.recs + (size_t)s * record_stride(D, GRP) + j * REC;
     const float m2 = r[0], l2 = r[1], o2 = r[2 + c];
     const float mn = fmaxf(M, m2);
     if (mn == -INFINITY) continue;

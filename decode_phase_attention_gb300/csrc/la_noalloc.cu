@@ -49,7 +49,7 @@ Layout layout_of(const la_schedule* s) {
   L.flags = off;
   off += la::flags_bytes(s->G);
   L.recs = off;
-  off = la::align_up(off + sizeof(float) * la::record_floats(s->d, s->R) * (size_t)s->G, 256);
+  off = la::align_up(off + sizeof(float) * la::record_floats(s->d, s->R * s->hp) * (size_t)s->G, 256);
   auto table = [&off](size_t words) {
     const size_t at = off;
     off = la::align_up(off + words * sizeof(int32_t), 16);

@@ -118,8 +118,9 @@ def test_decode_rejects_bad_pointers_before_any_launch():
 
 def test_workspace_size_formula():
     s = la.la_plan(1, 4, 4, 64, [0, 1024], 3)
-    # header 256 + flags (3 words padded to 256) + 3 records of 1 x (64 + 2) floats
-    assert la.la_workspace_size(s) == 256 + 256 + 3 * 66 * 4
+    # header 256 + flags (3 words padded to 256) + 3 records of 1 x (64 + 2)
+    # floats, each padded to a multiple of 4 floats (68)
+    assert la.la_workspace_size(s) == 256 + 256 + 3 * 68 * 4
     g = la.la_plan(2, 16, 2, 128, [0, 100, 300], 5)
     assert la.la_workspace_size(g) == 256 + 256 + 5 * 8 * 130 * 4
 

@@ -106,6 +106,13 @@ def named(name, seed=0):
         h, b, c, d = parts["h"], parts["b"], parts["c"], parts["d"]
         return Workload(name, b, h, h, d, "f16", [c] * b,
                         description=f"sweep: batch {b}, {h}/{h} heads, d {d}, ctx {c}, fp16")
+    if name.startswith("gqa_"):
+        # grouped-query sweep shapes, e.g. gqa_h32_k8_b1_c32768_d128: batch b, h query over k kv
+        # heads, d, equal contexts, bf16
+        parts = dict((p[0], int(p[1:])) for p in name.split("_")[1:])
+        h, kv, b, c, d = parts["h"], parts["k"], parts["b"], parts["c"], parts["d"]
+        return Workload(name, b, h, kv, d, "bf16", [c] * b,
+                        description=f"GQA sweep: batch {b}, {h} query over {kv} kv heads, d {d}, ctx {c}, bf16")
     if name.startswith("spec"):
         # speculative-decoding verification: 4 draft tokens per request
         return Workload(name, 8, 32, 32, 128, "bf16", [8192] * 8, nq=4,
