@@ -82,3 +82,57 @@ def test_random_configuration(seed):
         mant = 10 if out_dt == torch.float16 else 7
         ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - mant)
         assert np.all(np.abs(got - ref) <= MAX_ABS + ulp)
+
+
+BUILT_HP = {64: [1, 2], 80: [1, 2, 8], 96: [1, 2, 4], 128: [1], 256: [1]}
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_configuration_through_la_plan_kv(seed):
+    """Token-major and paged caches through la_plan_kv: a random built count
+    of kv heads per unit (or the default), hkv a multiple of it."""
+    r = np.random.default_rng(5000 + seed)
+    d = int(r.choice(la.HEAD_DIMS))
+    hp = int(r.choice(BUILT_HP[d]))
+    hkv = hp * int(r.integers(1, 3))
+    grp = int(r.choice([1, 2, 4, 8]))
+    nq = int(r.choice([1, 1, 2, 3])) if grp * 2 <= 8 else 1
+    while grp * nq > 8:
+        nq -= 1
+    batch = int(r.integers(1, 5))
+    lengths = [int(x) for x in np.maximum(nq, np.exp(r.uniform(0, np.log(5000), size=batch)).astype(int))]
+    dt = str(r.choice(["f16", "bf16"]))
+    layout = str(r.choice(["token_major", "paged"]))
+    page = int(r.choice([16, 32, 64, 128, 256]))
+    if layout == "paged" and d == 80 and grp * nq > 2 and hp == 1 and page < 32:
+        page = 32  # 32-byte swizzled boxes need pieces of >= 1 KiB
+    grid = int(r.choice([0, 0, 1, 5, 40]))
+    heads = int(r.choice([0, hp]))  # 0: la_plan_kv's default for this shape
+    w = workloads.custom(batch, hkv * grp, hkv, d, dt, lengths, nq=nq)
+    q, k, v, cu = workloads.make_inputs(w, seed=seed, device="cuda")
+    s = la.la_plan_kv(batch, w.hq, hkv, d, cu, nq=nq, heads_per_unit=heads, num_sms=grid)
+    if heads:
+        assert s.heads_per_unit == hp
+    ws = la.new_workspace(s)
+    out = torch.empty(*q.shape, dtype=torch.float32, device="cuda")
+    cu_dev = torch.as_tensor(cu, device="cuda")
+    if layout == "token_major":
+        kc, vc = workloads.to_token_major(w, k, v)
+        la.la_decode_kv(q, kc, vc, cu_dev, s, ws, out, w.scale, layout="token_major")
+        kk = layouts.gather_token_major(kc.cpu().view(torch.int16).numpy(), cu, hkv, d)
+        vv = layouts.gather_token_major(vc.cpu().view(torch.int16).numpy(), cu, hkv, d)
+    else:
+        kc, vc, table, npages = workloads.to_paged(w, k, v, page, seed=seed)
+        la.la_decode_kv(q, kc, vc, cu_dev, s, ws, out, w.scale, layout="paged", block_table=table.cuda(),
+                        page_size=page, num_pages=npages)
+        kk = layouts.gather_paged(kc.cpu().view(torch.int16).numpy(), table.numpy(), cu, page, hkv, d)
+        vv = layouts.gather_paged(vc.cpu().view(torch.int16).numpy(), table.numpy(), cu, page, hkv, d)
+    assert la.la_get_status(ws) == la.LA_OK
+    kk, vv = kk.astype(np.int16).view(np.uint16), vv.astype(np.int16).view(np.uint16)
+    code = oracle.F16 if dt == "f16" else oracle.BF16
+    ref = oracle.attend(q.cpu(), kk, vv, cu, w.hq, hkv, d, w.scale, code, nq=nq)
+    got = out.double().cpu().numpy().reshape(ref.shape)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref).max()
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
