@@ -221,9 +221,10 @@ def run_reference(args, rank, world):
     q, k, v, cu = workloads.make_inputs(w, seed=args.seed, device="cpu")
     code = {"f16": oracle.F16, "bf16": oracle.BF16}[w.dtype]
     cores = os.cpu_count() or 1
-    nrows = w.batch * w.hq
-    grp = w.hq // w.hkv
-    row_bytes = np.array([2 * (cu[r // w.hq + 1] - cu[r // w.hq]) * w.d * 2 / grp for r in range(nrows)])
+    nrows = w.batch * w.nq * w.hq  # row r = (b * nq + i) * hq + h
+    rows_per_kv = (w.hq // w.hkv) * w.nq
+    row_bytes = np.array([2 * (cu[r // (w.nq * w.hq) + 1] - cu[r // (w.nq * w.hq)]) * w.d * 2 / rows_per_kv
+                          for r in range(nrows)])
     per_step = cores
     qn, kn, vn = (t.view(torch.int16).numpy().view(np.uint16) for t in (q, k, v))
     pos = 0
@@ -232,7 +233,7 @@ def run_reference(args, rank, world):
         nonlocal pos
         rows = np.array([(pos + i) % nrows for i in range(per_step)], dtype=np.int64)
         pos = (pos + per_step) % nrows
-        oracle.attend(qn, kn, vn, cu, w.hq, w.hkv, w.d, w.scale, code, rows=rows, threads=cores)
+        oracle.attend(qn, kn, vn, cu, w.hq, w.hkv, w.d, w.scale, code, rows=rows, threads=cores, nq=w.nq)
         return float(row_bytes[rows].sum())
 
     for _ in range(args.warmup):
@@ -243,14 +244,15 @@ def run_reference(args, rank, world):
         total += step()
     dt = time.perf_counter() - t0
     gbs = total / dt / 1e9
-    sample = (f"{per_step} (request, head) rows per step, cycling over the {nrows} rows of the "
+    sample = (f"{per_step} (request, query, head) rows per step, cycling over the {nrows} rows of the "
               f"workload; float64 two-pass softmax over the exact {w.dtype} inputs")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.description, "seed": args.seed},
+        "config": {"workload": w.description, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
+                   "total_context_tokens": w.total_tokens, "kv_bytes": w.kv_bytes(), "seed": args.seed},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -258,7 +260,9 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(w, q, k, v, cu, seconds):
+def cpu_baseline(w, q, k, v, cu, seconds, single_seconds=2.0):
+    """The float64 oracle on the host cores over the workload's rows, cycled,
+    for about `seconds`; then the same with one thread for `single_seconds`."""
     import numpy as np
     import torch
 
@@ -267,23 +271,32 @@ def cpu_baseline(w, q, k, v, cu, seconds):
     code = {"f16": oracle.F16, "bf16": oracle.BF16}[w.dtype]
     cores = os.cpu_count() or 1
     qn, kn, vn = (t.view(torch.int16).numpy().view(np.uint16) for t in (q, k, v))
-    nrows = w.batch * w.hq
-    grp = w.hq // w.hkv
-    row_bytes = np.array([2 * (cu[r // w.hq + 1] - cu[r // w.hq]) * w.d * 2 / grp for r in range(nrows)])
-    # rows in chunks of one per core until the time budget is spent (at least one chunk)
-    t0 = time.perf_counter()
-    done, pos = 0.0, 0
-    while True:
-        rows = np.array([(pos + i) % nrows for i in range(cores)], dtype=np.int64)
-        pos = (pos + cores) % nrows
-        oracle.attend(qn, kn, vn, cu, w.hq, w.hkv, w.d, w.scale, code, rows=rows, threads=cores)
-        done += float(row_bytes[rows].sum())
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
+    nrows = w.batch * w.nq * w.hq  # row r = (b * nq + i) * hq + h
+    rows_per_kv = (w.hq // w.hkv) * w.nq
+    row_bytes = np.array([2 * (cu[r // (w.nq * w.hq) + 1] - cu[r // (w.nq * w.hq)]) * w.d * 2 / rows_per_kv
+                          for r in range(nrows)])
+
+    def run(threads, budget):
+        # rows in chunks of one per thread until the time budget is spent (at least one chunk)
+        t0 = time.perf_counter()
+        done, pos, evals = 0.0, 0, 0
+        while True:
+            rows = np.array([(pos + i) % nrows for i in range(threads)], dtype=np.int64)
+            pos = (pos + threads) % nrows
+            oracle.attend(qn, kn, vn, cu, w.hq, w.hkv, w.d, w.scale, code, rows=rows, threads=threads, nq=w.nq)
+            done += float(row_bytes[rows].sum())
+            evals += threads
+            if time.perf_counter() - t0 >= budget:
+                break
+        return done, evals, time.perf_counter() - t0
+
+    done, evals, dt = run(cores, seconds)
+    d1, e1, t1 = run(1, single_seconds)
     return {"value": round(done / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{int(round(done / w.kv_bytes() * nrows))} row evaluations (the workload's "
-                      f"{nrows} (request, head) rows, cycled) in {dt:.1f} s, {cores} rows at a time"}
+            "sample": f"{evals} row evaluations (the workload's {nrows} (request, query, head) rows, "
+                      f"cycled) in {dt:.1f} s, {cores} rows at a time",
+            "single_thread": {"value": round(d1 / t1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"{e1} row evaluations in {t1:.1f} s on one thread"}}
 
 
 # ------------------------------------------------------------------ our arm
@@ -427,6 +440,7 @@ def run_ours(args, rank, world, local_rank):
     cta_trace = summarize_trace(trace.view(G, la.TRACE_WORDS).cpu().numpy())
 
     kv_bytes, algo_bytes = algorithmic_bytes(w, la.la_schedule_export(dec.sched), out.element_size())
+    ws_bytes = algo_bytes - kv_bytes - q.numel() * q.element_size() - out.numel() * out.element_size()
     value = world * kv_bytes / (mean_ms * 1e-3) / 1e9
 
     e2e = None
@@ -496,7 +510,9 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": "measured hbm_gbs (copy, burst)" if peaks else "fallback 6.8 TB/s",
                      "traffic": (profiled_traffic(profile_name(args.workload, args.kv_layout, args.page_size))
                                  if args.kernel == "lean" and args.heads_per_unit == 0 else None),
-                     "algorithmic_bytes_per_launch": algo_bytes},
+                     "algorithmic_bytes_per_launch": algo_bytes,
+                     "workspace_bytes_per_call": ws_bytes,
+                     "workspace_frac_of_kv": round(ws_bytes / kv_bytes, 6)},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "cta_trace": cta_trace,
