@@ -174,7 +174,9 @@ int la_schedule_grid(const la_schedule* s);
 
 /*
  * Bytes of device workspace la_decode needs for this schedule: a header, G
- * ready flags and G partial records of grp * (d + 2) floats ("7.4
+ * ready flags and G partial records of rows * (d + 2) floats, rounded up to
+ * a multiple of 4 floats (rows = query rows per kv head, rounded up to 1, 2,
+ * 4 or 8, times the kv heads per unit) ("7.4
  * limitations": a small amount of global memory for sharing partial
  * results). Zero it once (la_workspace_init) before its first use; after
  * that it needs no clearing between calls. One workspace must not be used
