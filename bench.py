@@ -86,8 +86,9 @@ def profile_name(workload, kv_layout="slab", page_size=0):
     return f"lean_decode_kernel_{workload}{suffix}"
 
 
-def profiled_traffic(name):
-    """DRAM bytes per launch from the committed ncu summary, if it is for this kernel source."""
+def profiled_traffic(name, d, tile):
+    """DRAM bytes per launch from the committed ncu summary, if it is for this
+    kernel source and this kernel instance (head dim, LeanTile)."""
     path = os.path.join(ROOT, "profiles", f"{name}.md")
     try:
         text = open(path).read()
@@ -95,7 +96,10 @@ def profiled_traffic(name):
         return None
     src = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
     tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not src or not tr or src.group(1) != kernel_source_digest():
+    inst = re.search(r"lean_decode_kernel<(\d+), (\d+),", text)
+    if not src or not tr or not inst or src.group(1) != kernel_source_digest():
+        return None
+    if (int(inst.group(1)), int(inst.group(2))) != (d, tile):
         return None
     return int(tr.group(1))
 
@@ -508,7 +512,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": "measured hbm_gbs (copy, burst)" if peaks else "fallback 6.8 TB/s",
-                     "traffic": (profiled_traffic(profile_name(args.workload, args.kv_layout, args.page_size))
+                     "traffic": (profiled_traffic(profile_name(args.workload, args.kv_layout, args.page_size),
+                                                  w.d, la.la_schedule_export(dec.sched)[4])
                                  if args.kernel == "lean" and args.heads_per_unit == 0 else None),
                      "algorithmic_bytes_per_launch": algo_bytes,
                      "workspace_bytes_per_call": ws_bytes,

@@ -19,7 +19,9 @@ LA_OK, LA_ERR_INVALID, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_W
 LA_F16, LA_BF16 = 0, 1
 LA_OUT_F32, LA_OUT_F16, LA_OUT_BF16 = 0, 1, 2
 HEAD_DIMS = (64, 80, 96, 128, 256)
-TILE_SIZES = {64: (256, 128), 80: (128,), 96: (128,), 128: (128, 64), 256: (64,)}  # first = default
+# built LeanTile sizes; the first is the review's table size (the default, except at
+# d = 128 with <= 2 query rows per kv head on the slab layout, where it is 64)
+TILE_SIZES = {64: (256, 128), 80: (128,), 96: (128,), 128: (128, 64), 256: (64,)}
 SEG_WHOLE, SEG_NONHOST, SEG_HOST, SEG_PARTIAL = range(4)
 KV_SLAB, KV_TOKEN_MAJOR, KV_PAGED = range(3)
 

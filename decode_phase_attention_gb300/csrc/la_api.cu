@@ -163,13 +163,13 @@ void build_dev_segs(la_schedule* s) {
 }
 
 la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, int kind, int grid_or_splits,
-                        la_schedule** out, int tile = 0, int hp = 1) {
+                        la_schedule** out, int tile = 0, int hp = 1, int rows = 0) {
   if (out == nullptr) return LA_ERR_INVALID;
   *out = nullptr;
   const la_status st = check_shape(batch, hq, hkv, d, cu);
   if (st != LA_OK) return st;
   if (hp < 1 || hkv % hp != 0) return LA_ERR_INVALID;
-  if (tile == 0) tile = la::default_tile(d) / hp;
+  if (tile == 0) tile = hp == 1 ? la::slab_tile(d, rows > 0 ? rows : hq / hkv) : la::default_tile(d) / hp;
   if (tile < 0) return LA_ERR_INVALID;
   if (!la::tile_supported(d, tile, hp)) return LA_ERR_UNSUPPORTED;
   la_schedule* s = new (std::nothrow) la_schedule();
@@ -334,6 +334,8 @@ double predict_seconds(const la_schedule* s, int slots) {
 
 namespace la {
 
+int slab_tile(int d, int rows) { return (d == 128 && rows <= 2) ? 64 : default_tile(d); }
+
 int default_tile(int d) {
   switch (d) {
     case 64: return 256;   // the review's LeanTile table
@@ -489,7 +491,7 @@ la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlen
   if (G <= 0) {
     const la_status st = check_shape(batch, hq, hkv, d, cu_seqlens_k);
     if (st != LA_OK) return st;
-    const int T = tile_tokens == 0 ? la::default_tile(d) : tile_tokens;
+    const int T = tile_tokens == 0 ? la::slab_tile(d, hq / hkv) : tile_tokens;
     if (T <= 0) return LA_ERR_INVALID;
     if (!la::tile_supported(d, T)) return LA_ERR_UNSUPPORTED;
     int sms = 0, per_sm = 0;
@@ -524,12 +526,12 @@ la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t*
     int sms = 0, per_sm = 0;
     st = device_sms(&sms);
     if (st != LA_OK) return st;
-    st = capacity(d, la::default_tile(d), R, &per_sm);
+    st = capacity(d, la::slab_tile(d, rows), R, &per_sm);
     if (st != LA_OK) return st;
     G = sms * std::max(1, per_sm);
   }
   if (G > kMaxGrid) return LA_ERR_INVALID;
-  st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out);
+  st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out, 0, 1, rows);
   if (st != LA_OK) return st;
   (*out)->nq = nq;
   (*out)->R = R;
@@ -597,7 +599,7 @@ la_status la_plan_auto(int batch, int hq, int hkv, int d, const int32_t* cu_seql
     int sms = 0, per_sm = 0;
     st = device_sms(&sms);
     if (st != LA_OK) return st;
-    st = capacity(d, la::default_tile(d), hq / hkv, &per_sm);
+    st = capacity(d, la::slab_tile(d, hq / hkv), hq / hkv, &per_sm);
     if (st != LA_OK) return st;
     slots = sms * std::max(1, per_sm);
   }

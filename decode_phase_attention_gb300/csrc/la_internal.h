@@ -106,6 +106,10 @@ struct CParams {            // fixed-split merge launch
 // LeanTile sizes: the default per head dim, and whether (d, T) is built for
 // units of hp kv heads (T tokens of each head per tile).
 int default_tile(int d);
+// Default LeanTile of a slab-layout schedule with `rows` query rows per kv
+// head: the table's size, except 64 tokens at d = 128 on the CUDA-core path
+// (rows <= 2), which measured 1.1-1.3 % faster on GB300.
+int slab_tile(int d, int rows);
 bool tile_supported(int d, int T, int hp = 1);
 
 // Launches (la_kernels_d<d>.cu, one file per head dim; la_kernels_d<d>_hp<h>.cu

@@ -90,8 +90,9 @@ enum {
  *                      later CTAs inside the launch.
  *   out                receives the new schedule
  *
- * Rules: tiles(b) = ceil(L_b / T), T = 256 (d = 64) or 128 (d = 128),
- * for other head dims the default of la_plan_ex;
+ * Rules: tiles(b) = ceil(L_b / T) with the default T of la_plan_ex
+ * (the review's table: 256 at d = 64, 128 at d = 128; 64 at d = 128 with
+ * one or two query heads per kv head, measured faster on GB300);
  * units (b, kv head) in request-major order; I = total tiles; CTA g takes
  * floor(I/G) iterations plus one if g < I mod G, in order; the host of a
  * unit is the CTA holding its first tile, the finisher the one holding its
@@ -108,11 +109,16 @@ la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k
  *
  *   d            64, 80, 96, 128 or 256
  *   tile_tokens  0 for the default of d, else one of the built sizes:
- *                d = 64: 256 (default) or 128;  d = 128: 128 (default) or 64;
+ *                d = 64: 256 (default) or 128;  d = 128: 128 or 64;
  *                d = 80, 96: 128;  d = 256: 64.
  *                The table gives 256 and 128 tokens for d = 64 and 128
  *                (64 KiB of K+V per tile); the other defaults keep a tile
- *                near that size (40, 48 and 64 KiB).
+ *                near that size (40, 48 and 64 KiB). At d = 128 the default
+ *                is 64 when a unit has at most 2 query rows (group x query
+ *                tokens; the CUDA-core tile path): on GB300 the smaller
+ *                tile measured 1.1-1.3 % faster on uniform, ragged and
+ *                512k-context batches; with 4-8 rows (tensor-core path)
+ *                the table's 128 stays faster (2-3 %).
  * Other arguments and rules as la_plan. LA_ERR_UNSUPPORTED for a (d, T)
  * that is not built.
  */
@@ -277,7 +283,9 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
  *                   divides hkv, else the most built count that divides
  *                   hkv, else 1 (always 1 for d = 128, 256).
  *   tile_tokens     tokens of each head per tile; 0 picks the default:
- *                   la_plan_ex's divided by heads_per_unit, so a tile still
+ *                   the review's table size of d (128 at d = 128 also for
+ *                   one or two query rows: 16-token pages read 13 % slower
+ *                   with 64) divided by heads_per_unit, so a tile still
  *                   holds the same bytes (only these defaults are built for
  *                   more than one head per unit).
  *   num_sms, out    as la_plan

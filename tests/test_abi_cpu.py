@@ -33,6 +33,30 @@ def cu_of(lengths):
     return [0] + np.cumsum(lengths).tolist()
 
 
+def lib_tile(d, rows):
+    """The library's default LeanTile on the slab layout: the review's table
+    (the reference planner's) for d = 64 and 128, except 64 tokens at d = 128
+    with <= 2 query rows; 40-64 KiB tiles for the other head dims."""
+    if d in (64, 128):
+        return 64 if d == 128 and rows <= 2 else P.lean_tile(d)
+    return {80: 128, 96: 128, 256: 64}[d]
+
+
+@pytest.mark.parametrize("d", la.HEAD_DIMS)
+@pytest.mark.parametrize("grp", [1, 2, 4, 8])
+def test_default_lean_tile(d, grp):
+    expect = {64: 256, 80: 128, 96: 128, 256: 64, 128: 64 if grp <= 2 else 128}[d]
+    for s in (la.la_plan(2, 2 * grp, 2, d, [0, 900, 1000], 7), la.la_plan_fixed(2, 2 * grp, 2, d, [0, 900, 1000], 2)):
+        assert la.la_schedule_export(s)[4] == expect
+    if grp <= 2:  # query rows = group x query tokens decide it
+        nq = 8 // grp
+        assert la.la_schedule_export(la.la_plan_spec(1, 2 * grp, 2, d, nq, [0, 900], 7))[4] == \
+            {64: 256, 80: 128, 96: 128, 256: 64, 128: 128}[d]
+    # caches keep the table's size (divided over the kv heads of a unit)
+    s = la.la_plan_kv(1, 2 * grp, 2, d, [0, 900], heads_per_unit=1, num_sms=7)
+    assert la.la_schedule_export(s)[4] == {64: 256, 80: 128, 96: 128, 256: 64, 128: 128}[d]
+
+
 def shapes():
     r = np.random.default_rng(123)
     out = [(1, 4, 4, 64, [1024], 3), (8, 32, 32, 128, [8192] * 8, 148), (8, 32, 32, 128, [8192] * 8, 152),
@@ -51,7 +75,8 @@ def shapes():
 def test_planner_matches_reference_planner_exactly(shape):
     batch, hq, hkv, d, lengths, G = shape
     s = la.la_plan(batch, hq, hkv, d, cu_of(lengths), G)
-    assert la.la_schedule_export(s) == P.export(P.plan_lean(batch, hq, hkv, d, cu_of(lengths), G))
+    T = lib_tile(d, hq // hkv)
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(batch, hq, hkv, d, cu_of(lengths), G, T))
     assert s.grid == G
 
 
@@ -61,14 +86,15 @@ def test_planner_matches_on_the_ragged_and_gqa_workloads():
         w = workloads.named(name)
         for G in (148, 152, 304):
             s = la.la_plan(w.batch, w.hq, w.hkv, w.d, w.cu, G)
-            assert la.la_schedule_export(s) == P.export(P.plan_lean(w.batch, w.hq, w.hkv, w.d, w.cu.tolist(), G))
+            T = lib_tile(w.d, w.hq // w.hkv)
+            assert la.la_schedule_export(s) == P.export(P.plan_lean(w.batch, w.hq, w.hkv, w.d, w.cu.tolist(), G, T))
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 5, 16])
 def test_fixed_planner_matches_reference(splits):
     lengths = [1000, 17, 4096, 129, 8000]
     s = la.la_plan_fixed(5, 8, 2, 128, cu_of(lengths), splits)
-    assert la.la_schedule_export(s) == P.export(P.plan_fixed(5, 8, 2, 128, cu_of(lengths), splits))
+    assert la.la_schedule_export(s) == P.export(P.plan_fixed(5, 8, 2, 128, cu_of(lengths), splits, 128))
 
 
 @pytest.mark.parametrize("args,status", [
@@ -145,9 +171,10 @@ def test_auto_plan_is_exactly_one_of_the_explicit_partitions(shape):
     s, kind, pred = la.la_plan_auto(batch, hq, hkv, d, cu, 152)
     assert len(pred) == 3 and all(p > 0 for p in pred)
     units = batch * hkv
-    explicit = {"lean": P.plan_lean(batch, hq, hkv, d, cu, 152),
-                "naive": P.plan_fixed(batch, hq, hkv, d, cu, 1),
-                "fixed_split": P.plan_fixed(batch, hq, hkv, d, cu, max(2, -(-152 // units)))}
+    T = lib_tile(d, hq // hkv)
+    explicit = {"lean": P.plan_lean(batch, hq, hkv, d, cu, 152, T),
+                "naive": P.plan_fixed(batch, hq, hkv, d, cu, 1, T),
+                "fixed_split": P.plan_fixed(batch, hq, hkv, d, cu, max(2, -(-152 // units)), T)}
     assert la.la_schedule_export(s) == P.export(explicit[kind])
     idx = ["lean", "naive", "fixed_split"].index(kind)
     assert pred[idx] == min(pred)
@@ -185,9 +212,9 @@ def test_planner_parity_for_every_head_dim_and_tile_size(d):
             s = la.la_plan(batch, hkv * grp, hkv, d, cu_of(lengths), G, tile_tokens=T)
             assert la.la_schedule_export(s)[4] == T
             assert la.la_schedule_export(s) == P.export(P.plan_lean(batch, hkv * grp, hkv, d, cu_of(lengths), G, T))
-    # the default tile of every head dim
+    # the default tile of every head dim (one query row per kv head)
     s = la.la_plan(1, 2, 2, d, [0, 1000], 7)
-    assert la.la_schedule_export(s)[4] == la.TILE_SIZES[d][0]
+    assert la.la_schedule_export(s)[4] == lib_tile(d, 1)
 
 
 @pytest.mark.parametrize("d,T", [(64, 64), (64, 512), (128, 256), (80, 64), (256, 128), (96, 256)])
