@@ -169,7 +169,10 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   const la_status st = check_shape(batch, hq, hkv, d, cu);
   if (st != LA_OK) return st;
   if (hp < 1 || hkv % hp != 0) return LA_ERR_INVALID;
-  if (tile == 0) tile = hp == 1 ? la::slab_tile(d, rows > 0 ? rows : hq / hkv) : la::default_tile(d) / hp;
+  // stream-K on the slab layout: slab_tile; the fixed partitions keep the
+  // table's tile (with few busy SMs each CTA needs the deeper 192 KiB ring)
+  if (tile == 0)
+    tile = (hp == 1 && kind == 0) ? la::slab_tile(d, rows > 0 ? rows : hq / hkv) : la::default_tile(d) / hp;
   if (tile < 0) return LA_ERR_INVALID;
   if (!la::tile_supported(d, tile, hp)) return LA_ERR_UNSUPPORTED;
   la_schedule* s = new (std::nothrow) la_schedule();

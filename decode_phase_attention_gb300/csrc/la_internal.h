@@ -106,9 +106,10 @@ struct CParams {            // fixed-split merge launch
 // LeanTile sizes: the default per head dim, and whether (d, T) is built for
 // units of hp kv heads (T tokens of each head per tile).
 int default_tile(int d);
-// Default LeanTile of a slab-layout schedule with `rows` query rows per kv
-// head: the table's size, except 64 tokens at d = 128 on the CUDA-core path
-// (rows <= 2), which measured 1.1-1.3 % faster on GB300.
+// Default LeanTile of a stream-K slab-layout schedule with `rows` query rows
+// per kv head: the table's size, except 64 tokens at d = 128 on the CUDA-core
+// path (rows <= 2), which measured 1.1-1.3 % faster on GB300 with every SM
+// busy.
 int slab_tile(int d, int rows);
 bool tile_supported(int d, int T, int hp = 1);
 

@@ -118,7 +118,9 @@ la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k
  *                tokens; the CUDA-core tile path): on GB300 the smaller
  *                tile measured 1.1-1.3 % faster on uniform, ragged and
  *                512k-context batches; with 4-8 rows (tensor-core path)
- *                the table's 128 stays faster (2-3 %).
+ *                the table's 128 stays faster (2-3 %), and so it does for
+ *                la_plan_fixed, whose few busy SMs each need the deeper
+ *                shared-memory ring of the larger tile.
  * Other arguments and rules as la_plan. LA_ERR_UNSUPPORTED for a (d, T)
  * that is not built.
  */

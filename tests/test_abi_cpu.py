@@ -46,8 +46,10 @@ def lib_tile(d, rows):
 @pytest.mark.parametrize("grp", [1, 2, 4, 8])
 def test_default_lean_tile(d, grp):
     expect = {64: 256, 80: 128, 96: 128, 256: 64, 128: 64 if grp <= 2 else 128}[d]
-    for s in (la.la_plan(2, 2 * grp, 2, d, [0, 900, 1000], 7), la.la_plan_fixed(2, 2 * grp, 2, d, [0, 900, 1000], 2)):
-        assert la.la_schedule_export(s)[4] == expect
+    table = {64: 256, 80: 128, 96: 128, 256: 64, 128: 128}[d]
+    assert la.la_schedule_export(la.la_plan(2, 2 * grp, 2, d, [0, 900, 1000], 7))[4] == expect
+    # the fixed partitions keep the table's size
+    assert la.la_schedule_export(la.la_plan_fixed(2, 2 * grp, 2, d, [0, 900, 1000], 2))[4] == table
     if grp <= 2:  # query rows = group x query tokens decide it
         nq = 8 // grp
         assert la.la_schedule_export(la.la_plan_spec(1, 2 * grp, 2, d, nq, [0, 900], 7))[4] == \
@@ -173,8 +175,8 @@ def test_auto_plan_is_exactly_one_of_the_explicit_partitions(shape):
     units = batch * hkv
     T = lib_tile(d, hq // hkv)
     explicit = {"lean": P.plan_lean(batch, hq, hkv, d, cu, 152, T),
-                "naive": P.plan_fixed(batch, hq, hkv, d, cu, 1, T),
-                "fixed_split": P.plan_fixed(batch, hq, hkv, d, cu, max(2, -(-152 // units)), T)}
+                "naive": P.plan_fixed(batch, hq, hkv, d, cu, 1),
+                "fixed_split": P.plan_fixed(batch, hq, hkv, d, cu, max(2, -(-152 // units)))}
     assert la.la_schedule_export(s) == P.export(explicit[kind])
     idx = ["lean", "naive", "fixed_split"].index(kind)
     assert pred[idx] == min(pred)
