@@ -235,3 +235,14 @@ def test_offsets_beyond_two_to_the_31_elements():
     compare(out.view(32, 128)[rows].cpu(), ref)
     del q, k, v
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("batch,hq,hkv,d,hi", [(4096, 4, 4, 128, 64), (1500, 16, 2, 64, 600), (700, 8, 1, 128, 3000)])
+def test_many_short_requests(batch, hq, hkv, d, hi):
+    # thousands of units of a few tiles each: most CTAs run long lists of whole units
+    lengths = workloads.ragged_lengths(batch, 1, hi, seed=batch, log_uniform=True)
+    w = workloads.custom(batch, hq, hkv, d, "bf16", lengths)
+    q, k, v, _ = workloads.make_inputs(w, seed=batch, device="cuda")
+    out, dec = run_lean(w, q, k, v)
+    assert dec.sched.grid > 0
+    compare(out.cpu(), reference(w, q, k, v))
