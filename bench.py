@@ -69,14 +69,23 @@ def measured_peaks():
         return None
 
 
-def kernel_source_digest():
-    """Digest of the device-code sources (kernel template, its parameters and instances)."""
+def _code_only(text):
+    """Source text without comments and with whitespace collapsed."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_digest(csrc=None):
+    """Digest of the device code (kernel template, its parameters and
+    instances), comments and layout ignored: a profile stays valid across
+    edits that change no code."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "decode_phase_attention_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "decode_phase_attention_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f == "la_kernel.cuh" or f == "la_internal.h" or f.startswith("la_kernels_"):
             h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            h.update(_code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -13,10 +13,12 @@
 //   kPartial  fixed-split baseline piece: write the partial, no flag
 //
 // Warp roles (288 threads, one CTA per SM):
-//   warp 8, lane 0: producer. Streams the K and V rows of each LeanTile of
-//                   every segment, in order, from HBM into a 3-stage
-//                   shared-memory ring (completion counted in bytes on one
-//                   mbarrier per stage).
+//   warp 8:         producer. Streams the K and V rows of each LeanTile of
+//                   every segment, in order, from HBM into a shared-memory
+//                   ring of 2-4 stages (completion counted in bytes on one
+//                   mbarrier per stage); lane 0 issues the slab copies, lane
+//                   i the i-th page piece of a tile of a token-major or paged
+//                   cache.
 //   warps 0-7:      consumers. Each takes T/8 consecutive tokens of the tile
 //                   and keeps online-softmax statistics m, l and the
 //                   unnormalised output in fp32 ("3.3 LeanTile": S_f = Q K^T,
@@ -36,7 +38,9 @@
 //     movmatrix, and is split into a bf16/fp16 high and low part so that
 //     the P.V product keeps fp32-level accuracy.
 // At the end of a segment the lanes of a warp and then the 8 warps merge
-// with f (the warps through shared memory).
+// with f (the warps through shared memory); a host CTA then merges the
+// partials of the unit's later CTAs (staged in the idle ring when there
+// are many of them).
 //
 // Units of HP > 1 kv heads (token-major and paged caches with short rows):
 // a tile holds T tokens of each of the unit's HP heads, loaded as the cache
