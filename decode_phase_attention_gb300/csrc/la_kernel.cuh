@@ -262,7 +262,11 @@ struct Cfg {
   static constexpr int KS = D / 16;                 // 16-wide steps over the head dim
   static constexpr int TILE_ELEMS = ROWS * D;
   static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
-  static constexpr int STAGES = cmax(2, cmin(4, 196608 / STAGE_BYTES));
+  // ring of 2-4 stages within 192 KiB, but 128 KiB for the tensor-core path at
+  // d = 128: with every SM streaming, fewer bytes in flight measured 1-6 % faster
+  // there on GB300 (and 2-4 % slower at d = 64 and 256)
+  static constexpr int RING_BYTES = (D == 128 && TC) ? 131072 : 196608;
+  static constexpr int STAGES = cmax(2, cmin(4, RING_BYTES / STAGE_BYTES));
   static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
   static constexpr int REC = D + 2;                 // [m, l, O[d]]
   static constexpr int RS = record_stride(D, HP * GRP);  // floats per CTA record in the workspace
