@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--out-dtype", default="f32", choices=["f32", "f16", "bf16"])
     ap.add_argument("--kv-layout", default="slab", choices=["slab", "token_major", "paged"])
     ap.add_argument("--page-size", type=int, default=64)
+    ap.add_argument("--stages", type=int, default=0, help="ring stages (0: the library's choice)")
     ap.add_argument("--heads-per-unit", type=int, default=0,
                     help="token-major / paged caches: kv heads per unit (0 = la_plan_kv's choice)")
     ap.add_argument("--seed", type=int, default=0)
@@ -350,6 +351,8 @@ def run_ours(args, rank, world, local_rank):
         per_sm, sms = la.la_device_capacity(w.d, w.hq // w.hkv)
         splits = -(-sms // (w.batch * w.hkv))
         dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, device=dev, fixed_splits=max(1, splits))
+    if args.stages:
+        la.la_schedule_set_stages(dec.sched, args.stages)
     G = dec.sched.grid
     launches_per_call = 2 if (dec.kind == "fixed_split" and dec.sched.grid > w.batch * w.hkv) else 1
     stream = torch.cuda.current_stream(dev)
@@ -505,6 +508,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.description, "kernel": args.kernel, "schedule": dec.kind,
                    "tile_tokens": la.la_schedule_export(dec.sched)[4], "out_dtype": args.out_dtype,
                    "kv_heads_per_unit": dec.sched.heads_per_unit,
+                   "ring_stages": args.stages or "library default",
                    "kv_layout": args.kv_layout + (f" (page {args.page_size})" if args.kv_layout == "paged" else ""),
                    "predicted_us": dec.predicted_us, "grid": G,
                    "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,

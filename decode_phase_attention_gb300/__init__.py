@@ -32,7 +32,8 @@ class KvDesc(ctypes.Structure):
                 ("page_size", ctypes.c_int), ("num_pages", ctypes.c_longlong)]
 EXPORTED = ["la_plan", "la_plan_ex", "la_plan_spec", "la_plan_kv", "la_plan_fixed", "la_plan_auto", "la_decode_ex", "la_decode_kv", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
             "la_decode", "la_decode_static", "la_get_status", "la_schedule_export_size", "la_schedule_export",
-            "la_schedule_set_debug", "la_schedule_set_trace", "la_device_capacity", "la_schedule_destroy",
+            "la_schedule_set_debug", "la_schedule_set_stages", "la_schedule_set_trace", "la_device_capacity",
+            "la_schedule_destroy",
             "la_status_string"]
 
 
@@ -67,6 +68,7 @@ def _load():
         "la_schedule_export_size": (c_size, [vp]),
         "la_schedule_export": (c_int, [vp, vp, c_size]),
         "la_schedule_set_debug": (c_int, [vp, c_int, c_ll]),
+        "la_schedule_set_stages": (c_int, [vp, c_int]),
         "la_schedule_set_trace": (c_int, [vp, vp]),
         "la_device_capacity": (c_int, [c_int, c_int, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
         "la_schedule_destroy": (None, [vp]),
@@ -214,6 +216,11 @@ def la_schedule_export(sched):
 def la_schedule_set_debug(sched, skip_signal_cta=-1, spin_timeout_ns=2_000_000_000):
     _check(_lib.la_schedule_set_debug(sched.handle, int(skip_signal_cta), int(spin_timeout_ns)),
            "la_schedule_set_debug")
+
+
+def la_schedule_set_stages(sched, stages=0):
+    """Ring stages the decode kernel cycles through (0: the library's choice)."""
+    _check(_lib.la_schedule_set_stages(sched.handle, int(stages)), "la_schedule_set_stages")
 
 
 def la_schedule_set_trace(sched, trace=None):

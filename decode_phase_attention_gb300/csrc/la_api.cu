@@ -339,6 +339,17 @@ namespace la {
 
 int slab_tile(int d, int rows) { return (d == 128 && rows <= 2) ? 64 : default_tile(d); }
 
+int stream_stages(int d, int T, int hp, int kv_layout) {
+  // Measured on one GB300 (us per call, library default vs the whole ring):
+  // d 96, 48 KiB stages: 3 of 4 (slab 229.5 vs 232.7; token-major with 4
+  // kv heads per unit 239.3 vs 243.2); d 128 with 128-token tiles: 2 of 3
+  // (GQA d128 55.4 vs 59.2, at batch 1 35.2 vs 37.1; paged 16-token pages
+  // 164.7 vs 172.7), except token-major caches (161.4 vs 159.0 with 3).
+  if (d == 96 && T * hp == 128) return 3;
+  if (d == 128 && T == 128 && hp == 1 && kv_layout != kKvTokenMajor) return 2;
+  return 0;
+}
+
 int default_tile(int d) {
   switch (d) {
     case 64: return 256;   // the review's LeanTile table
@@ -738,6 +749,7 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
   p.grp = s->grp;
   p.nq = s->nq;
   p.rows = s->grp * s->nq;
+  p.stages = s->stages > 0 ? s->stages : (s->kind == 0 ? la::stream_stages(s->d, s->T, s->hp, kv_layout) : 0);
   cudaError_t ce = la::launch_decode(s->d, s->T, s->R, s->hp, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {
@@ -815,6 +827,12 @@ la_status la_schedule_set_debug(la_schedule* s, int skip_signal_cta, long long s
   if (s == nullptr || spin_timeout_ns <= 0) return LA_ERR_INVALID;
   s->skip_signal = skip_signal_cta;
   s->spin_ns = spin_timeout_ns;
+  return LA_OK;
+}
+
+la_status la_schedule_set_stages(la_schedule* s, int stages) {
+  if (s == nullptr || stages < 0 || stages > 4 || stages == 1) return LA_ERR_INVALID;
+  s->stages = stages;
   return LA_OK;
 }
 

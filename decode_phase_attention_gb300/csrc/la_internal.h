@@ -74,6 +74,7 @@ struct KParams {
   int bt_stride = 0;
   int page_size = 0;                     // paged: tokens per page
   int box_rows = 0;                      // 3-D TMA: token rows per load (T, or the page size if smaller)
+  int stages = 0;                        // ring stages to cycle through (0: all the instance holds)
 };
 
 // Per-CTA trace record (globaltimer ns): written when KParams::trace is set.
@@ -111,6 +112,11 @@ int default_tile(int d);
 // path (rows <= 2), which measured 1.1-1.3 % faster on GB300 with every SM
 // busy.
 int slab_tile(int d, int rows);
+// Ring stages a stream-K launch over every SM uses (0: all the instance
+// holds). With every SM streaming, fewer bytes in flight per SM measured
+// faster at d = 96 and at d = 128 with 128-token tiles (slab and paged
+// layouts); partitions with few busy SMs keep the whole ring.
+int stream_stages(int d, int T, int hp, int kv_layout);
 bool tile_supported(int d, int T, int hp = 1);
 
 // Launches (la_kernels_d<d>.cu, one file per head dim; la_kernels_d<d>_hp<h>.cu

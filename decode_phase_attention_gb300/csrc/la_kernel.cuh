@@ -262,11 +262,9 @@ struct Cfg {
   static constexpr int KS = D / 16;                 // 16-wide steps over the head dim
   static constexpr int TILE_ELEMS = ROWS * D;
   static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
-  // ring of 2-4 stages within 192 KiB, but 128 KiB for the tensor-core path at
-  // d = 128: with every SM streaming, fewer bytes in flight measured 1-6 % faster
-  // there on GB300 (and 2-4 % slower at d = 64 and 256)
-  static constexpr int RING_BYTES = (D == 128 && TC) ? 131072 : 196608;
-  static constexpr int STAGES = cmax(2, cmin(4, RING_BYTES / STAGE_BYTES));
+  // shared memory for a ring of 2-4 stages within 192 KiB; a launch may use
+  // fewer of them (KParams::stages)
+  static constexpr int STAGES = cmax(2, cmin(4, 196608 / STAGE_BYTES));
   static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
   static constexpr int REC = D + 2;                 // [m, l, O[d]]
   static constexpr int RS = record_stride(D, HP * GRP);  // floats per CTA record in the workspace
@@ -336,6 +334,14 @@ __device__ __forceinline__ bool unit_offsets_ok(const KParams& p, int b) {
   return p.cu[b] == p.sched_cu[b] && p.cu[b + 1] == p.sched_cu[b + 1];
 }
 
+// Stages of the ring this launch cycles through: the host's choice
+// (KParams::stages) within [2, STAGES]; 0 (or out of range) means STAGES.
+template <int D, int T, int GRP, int HP>
+__device__ __forceinline__ int ring_stages(const KParams& p) {
+  constexpr int S = Cfg<D, T, GRP, HP>::STAGES;
+  return (p.stages >= 2 && p.stages < S) ? p.stages : S;
+}
+
 // ------------------------------------------------------------------ producer
 template <int D, int T, int GRP, typename E, int HP>
 __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, int g,
@@ -357,6 +363,7 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
     prefetch_tmap(tmv);
   }
   const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
+  const int ns = ring_stages<D, T, GRP, HP>(p);
   int stage = 0;
   uint32_t phase = 1;  // a fresh barrier counts its previous (odd) phase as complete
   long long issued = 0;
@@ -439,7 +446,7 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
         }
       }
       ++issued;
-      if (++stage == C::STAGES) {
+      if (++stage == ns) {
         stage = 0;
         phase ^= 1u;
       }
@@ -448,8 +455,8 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
   if (aborted && leader) {
     // Do not leave the CTA while copies into its shared memory are in flight:
     // wait (bounded) for the latest fill of every stage that was used.
-    for (int s = 0; s < C::STAGES; ++s) {
-      const long long fills = issued / C::STAGES + (s < issued % C::STAGES ? 1 : 0);
+    for (int s = 0; s < ns; ++s) {
+      const long long fills = issued / ns + (s < issued % ns ? 1 : 0);
       if (fills == 0) continue;
       const uint32_t parity = (uint32_t)((fills - 1) & 1);
       volatile int no_abort = 0;
@@ -599,7 +606,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == C::STAGES) {
+    if (++stage == ring_stages<D, T, GRP, HP>(p)) {
       stage = 0;
       phase ^= 1u;
     }
@@ -784,7 +791,7 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == C::STAGES) {
+    if (++stage == ring_stages<D, T, GRP, HP>(p)) {
       stage = 0;
       phase ^= 1u;
     }

@@ -366,6 +366,20 @@ la_status la_schedule_export(const la_schedule* s, int32_t* buf, size_t n);
 la_status la_schedule_set_debug(la_schedule* s, int skip_signal_cta, long long spin_timeout_ns);
 
 /*
+ * Depth of the shared-memory ring the decode kernel cycles through (a
+ * tuning knob; the paper has no counterpart). Each CTA holds 2-4 stages of
+ * one LeanTile of K plus one of V within 192 KiB; stages = 0 restores the
+ * library's choice, 2-4 requests that many (capped at what the kernel
+ * instance holds). The library's choice: every stage for the fixed
+ * partitions, whose few busy SMs each need many bytes in flight; for
+ * stream-K over every SM, 3 stages at d = 96 and 2 at d = 128 with
+ * 128-token tiles (slab and paged layouts), where fewer bytes in flight
+ * per SM measured faster on GB300. Results do not depend on it (every warp
+ * sees the same tokens in the same order). LA_ERR_INVALID for other values.
+ */
+la_status la_schedule_set_stages(la_schedule* s, int stages);
+
+/*
  * Optional per-CTA timeline, to measure the balance of work across SMs and
  * how long host CTAs wait for partial results (the talk's "temporal skew").
  * trace_dev: device buffer of la_schedule_grid(s) * 8 uint64 words (8-byte

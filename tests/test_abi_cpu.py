@@ -334,3 +334,14 @@ def test_two_head_schedules_are_refused_for_the_slab_layout():
     assert la._lib.la_decode(p, p, p, 0, p, s.handle, ws, p, ctypes.c_float(0.125), None) == la.LA_ERR_UNSUPPORTED
     assert la._lib.la_decode_static(p, p, p, 0, p, s.handle, p, ctypes.c_float(0.125), None) \
         == la.LA_ERR_UNSUPPORTED
+
+
+def test_stage_setter_accepts_zero_and_two_to_four():
+    s = la.la_plan(1, 4, 4, 64, [0, 1024], 3)
+    for n in (0, 2, 3, 4):
+        la.la_schedule_set_stages(s, n)
+    for n in (-1, 1, 5):
+        with pytest.raises(la.LeanAttentionError) as e:
+            la.la_schedule_set_stages(s, n)
+        assert e.value.status == la.LA_ERR_INVALID
+    assert la._lib.la_schedule_set_stages(None, 2) == la.LA_ERR_INVALID

@@ -246,3 +246,23 @@ def test_many_short_requests(batch, hq, hkv, d, hi):
     out, dec = run_lean(w, q, k, v)
     assert dec.sched.grid > 0
     compare(out.cpu(), reference(w, q, k, v))
+
+
+@pytest.mark.parametrize("d,grp,T", [(128, 1, 64), (128, 1, 128), (128, 8, 128), (96, 2, 128), (64, 8, 256),
+                                     (256, 4, 64)])
+def test_ring_depth_does_not_change_the_result(d, grp, T):
+    # every warp sees the same tokens in the same order whatever the ring depth
+    w = workloads.custom(3, 2 * grp, 2, d, "bf16", [3000, 700, 129])
+    q, k, v, _ = workloads.make_inputs(w, seed=d + grp, device="cuda")
+    outs = []
+    for stages in (0, 2, 3, 4):
+        s = la.la_plan(w.batch, w.hq, w.hkv, w.d, w.cu, 0, T)
+        la.la_schedule_set_stages(s, stages)
+        ws = la.new_workspace(s)
+        out = torch.empty(w.batch, w.hq, w.d, device="cuda")
+        la.la_decode(q, k, v, torch.as_tensor(w.cu, device="cuda"), s, ws, out, w.scale)
+        assert la.la_get_status(ws) == la.LA_OK
+        outs.append(out)
+    compare(outs[0].cpu(), reference(w, q, k, v))
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
