@@ -846,14 +846,24 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
   // Outputs of a unit: item idx -> record row rr = idx / D = hh * GRP + j
   // (kv head hh of the unit, query row j, live when j < rows) and dim idx % D.
   constexpr int kItems = HP * GRP * D;
+  const int groups = p.hkv / HP;  // units per request
   int stage = 0;
   uint32_t phase = 0;
 
+  // Segment records are read one segment ahead, so a segment's record is in
+  // registers when it starts.
+  int4 w0n = make_int4(0, 0, 0, 0), w1n = w0n;
+  if (s_begin < s_end) {
+    w0n = *reinterpret_cast<const int4*>(p.segs + (size_t)s_begin * kDevSegWords);
+    w1n = *reinterpret_cast<const int4*>(p.segs + (size_t)s_begin * kDevSegWords + 4);
+  }
   for (int si = s_begin; si < s_end; ++si) {
-    const int4 w0 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords);
-    const int4 w1 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 4);
+    const int4 w0 = w0n, w1 = w1n;
+    if (si + 1 < s_end) {
+      w0n = *reinterpret_cast<const int4*>(p.segs + (size_t)(si + 1) * kDevSegWords);
+      w1n = *reinterpret_cast<const int4*>(p.segs + (size_t)(si + 1) * kDevSegWords + 4);
+    }
     const int unit = w0.x, t0 = w0.y, t1 = w0.z, kind = w0.w, peer = w1.x;
-    const int groups = p.hkv / HP;  // units per request
     const int b = unit / groups, kvh0 = (unit % groups) * HP;  // request, first kv head of the unit
     // Device offsets that disagree with the schedule: the tiles are still
     // taken from the ring (the producer streams them) but not used, and the
@@ -875,6 +885,19 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
       unsigned long long* tr = p.trace + (size_t)g * kTraceWords;
       tr[kTrTilesDone] = global_ns();
       tr[kTrSegs] += 1ull;
+    }
+    // Pull the next segment's query rows into L1 while this segment's
+    // partial is merged and written, so the next tile loop starts without
+    // a round trip to L2 for q (one 128-byte line per thread).
+    if (si + 1 < s_end) {
+      constexpr int kLines = (D * 2 + 127) / 128;  // lines of one query row
+      if (tid < HP * p.rows * kLines) {
+        const int nb = w0n.x / groups, nkvh0 = (w0n.x % groups) * HP;
+        const int rr = tid / kLines, hh = rr / p.rows, j = rr % p.rows;
+        const char* line = reinterpret_cast<const char*>(p.q) + row_index(p, nb, nkvh0 + hh, j) * D * 2 +
+                           (tid % kLines) * 128;
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(line));
+      }
     }
     consumer_sync(C::NCT);
 
