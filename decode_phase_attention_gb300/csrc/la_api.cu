@@ -42,7 +42,7 @@ la_status check_shape(int batch, int hq, int hkv, int d, const int32_t* cu) {
   if (d <= 0) return LA_ERR_INVALID;
   if (la::default_tile(d) == 0) return LA_ERR_UNSUPPORTED;
   const int grp = hq / hkv;
-  if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return LA_ERR_UNSUPPORTED;
+  if (grp != 1 && grp != 2 && grp != 4 && grp != 8 && grp != 16) return LA_ERR_UNSUPPORTED;
   // element offsets are formed in 64 bits, tile indices in 32 bits
   if ((int64_t)hkv * cu[batch] > (int64_t)INT32_MAX * 64) return LA_ERR_UNSUPPORTED;
   return LA_OK;
@@ -531,10 +531,10 @@ la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t*
   if (st != LA_OK) return st;
   if (nq < 1) return LA_ERR_INVALID;
   const int rows = (hq / hkv) * nq;
-  if (rows > 8) return LA_ERR_UNSUPPORTED;
+  if (rows > 16) return LA_ERR_UNSUPPORTED;
   for (int b = 0; b < batch; ++b)
     if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
-  const int R = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  const int R = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
   int G = num_sms;
   if (G <= 0) {
     int sms = 0, per_sm = 0;
@@ -560,6 +560,10 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
   if (st != LA_OK) return st;
   if (nq < 1 || tile_tokens < 0) return LA_ERR_INVALID;
   int hp = heads_per_unit;
+  if ((hq / hkv) * nq > 8) {  // 9-16 query rows per kv head: units of one kv head only
+    if (hp > 1) return LA_ERR_UNSUPPORTED;
+    hp = 1;
+  }
   if (hp == 0) {
     // the fewest kv heads whose rows together make whole 256-byte pieces
     // (d = 64: 2, 96: 4, 80: 8), else the most of those that divide hkv
@@ -572,10 +576,10 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
   }
   if ((hp != 1 && hp != 2 && hp != 4 && hp != 8) || hkv % hp != 0) return LA_ERR_INVALID;
   const int rows = (hq / hkv) * nq;
-  if (rows > 8) return LA_ERR_UNSUPPORTED;
+  if (rows > 16) return LA_ERR_UNSUPPORTED;
   for (int b = 0; b < batch; ++b)
     if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
-  const int R = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  const int R = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
   const int T = tile_tokens == 0 ? la::default_tile(d) / hp : tile_tokens;
   if (!la::tile_supported(d, T, hp)) return LA_ERR_UNSUPPORTED;
   int G = num_sms;
@@ -846,7 +850,7 @@ la_status la_schedule_set_trace(la_schedule* s, void* trace_dev) {
 la_status la_device_capacity(int d, int grp, int* ctas_per_sm, int* num_sms) {
   if (ctas_per_sm == nullptr || num_sms == nullptr) return LA_ERR_INVALID;
   if (la::default_tile(d) == 0) return LA_ERR_UNSUPPORTED;
-  if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return LA_ERR_UNSUPPORTED;
+  if (grp != 1 && grp != 2 && grp != 4 && grp != 8 && grp != 16) return LA_ERR_UNSUPPORTED;
   la_status e = device_sms(num_sms);
   if (e != LA_OK) return e;
   return capacity(d, la::default_tile(d), grp, ctas_per_sm);

@@ -260,24 +260,28 @@ struct Cfg {
   static constexpr int NB = D / W;                  // boxes per tile per tensor
   static constexpr int MT = TPW / 16;               // 16-token MMA tiles per warp
   static constexpr int KS = D / 16;                 // 16-wide steps over the head dim
+  static constexpr int NB8 = (GRP + 7) / 8;         // 8-row blocks of the tensor-core path
   static constexpr int TILE_ELEMS = ROWS * D;
   static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
-  // shared memory for a ring of 2-4 stages within 192 KiB; a launch may use
-  // fewer of them (KParams::stages)
-  static constexpr int STAGES = cmax(2, cmin(4, 196608 / STAGE_BYTES));
-  static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
   static constexpr int REC = D + 2;                 // [m, l, O[d]]
   static constexpr int RS = record_stride(D, HP * GRP);  // floats per CTA record in the workspace
   static constexpr size_t MERGE_BYTES = (size_t)NCW * GRP * REC * 4;
+  // shared memory for a ring of 2-4 stages within 192 KiB (less when a large
+  // merge area leaves less room); a launch may use fewer of them
+  // (KParams::stages)
+  static constexpr int RING_ROOM = cmin(196608, 232448 - (int)MERGE_BYTES - (2 * 4 * 8 + 16) - 1024);
+  static constexpr int STAGES = cmax(2, cmin(4, RING_ROOM / STAGE_BYTES));
+  static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
   static constexpr size_t BAR_BYTES = 2 * STAGES * 8 + 16;
   static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
   static constexpr int ITEMS = (HP * GRP * D + NCT - 1) / NCT;  // (row, dim) outputs per consumer thread
   static constexpr int PB = cmax(1, cmin(4, 16 / ITEMS));  // peer records per batch of host-merge loads
-  static constexpr int STAGE_RECS = (int)(KV_BYTES / (RS * 4));  // peer records the idle ring can hold
+  // peer records the idle ring and merge area can hold (they are contiguous)
+  static constexpr int STAGE_RECS = (int)((KV_BYTES + MERGE_BYTES) / (RS * 4));
   static_assert(D % 16 == 0 && T % 16 == 0, "tile shape");
   static_assert((HP == 1 || HP == 2 || HP == 4 || HP == 8) && NCW % HP == 0 && T % WPH == 0, "kv heads per unit");
   static_assert(STEPS % CH == 0 && TPW % TPS == 0, "CUDA-core tile shape");
-  static_assert(!TC || (TPW % 16 == 0 && GRP <= 8), "tensor-core tile shape");
+  static_assert(!TC || (TPW % 16 == 0 && (GRP <= 8 || GRP % 8 == 0) && GRP <= 16), "tensor-core tile shape");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
@@ -645,7 +649,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
   }
 }
 
-// -------------------------------------------- tensor-core tile path (grp 4, 8)
+// ----------------------------------- tensor-core tile path (4, 8 or 16 rows)
 // Swizzled shared-memory address (128-byte swizzle: 16-byte chunk c of row r
 // sits at chunk c ^ (r mod 8)) of row `row`, chunk `c` of 64-column block bk.
 template <int D, int T, int GRP, int HP>
@@ -661,33 +665,40 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
                                                 int& stage, uint32_t& phase, volatile int* abort_flag,
                                                 float* wrec) {
   using C = Cfg<D, T, GRP, HP>;
+  constexpr int NB8 = C::NB8;  // blocks of 8 query rows: the N = 8 side of each MMA
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int hh = HP == 1 ? 0 : warp / C::WPH;  // kv head of the unit this warp works on
   const int kvh = kvh0 + hh;
   const int gq = lane >> 2;  // fragment row group
   const int tq = lane & 3;   // fragment column pair
-  // B operand of S = K q^T: q^T (16 dims x 8 heads), raw q bits; heads past
-  // the group are zero columns that are never written out.
-  uint32_t qb[C::KS][2];
-  {
-    const bool live = gq < p.rows;
+  // B operand of S = K q^T per block of 8 rows: q^T (16 dims x 8 rows), raw
+  // q bits; rows past the unit's are zero columns that are never written out.
+  uint32_t qb[NB8][C::KS][2];
+#pragma unroll
+  for (int nb = 0; nb < NB8; ++nb) {
+    const int r = nb * 8 + gq;
+    const bool live = r < p.rows;
     const uint32_t* qrow =
-        reinterpret_cast<const uint32_t*>(static_cast<const E*>(p.q) + row_index(p, b, kvh, live ? gq : 0) * D);
+        reinterpret_cast<const uint32_t*>(static_cast<const E*>(p.q) + row_index(p, b, kvh, live ? r : 0) * D);
 #pragma unroll
     for (int ks = 0; ks < C::KS; ++ks) {
-      qb[ks][0] = live ? qrow[(ks * 16 + 2 * tq) / 2] : 0u;
-      qb[ks][1] = live ? qrow[(ks * 16 + 2 * tq + 8) / 2] : 0u;
+      qb[nb][ks][0] = live ? qrow[(ks * 16 + 2 * tq) / 2] : 0u;
+      qb[nb][ks][1] = live ? qrow[(ks * 16 + 2 * tq + 8) / 2] : 0u;
     }
   }
-  // State for heads 2tq and 2tq+1: m (uniform over the 8 row groups), the
-  // thread's share of l, and O^T fragments (dims x heads).
-  float m[2] = {-INFINITY, -INFINITY};
-  float l[2] = {0.f, 0.f};
-  float o[C::KS][4];
+  // State for rows nb*8 + 2tq and nb*8 + 2tq + 1 of every block: m (uniform
+  // over the 8 row groups), the thread's share of l, and O^T fragments
+  // (dims x rows).
+  float m[NB8][2], l[NB8][2], o[NB8][C::KS][4];
 #pragma unroll
-  for (int dm = 0; dm < C::KS; ++dm)
+  for (int nb = 0; nb < NB8; ++nb) {
+    m[nb][0] = m[nb][1] = -INFINITY;
+    l[nb][0] = l[nb][1] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) o[dm][i] = 0.f;
+    for (int dm = 0; dm < C::KS; ++dm)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[nb][dm][i] = 0.f;
+  }
 
   const uint32_t kv_base = smem_u32(kv);
   for (int it = 0; it < n_tiles; ++it) {
@@ -697,54 +708,58 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
       const uint32_t kb = kv_base + (uint32_t)(stage * 2 * C::TILE_ELEMS * 2);
       const uint32_t vb = kb + (uint32_t)(C::TILE_ELEMS * 2);
       const int wtok = (HP == 1 ? warp : warp % C::WPH) * C::TPW;
-      // S = K q^T for the warp's TPW tokens: MT tiles of 16 tokens x 8 heads
-      float s[C::MT][4];
+      // S = K q^T for the warp's TPW tokens: MT tiles of 16 tokens x 8 rows
+      // per block (one ldmatrix of K serves every block)
+      float s[C::MT][NB8][4];
 #pragma unroll
       for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s[mt][i] = 0.f;
+        for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s[mt][nb][i] = 0.f;
         const int row = (wtok + mt * 16 + (lane & 15)) * HP + hh;
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
           uint32_t a[4];
           ldsm_x4(a, swz<D, T, GRP, HP>(kb, ks * 16 / C::W, row, (ks * 16 % C::W) / 8 + (lane >> 4)));
-          Elem<E>::mma(s[mt], a, qb[ks][0], qb[ks][1]);
+#pragma unroll
+          for (int nb = 0; nb < NB8; ++nb) Elem<E>::mma(s[mt][nb], a, qb[nb][ks][0], qb[nb][ks][1]);
         }
       }
-      // scale to base-2 units, mask tokens each row may not see
-      const int vis0 = row_visible(p, L, t0 + it, C::T, 2 * tq);
-      const int vis1 = row_visible(p, L, t0 + it, C::T, 2 * tq + 1);
-      float mx[2] = {-INFINITY, -INFINITY};
+      // scale to base-2 units, mask tokens each row may not see, new maxima
+      float mn[NB8][2], alpha[NB8][2];
 #pragma unroll
-      for (int mt = 0; mt < C::MT; ++mt) {
+      for (int nb = 0; nb < NB8; ++nb) {
+        const int vis0 = row_visible(p, L, t0 + it, C::T, nb * 8 + 2 * tq);
+        const int vis1 = row_visible(p, L, t0 + it, C::T, nb * 8 + 2 * tq + 1);
+        float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tok = wtok + mt * 16 + gq + ((i & 2) ? 8 : 0);
-          s[mt][i] = (tok < ((i & 1) ? vis1 : vis0)) ? s[mt][i] * p.qscale : -INFINITY;
-          mx[i & 1] = fmaxf(mx[i & 1], s[mt][i]);
+        for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tok = wtok + mt * 16 + gq + ((i & 2) ? 8 : 0);
+            s[mt][nb][i] = (tok < ((i & 1) ? vis1 : vis0)) ? s[mt][nb][i] * p.qscale : -INFINITY;
+            mx[i & 1] = fmaxf(mx[i & 1], s[mt][nb][i]);
+          }
         }
-      }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 4));
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 8));
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 16));
-      }
-      float mn[2], alpha[2];
+        for (int h = 0; h < 2; ++h) {
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 4));
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 8));
+          mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], 16));
+          mn[nb][h] = fmaxf(m[nb][h], mx[h]);
+          alpha[nb][h] = (m[nb][h] == -INFINITY) ? 0.f : ex2(m[nb][h] - mn[nb][h]);
+          if (mn[nb][h] == -INFINITY) alpha[nb][h] = 1.f;  // nothing seen yet
+          m[nb][h] = mn[nb][h];
+          l[nb][h] *= alpha[nb][h];
+        }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        mn[h] = fmaxf(m[h], mx[h]);
-        alpha[h] = (m[h] == -INFINITY) ? 0.f : ex2(m[h] - mn[h]);
-        if (mn[h] == -INFINITY) alpha[h] = 1.f;  // nothing seen yet
-        m[h] = mn[h];
-        l[h] *= alpha[h];
-      }
-#pragma unroll
-      for (int dm = 0; dm < C::KS; ++dm) {
-        o[dm][0] *= alpha[0];
-        o[dm][1] *= alpha[1];
-        o[dm][2] *= alpha[0];
-        o[dm][3] *= alpha[1];
+        for (int dm = 0; dm < C::KS; ++dm) {
+          o[nb][dm][0] *= alpha[nb][0];
+          o[nb][dm][1] *= alpha[nb][1];
+          o[nb][dm][2] *= alpha[nb][0];
+          o[nb][dm][3] *= alpha[nb][1];
+        }
       }
       // Rows past the context may hold anything (another request's tokens,
       // an unused page slot): their P is zero, but 0 * NaN is not, so the
@@ -763,29 +778,39 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
         __syncwarp();
       }
       // P = 2^(s - m), split into high and low 16-bit parts; O^T += V^T P
+      // (one ldmatrix of V^T serves every block)
 #pragma unroll
       for (int mt = 0; mt < C::MT; ++mt) {
-        float pv[4];
+        uint32_t bh[NB8][2], bl[NB8][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float mi = mn[i & 1];
-          pv[i] = (mi == -INFINITY) ? 0.f : ex2(s[mt][i] - mi);
-          l[i & 1] += pv[i];
+        for (int nb = 0; nb < NB8; ++nb) {
+          float pv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float mi = mn[nb][i & 1];
+            pv[i] = (mi == -INFINITY) ? 0.f : ex2(s[mt][nb][i] - mi);
+            l[nb][i & 1] += pv[i];
+          }
+          const uint32_t h01 = Elem<E>::pack(pv[0], pv[1]);
+          const uint32_t h23 = Elem<E>::pack(pv[2], pv[3]);
+          const float2 f01 = Elem<E>::unpack(h01), f23 = Elem<E>::unpack(h23);
+          const uint32_t l01 = Elem<E>::pack(pv[0] - f01.x, pv[1] - f01.y);
+          const uint32_t l23 = Elem<E>::pack(pv[2] - f23.x, pv[3] - f23.y);
+          bh[nb][0] = movmatrix_trans(h01);
+          bh[nb][1] = movmatrix_trans(h23);
+          bl[nb][0] = movmatrix_trans(l01);
+          bl[nb][1] = movmatrix_trans(l23);
         }
-        const uint32_t h01 = Elem<E>::pack(pv[0], pv[1]);
-        const uint32_t h23 = Elem<E>::pack(pv[2], pv[3]);
-        const float2 f01 = Elem<E>::unpack(h01), f23 = Elem<E>::unpack(h23);
-        const uint32_t l01 = Elem<E>::pack(pv[0] - f01.x, pv[1] - f01.y);
-        const uint32_t l23 = Elem<E>::pack(pv[2] - f23.x, pv[3] - f23.y);
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
         const int vrow = (wtok + mt * 16 + (lane & 7) + ((lane >> 4) << 3)) * HP + hh;
 #pragma unroll
         for (int dm = 0; dm < C::KS; ++dm) {
           uint32_t a[4];
           ldsm_x4_trans(a, swz<D, T, GRP, HP>(vb, dm * 16 / C::W, vrow, (dm * 16 % C::W) / 8 + ((lane >> 3) & 1)));
-          Elem<E>::mma(o[dm], a, bh0, bh1);
-          Elem<E>::mma(o[dm], a, bl0, bl1);
+#pragma unroll
+          for (int nb = 0; nb < NB8; ++nb) {
+            Elem<E>::mma(o[nb][dm], a, bh[nb][0], bh[nb][1]);
+            Elem<E>::mma(o[nb][dm], a, bl[nb][0], bl[nb][1]);
+          }
         }
       }
     }
@@ -799,27 +824,31 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
 
   // l: sum the shares of the 8 row groups (m is already common to them)
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    l[h] += __shfl_xor_sync(kFull, l[h], 4);
-    l[h] += __shfl_xor_sync(kFull, l[h], 8);
-    l[h] += __shfl_xor_sync(kFull, l[h], 16);
-  }
+  for (int nb = 0; nb < NB8; ++nb)
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int head = 2 * tq + h;
-    if (head < p.rows) {
-      float* r = wrec + head * C::REC;
-      if (gq == 0) {
-        r[0] = m[h];
-        r[1] = l[h];
-      }
+    for (int h = 0; h < 2; ++h) {
+      l[nb][h] += __shfl_xor_sync(kFull, l[nb][h], 4);
+      l[nb][h] += __shfl_xor_sync(kFull, l[nb][h], 8);
+      l[nb][h] += __shfl_xor_sync(kFull, l[nb][h], 16);
+    }
 #pragma unroll
-      for (int dm = 0; dm < C::KS; ++dm) {
-        r[2 + dm * 16 + gq] = o[dm][h];
-        r[2 + dm * 16 + gq + 8] = o[dm][2 + h];
+  for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int head = nb * 8 + 2 * tq + h;
+      if (head < p.rows) {
+        float* r = wrec + head * C::REC;
+        if (gq == 0) {
+          r[0] = m[nb][h];
+          r[1] = l[nb][h];
+        }
+#pragma unroll
+        for (int dm = 0; dm < C::KS; ++dm) {
+          r[2 + dm * 16 + gq] = o[nb][dm][h];
+          r[2 + dm * 16 + gq + 8] = o[nb][dm][2 + h];
+        }
       }
     }
-  }
 }
 
 // ------------------------------------------------------------------ consumers
@@ -981,26 +1010,23 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
           int p0 = 0;
           if (si == s_end - 1 && npeer > C::PB) {
             // Many peers, and the CTA's last segment: every tile has been
-            // consumed and the producer issues no more copies, so the ring is
-            // idle. Stage the records of the first peers there with one
-            // cooperative round of 16-byte L2 loads (the records of
+            // consumed and the producer issues no more copies, so the ring
+            // and the merge area after it (read above) are idle. Stage the
+            // records of the first peers there, every 16-byte piece in flight
+            // at once (cp.async from L2 into shared memory; the records of
             // consecutive CTAs are contiguous), then apply f to all of them
             // at once: the maximum m over the partials, then the weighted
             // sums of l and O (f is associative, so k partials reduce in one
             // step).
             const int ns = npeer < C::STAGE_RECS ? npeer : C::STAGE_RECS;
-            float4* stg = reinterpret_cast<float4*>(kv);
-            const float4* src = reinterpret_cast<const float4*>(p.recs + (size_t)(g + 1) * C::RS);
+            const uint32_t stg = smem_u32(kv);
+            const char* src = reinterpret_cast<const char*>(p.recs + (size_t)(g + 1) * C::RS);
             const int n4 = ns * (C::RS / 4);
-            for (int i0 = tid; i0 < n4; i0 += 8 * C::NCT) {
-              float4 buf[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                if (i0 + u * C::NCT < n4) buf[u] = __ldcg(src + i0 + u * C::NCT);
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                if (i0 + u * C::NCT < n4) stg[i0 + u * C::NCT] = buf[u];
-            }
+            for (int i = tid; i < n4; i += C::NCT)
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(stg + 16u * (uint32_t)i),
+                           "l"(src + 16 * (size_t)i)
+                           : "memory");
+            asm volatile("cp.async.wait_all;" ::: "memory");
             consumer_sync(C::NCT);
             const float* st = reinterpret_cast<const float*>(kv);
 #pragma unroll

@@ -1,5 +1,5 @@
 // la_kernels_d128.cu -- instances of the decode kernels for head dim 128
-// (LeanTile sizes 128, 64 tokens), query-head groups 1, 2, 4 and 8, fp16 and bf16.
+// (LeanTile sizes 128, 64 tokens), query rows per kv head 1, 2, 4, 8 and 16, fp16 and bf16.
 #include "la_kernel.cuh"
 
 namespace la {
@@ -17,6 +17,9 @@ cudaError_t launch_decode_d128(int T, int grp, int dtype, const KParams& p, cuda
   if (T == 128 && grp == 8)
     return dtype ? launch_decode_t<128, 128, 8, __nv_bfloat16>(p, st)
                  : launch_decode_t<128, 128, 8, __half>(p, st);
+  if (T == 128 && grp == 16)
+    return dtype ? launch_decode_t<128, 128, 16, __nv_bfloat16>(p, st)
+                 : launch_decode_t<128, 128, 16, __half>(p, st);
   if (T == 64 && grp == 1)
     return dtype ? launch_decode_t<128, 64, 1, __nv_bfloat16>(p, st)
                  : launch_decode_t<128, 64, 1, __half>(p, st);
@@ -29,6 +32,9 @@ cudaError_t launch_decode_d128(int T, int grp, int dtype, const KParams& p, cuda
   if (T == 64 && grp == 8)
     return dtype ? launch_decode_t<128, 64, 8, __nv_bfloat16>(p, st)
                  : launch_decode_t<128, 64, 8, __half>(p, st);
+  if (T == 64 && grp == 16)
+    return dtype ? launch_decode_t<128, 64, 16, __nv_bfloat16>(p, st)
+                 : launch_decode_t<128, 64, 16, __half>(p, st);
   return cudaErrorInvalidValue;
 }
 
@@ -38,6 +44,7 @@ cudaError_t launch_combine_d128(int grp, const CParams& p, cudaStream_t st) {
     case 2: return launch_combine_t<128, 2>(p, st);
     case 4: return launch_combine_t<128, 4>(p, st);
     case 8: return launch_combine_t<128, 8>(p, st);
+    case 16: return launch_combine_t<128, 16>(p, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -47,10 +54,12 @@ cudaError_t decode_capacity_d128(int T, int grp, int* per_sm) {
   if (T == 128 && grp == 2) return capacity_t<128, 128, 2>(per_sm);
   if (T == 128 && grp == 4) return capacity_t<128, 128, 4>(per_sm);
   if (T == 128 && grp == 8) return capacity_t<128, 128, 8>(per_sm);
+  if (T == 128 && grp == 16) return capacity_t<128, 128, 16>(per_sm);
   if (T == 64 && grp == 1) return capacity_t<128, 64, 1>(per_sm);
   if (T == 64 && grp == 2) return capacity_t<128, 64, 2>(per_sm);
   if (T == 64 && grp == 4) return capacity_t<128, 64, 4>(per_sm);
   if (T == 64 && grp == 8) return capacity_t<128, 64, 8>(per_sm);
+  if (T == 64 && grp == 16) return capacity_t<128, 64, 16>(per_sm);
   return cudaErrorInvalidValue;
 }
 

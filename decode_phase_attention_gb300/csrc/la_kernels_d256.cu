@@ -1,5 +1,5 @@
 // la_kernels_d256.cu -- instances of the decode kernels for head dim 256
-// (LeanTile sizes 64 tokens), query-head groups 1, 2, 4 and 8, fp16 and bf16.
+// (LeanTile sizes 64 tokens), query rows per kv head 1, 2, 4, 8 and 16, fp16 and bf16.
 #include "la_kernel.cuh"
 
 namespace la {
@@ -17,6 +17,9 @@ cudaError_t launch_decode_d256(int T, int grp, int dtype, const KParams& p, cuda
   if (T == 64 && grp == 8)
     return dtype ? launch_decode_t<256, 64, 8, __nv_bfloat16>(p, st)
                  : launch_decode_t<256, 64, 8, __half>(p, st);
+  if (T == 64 && grp == 16)
+    return dtype ? launch_decode_t<256, 64, 16, __nv_bfloat16>(p, st)
+                 : launch_decode_t<256, 64, 16, __half>(p, st);
   return cudaErrorInvalidValue;
 }
 
@@ -26,6 +29,7 @@ cudaError_t launch_combine_d256(int grp, const CParams& p, cudaStream_t st) {
     case 2: return launch_combine_t<256, 2>(p, st);
     case 4: return launch_combine_t<256, 4>(p, st);
     case 8: return launch_combine_t<256, 8>(p, st);
+    case 16: return launch_combine_t<256, 16>(p, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -35,6 +39,7 @@ cudaError_t decode_capacity_d256(int T, int grp, int* per_sm) {
   if (T == 64 && grp == 2) return capacity_t<256, 64, 2>(per_sm);
   if (T == 64 && grp == 4) return capacity_t<256, 64, 4>(per_sm);
   if (T == 64 && grp == 8) return capacity_t<256, 64, 8>(per_sm);
+  if (T == 64 && grp == 16) return capacity_t<256, 64, 16>(per_sm);
   return cudaErrorInvalidValue;
 }
 

@@ -1,5 +1,5 @@
 // la_kernels_d80.cu -- instances of the decode kernels for head dim 80
-// (LeanTile sizes 128 tokens), query-head groups 1, 2, 4 and 8, fp16 and bf16.
+// (LeanTile sizes 128 tokens), query rows per kv head 1, 2, 4, 8 and 16, fp16 and bf16.
 #include "la_kernel.cuh"
 
 namespace la {
@@ -17,6 +17,9 @@ cudaError_t launch_decode_d80(int T, int grp, int dtype, const KParams& p, cudaS
   if (T == 128 && grp == 8)
     return dtype ? launch_decode_t<80, 128, 8, __nv_bfloat16>(p, st)
                  : launch_decode_t<80, 128, 8, __half>(p, st);
+  if (T == 128 && grp == 16)
+    return dtype ? launch_decode_t<80, 128, 16, __nv_bfloat16>(p, st)
+                 : launch_decode_t<80, 128, 16, __half>(p, st);
   return cudaErrorInvalidValue;
 }
 
@@ -26,6 +29,7 @@ cudaError_t launch_combine_d80(int grp, const CParams& p, cudaStream_t st) {
     case 2: return launch_combine_t<80, 2>(p, st);
     case 4: return launch_combine_t<80, 4>(p, st);
     case 8: return launch_combine_t<80, 8>(p, st);
+    case 16: return launch_combine_t<80, 16>(p, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -35,6 +39,7 @@ cudaError_t decode_capacity_d80(int T, int grp, int* per_sm) {
   if (T == 128 && grp == 2) return capacity_t<80, 128, 2>(per_sm);
   if (T == 128 && grp == 4) return capacity_t<80, 128, 4>(per_sm);
   if (T == 128 && grp == 8) return capacity_t<80, 128, 8>(per_sm);
+  if (T == 128 && grp == 16) return capacity_t<80, 128, 16>(per_sm);
   return cudaErrorInvalidValue;
 }
 

@@ -10,7 +10,7 @@
 struct la_schedule {
   int batch = 0, hq = 0, hkv = 0, d = 0, grp = 0, T = 0;
   int nq = 1;      // query tokens per request (speculative decoding: 2..8)
-  int R = 0;       // query rows per unit the kernel instance holds: grp * nq rounded up to 1, 2, 4 or 8
+  int R = 0;       // query rows per kv head the kernel instance holds: grp * nq rounded up to 1, 2, 4, 8 or 16
   int hp = 1;      // kv heads per unit: 1, or 2 for token-major / paged caches with short rows
   int stages = 0;  // ring stages requested with la_schedule_set_stages (0: the library's choice)
   int kind = 0;    // 0 stream-K, 1 fixed

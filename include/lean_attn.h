@@ -81,7 +81,7 @@ enum {
  * and "3.5 execution flow" of the xllm-io review).
  *
  *   batch, hq, hkv, d  shape; d in {64, 80, 96, 128, 256}; hq % hkv == 0 and
- *                      hq / hkv in {1, 2, 4, 8}
+ *                      hq / hkv in {1, 2, 4, 8, 16}
  *   cu_seqlens_k       HOST pointer to batch + 1 int32 offsets (read, not kept)
  *   num_sms            grid size G; <= 0 picks one persistent CTA per SM of
  *                      the current device (the kernel runs one CTA per SM).
@@ -138,7 +138,7 @@ la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlen
  * schedule la_decode / la_decode_ex / la_decode_kv / la_decode_static read
  * q as [batch, nq, hq, d] and write out as [batch, nq, hq, d]. The tiles and
  * their split are those of la_plan (K/V are read once per kv head for all
- * grp * nq query rows). Requires grp * nq <= 8 (LA_ERR_UNSUPPORTED) and
+ * grp * nq query rows). Requires grp * nq <= 16 (LA_ERR_UNSUPPORTED) and
  * L_b >= nq for every request (LA_ERR_INVALID); nq = 1 is la_plan.
  */
 la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t* cu_seqlens_k, int num_sms,

@@ -104,7 +104,7 @@ def test_fixed_planner_matches_reference(splits):
     ((2, 4, 4, 64, [0, 10, 10], 4), la.LA_ERR_INVALID),         # empty context
     ((1, 4, 4, 64, [1, 10], 4), la.LA_ERR_INVALID),             # cu[0] != 0
     ((1, 4, 4, 112, [0, 10], 4), la.LA_ERR_UNSUPPORTED),        # head dim not built
-    ((1, 64, 4, 64, [0, 10], 4), la.LA_ERR_UNSUPPORTED),        # group of 16 not built
+    ((1, 128, 4, 64, [0, 10], 4), la.LA_ERR_UNSUPPORTED),       # group of 32 not built
 ])
 def test_plan_rejects_bad_shapes(args, status):
     with pytest.raises(la.LeanAttentionError) as e:
@@ -243,7 +243,7 @@ def test_spec_schedule_matches_the_decode_plan_and_sizes_its_records():
 
 
 @pytest.mark.parametrize("hq,hkv,nq,lengths,status", [
-    (8, 2, 3, [100, 200], la.LA_ERR_UNSUPPORTED),   # 4 x 3 = 12 query rows per unit
+    (16, 2, 3, [100, 200], la.LA_ERR_UNSUPPORTED),  # 8 x 3 = 24 query rows per unit
     (4, 4, 5, [100, 4], la.LA_ERR_INVALID),          # a context shorter than its query tokens
     (4, 4, 0, [100, 200], la.LA_ERR_INVALID),
 ])
@@ -315,7 +315,8 @@ def test_two_head_records_hold_both_heads():
     (dict(hkv=4, hq=8, heads_per_unit=2, d=128), la.LA_ERR_UNSUPPORTED),   # rows already 256 bytes: not built
     (dict(hkv=4, hq=8, heads_per_unit=2, tile_tokens=256), la.LA_ERR_UNSUPPORTED),
     (dict(hkv=4, hq=8, tile_tokens=-1), la.LA_ERR_INVALID),
-    (dict(hkv=2, hq=16, nq=2), la.LA_ERR_UNSUPPORTED),            # 8 x 2 query rows per kv head
+    (dict(hkv=2, hq=16, nq=3), la.LA_ERR_UNSUPPORTED),            # 8 x 3 query rows per kv head
+    (dict(hkv=2, hq=16, nq=2, heads_per_unit=2), la.LA_ERR_UNSUPPORTED),  # 16 rows: one kv head per unit
 ])
 def test_plan_kv_rejections(kw, status):
     args = dict(batch=2, hq=8, hkv=4, d=64, cu=[0, 100, 300], nq=1, heads_per_unit=0, tile_tokens=0)
@@ -345,3 +346,16 @@ def test_stage_setter_accepts_zero_and_two_to_four():
             la.la_schedule_set_stages(s, n)
         assert e.value.status == la.LA_ERR_INVALID
     assert la._lib.la_schedule_set_stages(None, 2) == la.LA_ERR_INVALID
+
+
+def test_sixteen_query_rows_per_kv_head():
+    # group 16 (and group x query tokens up to 16) plans like any other group
+    s = la.la_plan(2, 32, 2, 128, [0, 900, 1000], 7)
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 32, 2, 128, [0, 900, 1000], 7, 128))
+    # records hold 16 rows of (d + 2) floats
+    assert la.la_workspace_size(s) == 256 + 256 + 7 * 16 * 130 * 4
+    sp = la.la_plan_spec(2, 16, 2, 64, 2, [0, 900, 1000], 7)
+    assert la.la_workspace_size(sp) == 256 + 256 + 7 * 16 * 66 * 4
+    # caches: units of one kv head once a kv head has more than 8 rows
+    assert la.la_plan_kv(1, 32, 2, 64, [0, 900], num_sms=7).heads_per_unit == 1
+    assert la.la_plan_kv(1, 16, 2, 64, [0, 900], num_sms=7).heads_per_unit == 2

@@ -41,6 +41,7 @@ def run(w, q, kc, vc, layout, grid=0, table=None, P=0, npages=0, out_dtype=torch
 
 CASES = [(64, 1, "f16"), (64, 8, "bf16"), (80, 1, "bf16"), (96, 4, "f16"), (128, 1, "bf16"), (128, 2, "f16"),
          (128, 8, "bf16"), (256, 1, "bf16"), (256, 4, "bf16")]
+CASES += [(64, 16, "bf16"), (128, 16, "f16")]
 
 
 @pytest.mark.parametrize("d,grp,dt", CASES)

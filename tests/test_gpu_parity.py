@@ -266,3 +266,33 @@ def test_ring_depth_does_not_change_the_result(d, grp, T):
     compare(outs[0].cpu(), reference(w, q, k, v))
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
+
+
+@pytest.mark.parametrize("d,T", [(64, 256), (64, 128), (80, 128), (96, 128), (128, 128), (128, 64), (256, 64)])
+@pytest.mark.parametrize("grid", [0, 5])
+def test_sixteen_query_heads_per_kv_head(d, T, grid):
+    # group 16 (two blocks of 8 rows on the tensor-core path) on ragged tails
+    w = workloads.custom(4, 32, 2, d, "bf16" if d % 128 else "f16", [1, 255, 257, 1000])
+    q, k, v, _ = workloads.make_inputs(w, seed=d + T + grid, device="cuda")
+    s = la.la_plan(w.batch, w.hq, w.hkv, w.d, w.cu, grid, T)
+    ws = la.new_workspace(s)
+    out = torch.empty(w.batch, w.hq, w.d, device="cuda")
+    la.la_decode(q, k, v, torch.as_tensor(w.cu, device="cuda"), s, ws, out, w.scale)
+    assert la.la_get_status(ws) == la.LA_OK
+    compare(out.cpu(), reference(w, q, k, v))
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_sixteen_query_heads_with_fixed_partitions_and_16_bit_output(splits):
+    w = workloads.custom(3, 64, 4, 128, "bf16", [3000, 700, 129])
+    q, k, v, _ = workloads.make_inputs(w, seed=splits, device="cuda")
+    out, _ = run_lean(w, q, k, v, fixed_splits=splits)
+    ref = reference(w, q, k, v)
+    compare(out.cpu(), ref)
+    s = la.la_plan(w.batch, w.hq, w.hkv, w.d, w.cu)
+    ws = la.new_workspace(s)
+    o16 = torch.empty(w.batch, w.hq, w.d, dtype=torch.bfloat16, device="cuda")
+    la.la_decode(q, k, v, torch.as_tensor(w.cu, device="cuda"), s, ws, o16, w.scale)
+    got = o16.double().cpu().numpy().reshape(ref.shape)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+    assert np.all(np.abs(got - ref) <= 2e-3 + ulp)
