@@ -29,10 +29,11 @@
 //     slab, moved by a 1-D bulk copy (cp.async.bulk). d/8 lanes share one
 //     token (16 bytes each, whole rows per warp, no bank conflicts); q.k is
 //     reduced across them with shuffles, P.V accumulates in registers.
-//   tensor cores (group 4 or 8, up to 8 flop per byte, which would saturate
-//     the fp32 pipes): tiles arrive by 2-D TMA (cp.async.bulk.tensor) with
-//     128-byte swizzle, so ldmatrix reads are conflict-free. With the query
-//     heads of the group as the N = 8 side of an m16n8k16 MMA, S = K q^T
+//   tensor cores (4-16 query rows per kv head, up to 16 flop per byte, which
+//     would saturate the fp32 pipes): tiles arrive by 2-D TMA
+//     (cp.async.bulk.tensor) with 128-byte swizzle, so ldmatrix reads are
+//     conflict-free. With the query rows as the N = 8 side of an m16n8k16
+//     MMA (two blocks of 8 above 8 rows), S = K q^T
 //     (tokens x heads) and O^T = V^T P (dims x heads) need no padding rows;
 //     P moves from the accumulator layout to the operand layout with
 //     movmatrix, and is split into a bf16/fp16 high and low part so that

@@ -280,10 +280,12 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
  *
  *   nq              query tokens per request, as la_plan_spec (1: decode)
  *   heads_per_unit  kv heads of one unit. Built: 1 (any d); d = 64: 2;
- *                   d = 80: 2, 8; d = 96: 2, 4. 0 picks the fewest heads
+ *                   d = 80: 2, 8; d = 96: 2, 4 (up to 8 query rows per kv
+ *                   head; more rows need 1). 0 picks the fewest heads
  *                   whose rows make whole 256-byte pieces if that count
  *                   divides hkv, else the most built count that divides
- *                   hkv, else 1 (always 1 for d = 128, 256).
+ *                   hkv, else 1 (always 1 for d = 128, 256 and for 9-16
+ *                   query rows per kv head).
  *   tile_tokens     tokens of each head per tile; 0 picks the default:
  *                   the review's table size of d (128 at d = 128 also for
  *                   one or two query rows: 16-token pages read 13 % slower
