@@ -136,3 +136,54 @@ def test_random_configuration_through_la_plan_kv(seed):
     err = np.abs(got - ref).max()
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_configuration_with_9_to_16_rows(seed):
+    """9-16 query rows per kv head (group 16, or a group times several query
+    tokens) through la_plan / la_plan_spec / la_plan_kv on every layout."""
+    r = np.random.default_rng(9000 + seed)
+    d = int(r.choice(la.HEAD_DIMS))
+    grp, nq = [(16, 1), (8, 2), (4, 3), (4, 4), (2, 5), (2, 8), (1, 12), (1, 16)][int(r.integers(0, 8))]
+    hkv = int(r.integers(1, 3))
+    batch = int(r.integers(1, 4))
+    lengths = [int(x) for x in np.maximum(nq, np.exp(r.uniform(0, np.log(4000), size=batch)).astype(int))]
+    dt = str(r.choice(["f16", "bf16"]))
+    layout = str(r.choice(["slab", "token_major", "paged"]))
+    page = int(r.choice([32, 64, 128]))
+    grid = int(r.choice([0, 0, 3, 29]))
+    w = workloads.custom(batch, hkv * grp, hkv, d, dt, lengths, nq=nq)
+    q, k, v, cu = workloads.make_inputs(w, seed=seed, device="cuda")
+    if layout == "slab":
+        s = (la.la_plan_spec(batch, w.hq, hkv, d, nq, cu, grid) if nq > 1
+             else la.la_plan(batch, w.hq, hkv, d, cu, grid))
+    else:
+        s = la.la_plan_kv(batch, w.hq, hkv, d, cu, nq=nq, num_sms=grid)
+        assert s.heads_per_unit == 1
+    ws = la.new_workspace(s)
+    out = torch.empty(*q.shape, dtype=torch.float32, device="cuda")
+    cu_dev = torch.as_tensor(cu, device="cuda")
+    if layout == "slab":
+        la.la_decode(q, k, v, cu_dev, s, ws, out, w.scale)
+        kk, vv = k.cpu(), v.cpu()
+    elif layout == "token_major":
+        kc, vc = workloads.to_token_major(w, k, v)
+        la.la_decode_kv(q, kc, vc, cu_dev, s, ws, out, w.scale, layout="token_major")
+        kk = layouts.gather_token_major(kc.cpu().view(torch.int16).numpy(), cu, hkv, d)
+        vv = layouts.gather_token_major(vc.cpu().view(torch.int16).numpy(), cu, hkv, d)
+        kk, vv = kk.astype(np.int16).view(np.uint16), vv.astype(np.int16).view(np.uint16)
+    else:
+        kc, vc, table, npages = workloads.to_paged(w, k, v, page, seed=seed)
+        la.la_decode_kv(q, kc, vc, cu_dev, s, ws, out, w.scale, layout="paged", block_table=table.cuda(),
+                        page_size=page, num_pages=npages)
+        kk = layouts.gather_paged(kc.cpu().view(torch.int16).numpy(), table.numpy(), cu, page, hkv, d)
+        vv = layouts.gather_paged(vc.cpu().view(torch.int16).numpy(), table.numpy(), cu, page, hkv, d)
+        kk, vv = kk.astype(np.int16).view(np.uint16), vv.astype(np.int16).view(np.uint16)
+    assert la.la_get_status(ws) == la.LA_OK
+    code = oracle.F16 if dt == "f16" else oracle.BF16
+    ref = oracle.attend(q.cpu(), kk, vv, cu, w.hq, hkv, d, w.scale, code, nq=nq)
+    got = out.double().cpu().numpy().reshape(ref.shape)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref).max()
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
