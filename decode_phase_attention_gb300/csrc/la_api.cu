@@ -33,6 +33,10 @@ namespace {
 
 constexpr int kMaxGrid = 1 << 20;
 
+// Query rows per kv head the kernel instance holds: rows rounded up to 1, 2,
+// 4, 8 or 16 (the spare rows are zero queries that are never written out).
+int instance_rows(int rows) { return rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : 16; }
+
 la_status check_shape(int batch, int hq, int hkv, int d, const int32_t* cu) {
   if (batch <= 0 || hq <= 0 || hkv <= 0 || cu == nullptr) return LA_ERR_INVALID;
   if (hq % hkv != 0) return LA_ERR_INVALID;
@@ -42,7 +46,7 @@ la_status check_shape(int batch, int hq, int hkv, int d, const int32_t* cu) {
   if (d <= 0) return LA_ERR_INVALID;
   if (la::default_tile(d) == 0) return LA_ERR_UNSUPPORTED;
   const int grp = hq / hkv;
-  if (grp != 1 && grp != 2 && grp != 4 && grp != 8 && grp != 16) return LA_ERR_UNSUPPORTED;
+  if (grp > 16) return LA_ERR_UNSUPPORTED;  // more query rows than the tile paths hold
   // element offsets are formed in 64 bits, tile indices in 32 bits
   if ((int64_t)hkv * cu[batch] > (int64_t)INT32_MAX * 64) return LA_ERR_UNSUPPORTED;
   return LA_OK;
@@ -183,7 +187,7 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   s->d = d;
   s->grp = hq / hkv;
   s->nq = 1;
-  s->R = s->grp;
+  s->R = instance_rows(s->grp);
   s->hp = hp;
   s->T = tile;
   s->kind = kind;
@@ -511,7 +515,7 @@ la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlen
     int sms = 0, per_sm = 0;
     la_status e = device_sms(&sms);
     if (e != LA_OK) return e;
-    e = capacity(d, T, hq / hkv, &per_sm);
+    e = capacity(d, T, instance_rows(hq / hkv), &per_sm);
     if (e != LA_OK) return e;
     G = sms * std::max(1, per_sm);
   }
@@ -534,7 +538,7 @@ la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t*
   if (rows > 16) return LA_ERR_UNSUPPORTED;
   for (int b = 0; b < batch; ++b)
     if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
-  const int R = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
+  const int R = instance_rows(rows);
   int G = num_sms;
   if (G <= 0) {
     int sms = 0, per_sm = 0;
@@ -579,7 +583,7 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
   if (rows > 16) return LA_ERR_UNSUPPORTED;
   for (int b = 0; b < batch; ++b)
     if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
-  const int R = rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
+  const int R = instance_rows(rows);
   const int T = tile_tokens == 0 ? la::default_tile(d) / hp : tile_tokens;
   if (!la::tile_supported(d, T, hp)) return LA_ERR_UNSUPPORTED;
   int G = num_sms;
@@ -617,7 +621,7 @@ la_status la_plan_auto(int batch, int hq, int hkv, int d, const int32_t* cu_seql
     int sms = 0, per_sm = 0;
     st = device_sms(&sms);
     if (st != LA_OK) return st;
-    st = capacity(d, la::slab_tile(d, hq / hkv), hq / hkv, &per_sm);
+    st = capacity(d, la::slab_tile(d, hq / hkv), instance_rows(hq / hkv), &per_sm);
     if (st != LA_OK) return st;
     slots = sms * std::max(1, per_sm);
   }
@@ -850,10 +854,10 @@ la_status la_schedule_set_trace(la_schedule* s, void* trace_dev) {
 la_status la_device_capacity(int d, int grp, int* ctas_per_sm, int* num_sms) {
   if (ctas_per_sm == nullptr || num_sms == nullptr) return LA_ERR_INVALID;
   if (la::default_tile(d) == 0) return LA_ERR_UNSUPPORTED;
-  if (grp != 1 && grp != 2 && grp != 4 && grp != 8 && grp != 16) return LA_ERR_UNSUPPORTED;
+  if (grp < 1 || grp > 16) return LA_ERR_UNSUPPORTED;
   la_status e = device_sms(num_sms);
   if (e != LA_OK) return e;
-  return capacity(d, la::default_tile(d), grp, ctas_per_sm);
+  return capacity(d, la::default_tile(d), instance_rows(grp), ctas_per_sm);
 }
 
 void la_schedule_destroy(la_schedule* s) {

@@ -81,7 +81,9 @@ enum {
  * and "3.5 execution flow" of the xllm-io review).
  *
  *   batch, hq, hkv, d  shape; d in {64, 80, 96, 128, 256}; hq % hkv == 0 and
- *                      hq / hkv in {1, 2, 4, 8, 16}
+ *                      1 <= hq / hkv <= 16 (a group that is not a power of
+ *                      two runs on the next larger kernel instance, whose
+ *                      spare rows are zero queries never written out)
  *   cu_seqlens_k       HOST pointer to batch + 1 int32 offsets (read, not kept)
  *   num_sms            grid size G; <= 0 picks one persistent CTA per SM of
  *                      the current device (the kernel runs one CTA per SM).

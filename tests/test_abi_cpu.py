@@ -359,3 +359,16 @@ def test_sixteen_query_rows_per_kv_head():
     # caches: units of one kv head once a kv head has more than 8 rows
     assert la.la_plan_kv(1, 32, 2, 64, [0, 900], num_sms=7).heads_per_unit == 1
     assert la.la_plan_kv(1, 16, 2, 64, [0, 900], num_sms=7).heads_per_unit == 2
+
+
+@pytest.mark.parametrize("grp", [3, 5, 6, 7, 9, 12, 15])
+def test_groups_that_are_not_powers_of_two(grp):
+    # units are still (request, kv head); the instance holds the next power of two rows
+    lengths = [700, 64, 3000]
+    s = la.la_plan(3, 2 * grp, 2, 128, cu_of(lengths), 11)
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(3, 2 * grp, 2, 128, cu_of(lengths), 11, 128))
+    R = 4 if grp <= 4 else 8 if grp <= 8 else 16
+    assert la.la_workspace_size(s) == 256 + 256 + 11 * R * 130 * 4
+    with pytest.raises(la.LeanAttentionError) as e:
+        la.la_plan(1, 34, 2, 64, [0, 100], 7)  # group 17
+    assert e.value.status == la.LA_ERR_UNSUPPORTED

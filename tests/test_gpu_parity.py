@@ -296,3 +296,40 @@ def test_sixteen_query_heads_with_fixed_partitions_and_16_bit_output(splits):
     got = o16.double().cpu().numpy().reshape(ref.shape)
     ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
     assert np.all(np.abs(got - ref) <= 2e-3 + ulp)
+
+
+@pytest.mark.parametrize("d,grp", [(64, 3), (128, 5), (128, 6), (96, 7), (80, 12), (256, 3), (64, 14)])
+@pytest.mark.parametrize("layout", ["slab", "paged"])
+def test_groups_that_are_not_powers_of_two(d, grp, layout):
+    # e.g. 28 query over 4 kv heads (group 7) or 40 over 8 (group 5)
+    from oracle import layouts
+    import oracle
+    w = workloads.custom(3, 2 * grp, 2, d, "bf16", [1000, 129, 2500])
+    q, k, v, cu = workloads.make_inputs(w, seed=d * grp, device="cuda")
+    cu_dev = torch.as_tensor(cu, device="cuda")
+    out = torch.empty(w.batch, w.hq, w.d, device="cuda")
+    if layout == "slab":
+        s = la.la_plan(w.batch, w.hq, w.hkv, w.d, cu, 0)
+        ws = la.new_workspace(s)
+        la.la_decode(q, k, v, cu_dev, s, ws, out, w.scale)
+        ref = reference(w, q, k, v)
+    else:
+        kc, vc, table, npages = workloads.to_paged(w, k, v, 64, seed=grp)
+        s = la.la_plan_kv(w.batch, w.hq, w.hkv, w.d, cu, num_sms=0)
+        ws = la.new_workspace(s)
+        la.la_decode_kv(q, kc, vc, cu_dev, s, ws, out, w.scale, layout="paged", block_table=table.cuda(),
+                        page_size=64, num_pages=npages)
+        kk = layouts.gather_paged(kc.cpu().view(torch.int16).numpy(), table.numpy(), cu, 64, w.hkv, w.d)
+        vv = layouts.gather_paged(vc.cpu().view(torch.int16).numpy(), table.numpy(), cu, 64, w.hkv, w.d)
+        ref = oracle.attend(q.cpu(), kk.astype(np.int16).view(np.uint16), vv.astype(np.int16).view(np.uint16),
+                            cu, w.hq, w.hkv, w.d, w.scale, oracle.BF16)
+    assert la.la_get_status(ws) == la.LA_OK
+    compare(out.cpu(), ref)
+
+
+@pytest.mark.parametrize("splits", [1, 4])
+def test_group_of_five_with_fixed_partitions(splits):
+    w = workloads.custom(2, 40, 8, 128, "bf16", [3000, 257])
+    q, k, v, _ = workloads.make_inputs(w, seed=5, device="cuda")
+    out, _ = run_lean(w, q, k, v, fixed_splits=splits)
+    compare(out.cpu(), reference(w, q, k, v))

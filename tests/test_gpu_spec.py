@@ -29,6 +29,8 @@ CASES = [(d, grp, nq) for d in (64, 128) for grp, nq in ((1, 2), (1, 3), (1, 4),
 CASES += [(80, 1, 4), (96, 2, 2), (256, 1, 5)]
 # 9-16 query rows per kv head (two blocks of 8 on the tensor-core path)
 CASES += [(64, 8, 2), (128, 8, 2), (128, 4, 4), (64, 2, 8), (128, 1, 16), (96, 4, 3), (256, 2, 6), (80, 8, 2)]
+# groups that are not powers of two, times several query tokens
+CASES += [(128, 3, 2), (64, 5, 3), (128, 7, 2)]
 
 
 @pytest.mark.parametrize("d,grp,nq", CASES)
