@@ -216,7 +216,7 @@ def algorithmic_bytes(w, export, out_bytes=4):
     G, U, nseg = export[1], export[2], export[5]
     base = 8 + 2 * (G + 1) + (U + 1)
     pieces = sum(1 for i in range(nseg) if export[base + 5 * i + 3] in (1, 3))
-    rows = (w.hq // w.hkv) * w.nq * (w.batch * w.hkv // U)  # query rows of a unit (all its kv heads)
+    rows = w.batch * w.nq * w.hq // U  # query rows of a unit (all its kv heads, or one query block)
     rec = rows * (w.d + 2) * 4
     return kv, kv + q + out + 2 * pieces * rec
 
@@ -508,6 +508,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.description, "kernel": args.kernel, "schedule": dec.kind,
                    "tile_tokens": la.la_schedule_export(dec.sched)[4], "out_dtype": args.out_dtype,
                    "kv_heads_per_unit": dec.sched.heads_per_unit,
+                   "query_blocks_per_kv_head": dec.sched.query_blocks,
                    "ring_stages": args.stages or "library default",
                    "kv_layout": args.kv_layout + (f" (page {args.page_size})" if args.kv_layout == "paged" else ""),
                    "predicted_us": dec.predicted_us, "grid": G,

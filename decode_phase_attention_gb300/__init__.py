@@ -101,8 +101,10 @@ class Schedule:
         self.batch, self.hq, self.hkv, self.d = batch, hq, hkv, d
         self.cu = cu
         self.nq = nq
-        head = la_schedule_export(self)[:3]
-        self.heads_per_unit = batch * hkv // head[2]  # kv heads of one unit (U = batch * hkv / that)
+        per_request = la_schedule_export(self)[2] // batch  # units per request: hkv * query_blocks / heads_per_unit
+        # kv heads of one unit, and query blocks per kv head (one of the two is 1)
+        self.heads_per_unit = max(1, hkv // per_request)
+        self.query_blocks = max(1, per_request // hkv)
 
     @property
     def handle(self):

@@ -37,6 +37,22 @@ constexpr int kMaxGrid = 1 << 20;
 // 4, 8 or 16 (the spare rows are zero queries that are never written out).
 int instance_rows(int rows) { return rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : 16; }
 
+// Query blocks per kv head: the fewest blocks of equal size (a divisor of
+// grp) whose grp / qb * nq query rows fit the 16 an instance holds; 0 when
+// none does (nq > 16).
+int query_blocks(int grp, int nq) {
+  if (grp < 1 || nq < 1 || nq > 16) return 0;
+  for (int qb = 1; qb <= grp; ++qb)
+    if (grp % qb == 0 && (grp / qb) * nq <= 16) return qb;
+  return 0;
+}
+
+// Query rows of one unit head (a kv head, or one query block of one).
+int unit_rows(int grp, int nq) {
+  const int qb = query_blocks(grp, nq);
+  return qb == 0 ? 0 : (grp / qb) * nq;
+}
+
 la_status check_shape(int batch, int hq, int hkv, int d, const int32_t* cu) {
   if (batch <= 0 || hq <= 0 || hkv <= 0 || cu == nullptr) return LA_ERR_INVALID;
   if (hq % hkv != 0) return LA_ERR_INVALID;
@@ -45,17 +61,15 @@ la_status check_shape(int batch, int hq, int hkv, int d, const int32_t* cu) {
     if (cu[b + 1] <= cu[b]) return LA_ERR_INVALID;  // every context holds >= 1 token
   if (d <= 0) return LA_ERR_INVALID;
   if (la::default_tile(d) == 0) return LA_ERR_UNSUPPORTED;
-  const int grp = hq / hkv;
-  if (grp > 16) return LA_ERR_UNSUPPORTED;  // more query rows than the tile paths hold
   // element offsets are formed in 64 bits, tile indices in 32 bits
   if ((int64_t)hkv * cu[batch] > (int64_t)INT32_MAX * 64) return LA_ERR_UNSUPPORTED;
   return LA_OK;
 }
 
-// Units (b, kv head group of hp heads) in request-major order and their tile
-// prefix sums.
+// Units (b, group of hp kv heads or one query block of a kv head) in
+// request-major order and their tile prefix sums.
 bool build_units(la_schedule* s) {
-  const int groups = s->hkv / s->hp;
+  const int groups = s->unit_heads() / s->hp;
   s->U = s->batch * groups;
   s->unit_iter.assign((size_t)s->U + 1, 0);
   int64_t acc = 0;
@@ -151,8 +165,9 @@ void build_dev_segs(la_schedule* s) {
   for (size_t i = 0; i < n; ++i) {
     const int32_t* sg = &s->segs[i * la::kSegWords];
     int32_t* dv = &s->dev_segs[i * la::kDevSegWords];
-    const int groups = s->hkv / s->hp;
-    const int b = sg[0] / groups, kvh = (sg[0] % groups) * s->hp;  // first kv head of the unit
+    const int groups = s->unit_heads() / s->hp;
+    // first kv head of the unit (the kv head of its query block)
+    const int b = sg[0] / groups, kvh = (sg[0] % groups) * s->hp / s->qb;
     const int64_t L = (int64_t)s->cu[b + 1] - s->cu[b];
     const int64_t row0 = (int64_t)s->hkv * s->cu[b] + (int64_t)kvh * L;
     for (int w = 0; w < la::kSegWords; ++w) dv[w] = sg[w];
@@ -167,16 +182,19 @@ void build_dev_segs(la_schedule* s) {
 }
 
 la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, int kind, int grid_or_splits,
-                        la_schedule** out, int tile = 0, int hp = 1, int rows = 0) {
+                        la_schedule** out, int tile = 0, int hp = 1, int nq = 1) {
   if (out == nullptr) return LA_ERR_INVALID;
   *out = nullptr;
   const la_status st = check_shape(batch, hq, hkv, d, cu);
   if (st != LA_OK) return st;
   if (hp < 1 || hkv % hp != 0) return LA_ERR_INVALID;
+  const int qb = query_blocks(hq / hkv, nq);
+  if (qb == 0) return LA_ERR_UNSUPPORTED;
+  if (qb > 1 && hp != 1) return LA_ERR_UNSUPPORTED;  // a query block is a unit of its own
+  const int rows = (hq / hkv / qb) * nq;
   // stream-K on the slab layout: slab_tile; the fixed partitions keep the
   // table's tile (with few busy SMs each CTA needs the deeper 192 KiB ring)
-  if (tile == 0)
-    tile = (hp == 1 && kind == 0) ? la::slab_tile(d, rows > 0 ? rows : hq / hkv) : la::default_tile(d) / hp;
+  if (tile == 0) tile = (hp == 1 && kind == 0) ? la::slab_tile(d, rows) : la::default_tile(d) / hp;
   if (tile < 0) return LA_ERR_INVALID;
   if (!la::tile_supported(d, tile, hp)) return LA_ERR_UNSUPPORTED;
   la_schedule* s = new (std::nothrow) la_schedule();
@@ -186,8 +204,9 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   s->hkv = hkv;
   s->d = d;
   s->grp = hq / hkv;
-  s->nq = 1;
-  s->R = instance_rows(s->grp);
+  s->nq = nq;
+  s->qb = qb;
+  s->R = instance_rows(rows);
   s->hp = hp;
   s->T = tile;
   s->kind = kind;
@@ -219,7 +238,7 @@ la_status capacity(int d, int T, int grp, int* per_sm, int hp = 1) {
   static std::map<long long, int> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
-  const long long key = ((((long long)dev * 1024 + d) * 1024 + T) * 16 + grp) * 4 + hp;
+  const long long key = ((((long long)dev * 1024 + d) * 1024 + T) * 32 + grp) * 16 + hp;
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it != cache.end()) {
@@ -306,7 +325,7 @@ double simulate_dispatch(const std::vector<double>& job_bytes, int slots, double
 
 // Bytes of K+V of tiles [t0, t1) of unit u.
 double piece_bytes(const la_schedule* s, int u, int t0, int t1) {
-  const int b = u / (s->hkv / s->hp);
+  const int b = u / (s->unit_heads() / s->hp);
   const int64_t L = (int64_t)s->cu[b + 1] - s->cu[b];
   const int64_t tok = std::min<int64_t>((int64_t)t1 * s->T, L) - (int64_t)t0 * s->T;
   return (double)tok * s->hp * s->d * 2.0 * 2.0;
@@ -509,13 +528,14 @@ la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlen
   if (G <= 0) {
     const la_status st = check_shape(batch, hq, hkv, d, cu_seqlens_k);
     if (st != LA_OK) return st;
-    const int T = tile_tokens == 0 ? la::slab_tile(d, hq / hkv) : tile_tokens;
+    const int rows = unit_rows(hq / hkv, 1);
+    const int T = tile_tokens == 0 ? la::slab_tile(d, rows) : tile_tokens;
     if (T <= 0) return LA_ERR_INVALID;
     if (!la::tile_supported(d, T)) return LA_ERR_UNSUPPORTED;
     int sms = 0, per_sm = 0;
     la_status e = device_sms(&sms);
     if (e != LA_OK) return e;
-    e = capacity(d, T, instance_rows(hq / hkv), &per_sm);
+    e = capacity(d, T, instance_rows(rows), &per_sm);
     if (e != LA_OK) return e;
     G = sms * std::max(1, per_sm);
   }
@@ -534,8 +554,8 @@ la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t*
   la_status st = check_shape(batch, hq, hkv, d, cu_seqlens_k);
   if (st != LA_OK) return st;
   if (nq < 1) return LA_ERR_INVALID;
-  const int rows = (hq / hkv) * nq;
-  if (rows > 16) return LA_ERR_UNSUPPORTED;
+  const int rows = unit_rows(hq / hkv, nq);
+  if (rows == 0) return LA_ERR_UNSUPPORTED;
   for (int b = 0; b < batch; ++b)
     if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
   const int R = instance_rows(rows);
@@ -549,11 +569,7 @@ la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t*
     G = sms * std::max(1, per_sm);
   }
   if (G > kMaxGrid) return LA_ERR_INVALID;
-  st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out, 0, 1, rows);
-  if (st != LA_OK) return st;
-  (*out)->nq = nq;
-  (*out)->R = R;
-  return LA_OK;
+  return make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out, 0, 1, nq);
 }
 
 la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* cu_seqlens_k, int heads_per_unit,
@@ -564,7 +580,10 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
   if (st != LA_OK) return st;
   if (nq < 1 || tile_tokens < 0) return LA_ERR_INVALID;
   int hp = heads_per_unit;
-  if ((hq / hkv) * nq > 8) {  // 9-16 query rows per kv head: units of one kv head only
+  const int rows = unit_rows(hq / hkv, nq);
+  if (rows == 0) return LA_ERR_UNSUPPORTED;
+  // 9-16 query rows per unit, or query blocks: units of one kv head only
+  if (rows > 8 || query_blocks(hq / hkv, nq) > 1) {
     if (hp > 1) return LA_ERR_UNSUPPORTED;
     hp = 1;
   }
@@ -579,8 +598,6 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
         if (hkv % h == 0 && la::tile_supported(d, la::default_tile(d) / h, h)) hp = h;
   }
   if ((hp != 1 && hp != 2 && hp != 4 && hp != 8) || hkv % hp != 0) return LA_ERR_INVALID;
-  const int rows = (hq / hkv) * nq;
-  if (rows > 16) return LA_ERR_UNSUPPORTED;
   for (int b = 0; b < batch; ++b)
     if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
   const int R = instance_rows(rows);
@@ -596,11 +613,7 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
     G = sms * std::max(1, per_sm);
   }
   if (G > kMaxGrid) return LA_ERR_INVALID;
-  st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out, T, hp);
-  if (st != LA_OK) return st;
-  (*out)->nq = nq;
-  (*out)->R = R;
-  return LA_OK;
+  return make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, G, out, T, hp, nq);
 }
 
 la_status la_plan_fixed(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k, int splits,
@@ -621,7 +634,9 @@ la_status la_plan_auto(int batch, int hq, int hkv, int d, const int32_t* cu_seql
     int sms = 0, per_sm = 0;
     st = device_sms(&sms);
     if (st != LA_OK) return st;
-    st = capacity(d, la::slab_tile(d, hq / hkv), instance_rows(hq / hkv), &per_sm);
+    const int rows = unit_rows(hq / hkv, 1);
+    if (rows == 0) return LA_ERR_UNSUPPORTED;
+    st = capacity(d, la::slab_tile(d, rows), instance_rows(rows), &per_sm);
     if (st != LA_OK) return st;
     slots = sms * std::max(1, per_sm);
   }
@@ -629,7 +644,7 @@ la_status la_plan_auto(int batch, int hq, int hkv, int d, const int32_t* cu_seql
   st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 0, slots, &cand[0]);  // stream-K over every SM
   if (st == LA_OK) st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 1, 1, &cand[1]);  // one CTA per unit
   if (st == LA_OK) {
-    const int units = batch * hkv;
+    const int units = cand[1]->U;
     const int k = std::max(2, (slots + units - 1) / units);  // fixed split that fills the SMs
     st = make_schedule(batch, hq, hkv, d, cu_seqlens_k, 1, k, &cand[2]);
   }
@@ -738,7 +753,8 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
   p.G = s->G;
   p.batch = s->batch;
   p.hq = s->hq;
-  p.hkv = s->hkv;
+  p.hkv = s->unit_heads();
+  p.kv_heads = s->hkv;
   p.qscale = scale * 1.4426950408889634f;  // log2(e): scores in base-2 units
   p.spin_ns = s->spin_ns;
   p.skip_signal = s->skip_signal;
@@ -754,9 +770,9 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
   }
   cudaStream_t st = (cudaStream_t)stream;
   const int dtype = dt == LA_BF16 ? 1 : 0;
-  p.grp = s->grp;
+  p.grp = s->unit_grp();
   p.nq = s->nq;
-  p.rows = s->grp * s->nq;
+  p.rows = s->unit_grp() * s->nq;
   p.stages = s->stages > 0 ? s->stages : (s->kind == 0 ? la::stream_stages(s->d, s->T, s->hp, kv_layout) : 0);
   cudaError_t ce = la::launch_decode(s->d, s->T, s->R, s->hp, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
@@ -768,11 +784,11 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
     c.out = out;
     c.U = s->U;
     c.hq = s->hq;
-    c.hkv = s->hkv;
+    c.hkv = s->unit_heads();
     c.out_dtype = out_dtype;
-    c.grp = s->grp;
+    c.grp = s->unit_grp();
     c.nq = s->nq;
-    c.rows = s->grp * s->nq;
+    c.rows = s->unit_grp() * s->nq;
     ce = la::launch_combine(s->d, s->R, c, st);
     if (ce != cudaSuccess) return LA_ERR_CUDA;
   }
@@ -854,10 +870,11 @@ la_status la_schedule_set_trace(la_schedule* s, void* trace_dev) {
 la_status la_device_capacity(int d, int grp, int* ctas_per_sm, int* num_sms) {
   if (ctas_per_sm == nullptr || num_sms == nullptr) return LA_ERR_INVALID;
   if (la::default_tile(d) == 0) return LA_ERR_UNSUPPORTED;
-  if (grp < 1 || grp > 16) return LA_ERR_UNSUPPORTED;
+  const int rows = unit_rows(grp, 1);
+  if (rows == 0) return LA_ERR_UNSUPPORTED;
   la_status e = device_sms(num_sms);
   if (e != LA_OK) return e;
-  return capacity(d, la::default_tile(d), instance_rows(grp), ctas_per_sm);
+  return capacity(d, la::default_tile(d), instance_rows(rows), ctas_per_sm);
 }
 
 void la_schedule_destroy(la_schedule* s) {

@@ -58,15 +58,17 @@ struct KParams {
   int G;
   int batch;
   int hq;
-  int hkv;
+  int hkv;                  // unit heads per request: kv heads x query blocks per kv head
+  int kv_heads = 0;         // kv heads of the K/V tensors (token-major / paged tensor maps)
   float qscale;             // scale * log2(e): scores are kept in base-2 units
   long long spin_ns;        // limit of every wait inside the kernel
   int skip_signal;          // test hook: this CTA never sets its flag (-1: none)
   unsigned long long* trace;  // optional per-CTA timeline (kTraceWords each), or null
   int out_dtype = 0;          // 0 fp32, 1 fp16, 2 bf16
   // Query rows of a unit: rows = grp * nq (<= the instance's row count);
-  // row r is query token r / grp of the request and head kvh * grp + r % grp.
-  int grp = 1;                // query heads per kv head
+  // row r is query token r / grp of the request and head kvh * grp + r % grp,
+  // kvh the unit head (a kv head, or one query block of one).
+  int grp = 1;                // query heads per unit head
   int nq = 1;                 // query tokens per request (speculative decoding: > 1)
   int rows = 1;               // grp * nq
   int kv_layout = kKvSlab;
@@ -97,9 +99,9 @@ struct CParams {            // fixed-split merge launch
   void* out;
   int U;
   int hq;
-  int hkv;
+  int hkv;                  // unit heads per request (KParams::hkv)
   int out_dtype = 0;        // 0 fp32, 1 fp16, 2 bf16
-  int grp = 1;              // query heads per kv head
+  int grp = 1;              // query heads per unit head
   int nq = 1;               // query tokens per request
   int rows = 1;             // grp * nq
 };

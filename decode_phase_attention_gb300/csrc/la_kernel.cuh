@@ -297,7 +297,8 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, int ou
 }
 
 // Element offset / D of query row r of unit (b, kvh) in q and out
-// ([batch, nq, hq, d]): query token r / grp, head kvh * grp + r % grp.
+// ([batch, nq, hq, d]): query token r / grp, head kvh * grp + r % grp (kvh
+// and grp count unit heads: a query block of a kv head is a head of its own).
 template <typename P>
 __device__ __forceinline__ size_t row_index(const P& p, int b, int kvh, int r) {
   return ((size_t)b * p.nq + r / p.grp) * p.hq + (size_t)kvh * p.grp + r % p.grp;
@@ -1210,7 +1211,7 @@ cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
   if (p.G <= 0) return cudaSuccess;
   CUtensorMap mk, mv;
   if (p.kv_layout != kKvSlab) {
-    e = encode_kv_maps_3d(p.k, p.v, p.kv_rows, p.hkv, D, C::TC ? C::W : D, HP, p.box_rows, C::TC,
+    e = encode_kv_maps_3d(p.k, p.v, p.kv_rows, p.kv_heads, D, C::TC ? C::W : D, HP, p.box_rows, C::TC,
                           (int)Elem<E>::kTmaType, &mk, &mv);
     if (e != cudaSuccess) return e;
   } else if (HP != 1) {

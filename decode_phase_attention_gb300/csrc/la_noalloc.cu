@@ -127,15 +127,16 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   p.G = s->G;
   p.batch = s->batch;
   p.hq = s->hq;
-  p.hkv = s->hkv;
+  p.hkv = s->unit_heads();
+  p.kv_heads = s->hkv;
   p.qscale = scale * 1.4426950408889634f;
   p.spin_ns = s->spin_ns;
   p.skip_signal = s->skip_signal;
   p.trace = s->trace;
   const int dtype = dt == LA_BF16 ? 1 : 0;
-  p.grp = s->grp;
+  p.grp = s->unit_grp();
   p.nq = s->nq;
-  p.rows = s->grp * s->nq;
+  p.rows = s->unit_grp() * s->nq;
   p.stages = s->stages > 0 ? s->stages : (s->kind == 0 ? la::stream_stages(s->d, s->T, s->hp, la::kKvSlab) : 0);
   cudaError_t ce = la::launch_decode(s->d, s->T, s->R, 1, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
@@ -147,10 +148,10 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
     c.out = out;
     c.U = s->U;
     c.hq = s->hq;
-    c.hkv = s->hkv;
-    c.grp = s->grp;
+    c.hkv = s->unit_heads();
+    c.grp = s->unit_grp();
     c.nq = s->nq;
-    c.rows = s->grp * s->nq;
+    c.rows = s->unit_grp() * s->nq;
     ce = la::launch_combine(s->d, s->R, c, st);
     if (ce != cudaSuccess) return LA_ERR_CUDA;
   }

@@ -80,10 +80,17 @@ enum {
  * la_plan -- the stream-K tile planner ("3.4 stream-K style decomposition"
  * and "3.5 execution flow" of the xllm-io review).
  *
- *   batch, hq, hkv, d  shape; d in {64, 80, 96, 128, 256}; hq % hkv == 0 and
- *                      1 <= hq / hkv <= 16 (a group that is not a power of
- *                      two runs on the next larger kernel instance, whose
- *                      spare rows are zero queries never written out)
+ *   batch, hq, hkv, d  shape; d in {64, 80, 96, 128, 256}; hq % hkv == 0
+ *                      (any group grp = hq / hkv). Up to 16 query rows per
+ *                      kv head run as one unit; a group that is not a power
+ *                      of two runs on the next larger kernel instance (1, 2,
+ *                      4, 8 or 16 rows), whose spare rows are zero queries
+ *                      never written out. A kv head with more than 16 rows
+ *                      (grp > 16, e.g. multi-query attention) is split into
+ *                      query blocks: the fewest equal blocks of consecutive
+ *                      query heads with at most 16 rows each (qb blocks of
+ *                      grp / qb heads, qb dividing grp); every block is a
+ *                      unit of its own that reads the kv head's K/V
  *   cu_seqlens_k       HOST pointer to batch + 1 int32 offsets (read, not kept)
  *   num_sms            grid size G; <= 0 picks one persistent CTA per SM of
  *                      the current device (the kernel runs one CTA per SM).
@@ -95,7 +102,8 @@ enum {
  * Rules: tiles(b) = ceil(L_b / T) with the default T of la_plan_ex
  * (the review's table: 256 at d = 64, 128 at d = 128; 64 at d = 128 with
  * one or two query heads per kv head, measured faster on GB300);
- * units (b, kv head) in request-major order; I = total tiles; CTA g takes
+ * units (b, kv head[, query block]) in request-major order, then kv head,
+ * then query block; I = total tiles; CTA g takes
  * floor(I/G) iterations plus one if g < I mod G, in order; the host of a
  * unit is the CTA holding its first tile, the finisher the one holding its
  * last. Pure host code when num_sms > 0. Returns LA_ERR_INVALID for bad
@@ -140,8 +148,10 @@ la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlen
  * schedule la_decode / la_decode_ex / la_decode_kv / la_decode_static read
  * q as [batch, nq, hq, d] and write out as [batch, nq, hq, d]. The tiles and
  * their split are those of la_plan (K/V are read once per kv head for all
- * grp * nq query rows). Requires grp * nq <= 16 (LA_ERR_UNSUPPORTED) and
- * L_b >= nq for every request (LA_ERR_INVALID); nq = 1 is la_plan.
+ * grp * nq query rows, up to 16; above that the kv head's query heads are
+ * split into query blocks as in la_plan, each of grp / qb * nq <= 16 rows).
+ * Requires nq <= 16 (LA_ERR_UNSUPPORTED) and L_b >= nq for every request
+ * (LA_ERR_INVALID); nq = 1 is la_plan.
  */
 la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t* cu_seqlens_k, int num_sms,
                        la_schedule** out);
@@ -185,8 +195,9 @@ int la_schedule_grid(const la_schedule* s);
 /*
  * Bytes of device workspace la_decode needs for this schedule: a header, G
  * ready flags and G partial records of rows * (d + 2) floats, rounded up to
- * a multiple of 4 floats (rows = query rows per kv head, rounded up to 1, 2,
- * 4 or 8, times the kv heads per unit) ("7.4
+ * a multiple of 4 floats (rows = query rows per unit head -- a kv head or
+ * one query block of one -- rounded up to 1, 2, 4, 8 or 16, times the kv
+ * heads per unit) ("7.4
  * limitations": a small amount of global memory for sharing partial
  * results). Zero it once (la_workspace_init) before its first use; after
  * that it needs no clearing between calls. One workspace must not be used
@@ -286,8 +297,8 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
  *                   head; more rows need 1). 0 picks the fewest heads
  *                   whose rows make whole 256-byte pieces if that count
  *                   divides hkv, else the most built count that divides
- *                   hkv, else 1 (always 1 for d = 128, 256 and for 9-16
- *                   query rows per kv head).
+ *                   hkv, else 1 (always 1 for d = 128, 256, for 9-16
+ *                   query rows per kv head and for query blocks).
  *   tile_tokens     tokens of each head per tile; 0 picks the default:
  *                   the review's table size of d (128 at d = 128 also for
  *                   one or two query rows: 16-token pages read 13 % slower
@@ -396,7 +407,8 @@ la_status la_schedule_set_stages(la_schedule* s, int stages);
 la_status la_schedule_set_trace(la_schedule* s, void* trace_dev);
 
 /* Most CTAs of the stream-K kernel one SM of the current device holds for
- * head dim d and group size grp, and the SM count. */
+ * head dim d and group size grp (any grp >= 1; above 16, the instance of its
+ * query blocks), and the SM count. */
 la_status la_device_capacity(int d, int grp, int* ctas_per_sm, int* num_sms);
 
 void la_schedule_destroy(la_schedule* s);

@@ -104,7 +104,6 @@ def test_fixed_planner_matches_reference(splits):
     ((2, 4, 4, 64, [0, 10, 10], 4), la.LA_ERR_INVALID),         # empty context
     ((1, 4, 4, 64, [1, 10], 4), la.LA_ERR_INVALID),             # cu[0] != 0
     ((1, 4, 4, 112, [0, 10], 4), la.LA_ERR_UNSUPPORTED),        # head dim not built
-    ((1, 128, 4, 64, [0, 10], 4), la.LA_ERR_UNSUPPORTED),       # group of 32 not built
 ])
 def test_plan_rejects_bad_shapes(args, status):
     with pytest.raises(la.LeanAttentionError) as e:
@@ -243,7 +242,7 @@ def test_spec_schedule_matches_the_decode_plan_and_sizes_its_records():
 
 
 @pytest.mark.parametrize("hq,hkv,nq,lengths,status", [
-    (16, 2, 3, [100, 200], la.LA_ERR_UNSUPPORTED),  # 8 x 3 = 24 query rows per unit
+    (4, 4, 17, [100, 200], la.LA_ERR_UNSUPPORTED),  # 17 query tokens: more rows than an instance holds
     (4, 4, 5, [100, 4], la.LA_ERR_INVALID),          # a context shorter than its query tokens
     (4, 4, 0, [100, 200], la.LA_ERR_INVALID),
 ])
@@ -315,7 +314,8 @@ def test_two_head_records_hold_both_heads():
     (dict(hkv=4, hq=8, heads_per_unit=2, d=128), la.LA_ERR_UNSUPPORTED),   # rows already 256 bytes: not built
     (dict(hkv=4, hq=8, heads_per_unit=2, tile_tokens=256), la.LA_ERR_UNSUPPORTED),
     (dict(hkv=4, hq=8, tile_tokens=-1), la.LA_ERR_INVALID),
-    (dict(hkv=2, hq=16, nq=3), la.LA_ERR_UNSUPPORTED),            # 8 x 3 query rows per kv head
+    (dict(hkv=2, hq=4, nq=17), la.LA_ERR_UNSUPPORTED),            # 17 query tokens per request
+    (dict(hkv=2, hq=64, heads_per_unit=2), la.LA_ERR_UNSUPPORTED),  # query blocks: one kv head per unit
     (dict(hkv=2, hq=16, nq=2, heads_per_unit=2), la.LA_ERR_UNSUPPORTED),  # 16 rows: one kv head per unit
 ])
 def test_plan_kv_rejections(kw, status):
@@ -369,6 +369,47 @@ def test_groups_that_are_not_powers_of_two(grp):
     assert la.la_schedule_export(s) == P.export(P.plan_lean(3, 2 * grp, 2, 128, cu_of(lengths), 11, 128))
     R = 4 if grp <= 4 else 8 if grp <= 8 else 16
     assert la.la_workspace_size(s) == 256 + 256 + 11 * R * 130 * 4
+
+
+# ---- query blocks: more than 16 query rows per kv head
+# (group, query tokens) -> (query blocks per kv head, rows of one block's
+# instance): the fewest equal blocks of whole query heads whose rows fit 16.
+QUERY_BLOCKS = [
+    (32, 1, 2, 16), (24, 1, 2, 16), (17, 1, 17, 1), (18, 1, 2, 16), (34, 1, 17, 2), (40, 1, 4, 16),
+    (48, 1, 3, 16), (64, 1, 4, 16), (128, 1, 8, 16), (8, 3, 2, 16), (8, 4, 2, 16), (16, 2, 2, 16),
+    (4, 5, 2, 16), (1, 16, 1, 16), (2, 16, 2, 16),
+]
+
+
+@pytest.mark.parametrize("grp,nq,qb,R", QUERY_BLOCKS)
+def test_query_blocks_are_units_of_their_own(grp, nq, qb, R):
+    # a kv head with more rows than an instance holds becomes qb units, one
+    # per block of grp / qb query heads: the schedule is the planner's over
+    # hkv * qb heads of grp / qb query heads each
+    lengths = [700, 64, 3000]
+    hkv, d, G = 2, 64, 11
+    s = la.la_plan_spec(3, hkv * grp, hkv, d, nq, cu_of(lengths), G)
+    assert s.query_blocks == qb and s.heads_per_unit == 1
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(3, hkv * grp, hkv * qb, d, cu_of(lengths),
+                                                            G, 256))
+    rec = -(-R * (d + 2) // 4) * 4  # a record: R rows of (d + 2) floats, padded to 16 bytes
+    assert la.la_workspace_size(s) == 256 + 256 + G * rec * 4
+    if nq == 1:
+        assert la.la_schedule_export(la.la_plan(3, hkv * grp, hkv, d, cu_of(lengths), G)) \
+            == la.la_schedule_export(s)
+        f = la.la_plan_fixed(3, hkv * grp, hkv, d, cu_of(lengths), 3)
+        assert la.la_schedule_export(f) == P.export(P.plan_fixed(3, hkv * grp, hkv * qb, d, cu_of(lengths), 3, 256))
+    kv = la.la_plan_kv(3, hkv * grp, hkv, d, cu_of(lengths), nq=nq, num_sms=G)
+    assert kv.query_blocks == qb and kv.heads_per_unit == 1
+
+
+def test_query_blocks_of_a_single_kv_head():
+    # multi-query attention: 64 query heads share one kv head (4 blocks of 16)
+    s = la.la_plan(2, 64, 1, 128, [0, 900, 1000], 7)
+    assert s.query_blocks == 4
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 64, 4, 128, [0, 900, 1000], 7, 128))
+    s, kind, _ = la.la_plan_auto(2, 64, 1, 128, [0, 900, 1000], 152)
+    assert s.query_blocks == 4
     with pytest.raises(la.LeanAttentionError) as e:
-        la.la_plan(1, 34, 2, 64, [0, 100], 7)  # group 17
-    assert e.value.status == la.LA_ERR_UNSUPPORTED
+        la.la_plan_kv(1, 64, 1, 128, [0, 900], heads_per_unit=2, num_sms=7)
+    assert e.value.status == la.LA_ERR_UNSUPPORTED  # query blocks: one kv head per unit
