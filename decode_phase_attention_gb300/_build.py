@@ -15,7 +15,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "liblean_attn.so")
 SOURCES = ["la_api.cu", "la_noalloc.cu", "la_kernels_d64.cu", "la_kernels_d80.cu", "la_kernels_d96.cu",
            "la_kernels_d128.cu", "la_kernels_d256.cu", "la_kernels_d64_hp2.cu",
-           "la_kernels_d80_hp2.cu", "la_kernels_d80_hp8.cu", "la_kernels_d96_hp2.cu", "la_kernels_d96_hp4.cu"]
+           "la_kernels_d80_hp2.cu", "la_kernels_d80_hp8.cu", "la_kernels_d96_hp2.cu", "la_kernels_d96_hp4.cu",
+           "la_kernels_wide.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

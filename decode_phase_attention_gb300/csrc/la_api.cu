@@ -33,24 +33,46 @@ namespace {
 
 constexpr int kMaxGrid = 1 << 20;
 
-// Query rows per kv head the kernel instance holds: rows rounded up to 1, 2,
-// 4, 8 or 16 (the spare rows are zero queries that are never written out).
-int instance_rows(int rows) { return rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : 16; }
+// Query rows per unit head the kernel instance holds: rows rounded up to 1,
+// 2, 4, 8 or 16 (the spare rows are zero queries that are never written
+// out); more than 16 rows run on the tcgen05 kernel's 128-row instance.
+int instance_rows(int rows) {
+  return rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : rows <= 16 ? 16 : la::kWideRows;
+}
+
+// Query rows one unit can hold at head dim d: 128 where the tcgen05 kernel
+// is built, else 16.
+int max_unit_rows(int d) { return la::wide_supported(d) ? la::kWideRows : 16; }
 
 // Query blocks per kv head: the fewest blocks of equal size (a divisor of
-// grp) whose grp / qb * nq query rows fit the 16 an instance holds; 0 when
-// none does (nq > 16).
-int query_blocks(int grp, int nq) {
-  if (grp < 1 || nq < 1 || nq > 16) return 0;
+// grp) whose grp / qb * nq query rows fit one unit; 0 when none does (nq
+// alone is more than a unit holds).
+int query_blocks(int grp, int nq, int d) {
+  const int lim = max_unit_rows(d);
+  if (grp < 1 || nq < 1 || nq > lim) return 0;
   for (int qb = 1; qb <= grp; ++qb)
-    if (grp % qb == 0 && (grp / qb) * nq <= 16) return qb;
+    if (grp % qb == 0 && (grp / qb) * nq <= lim) return qb;
   return 0;
 }
 
 // Query rows of one unit head (a kv head, or one query block of one).
-int unit_rows(int grp, int nq) {
-  const int qb = query_blocks(grp, nq);
+int unit_rows(int grp, int nq, int d) {
+  const int qb = query_blocks(grp, nq, d);
   return qb == 0 ? 0 : (grp / qb) * nq;
+}
+
+// LeanTile tokens a unit of `rows` query rows uses by default: 128 on the
+// tcgen05 kernel; else slab_tile for stream-K schedules and the table's
+// size for fixed partitions.
+int unit_tile(int d, int rows, int kind) {
+  if (rows > 16) return la::kWideTile;
+  return kind == 0 ? la::slab_tile(d, rows) : la::default_tile(d);
+}
+
+// Whether (d, T, hp) is built for units of `rows` query rows.
+bool unit_tile_supported(int d, int T, int hp, int rows) {
+  if (rows > 16) return la::wide_supported(d) && T == la::kWideTile && hp == 1;
+  return la::tile_supported(d, T, hp);
 }
 
 la_status check_shape(int batch, int hq, int hkv, int d, const int32_t* cu) {
@@ -188,15 +210,16 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   const la_status st = check_shape(batch, hq, hkv, d, cu);
   if (st != LA_OK) return st;
   if (hp < 1 || hkv % hp != 0) return LA_ERR_INVALID;
-  const int qb = query_blocks(hq / hkv, nq);
+  const int qb = query_blocks(hq / hkv, nq, d);
   if (qb == 0) return LA_ERR_UNSUPPORTED;
-  if (qb > 1 && hp != 1) return LA_ERR_UNSUPPORTED;  // a query block is a unit of its own
   const int rows = (hq / hkv / qb) * nq;
+  // a query block, or a unit of more than 16 rows, is one kv head
+  if ((qb > 1 || rows > 16) && hp != 1) return LA_ERR_UNSUPPORTED;
   // stream-K on the slab layout: slab_tile; the fixed partitions keep the
   // table's tile (with few busy SMs each CTA needs the deeper 192 KiB ring)
-  if (tile == 0) tile = (hp == 1 && kind == 0) ? la::slab_tile(d, rows) : la::default_tile(d) / hp;
+  if (tile == 0) tile = hp == 1 ? unit_tile(d, rows, kind) : la::default_tile(d) / hp;
   if (tile < 0) return LA_ERR_INVALID;
-  if (!la::tile_supported(d, tile, hp)) return LA_ERR_UNSUPPORTED;
+  if (!unit_tile_supported(d, tile, hp, rows)) return LA_ERR_UNSUPPORTED;
   la_schedule* s = new (std::nothrow) la_schedule();
   if (s == nullptr) return LA_ERR_INVALID;
   s->batch = batch;
@@ -238,7 +261,7 @@ la_status capacity(int d, int T, int grp, int* per_sm, int hp = 1) {
   static std::map<long long, int> cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
-  const long long key = ((((long long)dev * 1024 + d) * 1024 + T) * 32 + grp) * 16 + hp;
+  const long long key = ((((long long)dev * 1024 + d) * 1024 + T) * 256 + grp) * 16 + hp;
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
   if (it != cache.end()) {
@@ -404,6 +427,7 @@ bool tile_supported(int d, int T, int hp) {
 }
 
 cudaError_t launch_decode(int d, int T, int grp, int hp, int dtype, const KParams& p, cudaStream_t st) {
+  if (grp == kWideRows) return (hp == 1 && T == kWideTile) ? launch_wide(d, dtype, p, st) : cudaErrorInvalidValue;
   switch (d * 16 + hp) {
     case 64 * 16 + 2: return launch_decode_d64_hp2(T, grp, dtype, p, st);
     case 80 * 16 + 2: return launch_decode_d80_hp2(T, grp, dtype, p, st);
@@ -424,6 +448,7 @@ cudaError_t launch_decode(int d, int T, int grp, int hp, int dtype, const KParam
 }
 
 cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st) {
+  if (grp == kWideRows) return launch_combine_wide(d, p, st);
   switch (d) {
     case 64: return launch_combine_d64(grp, p, st);
     case 80: return launch_combine_d80(grp, p, st);
@@ -435,6 +460,7 @@ cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st) {
 }
 
 cudaError_t decode_capacity(int d, int T, int grp, int hp, int* per_sm) {
+  if (grp == kWideRows) return (hp == 1 && T == kWideTile) ? wide_capacity(d, per_sm) : cudaErrorInvalidValue;
   switch (d * 16 + hp) {
     case 64 * 16 + 2: return decode_capacity_d64_hp2(T, grp, per_sm);
     case 80 * 16 + 2: return decode_capacity_d80_hp2(T, grp, per_sm);
@@ -528,10 +554,10 @@ la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlen
   if (G <= 0) {
     const la_status st = check_shape(batch, hq, hkv, d, cu_seqlens_k);
     if (st != LA_OK) return st;
-    const int rows = unit_rows(hq / hkv, 1);
-    const int T = tile_tokens == 0 ? la::slab_tile(d, rows) : tile_tokens;
+    const int rows = unit_rows(hq / hkv, 1, d);
+    const int T = tile_tokens == 0 ? unit_tile(d, rows, 0) : tile_tokens;
     if (T <= 0) return LA_ERR_INVALID;
-    if (!la::tile_supported(d, T)) return LA_ERR_UNSUPPORTED;
+    if (!unit_tile_supported(d, T, 1, rows)) return LA_ERR_UNSUPPORTED;
     int sms = 0, per_sm = 0;
     la_status e = device_sms(&sms);
     if (e != LA_OK) return e;
@@ -554,7 +580,7 @@ la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t*
   la_status st = check_shape(batch, hq, hkv, d, cu_seqlens_k);
   if (st != LA_OK) return st;
   if (nq < 1) return LA_ERR_INVALID;
-  const int rows = unit_rows(hq / hkv, nq);
+  const int rows = unit_rows(hq / hkv, nq, d);
   if (rows == 0) return LA_ERR_UNSUPPORTED;
   for (int b = 0; b < batch; ++b)
     if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
@@ -564,7 +590,7 @@ la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t*
     int sms = 0, per_sm = 0;
     st = device_sms(&sms);
     if (st != LA_OK) return st;
-    st = capacity(d, la::slab_tile(d, rows), R, &per_sm);
+    st = capacity(d, unit_tile(d, rows, 0), R, &per_sm);
     if (st != LA_OK) return st;
     G = sms * std::max(1, per_sm);
   }
@@ -580,10 +606,10 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
   if (st != LA_OK) return st;
   if (nq < 1 || tile_tokens < 0) return LA_ERR_INVALID;
   int hp = heads_per_unit;
-  const int rows = unit_rows(hq / hkv, nq);
+  const int rows = unit_rows(hq / hkv, nq, d);
   if (rows == 0) return LA_ERR_UNSUPPORTED;
-  // 9-16 query rows per unit, or query blocks: units of one kv head only
-  if (rows > 8 || query_blocks(hq / hkv, nq) > 1) {
+  // more than 8 query rows per unit, or query blocks: units of one kv head only
+  if (rows > 8 || query_blocks(hq / hkv, nq, d) > 1) {
     if (hp > 1) return LA_ERR_UNSUPPORTED;
     hp = 1;
   }
@@ -601,8 +627,8 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
   for (int b = 0; b < batch; ++b)
     if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
   const int R = instance_rows(rows);
-  const int T = tile_tokens == 0 ? la::default_tile(d) / hp : tile_tokens;
-  if (!la::tile_supported(d, T, hp)) return LA_ERR_UNSUPPORTED;
+  const int T = tile_tokens != 0 ? tile_tokens : (rows > 16 ? la::kWideTile : la::default_tile(d) / hp);
+  if (!unit_tile_supported(d, T, hp, rows)) return LA_ERR_UNSUPPORTED;
   int G = num_sms;
   if (G <= 0) {
     int sms = 0, per_sm = 0;
@@ -634,9 +660,9 @@ la_status la_plan_auto(int batch, int hq, int hkv, int d, const int32_t* cu_seql
     int sms = 0, per_sm = 0;
     st = device_sms(&sms);
     if (st != LA_OK) return st;
-    const int rows = unit_rows(hq / hkv, 1);
+    const int rows = unit_rows(hq / hkv, 1, d);
     if (rows == 0) return LA_ERR_UNSUPPORTED;
-    st = capacity(d, la::slab_tile(d, rows), instance_rows(rows), &per_sm);
+    st = capacity(d, unit_tile(d, rows, 0), instance_rows(rows), &per_sm);
     if (st != LA_OK) return st;
     slots = sms * std::max(1, per_sm);
   }
@@ -773,7 +799,8 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
   p.grp = s->unit_grp();
   p.nq = s->nq;
   p.rows = s->unit_grp() * s->nq;
-  p.stages = s->stages > 0 ? s->stages : (s->kind == 0 ? la::stream_stages(s->d, s->T, s->hp, kv_layout) : 0);
+  p.stages = s->stages > 0 ? s->stages
+                           : (s->kind == 0 && s->R <= 16 ? la::stream_stages(s->d, s->T, s->hp, kv_layout) : 0);
   cudaError_t ce = la::launch_decode(s->d, s->T, s->R, s->hp, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {
@@ -870,11 +897,11 @@ la_status la_schedule_set_trace(la_schedule* s, void* trace_dev) {
 la_status la_device_capacity(int d, int grp, int* ctas_per_sm, int* num_sms) {
   if (ctas_per_sm == nullptr || num_sms == nullptr) return LA_ERR_INVALID;
   if (la::default_tile(d) == 0) return LA_ERR_UNSUPPORTED;
-  const int rows = unit_rows(grp, 1);
+  const int rows = unit_rows(grp, 1, d);
   if (rows == 0) return LA_ERR_UNSUPPORTED;
   la_status e = device_sms(num_sms);
   if (e != LA_OK) return e;
-  return capacity(d, la::default_tile(d), instance_rows(rows), ctas_per_sm);
+  return capacity(d, rows > 16 ? la::kWideTile : la::default_tile(d), instance_rows(rows), ctas_per_sm);
 }
 
 void la_schedule_destroy(la_schedule* s) {

@@ -121,8 +121,18 @@ int slab_tile(int d, int rows);
 int stream_stages(int d, int T, int hp, int kv_layout);
 bool tile_supported(int d, int T, int hp = 1);
 
+// Units of more than 16 query rows run on the tcgen05 kernel (la_wide.cuh),
+// whose instance holds kWideRows rows, with 128-token tiles and one kv head
+// per unit; head dims 64 and 128 (wide_supported).
+constexpr int kWideRows = 128;
+constexpr int kWideTile = 128;
+bool wide_supported(int d);
+cudaError_t launch_wide(int d, int dtype, const KParams& p, cudaStream_t st);
+cudaError_t wide_capacity(int d, int* per_sm);
+cudaError_t launch_combine_wide(int d, const CParams& p, cudaStream_t st);
+
 // Launches (la_kernels_d<d>.cu, one file per head dim; la_kernels_d<d>_hp<h>.cu
-// for units of h kv heads). dtype: 0 fp16, 1 bf16.
+// for units of h kv heads; grp == kWideRows: la_kernels_wide.cu). dtype: 0 fp16, 1 bf16.
 // cudaErrorInvalidValue for a (d, T, grp, hp) that is not built.
 cudaError_t launch_decode(int d, int T, int grp, int hp, int dtype, const KParams& p, cudaStream_t st);
 cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st);

@@ -203,6 +203,7 @@ struct Elem<__nv_bfloat16> {
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
   static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  static constexpr bool kBf16 = true;
 };
 template <>
 struct Elem<__half> {
@@ -231,6 +232,7 @@ struct Elem<__half> {
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
   static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  static constexpr bool kBf16 = false;
 };
 
 // ------------------------------------------------------------ configuration
@@ -239,6 +241,8 @@ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 template <int D, int T_, int GRP, int HP = 1>
 struct Cfg {
+  static constexpr int DIM = D;                     // head dim
+  static constexpr int HPU = HP;                    // kv heads per unit
   static constexpr int T = T_;                      // LeanTile tokens (of each kv head of the unit)
   static constexpr int ROWS = T * HP;               // K (and V) rows of a tile: T tokens x HP kv heads
   static constexpr bool TC = (GRP >= 4);            // tensor-core tile path
@@ -342,14 +346,15 @@ __device__ __forceinline__ bool unit_offsets_ok(const KParams& p, int b) {
 
 // Stages of the ring this launch cycles through: the host's choice
 // (KParams::stages) within [2, STAGES]; 0 (or out of range) means STAGES.
-template <int D, int T, int GRP, int HP>
+template <class C>
 __device__ __forceinline__ int ring_stages(const KParams& p) {
-  constexpr int S = Cfg<D, T, GRP, HP>::STAGES;
-  return (p.stages >= 2 && p.stages < S) ? p.stages : S;
+  return (p.stages >= 2 && p.stages < C::STAGES) ? p.stages : C::STAGES;
 }
 
 // ------------------------------------------------------------------ producer
-template <int D, int T, int GRP, typename E, int HP>
+// C: the kernel's configuration (tile tokens T, head dim DIM, kv heads per
+// unit HPU, tensor-core boxes TC / W / NB, TILE_ELEMS and STAGES).
+template <class C, typename E>
 __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, int g,
                                         E* kv, uint64_t* full, uint64_t* empty, volatile int* abort_flag) {
   // Run by the whole producer warp. Lane 0 posts byte counts and issues the
@@ -359,7 +364,7 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
   // (token-major and paged caches only) loads the HP heads of each token
   // row together: HP * d contiguous elements per row, kept interleaved in
   // shared memory (tile row = token * HP + head).
-  using C = Cfg<D, T, GRP, HP>;
+  constexpr int D = C::DIM, HP = C::HPU;
   const int lane = threadIdx.x & 31;
   const bool leader = lane == 0;
   const uint64_t pol = l2_evict_first_policy();
@@ -369,7 +374,7 @@ __device__ __forceinline__ void produce(const KParams& p, const CUtensorMap* tmk
     prefetch_tmap(tmv);
   }
   const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
-  const int ns = ring_stages<D, T, GRP, HP>(p);
+  const int ns = ring_stages<C>(p);
   int stage = 0;
   uint32_t phase = 1;  // a fresh barrier counts its previous (odd) phase as complete
   long long issued = 0;
@@ -612,7 +617,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == ring_stages<D, T, GRP, HP>(p)) {
+    if (++stage == ring_stages<C>(p)) {
       stage = 0;
       phase ^= 1u;
     }
@@ -818,7 +823,7 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == ring_stages<D, T, GRP, HP>(p)) {
+    if (++stage == ring_stages<C>(p)) {
       stage = 0;
       phase ^= 1u;
     }
@@ -1138,7 +1143,7 @@ __global__ void __launch_bounds__(Cfg<D, T, GRP, HP>::NTHREADS, 1)
   const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr[kEpoch]);
 
   if ((tid >> 5) == C::NCW) {
-    produce<D, T, GRP, E, HP>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
+    produce<C, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
   } else {
     consume<D, T, GRP, E, HP>(p, g, kv, full, empty, mrg, flags_smem, epoch);
   }

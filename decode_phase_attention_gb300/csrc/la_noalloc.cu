@@ -137,7 +137,8 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   p.grp = s->unit_grp();
   p.nq = s->nq;
   p.rows = s->unit_grp() * s->nq;
-  p.stages = s->stages > 0 ? s->stages : (s->kind == 0 ? la::stream_stages(s->d, s->T, s->hp, la::kKvSlab) : 0);
+  p.stages = s->stages > 0 ? s->stages
+                           : (s->kind == 0 && s->R <= 16 ? la::stream_stages(s->d, s->T, s->hp, la::kKvSlab) : 0);
   cudaError_t ce = la::launch_decode(s->d, s->T, s->R, 1, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {

@@ -1,0 +1,780 @@
+// la_wide.cuh -- the stream-K decode kernel for units of up to 128 query
+// rows (multi-query attention, wide query-head groups, a group times many
+// query tokens) on the 5th-generation tensor cores.
+//
+// With a whole query-head group in one unit, a LeanTile ("3.3 LeanTile" of
+// the xllm-io review: S_f = Q K^T, the running max m and sum l, O_acc =
+// P V + diag(rescale) O_acc) is a real matrix product: 128 query rows
+// against T = 128 tokens, up to 128 flop per K/V byte. The 16-row kernel's
+// mma.sync path cannot keep up with HBM there, so this kernel puts both
+// products on tcgen05 with the accumulators in tensor memory (TMEM):
+//
+//   S = Q K^T    M = 128 query rows (spare rows are zero queries), N = T
+//                tokens, K = d. A = Q in TMEM (written once per segment),
+//                B = the K tile as the TMA ring holds it (K-major, 128-byte
+//                swizzle).
+//   O += P V     M = 128 rows, N = d, K = T. A = P in TMEM, B = the V tile
+//                (d-major, i.e. MN-major, 128-byte swizzle).
+//
+// Warps: 0-15 the softmax warps (a TMEM lane quadrant -- 32 query rows --
+// is reachable only from one SM sub-partition, so four warps share each
+// quadrant, one quarter of the tile's tokens and of the head dims each);
+// 16 the TMA producer (the 16-row kernel's producer warp, unchanged); 17
+// the MMA warp (TMEM allocation, one thread issues every tcgen05.mma).
+//
+// TMEM (512 columns): NSB S buffers of 128 columns (3 at d = 64, 2 at
+// d = 128), then O (d columns), then Q (d / 2 columns: two 16-bit values
+// per column). The softmax of tile j reads S_j (buffer j % NSB), then
+// writes P_j over it as a bf16/fp16 high part (columns +0..63) and low part
+// (+64..127), so that P V keeps fp32-level accuracy (as in the 16-row
+// kernel). S of the next tile is computed into another buffer while the
+// softmax runs; it waits only for the P V that last used that buffer.
+// Keeping Q in TMEM leaves shared memory to the K/V ring (3 stages of
+// 64 KiB at d = 128, 6 of 32 KiB at d = 64). O accumulates over a segment's tiles in TMEM; a row's reference
+// maximum moves only when a tile's maximum exceeds it by more than 2^8
+// (p values stay below 256), and only then is that row of O rescaled.
+//
+// Everything else -- schedule, segments, ready flags with epochs, the
+// partial records (m, l, O per row), the host's merge with f, bounded
+// waits and the abort protocol -- is the 16-row kernel's.
+#pragma once
+
+#include "la_kernel.cuh"
+
+namespace la {
+
+// ---------------------------------------------------------- tcgen05 wrappers
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {  // whole warp
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrive once on `bar` when every tcgen05.mma this thread issued so far is done.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// The warp's 32 lanes x 16 consecutive 32-bit columns: thread i gets lane
+// (lane field of taddr) + i. Results are valid after tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// Registers written by tcgen05.ld are read only after the wait: tie them to
+// it so that the compiler cannot move a use above the wait.
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t* r) {
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+// Generic-proxy writes to shared memory become visible to the tensor
+// cores and TMA (the async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// The 16 softmax warps (named barrier 1).
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+// Four consecutive outputs (idx a multiple of 4) as fp32, fp16 or bf16.
+__device__ __forceinline__ void store_out4(void* out, size_t idx, float a, float b, float c, float d,
+                                           int out_dtype) {
+  if (out_dtype == 0) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = make_float4(a, b, c, d);
+  } else if (out_dtype == 1) {
+    __half2 x = __floats2half2_rn(a, b), y = __floats2half2_rn(c, d);
+    *reinterpret_cast<uint2*>(static_cast<__half*>(out) + idx) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&x), *reinterpret_cast<uint32_t*>(&y));
+  } else {
+    __nv_bfloat162 x = __floats2bfloat162_rn(a, b), y = __floats2bfloat162_rn(c, d);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + idx) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&x), *reinterpret_cast<uint32_t*>(&y));
+  }
+}
+
+// Shared-memory matrix descriptor of a tcgen05 operand in the 128-byte
+// swizzle layout (rows of 128 bytes, 8-row atoms of 1024 bytes, atoms
+// 1024-byte aligned): start address, leading and stride byte offsets,
+// the fixed version field and the swizzle mode.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of a dense kind::f16 MMA with fp32 accumulation:
+// operand format (0 fp16, 1 bf16) for A and B, B MN-major or K-major, N, M.
+template <typename E>
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((Elem<E>::kBf16 ? 1u : 0u) << 7) | ((Elem<E>::kBf16 ? 1u : 0u) << 10) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------ configuration
+template <int D>
+struct WCfg {
+  static constexpr int DIM = D;
+  static constexpr int HPU = 1;
+  static constexpr int M = 128;                 // query rows of a unit (MMA M; TMEM lanes)
+  static constexpr int T = 128;                 // LeanTile tokens (MMA N of S, K of P V)
+  static constexpr int ROWS = T;
+  static constexpr bool TC = true;              // the producer's swizzled TMA boxes
+  static constexpr int W = 64;                  // box columns: 128-byte rows
+  static constexpr int NB = D / W;              // boxes per tile per tensor
+  static constexpr int TILE_ELEMS = T * D;
+  static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
+  static constexpr int BOX_BYTES = T * 128;     // one box of a K or V tile
+  static constexpr int REC = D + 2;
+  static constexpr int RS = record_stride(D, M);
+  static constexpr int NSW = 16;                // softmax warps: 4 per TMEM lane quadrant
+  static constexpr int RED_BYTES = 3 * 4 * M * 4;  // quarter maxima (two tiles) and quarter sums of l
+  static constexpr int NSB = D == 64 ? 3 : 2;   // S / P buffers in TMEM
+  static constexpr int NBARS = 2 * 6 + 3 * NSB + 3;  // full, empty (<= 6 stages), s_full, p_full, pv_done, q_ready, drain, stg
+  static constexpr int STAGES = cmin(6, (232448 - RED_BYTES - 1024 - 256) / STAGE_BYTES);
+  static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
+  // + exchange area, barriers, TMEM slot, flags; alignment slack
+  static constexpr size_t SMEM = KV_BYTES + RED_BYTES + 256 + 1024;
+  static constexpr int NTHREADS = NSW * 32 + 64;  // softmax warps, producer warp, MMA warp
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t O_COL = NSB * T;    // S / P buffers first, then O
+  static constexpr uint32_t Q_COL = O_COL + D;  // then Q
+  static_assert(D == 64 || D == 128, "head dims of the wide kernel");
+  static_assert(STAGES >= 2 && SMEM <= 232448, "shared memory per CTA");
+  static_assert(NBARS * 8 + 16 <= 256, "barrier area");
+  static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor memory columns");
+};
+
+
+// One thread's bounded wait; a wait that runs out records LA_ERR_TIMEOUT and
+// raises the CTA's abort flag.
+__device__ __forceinline__ bool wide_wait(const KParams& p, int g, uint64_t* bar, uint32_t parity,
+                                          volatile int* abort_flag) {
+  if (mbar_wait_bounded(bar, parity, abort_flag, p.spin_ns)) return true;
+  if (!*abort_flag) record_error(p.hdr, kStatusTimeout, g, -1);
+  *abort_flag = 1;
+  return false;
+}
+// The same for a whole warp (the result is the same in every lane).
+__device__ __forceinline__ bool wide_wait_warp(const KParams& p, int g, uint64_t* bar, uint32_t parity,
+                                               volatile int* abort_flag) {
+  bool ok = mbar_wait_bounded(bar, parity, abort_flag, p.spin_ns);
+  ok = __all_sync(kFull, ok);
+  if (!ok && (threadIdx.x & 31) == 0) {
+    if (!*abort_flag) record_error(p.hdr, kStatusTimeout, g, -1);
+    *abort_flag = 1;
+  }
+  return ok;
+}
+
+// ------------------------------------------------------------------ MMA warp
+// One thread issues, for tile j of the CTA (segment by segment):
+//   S_j = Q K_j^T into S buffer j % NSB, committed to s_full[j % NSB];
+//   after the softmax has written P_j (p_full[j % NSB]): O (+)= P_j V_j,
+//   committed to pv_done[j % NSB] and to the ring stage's empty barrier.
+// S_{j+1} is issued before waiting for P_j, so the tensor cores compute the
+// next scores while the softmax runs; S buffer (j+1) % NSB holds
+// P_{j+1-NSB}, so that P V must be done first. Each buffer has its own
+// barriers, so no wait is ever two phases behind its barrier.
+template <int D, typename E>
+__device__ __forceinline__ void wide_mma(const KParams& p, int g, const E* kv,
+                                         uint64_t* full, uint64_t* empty, uint64_t* s_full, uint64_t* p_full,
+                                         uint64_t* pv_done, uint64_t* q_ready, uint64_t* drain, uint32_t tmem,
+                                         volatile int* abort_flag) {
+  using C = WCfg<D>;
+  constexpr uint32_t kIdS = idesc_f16<E>(C::M, C::T, false);  // A = Q, B = K tile: both K-major
+  constexpr uint32_t kIdO = idesc_f16<E>(C::M, D, true);      // A = P (TMEM), B = V tile: MN-major
+  const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
+  const int ns = ring_stages<C>(p);
+  const uint32_t kv0 = smem_u32(kv);
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t j = 0;  // tiles of this CTA issued so far
+  bool alive = true;
+
+  auto issue_s = [&](uint32_t jj, int stg) {
+    const uint32_t kb = kv0 + (uint32_t)stg * C::STAGE_BYTES;
+    const uint32_t ds = tmem + (jj % C::NSB) * (uint32_t)C::T;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      // 16 head dims per MMA: Q columns 8 kk .. (two dims per column); the K
+      // tile's box kk / 4, 32 bytes into its swizzled rows
+      const uint32_t ka = kb + (uint32_t)(kk >> 2) * C::BOX_BYTES + (uint32_t)(kk & 3) * 32u;
+      mma_ts(ds, tmem + C::Q_COL + 8u * (uint32_t)kk, sdesc_sw128(ka, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+    }
+    tc_commit(&s_full[jj % C::NSB]);
+  };
+
+  for (int si = s_begin, seg = 0; si < s_end && alive; ++si, ++seg) {
+    const int4 w0 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords);
+    const int n_tiles = w0.z - w0.y;
+    // the segment's Q rows are in shared memory and the previous segment's
+    // O has been read (every MMA before this point is done)
+    if (!wide_wait(p, g, q_ready, (uint32_t)seg & 1u, abort_flag)) break;
+    if (!wide_wait(p, g, &full[stage], phase, abort_flag)) break;
+    tc_fence_after();
+    issue_s(j, stage);
+    for (int t = 0; t < n_tiles; ++t) {
+      const int cur = stage;
+      if (++stage == ns) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (t + 1 < n_tiles) {
+        if (!wide_wait(p, g, &full[stage], phase, abort_flag) ||
+            (j + 1u >= (uint32_t)C::NSB &&
+             !wide_wait(p, g, &pv_done[(j + 1u - C::NSB) % C::NSB], ((j + 1u - C::NSB) / C::NSB) & 1u,
+                        abort_flag))) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(j + 1u, stage);
+      }
+      if (!wide_wait(p, g, &p_full[j % C::NSB], (j / C::NSB) & 1u, abort_flag)) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      // O (+)= P_j V_j: 16 tokens per MMA, the high and the low part of P
+      const uint32_t vb = kv0 + (uint32_t)cur * C::STAGE_BYTES + (uint32_t)C::TILE_ELEMS * 2u;
+      const uint32_t pc = tmem + (j % C::NSB) * (uint32_t)C::T;
+#pragma unroll
+      for (int kk = 0; kk < C::T / 16; ++kk) {
+        // LBO: the next 64 head dims (next box); SBO: the next 8 tokens
+        const uint64_t vd = sdesc_sw128(vb + (uint32_t)kk * 2048u, C::BOX_BYTES, 1024);
+        mma_ts(tmem + C::O_COL, pc + 8u * (uint32_t)kk, vd, kIdO, (t > 0 || kk > 0) ? 1u : 0u);
+        mma_ts(tmem + C::O_COL, pc + 64u + 8u * (uint32_t)kk, vd, kIdO, 1u);
+      }
+      tc_commit(&pv_done[j % C::NSB]);
+      tc_commit(&empty[cur]);
+      ++j;
+    }
+  }
+  // Leave no MMA in flight: TMEM is freed after the CTA's last barrier.
+  tc_commit(drain);
+  volatile int no_abort = 0;
+  mbar_wait_bounded(drain, 0, &no_abort, p.spin_ns);
+}
+
+
+// --------------------------------------------------------- softmax warps
+// Warp w (0..15) works on TMEM lane quadrant w % 4 (the lanes its SM
+// sub-partition reaches): thread (w, lane) owns row r = 32 (w % 4) + lane
+// and quarter cq = w / 4 of every S tile (tokens 32 cq .. 32 cq + 31) and
+// of O (head dims D/4 cq ..). Per segment: write the unit's Q rows to
+// TMEM; per tile: read the quarter row of S, mask and scale it,
+// exchange the quarter maxima of each row through shared memory, move the
+// reference maximum if the tile's maximum exceeds it by more than 8 (base-2
+// units), write P = 2^(s - m) as high and low 16-bit parts over S, update
+// the quarter sum of l; at the end: add the four quarter sums, read the O
+// quarter and write the record, or merge the peers' records with f and
+// store O / l. Every softmax thread passes the same named barriers, also
+// after an abort (the waits are skipped then, not the barriers).
+template <int D, typename E>
+__device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, float* red,
+                                             uint64_t* full, uint64_t* s_full, uint64_t* p_full,
+                                             uint64_t* pv_done, uint64_t* q_ready, uint64_t* stg,
+                                             uint32_t tmem, volatile int* abort_flag, uint32_t epoch) {
+  volatile int* flags_smem_copies = abort_flag + 1;  // staging copies issued in this batch
+  using C = WCfg<D>;
+  constexpr int T = C::T;
+  constexpr int OQ = D / 4;  // head dims of O per thread
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qd = warp & 3, cq = warp >> 2;
+  const int r = qd * 32 + lane;
+  const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);  // this warp's 32 lanes
+  const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
+  const uint32_t ready = epoch + 1u;
+  const int ns = ring_stages<C>(p);
+  float* lsum = red + 2 * 4 * C::M;  // [4][M] quarter sums of l
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t j = 0;  // tiles of this CTA consumed so far
+  unsigned long long* tr = (p.trace != nullptr && tid == 0) ? p.trace + (size_t)g * kTraceWords : nullptr;
+
+  for (int si = s_begin; si < s_end; ++si) {
+    const int4 w0 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords);
+    const int4 w1 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 4);
+    const int unit = w0.x, t0 = w0.y, t1 = w0.z, kind = w0.w, peer = w1.x;
+    const int b = unit / p.hkv, kvh = unit % p.hkv;
+    const bool ok = unit_offsets_ok(p, b);
+    if (!ok && tid == 0) record_error(p.hdr, kStatusInvalid, g, unit);
+    const long long L = w1.y;
+    const int n_tiles = t1 - t0;
+    const bool live = r < p.rows;
+    const bool warp_live = qd * 32 < p.rows;  // warp-uniform
+    // keys row r may see in the request: its query token sits at position
+    // L - nq + r / grp
+    const long long lim = live ? L - (p.nq - 1 - r / p.grp) : 0;
+
+    // ---- the unit's Q rows into TMEM (the A operand of S = Q K^T): this
+    // thread's quarter of row r, two 16-bit values per column; spare rows
+    // are zero
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) +
+                                                        row_index(p, b, kvh, live ? r : 0) * D + (D / 4) * cq);
+      uint32_t qw[D / 8];
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) {
+        const uint4 v = live ? src[k] : make_uint4(0u, 0u, 0u, 0u);
+        qw[4 * k] = v.x;
+        qw[4 * k + 1] = v.y;
+        qw[4 * k + 2] = v.z;
+        qw[4 * k + 3] = v.w;
+      }
+      if constexpr (D / 8 == 16)
+        tmem_st16(trow + C::Q_COL + 16u * cq, qw);
+      else
+        tmem_st8(trow + C::Q_COL + 8u * cq, qw);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(q_ready);
+
+    float m_use = -INFINITY, lq = 0.f;
+    bool alive = __all_sync(kFull, *abort_flag == 0);  // warp-uniform: TMEM accesses are warp-wide
+    for (int t = 0; t < n_tiles; ++t) {
+      if (alive) alive = wide_wait_warp(p, g, &s_full[j % C::NSB], (j / C::NSB) & 1u, abort_flag);
+      tc_fence_after();
+      if (tr != nullptr) {
+        if (tr[kTrFirstTile] == 0ull) tr[kTrFirstTile] = global_ns();
+        tr[kTrTiles] += 1ull;
+      }
+      const uint32_t sc = trow + (j % C::NSB) * (uint32_t)T;
+      const int tt = t0 + t;
+      const bool work = alive && warp_live;
+      uint32_t u[32];
+      float mq = -INFINITY;
+      float xs = 1.f;  // u holds scores to multiply by xs: raw (xs = qscale) or already scaled (1)
+      if (work) {
+        tmem_ld16(sc + 32u * cq, u);
+        tmem_ld16(sc + 32u * cq + 16u, u + 16);
+        tmem_wait_ld_regs<32>(u);
+        // visible tokens of this quarter
+        const long long lv = lim - (long long)tt * T - 32 * cq;
+        const int vis = lv < 0 ? 0 : (lv > 32 ? 32 : (int)lv);
+        if (vis == 32 && p.qscale > 0.f) {
+          // the whole quarter is visible: the maximum of the raw scores,
+          // scaled once (rounding is monotonic)
+          float m0 = __uint_as_float(u[0]), m1 = __uint_as_float(u[1]);
+#pragma unroll
+          for (int i = 2; i < 32; i += 2) {
+            m0 = fmaxf(m0, __uint_as_float(u[i]));
+            m1 = fmaxf(m1, __uint_as_float(u[i + 1]));
+          }
+          mq = fmaxf(m0, m1) * p.qscale;
+          xs = p.qscale;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = i < vis ? __uint_as_float(u[i]) * p.qscale : -INFINITY;
+            u[i] = __float_as_uint(x);
+            mq = fmaxf(mq, x);
+          }
+        }
+        red[(j & 1u) * 4 * C::M + cq * C::M + r] = mq;
+      }
+      softmax_sync();  // the four quarter maxima of every row are in shared memory
+      float alpha = 1.f;
+      bool resc = false;
+      if (work) {
+        const float* rm = red + (j & 1u) * 4 * C::M + r;
+        const float mt = fmaxf(fmaxf(rm[0], rm[C::M]), fmaxf(rm[2 * C::M], rm[3 * C::M]));
+        if (mt > m_use + 8.f) {  // move the reference maximum (always on a row's first visible tile)
+          alpha = (m_use == -INFINITY) ? 0.f : ex2(m_use - mt);
+          m_use = mt;
+          lq *= alpha;
+          resc = true;
+        }
+        const float nref = (m_use == -INFINITY) ? 0.f : -m_use;
+        uint32_t hi[16], lo[16];
+        float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          // p = 2^(s - m); masked scores are -inf and give 0
+          const float p0 = ex2(fmaf(__uint_as_float(u[2 * k]), xs, nref));
+          const float p1 = ex2(fmaf(__uint_as_float(u[2 * k + 1]), xs, nref));
+          ls0 += p0;
+          ls1 += p1;
+          if constexpr (Elem<E>::kBf16) {
+            // high part: p truncated to bf16 (its upper 16 bits); low part:
+            // the exact remainder, rounded to bf16
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            hi[k] = __byte_perm(b0, b1, 0x7632);
+            lo[k] = Elem<E>::pack(p0 - __uint_as_float(b0 & 0xffff0000u), p1 - __uint_as_float(b1 & 0xffff0000u));
+          } else {
+            hi[k] = Elem<E>::pack(p0, p1);
+            const float2 h = Elem<E>::unpack(hi[k]);
+            lo[k] = Elem<E>::pack(p0 - h.x, p1 - h.y);
+          }
+        }
+        tmem_st16(sc + 16u * cq, hi);        // tokens 32 cq .. 32 cq + 31: high parts
+        tmem_st16(sc + 64u + 16u * cq, lo);  // and low parts
+        lq += ls0 + ls1;
+      }
+      // V rows past the context: zero them, so that 0 * (whatever a cache
+      // holds there) adds nothing to O
+      const long long rem = L - (long long)tt * T;
+      if (rem < T && alive) {
+        if (mbar_wait_bounded(&full[stage], phase, abort_flag, p.spin_ns)) {  // already complete
+          const int ntok = (int)rem;
+          unsigned char* vt = reinterpret_cast<unsigned char*>(kv) + (size_t)stage * C::STAGE_BYTES +
+                              (size_t)C::TILE_ELEMS * 2;
+          const int n16 = (T - ntok) * 8;  // 16-byte pieces past the context in one box
+          for (int i = tid; i < n16 * C::NB; i += C::NSW * 32)
+            *reinterpret_cast<uint4*>(vt + (i / n16) * C::BOX_BYTES + ntok * 128 + (i % n16) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+        }
+      }
+      // a row whose reference maximum moved rescales its O quarter, once the
+      // previous tile's P V is in it
+      if (work && __any_sync(kFull, resc && t > 0)) {
+        if (wide_wait_warp(p, g, &pv_done[(j - 1u) % C::NSB], ((j - 1u) / C::NSB) & 1u, abort_flag)) {
+          tc_fence_after();
+          const float a = (resc && t > 0) ? alpha : 1.f;
+#pragma unroll
+          for (int c = 0; c < OQ / 16; ++c) {
+            uint32_t o[16];
+            const uint32_t oc = trow + C::O_COL + (uint32_t)(OQ * cq + 16 * c);
+            tmem_ld16(oc, o);
+            tmem_wait_ld_regs<16>(o);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * a);
+            tmem_st16(oc, o);
+          }
+        } else {
+          alive = false;
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[j % C::NSB]);
+      if (++stage == ns) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      ++j;
+    }
+    if (tr != nullptr) {
+      tr[kTrTilesDone] = global_ns();
+      tr[kTrSegs] += 1ull;
+    }
+
+    // ---- the segment's O quarter (after its last P V) and the row sum l
+    const bool have_o =
+        alive && wide_wait_warp(p, g, &pv_done[(j - 1u) % C::NSB], ((j - 1u) / C::NSB) & 1u, abort_flag);
+    tc_fence_after();
+    float o[OQ];
+#pragma unroll
+    for (int c = 0; c < OQ; ++c) o[c] = 0.f;
+    if (have_o && warp_live) {
+#pragma unroll
+      for (int c = 0; c < OQ / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(trow + C::O_COL + (uint32_t)(OQ * cq + 16 * c), v);
+        tmem_wait_ld_regs<16>(v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) o[16 * c + k] = __uint_as_float(v[k]);
+      }
+    }
+    tc_fence_before();
+    lsum[cq * C::M + r] = lq;
+    softmax_sync();  // every warp's waits are over; the quarter sums are in shared memory
+    const float l = (lsum[r] + lsum[C::M + r]) + (lsum[2 * C::M + r] + lsum[3 * C::M + r]);
+    const bool poisoned = (*abort_flag != 0) || !ok || !have_o;
+
+    // Records are column-major over the unit's rows (wide_rec): element
+    // (col, r) at [col * rows + r], col 0 = m, 1 = l, 2 + c = O dim c, so
+    // that a warp's 32 rows read and write whole 128-byte lines.
+    const int rows = p.rows;
+    if (kind == kNonHost || kind == kPartial) {
+      if (live) {
+        float* rec = p.recs + (size_t)g * C::RS;
+        if (cq == 0) {
+          rec[r] = poisoned ? __int_as_float(0x7fc00000) : m_use;
+          rec[rows + r] = l;
+        }
+#pragma unroll
+        for (int c = 0; c < OQ; ++c) rec[(size_t)(2 + OQ * cq + c) * rows + r] = o[c];
+      }
+      __threadfence();
+      softmax_sync();
+      if (kind == kNonHost && tid == 0 && g != p.skip_signal) st_release_gpu(&p.flags[g], ready);
+    } else {
+      bool fail = poisoned;
+      float Ls = l;
+      if (kind == kHost) {
+        // every later CTA of the unit: thread i spins (bounded) on the ready
+        // flags of peers i, i + 512, ...
+        const int npeer = peer - g;
+        const uint64_t twait = global_ns();
+        for (int i = tid; i < npeer; i += C::NSW * 32) {
+          const int g2 = g + 1 + i;
+          const uint64_t tstart = global_ns();
+          for (uint32_t it = 0; !*abort_flag; ++it) {
+            if (ld_acquire_gpu(&p.flags[g2]) == ready) break;
+            if ((it & 15u) == 15u) {
+              if ((long long)(global_ns() - tstart) > p.spin_ns) {
+                record_error(p.hdr, kStatusTimeout, g, g2);
+                *abort_flag = 1;
+                break;
+              }
+              __nanosleep(100);
+            }
+          }
+        }
+        softmax_sync();  // every flag seen (or the abort raised) before any record is read
+        if (tr != nullptr) tr[kTrWaitNs] += global_ns() - twait;
+        // The host segment is the CTA's last: every tile has been consumed
+        // and the producer issues no more copies, so the ring is idle. The
+        // peers' records come into it by bulk copies, as many at a time as
+        // fit, and are merged with f one after another (the running
+        // maximum M, then the rescaled sums of l and of this thread's O
+        // quarter).
+        const uint32_t rec_bytes = ((uint32_t)rows * (D + 2) * 4u + 15u) & ~15u;
+        const int cap = (int)(C::KV_BYTES / rec_bytes);
+        float M = m_use;
+        uint32_t sph = 0;
+        for (int p0 = 0; p0 < npeer; p0 += cap) {
+          const int nb = npeer - p0 < cap ? npeer - p0 : cap;
+          if (tid == 0 && !*abort_flag) {
+            mbar_arrive_expect_tx(stg, (uint32_t)nb * rec_bytes);
+            for (int k = 0; k < nb; ++k)
+              bulk_g2s(reinterpret_cast<unsigned char*>(kv) + (size_t)k * rec_bytes,
+                       p.recs + (size_t)(g + 1 + p0 + k) * C::RS, rec_bytes, stg, l2_evict_first_policy());
+            flags_smem_copies[0] = 1;  // copies in flight: wait for them even after an abort
+          }
+          softmax_sync();
+          const bool issued = flags_smem_copies[0] != 0;
+          volatile int no_abort = 0;
+          const bool got = issued && mbar_wait_bounded(stg, sph, &no_abort, p.spin_ns);
+          sph ^= issued ? 1u : 0u;
+          if (issued && !got) fail = true;
+          if (got && live && !*abort_flag) {
+            for (int k = 0; k < nb; ++k) {
+              const float* rk = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(kv) +
+                                                               (size_t)k * rec_bytes);
+              const float mk = rk[r];
+              const float mn = fmaxf(M, mk);
+              if (mn == -INFINITY) continue;
+              const float a = (M == -INFINITY) ? 0.f : ex2(M - mn);
+              const float wt = (mk == -INFINITY) ? 0.f : ex2(mk - mn);  // NaN m (poisoned) propagates
+              Ls = a * Ls + wt * rk[rows + r];
+#pragma unroll
+              for (int c = 0; c < OQ; ++c) o[c] = a * o[c] + wt * rk[(2 + OQ * cq + c) * rows + r];
+              M = mn;
+            }
+          }
+          softmax_sync();  // the staging area is rewritten by the next batch
+          if (tid == 0) flags_smem_copies[0] = 0;
+        }
+        if (*abort_flag) fail = true;
+      }
+      // normalise and store: O = Obar / l
+      if (live) {
+        const size_t base = row_index(p, b, kvh, r) * D + OQ * cq;
+        const float inv = 1.f / Ls;
+#pragma unroll
+        for (int c = 0; c < OQ; c += 4)
+          store_out4(p.out, base + c, fail ? __int_as_float(0x7fc00000) : o[c] * inv,
+                     fail ? __int_as_float(0x7fc00000) : o[c + 1] * inv,
+                     fail ? __int_as_float(0x7fc00000) : o[c + 2] * inv,
+                     fail ? __int_as_float(0x7fc00000) : o[c + 3] * inv, p.out_dtype);
+      }
+    }
+    softmax_sync();  // the quarter sums are rewritten by the next segment
+  }
+}
+
+// -------------------------------------------------------------------- kernel
+template <int D, typename E>
+__global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
+    lean_wide_kernel(const KParams p, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv) {
+  using C = WCfg<D>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  E* kv = reinterpret_cast<E*>(smem);
+  float* red = reinterpret_cast<float*>(smem + C::KV_BYTES);  // [2][4][M] quarter maxima, [4][M] quarter sums
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::KV_BYTES + C::RED_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* s_full = empty + C::STAGES;
+  uint64_t* p_full = s_full + C::NSB;
+  uint64_t* pv_done = p_full + C::NSB;
+  uint64_t* q_ready = pv_done + C::NSB;
+  uint64_t* drain = q_ready + 1;
+  uint64_t* stg = drain + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(stg + 1);
+  volatile int* flags_smem = reinterpret_cast<volatile int*>(tslot + 2);  // [0] abort, [1] staging copies issued
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int g = blockIdx.x;
+  if (tid == 0) {
+    if (p.trace != nullptr) {
+      unsigned long long* tr = p.trace + (size_t)g * kTraceWords;
+      uint32_t sm;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+      tr[kTrSm] = sm;
+      tr[kTrStart] = global_ns();
+      for (int w = 2; w < kTraceWords; ++w) tr[w] = 0ull;
+    }
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);  // one tcgen05.commit per tile
+    }
+    for (int b2 = 0; b2 < C::NSB; ++b2) {
+      mbar_init(&s_full[b2], 1);
+      mbar_init(&p_full[b2], C::NSW * 32);
+      mbar_init(&pv_done[b2], 1);
+    }
+    mbar_init(q_ready, C::NSW * 32);
+    mbar_init(drain, 1);
+    mbar_init(stg, 1);
+    flags_smem[0] = 0;
+    flags_smem[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::NSW + 1) {
+    tmem_alloc(tslot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tslot);
+  const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr[kEpoch]);
+
+  if (warp < C::NSW) {
+    wide_softmax<D, E>(p, g, kv, red, full, s_full, p_full, pv_done, q_ready, stg, tmem, flags_smem, epoch);
+  } else if (warp == C::NSW) {
+    produce<C, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
+  } else if ((tid & 31) == 0) {
+    wide_mma<D, E>(p, g, kv, full, empty, s_full, p_full, pv_done, q_ready, drain, tmem, flags_smem);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == C::NSW + 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (tid == 0) {
+    if (p.trace != nullptr) p.trace[(size_t)g * kTraceWords + kTrEnd] = global_ns();
+    // The last CTA to finish advances the epoch (as in the 16-row kernel).
+    __threadfence();
+    const uint32_t prev = atomicAdd(&p.hdr[kDone], 1u);
+    if (prev == (uint32_t)p.G - 1u) {
+      p.hdr[kDone] = 0u;
+      __threadfence();
+      p.hdr[kEpoch] = epoch + 1u;
+    }
+  }
+}
+
+// Fixed-split merge of the wide kernel's records (column-major over the
+// unit's rows): one block per (unit, query row), one thread per dimension.
+template <int D>
+__global__ void __launch_bounds__(D) lean_wide_combine_kernel(const CParams p) {
+  using C = WCfg<D>;
+  const int unit = blockIdx.x / C::M, j = blockIdx.x % C::M;
+  const int c = threadIdx.x;
+  const int rows = p.rows;
+  if (j >= rows) return;
+  const int h0 = p.unit_host[unit], h1 = p.unit_fin[unit];
+  if (h0 == h1) return;  // a whole unit was written by the decode kernel
+  float M = -INFINITY, Ls = 0.f, O = 0.f;
+  for (int s2 = h0; s2 <= h1; ++s2) {
+    const float* r = p.recs + (size_t)s2 * C::RS;
+    const float m2 = r[j], l2 = r[rows + j], o2 = r[(size_t)(2 + c) * rows + j];
+    const float mn = fmaxf(M, m2);
+    if (mn == -INFINITY) continue;
+    const float a = (M == -INFINITY) ? 0.f : ex2(M - mn);
+    const float bw = (m2 == -INFINITY) ? 0.f : ex2(m2 - mn);
+    Ls = a * Ls + bw * l2;
+    O = a * O + bw * o2;
+    M = mn;
+  }
+  const int b = unit / p.hkv, kvh = unit % p.hkv;
+  store_out(p.out, row_index(p, b, kvh, j) * D + c, O / Ls, p.out_dtype);
+}
+
+// ------------------------------------------------------------ host launchers
+template <int D, typename E>
+cudaError_t launch_wide_t(const KParams& p, cudaStream_t st) {
+  using C = WCfg<D>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(lean_wide_kernel<D, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  if (p.G <= 0) return cudaSuccess;
+  CUtensorMap mk, mv;
+  if (p.kv_layout != kKvSlab)
+    e = encode_kv_maps_3d(p.k, p.v, p.kv_rows, p.kv_heads, D, C::W, 1, p.box_rows, true, (int)Elem<E>::kTmaType,
+                          &mk, &mv);
+  else
+    e = encode_kv_maps(p.k, p.v, p.kv_rows, D, C::T, C::W, (int)Elem<E>::kTmaType, &mk, &mv);
+  if (e != cudaSuccess) return e;
+  lean_wide_kernel<D, E><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_wide_combine_t(const CParams& p, cudaStream_t st) {
+  if (p.U <= 0) return cudaSuccess;
+  lean_wide_combine_kernel<D><<<p.U * WCfg<D>::M, D, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t wide_capacity_t(int* per_sm) {
+  using C = WCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(lean_wide_kernel<D, __nv_bfloat16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lean_wide_kernel<D, __nv_bfloat16>, C::NTHREADS,
+                                                       C::SMEM);
+}
+
+}  // namespace la

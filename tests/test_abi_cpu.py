@@ -242,7 +242,7 @@ def test_spec_schedule_matches_the_decode_plan_and_sizes_its_records():
 
 
 @pytest.mark.parametrize("hq,hkv,nq,lengths,status", [
-    (4, 4, 17, [100, 200], la.LA_ERR_UNSUPPORTED),  # 17 query tokens: more rows than an instance holds
+    (4, 4, 129, [200, 300], la.LA_ERR_UNSUPPORTED),  # 129 query tokens: more rows than a unit holds
     (4, 4, 5, [100, 4], la.LA_ERR_INVALID),          # a context shorter than its query tokens
     (4, 4, 0, [100, 200], la.LA_ERR_INVALID),
 ])
@@ -314,7 +314,7 @@ def test_two_head_records_hold_both_heads():
     (dict(hkv=4, hq=8, heads_per_unit=2, d=128), la.LA_ERR_UNSUPPORTED),   # rows already 256 bytes: not built
     (dict(hkv=4, hq=8, heads_per_unit=2, tile_tokens=256), la.LA_ERR_UNSUPPORTED),
     (dict(hkv=4, hq=8, tile_tokens=-1), la.LA_ERR_INVALID),
-    (dict(hkv=2, hq=4, nq=17), la.LA_ERR_UNSUPPORTED),            # 17 query tokens per request
+    (dict(hkv=2, hq=4, nq=129, cu=[0, 200, 400]), la.LA_ERR_UNSUPPORTED),  # 129 query tokens per request
     (dict(hkv=2, hq=64, heads_per_unit=2), la.LA_ERR_UNSUPPORTED),  # query blocks: one kv head per unit
     (dict(hkv=2, hq=16, nq=2, heads_per_unit=2), la.LA_ERR_UNSUPPORTED),  # 16 rows: one kv head per unit
 ])
@@ -371,45 +371,67 @@ def test_groups_that_are_not_powers_of_two(grp):
     assert la.la_workspace_size(s) == 256 + 256 + 11 * R * 130 * 4
 
 
-# ---- query blocks: more than 16 query rows per kv head
-# (group, query tokens) -> (query blocks per kv head, rows of one block's
-# instance): the fewest equal blocks of whole query heads whose rows fit 16.
+# ---- query blocks: more query rows per kv head than one unit holds
+# (d, group, query tokens) -> (query blocks per kv head, rows of one
+# block's instance). A unit holds 128 rows where the tcgen05 kernel is built
+# (d = 64, 128), else 16: the fewest equal blocks of whole query heads whose
+# rows fit.
 QUERY_BLOCKS = [
-    (32, 1, 2, 16), (24, 1, 2, 16), (17, 1, 17, 1), (18, 1, 2, 16), (34, 1, 17, 2), (40, 1, 4, 16),
-    (48, 1, 3, 16), (64, 1, 4, 16), (128, 1, 8, 16), (8, 3, 2, 16), (8, 4, 2, 16), (16, 2, 2, 16),
-    (4, 5, 2, 16), (1, 16, 1, 16), (2, 16, 2, 16),
+    (96, 32, 1, 2, 16), (96, 24, 1, 2, 16), (96, 17, 1, 17, 1), (96, 18, 1, 2, 16), (96, 34, 1, 17, 2),
+    (96, 40, 1, 4, 16), (96, 48, 1, 3, 16), (96, 64, 1, 4, 16), (96, 128, 1, 8, 16), (96, 8, 3, 2, 16),
+    (96, 8, 4, 2, 16), (96, 16, 2, 2, 16), (96, 4, 5, 2, 16), (96, 1, 16, 1, 16), (96, 2, 16, 2, 16),
+    (64, 32, 1, 1, 128), (64, 17, 1, 1, 128), (64, 128, 1, 1, 128), (64, 256, 1, 2, 128), (64, 192, 1, 2, 128),
+    (64, 8, 4, 1, 128), (64, 16, 9, 2, 128), (64, 1, 16, 1, 16), (64, 3, 7, 1, 128), (64, 2, 100, 2, 128),
+    (128, 16, 1, 1, 16), (128, 64, 1, 1, 128), (128, 130, 1, 2, 128),
 ]
 
 
-@pytest.mark.parametrize("grp,nq,qb,R", QUERY_BLOCKS)
-def test_query_blocks_are_units_of_their_own(grp, nq, qb, R):
-    # a kv head with more rows than an instance holds becomes qb units, one
-    # per block of grp / qb query heads: the schedule is the planner's over
+@pytest.mark.parametrize("d,grp,nq,qb,R", QUERY_BLOCKS)
+def test_query_blocks_are_units_of_their_own(d, grp, nq, qb, R):
+    # a kv head with more rows than a unit holds becomes qb units, one per
+    # block of grp / qb query heads: the schedule is the planner's over
     # hkv * qb heads of grp / qb query heads each
-    lengths = [700, 64, 3000]
-    hkv, d, G = 2, 64, 11
+    lengths = [700, 128, 3000]
+    hkv, G = 2, 11
+    T = 128 if (R == 128 or d != 64) else 256  # units of more than 16 rows: 128-token tiles
     s = la.la_plan_spec(3, hkv * grp, hkv, d, nq, cu_of(lengths), G)
     assert s.query_blocks == qb and s.heads_per_unit == 1
-    assert la.la_schedule_export(s) == P.export(P.plan_lean(3, hkv * grp, hkv * qb, d, cu_of(lengths),
-                                                            G, 256))
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(3, hkv * grp, hkv * qb, d, cu_of(lengths), G, T))
     rec = -(-R * (d + 2) // 4) * 4  # a record: R rows of (d + 2) floats, padded to 16 bytes
     assert la.la_workspace_size(s) == 256 + 256 + G * rec * 4
     if nq == 1:
         assert la.la_schedule_export(la.la_plan(3, hkv * grp, hkv, d, cu_of(lengths), G)) \
             == la.la_schedule_export(s)
         f = la.la_plan_fixed(3, hkv * grp, hkv, d, cu_of(lengths), 3)
-        assert la.la_schedule_export(f) == P.export(P.plan_fixed(3, hkv * grp, hkv * qb, d, cu_of(lengths), 3, 256))
+        assert la.la_schedule_export(f) == P.export(P.plan_fixed(3, hkv * grp, hkv * qb, d, cu_of(lengths), 3, T))
     kv = la.la_plan_kv(3, hkv * grp, hkv, d, cu_of(lengths), nq=nq, num_sms=G)
     assert kv.query_blocks == qb and kv.heads_per_unit == 1
 
 
 def test_query_blocks_of_a_single_kv_head():
-    # multi-query attention: 64 query heads share one kv head (4 blocks of 16)
-    s = la.la_plan(2, 64, 1, 128, [0, 900, 1000], 7)
+    # multi-query attention at d = 96: 64 query heads on one kv head (4 blocks of 16)
+    s = la.la_plan(2, 64, 1, 96, [0, 900, 1000], 7)
     assert s.query_blocks == 4
-    assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 64, 4, 128, [0, 900, 1000], 7, 128))
-    s, kind, _ = la.la_plan_auto(2, 64, 1, 128, [0, 900, 1000], 152)
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 64, 4, 96, [0, 900, 1000], 7, 128))
+    s, kind, _ = la.la_plan_auto(2, 64, 1, 96, [0, 900, 1000], 152)
     assert s.query_blocks == 4
     with pytest.raises(la.LeanAttentionError) as e:
-        la.la_plan_kv(1, 64, 1, 128, [0, 900], heads_per_unit=2, num_sms=7)
+        la.la_plan_kv(1, 64, 1, 96, [0, 900], heads_per_unit=2, num_sms=7)
     assert e.value.status == la.LA_ERR_UNSUPPORTED  # query blocks: one kv head per unit
+
+
+def test_wide_units_hold_the_whole_group():
+    # d = 128: 64 query heads on one kv head are one unit of 64 rows on the
+    # 128-row tcgen05 instance, with 128-token tiles
+    s = la.la_plan(2, 64, 1, 128, [0, 900, 1000], 7)
+    assert s.query_blocks == 1
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 64, 1, 128, [0, 900, 1000], 7, 128))
+    assert la.la_workspace_size(s) == 256 + 256 + 7 * 128 * 130 * 4
+    assert la.la_schedule_export(la.la_plan(2, 64, 1, 64, [0, 900, 1000], 7))[4] == 128
+    for bad in (64, 256):  # the wide instance is built for 128-token tiles only
+        with pytest.raises(la.LeanAttentionError) as e:
+            la.la_plan(2, 64, 1, 64, [0, 900, 1000], 7, tile_tokens=bad)
+        assert e.value.status == la.LA_ERR_UNSUPPORTED
+    with pytest.raises(la.LeanAttentionError) as e:
+        la.la_plan_spec(1, 4, 4, 64, 129, [0, 1000], 7)  # 129 query tokens: more than a unit holds
+    assert e.value.status == la.LA_ERR_UNSUPPORTED
