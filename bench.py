@@ -77,23 +77,36 @@ def _code_only(text):
     return " ".join(text.split())
 
 
-def kernel_source_digest(csrc=None):
-    """Digest of the device code (kernel template, its parameters and
-    instances), comments and layout ignored: a profile stays valid across
-    edits that change no code."""
+def kernel_source_digest(kernel="lean_decode_kernel", csrc=None):
+    """Digest of one decode kernel's device code (its template, the shared
+    helpers and producer, its parameters and instances), comments and layout
+    ignored: a profile stays valid across edits that change no code of the
+    kernel it measured."""
+    if kernel == "lean_wide_kernel":
+        keep = lambda f: f in ("la_wide.cuh", "la_kernel.cuh", "la_internal.h", "la_kernels_wide.cu")
+    else:
+        keep = lambda f: (f in ("la_kernel.cuh", "la_internal.h") or
+                          (f.startswith("la_kernels_d") and f.endswith(".cu")))
     h = hashlib.sha256()
     csrc = csrc or os.path.join(ROOT, "decode_phase_attention_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f == "la_kernel.cuh" or f == "la_internal.h" or f.startswith("la_kernels_"):
+        if keep(f):
             h.update(f.encode())
             h.update(_code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 
-def profile_name(workload, kv_layout="slab", page_size=0):
-    """Name of the committed ncu summary of the stream-K kernel on a workload and cache layout."""
+def decode_kernel_name(w, sched):
+    """The stream-K kernel a schedule runs: the tcgen05 one for units of more
+    than 16 query rows, else the 16-row one."""
+    rows = w.hq // w.hkv // sched.query_blocks * w.nq
+    return "lean_wide_kernel" if rows > 16 else "lean_decode_kernel"
+
+
+def profile_name(workload, kv_layout="slab", page_size=0, kernel="lean_decode_kernel"):
+    """Name of the committed ncu summary of a stream-K kernel on a workload and cache layout."""
     suffix = "" if kv_layout == "slab" else ("_token_major" if kv_layout == "token_major" else f"_paged{page_size}")
-    return f"lean_decode_kernel_{workload}{suffix}"
+    return f"{kernel}_{workload}{suffix}"
 
 
 def profiled_traffic(name, d, tile):
@@ -107,9 +120,14 @@ def profiled_traffic(name, d, tile):
     src = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
     tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     inst = re.search(r"lean_decode_kernel<(\d+), (\d+),", text)
-    if not src or not tr or not inst or src.group(1) != kernel_source_digest():
+    wide = re.search(r"lean_wide_kernel<(\d+),", text)
+    if not src or not tr or not (inst or wide):
         return None
-    if (int(inst.group(1)), int(inst.group(2))) != (d, tile):
+    kernel = "lean_wide_kernel" if wide else "lean_decode_kernel"
+    if src.group(1) != kernel_source_digest(kernel):
+        return None
+    shape = (int(wide.group(1)), 128) if wide else (int(inst.group(1)), int(inst.group(2)))
+    if shape != (d, tile):
         return None
     return int(tr.group(1))
 
@@ -354,7 +372,8 @@ def run_ours(args, rank, world, local_rank):
     if args.stages:
         la.la_schedule_set_stages(dec.sched, args.stages)
     G = dec.sched.grid
-    launches_per_call = 2 if (dec.kind == "fixed_split" and dec.sched.grid > w.batch * w.hkv) else 1
+    units = la.la_schedule_export(dec.sched)[2]
+    launches_per_call = 2 if (dec.kind == "fixed_split" and dec.sched.grid > units) else 1
     stream = torch.cuda.current_stream(dev)
     out = torch.empty(*q.shape, dtype=out_torch, device=dev)
     # K+V well above L2 (129 MB) cannot be served from L2 by the next call; smaller
@@ -523,10 +542,12 @@ def run_ours(args, rank, world, local_rank):
                               "CUDA events around each call, after a 256 MiB L2 flush"),
                    "single_call_p10_us": round(times_ms[len(times_ms) // 10] * 1e3, 2),
                    "single_call_p90_us": round(times_ms[(9 * len(times_ms)) // 10] * 1e3, 2)},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": decode_kernel_name(w, dec.sched),
+                     "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": "measured hbm_gbs (copy, burst)" if peaks else "fallback 6.8 TB/s",
-                     "traffic": (profiled_traffic(profile_name(args.workload, args.kv_layout, args.page_size),
+                     "traffic": (profiled_traffic(profile_name(args.workload, args.kv_layout, args.page_size,
+                                                               decode_kernel_name(w, dec.sched)),
                                                   w.d, la.la_schedule_export(dec.sched)[4])
                                  if args.kernel == "lean" and args.heads_per_unit == 0 else None),
                      "algorithmic_bytes_per_launch": algo_bytes,

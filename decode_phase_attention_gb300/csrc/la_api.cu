@@ -319,8 +319,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // hardware's in-order block dispatch); while n CTAs run, together they read
 // R(n) = r_max * (1 - exp(-n / n0)) bytes/s, shared equally. Jobs finish in
 // order of their cumulative progress, so a heap of finish thresholds gives
-// the makespan.
-double simulate_dispatch(const std::vector<double>& job_bytes, int slots, double r_max, double n0) {
+// the makespan. cap > 0 bounds the rate of one CTA (a kernel whose tile
+// loop, not HBM, limits a lone CTA).
+double simulate_dispatch(const std::vector<double>& job_bytes, int slots, double r_max, double n0,
+                         double cap = 0.0) {
   if (job_bytes.empty()) return 0.0;
   std::vector<double> heap;  // min-heap of progress thresholds of running jobs
   auto cmp = [](double a, double b) { return a > b; };
@@ -332,7 +334,8 @@ double simulate_dispatch(const std::vector<double>& job_bytes, int slots, double
   }
   while (!heap.empty()) {
     const double n = (double)heap.size();
-    const double rate = r_max * (1.0 - std::exp(-n / n0)) / n;
+    double rate = r_max * (1.0 - std::exp(-n / n0)) / n;
+    if (cap > 0.0) rate = std::min(rate, cap);
     std::pop_heap(heap.begin(), heap.end(), cmp);
     const double thr = heap.back();
     heap.pop_back();
@@ -364,17 +367,30 @@ double piece_bytes(const la_schedule* s, int u, int t0, int t1) {
 double predict_seconds(const la_schedule* s, int slots) {
   constexpr double kRateMax = 7.5e12, kRateN0 = 60.0;
   constexpr double kLaunch = 8e-6, kMergeLaunch = 4e-6, kStartup = 3e-6, kHostMerge = 2.5e-6;
+  // a host of the tcgen05 kernel pulls its peers' records (rows x (d + 2)
+  // floats each) through one SM: 38 GB/s measured (151 records of 64 rows
+  // at d = 128 in 130 us)
+  constexpr double kWideMergeRate = 38e9;
   std::vector<double> jobs((size_t)s->G, 0.0);
   bool split = false;
+  int max_peers = 0;
   for (int g = 0; g < s->G; ++g)
     for (int i = s->cta_seg[g]; i < s->cta_seg[g + 1]; ++i) {
       const int32_t* sg = &s->segs[(size_t)i * la::kSegWords];
       jobs[g] += piece_bytes(s, sg[0], sg[1], sg[2]);
-      split = split || sg[3] == la::kHost;
+      if (sg[3] == la::kHost) {
+        split = true;
+        max_peers = std::max(max_peers, sg[4] - g);
+      }
     }
   const int rounds = (s->G + slots - 1) / std::max(1, slots);  // CTAs one SM runs in turn
-  double t = simulate_dispatch(jobs, slots, kRateMax, kRateN0) + kLaunch + kStartup * rounds;
+  // a CTA of the tcgen05 kernel streams one 128-token tile per 1.55 us at
+  // most (its softmax and MMA chain), whatever HBM could give it
+  const double cap = s->R == la::kWideRows ? (double)s->T * s->d * 4.0 / 1.55e-6 : 0.0;
+  double t = simulate_dispatch(jobs, slots, kRateMax, kRateN0, cap) + kLaunch + kStartup * rounds;
   if (split) t += kHostMerge;
+  if (split && s->R == la::kWideRows)
+    t += (double)max_peers * s->unit_grp() * s->nq * (s->d + 2) * 4.0 / kWideMergeRate;
   if (s->kind == 1 && s->splits > 1) t += kMergeLaunch;
   return t;
 }

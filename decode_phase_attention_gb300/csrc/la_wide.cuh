@@ -719,17 +719,21 @@ __global__ void __launch_bounds__(D) lean_wide_combine_kernel(const CParams p) {
   if (j >= rows) return;
   const int h0 = p.unit_host[unit], h1 = p.unit_fin[unit];
   if (h0 == h1) return;  // a whole unit was written by the decode kernel
-  float M = -INFINITY, Ls = 0.f, O = 0.f;
-  for (int s2 = h0; s2 <= h1; ++s2) {
-    const float* r = p.recs + (size_t)s2 * C::RS;
-    const float m2 = r[j], l2 = r[rows + j], o2 = r[(size_t)(2 + c) * rows + j];
-    const float mn = fmaxf(M, m2);
-    if (mn == -INFINITY) continue;
-    const float a = (M == -INFINITY) ? 0.f : ex2(M - mn);
-    const float bw = (m2 == -INFINITY) ? 0.f : ex2(m2 - mn);
-    Ls = a * Ls + bw * l2;
-    O = a * O + bw * o2;
-    M = mn;
+  // f over all pieces at once: the maximum m, then the weighted sums of l
+  // and O (independent loads, several pieces in flight)
+  float M = -INFINITY;
+#pragma unroll 8
+  for (int s2 = h0; s2 <= h1; ++s2) M = fmaxf(M, __ldcg(p.recs + (size_t)s2 * C::RS + j));
+  float Ls = 0.f, O = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll 8
+    for (int s2 = h0; s2 <= h1; ++s2) {
+      const float* r = p.recs + (size_t)s2 * C::RS;
+      const float m2 = __ldcg(r + j);
+      const float wt = (m2 == -INFINITY) ? 0.f : ex2(m2 - M);  // NaN m (poisoned) propagates
+      Ls = fmaf(wt, __ldcg(r + rows + j), Ls);
+      O = fmaf(wt, __ldcg(r + (size_t)(2 + c) * rows + j), O);
+    }
   }
   const int b = unit / p.hkv, kvh = unit % p.hkv;
   store_out(p.out, row_index(p, b, kvh, j) * D + c, O / Ls, p.out_dtype);

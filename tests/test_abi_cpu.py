@@ -435,3 +435,12 @@ def test_wide_units_hold_the_whole_group():
     with pytest.raises(la.LeanAttentionError) as e:
         la.la_plan_spec(1, 4, 4, 64, 129, [0, 1000], 7)  # 129 query tokens: more than a unit holds
     assert e.value.status == la.LA_ERR_UNSUPPORTED
+
+
+def test_partition_choice_for_wide_units():
+    # one unit over every SM: the host would pull 151 records of 64 rows
+    # through one SM, so the fixed split wins; 16 units: stream-K
+    s, kind, pred = la.la_plan_auto(1, 64, 1, 128, [0, 262144], 152)
+    assert kind == "fixed_split" and pred[0] > pred[2]
+    s, kind, pred = la.la_plan_auto(16, 64, 1, 128, cu_of([32768] * 16), 152)
+    assert kind == "lean" and pred[0] < pred[2] < pred[1]
