@@ -82,15 +82,18 @@ enum {
  *
  *   batch, hq, hkv, d  shape; d in {64, 80, 96, 128, 256}; hq % hkv == 0
  *                      (any group grp = hq / hkv). Up to 16 query rows per
- *                      kv head run as one unit; a group that is not a power
- *                      of two runs on the next larger kernel instance (1, 2,
- *                      4, 8 or 16 rows), whose spare rows are zero queries
- *                      never written out. A kv head with more than 16 rows
- *                      (grp > 16, e.g. multi-query attention) is split into
+ *                      kv head run as one unit on the 16-row kernel; a group
+ *                      that is not a power of two runs on the next larger
+ *                      instance (1, 2, 4, 8 or 16 rows), whose spare rows are
+ *                      zero queries never written out. At d = 64 and 128 a
+ *                      unit of 17-128 rows (e.g. multi-query attention) runs
+ *                      on the tcgen05 kernel (128-row instance, 128-token
+ *                      tiles). A kv head with more rows than a unit holds
+ *                      (128 at d = 64, 128; 16 otherwise) is split into
  *                      query blocks: the fewest equal blocks of consecutive
- *                      query heads with at most 16 rows each (qb blocks of
- *                      grp / qb heads, qb dividing grp); every block is a
- *                      unit of its own that reads the kv head's K/V
+ *                      query heads that fit (qb blocks of grp / qb heads, qb
+ *                      dividing grp); every block is a unit of its own that
+ *                      reads the kv head's K/V
  *   cu_seqlens_k       HOST pointer to batch + 1 int32 offsets (read, not kept)
  *   num_sms            grid size G; <= 0 picks one persistent CTA per SM of
  *                      the current device (the kernel runs one CTA per SM).
@@ -130,7 +133,8 @@ la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k
  *                512k-context batches; with 4-8 rows (tensor-core path)
  *                the table's 128 stays faster (2-3 %), and so it does for
  *                la_plan_fixed, whose few busy SMs each need the deeper
- *                shared-memory ring of the larger tile.
+ *                shared-memory ring of the larger tile. Units of more
+ *                than 16 query rows (the tcgen05 kernel) take 128 only.
  * Other arguments and rules as la_plan. LA_ERR_UNSUPPORTED for a (d, T)
  * that is not built.
  */
@@ -148,9 +152,10 @@ la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlen
  * schedule la_decode / la_decode_ex / la_decode_kv / la_decode_static read
  * q as [batch, nq, hq, d] and write out as [batch, nq, hq, d]. The tiles and
  * their split are those of la_plan (K/V are read once per kv head for all
- * grp * nq query rows, up to 16; above that the kv head's query heads are
- * split into query blocks as in la_plan, each of grp / qb * nq <= 16 rows).
- * Requires nq <= 16 (LA_ERR_UNSUPPORTED) and L_b >= nq for every request
+ * grp * nq query rows, as many as a unit holds; above that the kv head's
+ * query heads are split into query blocks as in la_plan, each of
+ * grp / qb * nq rows). Requires nq <= 128 at d = 64 and 128, nq <= 16
+ * otherwise (LA_ERR_UNSUPPORTED), and L_b >= nq for every request
  * (LA_ERR_INVALID); nq = 1 is la_plan.
  */
 la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t* cu_seqlens_k, int num_sms,
@@ -196,8 +201,8 @@ int la_schedule_grid(const la_schedule* s);
  * Bytes of device workspace la_decode needs for this schedule: a header, G
  * ready flags and G partial records of rows * (d + 2) floats, rounded up to
  * a multiple of 4 floats (rows = query rows per unit head -- a kv head or
- * one query block of one -- rounded up to 1, 2, 4, 8 or 16, times the kv
- * heads per unit) ("7.4
+ * one query block of one -- rounded up to 1, 2, 4, 8, 16, or 128 on the
+ * tcgen05 kernel, times the kv heads per unit) ("7.4
  * limitations": a small amount of global memory for sharing partial
  * results). Zero it once (la_workspace_init) before its first use; after
  * that it needs no clearing between calls. One workspace must not be used
@@ -297,14 +302,15 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
  *                   head; more rows need 1). 0 picks the fewest heads
  *                   whose rows make whole 256-byte pieces if that count
  *                   divides hkv, else the most built count that divides
- *                   hkv, else 1 (always 1 for d = 128, 256, for 9-16
- *                   query rows per kv head and for query blocks).
+ *                   hkv, else 1 (always 1 for d = 128, 256, for more
+ *                   than 8 query rows per kv head and for query blocks).
  *   tile_tokens     tokens of each head per tile; 0 picks the default:
  *                   the review's table size of d (128 at d = 128 also for
  *                   one or two query rows: 16-token pages read 13 % slower
  *                   with 64) divided by heads_per_unit, so a tile still
  *                   holds the same bytes (only these defaults are built for
- *                   more than one head per unit).
+ *                   more than one head per unit); 128 for units of more
+ *                   than 16 query rows (the tcgen05 kernel).
  *   num_sms, out    as la_plan
  * Units are (request, group of heads_per_unit consecutive kv heads) in
  * request-major order, tiles(b) = ceil(L_b / tile_tokens), and the split
