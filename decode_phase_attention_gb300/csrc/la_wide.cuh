@@ -165,7 +165,8 @@ struct WCfg {
   static constexpr int REC = D + 2;
   static constexpr int RS = record_stride(D, M);
   static constexpr int NSW = 16;                // softmax warps: 4 per TMEM lane quadrant
-  static constexpr int RED_BYTES = 3 * 4 * M * 4;  // quarter maxima (two tiles) and quarter sums of l
+  // quarter maxima (two tiles), quarter sums of l, O quarters handed between lane replicas ([64][65])
+  static constexpr int RED_BYTES = 3 * 4 * M * 4 + 64 * 65 * 4;
   static constexpr int NSB = D == 64 ? 3 : 2;   // S / P buffers in TMEM
   static constexpr int NBARS = 2 * 6 + 3 * NSB + 3;  // full, empty (<= 6 stages), s_full, p_full, pv_done, q_ready, drain, stg
   static constexpr int STAGES = cmin(6, (232448 - RED_BYTES - 1024 - 256) / STAGE_BYTES);
@@ -308,7 +309,7 @@ __device__ __forceinline__ void wide_mma(const KParams& p, int g, const E* kv,
 // quarter and write the record, or merge the peers' records with f and
 // store O / l. Every softmax thread passes the same named barriers, also
 // after an abort (the waits are skipped then, not the barriers).
-template <int D, typename E>
+template <int D, typename E, int NREP>
 __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, float* red,
                                              uint64_t* full, uint64_t* s_full, uint64_t* p_full,
                                              uint64_t* pv_done, uint64_t* q_ready, uint64_t* stg,
@@ -321,6 +322,17 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
   const int qd = warp & 3, cq = warp >> 2;
   const int r = qd * 32 + lane;
   const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);  // this warp's 32 lanes
+  // NREP = 2 (units of at most 64 rows): lanes r and r + 64 hold the same
+  // query row and each replica takes half of every tile's tokens, so that
+  // all four sub-partitions compute 2^x; P is zero in the other replica's
+  // half, and the two O rows are summed at the end.
+  constexpr int TPT = 32 / NREP;  // tokens of a tile per thread
+  constexpr int RM = C::M / NREP;  // rows of one exchange slot
+  const int half = NREP == 2 ? (qd >> 1) : 0;
+  const int row = NREP == 2 ? (r & 63) : r;  // the query row lane r holds
+  const int toff = NREP == 2 ? 64 * half + 16 * cq : 32 * cq;       // this thread's first token
+  const int tother = NREP == 2 ? 64 * (1 - half) + 16 * cq : 0;     // the other replica's (P = 0)
+  float* stage_o = red + 3 * 4 * C::M;  // [64][65] O quarters handed between replicas
   const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
   const uint32_t ready = epoch + 1u;
   const int ns = ring_stages<C>(p);
@@ -339,18 +351,19 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
     if (!ok && tid == 0) record_error(p.hdr, kStatusInvalid, g, unit);
     const long long L = w1.y;
     const int n_tiles = t1 - t0;
-    const bool live = r < p.rows;
-    const bool warp_live = qd * 32 < p.rows;  // warp-uniform
-    // keys row r may see in the request: its query token sits at position
-    // L - nq + r / grp
-    const long long lim = live ? L - (p.nq - 1 - r / p.grp) : 0;
+    const bool live = row < p.rows;
+    const bool owner = live && half == 0;  // writes the row's record or output
+    const bool warp_live = (NREP == 2 ? (qd & 1) * 32 : qd * 32) < p.rows;  // warp-uniform
+    // keys the row may see in the request: its query token sits at position
+    // L - nq + row / grp
+    const long long lim = live ? L - (p.nq - 1 - row / p.grp) : 0;
 
     // ---- the unit's Q rows into TMEM (the A operand of S = Q K^T): this
     // thread's quarter of row r, two 16-bit values per column; spare rows
     // are zero
     {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) +
-                                                        row_index(p, b, kvh, live ? r : 0) * D + (D / 4) * cq);
+                                                        row_index(p, b, kvh, live ? row : 0) * D + (D / 4) * cq);
       uint32_t qw[D / 8];
 #pragma unroll
       for (int k = 0; k < D / 32; ++k) {
@@ -385,18 +398,18 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
       float mq = -INFINITY;
       float xs = 1.f;  // u holds scores to multiply by xs: raw (xs = qscale) or already scaled (1)
       if (work) {
-        tmem_ld16(sc + 32u * cq, u);
-        tmem_ld16(sc + 32u * cq + 16u, u + 16);
-        tmem_wait_ld_regs<32>(u);
-        // visible tokens of this quarter
-        const long long lv = lim - (long long)tt * T - 32 * cq;
-        const int vis = lv < 0 ? 0 : (lv > 32 ? 32 : (int)lv);
-        if (vis == 32 && p.qscale > 0.f) {
+        tmem_ld16(sc + (uint32_t)toff, u);
+        if constexpr (TPT == 32) tmem_ld16(sc + (uint32_t)toff + 16u, u + 16);
+        tmem_wait_ld_regs<TPT>(u);
+        // visible tokens of this thread's share
+        const long long lv = lim - (long long)tt * T - toff;
+        const int vis = lv < 0 ? 0 : (lv > TPT ? TPT : (int)lv);
+        if (vis == TPT && p.qscale > 0.f) {
           // the whole quarter is visible: the maximum of the raw scores,
           // scaled once (rounding is monotonic)
           float m0 = __uint_as_float(u[0]), m1 = __uint_as_float(u[1]);
 #pragma unroll
-          for (int i = 2; i < 32; i += 2) {
+          for (int i = 2; i < TPT; i += 2) {
             m0 = fmaxf(m0, __uint_as_float(u[i]));
             m1 = fmaxf(m1, __uint_as_float(u[i + 1]));
           }
@@ -404,20 +417,21 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
           xs = p.qscale;
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < TPT; ++i) {
             const float x = i < vis ? __uint_as_float(u[i]) * p.qscale : -INFINITY;
             u[i] = __float_as_uint(x);
             mq = fmaxf(mq, x);
           }
         }
-        red[(j & 1u) * 4 * C::M + cq * C::M + r] = mq;
+        red[(j & 1u) * 4 * C::M + (half * 4 + cq) * RM + row] = mq;
       }
       softmax_sync();  // the four quarter maxima of every row are in shared memory
       float alpha = 1.f;
       bool resc = false;
       if (work) {
-        const float* rm = red + (j & 1u) * 4 * C::M + r;
-        const float mt = fmaxf(fmaxf(rm[0], rm[C::M]), fmaxf(rm[2 * C::M], rm[3 * C::M]));
+        const float* rm = red + (j & 1u) * 4 * C::M + row;
+        float mt = fmaxf(fmaxf(rm[0], rm[RM]), fmaxf(rm[2 * RM], rm[3 * RM]));
+        if constexpr (NREP == 2) mt = fmaxf(mt, fmaxf(fmaxf(rm[4 * RM], rm[5 * RM]), fmaxf(rm[6 * RM], rm[7 * RM])));
         if (mt > m_use + 8.f) {  // move the reference maximum (always on a row's first visible tile)
           alpha = (m_use == -INFINITY) ? 0.f : ex2(m_use - mt);
           m_use = mt;
@@ -428,7 +442,7 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
         uint32_t hi[16], lo[16];
         float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < TPT / 2; ++k) {
           // p = 2^(s - m); masked scores are -inf and give 0
           const float p0 = ex2(fmaf(__uint_as_float(u[2 * k]), xs, nref));
           const float p1 = ex2(fmaf(__uint_as_float(u[2 * k + 1]), xs, nref));
@@ -446,8 +460,16 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
             lo[k] = Elem<E>::pack(p0 - h.x, p1 - h.y);
           }
         }
-        tmem_st16(sc + 16u * cq, hi);        // tokens 32 cq .. 32 cq + 31: high parts
-        tmem_st16(sc + 64u + 16u * cq, lo);  // and low parts
+        if constexpr (NREP == 1) {
+          tmem_st16(sc + 16u * cq, hi);        // tokens 32 cq .. 32 cq + 31: high parts
+          tmem_st16(sc + 64u + 16u * cq, lo);  // and low parts
+        } else {
+          const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+          tmem_st8(sc + (uint32_t)(toff / 2), hi);  // this replica's 16 tokens
+          tmem_st8(sc + 64u + (uint32_t)(toff / 2), lo);
+          tmem_st8(sc + (uint32_t)(tother / 2), zero);  // the other replica's: P = 0 in this lane
+          tmem_st8(sc + 64u + (uint32_t)(tother / 2), zero);
+        }
         lq += ls0 + ls1;
       }
       // V rows past the context: zero them, so that 0 * (whatever a cache
@@ -517,9 +539,26 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
       }
     }
     tc_fence_before();
-    lsum[cq * C::M + r] = lq;
+    lsum[(half * 4 + cq) * RM + row] = lq;
     softmax_sync();  // every warp's waits are over; the quarter sums are in shared memory
-    const float l = (lsum[r] + lsum[C::M + r]) + (lsum[2 * C::M + r] + lsum[3 * C::M + r]);
+    float l = (lsum[row] + lsum[RM + row]) + (lsum[2 * RM + row] + lsum[3 * RM + row]);
+    if constexpr (NREP == 2) {
+      l += (lsum[4 * RM + row] + lsum[5 * RM + row]) + (lsum[6 * RM + row] + lsum[7 * RM + row]);
+      // the replica in lanes 64..127 hands its O quarter to the one in 0..63
+#pragma unroll
+      for (int c0 = 0; c0 < OQ; c0 += 16) {
+        if (half == 1) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) stage_o[row * 65 + cq * 16 + k] = o[c0 + k];
+        }
+        softmax_sync();
+        if (half == 0) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) o[c0 + k] += stage_o[row * 65 + cq * 16 + k];
+        }
+        softmax_sync();
+      }
+    }
     const bool poisoned = (*abort_flag != 0) || !ok || !have_o;
 
     // Records are column-major over the unit's rows (wide_rec): element
@@ -527,14 +566,14 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
     // that a warp's 32 rows read and write whole 128-byte lines.
     const int rows = p.rows;
     if (kind == kNonHost || kind == kPartial) {
-      if (live) {
+      if (owner) {
         float* rec = p.recs + (size_t)g * C::RS;
         if (cq == 0) {
-          rec[r] = poisoned ? __int_as_float(0x7fc00000) : m_use;
-          rec[rows + r] = l;
+          rec[row] = poisoned ? __int_as_float(0x7fc00000) : m_use;
+          rec[rows + row] = l;
         }
 #pragma unroll
-        for (int c = 0; c < OQ; ++c) rec[(size_t)(2 + OQ * cq + c) * rows + r] = o[c];
+        for (int c = 0; c < OQ; ++c) rec[(size_t)(2 + OQ * cq + c) * rows + row] = o[c];
       }
       __threadfence();
       softmax_sync();
@@ -589,18 +628,18 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
           const bool got = issued && mbar_wait_bounded(stg, sph, &no_abort, p.spin_ns);
           sph ^= issued ? 1u : 0u;
           if (issued && !got) fail = true;
-          if (got && live && !*abort_flag) {
+          if (got && owner && !*abort_flag) {
             for (int k = 0; k < nb; ++k) {
               const float* rk = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(kv) +
                                                                (size_t)k * rec_bytes);
-              const float mk = rk[r];
+              const float mk = rk[row];
               const float mn = fmaxf(M, mk);
               if (mn == -INFINITY) continue;
               const float a = (M == -INFINITY) ? 0.f : ex2(M - mn);
               const float wt = (mk == -INFINITY) ? 0.f : ex2(mk - mn);  // NaN m (poisoned) propagates
-              Ls = a * Ls + wt * rk[rows + r];
+              Ls = a * Ls + wt * rk[rows + row];
 #pragma unroll
-              for (int c = 0; c < OQ; ++c) o[c] = a * o[c] + wt * rk[(2 + OQ * cq + c) * rows + r];
+              for (int c = 0; c < OQ; ++c) o[c] = a * o[c] + wt * rk[(2 + OQ * cq + c) * rows + row];
               M = mn;
             }
           }
@@ -610,8 +649,8 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
         if (*abort_flag) fail = true;
       }
       // normalise and store: O = Obar / l
-      if (live) {
-        const size_t base = row_index(p, b, kvh, r) * D + OQ * cq;
+      if (owner) {
+        const size_t base = row_index(p, b, kvh, row) * D + OQ * cq;
         const float inv = 1.f / Ls;
 #pragma unroll
         for (int c = 0; c < OQ; c += 4)
@@ -626,7 +665,9 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
 }
 
 // -------------------------------------------------------------------- kernel
-template <int D, typename E>
+// NREP = 2 for units of at most 64 rows (lane replicas), 1 otherwise: two
+// instances, so that each gets its own register allocation.
+template <int D, typename E, int NREP>
 __global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
     lean_wide_kernel(const KParams p, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
@@ -685,7 +726,7 @@ __global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
   const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr[kEpoch]);
 
   if (warp < C::NSW) {
-    wide_softmax<D, E>(p, g, kv, red, full, s_full, p_full, pv_done, q_ready, stg, tmem, flags_smem, epoch);
+    wide_softmax<D, E, NREP>(p, g, kv, red, full, s_full, p_full, pv_done, q_ready, stg, tmem, flags_smem, epoch);
   } else if (warp == C::NSW) {
     produce<C, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
   } else if ((tid & 31) == 0) {
@@ -748,7 +789,9 @@ cudaError_t launch_wide_t(const KParams& p, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(lean_wide_kernel<D, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    e = cudaFuncSetAttribute(lean_wide_kernel<D, E, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(lean_wide_kernel<D, E, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
@@ -760,7 +803,10 @@ cudaError_t launch_wide_t(const KParams& p, cudaStream_t st) {
   else
     e = encode_kv_maps(p.k, p.v, p.kv_rows, D, C::T, C::W, (int)Elem<E>::kTmaType, &mk, &mv);
   if (e != cudaSuccess) return e;
-  lean_wide_kernel<D, E><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
+  if (p.rows <= 64)
+    lean_wide_kernel<D, E, 2><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
+  else
+    lean_wide_kernel<D, E, 1><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
   return cudaGetLastError();
 }
 
@@ -774,10 +820,10 @@ cudaError_t launch_wide_combine_t(const CParams& p, cudaStream_t st) {
 template <int D>
 cudaError_t wide_capacity_t(int* per_sm) {
   using C = WCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(lean_wide_kernel<D, __nv_bfloat16>,
+  cudaError_t e = cudaFuncSetAttribute(lean_wide_kernel<D, __nv_bfloat16, 1>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lean_wide_kernel<D, __nv_bfloat16>, C::NTHREADS,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lean_wide_kernel<D, __nv_bfloat16, 1>, C::NTHREADS,
                                                        C::SMEM);
 }
 

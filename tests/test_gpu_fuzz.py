@@ -187,3 +187,65 @@ def test_random_configuration_with_9_to_16_rows(seed):
     err = np.abs(got - ref).max()
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
+
+
+WIDE = [(17, 1), (20, 1), (24, 1), (32, 1), (40, 1), (48, 1), (64, 1), (96, 1), (128, 1), (130, 1), (256, 1),
+        (8, 3), (16, 2), (4, 5), (2, 16), (6, 7), (3, 11)]
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_configuration_with_more_than_16_rows(seed):
+    """More than 16 query rows per kv head: units of up to 128 rows on the
+    tcgen05 kernel (d = 64, 128) or query blocks, through la_plan,
+    la_plan_spec, la_plan_fixed, la_plan_auto and la_plan_kv on every layout."""
+    r = np.random.default_rng(13000 + seed)
+    d = int(r.choice(la.HEAD_DIMS))
+    grp, nq = WIDE[int(r.integers(0, len(WIDE)))]
+    hkv = int(r.integers(1, 3))
+    batch = int(r.integers(1, 4))
+    lengths = [int(x) for x in np.maximum(nq, np.exp(r.uniform(0, np.log(4000), size=batch)).astype(int))]
+    dt = str(r.choice(["f16", "bf16"]))
+    layout = str(r.choice(["slab", "slab", "token_major", "paged"]))
+    page = int(r.choice([16, 32, 64, 128])) if d != 80 else int(r.choice([32, 64, 128]))
+    grid = int(r.choice([0, 0, 3, 29]))
+    entry = str(r.choice(["plan", "fixed", "auto"])) if (layout == "slab" and nq == 1) else "plan"
+    w = workloads.custom(batch, hkv * grp, hkv, d, dt, lengths, nq=nq)
+    q, k, v, cu = workloads.make_inputs(w, seed=seed, device="cuda")
+    if layout != "slab":
+        s = la.la_plan_kv(batch, w.hq, hkv, d, cu, nq=nq, num_sms=grid)
+        assert s.heads_per_unit == 1
+    elif nq > 1:
+        s = la.la_plan_spec(batch, w.hq, hkv, d, nq, cu, grid)
+    elif entry == "fixed":
+        s = la.la_plan_fixed(batch, w.hq, hkv, d, cu, int(r.integers(1, 5)))
+    elif entry == "auto":
+        s, _, _ = la.la_plan_auto(batch, w.hq, hkv, d, cu, grid)
+    else:
+        s = la.la_plan(batch, w.hq, hkv, d, cu, grid)
+    ws = la.new_workspace(s)
+    out = torch.empty(*q.shape, dtype=torch.float32, device="cuda")
+    cu_dev = torch.as_tensor(cu, device="cuda")
+    if layout == "slab":
+        la.la_decode(q, k, v, cu_dev, s, ws, out, w.scale)
+        kk, vv = k.cpu(), v.cpu()
+    elif layout == "token_major":
+        kc, vc = workloads.to_token_major(w, k, v)
+        la.la_decode_kv(q, kc, vc, cu_dev, s, ws, out, w.scale, layout="token_major")
+        kk = layouts.gather_token_major(kc.cpu().view(torch.int16).numpy(), cu, hkv, d)
+        vv = layouts.gather_token_major(vc.cpu().view(torch.int16).numpy(), cu, hkv, d)
+        kk, vv = kk.astype(np.int16).view(np.uint16), vv.astype(np.int16).view(np.uint16)
+    else:
+        kc, vc, table, npages = workloads.to_paged(w, k, v, page, seed=seed)
+        la.la_decode_kv(q, kc, vc, cu_dev, s, ws, out, w.scale, layout="paged", block_table=table.cuda(),
+                        page_size=page, num_pages=npages)
+        kk = layouts.gather_paged(kc.cpu().view(torch.int16).numpy(), table.numpy(), cu, page, hkv, d)
+        vv = layouts.gather_paged(vc.cpu().view(torch.int16).numpy(), table.numpy(), cu, page, hkv, d)
+        kk, vv = kk.astype(np.int16).view(np.uint16), vv.astype(np.int16).view(np.uint16)
+    assert la.la_get_status(ws) == la.LA_OK
+    code = oracle.F16 if dt == "f16" else oracle.BF16
+    ref = oracle.attend(q.cpu(), kk, vv, cu, w.hq, hkv, d, w.scale, code, nq=nq)
+    got = out.double().cpu().numpy().reshape(ref.shape)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - ref).max()
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
