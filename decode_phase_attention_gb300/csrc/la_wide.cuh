@@ -629,18 +629,26 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
           sph ^= issued ? 1u : 0u;
           if (issued && !got) fail = true;
           if (got && owner && !*abort_flag) {
-            for (int k = 0; k < nb; ++k) {
-              const float* rk = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(kv) +
-                                                               (size_t)k * rec_bytes);
-              const float mk = rk[row];
-              const float mn = fmaxf(M, mk);
-              if (mn == -INFINITY) continue;
-              const float a = (M == -INFINITY) ? 0.f : ex2(M - mn);
-              const float wt = (mk == -INFINITY) ? 0.f : ex2(mk - mn);  // NaN m (poisoned) propagates
-              Ls = a * Ls + wt * rk[rows + row];
+            // f over the batch at once: its maximum, one rescale of the
+            // running partial, then the weighted sums
+            const float* r0 = reinterpret_cast<const float*>(kv);
+            const int rstride = (int)(rec_bytes / 4);  // floats between staged records
+            float mb = M;
+            for (int k = 0; k < nb; ++k) mb = fmaxf(mb, r0[k * rstride + row]);
+            if (mb != -INFINITY) {
+              const float a = (M == -INFINITY) ? 0.f : ex2(M - mb);
+              Ls *= a;
 #pragma unroll
-              for (int c = 0; c < OQ; ++c) o[c] = a * o[c] + wt * rk[(2 + OQ * cq + c) * rows + row];
-              M = mn;
+              for (int c = 0; c < OQ; ++c) o[c] *= a;
+              for (int k = 0; k < nb; ++k) {
+                const float* rk = r0 + k * rstride;
+                const float mk = rk[row];
+                const float wt = (mk == -INFINITY) ? 0.f : ex2(mk - mb);  // NaN m (poisoned) propagates
+                Ls = fmaf(wt, rk[rows + row], Ls);
+#pragma unroll
+                for (int c = 0; c < OQ; ++c) o[c] = fmaf(wt, rk[(2 + OQ * cq + c) * rows + row], o[c]);
+              }
+              M = mb;
             }
           }
           softmax_sync();  // the staging area is rewritten by the next batch
