@@ -30,13 +30,21 @@
 // kernel). S of the next tile is computed into another buffer while the
 // softmax runs; it waits only for the P V that last used that buffer.
 // Keeping Q in TMEM leaves shared memory to the K/V ring (3 stages of
-// 64 KiB at d = 128, 6 of 32 KiB at d = 64). O accumulates over a segment's tiles in TMEM; a row's reference
-// maximum moves only when a tile's maximum exceeds it by more than 2^8
-// (p values stay below 256), and only then is that row of O rescaled.
+// 64 KiB at d = 128, 6 of 32 KiB at d = 64). O accumulates over a
+// segment's tiles in TMEM; a row's reference maximum moves only when a
+// tile's maximum exceeds it by more than 2^8 (p values stay below 256), and
+// only then is that row of O rescaled.
 //
-// Everything else -- schedule, segments, ready flags with epochs, the
-// partial records (m, l, O per row), the host's merge with f, bounded
-// waits and the abort protocol -- is the 16-row kernel's.
+// Units of at most 64 rows (a second instance, NREP = 2) hold every query
+// row in two lane replicas, r and r + 64, that take half of each tile's
+// tokens each (P = 0 in the other half), so that all four sub-partitions
+// compute 2^x; their two partial O rows are summed at the end.
+//
+// Partial records hold (m, l, O) per row column-major over the unit's rows
+// (coalesced for a warp's 32 rows); a host pulls its peers' records into
+// the idle ring with bulk copies and merges them from shared memory. The
+// schedule, segments, ready flags with epochs, bounded waits and the abort
+// protocol are the 16-row kernel's.
 #pragma once
 
 #include "la_kernel.cuh"
