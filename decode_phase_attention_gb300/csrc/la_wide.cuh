@@ -306,17 +306,19 @@ __device__ __forceinline__ void wide_mma(const KParams& p, int g, const E* kv,
 
 // --------------------------------------------------------- softmax warps
 // Warp w (0..15) works on TMEM lane quadrant w % 4 (the lanes its SM
-// sub-partition reaches): thread (w, lane) owns row r = 32 (w % 4) + lane
-// and quarter cq = w / 4 of every S tile (tokens 32 cq .. 32 cq + 31) and
+// sub-partition reaches): thread (w, lane) owns lane r = 32 (w % 4) + lane
+// and quarter cq = w / 4 of its share of every S tile (with NREP = 1, tokens
+// 32 cq .. 32 cq + 31; with NREP = 2, 16 tokens of its replica's half) and
 // of O (head dims D/4 cq ..). Per segment: write the unit's Q rows to
-// TMEM; per tile: read the quarter row of S, mask and scale it,
-// exchange the quarter maxima of each row through shared memory, move the
-// reference maximum if the tile's maximum exceeds it by more than 8 (base-2
-// units), write P = 2^(s - m) as high and low 16-bit parts over S, update
-// the quarter sum of l; at the end: add the four quarter sums, read the O
-// quarter and write the record, or merge the peers' records with f and
-// store O / l. Every softmax thread passes the same named barriers, also
-// after an abort (the waits are skipped then, not the barriers).
+// TMEM; per tile: read the thread's scores, mask and scale them, exchange
+// the partial maxima of each row through shared memory, move the reference
+// maximum if the tile's maximum exceeds it by more than 8 (base-2 units),
+// write P = 2^(s - m) as high and low 16-bit parts over S, update the
+// partial sum of l; at the end: add the partial sums (and, with replicas,
+// the two O rows), read the O quarter and write the record, or merge the
+// peers' records with f and store O / l. Every softmax thread passes the
+// same named barriers, also after an abort (the waits are skipped then,
+// not the barriers).
 template <int D, typename E, int NREP>
 __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, float* red,
                                              uint64_t* full, uint64_t* s_full, uint64_t* p_full,
