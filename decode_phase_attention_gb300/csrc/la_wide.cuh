@@ -173,7 +173,7 @@ struct WCfg {
   static constexpr int REC = D + 2;
   static constexpr int RS = record_stride(D, M);
   static constexpr int NSW = 16;                // softmax warps: 4 per TMEM lane quadrant
-  // quarter maxima (two tiles), quarter sums of l, O quarters handed between lane replicas ([64][65])
+  // partial row maxima (two tiles), partial sums of l, O quarters handed between lane replicas ([64][65])
   static constexpr int RED_BYTES = 3 * 4 * M * 4 + 64 * 65 * 4;
   static constexpr int NSB = D == 64 ? 3 : 2;   // S / P buffers in TMEM
   static constexpr int NBARS = 2 * 6 + 3 * NSB + 3;  // full, empty (<= 6 stages), s_full, p_full, pv_done, q_ready, drain, stg

@@ -47,6 +47,16 @@ def test_schedule_too_large_for_the_fixed_array_is_rejected_before_any_launch():
         == la.LA_ERR_WORKSPACE
 
 
+def test_wide_unit_records_fill_the_fixed_array_sooner():
+    # units of more than 16 rows keep 128-row records (65 KiB each at
+    # d = 128): 152 CTAs need 9.9 MiB, 48 fit in the 4 MiB array
+    p = ctypes.c_void_p(0x100000)  # never dereferenced: the size check comes first
+    big = la.la_plan(1, 64, 1, 128, [0, 100000], 152)
+    assert la.la_workspace_size(big) > 4 << 20
+    assert la._lib.la_decode_static(p, p, p, la.LA_BF16, p, big.handle, p, ctypes.c_float(0.1), None) \
+        == la.LA_ERR_WORKSPACE
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("case", ["tiny", "ragged_gqa", "fixed_split", "three_query_tokens"])
 def test_static_scratch_matches_la_decode_on_two_calls_in_a_row(case):
