@@ -213,6 +213,9 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   const int qb = query_blocks(hq / hkv, nq, d);
   if (qb == 0) return LA_ERR_UNSUPPORTED;
   const int rows = (hq / hkv / qb) * nq;
+  // units are counted in 32 bits (and index q rows with their query heads)
+  if ((int64_t)batch * hkv * qb > (int64_t)INT32_MAX / 16 || (int64_t)batch * nq * hq > (int64_t)INT32_MAX / 16)
+    return LA_ERR_UNSUPPORTED;
   // a query block, or a unit of more than 16 rows, is one kv head
   if ((qb > 1 || rows > 16) && hp != 1) return LA_ERR_UNSUPPORTED;
   // stream-K on the slab layout: slab_tile; the fixed partitions keep the

@@ -444,3 +444,11 @@ def test_partition_choice_for_wide_units():
     assert kind == "fixed_split" and pred[0] > pred[2]
     s, kind, pred = la.la_plan_auto(16, 64, 1, 128, cu_of([32768] * 16), 152)
     assert kind == "lean" and pred[0] < pred[2] < pred[1]
+
+
+def test_unit_counts_beyond_32_bits_are_rejected():
+    # a million requests of 4096 query heads: more query rows than the
+    # planner counts in 32 bits
+    with pytest.raises(la.LeanAttentionError) as e:
+        la.la_plan(1 << 20, 4096, 1, 64, np.arange((1 << 20) + 1, dtype=np.int32), 7)
+    assert e.value.status == la.LA_ERR_UNSUPPORTED
