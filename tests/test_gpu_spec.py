@@ -82,3 +82,27 @@ def test_spec_workload_full_output():
     q, k, v, _ = workloads.make_inputs(w, seed=0, device="cuda")
     out = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, w.cu, nq=w.nq)(q, k, v, w.scale)
     compare(out.cpu(), ref_spec(w, q, k, v))
+
+
+@pytest.mark.parametrize("name", ["spec16", "spec32", "spec64"])
+def test_long_drafts_at_bench_size(name):
+    # batch 8, 32/32 heads, d 128, 8192-token contexts with 16, 32 or 64 draft
+    # tokens per request (16 rows per kv head on the 16-row kernel, 32 and 64
+    # on the tcgen05 kernel), in the launch configuration the bench times;
+    # rows sampled for the oracle, the causal last tokens included
+    import numpy as np
+    import oracle
+    w = workloads.named(name)
+    q, k, v, _ = workloads.make_inputs(w, seed=7, device="cuda")
+    dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, w.cu, nq=w.nq)
+    out = dec(q, k, v, w.scale)
+    assert dec.status() == la.LA_OK
+    rows = []
+    for b in (0, 3, 7):
+        for i in (0, w.nq // 2, w.nq - 1):
+            for h in (0, 17, 31):
+                rows.append((b * w.nq + i) * w.hq + h)
+    rows = np.array(rows, np.int64)
+    code = oracle.F16 if q.dtype == torch.float16 else oracle.BF16
+    ref = oracle.attend(q.cpu(), k.cpu(), v.cpu(), w.cu, w.hq, w.hkv, w.d, w.scale, code, rows=rows, nq=w.nq)
+    compare(out.view(-1, w.d)[rows].cpu(), ref)

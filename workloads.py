@@ -114,10 +114,12 @@ def named(name, seed=0):
         return Workload(name, b, h, kv, d, "bf16", [c] * b,
                         description=f"GQA sweep: batch {b}, {h} query over {kv} kv heads, d {d}, ctx {c}, bf16")
     if name.startswith("spec"):
-        # speculative-decoding verification: 4 draft tokens per request
-        return Workload(name, 8, 32, 32, 128, "bf16", [8192] * 8, nq=4,
-                        description="speculative verification: batch 8, 4 query tokens per request, "
-                                    "32/32 heads, d 128, ctx 8192, bf16, causal among the 4")
+        # speculative-decoding verification: specN = N draft tokens per
+        # request (spec4: 4), each attending causally to the ones before it
+        n = int(name[4:] or 4)
+        return Workload(name, 8, 32, 32, 128, "bf16", [8192] * 8, nq=n,
+                        description=f"speculative verification: batch 8, {n} query tokens per request, "
+                                    f"32/32 heads, d 128, ctx 8192, bf16, causal among the {n}")
     if name == "hd128gqa":
         return Workload(name, 4, 32, 4, 128, "bf16", [32768] * 4,
                         description="GQA d 128: batch 4, 32 query over 4 kv heads, d 128, ctx 32768, bf16")
