@@ -102,6 +102,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
                "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
@@ -140,13 +151,13 @@ __device__ __forceinline__ void store_out4(void* out, size_t idx, float a, float
   }
 }
 
-// Shared-memory matrix descriptor of a tcgen05 operand in the 128-byte
-// swizzle layout (rows of 128 bytes, 8-row atoms of 1024 bytes, atoms
-// 1024-byte aligned): start address, leading and stride byte offsets,
-// the fixed version field and the swizzle mode.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor of a tcgen05 operand in a swizzled
+// layout (rows of 128 or 64 bytes, 8-row atoms of 1024 or 512 bytes, atoms
+// aligned to their size): start address, leading and stride byte offsets,
+// the fixed version field and the swizzle mode (2: 128-byte, 4: 64-byte).
+__device__ __forceinline__ uint64_t sdesc_swz(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t mode) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (mode << 61);
 }
 // Instruction descriptor of a dense kind::f16 MMA with fp32 accumulation:
 // operand format (0 fp16, 1 bf16) for A and B, B MN-major or K-major, N, M.
@@ -165,17 +176,21 @@ struct WCfg {
   static constexpr int T = 128;                 // LeanTile tokens (MMA N of S, K of P V)
   static constexpr int ROWS = T;
   static constexpr bool TC = true;              // the producer's swizzled TMA boxes
-  static constexpr int W = 64;                  // box columns: 128-byte rows
+  static constexpr int W = D % 64 == 0 ? 64 : 32;  // box columns
+  static constexpr int RB = W * 2;              // box row bytes: 128 (128-byte swizzle) or 64 (64-byte)
   static constexpr int NB = D / W;              // boxes per tile per tensor
   static constexpr int TILE_ELEMS = T * D;
   static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
-  static constexpr int BOX_BYTES = T * 128;     // one box of a K or V tile
+  static constexpr int BOX_BYTES = T * RB;      // one box of a K or V tile
+  static constexpr int ATOM = 8 * RB;           // one 8-row swizzle atom
+  static constexpr uint64_t SWZ = W == 64 ? 2 : 4;  // descriptor swizzle mode
+  static constexpr int KPB = W / 16;            // MMA k-steps (16 head dims, 32 bytes) per box row
   static constexpr int REC = D + 2;
   static constexpr int RS = record_stride(D, M);
   static constexpr int NSW = 16;                // softmax warps: 4 per TMEM lane quadrant
   // partial row maxima (two tiles), partial sums of l, O quarters handed between lane replicas ([64][65])
   static constexpr int RED_BYTES = 3 * 4 * M * 4 + 64 * 65 * 4;
-  static constexpr int NSB = D == 64 ? 3 : 2;   // S / P buffers in TMEM
+  static constexpr int NSB = 3 * T + D + D / 2 <= 512 ? 3 : 2;  // S / P buffers in TMEM
   static constexpr int NBARS = 2 * 6 + 3 * NSB + 3;  // full, empty (<= 6 stages), s_full, p_full, pv_done, q_ready, drain, stg
   static constexpr int STAGES = cmin(6, (232448 - RED_BYTES - 1024 - 256) / STAGE_BYTES);
   static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
@@ -185,7 +200,7 @@ struct WCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = NSB * T;    // S / P buffers first, then O
   static constexpr uint32_t Q_COL = O_COL + D;  // then Q
-  static_assert(D == 64 || D == 128, "head dims of the wide kernel");
+  static_assert(D == 64 || D == 96 || D == 128, "head dims of the wide kernel");
   static_assert(STAGES >= 2 && SMEM <= 232448, "shared memory per CTA");
   static_assert(NBARS * 8 + 16 <= 256, "barrier area");
   static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor memory columns");
@@ -244,9 +259,10 @@ __device__ __forceinline__ void wide_mma(const KParams& p, int g, const E* kv,
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       // 16 head dims per MMA: Q columns 8 kk .. (two dims per column); the K
-      // tile's box kk / 4, 32 bytes into its swizzled rows
-      const uint32_t ka = kb + (uint32_t)(kk >> 2) * C::BOX_BYTES + (uint32_t)(kk & 3) * 32u;
-      mma_ts(ds, tmem + C::Q_COL + 8u * (uint32_t)kk, sdesc_sw128(ka, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+      // tile's box kk / KPB, 32 bytes per step into its swizzled rows
+      const uint32_t ka = kb + (uint32_t)(kk / C::KPB) * C::BOX_BYTES + (uint32_t)(kk % C::KPB) * 32u;
+      mma_ts(ds, tmem + C::Q_COL + 8u * (uint32_t)kk, sdesc_swz(ka, 16, C::ATOM, C::SWZ), kIdS,
+             kk > 0 ? 1u : 0u);
     }
     tc_commit(&s_full[jj % C::NSB]);
   };
@@ -287,8 +303,8 @@ __device__ __forceinline__ void wide_mma(const KParams& p, int g, const E* kv,
       const uint32_t pc = tmem + (j % C::NSB) * (uint32_t)C::T;
 #pragma unroll
       for (int kk = 0; kk < C::T / 16; ++kk) {
-        // LBO: the next 64 head dims (next box); SBO: the next 8 tokens
-        const uint64_t vd = sdesc_sw128(vb + (uint32_t)kk * 2048u, C::BOX_BYTES, 1024);
+        // 16 tokens per step; LBO: the next W head dims (next box); SBO: the next 8 tokens
+        const uint64_t vd = sdesc_swz(vb + (uint32_t)kk * 16u * C::RB, C::BOX_BYTES, C::ATOM, C::SWZ);
         mma_ts(tmem + C::O_COL, pc + 8u * (uint32_t)kk, vd, kIdO, (t > 0 || kk > 0) ? 1u : 0u);
         mma_ts(tmem + C::O_COL, pc + 64u + 8u * (uint32_t)kk, vd, kIdO, 1u);
       }
@@ -328,6 +344,7 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
   using C = WCfg<D>;
   constexpr int T = C::T;
   constexpr int OQ = D / 4;  // head dims of O per thread
+  constexpr int OC = OQ % 16 == 0 ? 16 : 8;  // O columns per TMEM access (aligned to its size)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, cq = warp >> 2;
   const int r = qd * 32 + lane;
@@ -383,10 +400,14 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
         qw[4 * k + 2] = v.z;
         qw[4 * k + 3] = v.w;
       }
-      if constexpr (D / 8 == 16)
+      if constexpr (D / 8 == 16) {
         tmem_st16(trow + C::Q_COL + 16u * cq, qw);
-      else
+      } else if constexpr (D / 8 == 8) {
         tmem_st8(trow + C::Q_COL + 8u * cq, qw);
+      } else {  // d = 96: 12 columns, in pieces of 4 (each access aligned to its size)
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) tmem_st4(trow + C::Q_COL + (uint32_t)(D / 8) * cq + 4u * k, qw + 4 * k);
+      }
     }
     tmem_wait_st();
     tc_fence_before();
@@ -490,9 +511,9 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
           const int ntok = (int)rem;
           unsigned char* vt = reinterpret_cast<unsigned char*>(kv) + (size_t)stage * C::STAGE_BYTES +
                               (size_t)C::TILE_ELEMS * 2;
-          const int n16 = (T - ntok) * 8;  // 16-byte pieces past the context in one box
+          const int n16 = (T - ntok) * (C::RB / 16);  // 16-byte pieces past the context in one box
           for (int i = tid; i < n16 * C::NB; i += C::NSW * 32)
-            *reinterpret_cast<uint4*>(vt + (i / n16) * C::BOX_BYTES + ntok * 128 + (i % n16) * 16) =
+            *reinterpret_cast<uint4*>(vt + (i / n16) * C::BOX_BYTES + ntok * C::RB + (i % n16) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
           fence_proxy_async_smem();
         }
@@ -504,14 +525,14 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
           tc_fence_after();
           const float a = (resc && t > 0) ? alpha : 1.f;
 #pragma unroll
-          for (int c = 0; c < OQ / 16; ++c) {
-            uint32_t o[16];
-            const uint32_t oc = trow + C::O_COL + (uint32_t)(OQ * cq + 16 * c);
-            tmem_ld16(oc, o);
-            tmem_wait_ld_regs<16>(o);
+          for (int c = 0; c < OQ / OC; ++c) {
+            uint32_t o[OC];
+            const uint32_t oc = trow + C::O_COL + (uint32_t)(OQ * cq + OC * c);
+            if constexpr (OC == 16) tmem_ld16(oc, o); else tmem_ld8(oc, o);
+            tmem_wait_ld_regs<OC>(o);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * a);
-            tmem_st16(oc, o);
+            for (int k = 0; k < OC; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * a);
+            if constexpr (OC == 16) tmem_st16(oc, o); else tmem_st8(oc, o);
           }
         } else {
           alive = false;
@@ -540,12 +561,13 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
     for (int c = 0; c < OQ; ++c) o[c] = 0.f;
     if (have_o && warp_live) {
 #pragma unroll
-      for (int c = 0; c < OQ / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16(trow + C::O_COL + (uint32_t)(OQ * cq + 16 * c), v);
-        tmem_wait_ld_regs<16>(v);
+      for (int c = 0; c < OQ / OC; ++c) {
+        uint32_t v[OC];
+        const uint32_t oc = trow + C::O_COL + (uint32_t)(OQ * cq + OC * c);
+        if constexpr (OC == 16) tmem_ld16(oc, v); else tmem_ld8(oc, v);
+        tmem_wait_ld_regs<OC>(v);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) o[16 * c + k] = __uint_as_float(v[k]);
+        for (int k = 0; k < OC; ++k) o[OC * c + k] = __uint_as_float(v[k]);
       }
     }
     tc_fence_before();
@@ -556,15 +578,15 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
       l += (lsum[4 * RM + row] + lsum[5 * RM + row]) + (lsum[6 * RM + row] + lsum[7 * RM + row]);
       // the replica in lanes 64..127 hands its O quarter to the one in 0..63
 #pragma unroll
-      for (int c0 = 0; c0 < OQ; c0 += 16) {
+      for (int c0 = 0; c0 < OQ; c0 += OC) {
         if (half == 1) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) stage_o[row * 65 + cq * 16 + k] = o[c0 + k];
+          for (int k = 0; k < OC; ++k) stage_o[row * 65 + cq * 16 + k] = o[c0 + k];
         }
         softmax_sync();
         if (half == 0) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) o[c0 + k] += stage_o[row * 65 + cq * 16 + k];
+          for (int k = 0; k < OC; ++k) o[c0 + k] += stage_o[row * 65 + cq * 16 + k];
         }
         softmax_sync();
       }

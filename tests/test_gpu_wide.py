@@ -1,4 +1,4 @@
-"""The tcgen05 kernel (units of 17-128 query rows at d = 64 and 128) under
+"""The tcgen05 kernel (units of 17-128 query rows at d = 64, 96 and 128) under
 the same checks as the 16-row kernel: a bounded wait made to run out and
 device offsets that disagree with the schedule come back as a status with
 the context still usable; the trace records the planned work; the ring
@@ -84,7 +84,7 @@ def test_trace_records_the_planned_work_of_every_cta():
     assert np.all(tr[:, 1] <= tr[:, 2]) and np.all(tr[:, 2] <= tr[:, 3]) and np.all(tr[:, 3] <= tr[:, 5])
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 def test_ring_depth_does_not_change_the_result(d):
     w = workloads.custom(2, 64, 2, d, "bf16", [3000, 777])
     q, k, v, cu = workloads.make_inputs(w, seed=d, device="cuda")
