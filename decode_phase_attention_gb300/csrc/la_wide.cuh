@@ -30,7 +30,9 @@
 // kernel). S of the next tile is computed into another buffer while the
 // softmax runs; it waits only for the P V that last used that buffer.
 // Keeping Q in TMEM leaves shared memory to the K/V ring (3 stages of
-// 64 KiB at d = 128, 6 of 32 KiB at d = 64). O accumulates over a
+// 64 KiB at d = 128, 4 of 48 KiB at d = 96, 6 of 32 KiB at d = 64). At
+// d = 64 and 128 the K/V boxes are 64 head dims wide (128-byte swizzle),
+// at d = 96 32 dims (64-byte swizzle). O accumulates over a
 // segment's tiles in TMEM; a row's reference maximum moves only when a
 // tile's maximum exceeds it by more than 2^8 (p values stay below 256), and
 // only then is that row of O rescaled.
