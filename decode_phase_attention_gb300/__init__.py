@@ -31,7 +31,7 @@ class KvDesc(ctypes.Structure):
     _fields_ = [("layout", ctypes.c_int), ("block_table", ctypes.c_void_p), ("max_blocks", ctypes.c_int),
                 ("page_size", ctypes.c_int), ("num_pages", ctypes.c_longlong)]
 EXPORTED = ["la_plan", "la_plan_ex", "la_plan_spec", "la_plan_kv", "la_plan_fixed", "la_plan_auto", "la_decode_ex", "la_decode_kv", "la_schedule_grid", "la_workspace_size", "la_workspace_init",
-            "la_decode", "la_decode_static", "la_get_status", "la_schedule_export_size", "la_schedule_export",
+            "la_decode", "la_decode_static", "la_decode_host", "la_get_status", "la_schedule_export_size", "la_schedule_export",
             "la_schedule_set_debug", "la_schedule_set_stages", "la_schedule_set_trace", "la_device_capacity",
             "la_schedule_destroy",
             "la_status_string"]
@@ -64,6 +64,7 @@ def _load():
         "la_workspace_init": (c_int, [vp, c_size, vp]),
         "la_decode": (c_int, [vp, vp, vp, c_int, vp, vp, vp, vp, c_float, vp]),
         "la_decode_static": (c_int, [vp, vp, vp, c_int, vp, vp, vp, c_float, vp]),
+        "la_decode_host": (c_int, [vp, vp, vp, c_int, vp, vp, vp, vp, vp, vp, vp, vp, c_float, vp]),
         "la_get_status": (c_int, [vp, vp]),
         "la_schedule_export_size": (c_size, [vp]),
         "la_schedule_export": (c_int, [vp, vp, c_size]),
@@ -333,6 +334,40 @@ def la_decode_static(q, k, v, cu_seqlens_k, sched, out, scale, stream=None):
                                  ctypes.c_void_p(out.data_ptr()), float(scale),
                                  _stream_handle(stream)), "la_decode_static")
     return out
+
+
+def la_decode_host(q_host, k_host, v_host, cu_seqlens_k, sched, workspace, q_dev, k_dev, v_dev, out_dev,
+                   out_host, scale, stream=None):
+    """One decode call on host inputs: the library enqueues the copies of q, k, v
+    to the device buffers, the decode and the copy of out back to out_host on
+    `stream` (no synchronisation). Host tensors should be pinned."""
+    import torch
+    for name, t, dev in (("q_host", q_host, False), ("k_host", k_host, False), ("v_host", v_host, False),
+                         ("out_host", out_host, False), ("q_dev", q_dev, True), ("k_dev", k_dev, True),
+                         ("v_dev", v_dev, True), ("out_dev", out_dev, True), ("cu_seqlens_k", cu_seqlens_k, True),
+                         ("workspace", workspace, True)):
+        if t.is_cuda != dev or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {'device' if dev else 'host'} tensor")
+    dt = {torch.float16: LA_F16, torch.bfloat16: LA_BF16}.get(q_host.dtype)
+    if dt is None or any(t.dtype != q_host.dtype for t in (k_host, v_host, q_dev, k_dev, v_dev)):
+        raise ValueError("q, k, v (host and device) must share one dtype, float16 or bfloat16")
+    if out_host.dtype != torch.float32 or out_dev.dtype != torch.float32 or cu_seqlens_k.dtype != torch.int32:
+        raise ValueError("out must be float32 and cu_seqlens_k int32")
+    b, hq, hkv, d = sched.batch, sched.hq, sched.hkv, sched.d
+    n_q = b * sched.nq * hq * d
+    kv_elems = int(sched.cu[-1]) * hkv * d
+    if any(t.numel() != n_q for t in (q_host, q_dev, out_host, out_dev)) or \
+            any(t.numel() < kv_elems for t in (k_host, v_host, k_dev, v_dev)) or cu_seqlens_k.numel() != b + 1:
+        raise ValueError("tensor sizes do not match the schedule")
+    if workspace.numel() * workspace.element_size() < la_workspace_size(sched):
+        raise ValueError("workspace smaller than la_workspace_size")
+    vp = ctypes.c_void_p
+    _check(_lib.la_decode_host(vp(q_host.data_ptr()), vp(k_host.data_ptr()), vp(v_host.data_ptr()), dt,
+                               vp(cu_seqlens_k.data_ptr()), sched.handle, vp(q_dev.data_ptr()),
+                               vp(k_dev.data_ptr()), vp(v_dev.data_ptr()), vp(workspace.data_ptr()),
+                               vp(out_dev.data_ptr()), vp(out_host.data_ptr()), float(scale),
+                               _stream_handle(stream)), "la_decode_host")
+    return out_host
 
 
 def la_decode_kv(q, k_cache, v_cache, cu_seqlens_k, sched, workspace, out, scale, layout="token_major",

@@ -225,6 +225,7 @@ la_status make_schedule(int batch, int hq, int hkv, int d, const int32_t* cu, in
   if (!unit_tile_supported(d, tile, hp, rows)) return LA_ERR_UNSUPPORTED;
   la_schedule* s = new (std::nothrow) la_schedule();
   if (s == nullptr) return LA_ERR_INVALID;
+  s->serial = la_next_schedule_serial();
   s->batch = batch;
   s->hq = hq;
   s->hkv = hkv;
@@ -401,6 +402,10 @@ double predict_seconds(const la_schedule* s, int slots) {
 }  // namespace
 
 namespace la {
+
+int cached_capacity(int d, int T, int grp, int hp, int* per_sm) { return capacity(d, T, grp, per_sm, hp); }
+
+int device_sm_count(int* sms) { return device_sms(sms); }
 
 int slab_tile(int d, int rows) { return (d == 128 && rows <= 2) ? 64 : default_tile(d); }
 
@@ -851,6 +856,37 @@ la_status la_decode_ex(const void* q, const void* k, const void* v, la_dtype dt,
 la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt, const int32_t* cu_seqlens_k_dev,
                     const la_schedule* s, void* workspace, float* out, float scale, la_stream_t stream) {
   return la_decode_ex(q, k, v, dt, cu_seqlens_k_dev, s, workspace, out, LA_OUT_F32, scale, stream);
+}
+
+la_status la_decode_host(const void* q_host, const void* k_host, const void* v_host, la_dtype dt,
+                         const int32_t* cu_seqlens_k_dev, const la_schedule* s, void* q_dev, void* k_dev,
+                         void* v_dev, void* workspace, float* out_dev, float* out_host, float scale,
+                         la_stream_t stream) {
+  if (s == nullptr || q_host == nullptr || k_host == nullptr || v_host == nullptr || out_host == nullptr)
+    return LA_ERR_INVALID;
+  if (s->hp != 1) return LA_ERR_UNSUPPORTED;  // units of several kv heads read token-major or paged caches
+  const size_t q_bytes = (size_t)s->batch * s->nq * s->hq * s->d * 2;
+  const size_t kv_bytes = (size_t)s->hkv * (size_t)s->cu[s->batch] * s->d * 2;
+  const size_t out_bytes = (size_t)s->batch * s->nq * s->hq * s->d * sizeof(float);
+  // la_decode's own argument checks, made before any copy is enqueued
+  if (q_dev == nullptr || k_dev == nullptr || v_dev == nullptr || out_dev == nullptr ||
+      cu_seqlens_k_dev == nullptr)
+    return LA_ERR_INVALID;
+  if (dt != LA_F16 && dt != LA_BF16) return LA_ERR_INVALID;
+  if (!aligned(q_dev, 16) || !aligned(k_dev, 16) || !aligned(v_dev, 16) || !aligned(out_dev, 16) ||
+      !aligned(cu_seqlens_k_dev, 4))
+    return LA_ERR_INVALID;
+  if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return LA_ERR_INVALID;
+  if (workspace == nullptr || !aligned(workspace, 256)) return LA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(k_dev, k_host, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(v_dev, v_host, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return LA_ERR_CUDA;
+  const la_status e = la_decode(q_dev, k_dev, v_dev, dt, cu_seqlens_k_dev, s, workspace, out_dev, scale, stream);
+  if (e != LA_OK) return e;
+  return cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess ? LA_OK
+                                                                                                   : LA_ERR_CUDA;
 }
 
 la_status la_get_status(void* workspace, la_stream_t stream) {

@@ -138,6 +138,10 @@ cudaError_t launch_decode(int d, int T, int grp, int hp, int dtype, const KParam
 cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st);
 // CTAs of the decode kernel one SM holds at once (cudaOccupancy...).
 cudaError_t decode_capacity(int d, int T, int grp, int hp, int* per_sm);
+// The same, cached per (device, d, T, grp, hp) on the host, and the current
+// device's SM count (la_api.cu). Both return an la_status value (0 = LA_OK).
+int cached_capacity(int d, int T, int grp, int hp, int* per_sm);
+int device_sm_count(int* sms);
 #define LA_DECLARE_HEAD_DIM(D)                                                           \
   cudaError_t launch_decode_d##D(int T, int grp, int dtype, const KParams& p, cudaStream_t st); \
   cudaError_t launch_combine_d##D(int grp, const CParams& p, cudaStream_t st);           \

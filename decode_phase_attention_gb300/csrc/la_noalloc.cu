@@ -27,6 +27,15 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {nullptr};
 
+// Which schedule's tables each device's array holds (its address and serial
+// number; serial 0: none yet), so that a run of calls with one schedule
+// copies the tables once instead of on every call.
+struct Held {
+  const la_schedule* s = nullptr;
+  uint64_t serial = 0;
+};
+Held g_held[kMaxDevices];
+
 la_status scratch_address(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) return LA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -90,9 +99,10 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
 
   if (s->kind == 0) {  // host CTAs wait on later CTAs: all of the grid must be resident
     int per_sm = 0, sms = 0;
-    la_status e = la_device_capacity(s->d, s->grp, &per_sm, &sms);
+    la_status e = (la_status)la::device_sm_count(&sms);
     if (e != LA_OK) return e;
-    if (la::decode_capacity(s->d, s->T, s->R, 1, &per_sm) != cudaSuccess) return LA_ERR_CUDA;
+    e = (la_status)la::cached_capacity(s->d, s->T, s->R, s->hp, &per_sm);
+    if (e != LA_OK) return e;
     if ((long long)s->G > (long long)per_sm * sms) return LA_ERR_INVALID;
   }
   int dev = 0;
@@ -104,12 +114,22 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   cudaStream_t st = (cudaStream_t)stream;
 
   // The array keeps whatever the previous call left: clear the header
-  // (epoch, done counter, status) and the ready flags, then copy the tables.
+  // (epoch, done counter, status) and the ready flags; copy the tables
+  // unless this device's array already holds this schedule's.
   if (cudaMemsetAsync(base, 0, L.recs, st) != cudaSuccess) return LA_ERR_CUDA;
-  if (put(base, L.cu, s->cu, st) != cudaSuccess || put(base, L.cta_seg, s->cta_seg, st) != cudaSuccess ||
-      put(base, L.segs, s->dev_segs, st) != cudaSuccess || put(base, L.host, s->unit_host, st) != cudaSuccess ||
-      put(base, L.fin, s->unit_fin, st) != cudaSuccess)
-    return LA_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    Held& h = g_held[dev];
+    if (h.s != s || h.serial != s->serial) {
+      h = Held{};  // a failed copy leaves no schedule recorded
+      if (put(base, L.cu, s->cu, st) != cudaSuccess || put(base, L.cta_seg, s->cta_seg, st) != cudaSuccess ||
+          put(base, L.segs, s->dev_segs, st) != cudaSuccess || put(base, L.host, s->unit_host, st) != cudaSuccess ||
+          put(base, L.fin, s->unit_fin, st) != cudaSuccess)
+        return LA_ERR_CUDA;
+      h.s = s;
+      h.serial = s->serial;
+    }
+  }
 
   la::KParams p;
   p.q = q;

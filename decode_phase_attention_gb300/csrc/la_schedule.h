@@ -4,6 +4,7 @@
 
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -22,6 +23,10 @@ struct la_schedule {
   int splits = 0;  // fixed partitions only
   int G = 0, U = 0;
   int64_t I = 0;
+  // Number of this schedule among all schedules the process has made (from
+  // 1): a table copy can be recognised even when a destroyed schedule's
+  // address is reused by a new one.
+  uint64_t serial = 0;
   std::vector<int32_t> cu, cta_iter, unit_iter, cta_seg, segs, unit_host, unit_fin;
   std::vector<int32_t> dev_segs;  // device records (kDevSegWords per segment)
   // debug hooks
@@ -41,3 +46,9 @@ struct la_schedule {
   int unit_heads() const { return hkv * qb; }
   int unit_grp() const { return grp / qb; }
 };
+
+// Source of la_schedule::serial.
+inline uint64_t la_next_schedule_serial() {
+  static std::atomic<uint64_t> next{0};
+  return ++next;
+}

@@ -344,17 +344,48 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
  *   - The first call on a device looks up the array's address on that
  *     device (cudaGetSymbolAddress) with the device current; make that
  *     first call before any stream capture.
- *   - Each call clears the flags and copies the schedule's tables from
- *     host memory into the array on `stream`, then launches the same
- *     kernel(s) as la_decode. All calls share the one array, which keeps
- *     the previous call's contents: calls that can overlap on the GPU (on
- *     different streams, or from several threads) race, so serialise them.
+ *   - Each call clears the array's header and ready flags on `stream`,
+ *     then launches the same kernel(s) as la_decode. The schedule's tables
+ *     are copied from host memory into the array only when the array on
+ *     this device does not already hold them (the first call with a
+ *     schedule, or a call after one with another schedule); a run of calls
+ *     with one schedule copies them once. All calls share the one array,
+ *     which keeps the previous call's contents: calls that can overlap on
+ *     the GPU (on different streams, or from several threads) race, so
+ *     serialise them.
  *   - There is no status word to read back: a failure detected inside the
  *     kernel shows up as NaN outputs.
  */
 la_status la_decode_static(const void* q, const void* k, const void* v, la_dtype dt,
                            const int32_t* cu_seqlens_k_dev, const la_schedule* s, float* out,
                            float scale, la_stream_t stream);
+
+/*
+ * la_decode_host -- one decode call on inputs in HOST memory, with the copies
+ * in and out enqueued on `stream` around it (the paper has no counterpart:
+ * its measurements start with q, K and V already on the device). On
+ * `stream`, in order: q_host -> q_dev, k_host -> k_dev, v_host -> v_dev
+ * (one cudaMemcpyAsync each), la_decode on the device copies, then
+ * out_dev -> out_host. Sizes follow the schedule: q and out hold
+ * batch * nq * hq * d elements (fp16/bf16 and fp32), k and v
+ * hkv * cu[batch] * d elements each, in la_decode's slab layout.
+ *
+ *   q_host, k_host, v_host, out_host  host buffers; page-locked memory
+ *                     (cudaHostAlloc / cudaHostRegister) makes the copies
+ *                     asynchronous. Read q/k/v and write out_host only
+ *                     after the stream has reached this call's end.
+ *   q_dev, k_dev, v_dev, out_dev      device buffers of those sizes,
+ *                     16-byte aligned, owned by the caller
+ *   other arguments   as la_decode
+ * Does not synchronise (except on a schedule's first use, as la_decode).
+ * The arguments are checked before anything is enqueued: LA_ERR_INVALID /
+ * LA_ERR_WORKSPACE as la_decode, LA_ERR_UNSUPPORTED for schedules of
+ * several kv heads per unit, LA_ERR_CUDA if a copy or launch fails.
+ */
+la_status la_decode_host(const void* q_host, const void* k_host, const void* v_host, la_dtype dt,
+                         const int32_t* cu_seqlens_k_dev, const la_schedule* s, void* q_dev, void* k_dev,
+                         void* v_dev, void* workspace, float* out_dev, float* out_host, float scale,
+                         la_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns and clears the first error a kernel

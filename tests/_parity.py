@@ -17,7 +17,7 @@ def oracle_code(dtype):
 
 def reference(w, q, k, v, rows=None):
     return oracle.attend(q.cpu(), k.cpu(), v.cpu(), w.cu, w.hq, w.hkv, w.d, w.scale,
-                         oracle_code(q.dtype), rows=rows)
+                         oracle_code(q.dtype), rows=rows, nq=w.nq)
 
 
 def compare(got, ref):

@@ -143,6 +143,32 @@ def test_decode_rejects_bad_pointers_before_any_launch():
     assert lib.la_decode(good, good, good, 0, good, None, ws, good, 0.125, None) == la.LA_ERR_INVALID
 
 
+def test_decode_host_rejects_bad_arguments_before_any_copy():
+    s = la.la_plan(1, 4, 4, 64, [0, 1024], 3)
+    lib = la._lib
+    vp = ctypes.c_void_p
+    h = vp(0x30000)     # host buffers: never read, validation fails first
+    good = vp(0x10000)  # device buffers: never dereferenced
+    ws = vp(0x20000)
+
+    def call(qh=h, kh=h, vh=h, dt=0, cu=good, sched=s.handle, qd=good, kd=good, vd=good, w=ws, od=good, oh=h,
+             scale=0.125):
+        return lib.la_decode_host(qh, kh, vh, dt, cu, sched, qd, kd, vd, w, od, oh, ctypes.c_float(scale), None)
+
+    assert call(qh=None) == la.LA_ERR_INVALID
+    assert call(oh=None) == la.LA_ERR_INVALID
+    assert call(kd=None) == la.LA_ERR_INVALID
+    assert call(vd=vp(0x10008)) == la.LA_ERR_INVALID       # misaligned device buffer
+    assert call(cu=vp(0x10002)) == la.LA_ERR_INVALID       # misaligned offsets
+    assert call(dt=7) == la.LA_ERR_INVALID
+    assert call(scale=float("nan")) == la.LA_ERR_INVALID
+    assert call(w=None) == la.LA_ERR_WORKSPACE
+    assert call(w=vp(0x20010)) == la.LA_ERR_WORKSPACE
+    assert call(sched=None) == la.LA_ERR_INVALID
+    two = la.la_plan_kv(1, 4, 4, 64, [0, 1024], heads_per_unit=2, num_sms=3)
+    assert call(sched=two.handle) == la.LA_ERR_UNSUPPORTED  # several kv heads per unit: caches only
+
+
 def test_workspace_size_formula():
     s = la.la_plan(1, 4, 4, 64, [0, 1024], 3)
     # header 256 + flags (3 words padded to 256) + 3 records of 1 x (64 + 2)
