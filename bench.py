@@ -6,21 +6,30 @@ one launch of the library's kernel (the schedule is planned once for the
 batch, outside the timed region; its host time is reported as plan_us).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--kernel lean|naive|fixed_split] [--impl ours|reference]
+                    [--kernel lean|naive|fixed_split|auto] [--impl ours|reference]
 
+The headline workload is the 512k-token context (batch 1, 32/32 heads,
+d 128, fp16: 8.6 GB of K+V), the largest of the decode configurations.
 value = K+V bytes read / kernel time, summed over ranks (GB/s); the kernel
 time is taken with CUDA events on the launching stream around the K timed
-back-to-back calls (single-call spread reported separately).
+back-to-back calls, which follow the warm-up calls with no idle gap (only
+the synchronisation the contract asks for). The same JSON line carries, as
+nested records measured the same way in the same process, the ragged batch,
+the uniform batch, the 64k and 256k contexts and the grouped-query batch,
+the headline at the LeanTile table's 128-token tile, and the two fixed
+partitions (one CTA per unit; fixed split plus merge launch) as ablations.
 Inputs larger than 4x L2 are not flushed between calls (the next call
-cannot hit in L2); smaller ones get a 256 MiB write before every call. e2e = the same metric with the
-inputs copied from pinned host memory and the output copied back inside
-every timed step. --impl reference times the float64 CPU oracle instead.
-Under torchrun every rank runs an independent replica (the path has no
-cross-GPU exchange) and the slowest rank's time is reported.
+cannot hit in L2); smaller ones get a 256 MiB write before every call.
+e2e = the same metric through la_decode_host: q, K, V copied from pinned
+host memory, the decode, and the output copied back, inside every timed
+step. --impl reference times the float64 CPU oracle instead. Under torchrun
+every rank runs an independent replica (the path has no cross-GPU exchange)
+and the slowest rank's time is reported.
 """
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import subprocess
@@ -35,14 +44,19 @@ METRIC = "decode-attention µs/call and KV-read GB/s as % of GB300 HBM peak, 1 G
 FLUSH_BYTES = 256 << 20
 L2_BYTES = 129 * 10**6
 NOMINAL_HBM_GBS = 8000.0
+HEADLINE = "long512k"
+# the other decode configurations, measured in the same run as nested records
+EXTRA_WORKLOADS = ["ragged", "uniform", "long64k", "long256k", "gqa"]
+EXTRA_STEPS_MAX = 200   # timed calls of a nested record: min(K, this)
+SETTLE_SECONDS = 0.1    # warm-up calls go on until at least this much GPU time
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="uniform")
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--kernel", default="lean", choices=["lean", "naive", "fixed_split", "auto"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--grid", type=int, default=0, help="stream-K grid; 0 = one CTA per SM")
@@ -59,6 +73,8 @@ def parse():
     ap.add_argument("--flush", action="store_true", help="flush L2 before every timed call")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="headline only: no nested workloads, table tile or ablations")
     return ap.parse_args()
 
 
@@ -133,14 +149,15 @@ def profiled_traffic(name, d, tile):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, interval_ms=20):
         self.index = index
+        self.interval_ms = interval_ms
         self.lines = []
         self.proc = None
 
@@ -148,7 +165,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -168,30 +185,45 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
-        if self.proc is None:
-            return None
+    def _rows(self, t0, t1):
         rows = []
-        for ts, line in self.lines:
+        for ts, line in list(self.lines):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            rows.append((ts, parts))
-        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.06]
-        used = inside if inside else rows
-        if not used:
-            return None
-        mhz = sorted(float(p[2]) for _, p in used if p[2].replace(".", "").isdigit())
+            if len(parts) >= 10 and t0 <= ts <= t1:
+                rows.append(parts)
+        return rows
+
+    @staticmethod
+    def _stats(rows):
+        mhz = sorted(float(p[2]) for p in rows if p[2].replace(".", "").isdigit())
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
-        for _, p in used:
+        for p in rows:
             for n, val in zip(names, p[6:10]):
                 if val.strip().lower() == "active":
                     reasons.add(n)
+        watts = [float(p[4]) for p in rows if p[4].replace(".", "").isdigit()]
         return {"sm_mhz": mhz[len(mhz) // 2] if mhz else None,
-                "sm_max_mhz": float(used[0][1][3]) if used[0][1][3].replace(".", "").isdigit() else None,
-                "reasons": sorted(reasons), "samples": len(used),
-                "in_timed_region": bool(inside)}
+                "sm_max_mhz": float(rows[0][3]) if rows and rows[0][3].replace(".", "").isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(watts) if watts else None}
+
+    def summary(self, load0, t0, t1):
+        """Clocks over [t0, t1] (the timed region, wall clock) and over the
+        loaded window [load0, t1] (warm-up and timed calls back to back).
+        The top-level figures are the timed region's when a sample fell
+        inside it, else the loaded window's."""
+        if self.proc is None:
+            return None
+        inside = self._stats(self._rows(t0, t1 + 0.03))
+        loaded = self._stats(self._rows(load0, t1 + 0.03))
+        if not loaded["samples"]:
+            return None
+        top = dict(inside if inside["samples"] else loaded)
+        top["in_timed_region"] = bool(inside["samples"])
+        top["timed_region"] = inside
+        top["warmup_and_timed"] = loaded
+        return top
 
 
 def max_over_ranks(x, device=None):
@@ -239,6 +271,33 @@ def algorithmic_bytes(w, export, out_bytes=4):
     return kv, kv + q + out + 2 * pieces * rec
 
 
+def uses_flush(w, args):
+    """Inputs under 4x L2 get an L2 flush before every timed call."""
+    return args.flush or w.kv_bytes() < L2_BYTES * 4
+
+
+def workload_config(w, args):
+    """The workload a line measures: the same dict in both arms."""
+    kv = w.kv_bytes()
+    return {"workload": w.description, "name": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv,
+            "head_dim": w.d, "query_tokens": w.nq, "dtype": w.dtype,
+            "total_context_tokens": w.total_tokens, "kv_bytes": kv, "seed": args.seed,
+            "l2": ("flushed before every timed call (256 MiB write, then 256 MiB read so no dirty line "
+                   "is written back inside the call)" if uses_flush(w, args) else
+                   f"no flush: K+V ({kv / 1e9:.2f} GB) exceed 4x the 129 MB L2, so no call finds its "
+                   f"inputs in L2")}
+
+
+def row_bytes_of(w, cu):
+    """K+V bytes attributed to each (request, query token, query head) row:
+    its kv head's K and V shared over the rows that read them."""
+    import numpy as np
+    nrows = w.batch * w.nq * w.hq  # row r = (b * nq + i) * hq + h
+    rows_per_kv = (w.hq // w.hkv) * w.nq
+    return np.array([2 * (cu[r // (w.nq * w.hq) + 1] - cu[r // (w.nq * w.hq)]) * w.d * 2 / rows_per_kv
+                     for r in range(nrows)])
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
     if rank != 0:
@@ -253,10 +312,8 @@ def run_reference(args, rank, world):
     q, k, v, cu = workloads.make_inputs(w, seed=args.seed, device="cpu")
     code = {"f16": oracle.F16, "bf16": oracle.BF16}[w.dtype]
     cores = os.cpu_count() or 1
-    nrows = w.batch * w.nq * w.hq  # row r = (b * nq + i) * hq + h
-    rows_per_kv = (w.hq // w.hkv) * w.nq
-    row_bytes = np.array([2 * (cu[r // (w.nq * w.hq) + 1] - cu[r // (w.nq * w.hq)]) * w.d * 2 / rows_per_kv
-                          for r in range(nrows)])
+    nrows = w.batch * w.nq * w.hq
+    row_bytes = row_bytes_of(w, cu)
     per_step = cores
     qn, kn, vn = (t.view(torch.int16).numpy().view(np.uint16) for t in (q, k, v))
     pos = 0
@@ -283,8 +340,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.description, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
-                   "total_context_tokens": w.total_tokens, "kv_bytes": w.kv_bytes(), "seed": args.seed},
+        "config": workload_config(w, args),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -294,7 +350,8 @@ def run_reference(args, rank, world):
 
 def cpu_baseline(w, q, k, v, cu, seconds, single_seconds=2.0):
     """The float64 oracle on the host cores over the workload's rows, cycled,
-    for about `seconds`; then the same with one thread for `single_seconds`."""
+    for about `seconds`; then the same with one thread for `single_seconds`.
+    q, k, v are host tensors (the pinned copies the e2e leg reads)."""
     import numpy as np
     import torch
 
@@ -303,10 +360,8 @@ def cpu_baseline(w, q, k, v, cu, seconds, single_seconds=2.0):
     code = {"f16": oracle.F16, "bf16": oracle.BF16}[w.dtype]
     cores = os.cpu_count() or 1
     qn, kn, vn = (t.view(torch.int16).numpy().view(np.uint16) for t in (q, k, v))
-    nrows = w.batch * w.nq * w.hq  # row r = (b * nq + i) * hq + h
-    rows_per_kv = (w.hq // w.hkv) * w.nq
-    row_bytes = np.array([2 * (cu[r // (w.nq * w.hq) + 1] - cu[r // (w.nq * w.hq)]) * w.d * 2 / rows_per_kv
-                          for r in range(nrows)])
+    nrows = w.batch * w.nq * w.hq
+    row_bytes = row_bytes_of(w, cu)
 
     def run(threads, budget):
         # rows in chunks of one per thread until the time budget is spent (at least one chunk)
@@ -332,189 +387,358 @@ def cpu_baseline(w, q, k, v, cu, seconds, single_seconds=2.0):
 
 
 # ------------------------------------------------------------------ our arm
+class Case:
+    """One workload on the device: its inputs, a schedule and the call."""
+
+    def __init__(self, la, torch, w, args, dev, stream, kernel="lean", tile=0, inputs=None, layout="slab"):
+        import workloads
+        self.la, self.torch, self.w, self.dev, self.stream = la, torch, w, dev, stream
+        if inputs is None:
+            inputs = workloads.make_inputs(w, seed=args.seed, device=dev)
+        self.q, self.k, self.v, self.cu = inputs
+        grid = args.grid if args.grid > 0 else (w.grid if w.name == "tiny" else 0)
+        self.layout = layout
+        slab = layout == "slab" or kernel != "lean"
+        plan_times = []
+        for _ in range(21):
+            t0 = time.perf_counter()
+            if not slab:
+                la.la_plan_kv(w.batch, w.hq, w.hkv, w.d, self.cu, w.nq, args.heads_per_unit, tile, grid)
+            elif w.nq > 1:
+                la.la_plan_spec(w.batch, w.hq, w.hkv, w.d, w.nq, self.cu, grid)
+            else:
+                la.la_plan(w.batch, w.hq, w.hkv, w.d, self.cu, grid, tile)
+            plan_times.append((time.perf_counter() - t0) * 1e6)
+        self.plan_us = sorted(plan_times)[len(plan_times) // 2]
+        if not slab:
+            dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, self.cu, num_sms=grid, device=dev, nq=w.nq,
+                                 tile_tokens=tile, heads_per_unit=args.heads_per_unit)
+        elif w.nq > 1:
+            dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, self.cu, num_sms=grid, device=dev, nq=w.nq)
+        elif kernel == "lean":
+            dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, self.cu, num_sms=grid, device=dev, tile_tokens=tile)
+        elif kernel == "naive":
+            dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, self.cu, device=dev, fixed_splits=1)
+        elif kernel == "auto":
+            dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, self.cu, num_sms=grid, device=dev, auto=True)
+        else:
+            per_sm, sms = la.la_device_capacity(w.d, w.hq // w.hkv)
+            splits = -(-sms // (w.batch * w.hkv))
+            dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, self.cu, device=dev, fixed_splits=max(1, splits))
+        if args.stages:
+            la.la_schedule_set_stages(dec.sched, args.stages)
+        self.dec = dec
+        self.kernel = kernel
+        self.export = la.la_schedule_export(dec.sched)
+        units = self.export[2]
+        self.launches_per_call = 2 if (dec.kind == "fixed_split" and dec.sched.grid > units) else 1
+        out_torch = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[args.out_dtype]
+        self.out = torch.empty(*self.q.shape, dtype=out_torch, device=dev)
+        self.use_flush = uses_flush(w, args)
+        self.flush = torch.empty(FLUSH_BYTES if self.use_flush else 1, dtype=torch.uint8, device=dev)
+        self.clean = torch.ones(FLUSH_BYTES // 4 if self.use_flush else 1, dtype=torch.int32, device=dev)
+        if slab:
+            q, k, v, out = self.q, self.k, self.v, self.out
+
+            def call():
+                dec(q, k, v, w.scale, out=out, stream=stream)
+        else:
+            if layout == "token_major":
+                kc, vc = workloads.to_token_major(w, self.k, self.v)
+                table, npages = None, 0
+            else:
+                kc, vc, table, npages = workloads.to_paged(w, self.k, self.v, args.page_size, seed=args.seed)
+                table = table.to(dev)
+            self.k, self.v = kc, vc  # the caches are what the call reads
+            cu_dev = torch.as_tensor(self.cu, dtype=torch.int32, device=dev)
+            q, out = self.q, self.out
+
+            def call():
+                la.la_decode_kv(q, kc, vc, cu_dev, dec.sched, dec.workspace, out, w.scale, layout=layout,
+                                block_table=table, page_size=args.page_size, num_pages=npages, stream=stream)
+        self.call = call
+
+    def flush_l2(self):
+        # write 256 MiB (evicts every line), then read another 256 MiB so the
+        # written lines go back to HBM before the timed call, not during it
+        self.flush.zero_()
+        self.clean.max()
+
+    def one(self):
+        if self.use_flush:
+            self.flush_l2()
+        self.call()
+
+    def check(self):
+        st = self.dec.status()
+        if st != self.la.LA_OK:
+            raise RuntimeError(f"kernel reported: {self.la.status_string(st)}")
+
+    def time(self, steps, warmup, world, marks=None):
+        """Warm-up, then `steps` timed calls; returns the mean call time (ms).
+
+        Warm-up: max(3, warmup) calls, then more back to back until at least
+        SETTLE_SECONDS of GPU time has run, so clocks and power are in their
+        loaded state. The timed calls follow after only the synchronisation
+        (and, under torchrun, the barrier) that brackets the timed region.
+        marks, if given, receives the wall-clock bounds of the loaded window
+        and of the timed region for the clock record."""
+        import torch.distributed as dist
+        torch, stream, dev = self.torch, self.stream, self.dev
+        n0 = max(3, warmup)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        load0 = time.time()
+        e0.record(stream)
+        for _ in range(n0):
+            self.one()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        self.check()
+        est = max(e0.elapsed_time(e1) / 1e3 / n0, 1e-6)
+        n_settle = min(20000, max(0, math.ceil(SETTLE_SECONDS / est) - n0))
+        for _ in range(n_settle):
+            self.one()
+        self.warmup_calls = n0 + n_settle
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        wall0 = time.time()
+        if marks is not None:
+            torch.cuda.nvtx.range_push("timed")
+        if self.use_flush:
+            starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            for i in range(steps):
+                self.flush_l2()
+                starts[i].record(stream)
+                self.call()
+                ends[i].record(stream)
+        else:
+            starts = [torch.cuda.Event(enable_timing=True)]
+            ends = [torch.cuda.Event(enable_timing=True)]
+            starts[0].record(stream)
+            for _ in range(steps):
+                self.call()
+            ends[0].record(stream)
+        if marks is not None:
+            torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        wall1 = time.time()
+        if marks is not None:
+            marks.update(load0=load0, t0=wall0, t1=wall1)
+        mean_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps
+        self.check()
+        return mean_ms
+
+    def spread(self, n):
+        """Single calls, events around each (p10, p90 in microseconds)."""
+        torch = self.torch
+        sp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, e in sp:
+            if self.use_flush:
+                self.flush_l2()
+            a.record(self.stream)
+            self.call()
+            e.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        t = sorted(a.elapsed_time(e) for a, e in sp)
+        return round(t[len(t) // 10] * 1e3, 2), round(t[(9 * len(t)) // 10] * 1e3, 2)
+
+    def kernel_name(self):
+        return decode_kernel_name(self.w, self.dec.sched)
+
+    def tile(self):
+        return self.export[4]
+
+    def roofline(self, mean_ms, peak, peaks_measured, args, profile_key=None):
+        w = self.w
+        kv_bytes, algo = algorithmic_bytes(w, self.export, self.out.element_size())
+        ws = algo - kv_bytes - self.q.numel() * self.q.element_size() - self.out.numel() * self.out.element_size()
+        achieved = algo / (mean_ms * 1e-3) / 1e9
+        traffic = None
+        if self.kernel == "lean" and args.heads_per_unit == 0:
+            name = profile_name(profile_key or w.name, self.layout, args.page_size, self.kernel_name())
+            traffic = profiled_traffic(name, w.d, self.tile())
+        return {"bound": "hbm", "kernel": self.kernel_name(),
+                "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_source": "measured hbm_gbs (copy, burst)" if peaks_measured else "fallback 6.8 TB/s",
+                "traffic": traffic, "algorithmic_bytes_per_launch": algo,
+                "workspace_bytes_per_call": ws, "workspace_frac_of_kv": round(ws / kv_bytes, 6)}
+
+    def free(self):
+        for name in ("q", "k", "v", "out", "flush", "clean", "dec", "call"):
+            if hasattr(self, name):
+                delattr(self, name)
+
+
+def record(case, mean_ms, peak, peaks_measured, args, world, steps):
+    """A nested record: one workload measured like the headline."""
+    kv = case.w.kv_bytes()
+    p10, p90 = case.spread(min(20, steps))
+    return {"workload": case.w.description, "us_per_call": round(mean_ms * 1e3, 3),
+            "value": round(world * kv / (mean_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+            "kv_read_frac_of_measured_hbm": round(kv / (mean_ms * 1e-3) / 1e9 / peak, 4),
+            "kv_read_frac_of_8tbs_nominal": round(kv / (mean_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+            "steps": steps, "warmup_calls": case.warmup_calls, "tile_tokens": case.tile(),
+            "schedule": case.dec.kind, "grid": case.dec.sched.grid, "kv_bytes": kv,
+            "single_call_p10_us": p10, "single_call_p90_us": p90,
+            "gpu_launches": steps * case.launches_per_call,
+            "roofline": case.roofline(mean_ms, peak, peaks_measured, args)}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
-    import torch.distributed as dist
 
     import decode_phase_attention_gb300 as la
     import workloads
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = workloads.named(args.workload, seed=args.seed)
-    q, k, v, cu = workloads.make_inputs(w, seed=args.seed, device=dev)
-    grid = args.grid if args.grid > 0 else (w.grid if args.workload == "tiny" else 0)
-    plan_times = []
-    for _ in range(21):
-        t0 = time.perf_counter()
-        if args.kv_layout != "slab" and args.kernel == "lean":
-            la.la_plan_kv(w.batch, w.hq, w.hkv, w.d, cu, w.nq, args.heads_per_unit, args.tile, grid)
-        else:
-            la.la_plan(w.batch, w.hq, w.hkv, w.d, cu, grid if grid > 0 else 0, args.tile)
-        plan_times.append((time.perf_counter() - t0) * 1e6)
-    plan_us = sorted(plan_times)[len(plan_times) // 2]
-    out_torch = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[args.out_dtype]
-    if args.kv_layout != "slab" and args.kernel == "lean":
-        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, nq=w.nq,
-                             tile_tokens=args.tile, heads_per_unit=args.heads_per_unit)
-    elif w.nq > 1:
-        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, nq=w.nq)
-    elif args.kernel == "lean":
-        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, tile_tokens=args.tile)
-    elif args.kernel == "naive":
-        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, device=dev, fixed_splits=1)
-    elif args.kernel == "auto":
-        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, num_sms=grid, device=dev, auto=True)
-    else:
-        per_sm, sms = la.la_device_capacity(w.d, w.hq // w.hkv)
-        splits = -(-sms // (w.batch * w.hkv))
-        dec = la.LeanDecoder(w.batch, w.hq, w.hkv, w.d, cu, device=dev, fixed_splits=max(1, splits))
-    if args.stages:
-        la.la_schedule_set_stages(dec.sched, args.stages)
-    G = dec.sched.grid
-    units = la.la_schedule_export(dec.sched)[2]
-    launches_per_call = 2 if (dec.kind == "fixed_split" and dec.sched.grid > units) else 1
     stream = torch.cuda.current_stream(dev)
-    out = torch.empty(*q.shape, dtype=out_torch, device=dev)
-    # K+V well above L2 (129 MB) cannot be served from L2 by the next call; smaller
-    # inputs get a 256 MiB write between calls to flush L2.
-    use_flush = args.flush or w.kv_bytes() < L2_BYTES * 4
-    flush = torch.empty(FLUSH_BYTES if use_flush else 1, dtype=torch.uint8, device=dev)
-    clean = torch.ones(FLUSH_BYTES // 4 if use_flush else 1, dtype=torch.int32, device=dev)
-
-    def flush_l2():
-        # write 256 MiB (evicts every line), then read another 256 MiB so the
-        # written lines go back to HBM before the timed call, not during it
-        flush.zero_()
-        clean.max()
-
-    if args.kv_layout == "slab":
-        def call():
-            dec(q, k, v, w.scale, out=out, stream=stream)
-    else:
-        if args.kv_layout == "token_major":
-            kc, vc = workloads.to_token_major(w, k, v)
-            table, npages = None, 0
-        else:
-            kc, vc, table, npages = workloads.to_paged(w, k, v, args.page_size, seed=args.seed)
-            table = table.to(dev)
-        del k, v
-        k, v = kc, vc  # the e2e leg copies these caches
-        cu_dev = torch.as_tensor(cu, dtype=torch.int32, device=dev)
-
-        def call():
-            la.la_decode_kv(q, kc, vc, cu_dev, dec.sched, dec.workspace, out, w.scale, layout=args.kv_layout,
-                            block_table=table, page_size=args.page_size, num_pages=npages, stream=stream)
-
-    # warm-up (also uploads the schedule)
-    for _ in range(max(3, args.warmup)):
-        if use_flush:
-            flush_l2()
-        call()
-    torch.cuda.synchronize(dev)
-    st = dec.status()
-    if st != la.LA_OK:
-        raise RuntimeError(f"kernel reported: {la.status_string(st)}")
-
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    w = workloads.named(args.workload, seed=args.seed)
     sampler = ClockSampler(local_rank)
     if rank == 0:
         sampler.start()
-        time.sleep(0.2)
-    # Timed region: K back-to-back calls between two events on the launching
-    # stream (with L2 flushes, when used, timed per call instead).
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps if use_flush else 1)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps if use_flush else 1)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    wall0 = time.time()
-    torch.cuda.nvtx.range_push("timed")
-    if use_flush:
-        for i in range(args.steps):
-            flush_l2()
-            starts[i].record(stream)
-            call()
-            ends[i].record(stream)
-    else:
-        starts[0].record(stream)
-        for i in range(args.steps):
-            call()
-        ends[0].record(stream)
-    torch.cuda.nvtx.range_pop()
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    wall1 = time.time()
-    sampler.stop()
-    if use_flush:
-        mean_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
-    else:
-        mean_ms = starts[0].elapsed_time(ends[0]) / args.steps
-    # spread of single calls (outside the timed region): events around each call
-    n_spread = min(50, args.steps)
-    sp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_spread)]
-    for a, e in sp:
-        if use_flush:
-            flush_l2()
-        a.record(stream)
-        call()
-        e.record(stream)
-    torch.cuda.synchronize(dev)
-    times_ms = sorted(a.elapsed_time(e) for a, e in sp)
+
+    case = Case(la, torch, w, args, dev, stream, kernel=args.kernel, tile=args.tile, layout=args.kv_layout)
+    marks = {}
+    mean_ms = case.time(args.steps, args.warmup, world, marks)
     mean_ms = max_over_ranks(mean_ms, dev)
-    st = dec.status()
-    if st != la.LA_OK:
-        raise RuntimeError(f"kernel reported: {la.status_string(st)}")
+    p10, p90 = case.spread(min(50, args.steps))
+    G = case.dec.sched.grid
 
     # one extra traced call (outside the timed region): per-CTA balance and host waits
     trace = torch.zeros(G * la.TRACE_WORDS, dtype=torch.int64, device=dev)
-    la.la_schedule_set_trace(dec.sched, trace)
-    call()
+    la.la_schedule_set_trace(case.dec.sched, trace)
+    case.call()
     torch.cuda.synchronize(dev)
-    la.la_schedule_set_trace(dec.sched, None)
+    la.la_schedule_set_trace(case.dec.sched, None)
     cta_trace = summarize_trace(trace.view(G, la.TRACE_WORDS).cpu().numpy())
+    case.check()
 
-    kv_bytes, algo_bytes = algorithmic_bytes(w, la.la_schedule_export(dec.sched), out.element_size())
-    ws_bytes = algo_bytes - kv_bytes - q.numel() * q.element_size() - out.numel() * out.element_size()
+    kv_bytes = w.kv_bytes()
     value = world * kv_bytes / (mean_ms * 1e-3) / 1e9
+    roof = case.roofline(mean_ms, peak, peaks is not None, args)
 
+    # the same workload at the LeanTile table's size (128 tokens at d = 128)
+    # and the two fixed partitions, on the same inputs
+    variants = {}
+    if not args.no_extras and args.kernel == "lean" and args.kv_layout == "slab" and w.nq == 1:
+        runs = []
+        if w.d == 128 and case.tile() != 128:
+            runs.append(("table_tile", "lean", 128))
+        runs += [("naive_one_cta_per_unit", "naive", 0), ("fixed_split_plus_merge", "fixed_split", 0)]
+        for key, kern, tile in runs:
+            c = Case(la, torch, w, args, dev, stream, kernel=kern, tile=tile,
+                     inputs=(case.q, case.k, case.v, case.cu))
+            ms = max_over_ranks(c.time(args.steps, args.warmup, world), dev)
+            variants[key] = {"us_per_call": round(ms * 1e3, 3), "tile_tokens": c.tile(),
+                             "schedule": c.dec.kind, "grid": c.dec.sched.grid,
+                             "value": round(world * kv_bytes / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+                             "kv_read_frac_of_measured_hbm": round(kv_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+                             "ratio_to_headline_time": round(ms / mean_ms, 4)}
+            c.free()
+
+    # end to end through the C ABI: la_decode_host copies q, K, V from pinned
+    # host memory, decodes, and copies the output back, every step
     e2e = None
-    if not args.no_e2e:
-        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
-        outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host = None
+    slab_f32 = args.kv_layout == "slab" and args.out_dtype == "f32"
+    if (not args.no_e2e and slab_f32) or (not args.no_cpu_baseline and world == 1 and rank == 0):
+        host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (case.q, case.k, case.v)]
+        for h, t in zip(host, (case.q, case.k, case.v)):
+            h.copy_(t)
+    if not args.no_e2e and slab_f32:
+        qh, kh, vh = host
+        outh = torch.empty(case.out.shape, dtype=torch.float32, pin_memory=True)
+        dec = case.dec
         n_e2e = max(1, min(args.e2e_steps, args.steps))
+
+        def e2e_step():
+            la.la_decode_host(qh, kh, vh, dec.cu_dev, dec.sched, dec.workspace, case.q, case.k, case.v,
+                              case.out, outh, w.scale, stream=stream)
         for _ in range(2):
-            q.copy_(qh, non_blocking=True), k.copy_(kh, non_blocking=True), v.copy_(vh, non_blocking=True)
-            call()
-            outh.copy_(out, non_blocking=True)
+            e2e_step()
         torch.cuda.synchronize(dev)
+        case.check()
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
+        torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(n_e2e):
-            q.copy_(qh, non_blocking=True)
-            k.copy_(kh, non_blocking=True)
-            v.copy_(vh, non_blocking=True)
-            call()
-            outh.copy_(out, non_blocking=True)
+            e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
-        e2e_ms = max_over_ranks(e2e_ms, dev)
-        h2d = (q.numel() + k.numel() + v.numel()) * q.element_size()
+        case.check()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
+        h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
         e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
                "us_per_call": round(e2e_ms * 1e3, 2), "steps": n_e2e,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * out.element_size()}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": outh.numel() * outh.element_size(),
+               "api": "la_decode_host (one C-ABI call per step: three host-to-device copies, the decode, "
+                      "one device-to-host copy, on one stream)"}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1 and rank == 0:
+        cpu = cpu_baseline(w, host[0], host[1], host[2], case.cu, args.cpu_seconds)
+    host = None
+
+    config = workload_config(w, args)
+    run = {"kernel": args.kernel, "schedule": case.dec.kind, "tile_tokens": case.tile(),
+           "out_dtype": args.out_dtype, "kv_heads_per_unit": case.dec.sched.heads_per_unit,
+           "query_blocks_per_kv_head": case.dec.sched.query_blocks,
+           "ring_stages": args.stages or "library default",
+           "kv_layout": args.kv_layout + (f" (page {args.page_size})" if args.kv_layout == "paged" else ""),
+           "predicted_us": case.dec.predicted_us, "grid": G,
+           "plan_us": round(case.plan_us, 1),
+           "plan_note": "median host time of the planner call, outside the timed region",
+           "timing": ("CUDA events around the K back-to-back calls" if not case.use_flush else
+                      "CUDA events around each call, after a 256 MiB L2 flush"),
+           "warmup_calls_issued": case.warmup_calls,
+           "warmup_note": (f"max(3, W) warm-up calls, then more back to back until >= {SETTLE_SECONDS} s of "
+                           "GPU time; the timed calls follow after one synchronisation"),
+           "single_call_p10_us": p10, "single_call_p90_us": p90}
+    launches = case.launches_per_call
+    case.free()
+    del case
+    torch.cuda.empty_cache()
+
+    configs = {}
+    if not args.no_extras and args.kv_layout == "slab" and args.kernel == "lean":
+        steps = min(args.steps, EXTRA_STEPS_MAX)
+        for name in EXTRA_WORKLOADS:
+            if name == args.workload:
+                continue
+            wx = workloads.named(name, seed=args.seed)
+            c = Case(la, torch, wx, args, dev, stream)
+            ms = max_over_ranks(c.time(steps, args.warmup, world), dev)
+            rec = record(c, ms, peak, peaks is not None, args, world, steps)
+            if name == "ragged" and wx.d == 128 and c.tile() != 128:
+                inputs = (c.q, c.k, c.v, c.cu)
+                for key, kern, tile in (("table_tile", "lean", 128), ("naive_one_cta_per_unit", "naive", 0),
+                                        ("fixed_split_plus_merge", "fixed_split", 0)):
+                    cv = Case(la, torch, wx, args, dev, stream, kernel=kern, tile=tile, inputs=inputs)
+                    msv = max_over_ranks(cv.time(steps, args.warmup, world), dev)
+                    rec[key] = {"us_per_call": round(msv * 1e3, 3), "tile_tokens": cv.tile(),
+                                "schedule": cv.dec.kind, "grid": cv.dec.sched.grid,
+                                "value": round(world * wx.kv_bytes() / (msv * 1e-3) / 1e9, 3),
+                                "ratio_to_default_time": round(msv / ms, 4)}
+                    cv.free()
+            configs[name] = rec
+            c.free()
+            del c
+            torch.cuda.empty_cache()
+    sampler.stop()
 
     if rank != 0:
         return
-    peaks = measured_peaks()
-    peak = peaks["hbm_gbs"] if peaks else 6800.0
-    achieved = algo_bytes / (mean_ms * 1e-3) / 1e9
-    cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(w, q.cpu(), k.cpu(), v.cpu(), cu, args.cpu_seconds)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -524,40 +748,17 @@ def run_ours(args, rank, world, local_rank):
         "kv_read_frac_of_8tbs_nominal": round(kv_bytes / (mean_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.description, "kernel": args.kernel, "schedule": dec.kind,
-                   "tile_tokens": la.la_schedule_export(dec.sched)[4], "out_dtype": args.out_dtype,
-                   "kv_heads_per_unit": dec.sched.heads_per_unit,
-                   "query_blocks_per_kv_head": dec.sched.query_blocks,
-                   "ring_stages": args.stages or "library default",
-                   "kv_layout": args.kv_layout + (f" (page {args.page_size})" if args.kv_layout == "paged" else ""),
-                   "predicted_us": dec.predicted_us, "grid": G,
-                   "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.d,
-                   "total_context_tokens": w.total_tokens, "kv_bytes": kv_bytes,
-                   "l2": ("flushed before every timed call (256 MiB write, then 256 MiB read so no "
-                          "dirty line is written back inside the call)" if use_flush else
-                          f"no flush: K+V ({kv_bytes / 1e9:.2f} GB) exceed 4x the 129 MB L2"),
-                   "plan_us": round(plan_us, 1), "plan_note": "median host time of the planner call, outside the timed region",
-                   "seed": args.seed,
-                   "timing": ("CUDA events around the K back-to-back calls" if not use_flush else
-                              "CUDA events around each call, after a 256 MiB L2 flush"),
-                   "single_call_p10_us": round(times_ms[len(times_ms) // 10] * 1e3, 2),
-                   "single_call_p90_us": round(times_ms[(9 * len(times_ms)) // 10] * 1e3, 2)},
-        "roofline": {"bound": "hbm", "kernel": decode_kernel_name(w, dec.sched),
-                     "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": "measured hbm_gbs (copy, burst)" if peaks else "fallback 6.8 TB/s",
-                     "traffic": (profiled_traffic(profile_name(args.workload, args.kv_layout, args.page_size,
-                                                               decode_kernel_name(w, dec.sched)),
-                                                  w.d, la.la_schedule_export(dec.sched)[4])
-                                 if args.kernel == "lean" and args.heads_per_unit == 0 else None),
-                     "algorithmic_bytes_per_launch": algo_bytes,
-                     "workspace_bytes_per_call": ws_bytes,
-                     "workspace_frac_of_kv": round(ws_bytes / kv_bytes, 6)},
+        "config": config,
+        "run": run,
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "table_tile_us": variants.get("table_tile", {}).get("us_per_call"),
+        "variants": variants,
+        "configs": configs,
         "cta_trace": cta_trace,
-        "gpu_launches": args.steps * launches_per_call,
-        "clocks": sampler.summary(wall0, wall1),
+        "gpu_launches": args.steps * launches,
+        "clocks": sampler.summary(marks["load0"], marks["t0"], marks["t1"]),
     }
     print(json.dumps(line), flush=True)
 

@@ -90,6 +90,14 @@ def named(name, seed=0):
         return Workload(name, 16, 32, 32, 128, "bf16", lens,
                         description="ragged batch: 16 requests, 32/32 heads, d 128, ctx "
                                     "log-uniform in [1024, 131072], bf16")
+    if name == "ragged_div5":
+        # the ragged batch with every length divided by 5 (1.74 GB of K+V
+        # instead of 8.7): the same mix of short and long requests at a size
+        # a many-pass profiler capture can hold
+        lens = [max(1, n // 5) for n in ragged_lengths(16, 1024, 131072, seed, log_uniform=True)]
+        return Workload(name, 16, 32, 32, 128, "bf16", lens,
+                        description="ragged batch, lengths / 5: 16 requests, 32/32 heads, d 128, ctx "
+                                    "log-uniform in [1024, 131072] divided by 5, bf16")
     if name == "gqa":
         lens = ragged_lengths(8, 16384, 65536, seed, log_uniform=False)
         return Workload(name, 8, 64, 8, 64, "bf16", lens, outlier_frac=0.01,
