@@ -405,6 +405,8 @@ namespace la {
 
 int cached_capacity(int d, int T, int grp, int hp, int* per_sm) { return capacity(d, T, grp, per_sm, hp); }
 
+
+
 int device_sm_count(int* sms) { return device_sms(sms); }
 
 int slab_tile(int d, int rows) { return (d == 128 && rows <= 2) ? 64 : default_tile(d); }
@@ -796,9 +798,10 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
   p.cta_seg = s->dev + s->off_cta_seg;
   p.segs = s->dev + s->off_segs;
   p.out = out;
+  const la::WsLayout wl = la::workspace_layout(s->G, s->d, s->R * s->hp);
   p.hdr = reinterpret_cast<uint32_t*>(ws);
-  p.flags = reinterpret_cast<uint32_t*>(ws + la::kHeaderBytes);
-  p.recs = reinterpret_cast<float*>(ws + la::kHeaderBytes + la::flags_bytes(s->G));
+  p.flags = reinterpret_cast<uint32_t*>(ws + wl.flags);
+  p.recs = reinterpret_cast<float*>(ws + wl.recs);
   p.kv_rows = (long long)s->hkv * s->cu[s->batch];
   p.G = s->G;
   p.batch = s->batch;

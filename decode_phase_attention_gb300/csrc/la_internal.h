@@ -27,19 +27,41 @@ enum KvLayout : int {
 };
 
 // Workspace: a 256-byte header, G ready flags (padded to 256 bytes), then G
-// partial records of rows * (d + 2) floats, per query row [m, l, O[d]]
-// (rows = the instance's rows per kv head x kv heads per unit), each record
-// padded to a multiple of 4 floats so that records can be moved as 16-byte
-// vectors.
+// partial records (one per CTA: a CTA has at most one non-host or
+// fixed-split piece, its first segment), each of rows * (d + 4) floats for
+// the 16-row kernel (per query row [m, l, 0, 0, O[d]]; rows = the
+// instance's rows per kv head x kv heads per unit) or the tcgen05 kernel's
+// column-major layout.
 constexpr size_t kHeaderBytes = 256;
 enum HeaderWord { kEpoch = 0, kDone = 1, kStatus = 2, kInfoCta = 3, kInfoPeer = 4 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline size_t flags_bytes(int G) { return align_up(sizeof(uint32_t) * (size_t)G, 256); }
-__host__ __device__ constexpr int record_stride(int d, int rows) { return (rows * (d + 2) + 3) / 4 * 4; }
-inline size_t record_floats(int d, int rows) { return (size_t)record_stride(d, rows); }
+// Records of the 16-row kernel hold rows of [m, l, 0, 0, O[d]] (O 16-byte
+// aligned, so that partials move as 16-byte vectors); the tcgen05 kernel's
+// hold columns [m], [l], [O dim c] over the unit's rows (128-row instance),
+// padded to a multiple of 4 floats.
+constexpr int kRecO = 4;  // offset of O in a row of a 16-row kernel record
+__host__ __device__ constexpr int record_stride(int d, int rows) { return rows * (d + kRecO); }
+__host__ __device__ constexpr int record_stride_wide(int d, int rows) { return (rows * (d + 2) + 3) / 4 * 4; }
+constexpr int kWideInstanceRows = 128;  // rows of the tcgen05 kernel's instance (kWideRows)
+inline size_t record_floats(int d, int rows) {
+  return (size_t)(rows >= kWideInstanceRows ? record_stride_wide(d, rows) : record_stride(d, rows));
+}
+inline size_t records_bytes(int G, int d, int rows) { return sizeof(float) * record_floats(d, rows) * (size_t)G; }
 inline size_t workspace_bytes(int G, int d, int rows) {
-  return kHeaderBytes + flags_bytes(G) + sizeof(float) * record_floats(d, rows) * (size_t)G;
+  return kHeaderBytes + flags_bytes(G) + records_bytes(G, d, rows);
+}
+// Byte offsets of the flags and the records inside a workspace.
+struct WsLayout {
+  size_t flags, recs, end;
+};
+inline WsLayout workspace_layout(int G, int d, int rows) {
+  WsLayout w;
+  w.flags = kHeaderBytes;
+  w.recs = w.flags + flags_bytes(G);
+  w.end = w.recs + records_bytes(G, d, rows);
+  return w;
 }
 
 struct KParams {

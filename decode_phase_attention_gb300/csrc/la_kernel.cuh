@@ -236,8 +236,8 @@ struct Elem<__half> {
 };
 
 // ------------------------------------------------------------ configuration
-constexpr int cmin(int a, int b) { return a < b ? a : b; }
-constexpr int cmax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+__host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 template <int D, int T_, int GRP, int HP = 1>
 struct Cfg {
@@ -268,7 +268,7 @@ struct Cfg {
   static constexpr int NB8 = (GRP + 7) / 8;         // 8-row blocks of the tensor-core path
   static constexpr int TILE_ELEMS = ROWS * D;
   static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
-  static constexpr int REC = D + 2;                 // [m, l, O[d]]
+  static constexpr int REC = D + kRecO;             // [m, l, 0, 0, O[d]]
   static constexpr int RS = record_stride(D, HP * GRP);  // floats per CTA record in the workspace
   static constexpr size_t MERGE_BYTES = (size_t)NCW * GRP * REC * 4;
   // shared memory for a ring of 2-4 stages within 192 KiB (less when a large
@@ -277,18 +277,31 @@ struct Cfg {
   static constexpr int RING_ROOM = cmin(196608, 232448 - (int)MERGE_BYTES - (2 * 4 * 8 + 16) - 1024);
   static constexpr int STAGES = cmax(2, cmin(4, RING_ROOM / STAGE_BYTES));
   static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
-  static constexpr size_t BAR_BYTES = 2 * STAGES * 8 + 16;
+  static constexpr size_t BAR_BYTES = 2 * STAGES * 8 + 16 + 16;  // full, empty, 2 flag words, 2 staging barriers
   static constexpr size_t SMEM = KV_BYTES + MERGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
-  static constexpr int ITEMS = (HP * GRP * D + NCT - 1) / NCT;  // (row, dim) outputs per consumer thread
-  static constexpr int PB = cmax(1, cmin(4, 16 / ITEMS));  // peer records per batch of host-merge loads
-  // peer records the idle ring and merge area can hold (they are contiguous)
-  static constexpr int STAGE_RECS = (int)((KV_BYTES + MERGE_BYTES) / (RS * 4));
+  static constexpr int V4 = (HP * GRP * D / 4 + NCT - 1) / NCT;  // vectors of 4 (row, dim) outputs per consumer thread
+  static constexpr int PB = cmax(1, cmin(4, 4 / V4));  // peer records per batch of host-merge loads
+  // Host merge of many peers, in the idle ring and merge area (contiguous):
+  // two buffers of up to NBAT staged peer records, then per-row scalars
+  // (running maximum, running l, this batch's rescale, NBAT peer weights).
+  static constexpr int MROWS = HP * GRP;            // record rows
+  static constexpr int NBAT_MAX = 64;
+  static constexpr size_t SCAL_BYTES = ((size_t)MROWS * (3 + NBAT_MAX) * 4 + 15) / 16 * 16;
+  static constexpr int NBAT = cmin(NBAT_MAX, (int)((KV_BYTES + MERGE_BYTES - SCAL_BYTES) / (2 * RS * 4)));
+  static constexpr size_t SCAL_OFF = (size_t)2 * NBAT * RS * 4;
   static_assert(D % 16 == 0 && T % 16 == 0, "tile shape");
   static_assert((HP == 1 || HP == 2 || HP == 4 || HP == 8) && NCW % HP == 0 && T % WPH == 0, "kv heads per unit");
   static_assert(STEPS % CH == 0 && TPW % TPS == 0, "CUDA-core tile shape");
   static_assert(!TC || (TPW % 16 == 0 && (GRP <= 8 || GRP % 8 == 0) && GRP <= 16), "tensor-core tile shape");
   static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(NBAT >= 1 && SCAL_OFF + SCAL_BYTES <= KV_BYTES + MERGE_BYTES, "host-merge staging");
 };
+
+// a * x + y and a * x on 4-vectors.
+__device__ __forceinline__ float4 fma4(float a, float4 x, float4 y) {
+  return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+}
+__device__ __forceinline__ float4 scale4(float a, float4 x) { return make_float4(a * x.x, a * x.y, a * x.z, a * x.w); }
 
 // Output element store (fp32, fp16 or bf16, chosen per call).
 __device__ __forceinline__ void store_out(void* out, size_t idx, float v, int out_dtype) {
@@ -298,6 +311,21 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, int ou
     static_cast<__half*>(out)[idx] = __float2half_rn(v);
   else
     static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+}
+// Four consecutive outputs (idx a multiple of 4) as fp32, fp16 or bf16.
+__device__ __forceinline__ void store_out4(void* out, size_t idx, float a, float b, float c, float d,
+                                           int out_dtype) {
+  if (out_dtype == 0) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = make_float4(a, b, c, d);
+  } else if (out_dtype == 1) {
+    __half2 x = __floats2half2_rn(a, b), y = __floats2half2_rn(c, d);
+    *reinterpret_cast<uint2*>(static_cast<__half*>(out) + idx) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&x), *reinterpret_cast<uint32_t*>(&y));
+  } else {
+    __nv_bfloat162 x = __floats2bfloat162_rn(a, b), y = __floats2bfloat162_rn(c, d);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + idx) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&x), *reinterpret_cast<uint32_t*>(&y));
+  }
 }
 
 // Element offset / D of query row r of unit (b, kvh) in q and out
@@ -651,7 +679,7 @@ __device__ __forceinline__ void warp_segment_cc(const KParams& p, int g, int b, 
         r[1] = l[j];
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) r[2 + c0 + e] = o[j][e];
+      for (int e = 0; e < 8; ++e) r[kRecO + c0 + e] = o[j][e];
     }
   }
 }
@@ -851,8 +879,8 @@ __device__ __forceinline__ void warp_segment_tc(const KParams& p, int g, int b, 
         }
 #pragma unroll
         for (int dm = 0; dm < C::KS; ++dm) {
-          r[2 + dm * 16 + gq] = o[nb][dm][h];
-          r[2 + dm * 16 + gq + 8] = o[nb][dm][2 + h];
+          r[kRecO + dm * 16 + gq] = o[nb][dm][h];
+          r[kRecO + dm * 16 + gq + 8] = o[nb][dm][2 + h];
         }
       }
     }
@@ -871,17 +899,28 @@ __device__ __forceinline__ void merge_f(float& M, float& Ls, float& O, float m2,
   O = a * O + bw * o2;
   M = mn;
 }
+// The same for 4 outputs of one row (one m and l).
+__device__ __forceinline__ void merge_f4(float& M, float& Ls, float4& O, float m2, float l2, float4 o2) {
+  const float mn = fmaxf(M, m2);
+  if (mn == -INFINITY) return;
+  const float a = (M == -INFINITY) ? 0.f : ex2(M - mn);
+  const float bw = (m2 == -INFINITY) ? 0.f : ex2(m2 - mn);
+  Ls = a * Ls + bw * l2;
+  O = fma4(bw, o2, scale4(a, O));
+  M = mn;
+}
 
 template <int D, int T, int GRP, typename E, int HP>
-__device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t* full, uint64_t* empty,
+__device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t* full, uint64_t* empty, uint64_t* stg,
                                         float* mrg, volatile int* abort_flag, uint32_t epoch) {
   using C = Cfg<D, T, GRP, HP>;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
   const uint32_t ready = epoch + 1u;
-  // Outputs of a unit: item idx -> record row rr = idx / D = hh * GRP + j
+  // Outputs of a unit: output idx -> record row rr = idx / D = hh * GRP + j
   // (kv head hh of the unit, query row j, live when j < rows) and dim idx % D.
   constexpr int kItems = HP * GRP * D;
+  constexpr int kVecs = kItems / 4;  // vectors of 4 consecutive outputs
   const int groups = p.hkv / HP;  // units per request
   int stage = 0;
   uint32_t phase = 0;
@@ -937,28 +976,34 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
     }
     consumer_sync(C::NCT);
 
-    // ---- merge the warps of each kv head with f: thread -> (head, row, dim) items
-    float M[C::ITEMS], Lsum[C::ITEMS], O[C::ITEMS];
+    // ---- merge the warps of each kv head with f. Each thread takes
+    // vectors of 4 consecutive outputs: vector v covers record row
+    // rr = 4v / D (kv head hh = rr / GRP of the unit, query row j = rr % GRP,
+    // live when j < rows) and dims 4v % D .. + 3, so that records move as
+    // 16-byte loads and stores (O starts 16-byte aligned in every row).
+    float M[C::V4], Lsum[C::V4];
+    float4 O[C::V4];
 #pragma unroll
-    for (int i = 0; i < C::ITEMS; ++i) {
-      const int idx = tid + i * C::NCT;
-      const int rr = idx / D, cc = idx % D, hh = rr / GRP, j = rr % GRP;
+    for (int i = 0; i < C::V4; ++i) {
+      const int v = tid + i * C::NCT;
+      const int rr = 4 * v / D, cc = 4 * v % D, hh = rr / GRP, j = rr % GRP;
       M[i] = -INFINITY;
       Lsum[i] = 0.f;
-      O[i] = 0.f;
-      if (idx < kItems && j < p.rows) {
+      O[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (v < kVecs && j < p.rows) {
         const float* base = mrg + ((size_t)hh * C::WPH * GRP + j) * C::REC;
         float mm = -INFINITY;
 #pragma unroll
         for (int w = 0; w < C::WPH; ++w) mm = fmaxf(mm, base[w * GRP * C::REC]);
         if (mm != -INFINITY) {
-          float ls = 0.f, os = 0.f;
+          float ls = 0.f;
+          float4 os = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int w = 0; w < C::WPH; ++w) {
             const float* r = base + w * GRP * C::REC;
             const float wt = (r[0] == -INFINITY) ? 0.f : ex2(r[0] - mm);
             ls = fmaf(wt, r[1], ls);
-            os = fmaf(wt, r[2 + cc], os);
+            os = fma4(wt, *reinterpret_cast<const float4*>(r + kRecO + cc), os);
           }
           M[i] = mm;
           Lsum[i] = ls;
@@ -971,16 +1016,14 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
     if (kind == kNonHost || kind == kPartial) {
       float* rec = p.recs + (size_t)g * C::RS;
 #pragma unroll
-      for (int i = 0; i < C::ITEMS; ++i) {
-        const int idx = tid + i * C::NCT;
-        const int rr = idx / D, cc = idx % D;
-        if (idx < kItems && rr % GRP < p.rows) {
+      for (int i = 0; i < C::V4; ++i) {
+        const int v = tid + i * C::NCT;
+        const int rr = 4 * v / D, cc = 4 * v % D;
+        if (v < kVecs && rr % GRP < p.rows) {
           float* r = rec + rr * C::REC;
-          r[2 + cc] = O[i];
-          if (cc == 0) {
-            r[0] = poisoned ? __int_as_float(0x7fc00000) : M[i];
-            r[1] = Lsum[i];
-          }
+          *reinterpret_cast<float4*>(r + kRecO + cc) = O[i];
+          if (cc == 0)
+            *reinterpret_cast<float4*>(r) = make_float4(poisoned ? __int_as_float(0x7fc00000) : M[i], Lsum[i], 0.f, 0.f);
         }
       }
       __threadfence();
@@ -1018,85 +1061,179 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
           if (si == s_end - 1 && npeer > C::PB) {
             // Many peers, and the CTA's last segment: every tile has been
             // consumed and the producer issues no more copies, so the ring
-            // and the merge area after it (read above) are idle. Stage the
-            // records of the first peers there, every 16-byte piece in flight
-            // at once (cp.async from L2 into shared memory; the records of
-            // consecutive CTAs are contiguous), then apply f to all of them
-            // at once: the maximum m over the partials, then the weighted
-            // sums of l and O (f is associative, so k partials reduce in one
-            // step).
-            const int ns = npeer < C::STAGE_RECS ? npeer : C::STAGE_RECS;
-            const uint32_t stg = smem_u32(kv);
-            const char* src = reinterpret_cast<const char*>(p.recs + (size_t)(g + 1) * C::RS);
-            const int n4 = ns * (C::RS / 4);
-            for (int i = tid; i < n4; i += C::NCT)
-              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(stg + 16u * (uint32_t)i),
-                           "l"(src + 16 * (size_t)i)
-                           : "memory");
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            consumer_sync(C::NCT);
-            const float* st = reinterpret_cast<const float*>(kv);
+            // and the merge area after it (read above) are idle. The peers'
+            // records come in by bulk copies (one per batch: the records of
+            // consecutive CTAs are contiguous) in batches of up to NBAT into
+            // two buffers, so the next batch's copy overlaps this batch's
+            // merge. f is associative, so a batch of k partials reduces in
+            // one step: per record row, the new maximum and the rescale of
+            // the running partial, then every peer's weight 2^(m - max) --
+            // each computed once per (row, peer) into shared memory -- then
+            // the weighted sums of O (16-byte vectors) and of l.
+            constexpr int kRows = C::MROWS;
+            float* scal = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(kv) + C::SCAL_OFF);
+            float* s_m = scal;              // [kRows] running maximum
+            float* s_a = scal + kRows;      // [kRows] rescale of the running partial in this batch
+            float* s_l = scal + 2 * kRows;  // [kRows] running l
+            float* s_w = scal + 3 * kRows;  // [NBAT][kRows] peer weights of this batch
 #pragma unroll
-            for (int i = 0; i < C::ITEMS; ++i) {
-              const int idx = tid + i * C::NCT;
-              const int rr = idx / D, cc = idx % D;
-              if (!(idx < kItems && rr % GRP < p.rows)) continue;
-              float mm = M[i];
-#pragma unroll 4
-              for (int u = 0; u < ns; ++u) mm = fmaxf(mm, st[u * C::RS + rr * C::REC]);
-              if (mm == -INFINITY) continue;
-              const float a = (M[i] == -INFINITY) ? 0.f : ex2(M[i] - mm);
-              float ls = a * Lsum[i], os = a * O[i];
-#pragma unroll 4
-              for (int u = 0; u < ns; ++u) {
-                const float* r = st + u * C::RS + rr * C::REC;
-                const float w = (r[0] == -INFINITY) ? 0.f : ex2(r[0] - mm);  // NaN m (poisoned) propagates
-                ls = fmaf(w, r[1], ls);
-                os = fmaf(w, r[2 + cc], os);
+            for (int i = 0; i < C::V4; ++i) {
+              const int v = tid + i * C::NCT;
+              if (v < kVecs && 4 * v % D == 0) {
+                s_m[4 * v / D] = M[i];
+                s_l[4 * v / D] = Lsum[i];
               }
-              M[i] = mm;
-              Lsum[i] = ls;
-              O[i] = os;
             }
-            p0 = ns;
+            // A few KB (long MHA contexts: a handful of one-row records)
+            // arrive sooner as every thread's 16-byte copies; more, as one
+            // bulk copy per batch.
+            const bool by_thread = (size_t)npeer * C::RS * 4 <= 32768;
+            auto issue = [&](int first, int n, int buf) {
+              unsigned char* dst = reinterpret_cast<unsigned char*>(kv) + (size_t)buf * C::NBAT * C::RS * 4;
+              const float* src = p.recs + (size_t)(g + 1 + first) * C::RS;
+              if (by_thread) {
+                const uint32_t d0 = smem_u32(dst);
+                for (int i = tid; i < n * (C::RS / 4); i += C::NCT)
+                  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d0 + 16u * (uint32_t)i),
+                               "l"(src + 4 * (size_t)i)
+                               : "memory");
+                asm volatile("cp.async.commit_group;" ::: "memory");
+              } else if (tid == 0) {
+                const uint32_t bytes = (uint32_t)n * (uint32_t)(C::RS * 4);
+                asm volatile("fence.proxy.async.global;" ::: "memory");  // records written by other CTAs
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring was last read here
+                mbar_arrive_expect_tx(&stg[buf], bytes);
+                bulk_g2s(dst, src, bytes, &stg[buf], l2_evict_first_policy());
+              }
+            };
+            const int nbat = (npeer + C::NBAT - 1) / C::NBAT;
+            issue(0, npeer < C::NBAT ? npeer : C::NBAT, 0);
+            bool staged = true;
+            for (int bi = 0; bi < nbat; ++bi) {
+              const int first = bi * C::NBAT;
+              const int n = npeer - first < C::NBAT ? npeer - first : C::NBAT;
+              if (bi + 1 < nbat) {
+                const int rest = npeer - first - C::NBAT;
+                issue(first + C::NBAT, rest < C::NBAT ? rest : C::NBAT, (bi + 1) & 1);
+              }
+              if (by_thread) {
+                if (bi + 1 < nbat)
+                  asm volatile("cp.async.wait_group 1;" ::: "memory");
+                else
+                  asm volatile("cp.async.wait_group 0;" ::: "memory");
+              } else {
+                // an issued copy is waited for (bounded) even after an abort
+                volatile int no_abort = 0;
+                if (!mbar_wait_bounded(&stg[bi & 1], (uint32_t)(bi >> 1) & 1u, &no_abort, p.spin_ns)) staged = false;
+              }
+              consumer_sync(C::NCT);  // batch bi is in shared memory (and s_m, s_l written)
+              const float* st = reinterpret_cast<const float*>(kv) + (size_t)(bi & 1) * C::NBAT * C::RS;
+              // per row, one warp (lanes over the batch's peers): the new
+              // maximum, the rescale of the running partial, every peer's
+              // weight and the new l
+              static_assert(C::NBAT <= 64, "two peers per lane");
+              for (int rr = warp; rr < kRows; rr += C::NCW) {
+                const int lane = tid & 31;
+                const float mo = s_m[rr];
+                float mu[2], lu[2];
+                float mb = mo;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                  const int u = lane + 32 * q;
+                  mu[q] = u < n ? st[u * C::RS + rr * C::REC] : -INFINITY;
+                  lu[q] = u < n ? st[u * C::RS + rr * C::REC + 1] : 0.f;
+                  mb = fmaxf(mb, mu[q]);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
+                float ls = 0.f;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                  const int u = lane + 32 * q;
+                  const float w = (mu[q] == -INFINITY) ? 0.f : ex2(mu[q] - mb);  // NaN m (poisoned) propagates
+                  if (u < n) s_w[u * kRows + rr] = w;
+                  ls = fmaf(w, lu[q], ls);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(kFull, ls, off);
+                if (lane == 0) {
+                  const float a = (mb == -INFINITY || mo == -INFINITY) ? (mb == -INFINITY ? 1.f : 0.f) : ex2(mo - mb);
+                  s_a[rr] = a;
+                  s_m[rr] = mb;
+                  s_l[rr] = fmaf(a, s_l[rr], ls);
+                }
+              }
+              consumer_sync(C::NCT);  // the batch's scalars are in shared memory
+              // the weighted sums of O: peers outer, this thread's vectors
+              // inner (V4 independent chains per step, 16-byte loads)
+              {
+                const float* rp[C::V4];
+                const float* wp[C::V4];
+#pragma unroll
+                for (int i = 0; i < C::V4; ++i) {
+                  const int v = tid + i * C::NCT;
+                  const int rr = v < kVecs ? 4 * v / D : 0, cc = 4 * v % D;
+                  rp[i] = st + rr * C::REC + kRecO + cc;
+                  wp[i] = s_w + rr;
+                  O[i] = scale4(s_a[rr], O[i]);
+                }
+#pragma unroll 2
+                for (int u = 0; u < n; ++u) {
+#pragma unroll
+                  for (int i = 0; i < C::V4; ++i)
+                    O[i] = fma4(wp[i][u * kRows], *reinterpret_cast<const float4*>(rp[i] + u * C::RS), O[i]);
+                }
+              }
+              consumer_sync(C::NCT);  // buffer bi & 1, the scalars and s_l are settled
+            }
+            if (!staged) fail = true;
+#pragma unroll
+            for (int i = 0; i < C::V4; ++i) {
+              const int v = tid + i * C::NCT;
+              if (v < kVecs) Lsum[i] = s_l[4 * v / D];
+            }
+            p0 = npeer;
           }
           // Few peers (or peers beyond the staged ones): the loads of PB
           // peers for all of this thread's outputs are issued before any of
           // them is used, so a batch costs one L2 round trip.
           for (; p0 < npeer; p0 += C::PB) {
-            float m2[C::ITEMS][C::PB], l2[C::ITEMS][C::PB], o2[C::ITEMS][C::PB];
+            float m2[C::V4][C::PB], l2[C::V4][C::PB];
+            float4 o2[C::V4][C::PB];
 #pragma unroll
-            for (int i = 0; i < C::ITEMS; ++i) {
-              const int idx = tid + i * C::NCT;
-              const int rr = idx / D, cc = idx % D;
+            for (int i = 0; i < C::V4; ++i) {
+              const int v = tid + i * C::NCT;
+              const int rr = 4 * v / D, cc = 4 * v % D;
 #pragma unroll
               for (int u = 0; u < C::PB; ++u) {
                 m2[i][u] = -INFINITY;
                 l2[i][u] = 0.f;
-                o2[i][u] = 0.f;
-                if (idx < kItems && rr % GRP < p.rows && p0 + u < npeer) {
+                o2[i][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (v < kVecs && rr % GRP < p.rows && p0 + u < npeer) {
                   const float* r = p.recs + (size_t)(g + 1 + p0 + u) * C::RS + rr * C::REC;
                   m2[i][u] = __ldcg(r);
                   l2[i][u] = __ldcg(r + 1);
-                  o2[i][u] = __ldcg(r + 2 + cc);
+                  o2[i][u] = __ldcg(reinterpret_cast<const float4*>(r + kRecO + cc));
                 }
               }
             }
 #pragma unroll
-            for (int i = 0; i < C::ITEMS; ++i)
+            for (int i = 0; i < C::V4; ++i)
 #pragma unroll
-              for (int u = 0; u < C::PB; ++u) merge_f(M[i], Lsum[i], O[i], m2[i][u], l2[i][u], o2[i][u]);
+              for (int u = 0; u < C::PB; ++u) merge_f4(M[i], Lsum[i], O[i], m2[i][u], l2[i][u], o2[i][u]);
           }
         }
       }
       // normalise and store: O = Obar / l
 #pragma unroll
-      for (int i = 0; i < C::ITEMS; ++i) {
-        const int idx = tid + i * C::NCT;
-        const int rr = idx / D, cc = idx % D;
-        if (idx < kItems && rr % GRP < p.rows) {
-          const float val = fail ? __int_as_float(0x7fc00000) : O[i] / Lsum[i];
-          store_out(p.out, row_index(p, b, kvh0 + rr / GRP, rr % GRP) * D + cc, val, p.out_dtype);
+      for (int i = 0; i < C::V4; ++i) {
+        const int v = tid + i * C::NCT;
+        const int rr = 4 * v / D, cc = 4 * v % D;
+        if (v < kVecs && rr % GRP < p.rows) {
+          const float nan = __int_as_float(0x7fc00000);
+          const float inv = 1.f / Lsum[i];
+          store_out4(p.out, row_index(p, b, kvh0 + rr / GRP, rr % GRP) * D + cc, fail ? nan : O[i].x * inv,
+                     fail ? nan : O[i].y * inv, fail ? nan : O[i].z * inv, fail ? nan : O[i].w * inv, p.out_dtype);
         }
       }
     }
@@ -1119,6 +1256,7 @@ __global__ void __launch_bounds__(Cfg<D, T, GRP, HP>::NTHREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::KV_BYTES + C::MERGE_BYTES);
   uint64_t* empty = full + C::STAGES;
   volatile int* flags_smem = reinterpret_cast<volatile int*>(empty + C::STAGES);  // [0] abort, [1] spare
+  uint64_t* stg = empty + C::STAGES + 1;  // two barriers of the host merge's staged copies
 
   const int tid = threadIdx.x;
   const int g = blockIdx.x;
@@ -1135,6 +1273,8 @@ __global__ void __launch_bounds__(Cfg<D, T, GRP, HP>::NTHREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C::NCW);
     }
+    mbar_init(&stg[0], 1);
+    mbar_init(&stg[1], 1);
     flags_smem[0] = 0;
     flags_smem[1] = 0;
     fence_mbar_init();
@@ -1145,7 +1285,7 @@ __global__ void __launch_bounds__(Cfg<D, T, GRP, HP>::NTHREADS, 1)
   if ((tid >> 5) == C::NCW) {
     produce<C, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
   } else {
-    consume<D, T, GRP, E, HP>(p, g, kv, full, empty, mrg, flags_smem, epoch);
+    consume<D, T, GRP, E, HP>(p, g, kv, full, empty, stg, mrg, flags_smem, epoch);
   }
   __syncthreads();
   if (tid == 0) {
@@ -1166,7 +1306,7 @@ __global__ void __launch_bounds__(Cfg<D, T, GRP, HP>::NTHREADS, 1)
 // (unit, query head of the group), one thread per dimension).
 template <int D, int GRP>
 __global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
-  constexpr int REC = D + 2;
+  constexpr int REC = D + kRecO;
   const int row = blockIdx.x;  // unit * GRP + j
   const int unit = row / GRP, j = row % GRP;
   const int c = threadIdx.x;
@@ -1176,7 +1316,7 @@ __global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
   float M = -INFINITY, Ls = 0.f, O = 0.f;
   for (int s = h0; s <= h1; ++s) {
     const float* r = p.recs + (size_t)s * record_stride(D, GRP) + j * REC;
-    const float m2 = r[0], l2 = r[1], o2 = r[2 + c];
+    const float m2 = r[0], l2 = r[1], o2 = r[kRecO + c];
     const float mn = fmaxf(M, m2);
     if (mn == -INFINITY) continue;
     const float a = (M == -INFINITY) ? 0.f : ex2(M - mn);

@@ -49,16 +49,14 @@ la_status scratch_address(int dev, void** out) {
 }
 
 struct Layout {
-  size_t flags, recs, cu, cta_seg, segs, host, fin, total;
+  la::WsLayout ws;
+  size_t cu, cta_seg, segs, host, fin, total;
 };
 
 Layout layout_of(const la_schedule* s) {
   Layout L;
-  size_t off = la::kHeaderBytes;
-  L.flags = off;
-  off += la::flags_bytes(s->G);
-  L.recs = off;
-  off = la::align_up(off + sizeof(float) * la::record_floats(s->d, s->R * s->hp) * (size_t)s->G, 256);
+  L.ws = la::workspace_layout(s->G, s->d, s->R * s->hp);  // header, flags and records as in a workspace
+  size_t off = la::align_up(L.ws.end, 256);
   auto table = [&off](size_t words) {
     const size_t at = off;
     off = la::align_up(off + words * sizeof(int32_t), 16);
@@ -116,7 +114,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   // The array keeps whatever the previous call left: clear the header
   // (epoch, done counter, status) and the ready flags; copy the tables
   // unless this device's array already holds this schedule's.
-  if (cudaMemsetAsync(base, 0, L.recs, st) != cudaSuccess) return LA_ERR_CUDA;
+  if (cudaMemsetAsync(base, 0, L.ws.recs, st) != cudaSuccess) return LA_ERR_CUDA;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     Held& h = g_held[dev];
@@ -141,8 +139,8 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   p.segs = reinterpret_cast<const int32_t*>(base + L.segs);
   p.out = out;
   p.hdr = reinterpret_cast<uint32_t*>(base);
-  p.flags = reinterpret_cast<uint32_t*>(base + L.flags);
-  p.recs = reinterpret_cast<float*>(base + L.recs);
+  p.flags = reinterpret_cast<uint32_t*>(base + L.ws.flags);
+  p.recs = reinterpret_cast<float*>(base + L.ws.recs);
   p.kv_rows = (long long)s->hkv * s->cu[s->batch];
   p.G = s->G;
   p.batch = s->batch;

@@ -137,22 +137,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 // The 16 softmax warps (named barrier 1).
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
-// Four consecutive outputs (idx a multiple of 4) as fp32, fp16 or bf16.
-__device__ __forceinline__ void store_out4(void* out, size_t idx, float a, float b, float c, float d,
-                                           int out_dtype) {
-  if (out_dtype == 0) {
-    *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = make_float4(a, b, c, d);
-  } else if (out_dtype == 1) {
-    __half2 x = __floats2half2_rn(a, b), y = __floats2half2_rn(c, d);
-    *reinterpret_cast<uint2*>(static_cast<__half*>(out) + idx) =
-        make_uint2(*reinterpret_cast<uint32_t*>(&x), *reinterpret_cast<uint32_t*>(&y));
-  } else {
-    __nv_bfloat162 x = __floats2bfloat162_rn(a, b), y = __floats2bfloat162_rn(c, d);
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + idx) =
-        make_uint2(*reinterpret_cast<uint32_t*>(&x), *reinterpret_cast<uint32_t*>(&y));
-  }
-}
-
 // Shared-memory matrix descriptor of a tcgen05 operand in a swizzled
 // layout (rows of 128 or 64 bytes, 8-row atoms of 1024 or 512 bytes, atoms
 // aligned to their size): start address, leading and stride byte offsets,
@@ -188,7 +172,7 @@ struct WCfg {
   static constexpr uint64_t SWZ = W == 64 ? 2 : 4;  // descriptor swizzle mode
   static constexpr int KPB = W / 16;            // MMA k-steps (16 head dims, 32 bytes) per box row
   static constexpr int REC = D + 2;
-  static constexpr int RS = record_stride(D, M);
+  static constexpr int RS = record_stride_wide(D, M);
   static constexpr int NSW = 16;                // softmax warps: 4 per TMEM lane quadrant
   // partial row maxima (two tiles), partial sums of l, O quarters handed between lane replicas ([64][65])
   static constexpr int RED_BYTES = 3 * 4 * M * 4 + 64 * 65 * 4;
@@ -203,6 +187,7 @@ struct WCfg {
   static constexpr uint32_t O_COL = NSB * T;    // S / P buffers first, then O
   static constexpr uint32_t Q_COL = O_COL + D;  // then Q
   static_assert(D == 64 || D == 96 || D == 128, "head dims of the wide kernel");
+  static_assert(M == kWideInstanceRows, "record layout of the wide kernel");
   static_assert(STAGES >= 2 && SMEM <= 232448, "shared memory per CTA");
   static_assert(NBARS * 8 + 16 <= 256, "barrier area");
   static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor memory columns");
@@ -594,7 +579,6 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
       }
     }
     const bool poisoned = (*abort_flag != 0) || !ok || !have_o;
-
     // Records are column-major over the unit's rows (wide_rec): element
     // (col, r) at [col * rows + r], col 0 = m, 1 = l, 2 + c = O dim c, so
     // that a warp's 32 rows read and write whole 128-byte lines.
@@ -650,6 +634,7 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
         for (int p0 = 0; p0 < npeer; p0 += cap) {
           const int nb = npeer - p0 < cap ? npeer - p0 : cap;
           if (tid == 0 && !*abort_flag) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // records written by other CTAs
             mbar_arrive_expect_tx(stg, (uint32_t)nb * rec_bytes);
             for (int k = 0; k < nb; ++k)
               bulk_g2s(reinterpret_cast<unsigned char*>(kv) + (size_t)k * rec_bytes,

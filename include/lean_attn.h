@@ -199,12 +199,12 @@ int la_schedule_grid(const la_schedule* s);
 
 /*
  * Bytes of device workspace la_decode needs for this schedule: a header, G
- * ready flags and G partial records of rows * (d + 2) floats, rounded up to
- * a multiple of 4 floats (rows = query rows per unit head -- a kv head or
- * one query block of one -- rounded up to 1, 2, 4, 8, 16, or 128 on the
- * tcgen05 kernel, times the kv heads per unit) ("7.4
- * limitations": a small amount of global memory for sharing partial
- * results). Zero it once (la_workspace_init) before its first use; after
+ * ready flags and G partial records ("7.4 limitations": a small amount of
+ * global memory for sharing partial results). A record holds rows rows of
+ * [m, l, 0, 0, O[d]] floats (rows = query rows per unit head -- a kv head
+ * or one query block of one -- rounded up to 1, 2, 4, 8 or 16, times the kv
+ * heads per unit), or, on the tcgen05 kernel (128 rows), the same triples
+ * column-major over the rows, rounded up to a multiple of 4 floats. Zero it once (la_workspace_init) before its first use; after
  * that it needs no clearing between calls. One workspace must not be used
  * by two launches that can run at the same time.
  */

@@ -171,11 +171,11 @@ def test_decode_host_rejects_bad_arguments_before_any_copy():
 
 def test_workspace_size_formula():
     s = la.la_plan(1, 4, 4, 64, [0, 1024], 3)
-    # header 256 + flags (3 words padded to 256) + 3 records of 1 x (64 + 2)
-    # floats, each padded to a multiple of 4 floats (68)
+    # header 256 + flags (3 words padded to 256) + 3 records of 1 row of
+    # [m, l, 0, 0, O[64]] (68 floats)
     assert la.la_workspace_size(s) == 256 + 256 + 3 * 68 * 4
     g = la.la_plan(2, 16, 2, 128, [0, 100, 300], 5)
-    assert la.la_workspace_size(g) == 256 + 256 + 5 * 8 * 130 * 4
+    assert la.la_workspace_size(g) == 256 + 256 + 5 * 8 * 132 * 4
 
 
 def test_export_size_and_short_buffer():
@@ -264,7 +264,7 @@ def test_spec_schedule_matches_the_decode_plan_and_sizes_its_records():
     assert s.nq == 3
     assert la.la_schedule_export(s) == P.export(P.plan_lean(3, 4, 2, 128, cu_of(lengths), 11))
     # grp 2 x nq 3 = 6 query rows per unit: records of 8 rows (the instance's row count)
-    assert la.la_workspace_size(s) == 256 + 256 + 11 * 8 * 130 * 4
+    assert la.la_workspace_size(s) == 256 + 256 + 11 * 8 * 132 * 4
 
 
 @pytest.mark.parametrize("hq,hkv,nq,lengths,status", [
@@ -327,7 +327,7 @@ def test_two_head_records_hold_both_heads():
     # d 64, grp 4, nq 2: 8 query rows per kv head, two kv heads per unit
     s = la.la_plan_kv(2, 16, 4, 64, [0, 300, 700], nq=2, num_sms=9)
     assert s.heads_per_unit == 2
-    assert la.la_workspace_size(s) == 256 + 256 + 9 * 2 * 8 * 66 * 4
+    assert la.la_workspace_size(s) == 256 + 256 + 9 * 2 * 8 * 68 * 4
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -379,9 +379,9 @@ def test_sixteen_query_rows_per_kv_head():
     s = la.la_plan(2, 32, 2, 128, [0, 900, 1000], 7)
     assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 32, 2, 128, [0, 900, 1000], 7, 128))
     # records hold 16 rows of (d + 2) floats
-    assert la.la_workspace_size(s) == 256 + 256 + 7 * 16 * 130 * 4
+    assert la.la_workspace_size(s) == 256 + 256 + 7 * 16 * 132 * 4
     sp = la.la_plan_spec(2, 16, 2, 64, 2, [0, 900, 1000], 7)
-    assert la.la_workspace_size(sp) == 256 + 256 + 7 * 16 * 66 * 4
+    assert la.la_workspace_size(sp) == 256 + 256 + 7 * 16 * 68 * 4
     # caches: units of one kv head once a kv head has more than 8 rows
     assert la.la_plan_kv(1, 32, 2, 64, [0, 900], num_sms=7).heads_per_unit == 1
     assert la.la_plan_kv(1, 16, 2, 64, [0, 900], num_sms=7).heads_per_unit == 2
@@ -394,7 +394,7 @@ def test_groups_that_are_not_powers_of_two(grp):
     s = la.la_plan(3, 2 * grp, 2, 128, cu_of(lengths), 11)
     assert la.la_schedule_export(s) == P.export(P.plan_lean(3, 2 * grp, 2, 128, cu_of(lengths), 11, 128))
     R = 4 if grp <= 4 else 8 if grp <= 8 else 16
-    assert la.la_workspace_size(s) == 256 + 256 + 11 * R * 130 * 4
+    assert la.la_workspace_size(s) == 256 + 256 + 11 * R * 132 * 4
 
 
 # ---- query blocks: more query rows per kv head than one unit holds
@@ -423,7 +423,9 @@ def test_query_blocks_are_units_of_their_own(d, grp, nq, qb, R):
     s = la.la_plan_spec(3, hkv * grp, hkv, d, nq, cu_of(lengths), G)
     assert s.query_blocks == qb and s.heads_per_unit == 1
     assert la.la_schedule_export(s) == P.export(P.plan_lean(3, hkv * grp, hkv * qb, d, cu_of(lengths), G, T))
-    rec = -(-R * (d + 2) // 4) * 4  # a record: R rows of (d + 2) floats, padded to 16 bytes
+    # a record: R rows of [m, l, 0, 0, O[d]] on the 16-row kernel; on the
+    # tcgen05 kernel (R = 128) columns over the rows, padded to 16 bytes
+    rec = R * (d + 4) if R < 128 else -(-R * (d + 2) // 4) * 4
     assert la.la_workspace_size(s) == 256 + 256 + G * rec * 4
     if nq == 1:
         assert la.la_schedule_export(la.la_plan(3, hkv * grp, hkv, d, cu_of(lengths), G)) \
