@@ -177,7 +177,7 @@ struct WCfg {
   // partial row maxima (two tiles), partial sums of l, O quarters handed between lane replicas ([64][65])
   static constexpr int RED_BYTES = 3 * 4 * M * 4 + 64 * 65 * 4;
   static constexpr int NSB = 3 * T + D + D / 2 <= 512 ? 3 : 2;  // S / P buffers in TMEM
-  static constexpr int NBARS = 2 * 6 + 3 * NSB + 3;  // full, empty (<= 6 stages), s_full, p_full, pv_done, q_ready, drain, stg
+  static constexpr int NBARS = 2 * 6 + 3 * NSB + 4;  // full, empty (<= 6 stages), s_full, p_full, pv_done, q_ready, drain, stg[2]
   static constexpr int STAGES = cmin(6, (232448 - RED_BYTES - 1024 - 256) / STAGE_BYTES);
   static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
   // + exchange area, barriers, TMEM slot, flags; alignment slack
@@ -189,7 +189,7 @@ struct WCfg {
   static_assert(D == 64 || D == 96 || D == 128, "head dims of the wide kernel");
   static_assert(M == kWideInstanceRows, "record layout of the wide kernel");
   static_assert(STAGES >= 2 && SMEM <= 232448, "shared memory per CTA");
-  static_assert(NBARS * 8 + 16 <= 256, "barrier area");
+  static_assert(NBARS * 8 + 8 + 12 <= 256, "barrier area");  // barriers, TMEM slot, 3 flag words
   static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor memory columns");
 };
 
@@ -327,7 +327,7 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
                                              uint64_t* full, uint64_t* s_full, uint64_t* p_full,
                                              uint64_t* pv_done, uint64_t* q_ready, uint64_t* stg,
                                              uint32_t tmem, volatile int* abort_flag, uint32_t epoch) {
-  volatile int* flags_smem_copies = abort_flag + 1;  // staging copies issued in this batch
+  volatile int* flags_smem_copies = abort_flag + 1;  // [2]: staging copies issued into each half of the ring
   using C = WCfg<D>;
   constexpr int T = C::T;
   constexpr int OQ = D / 4;  // head dims of O per thread
@@ -560,131 +560,312 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
     tc_fence_before();
     lsum[(half * 4 + cq) * RM + row] = lq;
     softmax_sync();  // every warp's waits are over; the quarter sums are in shared memory
-    float l = (lsum[row] + lsum[RM + row]) + (lsum[2 * RM + row] + lsum[3 * RM + row]);
-    if constexpr (NREP == 2) {
-      l += (lsum[4 * RM + row] + lsum[5 * RM + row]) + (lsum[6 * RM + row] + lsum[7 * RM + row]);
-      // the replica in lanes 64..127 hands its O quarter to the one in 0..63
-#pragma unroll
-      for (int c0 = 0; c0 < OQ; c0 += OC) {
-        if (half == 1) {
-#pragma unroll
-          for (int k = 0; k < OC; ++k) stage_o[row * 65 + cq * 16 + k] = o[c0 + k];
-        }
-        softmax_sync();
-        if (half == 0) {
-#pragma unroll
-          for (int k = 0; k < OC; ++k) o[c0 + k] += stage_o[row * 65 + cq * 16 + k];
-        }
-        softmax_sync();
-      }
-    }
-    const bool poisoned = (*abort_flag != 0) || !ok || !have_o;
-    // Records are column-major over the unit's rows (wide_rec): element
-    // (col, r) at [col * rows + r], col 0 = m, 1 = l, 2 + c = O dim c, so
-    // that a warp's 32 rows read and write whole 128-byte lines.
-    const int rows = p.rows;
-    if (kind == kNonHost || kind == kPartial) {
-      if (owner) {
-        float* rec = p.recs + (size_t)g * C::RS;
-        if (cq == 0) {
-          rec[row] = poisoned ? __int_as_float(0x7fc00000) : m_use;
-          rec[rows + row] = l;
-        }
-#pragma unroll
-        for (int c = 0; c < OQ; ++c) rec[(size_t)(2 + OQ * cq + c) * rows + row] = o[c];
-      }
-      __threadfence();
-      softmax_sync();
-      if (kind == kNonHost && tid == 0 && g != p.skip_signal) st_release_gpu(&p.flags[g], ready);
-    } else {
-      bool fail = poisoned;
-      float Ls = l;
-      if (kind == kHost) {
-        // every later CTA of the unit: thread i spins (bounded) on the ready
-        // flags of peers i, i + 512, ...
-        const int npeer = peer - g;
-        const uint64_t twait = global_ns();
-        for (int i = tid; i < npeer; i += C::NSW * 32) {
-          const int g2 = g + 1 + i;
-          const uint64_t tstart = global_ns();
-          for (uint32_t it = 0; !*abort_flag; ++it) {
-            if (ld_acquire_gpu(&p.flags[g2]) == ready) break;
-            if ((it & 15u) == 15u) {
-              if ((long long)(global_ns() - tstart) > p.spin_ns) {
-                record_error(p.hdr, kStatusTimeout, g, g2);
-                *abort_flag = 1;
-                break;
-              }
-              __nanosleep(100);
-            }
-          }
-        }
-        softmax_sync();  // every flag seen (or the abort raised) before any record is read
-        if (tr != nullptr) tr[kTrWaitNs] += global_ns() - twait;
-        // The host segment is the CTA's last: every tile has been consumed
-        // and the producer issues no more copies, so the ring is idle. The
-        // peers' records come into it by bulk copies, as many at a time as
-        // fit, and are merged with f one after another (the running
-        // maximum M, then the rescaled sums of l and of this thread's O
-        // quarter).
-        const uint32_t rec_bytes = ((uint32_t)rows * (D + 2) * 4u + 15u) & ~15u;
-        const int cap = (int)(C::KV_BYTES / rec_bytes);
-        float M = m_use;
-        uint32_t sph = 0;
-        for (int p0 = 0; p0 < npeer; p0 += cap) {
-          const int nb = npeer - p0 < cap ? npeer - p0 : cap;
-          if (tid == 0 && !*abort_flag) {
-            asm volatile("fence.proxy.async.global;" ::: "memory");  // records written by other CTAs
-            mbar_arrive_expect_tx(stg, (uint32_t)nb * rec_bytes);
-            for (int k = 0; k < nb; ++k)
-              bulk_g2s(reinterpret_cast<unsigned char*>(kv) + (size_t)k * rec_bytes,
-                       p.recs + (size_t)(g + 1 + p0 + k) * C::RS, rec_bytes, stg, l2_evict_first_policy());
-            flags_smem_copies[0] = 1;  // copies in flight: wait for them even after an abort
+    if constexpr (NREP == 1) {
+      // 128-row instance (96 registers a thread): one replica owns each
+      // quarter; one staging buffer; direct stores
+      float l = (lsum[row] + lsum[RM + row]) + (lsum[2 * RM + row] + lsum[3 * RM + row]);
+      if constexpr (NREP == 2) {
+        l += (lsum[4 * RM + row] + lsum[5 * RM + row]) + (lsum[6 * RM + row] + lsum[7 * RM + row]);
+        // the replica in lanes 64..127 hands its O quarter to the one in 0..63
+  #pragma unroll
+        for (int c0 = 0; c0 < OQ; c0 += OC) {
+          if (half == 1) {
+  #pragma unroll
+            for (int k = 0; k < OC; ++k) stage_o[row * 65 + cq * 16 + k] = o[c0 + k];
           }
           softmax_sync();
-          const bool issued = flags_smem_copies[0] != 0;
-          volatile int no_abort = 0;
-          const bool got = issued && mbar_wait_bounded(stg, sph, &no_abort, p.spin_ns);
-          sph ^= issued ? 1u : 0u;
-          if (issued && !got) fail = true;
-          if (got && owner && !*abort_flag) {
-            // f over the batch at once: its maximum, one rescale of the
-            // running partial, then the weighted sums
-            const float* r0 = reinterpret_cast<const float*>(kv);
-            const int rstride = (int)(rec_bytes / 4);  // floats between staged records
-            float mb = M;
-            for (int k = 0; k < nb; ++k) mb = fmaxf(mb, r0[k * rstride + row]);
-            if (mb != -INFINITY) {
-              const float a = (M == -INFINITY) ? 0.f : ex2(M - mb);
-              Ls *= a;
-#pragma unroll
-              for (int c = 0; c < OQ; ++c) o[c] *= a;
-              for (int k = 0; k < nb; ++k) {
-                const float* rk = r0 + k * rstride;
-                const float mk = rk[row];
-                const float wt = (mk == -INFINITY) ? 0.f : ex2(mk - mb);  // NaN m (poisoned) propagates
-                Ls = fmaf(wt, rk[rows + row], Ls);
-#pragma unroll
-                for (int c = 0; c < OQ; ++c) o[c] = fmaf(wt, rk[(2 + OQ * cq + c) * rows + row], o[c]);
+          if (half == 0) {
+  #pragma unroll
+            for (int k = 0; k < OC; ++k) o[c0 + k] += stage_o[row * 65 + cq * 16 + k];
+          }
+          softmax_sync();
+        }
+      }
+      const bool poisoned = (*abort_flag != 0) || !ok || !have_o;
+      // Records are column-major over the unit's rows (wide_rec): element
+      // (col, r) at [col * rows + r], col 0 = m, 1 = l, 2 + c = O dim c, so
+      // that a warp's 32 rows read and write whole 128-byte lines.
+      const int rows = p.rows;
+      if (kind == kNonHost || kind == kPartial) {
+        if (owner) {
+          float* rec = p.recs + (size_t)g * C::RS;
+          if (cq == 0) {
+            rec[row] = poisoned ? __int_as_float(0x7fc00000) : m_use;
+            rec[rows + row] = l;
+          }
+  #pragma unroll
+          for (int c = 0; c < OQ; ++c) rec[(size_t)(2 + OQ * cq + c) * rows + row] = o[c];
+        }
+        __threadfence();
+        softmax_sync();
+        if (kind == kNonHost && tid == 0 && g != p.skip_signal) st_release_gpu(&p.flags[g], ready);
+      } else {
+        bool fail = poisoned;
+        float Ls = l;
+        if (kind == kHost) {
+          // every later CTA of the unit: thread i spins (bounded) on the ready
+          // flags of peers i, i + 512, ...
+          const int npeer = peer - g;
+          const uint64_t twait = global_ns();
+          for (int i = tid; i < npeer; i += C::NSW * 32) {
+            const int g2 = g + 1 + i;
+            const uint64_t tstart = global_ns();
+            for (uint32_t it = 0; !*abort_flag; ++it) {
+              if (ld_acquire_gpu(&p.flags[g2]) == ready) break;
+              if ((it & 15u) == 15u) {
+                if ((long long)(global_ns() - tstart) > p.spin_ns) {
+                  record_error(p.hdr, kStatusTimeout, g, g2);
+                  *abort_flag = 1;
+                  break;
+                }
+                __nanosleep(100);
               }
-              M = mb;
             }
           }
-          softmax_sync();  // the staging area is rewritten by the next batch
-          if (tid == 0) flags_smem_copies[0] = 0;
+          softmax_sync();  // every flag seen (or the abort raised) before any record is read
+          if (tr != nullptr) tr[kTrWaitNs] += global_ns() - twait;
+          // The host segment is the CTA's last: every tile has been consumed
+          // and the producer issues no more copies, so the ring is idle. The
+          // peers' records come into it by bulk copies, as many at a time as
+          // fit, and are merged with f one after another (the running
+          // maximum M, then the rescaled sums of l and of this thread's O
+          // quarter).
+          const uint32_t rec_bytes = ((uint32_t)rows * (D + 2) * 4u + 15u) & ~15u;
+          const int cap = (int)(C::KV_BYTES / rec_bytes);
+          float M = m_use;
+          uint32_t sph = 0;
+          for (int p0 = 0; p0 < npeer; p0 += cap) {
+            const int nb = npeer - p0 < cap ? npeer - p0 : cap;
+            if (tid == 0 && !*abort_flag) {
+              asm volatile("fence.proxy.async.global;" ::: "memory");  // records written by other CTAs
+              mbar_arrive_expect_tx(stg, (uint32_t)nb * rec_bytes);
+              for (int k = 0; k < nb; ++k)
+                bulk_g2s(reinterpret_cast<unsigned char*>(kv) + (size_t)k * rec_bytes,
+                         p.recs + (size_t)(g + 1 + p0 + k) * C::RS, rec_bytes, stg, l2_evict_first_policy());
+              flags_smem_copies[0] = 1;  // copies in flight: wait for them even after an abort
+            }
+            softmax_sync();
+            const bool issued = flags_smem_copies[0] != 0;
+            volatile int no_abort = 0;
+            const bool got = issued && mbar_wait_bounded(stg, sph, &no_abort, p.spin_ns);
+            sph ^= issued ? 1u : 0u;
+            if (issued && !got) fail = true;
+            if (got && owner && !*abort_flag) {
+              // f over the batch at once: its maximum, one rescale of the
+              // running partial, then the weighted sums
+              const float* r0 = reinterpret_cast<const float*>(kv);
+              const int rstride = (int)(rec_bytes / 4);  // floats between staged records
+              float mb = M;
+              for (int k = 0; k < nb; ++k) mb = fmaxf(mb, r0[k * rstride + row]);
+              if (mb != -INFINITY) {
+                const float a = (M == -INFINITY) ? 0.f : ex2(M - mb);
+                Ls *= a;
+  #pragma unroll
+                for (int c = 0; c < OQ; ++c) o[c] *= a;
+                for (int k = 0; k < nb; ++k) {
+                  const float* rk = r0 + k * rstride;
+                  const float mk = rk[row];
+                  const float wt = (mk == -INFINITY) ? 0.f : ex2(mk - mb);  // NaN m (poisoned) propagates
+                  Ls = fmaf(wt, rk[rows + row], Ls);
+  #pragma unroll
+                  for (int c = 0; c < OQ; ++c) o[c] = fmaf(wt, rk[(2 + OQ * cq + c) * rows + row], o[c]);
+                }
+                M = mb;
+              }
+            }
+            softmax_sync();  // the staging area is rewritten by the next batch
+            if (tid == 0) flags_smem_copies[0] = 0;
+          }
+          if (*abort_flag) fail = true;
         }
-        if (*abort_flag) fail = true;
+        // normalise and store: O = Obar / l
+        if (owner) {
+          const size_t base = row_index(p, b, kvh, row) * D + OQ * cq;
+          const float inv = 1.f / Ls;
+  #pragma unroll
+          for (int c = 0; c < OQ; c += 4)
+            store_out4(p.out, base + c, fail ? __int_as_float(0x7fc00000) : o[c] * inv,
+                       fail ? __int_as_float(0x7fc00000) : o[c + 1] * inv,
+                       fail ? __int_as_float(0x7fc00000) : o[c + 2] * inv,
+                       fail ? __int_as_float(0x7fc00000) : o[c + 3] * inv, p.out_dtype);
+        }
       }
-      // normalise and store: O = Obar / l
-      if (owner) {
-        const size_t base = row_index(p, b, kvh, row) * D + OQ * cq;
-        const float inv = 1.f / Ls;
-#pragma unroll
-        for (int c = 0; c < OQ; c += 4)
-          store_out4(p.out, base + c, fail ? __int_as_float(0x7fc00000) : o[c] * inv,
-                     fail ? __int_as_float(0x7fc00000) : o[c + 1] * inv,
-                     fail ? __int_as_float(0x7fc00000) : o[c + 2] * inv,
-                     fail ? __int_as_float(0x7fc00000) : o[c + 3] * inv, p.out_dtype);
+    } else {
+      float l = (lsum[row] + lsum[RM + row]) + (lsum[2 * RM + row] + lsum[3 * RM + row]);
+      // The dims of the O quarter this thread owns from here on: with lane
+      // replicas the two halves split the quarter (each adds the other
+      // replica's partial O row for its half), so that all 16 warps share the
+      // record write, the host merge and the stores; without, the whole
+      // quarter.
+      constexpr int NO = OQ / NREP;
+      const int db = OQ * cq + (NREP == 2 ? NO * half : 0);  // first dim this thread owns
+      if constexpr (NREP == 2) {
+        l += (lsum[4 * RM + row] + lsum[5 * RM + row]) + (lsum[6 * RM + row] + lsum[7 * RM + row]);
+        // round 0: the replica in lanes 64..127 hands dims [0, NO) of its
+        // quarter to the one in 0..63; round 1: the other way, dims [NO, OQ)
+  #pragma unroll
+        for (int rnd = 0; rnd < 2; ++rnd) {
+          if (half != rnd) {
+  #pragma unroll
+            for (int k = 0; k < NO; ++k) stage_o[row * 65 + cq * 16 + k] = o[NO * rnd + k];
+          }
+          softmax_sync();
+          if (half == rnd) {
+  #pragma unroll
+            for (int k = 0; k < NO; ++k) o[NO * rnd + k] += stage_o[row * 65 + cq * 16 + k];
+          }
+          softmax_sync();
+        }
+  #pragma unroll
+        for (int k = 0; k < NO; ++k) o[k] = half ? o[NO + k] : o[k];  // this thread's dims into o[0, NO)
+      }
+      const bool poisoned = (*abort_flag != 0) || !ok || !have_o;
+      // Records are column-major over the unit's rows (wide_rec): element
+      // (col, r) at [col * rows + r], col 0 = m, 1 = l, 2 + c = O dim c, so
+      // that a warp's 32 rows read and write whole 128-byte lines.
+      const int rows = p.rows;
+      if (kind == kNonHost || kind == kPartial) {
+        if (live) {
+          float* rec = p.recs + (size_t)g * C::RS;
+          if (owner && cq == 0) {
+            rec[row] = poisoned ? __int_as_float(0x7fc00000) : m_use;
+            rec[rows + row] = l;
+          }
+  #pragma unroll
+          for (int c = 0; c < NO; ++c) rec[(size_t)(2 + db + c) * rows + row] = o[c];
+        }
+        __threadfence();
+        softmax_sync();
+        if (kind == kNonHost && tid == 0 && g != p.skip_signal) st_release_gpu(&p.flags[g], ready);
+      } else {
+        bool fail = poisoned;
+        float Ls = l;
+        if (kind == kHost) {
+          // every later CTA of the unit: thread i spins (bounded) on the ready
+          // flags of peers i, i + 512, ...
+          const int npeer = peer - g;
+          const uint64_t twait = global_ns();
+          for (int i = tid; i < npeer; i += C::NSW * 32) {
+            const int g2 = g + 1 + i;
+            const uint64_t tstart = global_ns();
+            for (uint32_t it = 0; !*abort_flag; ++it) {
+              if (ld_acquire_gpu(&p.flags[g2]) == ready) break;
+              if ((it & 15u) == 15u) {
+                if ((long long)(global_ns() - tstart) > p.spin_ns) {
+                  record_error(p.hdr, kStatusTimeout, g, g2);
+                  *abort_flag = 1;
+                  break;
+                }
+                __nanosleep(100);
+              }
+            }
+          }
+          softmax_sync();  // every flag seen (or the abort raised) before any record is read
+          if (tr != nullptr) tr[kTrWaitNs] += global_ns() - twait;
+          // The host segment is the CTA's last: every tile has been consumed
+          // and the producer issues no more copies, so the ring is idle. The
+          // peers' records come into its two halves by bulk copies, a batch
+          // per half, so the next batch's copies overlap this batch's merge;
+          // each batch is merged with f at once (its maximum, one rescale of
+          // the running partial, then the weighted sums of l and of this
+          // thread's dims).
+          // Records small enough for two per half of the ring are double
+          // buffered; larger ones fill the whole ring per batch. The 128-row
+          // instance (NREP = 1, 96 registers a thread) keeps one buffer and
+          // direct stores: the extra state spilled into its tile loop.
+          const uint32_t rec_bytes = ((uint32_t)rows * (D + 2) * 4u + 15u) & ~15u;
+          constexpr size_t kHalf = C::KV_BYTES / 2;
+          const bool dbl = NREP == 2 && kHalf / rec_bytes >= 2;
+          const int cap = (int)((dbl ? kHalf : C::KV_BYTES) / rec_bytes);  // >= 1: a record is at most 66.5 KB
+          const int nbat = (npeer + cap - 1) / cap;
+          float M = m_use;
+          auto issue = [&](int bi) {  // thread 0: batch bi into its buffer
+            if (tid != 0 || *abort_flag) return;
+            const int p0 = bi * cap, nb = npeer - p0 < cap ? npeer - p0 : cap;
+            const int slot = dbl ? (bi & 1) : 0;
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // records written by other CTAs
+            mbar_arrive_expect_tx(&stg[slot], (uint32_t)nb * rec_bytes);
+            for (int k = 0; k < nb; ++k)
+              bulk_g2s(reinterpret_cast<unsigned char*>(kv) + slot * kHalf + (size_t)k * rec_bytes,
+                       p.recs + (size_t)(g + 1 + p0 + k) * C::RS, rec_bytes, &stg[slot], l2_evict_first_policy());
+            flags_smem_copies[slot] = 1;  // copies in flight: wait for them even after an abort
+          };
+          if (nbat > 0) issue(0);
+          for (int bi = 0; bi < nbat; ++bi) {
+            const int p0 = bi * cap, nb = npeer - p0 < cap ? npeer - p0 : cap;
+            const int slot = dbl ? (bi & 1) : 0;
+            const uint32_t parity = dbl ? ((uint32_t)(bi >> 1) & 1u) : ((uint32_t)bi & 1u);
+            if (dbl ? bi + 1 < nbat : bi > 0) issue(dbl ? bi + 1 : bi);  // one buffer: the last batch is merged
+            softmax_sync();
+            const bool issued = flags_smem_copies[slot] != 0;
+            volatile int no_abort = 0;
+            const bool got = issued && mbar_wait_bounded(&stg[slot], parity, &no_abort, p.spin_ns);
+            if (issued && !got) fail = true;
+            if (got && live && !*abort_flag) {
+              const float* r0 = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(kv) +
+                                                               slot * kHalf);
+              const int rstride = (int)(rec_bytes / 4);  // floats between staged records
+              float mb = M;
+              for (int k = 0; k < nb; ++k) mb = fmaxf(mb, r0[k * rstride + row]);
+              if (mb != -INFINITY) {
+                const float a = (M == -INFINITY) ? 0.f : ex2(M - mb);
+                Ls *= a;
+  #pragma unroll
+                for (int c = 0; c < NO; ++c) o[c] *= a;
+                for (int k = 0; k < nb; ++k) {
+                  const float* rk = r0 + k * rstride;
+                  const float mk = rk[row];
+                  const float wt = (mk == -INFINITY) ? 0.f : ex2(mk - mb);  // NaN m (poisoned) propagates
+                  Ls = fmaf(wt, rk[rows + row], Ls);
+  #pragma unroll
+                  for (int c = 0; c < NO; ++c) o[c] = fmaf(wt, rk[(2 + db + c) * rows + row], o[c]);
+                }
+                M = mb;
+              }
+            }
+            softmax_sync();  // the batch's buffer is free again
+            if (tid == 0) flags_smem_copies[slot] = 0;
+          }
+          if (*abort_flag) fail = true;
+          // normalise and store; with lane replicas through the ring as
+          // [row][D] (rows 16-byte aligned), then whole rows: a warp writes
+          // 512 contiguous bytes, not 32 separate 16-byte pieces
+          if constexpr (NREP == 2) {
+            constexpr int OS = D + 4;  // floats between rows in the ring
+            float* ob = reinterpret_cast<float*>(kv);
+            if (live) {
+              const float inv = 1.f / Ls;
+              const float nan = __int_as_float(0x7fc00000);
+  #pragma unroll
+              for (int c = 0; c < NO; c += 4)
+                *reinterpret_cast<float4*>(ob + row * OS + db + c) =
+                    fail ? make_float4(nan, nan, nan, nan)
+                         : make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+            }
+            softmax_sync();
+            for (int i = tid; i < rows * (D / 4); i += C::NSW * 32) {
+              const int r = i / (D / 4), c4 = 4 * (i % (D / 4));
+              const float4 v = *reinterpret_cast<const float4*>(ob + r * OS + c4);
+              store_out4(p.out, row_index(p, b, kvh, r) * D + c4, v.x, v.y, v.z, v.w, p.out_dtype);
+            }
+          } else if (live) {
+            const size_t base = row_index(p, b, kvh, row) * D + db;
+            const float inv = 1.f / Ls;
+            const float nan = __int_as_float(0x7fc00000);
+  #pragma unroll
+            for (int c = 0; c < NO; c += 4)
+              store_out4(p.out, base + c, fail ? nan : o[c] * inv, fail ? nan : o[c + 1] * inv,
+                         fail ? nan : o[c + 2] * inv, fail ? nan : o[c + 3] * inv, p.out_dtype);
+          }
+        } else if (live) {  // a whole unit: normalise and store this thread's dims
+          const size_t base = row_index(p, b, kvh, row) * D + db;
+          const float inv = 1.f / Ls;
+          const float nan = __int_as_float(0x7fc00000);
+  #pragma unroll
+          for (int c = 0; c < NO; c += 4)
+            store_out4(p.out, base + c, fail ? nan : o[c] * inv, fail ? nan : o[c + 1] * inv,
+                       fail ? nan : o[c + 2] * inv, fail ? nan : o[c + 3] * inv, p.out_dtype);
+        }
       }
     }
     softmax_sync();  // the quarter sums are rewritten by the next segment
@@ -711,9 +892,10 @@ __global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
   uint64_t* pv_done = p_full + C::NSB;
   uint64_t* q_ready = pv_done + C::NSB;
   uint64_t* drain = q_ready + 1;
-  uint64_t* stg = drain + 1;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(stg + 1);
-  volatile int* flags_smem = reinterpret_cast<volatile int*>(tslot + 2);  // [0] abort, [1] staging copies issued
+  uint64_t* stg = drain + 1;  // two barriers: staged peer records, one per half of the ring
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(stg + 2);
+  // [0] abort, [1] and [2] staging copies issued into each half of the ring
+  volatile int* flags_smem = reinterpret_cast<volatile int*>(tslot + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int g = blockIdx.x;
@@ -737,9 +919,11 @@ __global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
     }
     mbar_init(q_ready, C::NSW * 32);
     mbar_init(drain, 1);
-    mbar_init(stg, 1);
+    mbar_init(&stg[0], 1);
+    mbar_init(&stg[1], 1);
     flags_smem[0] = 0;
     flags_smem[1] = 0;
+    flags_smem[2] = 0;
     fence_mbar_init();
   }
   if (warp == C::NSW + 1) {
