@@ -145,7 +145,7 @@ bool tile_supported(int d, int T, int hp = 1);
 
 // Units of more than 16 query rows run on the tcgen05 kernel (la_wide.cuh),
 // whose instance holds kWideRows rows, with 128-token tiles and one kv head
-// per unit; head dims 64, 96 and 128 (wide_supported).
+// per unit; head dims 64, 80, 96 and 128 (wide_supported).
 constexpr int kWideRows = 128;
 constexpr int kWideTile = 128;
 bool wide_supported(int d);

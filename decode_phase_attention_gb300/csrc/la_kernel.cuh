@@ -312,6 +312,18 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, int ou
   else
     static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
 }
+// Two consecutive outputs (idx even) as fp32, fp16 or bf16.
+__device__ __forceinline__ void store_out2(void* out, size_t idx, float a, float b, int out_dtype) {
+  if (out_dtype == 0) {
+    *reinterpret_cast<float2*>(static_cast<float*>(out) + idx) = make_float2(a, b);
+  } else if (out_dtype == 1) {
+    __half2 x = __floats2half2_rn(a, b);
+    *reinterpret_cast<uint32_t*>(static_cast<__half*>(out) + idx) = *reinterpret_cast<uint32_t*>(&x);
+  } else {
+    __nv_bfloat162 x = __floats2bfloat162_rn(a, b);
+    *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(out) + idx) = *reinterpret_cast<uint32_t*>(&x);
+  }
+}
 // Four consecutive outputs (idx a multiple of 4) as fp32, fp16 or bf16.
 __device__ __forceinline__ void store_out4(void* out, size_t idx, float a, float b, float c, float d,
                                            int out_dtype) {

@@ -30,9 +30,11 @@
 // kernel). S of the next tile is computed into another buffer while the
 // softmax runs; it waits only for the P V that last used that buffer.
 // Keeping Q in TMEM leaves shared memory to the K/V ring (3 stages of
-// 64 KiB at d = 128, 4 of 48 KiB at d = 96, 6 of 32 KiB at d = 64). At
-// d = 64 and 128 the K/V boxes are 64 head dims wide (128-byte swizzle),
-// at d = 96 32 dims (64-byte swizzle). O accumulates over a
+// 64 KiB at d = 128, 4 of 48 KiB at d = 96, 5 of 40 KiB at d = 80, 6 of
+// 32 KiB at d = 64). At d = 64 and 128 the K/V boxes are 64 head dims wide
+// (128-byte swizzle), at d = 96 32 dims (64-byte swizzle), at d = 80 16 dims
+// (32-byte swizzle: one MMA k-step per box row; O quarters of 20 columns are
+// read in pieces of 4, Q quarters of 10 written in pieces of 2). O accumulates over a
 // segment's tiles in TMEM; a row's reference maximum moves only when a
 // tile's maximum exceeds it by more than 2^8 (p values stay below 256), and
 // only then is that row of O rescaled.
@@ -110,6 +112,15 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
                : "r"(taddr)
                : "memory");
 }
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(r[0]), "r"(r[1]) : "memory");
+}
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* r) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
                "r"(r[2]), "r"(r[3])
@@ -122,6 +133,15 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// A TMEM access of N (16, 8 or 4) consecutive columns, aligned to N.
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t* r) {
+  if constexpr (N == 16) tmem_ld16(taddr, r); else if constexpr (N == 8) tmem_ld8(taddr, r); else tmem_ld4(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t* r) {
+  if constexpr (N == 16) tmem_st16(taddr, r); else if constexpr (N == 8) tmem_st8(taddr, r); else tmem_st4(taddr, r);
+}
 // Registers written by tcgen05.ld are read only after the wait: tie them to
 // it so that the compiler cannot move a use above the wait.
 template <int N>
@@ -162,14 +182,14 @@ struct WCfg {
   static constexpr int T = 128;                 // LeanTile tokens (MMA N of S, K of P V)
   static constexpr int ROWS = T;
   static constexpr bool TC = true;              // the producer's swizzled TMA boxes
-  static constexpr int W = D % 64 == 0 ? 64 : 32;  // box columns
+  static constexpr int W = D % 64 == 0 ? 64 : (D % 32 == 0 ? 32 : 16);  // box columns
   static constexpr int RB = W * 2;              // box row bytes: 128 (128-byte swizzle) or 64 (64-byte)
   static constexpr int NB = D / W;              // boxes per tile per tensor
   static constexpr int TILE_ELEMS = T * D;
   static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
   static constexpr int BOX_BYTES = T * RB;      // one box of a K or V tile
   static constexpr int ATOM = 8 * RB;           // one 8-row swizzle atom
-  static constexpr uint64_t SWZ = W == 64 ? 2 : 4;  // descriptor swizzle mode
+  static constexpr uint64_t SWZ = W == 64 ? 2 : (W == 32 ? 4 : 6);  // descriptor swizzle mode: 128, 64, 32 bytes
   static constexpr int KPB = W / 16;            // MMA k-steps (16 head dims, 32 bytes) per box row
   static constexpr int REC = D + 2;
   static constexpr int RS = record_stride_wide(D, M);
@@ -186,7 +206,7 @@ struct WCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = NSB * T;    // S / P buffers first, then O
   static constexpr uint32_t Q_COL = O_COL + D;  // then Q
-  static_assert(D == 64 || D == 96 || D == 128, "head dims of the wide kernel");
+  static_assert(D == 64 || D == 80 || D == 96 || D == 128, "head dims of the wide kernel");
   static_assert(M == kWideInstanceRows, "record layout of the wide kernel");
   static_assert(STAGES >= 2 && SMEM <= 232448, "shared memory per CTA");
   static_assert(NBARS * 8 + 8 + 12 <= 256, "barrier area");  // barriers, TMEM slot, 3 flag words
@@ -331,7 +351,7 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
   using C = WCfg<D>;
   constexpr int T = C::T;
   constexpr int OQ = D / 4;  // head dims of O per thread
-  constexpr int OC = OQ % 16 == 0 ? 16 : 8;  // O columns per TMEM access (aligned to its size)
+  constexpr int OC = OQ % 16 == 0 ? 16 : (OQ % 8 == 0 ? 8 : 4);  // O columns per TMEM access (aligned to its size)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, cq = warp >> 2;
   const int r = qd * 32 + lane;
@@ -379,21 +399,34 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) +
                                                         row_index(p, b, kvh, live ? row : 0) * D + (D / 4) * cq);
       uint32_t qw[D / 8];
+      if constexpr (D % 32 == 0) {
 #pragma unroll
-      for (int k = 0; k < D / 32; ++k) {
-        const uint4 v = live ? src[k] : make_uint4(0u, 0u, 0u, 0u);
-        qw[4 * k] = v.x;
-        qw[4 * k + 1] = v.y;
-        qw[4 * k + 2] = v.z;
-        qw[4 * k + 3] = v.w;
+        for (int k = 0; k < D / 32; ++k) {
+          const uint4 v = live ? src[k] : make_uint4(0u, 0u, 0u, 0u);
+          qw[4 * k] = v.x;
+          qw[4 * k + 1] = v.y;
+          qw[4 * k + 2] = v.z;
+          qw[4 * k + 3] = v.w;
+        }
+      } else {  // d = 80: 40 bytes of a quarter row, 8-byte aligned
+        const uint2* src2 = reinterpret_cast<const uint2*>(src);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint2 v = live ? src2[k] : make_uint2(0u, 0u);
+          qw[2 * k] = v.x;
+          qw[2 * k + 1] = v.y;
+        }
       }
       if constexpr (D / 8 == 16) {
         tmem_st16(trow + C::Q_COL + 16u * cq, qw);
       } else if constexpr (D / 8 == 8) {
         tmem_st8(trow + C::Q_COL + 8u * cq, qw);
-      } else {  // d = 96: 12 columns, in pieces of 4 (each access aligned to its size)
+      } else if constexpr (D % 32 == 0) {  // d = 96: 12 columns, in pieces of 4 (each access aligned to its size)
 #pragma unroll
         for (int k = 0; k < D / 32; ++k) tmem_st4(trow + C::Q_COL + (uint32_t)(D / 8) * cq + 4u * k, qw + 4 * k);
+      } else {  // d = 80: 10 columns, in pieces of 2
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) tmem_st2(trow + C::Q_COL + (uint32_t)(D / 8) * cq + 2u * k, qw + 2 * k);
       }
     }
     tmem_wait_st();
@@ -515,11 +548,11 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
           for (int c = 0; c < OQ / OC; ++c) {
             uint32_t o[OC];
             const uint32_t oc = trow + C::O_COL + (uint32_t)(OQ * cq + OC * c);
-            if constexpr (OC == 16) tmem_ld16(oc, o); else tmem_ld8(oc, o);
+            tmem_ldn<OC>(oc, o);
             tmem_wait_ld_regs<OC>(o);
 #pragma unroll
             for (int k = 0; k < OC; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * a);
-            if constexpr (OC == 16) tmem_st16(oc, o); else tmem_st8(oc, o);
+            tmem_stn<OC>(oc, o);
           }
         } else {
           alive = false;
@@ -551,7 +584,7 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
       for (int c = 0; c < OQ / OC; ++c) {
         uint32_t v[OC];
         const uint32_t oc = trow + C::O_COL + (uint32_t)(OQ * cq + OC * c);
-        if constexpr (OC == 16) tmem_ld16(oc, v); else tmem_ld8(oc, v);
+        tmem_ldn<OC>(oc, v);
         tmem_wait_ld_regs<OC>(v);
 #pragma unroll
         for (int k = 0; k < OC; ++k) o[OC * c + k] = __uint_as_float(v[k]);
@@ -836,11 +869,18 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
             if (live) {
               const float inv = 1.f / Ls;
               const float nan = __int_as_float(0x7fc00000);
+              if constexpr (NO % 4 == 0) {
   #pragma unroll
-              for (int c = 0; c < NO; c += 4)
-                *reinterpret_cast<float4*>(ob + row * OS + db + c) =
-                    fail ? make_float4(nan, nan, nan, nan)
-                         : make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+                for (int c = 0; c < NO; c += 4)
+                  *reinterpret_cast<float4*>(ob + row * OS + db + c) =
+                      fail ? make_float4(nan, nan, nan, nan)
+                           : make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+              } else {  // d = 80: 10 dims per half
+  #pragma unroll
+                for (int c = 0; c < NO; c += 2)
+                  *reinterpret_cast<float2*>(ob + row * OS + db + c) =
+                      fail ? make_float2(nan, nan) : make_float2(o[c] * inv, o[c + 1] * inv);
+              }
             }
             softmax_sync();
             for (int i = tid; i < rows * (D / 4); i += C::NSW * 32) {
@@ -861,10 +901,16 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
           const size_t base = row_index(p, b, kvh, row) * D + db;
           const float inv = 1.f / Ls;
           const float nan = __int_as_float(0x7fc00000);
+          if constexpr (NO % 4 == 0) {
   #pragma unroll
-          for (int c = 0; c < NO; c += 4)
-            store_out4(p.out, base + c, fail ? nan : o[c] * inv, fail ? nan : o[c + 1] * inv,
-                       fail ? nan : o[c + 2] * inv, fail ? nan : o[c + 3] * inv, p.out_dtype);
+            for (int c = 0; c < NO; c += 4)
+              store_out4(p.out, base + c, fail ? nan : o[c] * inv, fail ? nan : o[c + 1] * inv,
+                         fail ? nan : o[c + 2] * inv, fail ? nan : o[c + 3] * inv, p.out_dtype);
+          } else {  // d = 80: 10 dims per half
+  #pragma unroll
+            for (int c = 0; c < NO; c += 2)
+              store_out2(p.out, base + c, fail ? nan : o[c] * inv, fail ? nan : o[c + 1] * inv, p.out_dtype);
+          }
         }
       }
     }

@@ -85,11 +85,11 @@ enum {
  *                      kv head run as one unit on the 16-row kernel; a group
  *                      that is not a power of two runs on the next larger
  *                      instance (1, 2, 4, 8 or 16 rows), whose spare rows are
- *                      zero queries never written out. At d = 64, 96 and 128
+ *                      zero queries never written out. At d = 64, 80, 96, 128
  *                      a unit of 17-128 rows (e.g. multi-query attention) runs
  *                      on the tcgen05 kernel (128-row instance, 128-token
  *                      tiles). A kv head with more rows than a unit holds
- *                      (128 at d = 64, 96, 128; 16 otherwise) is split into
+ *                      (128 at d = 64, 80, 96, 128; 16 at d = 256) is split into
  *                      query blocks: the fewest equal blocks of consecutive
  *                      query heads that fit (qb blocks of grp / qb heads, qb
  *                      dividing grp); every block is a unit of its own that
@@ -154,7 +154,7 @@ la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlen
  * their split are those of la_plan (K/V are read once per kv head for all
  * grp * nq query rows, as many as a unit holds; above that the kv head's
  * query heads are split into query blocks as in la_plan, each of
- * grp / qb * nq rows). Requires nq <= 128 at d = 64, 96 and 128, nq <= 16
+ * grp / qb * nq rows). Requires nq <= 128 at d = 64, 80, 96 and 128, nq <= 16
  * otherwise (LA_ERR_UNSUPPORTED), and L_b >= nq for every request
  * (LA_ERR_INVALID); nq = 1 is la_plan.
  */

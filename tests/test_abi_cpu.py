@@ -403,9 +403,11 @@ def test_groups_that_are_not_powers_of_two(grp):
 # (d = 64, 96, 128), else 16: the fewest equal blocks of whole query heads
 # whose rows fit.
 QUERY_BLOCKS = [
-    (80, 32, 1, 2, 16), (80, 24, 1, 2, 16), (80, 17, 1, 17, 1), (80, 18, 1, 2, 16), (80, 34, 1, 17, 2),
-    (80, 40, 1, 4, 16), (80, 48, 1, 3, 16), (80, 64, 1, 4, 16), (80, 128, 1, 8, 16), (80, 8, 3, 2, 16),
-    (80, 8, 4, 2, 16), (80, 16, 2, 2, 16), (80, 4, 5, 2, 16), (80, 1, 16, 1, 16), (80, 2, 16, 2, 16),
+    (256, 32, 1, 2, 16), (256, 24, 1, 2, 16), (256, 17, 1, 17, 1), (256, 18, 1, 2, 16), (256, 34, 1, 17, 2),
+    (256, 40, 1, 4, 16), (256, 48, 1, 3, 16), (256, 64, 1, 4, 16), (256, 128, 1, 8, 16), (256, 8, 3, 2, 16),
+    (256, 8, 4, 2, 16), (256, 16, 2, 2, 16), (256, 4, 5, 2, 16), (256, 1, 16, 1, 16), (256, 2, 16, 2, 16),
+    (80, 32, 1, 1, 128), (80, 17, 1, 1, 128), (80, 128, 1, 1, 128), (80, 256, 1, 2, 128), (80, 8, 3, 1, 128),
+    (80, 1, 16, 1, 16), (80, 2, 100, 2, 128),
     (64, 32, 1, 1, 128), (64, 17, 1, 1, 128), (64, 128, 1, 1, 128), (64, 256, 1, 2, 128), (64, 192, 1, 2, 128),
     (64, 8, 4, 1, 128), (64, 16, 9, 2, 128), (64, 1, 16, 1, 16), (64, 3, 7, 1, 128), (64, 2, 100, 2, 128),
     (128, 16, 1, 1, 16), (128, 64, 1, 1, 128), (128, 130, 1, 2, 128),
@@ -419,7 +421,8 @@ def test_query_blocks_are_units_of_their_own(d, grp, nq, qb, R):
     # hkv * qb heads of grp / qb query heads each
     lengths = [700, 128, 3000]
     hkv, G = 2, 11
-    T = 128 if (R == 128 or d != 64) else 256  # units of more than 16 rows: 128-token tiles
+    # units of more than 16 rows: 128-token tiles; else the head dim's default tile
+    T = 128 if R == 128 else {64: 256, 80: 128, 96: 128, 128: 128, 256: 64}[d]
     s = la.la_plan_spec(3, hkv * grp, hkv, d, nq, cu_of(lengths), G)
     assert s.query_blocks == qb and s.heads_per_unit == 1
     assert la.la_schedule_export(s) == P.export(P.plan_lean(3, hkv * grp, hkv * qb, d, cu_of(lengths), G, T))
@@ -437,17 +440,18 @@ def test_query_blocks_are_units_of_their_own(d, grp, nq, qb, R):
 
 
 def test_query_blocks_of_a_single_kv_head():
-    # multi-query attention at d = 80: 64 query heads on one kv head (4 blocks of 16)
-    s = la.la_plan(2, 64, 1, 80, [0, 900, 1000], 7)
+    # multi-query attention at d = 256: 64 query heads on one kv head (4 blocks of 16)
+    s = la.la_plan(2, 64, 1, 256, [0, 900, 1000], 7)
     assert s.query_blocks == 4
-    assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 64, 4, 80, [0, 900, 1000], 7, 128))
-    s, kind, _ = la.la_plan_auto(2, 64, 1, 80, [0, 900, 1000], 152)
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 64, 4, 256, [0, 900, 1000], 7, 64))
+    s, kind, _ = la.la_plan_auto(2, 64, 1, 256, [0, 900, 1000], 152)
     assert s.query_blocks == 4
-    # at d = 96 the tcgen05 kernel holds all 64 rows
+    # at d = 80 and 96 the tcgen05 kernel holds all 64 rows
+    assert la.la_plan(2, 64, 1, 80, [0, 900, 1000], 7).query_blocks == 1
     assert la.la_plan(2, 64, 1, 96, [0, 900, 1000], 7).query_blocks == 1
     with pytest.raises(la.LeanAttentionError) as e:
         la.la_plan_kv(1, 64, 1, 80, [0, 900], heads_per_unit=2, num_sms=7)
-    assert e.value.status == la.LA_ERR_UNSUPPORTED  # query blocks: one kv head per unit
+    assert e.value.status == la.LA_ERR_UNSUPPORTED  # more than 16 rows: one kv head per unit
 
 
 def test_wide_units_hold_the_whole_group():
