@@ -40,9 +40,9 @@ int instance_rows(int rows) {
   return rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : rows <= 16 ? 16 : la::kWideRows;
 }
 
-// Query rows one unit can hold at head dim d: 128 where the tcgen05 kernel
-// is built, else 16.
-int max_unit_rows(int d) { return la::wide_supported(d) ? la::kWideRows : 16; }
+// Query rows one unit can hold at head dim d: where the tcgen05 kernel is
+// built, 128 (64 at d = 256); else 16.
+int max_unit_rows(int d) { return la::wide_supported(d) ? la::wide_max_rows(d) : 16; }
 
 // Query blocks per kv head: the fewest blocks of equal size (a divisor of
 // grp) whose grp / qb * nq query rows fit one unit; 0 when none does (nq
@@ -62,16 +62,16 @@ int unit_rows(int grp, int nq, int d) {
 }
 
 // LeanTile tokens a unit of `rows` query rows uses by default: 128 on the
-// tcgen05 kernel; else slab_tile for stream-K schedules and the table's
-// size for fixed partitions.
+// tcgen05 kernel (64 at d = 256); else slab_tile for stream-K schedules and
+// the table's size for fixed partitions.
 int unit_tile(int d, int rows, int kind) {
-  if (rows > 16) return la::kWideTile;
+  if (rows > 16) return la::wide_tile(d);
   return kind == 0 ? la::slab_tile(d, rows) : la::default_tile(d);
 }
 
 // Whether (d, T, hp) is built for units of `rows` query rows.
 bool unit_tile_supported(int d, int T, int hp, int rows) {
-  if (rows > 16) return la::wide_supported(d) && T == la::kWideTile && hp == 1;
+  if (rows > 16) return la::wide_supported(d) && T == la::wide_tile(d) && hp == 1;
   return la::tile_supported(d, T, hp);
 }
 
@@ -453,7 +453,7 @@ bool tile_supported(int d, int T, int hp) {
 }
 
 cudaError_t launch_decode(int d, int T, int grp, int hp, int dtype, const KParams& p, cudaStream_t st) {
-  if (grp == kWideRows) return (hp == 1 && T == kWideTile) ? launch_wide(d, dtype, p, st) : cudaErrorInvalidValue;
+  if (grp == kWideRows) return (hp == 1 && T == wide_tile(d)) ? launch_wide(d, dtype, p, st) : cudaErrorInvalidValue;
   switch (d * 16 + hp) {
     case 64 * 16 + 2: return launch_decode_d64_hp2(T, grp, dtype, p, st);
     case 80 * 16 + 2: return launch_decode_d80_hp2(T, grp, dtype, p, st);
@@ -486,7 +486,7 @@ cudaError_t launch_combine(int d, int grp, const CParams& p, cudaStream_t st) {
 }
 
 cudaError_t decode_capacity(int d, int T, int grp, int hp, int* per_sm) {
-  if (grp == kWideRows) return (hp == 1 && T == kWideTile) ? wide_capacity(d, per_sm) : cudaErrorInvalidValue;
+  if (grp == kWideRows) return (hp == 1 && T == wide_tile(d)) ? wide_capacity(d, per_sm) : cudaErrorInvalidValue;
   switch (d * 16 + hp) {
     case 64 * 16 + 2: return decode_capacity_d64_hp2(T, grp, per_sm);
     case 80 * 16 + 2: return decode_capacity_d80_hp2(T, grp, per_sm);
@@ -653,7 +653,7 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
   for (int b = 0; b < batch; ++b)
     if (cu_seqlens_k[b + 1] - cu_seqlens_k[b] < nq) return LA_ERR_INVALID;  // the query tokens are in the context
   const int R = instance_rows(rows);
-  const int T = tile_tokens != 0 ? tile_tokens : (rows > 16 ? la::kWideTile : la::default_tile(d) / hp);
+  const int T = tile_tokens != 0 ? tile_tokens : (rows > 16 ? la::wide_tile(d) : la::default_tile(d) / hp);
   if (!unit_tile_supported(d, T, hp, rows)) return LA_ERR_UNSUPPORTED;
   int G = num_sms;
   if (G <= 0) {
@@ -959,7 +959,7 @@ la_status la_device_capacity(int d, int grp, int* ctas_per_sm, int* num_sms) {
   if (rows == 0) return LA_ERR_UNSUPPORTED;
   la_status e = device_sms(num_sms);
   if (e != LA_OK) return e;
-  return capacity(d, rows > 16 ? la::kWideTile : la::default_tile(d), instance_rows(rows), ctas_per_sm);
+  return capacity(d, rows > 16 ? la::wide_tile(d) : la::default_tile(d), instance_rows(rows), ctas_per_sm);
 }
 
 void la_schedule_destroy(la_schedule* s) {

@@ -144,11 +144,15 @@ int stream_stages(int d, int T, int hp, int kv_layout);
 bool tile_supported(int d, int T, int hp = 1);
 
 // Units of more than 16 query rows run on the tcgen05 kernel (la_wide.cuh),
-// whose instance holds kWideRows rows, with 128-token tiles and one kv head
-// per unit; head dims 64, 80, 96 and 128 (wide_supported).
+// whose instance holds kWideRows rows, with one kv head per unit; head dims
+// 64, 80, 96 and 128 with 128-token tiles and up to 128 rows, 256 with
+// 64-token tiles and up to 64 rows (wide_supported, wide_tile,
+// wide_max_rows).
 constexpr int kWideRows = 128;
 constexpr int kWideTile = 128;
 bool wide_supported(int d);
+int wide_tile(int d);
+int wide_max_rows(int d);
 cudaError_t launch_wide(int d, int dtype, const KParams& p, cudaStream_t st);
 cudaError_t wide_capacity(int d, int* per_sm);
 cudaError_t launch_combine_wide(int d, const CParams& p, cudaStream_t st);

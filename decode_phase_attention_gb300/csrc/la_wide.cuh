@@ -1,6 +1,6 @@
 // la_wide.cuh -- the stream-K decode kernel for units of up to 128 query
-// rows (multi-query attention, wide query-head groups, a group times many
-// query tokens) on the 5th-generation tensor cores.
+// rows (64 at d = 256; multi-query attention, wide query-head groups, a
+// group times many query tokens) on the 5th-generation tensor cores.
 //
 // With a whole query-head group in one unit, a LeanTile ("3.3 LeanTile" of
 // the xllm-io review: S_f = Q K^T, the running max m and sum l, O_acc =
@@ -22,12 +22,16 @@
 // 16 the TMA producer (the 16-row kernel's producer warp, unchanged); 17
 // the MMA warp (TMEM allocation, one thread issues every tcgen05.mma).
 //
-// TMEM (512 columns): NSB S buffers of 128 columns (3 at d = 64, 2 at
-// d = 128), then O (d columns), then Q (d / 2 columns: two 16-bit values
-// per column). The softmax of tile j reads S_j (buffer j % NSB), then
-// writes P_j over it as a bf16/fp16 high part (columns +0..63) and low part
-// (+64..127), so that P V keeps fp32-level accuracy (as in the 16-row
-// kernel). S of the next tile is computed into another buffer while the
+// TMEM (512 columns): NSB S buffers of T columns (3 of 128 at d = 64 and
+// 80, 2 of 128 at d = 96 and 128, 2 of 64 at d = 256, whose LeanTile is 64
+// tokens so that S, O and Q fit), then O (d columns), then Q (d / 2
+// columns: two 16-bit values per column). At d = 256 units hold at most 64
+// rows (lane replicas): a thread then holds 32 O values, the 32 dims of
+// its quarter its replica owns; the rest come from tensor memory through
+// shared memory in pieces of 16. The softmax of tile j reads S_j (buffer
+// j % NSB), then writes P_j over it as a bf16/fp16 high part (columns
+// +0 .. T/2 - 1) and low part (+T/2 .. T - 1), so that P V keeps
+// fp32-level accuracy (as in the 16-row kernel). S of the next tile is computed into another buffer while the
 // softmax runs; it waits only for the P V that last used that buffer.
 // Keeping Q in TMEM leaves shared memory to the K/V ring (3 stages of
 // 64 KiB at d = 128, 4 of 48 KiB at d = 96, 5 of 40 KiB at d = 80, 6 of
@@ -179,7 +183,13 @@ struct WCfg {
   static constexpr int DIM = D;
   static constexpr int HPU = 1;
   static constexpr int M = 128;                 // query rows of a unit (MMA M; TMEM lanes)
-  static constexpr int T = 128;                 // LeanTile tokens (MMA N of S, K of P V)
+  // Rows a unit may hold: 128, or 64 at d = 256 (lane replicas only: 64 O
+  // values a thread for one replica would not fit the 96 registers a
+  // thread has; wider units are split into query blocks)
+  static constexpr int MAX_ROWS = D == 256 ? 64 : 128;
+  // LeanTile tokens (MMA N of S, K of P V): 128, or 64 at d = 256 so that
+  // two S buffers, O and Q fit the 512 tensor-memory columns
+  static constexpr int T = D == 256 ? 64 : 128;
   static constexpr int ROWS = T;
   static constexpr bool TC = true;              // the producer's swizzled TMA boxes
   static constexpr int W = D % 64 == 0 ? 64 : (D % 32 == 0 ? 32 : 16);  // box columns
@@ -206,7 +216,7 @@ struct WCfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = NSB * T;    // S / P buffers first, then O
   static constexpr uint32_t Q_COL = O_COL + D;  // then Q
-  static_assert(D == 64 || D == 80 || D == 96 || D == 128, "head dims of the wide kernel");
+  static_assert(D == 64 || D == 80 || D == 96 || D == 128 || D == 256, "head dims of the wide kernel");
   static_assert(M == kWideInstanceRows, "record layout of the wide kernel");
   static_assert(STAGES >= 2 && SMEM <= 232448, "shared memory per CTA");
   static_assert(NBARS * 8 + 8 + 12 <= 256, "barrier area");  // barriers, TMEM slot, 3 flag words
@@ -313,7 +323,7 @@ __device__ __forceinline__ void wide_mma(const KParams& p, int g, const E* kv,
         // 16 tokens per step; LBO: the next W head dims (next box); SBO: the next 8 tokens
         const uint64_t vd = sdesc_swz(vb + (uint32_t)kk * 16u * C::RB, C::BOX_BYTES, C::ATOM, C::SWZ);
         mma_ts(tmem + C::O_COL, pc + 8u * (uint32_t)kk, vd, kIdO, (t > 0 || kk > 0) ? 1u : 0u);
-        mma_ts(tmem + C::O_COL, pc + 64u + 8u * (uint32_t)kk, vd, kIdO, 1u);
+        mma_ts(tmem + C::O_COL, pc + (uint32_t)(C::T / 2) + 8u * (uint32_t)kk, vd, kIdO, 1u);
       }
       tc_commit(&pv_done[j % C::NSB]);
       tc_commit(&empty[cur]);
@@ -360,12 +370,12 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
   // query row and each replica takes half of every tile's tokens, so that
   // all four sub-partitions compute 2^x; P is zero in the other replica's
   // half, and the two O rows are summed at the end.
-  constexpr int TPT = 32 / NREP;  // tokens of a tile per thread
+  constexpr int TPT = T / 4 / NREP;  // tokens of a tile per thread
   constexpr int RM = C::M / NREP;  // rows of one exchange slot
   const int half = NREP == 2 ? (qd >> 1) : 0;
   const int row = NREP == 2 ? (r & 63) : r;  // the query row lane r holds
-  const int toff = NREP == 2 ? 64 * half + 16 * cq : 32 * cq;       // this thread's first token
-  const int tother = NREP == 2 ? 64 * (1 - half) + 16 * cq : 0;     // the other replica's (P = 0)
+  const int toff = NREP == 2 ? (T / 2) * half + TPT * cq : TPT * cq;        // this thread's first token
+  const int tother = NREP == 2 ? (T / 2) * (1 - half) + TPT * cq : 0;      // the other replica's (P = 0)
   float* stage_o = red + 3 * 4 * C::M;  // [64][65] O quarters handed between replicas
   const int s_begin = p.cta_seg[g], s_end = p.cta_seg[g + 1];
   const uint32_t ready = epoch + 1u;
@@ -417,7 +427,10 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
           qw[2 * k + 1] = v.y;
         }
       }
-      if constexpr (D / 8 == 16) {
+      if constexpr (D / 8 == 32) {  // d = 256: 32 columns, in pieces of 16
+        tmem_st16(trow + C::Q_COL + 32u * cq, qw);
+        tmem_st16(trow + C::Q_COL + 32u * cq + 16u, qw + 16);
+      } else if constexpr (D / 8 == 16) {
         tmem_st16(trow + C::Q_COL + 16u * cq, qw);
       } else if constexpr (D / 8 == 8) {
         tmem_st8(trow + C::Q_COL + 8u * cq, qw);
@@ -449,7 +462,7 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
       float mq = -INFINITY;
       float xs = 1.f;  // u holds scores to multiply by xs: raw (xs = qscale) or already scaled (1)
       if (work) {
-        tmem_ld16(sc + (uint32_t)toff, u);
+        if constexpr (TPT >= 16) tmem_ld16(sc + (uint32_t)toff, u); else tmem_ld8(sc + (uint32_t)toff, u);
         if constexpr (TPT == 32) tmem_ld16(sc + (uint32_t)toff + 16u, u + 16);
         tmem_wait_ld_regs<TPT>(u);
         // visible tokens of this thread's share
@@ -511,15 +524,17 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
             lo[k] = Elem<E>::pack(p0 - h.x, p1 - h.y);
           }
         }
+        // high parts in columns 0 .. T/2 - 1 of the buffer, low parts in
+        // T/2 .. T - 1 (two 16-bit values a column)
         if constexpr (NREP == 1) {
-          tmem_st16(sc + 16u * cq, hi);        // tokens 32 cq .. 32 cq + 31: high parts
-          tmem_st16(sc + 64u + 16u * cq, lo);  // and low parts
+          tmem_stn<TPT / 2>(sc + (uint32_t)(toff / 2), hi);  // this thread's TPT tokens
+          tmem_stn<TPT / 2>(sc + (uint32_t)(T / 2 + toff / 2), lo);
         } else {
           const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-          tmem_st8(sc + (uint32_t)(toff / 2), hi);  // this replica's 16 tokens
-          tmem_st8(sc + 64u + (uint32_t)(toff / 2), lo);
-          tmem_st8(sc + (uint32_t)(tother / 2), zero);  // the other replica's: P = 0 in this lane
-          tmem_st8(sc + 64u + (uint32_t)(tother / 2), zero);
+          tmem_stn<TPT / 2>(sc + (uint32_t)(toff / 2), hi);  // this replica's tokens
+          tmem_stn<TPT / 2>(sc + (uint32_t)(T / 2 + toff / 2), lo);
+          tmem_stn<TPT / 2>(sc + (uint32_t)(tother / 2), zero);  // the other replica's: P = 0 in this lane
+          tmem_stn<TPT / 2>(sc + (uint32_t)(T / 2 + tother / 2), zero);
         }
         lq += ls0 + ls1;
       }
@@ -576,14 +591,18 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
     const bool have_o =
         alive && wide_wait_warp(p, g, &pv_done[(j - 1u) % C::NSB], ((j - 1u) / C::NSB) & 1u, abort_flag);
     tc_fence_after();
-    float o[OQ];
+    // d = 256 (lane replicas only): each thread reads just the 32 dims of
+    // its quarter it will own (its replica half's), so no thread holds more
+    // than 32 O values; the other half's come through shared memory below
+    constexpr int OR = D == 256 ? OQ / 2 : OQ;  // O values a thread holds
+    float o[OR];
 #pragma unroll
-    for (int c = 0; c < OQ; ++c) o[c] = 0.f;
+    for (int c = 0; c < OR; ++c) o[c] = 0.f;
     if (have_o && warp_live) {
 #pragma unroll
-      for (int c = 0; c < OQ / OC; ++c) {
+      for (int c = 0; c < OR / OC; ++c) {
         uint32_t v[OC];
-        const uint32_t oc = trow + C::O_COL + (uint32_t)(OQ * cq + OC * c);
+        const uint32_t oc = trow + C::O_COL + (uint32_t)(OQ * cq + (D == 256 ? OR * half : 0) + OC * c);
         tmem_ldn<OC>(oc, v);
         tmem_wait_ld_regs<OC>(v);
 #pragma unroll
@@ -734,23 +753,48 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
       const int db = OQ * cq + (NREP == 2 ? NO * half : 0);  // first dim this thread owns
       if constexpr (NREP == 2) {
         l += (lsum[4 * RM + row] + lsum[5 * RM + row]) + (lsum[6 * RM + row] + lsum[7 * RM + row]);
-        // round 0: the replica in lanes 64..127 hands dims [0, NO) of its
-        // quarter to the one in 0..63; round 1: the other way, dims [NO, OQ)
+        if constexpr (D == 256) {
+          // each half already holds its own 32 dims in o[0, 32); the other
+          // half's partial for them comes from its tensor memory in pieces
+          // of 16 (round rnd: half 1 - rnd gives, half rnd receives)
   #pragma unroll
-        for (int rnd = 0; rnd < 2; ++rnd) {
-          if (half != rnd) {
+          for (int rnd = 0; rnd < 2; ++rnd)
   #pragma unroll
-            for (int k = 0; k < NO; ++k) stage_o[row * 65 + cq * 16 + k] = o[NO * rnd + k];
+            for (int ch = 0; ch < NO / 16; ++ch) {
+              if (half != rnd && have_o && warp_live) {
+                uint32_t v[16];
+                tc_fence_after();
+                tmem_ld16(trow + C::O_COL + (uint32_t)(OQ * cq + NO * rnd + 16 * ch), v);
+                tmem_wait_ld_regs<16>(v);
+  #pragma unroll
+                for (int k = 0; k < 16; ++k) stage_o[row * 65 + cq * 16 + k] = __uint_as_float(v[k]);
+              }
+              softmax_sync();
+              if (half == rnd) {
+  #pragma unroll
+                for (int k = 0; k < 16; ++k) o[16 * ch + k] += stage_o[row * 65 + cq * 16 + k];
+              }
+              softmax_sync();
+            }
+        } else {
+          // round 0: the replica in lanes 64..127 hands dims [0, NO) of its
+          // quarter to the one in 0..63; round 1: the other way, dims [NO, OQ)
+  #pragma unroll
+          for (int rnd = 0; rnd < 2; ++rnd) {
+            if (half != rnd) {
+  #pragma unroll
+              for (int k = 0; k < NO; ++k) stage_o[row * 65 + cq * 16 + k] = o[NO * rnd + k];
+            }
+            softmax_sync();
+            if (half == rnd) {
+  #pragma unroll
+              for (int k = 0; k < NO; ++k) o[NO * rnd + k] += stage_o[row * 65 + cq * 16 + k];
+            }
+            softmax_sync();
           }
-          softmax_sync();
-          if (half == rnd) {
   #pragma unroll
-            for (int k = 0; k < NO; ++k) o[NO * rnd + k] += stage_o[row * 65 + cq * 16 + k];
-          }
-          softmax_sync();
+          for (int k = 0; k < NO; ++k) o[k] = half ? o[NO + k] : o[k];  // this thread's dims into o[0, NO)
         }
-  #pragma unroll
-        for (int k = 0; k < NO; ++k) o[k] = half ? o[NO + k] : o[k];  // this thread's dims into o[0, NO)
       }
       const bool poisoned = (*abort_flag != 0) || !ok || !have_o;
       // Records are column-major over the unit's rows (wide_rec): element
@@ -1046,8 +1090,10 @@ cudaError_t launch_wide_t(const KParams& p, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(lean_wide_kernel<D, E, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    if (e != cudaSuccess) return e;
+    if constexpr (C::MAX_ROWS > 64) {
+      e = cudaFuncSetAttribute(lean_wide_kernel<D, E, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+      if (e != cudaSuccess) return e;
+    }
     e = cudaFuncSetAttribute(lean_wide_kernel<D, E, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     configured_device = dev;
@@ -1060,10 +1106,14 @@ cudaError_t launch_wide_t(const KParams& p, cudaStream_t st) {
   else
     e = encode_kv_maps(p.k, p.v, p.kv_rows, D, C::T, C::W, (int)Elem<E>::kTmaType, &mk, &mv);
   if (e != cudaSuccess) return e;
-  if (p.rows <= 64)
-    lean_wide_kernel<D, E, 2><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
-  else
-    lean_wide_kernel<D, E, 1><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
+  if (p.rows > C::MAX_ROWS) return cudaErrorInvalidValue;  // the planner splits wider units into query blocks
+  if constexpr (C::MAX_ROWS > 64) {
+    if (p.rows > 64) {
+      lean_wide_kernel<D, E, 1><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
+      return cudaGetLastError();
+    }
+  }
+  lean_wide_kernel<D, E, 2><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
   return cudaGetLastError();
 }
 
@@ -1077,10 +1127,11 @@ cudaError_t launch_wide_combine_t(const CParams& p, cudaStream_t st) {
 template <int D>
 cudaError_t wide_capacity_t(int* per_sm) {
   using C = WCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(lean_wide_kernel<D, __nv_bfloat16, 1>,
+  constexpr int kRep = C::MAX_ROWS > 64 ? 1 : 2;  // an instance the head dim builds
+  cudaError_t e = cudaFuncSetAttribute(lean_wide_kernel<D, __nv_bfloat16, kRep>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lean_wide_kernel<D, __nv_bfloat16, 1>, C::NTHREADS,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, lean_wide_kernel<D, __nv_bfloat16, kRep>, C::NTHREADS,
                                                        C::SMEM);
 }
 

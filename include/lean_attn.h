@@ -85,11 +85,11 @@ enum {
  *                      kv head run as one unit on the 16-row kernel; a group
  *                      that is not a power of two runs on the next larger
  *                      instance (1, 2, 4, 8 or 16 rows), whose spare rows are
- *                      zero queries never written out. At d = 64, 80, 96, 128
- *                      a unit of 17-128 rows (e.g. multi-query attention) runs
- *                      on the tcgen05 kernel (128-row instance, 128-token
- *                      tiles). A kv head with more rows than a unit holds
- *                      (128 at d = 64, 80, 96, 128; 16 at d = 256) is split into
+ *                      zero queries never written out. A unit of 17-128
+ *                      rows (17-64 at d = 256; e.g. multi-query attention)
+ *                      runs on the tcgen05 kernel (128-lane instance,
+ *                      128-token tiles, 64 at d = 256). A kv head with more
+ *                      rows than a unit holds (128; 64 at d = 256) is split into
  *                      query blocks: the fewest equal blocks of consecutive
  *                      query heads that fit (qb blocks of grp / qb heads, qb
  *                      dividing grp); every block is a unit of its own that
@@ -134,7 +134,8 @@ la_status la_plan(int batch, int hq, int hkv, int d, const int32_t* cu_seqlens_k
  *                the table's 128 stays faster (2-3 %), and so it does for
  *                la_plan_fixed, whose few busy SMs each need the deeper
  *                shared-memory ring of the larger tile. Units of more
- *                than 16 query rows (the tcgen05 kernel) take 128 only.
+ *                than 16 query rows (the tcgen05 kernel) take 128 only
+ *                (64 at d = 256).
  * Other arguments and rules as la_plan. LA_ERR_UNSUPPORTED for a (d, T)
  * that is not built.
  */
@@ -154,8 +155,8 @@ la_status la_plan_ex(int batch, int hq, int hkv, int d, const int32_t* cu_seqlen
  * their split are those of la_plan (K/V are read once per kv head for all
  * grp * nq query rows, as many as a unit holds; above that the kv head's
  * query heads are split into query blocks as in la_plan, each of
- * grp / qb * nq rows). Requires nq <= 128 at d = 64, 80, 96 and 128, nq <= 16
- * otherwise (LA_ERR_UNSUPPORTED), and L_b >= nq for every request
+ * grp / qb * nq rows). Requires nq <= 128 (64 at d = 256;
+ * LA_ERR_UNSUPPORTED), and L_b >= nq for every request
  * (LA_ERR_INVALID); nq = 1 is la_plan.
  */
 la_status la_plan_spec(int batch, int hq, int hkv, int d, int nq, const int32_t* cu_seqlens_k, int num_sms,
@@ -309,8 +310,8 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
  *                   one or two query rows: 16-token pages read 13 % slower
  *                   with 64) divided by heads_per_unit, so a tile still
  *                   holds the same bytes (only these defaults are built for
- *                   more than one head per unit); 128 for units of more
- *                   than 16 query rows (the tcgen05 kernel).
+ *                   more than one head per unit); 128 (64 at d = 256) for
+ *                   units of more than 16 query rows (the tcgen05 kernel).
  *   num_sms, out    as la_plan
  * Units are (request, group of heads_per_unit consecutive kv heads) in
  * request-major order, tiles(b) = ceil(L_b / tile_tokens), and the split

@@ -403,9 +403,9 @@ def test_groups_that_are_not_powers_of_two(grp):
 # (d = 64, 96, 128), else 16: the fewest equal blocks of whole query heads
 # whose rows fit.
 QUERY_BLOCKS = [
-    (256, 32, 1, 2, 16), (256, 24, 1, 2, 16), (256, 17, 1, 17, 1), (256, 18, 1, 2, 16), (256, 34, 1, 17, 2),
-    (256, 40, 1, 4, 16), (256, 48, 1, 3, 16), (256, 64, 1, 4, 16), (256, 128, 1, 8, 16), (256, 8, 3, 2, 16),
-    (256, 8, 4, 2, 16), (256, 16, 2, 2, 16), (256, 4, 5, 2, 16), (256, 1, 16, 1, 16), (256, 2, 16, 2, 16),
+    (256, 32, 1, 1, 128), (256, 17, 1, 1, 128), (256, 64, 1, 1, 128), (256, 128, 1, 2, 128),
+    (256, 96, 1, 2, 128), (256, 200, 1, 4, 128), (256, 65, 1, 5, 16), (256, 2, 40, 2, 128), (256, 8, 3, 1, 128),
+    (256, 1, 16, 1, 16), (256, 34, 2, 2, 128), (256, 130, 1, 5, 128),
     (80, 32, 1, 1, 128), (80, 17, 1, 1, 128), (80, 128, 1, 1, 128), (80, 256, 1, 2, 128), (80, 8, 3, 1, 128),
     (80, 1, 16, 1, 16), (80, 2, 100, 2, 128),
     (64, 32, 1, 1, 128), (64, 17, 1, 1, 128), (64, 128, 1, 1, 128), (64, 256, 1, 2, 128), (64, 192, 1, 2, 128),
@@ -421,8 +421,8 @@ def test_query_blocks_are_units_of_their_own(d, grp, nq, qb, R):
     # hkv * qb heads of grp / qb query heads each
     lengths = [700, 128, 3000]
     hkv, G = 2, 11
-    # units of more than 16 rows: 128-token tiles; else the head dim's default tile
-    T = 128 if R == 128 else {64: 256, 80: 128, 96: 128, 128: 128, 256: 64}[d]
+    # units of more than 16 rows: 128-token tiles (64 at d = 256); else the head dim's default tile
+    T = (64 if d == 256 else 128) if R == 128 else {64: 256, 80: 128, 96: 128, 128: 128, 256: 64}[d]
     s = la.la_plan_spec(3, hkv * grp, hkv, d, nq, cu_of(lengths), G)
     assert s.query_blocks == qb and s.heads_per_unit == 1
     assert la.la_schedule_export(s) == P.export(P.plan_lean(3, hkv * grp, hkv * qb, d, cu_of(lengths), G, T))
@@ -440,15 +440,16 @@ def test_query_blocks_are_units_of_their_own(d, grp, nq, qb, R):
 
 
 def test_query_blocks_of_a_single_kv_head():
-    # multi-query attention at d = 256: 64 query heads on one kv head (4 blocks of 16)
-    s = la.la_plan(2, 64, 1, 256, [0, 900, 1000], 7)
-    assert s.query_blocks == 4
-    assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 64, 4, 256, [0, 900, 1000], 7, 64))
-    s, kind, _ = la.la_plan_auto(2, 64, 1, 256, [0, 900, 1000], 152)
-    assert s.query_blocks == 4
-    # at d = 80 and 96 the tcgen05 kernel holds all 64 rows
-    assert la.la_plan(2, 64, 1, 80, [0, 900, 1000], 7).query_blocks == 1
-    assert la.la_plan(2, 64, 1, 96, [0, 900, 1000], 7).query_blocks == 1
+    # multi-query attention at d = 256: 128 query heads on one kv head (2 blocks of 64)
+    s = la.la_plan(2, 128, 1, 256, [0, 900, 1000], 7)
+    assert s.query_blocks == 2
+    assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 128, 2, 256, [0, 900, 1000], 7, 64))
+    s, kind, _ = la.la_plan_auto(2, 128, 1, 256, [0, 900, 1000], 152)
+    assert s.query_blocks == 2
+    # at d = 80 and 96 the tcgen05 kernel holds all 128 rows, at d = 256 64
+    assert la.la_plan(2, 128, 1, 80, [0, 900, 1000], 7).query_blocks == 1
+    assert la.la_plan(2, 128, 1, 96, [0, 900, 1000], 7).query_blocks == 1
+    assert la.la_plan(2, 64, 1, 256, [0, 900, 1000], 7).query_blocks == 1
     with pytest.raises(la.LeanAttentionError) as e:
         la.la_plan_kv(1, 64, 1, 80, [0, 900], heads_per_unit=2, num_sms=7)
     assert e.value.status == la.LA_ERR_UNSUPPORTED  # more than 16 rows: one kv head per unit

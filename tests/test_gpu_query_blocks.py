@@ -1,7 +1,7 @@
 """GPU parity for kv heads with more than 16 query rows (grouped-query groups
 above 16, multi-query attention, or group x query tokens above 16). At
-d = 64, 80, 96 and 128 a unit of up to 128 rows runs on the tcgen05 kernel;
-above that, and at d = 256 above 16 rows, the query heads of a kv head
+d = 64, 80, 96 and 128 a unit of up to 128 rows (64 at d = 256) runs on the
+tcgen05 kernel; above that the query heads of a kv head
 are split into equal blocks, each a stream-K unit of its own over the kv
 head's K/V. The float64 oracle computes every row from the plain definition,
 unaware of units and blocks."""
@@ -26,9 +26,9 @@ def _device():
 
 # (d, hq, hkv, query blocks per kv head)
 SLAB = [(128, 32, 1, 1), (128, 64, 1, 1), (64, 48, 2, 1), (96, 34, 2, 1), (80, 34, 2, 1), (80, 48, 2, 1),
-        (256, 64, 2, 2), (128, 40, 2, 1), (64, 128, 1, 1), (128, 256, 1, 2), (64, 17, 1, 1), (128, 130, 1, 2),
+        (256, 64, 2, 1), (128, 40, 2, 1), (64, 128, 1, 1), (128, 256, 1, 2), (64, 17, 1, 1), (128, 130, 1, 2),
         (96, 64, 1, 1), (96, 128, 1, 1), (80, 64, 1, 1), (96, 256, 1, 2), (80, 128, 1, 1), (80, 17, 1, 1),
-        (80, 256, 1, 2), (256, 34, 2, 17), (256, 48, 2, 2)]
+        (80, 256, 1, 2), (256, 34, 2, 1), (256, 48, 2, 1), (256, 128, 1, 2), (256, 17, 1, 1), (256, 200, 2, 2)]
 
 
 @pytest.mark.parametrize("d,hq,hkv,qb", SLAB)
@@ -51,7 +51,7 @@ def ref_spec(w, q, k, v):
 # (d, grp, nq, query blocks): group x query tokens above 16
 SPEC = [(128, 8, 4, 1), (64, 16, 2, 1), (64, 4, 5, 1), (128, 32, 2, 1), (96, 3, 7, 1), (80, 3, 7, 1),
         (128, 2, 16, 1), (128, 16, 9, 2), (64, 1, 100, 1), (96, 8, 4, 1), (80, 8, 4, 1), (128, 3, 40, 1),
-        (80, 1, 100, 1), (256, 3, 7, 3), (256, 8, 4, 2)]
+        (80, 1, 100, 1), (256, 3, 7, 1), (256, 8, 4, 1), (256, 8, 9, 2), (256, 1, 40, 1)]
 
 
 @pytest.mark.parametrize("d,grp,nq,qb", SPEC)
@@ -69,7 +69,8 @@ def test_query_blocks_with_several_query_tokens(d, grp, nq, qb):
 @pytest.mark.parametrize("layout", ["token_major", "paged"])
 @pytest.mark.parametrize("d,hq,hkv,nq,qb", [(128, 32, 1, 1, 1), (64, 48, 2, 1, 1), (80, 64, 2, 1, 1),
                                             (128, 16, 2, 3, 1), (96, 40, 2, 1, 1), (80, 40, 2, 1, 1),
-                                            (64, 256, 1, 1, 2), (256, 64, 2, 1, 2), (80, 20, 2, 2, 1)])
+                                            (64, 256, 1, 1, 2), (256, 64, 2, 1, 1), (80, 20, 2, 2, 1),
+                                            (256, 256, 2, 1, 2)])
 def test_query_blocks_on_caches(layout, d, hq, hkv, nq, qb):
     from oracle import layouts
     lengths = [700, 64, 2000]

@@ -84,7 +84,7 @@ def test_trace_records_the_planned_work_of_every_cta():
     assert np.all(tr[:, 1] <= tr[:, 2]) and np.all(tr[:, 2] <= tr[:, 3]) and np.all(tr[:, 3] <= tr[:, 5])
 
 
-@pytest.mark.parametrize("d", [64, 80, 96, 128])
+@pytest.mark.parametrize("d", [64, 80, 96, 128, 256])
 def test_ring_depth_does_not_change_the_result(d):
     w = workloads.custom(2, 64, 2, d, "bf16", [3000, 777])
     q, k, v, cu = workloads.make_inputs(w, seed=d, device="cuda")
@@ -102,7 +102,7 @@ def test_ring_depth_does_not_change_the_result(d):
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("d,hq", [(128, 32), (80, 32), (80, 96)])
+@pytest.mark.parametrize("d,hq", [(128, 32), (80, 32), (80, 96), (256, 48)])
 def test_sixteen_bit_outputs_are_the_fp32_outputs_rounded(out_dtype, d, hq):
     # 32 rows: lane replicas; 96 rows at d = 80: one replica (20-dim O quarters)
     w = workloads.custom(2, hq, 1, d, "f16", [2000, 513])
