@@ -922,6 +922,151 @@ __device__ __forceinline__ void merge_f4(float& M, float& Ls, float4& O, float m
   M = mn;
 }
 
+// The host merge of many peers on the CTA's last segment (called from
+// consume). Out of line: compiled inline, its code slowed the CUDA-core tile
+// loop of the d = 80 and 96 instances by 12 % (same-box A/B, one CTA per
+// unit and stream-K), though the loop's own code did not change.
+template <class C, typename E>
+__device__ __noinline__ void host_merge_staged(const KParams& p, int g, int npeer, E* kv, uint64_t* stg, float* M,
+                                               float* Lsum, float4* O, bool* fail) {
+  constexpr int D = C::DIM;
+  constexpr int kVecs = C::MROWS * D / 4;  // vectors of 4 consecutive outputs of a unit
+  const int tid = threadIdx.x, warp = tid >> 5;
+  // Many peers, and the CTA's last segment: every tile has been
+  // consumed and the producer issues no more copies, so the ring
+  // and the merge area after it (read above) are idle. The peers'
+  // records come in by bulk copies (one per batch: the records of
+  // consecutive CTAs are contiguous) in batches of up to NBAT into
+  // two buffers, so the next batch's copy overlaps this batch's
+  // merge. f is associative, so a batch of k partials reduces in
+  // one step: per record row, the new maximum and the rescale of
+  // the running partial, then every peer's weight 2^(m - max) --
+  // each computed once per (row, peer) into shared memory -- then
+  // the weighted sums of O (16-byte vectors) and of l.
+  constexpr int kRows = C::MROWS;
+  float* scal = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(kv) + C::SCAL_OFF);
+  float* s_m = scal;              // [kRows] running maximum
+  float* s_a = scal + kRows;      // [kRows] rescale of the running partial in this batch
+  float* s_l = scal + 2 * kRows;  // [kRows] running l
+  float* s_w = scal + 3 * kRows;  // [NBAT][kRows] peer weights of this batch
+#pragma unroll
+  for (int i = 0; i < C::V4; ++i) {
+    const int v = tid + i * C::NCT;
+    if (v < kVecs && 4 * v % D == 0) {
+      s_m[4 * v / D] = M[i];
+      s_l[4 * v / D] = Lsum[i];
+    }
+  }
+  // A few KB (long MHA contexts: a handful of one-row records)
+  // arrive sooner as every thread's 16-byte copies; more, as one
+  // bulk copy per batch.
+  const bool by_thread = (size_t)npeer * C::RS * 4 <= 32768;
+  auto issue = [&](int first, int n, int buf) {
+    unsigned char* dst = reinterpret_cast<unsigned char*>(kv) + (size_t)buf * C::NBAT * C::RS * 4;
+    const float* src = p.recs + (size_t)(g + 1 + first) * C::RS;
+    if (by_thread) {
+      const uint32_t d0 = smem_u32(dst);
+      for (int i = tid; i < n * (C::RS / 4); i += C::NCT)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d0 + 16u * (uint32_t)i),
+                     "l"(src + 4 * (size_t)i)
+                     : "memory");
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    } else if (tid == 0) {
+      const uint32_t bytes = (uint32_t)n * (uint32_t)(C::RS * 4);
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // records written by other CTAs
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring was last read here
+      mbar_arrive_expect_tx(&stg[buf], bytes);
+      bulk_g2s(dst, src, bytes, &stg[buf], l2_evict_first_policy());
+    }
+  };
+  const int nbat = (npeer + C::NBAT - 1) / C::NBAT;
+  issue(0, npeer < C::NBAT ? npeer : C::NBAT, 0);
+  bool staged = true;
+  for (int bi = 0; bi < nbat; ++bi) {
+    const int first = bi * C::NBAT;
+    const int n = npeer - first < C::NBAT ? npeer - first : C::NBAT;
+    if (bi + 1 < nbat) {
+      const int rest = npeer - first - C::NBAT;
+      issue(first + C::NBAT, rest < C::NBAT ? rest : C::NBAT, (bi + 1) & 1);
+    }
+    if (by_thread) {
+      if (bi + 1 < nbat)
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+      else
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+    } else {
+      // an issued copy is waited for (bounded) even after an abort
+      volatile int no_abort = 0;
+      if (!mbar_wait_bounded(&stg[bi & 1], (uint32_t)(bi >> 1) & 1u, &no_abort, p.spin_ns)) staged = false;
+    }
+    consumer_sync(C::NCT);  // batch bi is in shared memory (and s_m, s_l written)
+    const float* st = reinterpret_cast<const float*>(kv) + (size_t)(bi & 1) * C::NBAT * C::RS;
+    // per row, one warp (lanes over the batch's peers): the new
+    // maximum, the rescale of the running partial, every peer's
+    // weight and the new l
+    static_assert(C::NBAT <= 64, "two peers per lane");
+    for (int rr = warp; rr < kRows; rr += C::NCW) {
+      const int lane = tid & 31;
+      const float mo = s_m[rr];
+      float mu[2], lu[2];
+      float mb = mo;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int u = lane + 32 * q;
+        mu[q] = u < n ? st[u * C::RS + rr * C::REC] : -INFINITY;
+        lu[q] = u < n ? st[u * C::RS + rr * C::REC + 1] : 0.f;
+        mb = fmaxf(mb, mu[q]);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
+      float ls = 0.f;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int u = lane + 32 * q;
+        const float w = (mu[q] == -INFINITY) ? 0.f : ex2(mu[q] - mb);  // NaN m (poisoned) propagates
+        if (u < n) s_w[u * kRows + rr] = w;
+        ls = fmaf(w, lu[q], ls);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(kFull, ls, off);
+      if (lane == 0) {
+        const float a = (mb == -INFINITY || mo == -INFINITY) ? (mb == -INFINITY ? 1.f : 0.f) : ex2(mo - mb);
+        s_a[rr] = a;
+        s_m[rr] = mb;
+        s_l[rr] = fmaf(a, s_l[rr], ls);
+      }
+    }
+    consumer_sync(C::NCT);  // the batch's scalars are in shared memory
+    // the weighted sums of O: peers outer, this thread's vectors
+    // inner (V4 independent chains per step, 16-byte loads)
+    {
+      const float* rp[C::V4];
+      const float* wp[C::V4];
+#pragma unroll
+      for (int i = 0; i < C::V4; ++i) {
+        const int v = tid + i * C::NCT;
+        const int rr = v < kVecs ? 4 * v / D : 0, cc = 4 * v % D;
+        rp[i] = st + rr * C::REC + kRecO + cc;
+        wp[i] = s_w + rr;
+        O[i] = scale4(s_a[rr], O[i]);
+      }
+#pragma unroll 2
+      for (int u = 0; u < n; ++u) {
+#pragma unroll
+        for (int i = 0; i < C::V4; ++i)
+          O[i] = fma4(wp[i][u * kRows], *reinterpret_cast<const float4*>(rp[i] + u * C::RS), O[i]);
+      }
+    }
+    consumer_sync(C::NCT);  // buffer bi & 1, the scalars and s_l are settled
+  }
+  if (!staged) *fail = true;
+#pragma unroll
+  for (int i = 0; i < C::V4; ++i) {
+    const int v = tid + i * C::NCT;
+    if (v < kVecs) Lsum[i] = s_l[4 * v / D];
+  }
+}
+
 template <int D, int T, int GRP, typename E, int HP>
 __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t* full, uint64_t* empty, uint64_t* stg,
                                         float* mrg, volatile int* abort_flag, uint32_t epoch) {
@@ -1071,139 +1216,7 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
         } else {
           int p0 = 0;
           if (si == s_end - 1 && npeer > C::PB) {
-            // Many peers, and the CTA's last segment: every tile has been
-            // consumed and the producer issues no more copies, so the ring
-            // and the merge area after it (read above) are idle. The peers'
-            // records come in by bulk copies (one per batch: the records of
-            // consecutive CTAs are contiguous) in batches of up to NBAT into
-            // two buffers, so the next batch's copy overlaps this batch's
-            // merge. f is associative, so a batch of k partials reduces in
-            // one step: per record row, the new maximum and the rescale of
-            // the running partial, then every peer's weight 2^(m - max) --
-            // each computed once per (row, peer) into shared memory -- then
-            // the weighted sums of O (16-byte vectors) and of l.
-            constexpr int kRows = C::MROWS;
-            float* scal = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(kv) + C::SCAL_OFF);
-            float* s_m = scal;              // [kRows] running maximum
-            float* s_a = scal + kRows;      // [kRows] rescale of the running partial in this batch
-            float* s_l = scal + 2 * kRows;  // [kRows] running l
-            float* s_w = scal + 3 * kRows;  // [NBAT][kRows] peer weights of this batch
-#pragma unroll
-            for (int i = 0; i < C::V4; ++i) {
-              const int v = tid + i * C::NCT;
-              if (v < kVecs && 4 * v % D == 0) {
-                s_m[4 * v / D] = M[i];
-                s_l[4 * v / D] = Lsum[i];
-              }
-            }
-            // A few KB (long MHA contexts: a handful of one-row records)
-            // arrive sooner as every thread's 16-byte copies; more, as one
-            // bulk copy per batch.
-            const bool by_thread = (size_t)npeer * C::RS * 4 <= 32768;
-            auto issue = [&](int first, int n, int buf) {
-              unsigned char* dst = reinterpret_cast<unsigned char*>(kv) + (size_t)buf * C::NBAT * C::RS * 4;
-              const float* src = p.recs + (size_t)(g + 1 + first) * C::RS;
-              if (by_thread) {
-                const uint32_t d0 = smem_u32(dst);
-                for (int i = tid; i < n * (C::RS / 4); i += C::NCT)
-                  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d0 + 16u * (uint32_t)i),
-                               "l"(src + 4 * (size_t)i)
-                               : "memory");
-                asm volatile("cp.async.commit_group;" ::: "memory");
-              } else if (tid == 0) {
-                const uint32_t bytes = (uint32_t)n * (uint32_t)(C::RS * 4);
-                asm volatile("fence.proxy.async.global;" ::: "memory");  // records written by other CTAs
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the ring was last read here
-                mbar_arrive_expect_tx(&stg[buf], bytes);
-                bulk_g2s(dst, src, bytes, &stg[buf], l2_evict_first_policy());
-              }
-            };
-            const int nbat = (npeer + C::NBAT - 1) / C::NBAT;
-            issue(0, npeer < C::NBAT ? npeer : C::NBAT, 0);
-            bool staged = true;
-            for (int bi = 0; bi < nbat; ++bi) {
-              const int first = bi * C::NBAT;
-              const int n = npeer - first < C::NBAT ? npeer - first : C::NBAT;
-              if (bi + 1 < nbat) {
-                const int rest = npeer - first - C::NBAT;
-                issue(first + C::NBAT, rest < C::NBAT ? rest : C::NBAT, (bi + 1) & 1);
-              }
-              if (by_thread) {
-                if (bi + 1 < nbat)
-                  asm volatile("cp.async.wait_group 1;" ::: "memory");
-                else
-                  asm volatile("cp.async.wait_group 0;" ::: "memory");
-              } else {
-                // an issued copy is waited for (bounded) even after an abort
-                volatile int no_abort = 0;
-                if (!mbar_wait_bounded(&stg[bi & 1], (uint32_t)(bi >> 1) & 1u, &no_abort, p.spin_ns)) staged = false;
-              }
-              consumer_sync(C::NCT);  // batch bi is in shared memory (and s_m, s_l written)
-              const float* st = reinterpret_cast<const float*>(kv) + (size_t)(bi & 1) * C::NBAT * C::RS;
-              // per row, one warp (lanes over the batch's peers): the new
-              // maximum, the rescale of the running partial, every peer's
-              // weight and the new l
-              static_assert(C::NBAT <= 64, "two peers per lane");
-              for (int rr = warp; rr < kRows; rr += C::NCW) {
-                const int lane = tid & 31;
-                const float mo = s_m[rr];
-                float mu[2], lu[2];
-                float mb = mo;
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                  const int u = lane + 32 * q;
-                  mu[q] = u < n ? st[u * C::RS + rr * C::REC] : -INFINITY;
-                  lu[q] = u < n ? st[u * C::RS + rr * C::REC + 1] : 0.f;
-                  mb = fmaxf(mb, mu[q]);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, off));
-                float ls = 0.f;
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                  const int u = lane + 32 * q;
-                  const float w = (mu[q] == -INFINITY) ? 0.f : ex2(mu[q] - mb);  // NaN m (poisoned) propagates
-                  if (u < n) s_w[u * kRows + rr] = w;
-                  ls = fmaf(w, lu[q], ls);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(kFull, ls, off);
-                if (lane == 0) {
-                  const float a = (mb == -INFINITY || mo == -INFINITY) ? (mb == -INFINITY ? 1.f : 0.f) : ex2(mo - mb);
-                  s_a[rr] = a;
-                  s_m[rr] = mb;
-                  s_l[rr] = fmaf(a, s_l[rr], ls);
-                }
-              }
-              consumer_sync(C::NCT);  // the batch's scalars are in shared memory
-              // the weighted sums of O: peers outer, this thread's vectors
-              // inner (V4 independent chains per step, 16-byte loads)
-              {
-                const float* rp[C::V4];
-                const float* wp[C::V4];
-#pragma unroll
-                for (int i = 0; i < C::V4; ++i) {
-                  const int v = tid + i * C::NCT;
-                  const int rr = v < kVecs ? 4 * v / D : 0, cc = 4 * v % D;
-                  rp[i] = st + rr * C::REC + kRecO + cc;
-                  wp[i] = s_w + rr;
-                  O[i] = scale4(s_a[rr], O[i]);
-                }
-#pragma unroll 2
-                for (int u = 0; u < n; ++u) {
-#pragma unroll
-                  for (int i = 0; i < C::V4; ++i)
-                    O[i] = fma4(wp[i][u * kRows], *reinterpret_cast<const float4*>(rp[i] + u * C::RS), O[i]);
-                }
-              }
-              consumer_sync(C::NCT);  // buffer bi & 1, the scalars and s_l are settled
-            }
-            if (!staged) fail = true;
-#pragma unroll
-            for (int i = 0; i < C::V4; ++i) {
-              const int v = tid + i * C::NCT;
-              if (v < kVecs) Lsum[i] = s_l[4 * v / D];
-            }
+            host_merge_staged<C, E>(p, g, npeer, kv, stg, M, Lsum, O, &fail);
             p0 = npeer;
           }
           // Few peers (or peers beyond the staged ones): the loads of PB
