@@ -180,7 +180,8 @@ la_status plan_fixed(la_schedule* s) {
   return LA_OK;
 }
 
-// Device segment records: the planner's words plus L and the slab's first row.
+// Device segment records: the planner's words plus L and the slab's first row
+// (and, for a piece of a split unit, its finisher and host CTAs).
 void build_dev_segs(la_schedule* s) {
   const size_t n = s->segs.size() / la::kSegWords;
   s->dev_segs.assign(n * la::kDevSegWords, 0);
@@ -200,6 +201,10 @@ void build_dev_segs(la_schedule* s) {
     dv[9] = b;
     dv[10] = kvh;
     dv[11] = 0;
+    if (sg[3] == la::kHost || sg[3] == la::kNonHost) {  // a piece of a split unit: its host and finisher CTAs
+      dv[4] = s->unit_fin[sg[0]];
+      dv[11] = s->unit_host[sg[0]];
+    }
   }
 }
 
@@ -367,14 +372,19 @@ double piece_bytes(const la_schedule* s, int u, int t0, int t1) {
 // within the launch, and launch overheads (two launches for fixed splits > 1).
 // Constants fitted to GB300 measurements: aggregate read rate with n busy SMs
 // 7.5 TB/s * (1 - exp(-n / 60)) (3.1 TB/s at 32, 6.6 at 128, 6.9 at 152);
-// 3 us from CTA start to its first tile; 2.5 us for a host CTA's merge.
+// 3 us from CTA start to its first tile; 2.5 us for a host CTA's merge on
+// the 16-row kernel.
 double predict_seconds(const la_schedule* s, int slots) {
   constexpr double kRateMax = 7.5e12, kRateN0 = 60.0;
   constexpr double kLaunch = 8e-6, kMergeLaunch = 4e-6, kStartup = 3e-6, kHostMerge = 2.5e-6;
-  // a host of the tcgen05 kernel pulls its peers' records (rows x (d + 2)
-  // floats each) through one SM: 38 GB/s measured (151 records of 64 rows
-  // at d = 128 in 130 us)
-  constexpr double kWideMergeRate = 38e9;
+  // the tcgen05 kernel's merge of a split unit, shared by the unit's CTAs:
+  // about 3 us plus 0.11 us per piece of the unit (GB300: 10 pieces of 64
+  // rows at d = 128 ~4 us after the last piece; 152 pieces ~20 us)
+  constexpr double kWideMerge = 3e-6, kWideMergePerPiece = 0.11e-6;
+  // the fixed split's merge launch for tcgen05 records: 0.13 us per piece of
+  // a unit (152 pieces of 64 rows at d = 128: 64 us in all, 21 of them the
+  // pieces' tile loops)
+  constexpr double kWideCombinePerPiece = 0.13e-6;
   std::vector<double> jobs((size_t)s->G, 0.0);
   bool split = false;
   int max_peers = 0;
@@ -392,10 +402,15 @@ double predict_seconds(const la_schedule* s, int slots) {
   // most (its softmax and MMA chain), whatever HBM could give it
   const double cap = s->R == la::kWideRows ? (double)s->T * s->d * 4.0 / 1.55e-6 : 0.0;
   double t = simulate_dispatch(jobs, slots, kRateMax, kRateN0, cap) + kLaunch + kStartup * rounds;
-  if (split) t += kHostMerge;
-  if (split && s->R == la::kWideRows)
-    t += (double)max_peers * s->unit_grp() * s->nq * (s->d + 2) * 4.0 / kWideMergeRate;
-  if (s->kind == 1 && s->splits > 1) t += kMergeLaunch;
+  if (split) t += s->R == la::kWideRows ? kWideMerge + kWideMergePerPiece * (max_peers + 1) : kHostMerge;
+  if (s->kind == 1 && s->splits > 1) {
+    t += kMergeLaunch;
+    if (s->R == la::kWideRows) {  // the tcgen05 records' merge reads each row's pieces one after another
+      int most = 1;
+      for (int u = 0; u < s->U; ++u) most = std::max(most, s->unit_fin[u] - s->unit_host[u] + 1);
+      t += kWideCombinePerPiece * most;
+    }
+  }
   return t;
 }
 

@@ -16,7 +16,8 @@ enum SegKind : int32_t { kWhole = 0, kNonHost = 1, kHost = 2, kPartial = 3 };
 // the request's context length and the slab's first K/V row (64-bit), so the
 // producer can issue its first copy after two dependent loads.
 constexpr int kSegWords = 5;
-// unit, t0, t1, kind, peer, L, row0 low, row0 high, cu[b], b, first kv head of the unit, 0
+// unit, t0, t1, kind, peer, L, row0 low, row0 high, cu[b], b, first kv head of the unit, host;
+// for host and non-host pieces peer is the unit's finisher CTA and host its host CTA (else -1, 0)
 constexpr int kDevSegWords = 12;
 
 // Where the K/V rows of a (request, kv head, token) live.
@@ -26,17 +27,20 @@ enum KvLayout : int {
   kKvPaged = 2        // [pages, page_size, hkv, d] with a block table per request (3-D TMA)
 };
 
-// Workspace: a 256-byte header, G ready flags (padded to 256 bytes), then G
-// partial records (one per CTA: a CTA has at most one non-host or
-// fixed-split piece, its first segment), each of rows * (d + 4) floats for
-// the 16-row kernel (per query row [m, l, 0, 0, O[d]]; rows = the
-// instance's rows per kv head x kv heads per unit) or the tcgen05 kernel's
-// column-major layout.
+// Workspace: a 256-byte header, ready flags (padded to 256 bytes), then
+// partial records, one flag per record slot. The 16-row kernel has one slot
+// per CTA (a CTA writes at most one record: its first segment's, when that
+// is a non-host or fixed-split piece; hosts merge from registers), each of
+// rows * (d + 4) floats (per query row [m, l, 0, 0, O[d]]; rows = the
+// instance's rows per kv head x kv heads per unit). The tcgen05 kernel has
+// two per CTA in its column-major layout: every piece of a split unit
+// writes a record, in slot CTA when it is not the CTA's last segment, else
+// in slot G + CTA (see wide_merge_unit).
 constexpr size_t kHeaderBytes = 256;
 enum HeaderWord { kEpoch = 0, kDone = 1, kStatus = 2, kInfoCta = 3, kInfoPeer = 4 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-inline size_t flags_bytes(int G) { return align_up(sizeof(uint32_t) * (size_t)G, 256); }
+inline size_t flags_bytes(int n) { return align_up(sizeof(uint32_t) * (size_t)n, 256); }
 // Records of the 16-row kernel hold rows of [m, l, 0, 0, O[d]] (O 16-byte
 // aligned, so that partials move as 16-byte vectors); the tcgen05 kernel's
 // hold columns [m], [l], [O dim c] over the unit's rows (128-row instance),
@@ -48,9 +52,12 @@ constexpr int kWideInstanceRows = 128;  // rows of the tcgen05 kernel's instance
 inline size_t record_floats(int d, int rows) {
   return (size_t)(rows >= kWideInstanceRows ? record_stride_wide(d, rows) : record_stride(d, rows));
 }
-inline size_t records_bytes(int G, int d, int rows) { return sizeof(float) * record_floats(d, rows) * (size_t)G; }
+inline int record_slots(int G, int rows) { return rows >= kWideInstanceRows ? 2 * G : G; }
+inline size_t records_bytes(int G, int d, int rows) {
+  return sizeof(float) * record_floats(d, rows) * (size_t)record_slots(G, rows);
+}
 inline size_t workspace_bytes(int G, int d, int rows) {
-  return kHeaderBytes + flags_bytes(G) + records_bytes(G, d, rows);
+  return kHeaderBytes + flags_bytes(record_slots(G, rows)) + records_bytes(G, d, rows);
 }
 // Byte offsets of the flags and the records inside a workspace.
 struct WsLayout {
@@ -59,7 +66,7 @@ struct WsLayout {
 inline WsLayout workspace_layout(int G, int d, int rows) {
   WsLayout w;
   w.flags = kHeaderBytes;
-  w.recs = w.flags + flags_bytes(G);
+  w.recs = w.flags + flags_bytes(record_slots(G, rows));
   w.end = w.recs + records_bytes(G, d, rows);
   return w;
 }
@@ -84,7 +91,7 @@ struct KParams {
   int kv_heads = 0;         // kv heads of the K/V tensors (token-major / paged tensor maps)
   float qscale;             // scale * log2(e): scores are kept in base-2 units
   long long spin_ns;        // limit of every wait inside the kernel
-  int skip_signal;          // test hook: this CTA never sets its flag (-1: none)
+  int skip_signal;          // test hook: this CTA never sets its first segment's flag (-1: none)
   unsigned long long* trace;  // optional per-CTA timeline (kTraceWords each), or null
   int out_dtype = 0;          // 0 fp32, 1 fp16, 2 bf16
   // Query rows of a unit: rows = grp * nq (<= the instance's row count);

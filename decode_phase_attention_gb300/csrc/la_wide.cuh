@@ -49,8 +49,10 @@
 // compute 2^x; their two partial O rows are summed at the end.
 //
 // Partial records hold (m, l, O) per row column-major over the unit's rows
-// (coalesced for a warp's 32 rows); a host pulls its peers' records into
-// the idle ring with bulk copies and merges them from shared memory. The
+// (coalesced for a warp's 32 rows). Every piece of a split unit writes one,
+// host included, and the CTAs that end on a piece of the unit each merge an
+// equal share of its outputs (wide_merge_unit), so a unit split over many
+// SMs is reduced by all of them rather than through its host's SM. The
 // schedule, segments, ready flags with epochs, bounded waits and the abort
 // protocol are the 16-row kernel's.
 #pragma once
@@ -207,7 +209,7 @@ struct WCfg {
   // partial row maxima (two tiles), partial sums of l, O quarters handed between lane replicas ([64][65])
   static constexpr int RED_BYTES = 3 * 4 * M * 4 + 64 * 65 * 4;
   static constexpr int NSB = 3 * T + D + D / 2 <= 512 ? 3 : 2;  // S / P buffers in TMEM
-  static constexpr int NBARS = 2 * 6 + 3 * NSB + 4;  // full, empty (<= 6 stages), s_full, p_full, pv_done, q_ready, drain, stg[2]
+  static constexpr int NBARS = 2 * 6 + 3 * NSB + 2;  // full, empty (<= 6 stages), s_full, p_full, pv_done, q_ready, drain
   static constexpr int STAGES = cmin(6, (232448 - RED_BYTES - 1024 - 256) / STAGE_BYTES);
   static constexpr size_t KV_BYTES = (size_t)STAGES * STAGE_BYTES;
   // + exchange area, barriers, TMEM slot, flags; alignment slack
@@ -219,7 +221,7 @@ struct WCfg {
   static_assert(D == 64 || D == 80 || D == 96 || D == 128 || D == 256, "head dims of the wide kernel");
   static_assert(M == kWideInstanceRows, "record layout of the wide kernel");
   static_assert(STAGES >= 2 && SMEM <= 232448, "shared memory per CTA");
-  static_assert(NBARS * 8 + 8 + 12 <= 256, "barrier area");  // barriers, TMEM slot, 3 flag words
+  static_assert(NBARS * 8 + 8 + 4 <= 256, "barrier area");  // barriers, TMEM slot, abort flag
   static_assert(Q_COL + D / 2 <= TMEM_COLS, "tensor memory columns");
 };
 
@@ -337,6 +339,210 @@ __device__ __forceinline__ void wide_mma(const KParams& p, int g, const E* kv,
 }
 
 
+// ------------------------------------------------------ merge of a split unit
+// A unit split over CTAs h0 .. h1 (h0 the host: the unit's first tiles, at
+// the end of its range; h1 the finisher: the unit's last tiles, at the
+// start of its range) is complete only when its last piece is, at the end
+// of the launch. Rather than reduce every piece through the host's SM,
+// each CTA whose last segment is a piece of the unit (the host, the CTAs in
+// between, and the finisher when that piece is its only segment) takes an
+// equal share of the unit's rows x d outputs: it waits (bounded) for every
+// other piece's ready flag, then applies f to its share: per row the
+// maximum m over the pieces, the weights 2^(m_i - m) and l = sum w_i l_i,
+// then per output sum w_i O_i / l. A piece's record and flag sit in its
+// CTA's first slot when the piece is not that CTA's last segment, else in
+// its second slot (G + CTA), so a CTA can hold both kinds at once. Every
+// softmax thread passes the same named barriers; after a timeout or an
+// abort the share is written as NaN.
+template <int D>
+__device__ __noinline__ void wide_merge_unit(const KParams& p, int g, int h0, int h1, int b, int kvh,
+                                                float* sm, volatile int* abort_flag, uint32_t ready,
+                                                unsigned long long* tr) {
+  using C = WCfg<D>;
+  constexpr int NT = C::NSW * 32;  // softmax threads
+  const int tid = threadIdx.x;
+  const int rows = p.rows;
+  const bool fin_last = p.cta_seg[h1 + 1] - p.cta_seg[h1] == 1;  // the finisher's piece is its only segment
+  const int np = h1 - h0 + 1;                                     // pieces
+  const int npart = fin_last ? np : np - 1;                       // CTAs that merge a share
+  auto slot = [&](int c) { return (c < h1 || fin_last) ? p.G + c : c; };
+  // thread i waits for the flags of pieces i, i + 512, ...
+  const uint64_t twait = global_ns();
+  for (int i = tid; i < np; i += NT) {
+    const int c = h0 + i;
+    if (c == g) continue;
+    const uint32_t* f = p.flags + slot(c);
+    const uint64_t tstart = global_ns();
+    for (uint32_t it = 0; !*abort_flag; ++it) {
+      if (ld_acquire_gpu(f) == ready) break;
+      if ((it & 15u) == 15u) {
+        if ((long long)(global_ns() - tstart) > p.spin_ns) {
+          record_error(p.hdr, kStatusTimeout, g, c);
+          *abort_flag = 1;
+          break;
+        }
+        __nanosleep(100);
+      }
+    }
+  }
+  softmax_sync();  // every flag seen (or the abort raised) before any record is read
+  if (tr != nullptr) tr[kTrWaitNs] += global_ns() - twait;
+  const bool fail = *abort_flag != 0;
+  // This CTA's share of the outputs e = c * rows + r (dim c, row r): a
+  // range in the records' column-major order of O, its ends on 16-byte
+  // boundaries of a record, so that each piece's part of it moves as
+  // 16-byte async copies (in flight while m and l are read).
+  const int E = rows * D, base = 2 * rows, k = g - h0;
+  auto bound = [&](int kk) {
+    if (kk <= 0) return 0;
+    if (kk >= npart) return E;
+    const int x = ((base + (int)((long long)E * kk / npart)) & ~3) - base;
+    return x < 0 ? 0 : x;
+  };
+  const int e0 = bound(k), e1 = bound(k + 1), ne = e1 - e0;
+  const int a0 = (base + e0) & ~3, span = ((base + e1 + 3) & ~3) - a0;  // floats of each piece's part
+  // shared memory (the idle ring)
+  float* so = sm;                  // [np][span]: the share's O of every piece
+  float* wm = so + np * span;      // [np][rows]: m of every piece, then its weight
+  float* mr = wm + np * rows;      // [rows]: the row maxima
+  float* lr = mr + rows;           // [rows]: the row sums l
+  float* part = lr + rows;         // [2][NT]: partial results
+  {
+    const int q4 = span / 4;
+    const uint32_t s0 = smem_u32(so);
+    for (int i = tid; i < np * q4; i += NT) {
+      const int pi = i / q4, c4 = i - pi * q4;
+      const float* src = p.recs + (size_t)slot(h0 + pi) * C::RS + a0 + 4 * c4;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s0 + 16u * (uint32_t)i), "l"(src) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  // nt threads per row r, thread j taking pieces j, j + nt, ...: the
+  // running maximum and sum of l (each m kept for the weights)
+  const int nt = NT / rows, r = tid % rows, jr = tid / rows;
+  if (jr < nt) {
+    float m = -INFINITY, l = 0.f;
+#pragma unroll 4
+    for (int pi = jr; pi < np; pi += nt) {
+      const float* rp = p.recs + (size_t)slot(h0 + pi) * C::RS;
+      const float mi = __ldcg(rp + r), li = __ldcg(rp + rows + r);
+      wm[pi * rows + r] = mi;
+      if (mi > m) {
+        l = (m == -INFINITY) ? 0.f : l * ex2(m - mi);
+        m = mi;
+      }
+      l = fmaf((mi == -INFINITY) ? 0.f : ex2(mi - m), li, l);  // NaN m (a poisoned piece) propagates
+    }
+    part[jr * rows + r] = m;
+    part[NT + jr * rows + r] = l;
+  }
+  softmax_sync();
+  if (tid < rows) {
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < nt; ++j) m = fmaxf(m, part[j * rows + tid]);
+    for (int j = 0; j < nt; ++j) {
+      const float mj = part[j * rows + tid];
+      l = fmaf((mj == -INFINITY) ? 0.f : ex2(mj - m), part[NT + j * rows + tid], l);
+    }
+    mr[tid] = m;
+    lr[tid] = l;
+  }
+  softmax_sync();
+  for (int i = tid; i < np * rows; i += NT) {  // the weights 2^(m_i - m)
+    const float mi = wm[i];
+    wm[i] = (mi == -INFINITY) ? 0.f : ex2(mi - mr[i % rows]);
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  softmax_sync();  // the weights and every thread's copies are in shared memory
+  // the weighted sums; with fewer outputs than threads, ng threads split the
+  // pieces of each output
+  const int ng = (ne >= NT || ne <= 0) ? 1 : min(np, NT / ne);
+  const float nan = __int_as_float(0x7fc00000);
+  const float* sx = so + (base - a0);  // piece pi's element e at sx[pi * span + e]
+  if (ng == 1) {
+    for (int e = e0 + tid; e < e1; e += NT) {
+      const int rr = e % rows;
+      float o = 0.f;
+#pragma unroll 4
+      for (int pi = 0; pi < np; ++pi) o = fmaf(wm[pi * rows + rr], sx[pi * span + e], o);
+      store_out(p.out, row_index(p, b, kvh, rr) * D + e / rows, fail ? nan : o / lr[rr], p.out_dtype);
+    }
+  } else {
+    const int ei = tid % ne, jg = tid / ne;
+    if (jg < ng) {
+      const int e = e0 + ei, rr = e % rows;
+      float o = 0.f;
+#pragma unroll 4
+      for (int pi = jg; pi < np; pi += ng) o = fmaf(wm[pi * rows + rr], sx[pi * span + e], o);
+      part[jg * ne + ei] = o;
+    }
+    softmax_sync();
+    if (tid < ne) {
+      const int e = e0 + tid, rr = e % rows;
+      float o = part[tid];
+      for (int k2 = 1; k2 < ng; ++k2) o += part[k2 * ne + tid];
+      store_out(p.out, row_index(p, b, kvh, rr) * D + e / rows, fail ? nan : o / lr[rr], p.out_dtype);
+    }
+  }
+}
+
+// A host whose unit has just one other piece, written by its finisher as
+// that CTA's first segment (so long before this, the host's last): the host
+// merges alone and from registers, without a record of its own. Thread 0
+// waits (bounded) for the finisher's flag; each thread then applies f to
+// its row's partial (m, l and its dims db .. db + N - 1 of O) and the
+// finisher's record, and stores O / l.
+template <int D, int N, int OR>
+__device__ __forceinline__ void wide_sole_host(const KParams& p, int g, int fin, int b, int kvh, int row, bool live,
+                                               int db, const float (&o)[OR], float m_use, float l, bool poisoned,
+                                               volatile int* abort_flag, uint32_t ready, unsigned long long* tr) {
+  using C = WCfg<D>;
+  static_assert(N <= OR && N % 2 == 0, "dims of a thread");
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0; !*abort_flag; ++it) {
+      if (ld_acquire_gpu(p.flags + fin) == ready) break;
+      if ((it & 15u) == 15u) {
+        if ((long long)(global_ns() - t0) > p.spin_ns) {
+          record_error(p.hdr, kStatusTimeout, g, fin);
+          *abort_flag = 1;
+          break;
+        }
+        __nanosleep(100);
+      }
+    }
+    if (tr != nullptr) tr[kTrWaitNs] += global_ns() - t0;
+  }
+  softmax_sync();  // the flag seen (or the abort raised) before the record is read
+  const bool fail = poisoned || *abort_flag != 0;
+  if (!live) return;
+  const int rows = p.rows;
+  const float* rec = p.recs + (size_t)fin * C::RS;  // the finisher's first slot
+  const float m2 = __ldcg(rec + row), l2 = __ldcg(rec + rows + row);
+  const float m = fmaxf(m_use, m2);
+  const float a = (m_use == -INFINITY) ? 0.f : ex2(m_use - m);
+  const float w = (m2 == -INFINITY) ? 0.f : ex2(m2 - m);  // NaN m (a poisoned piece) propagates
+  const float inv = 1.f / fmaf(w, l2, a * l);
+  const float nan = __int_as_float(0x7fc00000);
+  const size_t base = row_index(p, b, kvh, row) * D + db;
+  constexpr int CH = N % 16 == 0 ? 16 : N;  // dims per batch of loads
+#pragma unroll
+  for (int c0 = 0; c0 < N; c0 += CH) {
+    float v[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) v[c] = __ldcg(rec + (size_t)(2 + db + c0 + c) * rows + row);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) v[c] = fail ? nan : fmaf(w, v[c], a * o[c0 + c]) * inv;
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+      for (int c = 0; c < CH; c += 4) store_out4(p.out, base + c0 + c, v[c], v[c + 1], v[c + 2], v[c + 3], p.out_dtype);
+    } else {
+#pragma unroll
+      for (int c = 0; c < CH; c += 2) store_out2(p.out, base + c0 + c, v[c], v[c + 1], p.out_dtype);
+    }
+  }
+}
+
 // --------------------------------------------------------- softmax warps
 // Warp w (0..15) works on TMEM lane quadrant w % 4 (the lanes its SM
 // sub-partition reaches): thread (w, lane) owns lane r = 32 (w % 4) + lane
@@ -348,16 +554,16 @@ __device__ __forceinline__ void wide_mma(const KParams& p, int g, const E* kv,
 // maximum if the tile's maximum exceeds it by more than 8 (base-2 units),
 // write P = 2^(s - m) as high and low 16-bit parts over S, update the
 // partial sum of l; at the end: add the partial sums (and, with replicas,
-// the two O rows), read the O quarter and write the record, or merge the
-// peers' records with f and store O / l. Every softmax thread passes the
+// the two O rows), read the O quarter and store O / l (a whole unit) or
+// write the record (a piece of a split unit) and, on the CTA's last
+// segment, merge this CTA's share of the unit. Every softmax thread passes the
 // same named barriers, also after an abort (the waits are skipped then,
 // not the barriers).
 template <int D, typename E, int NREP>
 __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, float* red,
                                              uint64_t* full, uint64_t* s_full, uint64_t* p_full,
-                                             uint64_t* pv_done, uint64_t* q_ready, uint64_t* stg,
+                                             uint64_t* pv_done, uint64_t* q_ready,
                                              uint32_t tmem, volatile int* abort_flag, uint32_t epoch) {
-  volatile int* flags_smem_copies = abort_flag + 1;  // [2]: staging copies issued into each half of the ring
   using C = WCfg<D>;
   constexpr int T = C::T;
   constexpr int OQ = D / 4;  // head dims of O per thread
@@ -389,7 +595,7 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
   for (int si = s_begin; si < s_end; ++si) {
     const int4 w0 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords);
     const int4 w1 = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords + 4);
-    const int unit = w0.x, t0 = w0.y, t1 = w0.z, kind = w0.w, peer = w1.x;
+    const int unit = w0.x, t0 = w0.y, t1 = w0.z;
     const int b = unit / p.hkv, kvh = unit % p.hkv;
     const bool ok = unit_offsets_ok(p, b);
     if (!ok && tid == 0) record_error(p.hdr, kStatusInvalid, g, unit);
@@ -612,35 +818,32 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
     tc_fence_before();
     lsum[(half * 4 + cq) * RM + row] = lq;
     softmax_sync();  // every warp's waits are over; the quarter sums are in shared memory
+    // the segment's kind, finisher and host CTAs and unit head, read again
+    // here rather than held in registers through the tile loop
+    const int4 e0w = *reinterpret_cast<const int4*>(p.segs + (size_t)si * kDevSegWords);
+    const int kind = e0w.w, fin = p.segs[(size_t)si * kDevSegWords + 4], host = p.segs[(size_t)si * kDevSegWords + 11];
+    const int ub = e0w.x / p.hkv, ukvh = e0w.x % p.hkv;
     if constexpr (NREP == 1) {
       // 128-row instance (96 registers a thread): one replica owns each
-      // quarter; one staging buffer; direct stores
-      float l = (lsum[row] + lsum[RM + row]) + (lsum[2 * RM + row] + lsum[3 * RM + row]);
-      if constexpr (NREP == 2) {
-        l += (lsum[4 * RM + row] + lsum[5 * RM + row]) + (lsum[6 * RM + row] + lsum[7 * RM + row]);
-        // the replica in lanes 64..127 hands its O quarter to the one in 0..63
-  #pragma unroll
-        for (int c0 = 0; c0 < OQ; c0 += OC) {
-          if (half == 1) {
-  #pragma unroll
-            for (int k = 0; k < OC; ++k) stage_o[row * 65 + cq * 16 + k] = o[c0 + k];
-          }
-          softmax_sync();
-          if (half == 0) {
-  #pragma unroll
-            for (int k = 0; k < OC; ++k) o[c0 + k] += stage_o[row * 65 + cq * 16 + k];
-          }
-          softmax_sync();
-        }
-      }
+      // quarter
+      const float l = (lsum[row] + lsum[RM + row]) + (lsum[2 * RM + row] + lsum[3 * RM + row]);
       const bool poisoned = (*abort_flag != 0) || !ok || !have_o;
       // Records are column-major over the unit's rows (wide_rec): element
       // (col, r) at [col * rows + r], col 0 = m, 1 = l, 2 + c = O dim c, so
       // that a warp's 32 rows read and write whole 128-byte lines.
       const int rows = p.rows;
-      if (kind == kNonHost || kind == kPartial) {
+      // a host whose unit's only other piece is its finisher's first segment
+      const bool sole = kind == kHost && fin == g + 1 && p.cta_seg[fin + 1] - p.cta_seg[fin] > 1;
+      if (sole) {
+        wide_sole_host<D, OQ>(p, g, fin, ub, ukvh, row, owner, OQ * cq, o, m_use, l, poisoned, abort_flag, ready, tr);
+      } else if (kind != kWhole) {
+        // a piece of a split unit: its record (the second slot when this is
+        // the CTA's last segment) and its ready flag; on the CTA's last
+        // segment, this CTA's share of the unit's merge follows the loop
+        const bool last = si == s_end - 1;
+        const int slot = (kind != kPartial && last) ? p.G + g : g;
         if (owner) {
-          float* rec = p.recs + (size_t)g * C::RS;
+          float* rec = p.recs + (size_t)slot * C::RS;
           if (cq == 0) {
             rec[row] = poisoned ? __int_as_float(0x7fc00000) : m_use;
             rec[rows + row] = l;
@@ -648,106 +851,27 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
   #pragma unroll
           for (int c = 0; c < OQ; ++c) rec[(size_t)(2 + OQ * cq + c) * rows + row] = o[c];
         }
-        __threadfence();
+        // the CTA barrier orders every thread's record stores before thread
+        // 0's release store, which is cumulative at gpu scope: a CTA that
+        // acquires the flag sees the whole record (no fence per thread)
         softmax_sync();
-        if (kind == kNonHost && tid == 0 && g != p.skip_signal) st_release_gpu(&p.flags[g], ready);
-      } else {
-        bool fail = poisoned;
-        float Ls = l;
-        if (kind == kHost) {
-          // every later CTA of the unit: thread i spins (bounded) on the ready
-          // flags of peers i, i + 512, ...
-          const int npeer = peer - g;
-          const uint64_t twait = global_ns();
-          for (int i = tid; i < npeer; i += C::NSW * 32) {
-            const int g2 = g + 1 + i;
-            const uint64_t tstart = global_ns();
-            for (uint32_t it = 0; !*abort_flag; ++it) {
-              if (ld_acquire_gpu(&p.flags[g2]) == ready) break;
-              if ((it & 15u) == 15u) {
-                if ((long long)(global_ns() - tstart) > p.spin_ns) {
-                  record_error(p.hdr, kStatusTimeout, g, g2);
-                  *abort_flag = 1;
-                  break;
-                }
-                __nanosleep(100);
-              }
-            }
-          }
-          softmax_sync();  // every flag seen (or the abort raised) before any record is read
-          if (tr != nullptr) tr[kTrWaitNs] += global_ns() - twait;
-          // The host segment is the CTA's last: every tile has been consumed
-          // and the producer issues no more copies, so the ring is idle. The
-          // peers' records come into it by bulk copies, as many at a time as
-          // fit, and are merged with f one after another (the running
-          // maximum M, then the rescaled sums of l and of this thread's O
-          // quarter).
-          const uint32_t rec_bytes = ((uint32_t)rows * (D + 2) * 4u + 15u) & ~15u;
-          const int cap = (int)(C::KV_BYTES / rec_bytes);
-          float M = m_use;
-          uint32_t sph = 0;
-          for (int p0 = 0; p0 < npeer; p0 += cap) {
-            const int nb = npeer - p0 < cap ? npeer - p0 : cap;
-            if (tid == 0 && !*abort_flag) {
-              asm volatile("fence.proxy.async.global;" ::: "memory");  // records written by other CTAs
-              mbar_arrive_expect_tx(stg, (uint32_t)nb * rec_bytes);
-              for (int k = 0; k < nb; ++k)
-                bulk_g2s(reinterpret_cast<unsigned char*>(kv) + (size_t)k * rec_bytes,
-                         p.recs + (size_t)(g + 1 + p0 + k) * C::RS, rec_bytes, stg, l2_evict_first_policy());
-              flags_smem_copies[0] = 1;  // copies in flight: wait for them even after an abort
-            }
-            softmax_sync();
-            const bool issued = flags_smem_copies[0] != 0;
-            volatile int no_abort = 0;
-            const bool got = issued && mbar_wait_bounded(stg, sph, &no_abort, p.spin_ns);
-            sph ^= issued ? 1u : 0u;
-            if (issued && !got) fail = true;
-            if (got && owner && !*abort_flag) {
-              // f over the batch at once: its maximum, one rescale of the
-              // running partial, then the weighted sums
-              const float* r0 = reinterpret_cast<const float*>(kv);
-              const int rstride = (int)(rec_bytes / 4);  // floats between staged records
-              float mb = M;
-              for (int k = 0; k < nb; ++k) mb = fmaxf(mb, r0[k * rstride + row]);
-              if (mb != -INFINITY) {
-                const float a = (M == -INFINITY) ? 0.f : ex2(M - mb);
-                Ls *= a;
+        if (kind != kPartial && tid == 0 && !(g == p.skip_signal && si == p.cta_seg[g]))
+          st_release_gpu(&p.flags[slot], ready);
+      } else if (owner) {  // a whole unit: normalise and store O = Obar / l
+        const size_t base = row_index(p, ub, ukvh, row) * D + OQ * cq;
+        const float inv = 1.f / l;
+        const float nan = __int_as_float(0x7fc00000);
   #pragma unroll
-                for (int c = 0; c < OQ; ++c) o[c] *= a;
-                for (int k = 0; k < nb; ++k) {
-                  const float* rk = r0 + k * rstride;
-                  const float mk = rk[row];
-                  const float wt = (mk == -INFINITY) ? 0.f : ex2(mk - mb);  // NaN m (poisoned) propagates
-                  Ls = fmaf(wt, rk[rows + row], Ls);
-  #pragma unroll
-                  for (int c = 0; c < OQ; ++c) o[c] = fmaf(wt, rk[(2 + OQ * cq + c) * rows + row], o[c]);
-                }
-                M = mb;
-              }
-            }
-            softmax_sync();  // the staging area is rewritten by the next batch
-            if (tid == 0) flags_smem_copies[0] = 0;
-          }
-          if (*abort_flag) fail = true;
-        }
-        // normalise and store: O = Obar / l
-        if (owner) {
-          const size_t base = row_index(p, b, kvh, row) * D + OQ * cq;
-          const float inv = 1.f / Ls;
-  #pragma unroll
-          for (int c = 0; c < OQ; c += 4)
-            store_out4(p.out, base + c, fail ? __int_as_float(0x7fc00000) : o[c] * inv,
-                       fail ? __int_as_float(0x7fc00000) : o[c + 1] * inv,
-                       fail ? __int_as_float(0x7fc00000) : o[c + 2] * inv,
-                       fail ? __int_as_float(0x7fc00000) : o[c + 3] * inv, p.out_dtype);
-        }
+        for (int c = 0; c < OQ; c += 4)
+          store_out4(p.out, base + c, poisoned ? nan : o[c] * inv, poisoned ? nan : o[c + 1] * inv,
+                     poisoned ? nan : o[c + 2] * inv, poisoned ? nan : o[c + 3] * inv, p.out_dtype);
       }
     } else {
       float l = (lsum[row] + lsum[RM + row]) + (lsum[2 * RM + row] + lsum[3 * RM + row]);
       // The dims of the O quarter this thread owns from here on: with lane
       // replicas the two halves split the quarter (each adds the other
       // replica's partial O row for its half), so that all 16 warps share the
-      // record write, the host merge and the stores; without, the whole
+      // record write and the stores; without, the whole
       // quarter.
       constexpr int NO = OQ / NREP;
       const int db = OQ * cq + (NREP == 2 ? NO * half : 0);  // first dim this thread owns
@@ -801,9 +925,15 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
       // (col, r) at [col * rows + r], col 0 = m, 1 = l, 2 + c = O dim c, so
       // that a warp's 32 rows read and write whole 128-byte lines.
       const int rows = p.rows;
-      if (kind == kNonHost || kind == kPartial) {
+      const bool sole = kind == kHost && fin == g + 1 && p.cta_seg[fin + 1] - p.cta_seg[fin] > 1;  // as above
+      if (sole) {
+        wide_sole_host<D, NO>(p, g, fin, ub, ukvh, row, live, db, o, m_use, l, poisoned, abort_flag, ready, tr);
+      } else if (kind != kWhole) {
+        // a piece of a split unit: its record and its ready flag (as above)
+        const bool last = si == s_end - 1;
+        const int slot = (kind != kPartial && last) ? p.G + g : g;
         if (live) {
-          float* rec = p.recs + (size_t)g * C::RS;
+          float* rec = p.recs + (size_t)slot * C::RS;
           if (owner && cq == 0) {
             rec[row] = poisoned ? __int_as_float(0x7fc00000) : m_use;
             rec[rows + row] = l;
@@ -811,154 +941,41 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
   #pragma unroll
           for (int c = 0; c < NO; ++c) rec[(size_t)(2 + db + c) * rows + row] = o[c];
         }
-        __threadfence();
+        // the CTA barrier orders every thread's record stores before thread
+        // 0's release store, which is cumulative at gpu scope: a CTA that
+        // acquires the flag sees the whole record (no fence per thread)
         softmax_sync();
-        if (kind == kNonHost && tid == 0 && g != p.skip_signal) st_release_gpu(&p.flags[g], ready);
-      } else {
-        bool fail = poisoned;
-        float Ls = l;
-        if (kind == kHost) {
-          // every later CTA of the unit: thread i spins (bounded) on the ready
-          // flags of peers i, i + 512, ...
-          const int npeer = peer - g;
-          const uint64_t twait = global_ns();
-          for (int i = tid; i < npeer; i += C::NSW * 32) {
-            const int g2 = g + 1 + i;
-            const uint64_t tstart = global_ns();
-            for (uint32_t it = 0; !*abort_flag; ++it) {
-              if (ld_acquire_gpu(&p.flags[g2]) == ready) break;
-              if ((it & 15u) == 15u) {
-                if ((long long)(global_ns() - tstart) > p.spin_ns) {
-                  record_error(p.hdr, kStatusTimeout, g, g2);
-                  *abort_flag = 1;
-                  break;
-                }
-                __nanosleep(100);
-              }
-            }
-          }
-          softmax_sync();  // every flag seen (or the abort raised) before any record is read
-          if (tr != nullptr) tr[kTrWaitNs] += global_ns() - twait;
-          // The host segment is the CTA's last: every tile has been consumed
-          // and the producer issues no more copies, so the ring is idle. The
-          // peers' records come into its two halves by bulk copies, a batch
-          // per half, so the next batch's copies overlap this batch's merge;
-          // each batch is merged with f at once (its maximum, one rescale of
-          // the running partial, then the weighted sums of l and of this
-          // thread's dims).
-          // Records small enough for two per half of the ring are double
-          // buffered; larger ones fill the whole ring per batch. The 128-row
-          // instance (NREP = 1, 96 registers a thread) keeps one buffer and
-          // direct stores: the extra state spilled into its tile loop.
-          const uint32_t rec_bytes = ((uint32_t)rows * (D + 2) * 4u + 15u) & ~15u;
-          constexpr size_t kHalf = C::KV_BYTES / 2;
-          const bool dbl = NREP == 2 && kHalf / rec_bytes >= 2;
-          const int cap = (int)((dbl ? kHalf : C::KV_BYTES) / rec_bytes);  // >= 1: a record is at most 66.5 KB
-          const int nbat = (npeer + cap - 1) / cap;
-          float M = m_use;
-          auto issue = [&](int bi) {  // thread 0: batch bi into its buffer
-            if (tid != 0 || *abort_flag) return;
-            const int p0 = bi * cap, nb = npeer - p0 < cap ? npeer - p0 : cap;
-            const int slot = dbl ? (bi & 1) : 0;
-            asm volatile("fence.proxy.async.global;" ::: "memory");  // records written by other CTAs
-            mbar_arrive_expect_tx(&stg[slot], (uint32_t)nb * rec_bytes);
-            for (int k = 0; k < nb; ++k)
-              bulk_g2s(reinterpret_cast<unsigned char*>(kv) + slot * kHalf + (size_t)k * rec_bytes,
-                       p.recs + (size_t)(g + 1 + p0 + k) * C::RS, rec_bytes, &stg[slot], l2_evict_first_policy());
-            flags_smem_copies[slot] = 1;  // copies in flight: wait for them even after an abort
-          };
-          if (nbat > 0) issue(0);
-          for (int bi = 0; bi < nbat; ++bi) {
-            const int p0 = bi * cap, nb = npeer - p0 < cap ? npeer - p0 : cap;
-            const int slot = dbl ? (bi & 1) : 0;
-            const uint32_t parity = dbl ? ((uint32_t)(bi >> 1) & 1u) : ((uint32_t)bi & 1u);
-            if (dbl ? bi + 1 < nbat : bi > 0) issue(dbl ? bi + 1 : bi);  // one buffer: the last batch is merged
-            softmax_sync();
-            const bool issued = flags_smem_copies[slot] != 0;
-            volatile int no_abort = 0;
-            const bool got = issued && mbar_wait_bounded(&stg[slot], parity, &no_abort, p.spin_ns);
-            if (issued && !got) fail = true;
-            if (got && live && !*abort_flag) {
-              const float* r0 = reinterpret_cast<const float*>(reinterpret_cast<const unsigned char*>(kv) +
-                                                               slot * kHalf);
-              const int rstride = (int)(rec_bytes / 4);  // floats between staged records
-              float mb = M;
-              for (int k = 0; k < nb; ++k) mb = fmaxf(mb, r0[k * rstride + row]);
-              if (mb != -INFINITY) {
-                const float a = (M == -INFINITY) ? 0.f : ex2(M - mb);
-                Ls *= a;
+        if (kind != kPartial && tid == 0 && !(g == p.skip_signal && si == p.cta_seg[g]))
+          st_release_gpu(&p.flags[slot], ready);
+      } else if (live) {  // a whole unit: normalise and store this thread's dims
+        const size_t base = row_index(p, ub, ukvh, row) * D + db;
+        const float inv = 1.f / l;
+        const float nan = __int_as_float(0x7fc00000);
+        if constexpr (NO % 4 == 0) {
   #pragma unroll
-                for (int c = 0; c < NO; ++c) o[c] *= a;
-                for (int k = 0; k < nb; ++k) {
-                  const float* rk = r0 + k * rstride;
-                  const float mk = rk[row];
-                  const float wt = (mk == -INFINITY) ? 0.f : ex2(mk - mb);  // NaN m (poisoned) propagates
-                  Ls = fmaf(wt, rk[rows + row], Ls);
+          for (int c = 0; c < NO; c += 4)
+            store_out4(p.out, base + c, poisoned ? nan : o[c] * inv, poisoned ? nan : o[c + 1] * inv,
+                       poisoned ? nan : o[c + 2] * inv, poisoned ? nan : o[c + 3] * inv, p.out_dtype);
+        } else {  // d = 80: 10 dims per half
   #pragma unroll
-                  for (int c = 0; c < NO; ++c) o[c] = fmaf(wt, rk[(2 + db + c) * rows + row], o[c]);
-                }
-                M = mb;
-              }
-            }
-            softmax_sync();  // the batch's buffer is free again
-            if (tid == 0) flags_smem_copies[slot] = 0;
-          }
-          if (*abort_flag) fail = true;
-          // normalise and store; with lane replicas through the ring as
-          // [row][D] (rows 16-byte aligned), then whole rows: a warp writes
-          // 512 contiguous bytes, not 32 separate 16-byte pieces
-          if constexpr (NREP == 2) {
-            constexpr int OS = D + 4;  // floats between rows in the ring
-            float* ob = reinterpret_cast<float*>(kv);
-            if (live) {
-              const float inv = 1.f / Ls;
-              const float nan = __int_as_float(0x7fc00000);
-              if constexpr (NO % 4 == 0) {
-  #pragma unroll
-                for (int c = 0; c < NO; c += 4)
-                  *reinterpret_cast<float4*>(ob + row * OS + db + c) =
-                      fail ? make_float4(nan, nan, nan, nan)
-                           : make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
-              } else {  // d = 80: 10 dims per half
-  #pragma unroll
-                for (int c = 0; c < NO; c += 2)
-                  *reinterpret_cast<float2*>(ob + row * OS + db + c) =
-                      fail ? make_float2(nan, nan) : make_float2(o[c] * inv, o[c + 1] * inv);
-              }
-            }
-            softmax_sync();
-            for (int i = tid; i < rows * (D / 4); i += C::NSW * 32) {
-              const int r = i / (D / 4), c4 = 4 * (i % (D / 4));
-              const float4 v = *reinterpret_cast<const float4*>(ob + r * OS + c4);
-              store_out4(p.out, row_index(p, b, kvh, r) * D + c4, v.x, v.y, v.z, v.w, p.out_dtype);
-            }
-          } else if (live) {
-            const size_t base = row_index(p, b, kvh, row) * D + db;
-            const float inv = 1.f / Ls;
-            const float nan = __int_as_float(0x7fc00000);
-  #pragma unroll
-            for (int c = 0; c < NO; c += 4)
-              store_out4(p.out, base + c, fail ? nan : o[c] * inv, fail ? nan : o[c + 1] * inv,
-                         fail ? nan : o[c + 2] * inv, fail ? nan : o[c + 3] * inv, p.out_dtype);
-          }
-        } else if (live) {  // a whole unit: normalise and store this thread's dims
-          const size_t base = row_index(p, b, kvh, row) * D + db;
-          const float inv = 1.f / Ls;
-          const float nan = __int_as_float(0x7fc00000);
-          if constexpr (NO % 4 == 0) {
-  #pragma unroll
-            for (int c = 0; c < NO; c += 4)
-              store_out4(p.out, base + c, fail ? nan : o[c] * inv, fail ? nan : o[c + 1] * inv,
-                         fail ? nan : o[c + 2] * inv, fail ? nan : o[c + 3] * inv, p.out_dtype);
-          } else {  // d = 80: 10 dims per half
-  #pragma unroll
-            for (int c = 0; c < NO; c += 2)
-              store_out2(p.out, base + c, fail ? nan : o[c] * inv, fail ? nan : o[c + 1] * inv, p.out_dtype);
-          }
+          for (int c = 0; c < NO; c += 2)
+            store_out2(p.out, base + c, poisoned ? nan : o[c] * inv, poisoned ? nan : o[c + 1] * inv, p.out_dtype);
         }
       }
     }
     softmax_sync();  // the quarter sums are rewritten by the next segment
+  }
+  // The CTA's last segment, when a piece of a split unit that it does not
+  // merge alone: this CTA's share of the unit's merge. Called here, after
+  // the segment loop, so that no state of the loop is live across the call.
+  if (s_end > s_begin) {
+    const int sl = s_end - 1;
+    const int* w = p.segs + (size_t)sl * kDevSegWords;
+    const int kind = w[3], fin = w[4], host = w[11];
+    const bool sole = kind == kHost && fin == g + 1 && p.cta_seg[fin + 1] - p.cta_seg[fin] > 1;
+    if ((kind == kHost || kind == kNonHost) && !sole)
+      wide_merge_unit<D>(p, g, host, fin, w[0] / p.hkv, w[0] % p.hkv, reinterpret_cast<float*>(kv), abort_flag, ready,
+                         tr);
   }
 }
 
@@ -982,9 +999,8 @@ __global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
   uint64_t* pv_done = p_full + C::NSB;
   uint64_t* q_ready = pv_done + C::NSB;
   uint64_t* drain = q_ready + 1;
-  uint64_t* stg = drain + 1;  // two barriers: staged peer records, one per half of the ring
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(stg + 2);
-  // [0] abort, [1] and [2] staging copies issued into each half of the ring
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
+  // [0] the CTA's abort flag
   volatile int* flags_smem = reinterpret_cast<volatile int*>(tslot + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -1009,11 +1025,7 @@ __global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
     }
     mbar_init(q_ready, C::NSW * 32);
     mbar_init(drain, 1);
-    mbar_init(&stg[0], 1);
-    mbar_init(&stg[1], 1);
     flags_smem[0] = 0;
-    flags_smem[1] = 0;
-    flags_smem[2] = 0;
     fence_mbar_init();
   }
   if (warp == C::NSW + 1) {
@@ -1027,7 +1039,7 @@ __global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
   const uint32_t epoch = *reinterpret_cast<volatile uint32_t*>(&p.hdr[kEpoch]);
 
   if (warp < C::NSW) {
-    wide_softmax<D, E, NREP>(p, g, kv, red, full, s_full, p_full, pv_done, q_ready, stg, tmem, flags_smem, epoch);
+    wide_softmax<D, E, NREP>(p, g, kv, red, full, s_full, p_full, pv_done, q_ready, tmem, flags_smem, epoch);
   } else if (warp == C::NSW) {
     produce<C, E>(p, &tmk, &tmv, g, kv, full, empty, flags_smem);
   } else if ((tid & 31) == 0) {
@@ -1107,6 +1119,18 @@ cudaError_t launch_wide_t(const KParams& p, cudaStream_t st) {
     e = encode_kv_maps(p.k, p.v, p.kv_rows, D, C::T, C::W, (int)Elem<E>::kTmaType, &mk, &mv);
   if (e != cudaSuccess) return e;
   if (p.rows > C::MAX_ROWS) return cudaErrorInvalidValue;  // the planner splits wider units into query blocks
+  // The merge of a split unit of np pieces over npart >= np - 1 CTAs holds,
+  // in the ring, each piece's part of a share (at most rows x d / npart +
+  // 12 floats) and m of every row, plus 2 rows + 2 x 512 floats; the total is
+  // convex in np, so it is largest at np = 2 or np = G.
+  {
+    const size_t outs = (size_t)p.rows * D;
+    auto need = [&](size_t np, size_t npart) {
+      return (np * ((outs + npart - 1) / npart + 12 + p.rows) + 2 * (size_t)p.rows + 2 * C::NSW * 32) * sizeof(float);
+    };
+    if (need(2, 1) > C::KV_BYTES || (p.G > 2 && need((size_t)p.G, (size_t)p.G - 1) > C::KV_BYTES))
+      return cudaErrorInvalidValue;
+  }
   if constexpr (C::MAX_ROWS > 64) {
     if (p.rows > 64) {
       lean_wide_kernel<D, E, 1><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);

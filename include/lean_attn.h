@@ -199,15 +199,18 @@ la_status la_plan_auto(int batch, int hq, int hkv, int d, const int32_t* cu_seql
 int la_schedule_grid(const la_schedule* s);
 
 /*
- * Bytes of device workspace la_decode needs for this schedule: a header, G
- * ready flags and G partial records ("7.4 limitations": a small amount of
- * global memory for sharing partial results). A record holds rows rows of
+ * Bytes of device workspace la_decode needs for this schedule: a 256-byte
+ * header, ready flags (padded to 256 bytes) and partial records, one flag
+ * per record ("7.4 limitations": a small amount of global memory for
+ * sharing partial results). The 16-row kernel has G records of rows rows of
  * [m, l, 0, 0, O[d]] floats (rows = query rows per unit head -- a kv head
  * or one query block of one -- rounded up to 1, 2, 4, 8 or 16, times the kv
- * heads per unit), or, on the tcgen05 kernel (128 rows), the same triples
- * column-major over the rows, rounded up to a multiple of 4 floats. Zero it once (la_workspace_init) before its first use; after
- * that it needs no clearing between calls. One workspace must not be used
- * by two launches that can run at the same time.
+ * heads per unit); the tcgen05 kernel (128 rows) 2 G records of the same
+ * triples column-major over the rows, rounded up to a multiple of 4 floats
+ * (every piece of a split unit writes one, and a CTA can hold two). Zero it
+ * once (la_workspace_init) before its first use; after that it needs no
+ * clearing between calls. One workspace must not be used by two launches
+ * that can run at the same time.
  */
 size_t la_workspace_size(const la_schedule* s);
 
@@ -412,8 +415,9 @@ la_status la_schedule_export(const la_schedule* s, int32_t* buf, size_t n);
 
 /*
  * Test hooks for failure detection (no GPU fault is ever needed):
- *   skip_signal_cta  CTA whose ready flag is never set (-1: none), so its
- *                    host's bounded wait runs out and reports LA_ERR_TIMEOUT
+ *   skip_signal_cta  CTA that never sets the ready flag of its first segment
+ *                    (-1: none), so the bounded waits of the CTAs merging that
+ *                    segment's unit run out and report LA_ERR_TIMEOUT
  *   spin_timeout_ns  limit of every wait inside the kernel (default 2 s)
  */
 la_status la_schedule_set_debug(la_schedule* s, int skip_signal_cta, long long spin_timeout_ns);

@@ -426,10 +426,12 @@ def test_query_blocks_are_units_of_their_own(d, grp, nq, qb, R):
     s = la.la_plan_spec(3, hkv * grp, hkv, d, nq, cu_of(lengths), G)
     assert s.query_blocks == qb and s.heads_per_unit == 1
     assert la.la_schedule_export(s) == P.export(P.plan_lean(3, hkv * grp, hkv * qb, d, cu_of(lengths), G, T))
-    # a record: R rows of [m, l, 0, 0, O[d]] on the 16-row kernel; on the
-    # tcgen05 kernel (R = 128) columns over the rows, padded to 16 bytes
+    # a record: R rows of [m, l, 0, 0, O[d]] on the 16-row kernel, one per
+    # CTA; on the tcgen05 kernel (R = 128) columns over the rows, padded to
+    # 16 bytes, two per CTA (with a ready flag each)
     rec = R * (d + 4) if R < 128 else -(-R * (d + 2) // 4) * 4
-    assert la.la_workspace_size(s) == 256 + 256 + G * rec * 4
+    slots = G if R < 128 else 2 * G
+    assert la.la_workspace_size(s) == 256 + 256 + slots * rec * 4
     if nq == 1:
         assert la.la_schedule_export(la.la_plan(3, hkv * grp, hkv, d, cu_of(lengths), G)) \
             == la.la_schedule_export(s)
@@ -461,7 +463,7 @@ def test_wide_units_hold_the_whole_group():
     s = la.la_plan(2, 64, 1, 128, [0, 900, 1000], 7)
     assert s.query_blocks == 1
     assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 64, 1, 128, [0, 900, 1000], 7, 128))
-    assert la.la_workspace_size(s) == 256 + 256 + 7 * 128 * 130 * 4
+    assert la.la_workspace_size(s) == 256 + 256 + 2 * 7 * 128 * 130 * 4  # two record slots per CTA
     assert la.la_schedule_export(la.la_plan(2, 64, 1, 64, [0, 900, 1000], 7))[4] == 128
     for bad in (64, 256):  # the wide instance is built for 128-token tiles only
         with pytest.raises(la.LeanAttentionError) as e:
@@ -473,10 +475,10 @@ def test_wide_units_hold_the_whole_group():
 
 
 def test_partition_choice_for_wide_units():
-    # one unit over every SM: the host would pull 151 records of 64 rows
-    # through one SM, so the fixed split wins; 16 units: stream-K
+    # one unit over every SM: its 152 CTAs share the merge, so stream-K
+    # still wins over the fixed split; 16 units: stream-K
     s, kind, pred = la.la_plan_auto(1, 64, 1, 128, [0, 262144], 152)
-    assert kind == "fixed_split" and pred[0] > pred[2]
+    assert kind == "lean" and pred[0] < pred[2] < pred[1]
     s, kind, pred = la.la_plan_auto(16, 64, 1, 128, cu_of([32768] * 16), 152)
     assert kind == "lean" and pred[0] < pred[2] < pred[1]
 
