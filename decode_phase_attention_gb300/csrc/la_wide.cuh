@@ -422,16 +422,28 @@ __device__ __noinline__ void wide_merge_unit(const KParams& p, int g, int h0, in
   const int nt = NT / rows, r = tid % rows, jr = tid / rows;
   if (jr < nt) {
     float m = -INFINITY, l = 0.f;
-#pragma unroll 4
-    for (int pi = jr; pi < np; pi += nt) {
-      const float* rp = p.recs + (size_t)slot(h0 + pi) * C::RS;
-      const float mi = __ldcg(rp + r), li = __ldcg(rp + rows + r);
-      wm[pi * rows + r] = mi;
-      if (mi > m) {
-        l = (m == -INFINITY) ? 0.f : l * ex2(m - mi);
-        m = mi;
+    constexpr int KB = 8;  // pieces whose loads are in flight together
+    for (int p0 = jr; p0 < np; p0 += KB * nt) {
+      float mv[KB], lv[KB];
+#pragma unroll
+      for (int u = 0; u < KB; ++u) {
+        const int pi = p0 + u * nt;
+        const float* rp = p.recs + (size_t)slot(h0 + (pi < np ? pi : 0)) * C::RS;
+        mv[u] = pi < np ? __ldcg(rp + r) : -INFINITY;
+        lv[u] = pi < np ? __ldcg(rp + rows + r) : 0.f;
       }
-      l = fmaf((mi == -INFINITY) ? 0.f : ex2(mi - m), li, l);  // NaN m (a poisoned piece) propagates
+#pragma unroll
+      for (int u = 0; u < KB; ++u) {
+        const int pi = p0 + u * nt;
+        if (pi >= np) break;
+        wm[pi * rows + r] = mv[u];
+        const float mi = mv[u];
+        if (mi > m) {
+          l = (m == -INFINITY) ? 0.f : l * ex2(m - mi);
+          m = mi;
+        }
+        l = fmaf((mi == -INFINITY) ? 0.f : ex2(mi - m), lv[u], l);  // NaN m (a poisoned piece) propagates
+      }
     }
     part[jr * rows + r] = m;
     part[NT + jr * rows + r] = l;
