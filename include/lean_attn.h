@@ -15,7 +15,9 @@
  * tokens at d = 128); all tiles are laid out on one line and split evenly
  * over G CTAs, which may cross head and request boundaries; each CTA
  * produces partial results (m, l, unscaled O) that the unit's host CTA
- * merges with the rescaling reduction f and normalises, all in one launch.
+ * merges with the rescaling reduction f and normalises, all in one launch
+ * (for units of more than 16 query rows every CTA that ends on a piece of
+ * the unit merges an equal share of its outputs instead).
  *
  * Data layout (device memory, row-major, no padding):
  *   q    [batch, hq, d]                         fp16 or bf16
@@ -186,8 +188,10 @@ la_status la_plan_fixed(int batch, int hq, int hkv, int d, const int32_t* cu_seq
  * the fastest. Time model: CTAs dispatched in order onto the SMs as they
  * free up; n running CTAs read 7.5 TB/s * (1 - exp(-n / 60)) together
  * (fitted to GB300 measurements); 3 us of start-up per CTA an SM runs in
- * turn, 2.5 us for host CTAs' merges, 8 us per launch and 4 us for the
- * second (merge) launch of a fixed split.
+ * turn, 2.5 us for host CTAs' merges (for units of more than 16 rows,
+ * 3 us + 0.11 us per piece of a unit), 8 us per launch and 4 us for the
+ * second (merge) launch of a fixed split (+ 0.13 us per piece of a unit
+ * above 16 rows).
  * predicted_us: NULL, or 3 doubles receiving the predictions (stream-K,
  * one per unit, fixed split). The returned schedule is used like any
  * other; la_schedule_export tells which kind it is (word 6, word 7).
