@@ -1266,12 +1266,42 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
   }
 }
 
+// Programmatic dependent launch. Every kernel of the library first lets
+// the next grid on its stream be launched (griddepcontrol.launch_dependents)
+// and then waits until the grid before it has completed and its memory is
+// visible (griddepcontrol.wait), before it touches global memory: launched
+// with the attribute below, a kernel's CTAs can be placed on SMs as soon as
+// the previous kernel's CTAs leave them, which hides the launch latency
+// between back-to-back calls without reading anything early. Without a
+// prerequisite grid, the wait returns at once.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // -------------------------------------------------------------------- kernel
 template <int D, int T, int GRP, typename E, int HP>
 __global__ void __launch_bounds__(Cfg<D, T, GRP, HP>::NTHREADS, 1)
     lean_decode_kernel(const KParams p, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv) {
   using C = Cfg<D, T, GRP, HP>;
+  grid_dependency_sync();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // swizzled TMA tiles need 1024-byte aligned destinations, plain ones 128
   unsigned char* smem =
@@ -1331,6 +1361,7 @@ __global__ void __launch_bounds__(Cfg<D, T, GRP, HP>::NTHREADS, 1)
 // (unit, query head of the group), one thread per dimension).
 template <int D, int GRP>
 __global__ void __launch_bounds__(D) lean_combine_kernel(const CParams p) {
+  grid_dependency_sync();
   constexpr int REC = D + kRecO;
   const int row = blockIdx.x;  // unit * GRP + j
   const int unit = row / GRP, j = row % GRP;
@@ -1393,8 +1424,7 @@ cudaError_t launch_decode_t(const KParams& p, cudaStream_t st) {
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
   }
-  lean_decode_kernel<D, T, GRP, E, HP><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
-  return cudaGetLastError();
+  return launch_dependent(lean_decode_kernel<D, T, GRP, E, HP>, (unsigned)p.G, C::NTHREADS, C::SMEM, st, p, mk, mv);
 }
 
 template <int D, int T, int GRP, int HP = 1>
@@ -1410,8 +1440,7 @@ cudaError_t capacity_t(int* per_sm) {
 template <int D, int GRP>
 cudaError_t launch_combine_t(const CParams& p, cudaStream_t st) {
   if (p.U <= 0) return cudaSuccess;
-  lean_combine_kernel<D, GRP><<<p.U * GRP, D, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(lean_combine_kernel<D, GRP>, (unsigned)(p.U * GRP), D, 0, st, p);
 }
 
 }  // namespace la

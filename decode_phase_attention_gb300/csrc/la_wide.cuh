@@ -999,6 +999,7 @@ __global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
     lean_wide_kernel(const KParams p, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv) {
   using C = WCfg<D>;
+  grid_dependency_sync();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1078,6 +1079,7 @@ __global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
 // unit's rows): one block per (unit, query row), one thread per dimension.
 template <int D>
 __global__ void __launch_bounds__(D) lean_wide_combine_kernel(const CParams p) {
+  grid_dependency_sync();
   using C = WCfg<D>;
   const int unit = blockIdx.x / C::M, j = blockIdx.x % C::M;
   const int c = threadIdx.x;
@@ -1145,19 +1147,16 @@ cudaError_t launch_wide_t(const KParams& p, cudaStream_t st) {
   }
   if constexpr (C::MAX_ROWS > 64) {
     if (p.rows > 64) {
-      lean_wide_kernel<D, E, 1><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
-      return cudaGetLastError();
+      return launch_dependent(lean_wide_kernel<D, E, 1>, (unsigned)p.G, C::NTHREADS, C::SMEM, st, p, mk, mv);
     }
   }
-  lean_wide_kernel<D, E, 2><<<p.G, C::NTHREADS, C::SMEM, st>>>(p, mk, mv);
-  return cudaGetLastError();
+  return launch_dependent(lean_wide_kernel<D, E, 2>, (unsigned)p.G, C::NTHREADS, C::SMEM, st, p, mk, mv);
 }
 
 template <int D>
 cudaError_t launch_wide_combine_t(const CParams& p, cudaStream_t st) {
   if (p.U <= 0) return cudaSuccess;
-  lean_wide_combine_kernel<D><<<p.U * WCfg<D>::M, D, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(lean_wide_combine_kernel<D>, (unsigned)(p.U * WCfg<D>::M), D, 0, st, p);
 }
 
 template <int D>

@@ -239,8 +239,13 @@ la_status la_workspace_init(void* workspace, size_t bytes, la_stream_t stream);
  *
  * One kernel launch for stream-K schedules (plus one merge launch for
  * fixed splits > 1). Does not synchronise, except on a schedule's first
- * use (upload of its tables). Returns LA_ERR_INVALID / LA_ERR_WORKSPACE
- * for bad arguments, LA_ERR_CUDA if a launch fails.
+ * use (upload of its tables). Kernels are launched as programmatic
+ * dependents (cudaLaunchAttributeProgrammaticStreamSerialization): their
+ * CTAs may be placed while the kernel before them on the stream finishes,
+ * but each first waits (griddepcontrol.wait) until that kernel has
+ * completed and its writes are visible, so stream order is kept for every
+ * byte read or written. Returns LA_ERR_INVALID / LA_ERR_WORKSPACE for bad
+ * arguments, LA_ERR_CUDA if a launch fails.
  */
 la_status la_decode(const void* q, const void* k, const void* v, la_dtype dt,
                     const int32_t* cu_seqlens_k_dev, const la_schedule* s, void* workspace,
