@@ -892,7 +892,7 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
         if constexpr (D == 256) {
           // each half already holds its own 32 dims in o[0, 32); the other
           // half's partial for them comes from its tensor memory in pieces
-          // of 16 (round rnd: half 1 - rnd gives, half rnd receives)
+          // of 16 (pass rnd: half 1 - rnd gives, half rnd receives)
   #pragma unroll
           for (int rnd = 0; rnd < 2; ++rnd)
   #pragma unroll
@@ -913,8 +913,9 @@ __device__ __forceinline__ void wide_softmax(const KParams& p, int g, E* kv, flo
               softmax_sync();
             }
         } else {
-          // round 0: the replica in lanes 64..127 hands dims [0, NO) of its
-          // quarter to the one in 0..63; round 1: the other way, dims [NO, OQ)
+          // first pass: the replica in lanes 64..127 hands dims [0, NO) of
+          // its quarter to the one in 0..63; second pass: the other way,
+          // dims [NO, OQ)
   #pragma unroll
           for (int rnd = 0; rnd < 2; ++rnd) {
             if (half != rnd) {
