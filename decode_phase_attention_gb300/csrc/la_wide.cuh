@@ -404,9 +404,9 @@ __device__ __noinline__ void wide_merge_unit(const KParams& p, int g, int h0, in
   // shared memory (the idle ring)
   float* so = sm;                  // [np][span]: the share's O of every piece
   float* wm = so + np * span;      // [np][rows]: m of every piece, then its weight
-  float* mr = wm + np * rows;      // [rows]: the row maxima
-  float* lr = mr + rows;           // [rows]: the row sums l
+  float* lr = wm + np * rows;      // [rows]: the row sums l
   float* part = lr + rows;         // [2][NT]: partial results
+  long long* ob = reinterpret_cast<long long*>(part + 2 * NT + ((np * (span + rows) + rows) & 1));  // [rows]: output offsets
   {
     const int q4 = span / 4;
     const uint32_t s0 = smem_u32(so);
@@ -449,23 +449,27 @@ __device__ __noinline__ void wide_merge_unit(const KParams& p, int g, int h0, in
     part[NT + jr * rows + r] = l;
   }
   softmax_sync();
-  if (tid < rows) {
+  // each of the row's nt threads: the row's maximum m and l from the nt
+  // partials, then the weights 2^(m_i - m) of its own pieces; the row's
+  // first thread keeps l and the row's offset in the output
+  if (jr < nt) {
     float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < nt; ++j) m = fmaxf(m, part[j * rows + tid]);
+    for (int j = 0; j < nt; ++j) m = fmaxf(m, part[j * rows + r]);
     for (int j = 0; j < nt; ++j) {
-      const float mj = part[j * rows + tid];
-      l = fmaf((mj == -INFINITY) ? 0.f : ex2(mj - m), part[NT + j * rows + tid], l);
+      const float mj = part[j * rows + r];
+      l = fmaf((mj == -INFINITY) ? 0.f : ex2(mj - m), part[NT + j * rows + r], l);
     }
-    mr[tid] = m;
-    lr[tid] = l;
-  }
-  softmax_sync();
-  for (int i = tid; i < np * rows; i += NT) {  // the weights 2^(m_i - m)
-    const float mi = wm[i];
-    wm[i] = (mi == -INFINITY) ? 0.f : ex2(mi - mr[i % rows]);
+    for (int pi = jr; pi < np; pi += nt) {
+      const float mi = wm[pi * rows + r];
+      wm[pi * rows + r] = (mi == -INFINITY) ? 0.f : ex2(mi - m);
+    }
+    if (jr == 0) {
+      lr[r] = l;
+      ob[r] = (long long)row_index(p, b, kvh, r) * D;
+    }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
-  softmax_sync();  // the weights and every thread's copies are in shared memory
+  softmax_sync();  // the weights, l, the offsets and every thread's copies are in shared memory
   // the weighted sums; with fewer outputs than threads, ng threads split the
   // pieces of each output
   const int ng = (ne >= NT || ne <= 0) ? 1 : min(np, NT / ne);
@@ -477,7 +481,7 @@ __device__ __noinline__ void wide_merge_unit(const KParams& p, int g, int h0, in
       float o = 0.f;
 #pragma unroll 4
       for (int pi = 0; pi < np; ++pi) o = fmaf(wm[pi * rows + rr], sx[pi * span + e], o);
-      store_out(p.out, row_index(p, b, kvh, rr) * D + e / rows, fail ? nan : o / lr[rr], p.out_dtype);
+      store_out(p.out, (size_t)(ob[rr] + e / rows), fail ? nan : o / lr[rr], p.out_dtype);
     }
   } else {
     const int ei = tid % ne, jg = tid / ne;
@@ -493,7 +497,7 @@ __device__ __noinline__ void wide_merge_unit(const KParams& p, int g, int h0, in
       const int e = e0 + tid, rr = e % rows;
       float o = part[tid];
       for (int k2 = 1; k2 < ng; ++k2) o += part[k2 * ne + tid];
-      store_out(p.out, row_index(p, b, kvh, rr) * D + e / rows, fail ? nan : o / lr[rr], p.out_dtype);
+      store_out(p.out, (size_t)(ob[rr] + e / rows), fail ? nan : o / lr[rr], p.out_dtype);
     }
   }
 }
@@ -1136,12 +1140,12 @@ cudaError_t launch_wide_t(const KParams& p, cudaStream_t st) {
   if (p.rows > C::MAX_ROWS) return cudaErrorInvalidValue;  // the planner splits wider units into query blocks
   // The merge of a split unit of np pieces over npart >= np - 1 CTAs holds,
   // in the ring, each piece's part of a share (at most rows x d / npart +
-  // 12 floats) and m of every row, plus 2 rows + 2 x 512 floats; the total is
+  // 12 floats) and m of every row, plus 4 rows + 2 x 512 + 2 floats; the total is
   // convex in np, so it is largest at np = 2 or np = G.
   {
     const size_t outs = (size_t)p.rows * D;
     auto need = [&](size_t np, size_t npart) {
-      return (np * ((outs + npart - 1) / npart + 12 + p.rows) + 2 * (size_t)p.rows + 2 * C::NSW * 32) * sizeof(float);
+      return (np * ((outs + npart - 1) / npart + 12 + p.rows) + 4 * (size_t)p.rows + 2 + 2 * C::NSW * 32) * sizeof(float);
     };
     if (need(2, 1) > C::KV_BYTES || (p.G > 2 && need((size_t)p.G, (size_t)p.G - 1) > C::KV_BYTES))
       return cudaErrorInvalidValue;
