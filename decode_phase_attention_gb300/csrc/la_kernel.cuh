@@ -1273,7 +1273,9 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
 // with the attribute below, a kernel's CTAs can be placed on SMs as soon as
 // the previous kernel's CTAs leave them, which hides the launch latency
 // between back-to-back calls without reading anything early. Without a
-// prerequisite grid, the wait returns at once.
+// prerequisite grid, the wait returns at once. (The tcgen05 kernel's merge
+// launch for fixed splits, thousands of small blocks, is the exception: its
+// blocks, launched early, made those calls about 10 % slower.)
 __device__ __forceinline__ void grid_dependency_sync() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");

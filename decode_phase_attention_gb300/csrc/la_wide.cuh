@@ -1084,7 +1084,6 @@ __global__ void __launch_bounds__(WCfg<D>::NTHREADS, 1)
 // unit's rows): one block per (unit, query row), one thread per dimension.
 template <int D>
 __global__ void __launch_bounds__(D) lean_wide_combine_kernel(const CParams p) {
-  grid_dependency_sync();
   using C = WCfg<D>;
   const int unit = blockIdx.x / C::M, j = blockIdx.x % C::M;
   const int c = threadIdx.x;
@@ -1161,7 +1160,8 @@ cudaError_t launch_wide_t(const KParams& p, cudaStream_t st) {
 template <int D>
 cudaError_t launch_wide_combine_t(const CParams& p, cudaStream_t st) {
   if (p.U <= 0) return cudaSuccess;
-  return launch_dependent(lean_wide_combine_kernel<D>, (unsigned)(p.U * WCfg<D>::M), D, 0, st, p);
+  lean_wide_combine_kernel<D><<<p.U * WCfg<D>::M, D, 0, st>>>(p);  // an ordinary launch: see launch_dependent
+  return cudaGetLastError();
 }
 
 template <int D>
