@@ -55,6 +55,9 @@ CASES = [
     (1, 100, 1, 96, "f16", [9000], 0),          # 100 rows, d 96
     (4, 32, 1, 128, "bf16", [5000, 3000, 7000, 100], 7),  # units over two or three CTAs
     (3, 48, 2, 64, "bf16", [777, 4096, 2000], 19),
+    (1, 128, 1, 128, "bf16", [200000], 0),      # 128 rows over every CTA: the most shared memory a merge takes
+    (1, 64, 1, 256, "f16", [60000], 0),         # d = 256 over every CTA
+    (1, 128, 1, 80, "bf16", [100000], 0),       # d = 80, 128 rows over every CTA
 ]
 
 
