@@ -57,6 +57,10 @@
 // LA_ERR_TIMEOUT in the workspace header, raises a CTA-wide abort flag that
 // makes every other wait return at once, the producer waits (bounded) for
 // its copies still in flight, and the affected outputs are written as NaN.
+//
+// The kernel is launched as a programmatic dependent of the kernel before
+// it on the stream and waits for that grid before touching memory
+// (grid_dependency_sync), so back-to-back calls overlap only their launch.
 #pragma once
 
 #include <cuda.h>
