@@ -489,3 +489,53 @@ def test_unit_counts_beyond_32_bits_are_rejected():
     with pytest.raises(la.LeanAttentionError) as e:
         la.la_plan(1 << 20, 4096, 1, 64, np.arange((1 << 20) + 1, dtype=np.int32), 7)
     assert e.value.status == la.LA_ERR_UNSUPPORTED
+
+
+def _structure(exp):
+    """(G, U, segments, cta_seg, unit_host, unit_fin) from a schedule export."""
+    G, U, nseg = exp[1], exp[2], exp[5]
+    base = 8 + 2 * (G + 1) + (U + 1)
+    segs = [exp[base + 5 * i: base + 5 * i + 5] for i in range(nseg)]
+    cta_seg = exp[8 + G + 1 + U + 1: 8 + G + 1 + U + 1 + G + 1]
+    rest = base + 5 * nseg
+    return G, U, segs, cta_seg, exp[rest: rest + U], exp[rest + U: rest + 2 * U]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_split_units_of_wide_schedules_have_the_shape_the_shared_merge_needs(seed):
+    # The tcgen05 kernel merges a split unit on every CTA whose last segment
+    # is a piece of it, and a CTA keeps at most two records (its first
+    # segment's, its last segment's). Both rest on the stream-K structure:
+    # a host piece is its CTA's last segment, the CTAs between host and
+    # finisher hold only that unit, the finisher's piece is its first segment,
+    # and no split piece sits between a CTA's first and last segments.
+    rng = np.random.default_rng(seed)
+    batch = int(rng.integers(1, 6))
+    lengths = rng.integers(1, 40000, size=batch).tolist()
+    grp = int(rng.choice([32, 48, 64, 128]))
+    hkv = int(rng.integers(1, 3))
+    d = int(rng.choice([64, 80, 96, 128]))
+    G = int(rng.choice([5, 19, 64, 152]))
+    s = la.la_plan(batch, grp * hkv, hkv, d, cu_of(lengths), G)
+    G, U, segs, cta_seg, host, fin = _structure(la.la_schedule_export(s))
+    split = {P.HOST, P.NONHOST}
+    merges = {}
+    for g in range(G):
+        mine = segs[cta_seg[g]:cta_seg[g + 1]]
+        for i, sg in enumerate(mine):
+            if sg[3] in split:
+                assert i == 0 or i == len(mine) - 1  # only a first or last segment is a split piece
+            if sg[3] == P.HOST:
+                assert i == len(mine) - 1 and host[sg[0]] == g
+        if mine and mine[-1][3] in split:
+            merges.setdefault(mine[-1][0], []).append(g)  # this CTA merges a share of that unit
+    for u in range(U):
+        h0, h1 = host[u], fin[u]
+        if h0 == h1:
+            assert u not in merges  # a whole unit
+            continue
+        for c in range(h0 + 1, h1):  # the CTAs between hold only this unit
+            assert cta_seg[c + 1] - cta_seg[c] == 1 and segs[cta_seg[c]][0] == u
+        assert segs[cta_seg[h1]][0] == u and segs[cta_seg[h1]][3] == P.NONHOST  # the finisher's first segment
+        fin_only = cta_seg[h1 + 1] - cta_seg[h1] == 1
+        assert merges[u] == list(range(h0, h1 + (1 if fin_only else 0)))
