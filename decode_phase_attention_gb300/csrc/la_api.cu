@@ -843,6 +843,7 @@ la_status la_decode_kv(const void* q, const void* k, const void* v, la_dtype dt,
   p.rows = s->unit_grp() * s->nq;
   p.stages = s->stages > 0 ? s->stages
                            : (s->kind == 0 && s->R <= 16 ? la::stream_stages(s->d, s->T, s->hp, kv_layout) : 0);
+  p.shared_pieces = la::shared_merge_pieces(s->R * s->hp);
   cudaError_t ce = la::launch_decode(s->d, s->T, s->R, s->hp, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {

@@ -28,14 +28,18 @@ enum KvLayout : int {
 };
 
 // Workspace: a 256-byte header, ready flags (padded to 256 bytes), then
-// partial records, one flag per record slot. The 16-row kernel has one slot
-// per CTA (a CTA writes at most one record: its first segment's, when that
-// is a non-host or fixed-split piece; hosts merge from registers), each of
-// rows * (d + 4) floats (per query row [m, l, 0, 0, O[d]]; rows = the
-// instance's rows per kv head x kv heads per unit). The tcgen05 kernel has
-// two per CTA in its column-major layout: every piece of a split unit
-// writes a record, in slot CTA when it is not the CTA's last segment, else
-// in slot G + CTA (see wide_merge_unit).
+// partial records, one flag per record slot. Records of the 16-row kernel
+// hold rows * (d + 4) floats (per query row [m, l, 0, 0, O[d]]; rows = the
+// instance's rows per kv head x kv heads per unit). With fewer than
+// kSharedMergeRows rows it has one slot per CTA: a CTA writes at most one
+// record (its first segment's, when that is a non-host or fixed-split
+// piece), and hosts merge their peers from registers. From
+// kSharedMergeRows rows a split unit of many pieces (kSharedMergeBytes),
+// and on the tcgen05 kernel (its records column-major) every split unit,
+// is merged by every CTA that ends on one of its pieces, so each of
+// its pieces writes a record: in slot CTA when the piece is not the CTA's
+// last segment, else in slot G + CTA; such instances have two slots per
+// CTA.
 constexpr size_t kHeaderBytes = 256;
 enum HeaderWord { kEpoch = 0, kDone = 1, kStatus = 2, kInfoCta = 3, kInfoPeer = 4 };
 
@@ -49,25 +53,42 @@ constexpr int kRecO = 4;  // offset of O in a row of a 16-row kernel record
 __host__ __device__ constexpr int record_stride(int d, int rows) { return rows * (d + kRecO); }
 __host__ __device__ constexpr int record_stride_wide(int d, int rows) { return (rows * (d + 2) + 3) / 4 * 4; }
 constexpr int kWideInstanceRows = 128;  // rows of the tcgen05 kernel's instance (kWideRows)
+// 16-row kernel: from kSharedMergeRows record rows, a split unit of at
+// least kSharedMergePieces pieces whose host would read at least
+// kSharedMergeBytes of its peers' records is merged by every CTA that ends
+// on one of its pieces (KParams::shared_pieces), not by its host alone.
+// Below that the host's merge is as fast (same-box measurements: the shared
+// merge's chain of flag, copy and sum after the last piece costs what the
+// host spends on about 100 KB of records).
+constexpr int kSharedMergeRows = 4;
+constexpr int kSharedMergePieces = 4;
+constexpr size_t kSharedMergeBytes = 96 * 1024;
+inline int shared_merge_pieces(int rows) {
+  return rows >= kSharedMergeRows && rows < kWideInstanceRows ? kSharedMergePieces : 0;
+}
 inline size_t record_floats(int d, int rows) {
   return (size_t)(rows >= kWideInstanceRows ? record_stride_wide(d, rows) : record_stride(d, rows));
 }
-inline int record_slots(int G, int rows) { return rows >= kWideInstanceRows ? 2 * G : G; }
-inline size_t records_bytes(int G, int d, int rows) {
-  return sizeof(float) * record_floats(d, rows) * (size_t)record_slots(G, rows);
+// shared = false: the layout of a launch whose 16-row kernel merges every
+// split unit at its host (KParams::shared_pieces = 0), one slot per CTA.
+inline int record_slots(int G, int rows, bool shared = true) {
+  return rows >= kWideInstanceRows || (shared && rows >= kSharedMergeRows) ? 2 * G : G;
 }
-inline size_t workspace_bytes(int G, int d, int rows) {
-  return kHeaderBytes + flags_bytes(record_slots(G, rows)) + records_bytes(G, d, rows);
+inline size_t records_bytes(int G, int d, int rows, bool shared = true) {
+  return sizeof(float) * record_floats(d, rows) * (size_t)record_slots(G, rows, shared);
+}
+inline size_t workspace_bytes(int G, int d, int rows, bool shared = true) {
+  return kHeaderBytes + flags_bytes(record_slots(G, rows, shared)) + records_bytes(G, d, rows, shared);
 }
 // Byte offsets of the flags and the records inside a workspace.
 struct WsLayout {
   size_t flags, recs, end;
 };
-inline WsLayout workspace_layout(int G, int d, int rows) {
+inline WsLayout workspace_layout(int G, int d, int rows, bool shared = true) {
   WsLayout w;
   w.flags = kHeaderBytes;
-  w.recs = w.flags + flags_bytes(record_slots(G, rows));
-  w.end = w.recs + records_bytes(G, d, rows);
+  w.recs = w.flags + flags_bytes(record_slots(G, rows, shared));
+  w.end = w.recs + records_bytes(G, d, rows, shared);
   return w;
 }
 
@@ -106,6 +127,10 @@ struct KParams {
   int page_size = 0;                     // paged: tokens per page
   int box_rows = 0;                      // 3-D TMA: token rows per load (T, or the page size if smaller)
   int stages = 0;                        // ring stages to cycle through (0: all the instance holds)
+  // 16-row kernel: split units of at least this many pieces are merged by
+  // every CTA that ends on one of their pieces (0: each by its host alone);
+  // nonzero only with two record slots per CTA (record_slots)
+  int shared_pieces = 0;
 };
 
 // Per-CTA trace record (globaltimer ns): written when KParams::trace is set.

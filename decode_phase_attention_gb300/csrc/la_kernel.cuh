@@ -1071,6 +1071,193 @@ __device__ __noinline__ void host_merge_staged(const KParams& p, int g, int npee
   }
 }
 
+// Shared memory the shared merge of a unit of np pieces (np >= 4) needs at
+// most, for any CTA's share: per-thread partial sums, per piece its share of
+// O with the row headers it crosses and one weight per share row, and the
+// row sums. A unit whose merge would not fit in the idle ring and merge area
+// is merged at its host.
+template <class C>
+__host__ __device__ constexpr size_t shared_merge_bytes(int np) {
+  constexpr int NV = C::MROWS * C::DIM / 4;  // vectors of 4 outputs of a unit
+  const int sv = (NV + np - 2) / (np - 1);    // vectors of the largest share (at least np - 1 CTAs share)
+  const int nrs = cmin(C::MROWS, (4 * sv + C::DIM - 1) / C::DIM + 1);  // record rows a share touches
+  const int span = 4 * sv + 4 * (nrs - 1);    // floats of one piece's part, headers included
+  return sizeof(float) * ((size_t)4 * C::NCT + (size_t)np * (span + nrs) + nrs);
+}
+// Whether the split unit of CTAs host .. fin is merged shared: records of
+// at least kSharedMergeRows rows, at least KParams::shared_pieces pieces,
+// at least kSharedMergeBytes of peer records, and room for the merge.
+template <class C>
+__device__ __forceinline__ bool merged_shared(const KParams& p, int host, int fin) {
+  const int np = fin - host + 1;
+  return C::MROWS >= kSharedMergeRows && p.shared_pieces > 0 && np >= p.shared_pieces &&
+         (size_t)(np - 1) * C::RS * sizeof(float) >= kSharedMergeBytes &&
+         shared_merge_bytes<C>(np) <= C::KV_BYTES + C::MERGE_BYTES;
+}
+
+// The merge of a split unit (CTAs h0 .. h1, records in slots given by
+// slot()) shared by the CTAs whose last segment is one of its pieces: the
+// host, the CTAs between, and the finisher when the piece is its only
+// segment. Each takes an equal share of the unit's rows x d outputs (a range
+// of 4-output vectors in record order), waits for every piece's ready flag,
+// copies its share of each record into the idle ring (16-byte async copies,
+// in flight while the row maxima and sums are read), and sums the pieces
+// with the weights 2^(m_i - m) of f: the same result as folding f over the
+// pieces in any order. Out of line, called after the segment loop.
+template <class C>
+__device__ __noinline__ void merge_unit_shared(const KParams& p, int g, int h0, int h1, int b, int kvh0, float* sm,
+                                               volatile int* abort_flag, uint32_t ready) {
+  constexpr int D = C::DIM, NT = C::NCT, REC = C::REC, GRP = C::MROWS / C::HPU;
+  constexpr int NV = C::MROWS * D / 4;
+  const int tid = threadIdx.x;
+  const bool fin_last = p.cta_seg[h1 + 1] - p.cta_seg[h1] == 1;  // the finisher's piece is its only segment
+  const int np = h1 - h0 + 1;
+  const int npart = fin_last ? np : np - 1;
+  auto slot = [&](int c) { return (c < h1 || fin_last) ? p.G + c : c; };
+  // thread i waits for the flags of pieces i, i + NT, ... (not its own)
+  const uint64_t twait = global_ns();
+  for (int i = tid; i < np; i += NT) {
+    const int c = h0 + i;
+    if (c == g) continue;
+    const uint32_t* f = p.flags + slot(c);
+    const uint64_t tstart = global_ns();
+    for (uint32_t it = 0; !*abort_flag; ++it) {
+      if (ld_acquire_gpu(f) == ready) break;
+      if ((it & 15u) == 15u) {
+        if ((long long)(global_ns() - tstart) > p.spin_ns) {
+          record_error(p.hdr, kStatusTimeout, g, c);
+          *abort_flag = 1;
+          break;
+        }
+        __nanosleep(100);
+      }
+    }
+  }
+  consumer_sync(NT);  // every flag seen (or the abort raised) before any record is read
+  if (p.trace != nullptr && tid == 0) p.trace[(size_t)g * kTraceWords + kTrWaitNs] += global_ns() - twait;
+  const bool fail = *abort_flag != 0;
+  // this CTA's share: vectors [v0, v1), record rows rr0 .. rr0 + nrs - 1;
+  // vector v sits at float off(v) of a record
+  const int k = g - h0;
+  const int v0 = (int)((long long)NV * k / npart), v1 = (int)((long long)NV * (k + 1) / npart);
+  const int nev = v1 - v0;
+  auto off = [](int v) { return (4 * v / D) * REC + kRecO + 4 * v % D; };
+  const int rr0 = 4 * v0 / D;
+  const int nrs = nev > 0 ? 4 * (v1 - 1) / D - rr0 + 1 : 0;
+  const int a0 = off(v0), span = nev > 0 ? off(v1 - 1) + 4 - a0 : 0;
+  // shared memory (the idle ring and merge area)
+  float4* part4 = reinterpret_cast<float4*>(sm);  // [NT] partial sums of phase 2
+  float* so = sm + 4 * NT;                        // [np][span]: every piece's part
+  float* wm = so + (size_t)np * span;             // [np][nrs]: m of every piece, then its weight
+  float* lr = wm + (size_t)np * nrs;              // [nrs]: the row sums l
+  if (nev > 0) {
+    const int q4 = span / 4;
+    const uint32_t s0 = smem_u32(so);
+    for (int i = tid; i < np * q4; i += NT) {
+      const int pi = i / q4, c4 = i - pi * q4;
+      const float* src = p.recs + (size_t)slot(h0 + pi) * C::RS + a0 + 4 * c4;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s0 + 16u * (uint32_t)i), "l"(src) : "memory");
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  // one warp per share row, lane j taking pieces j, j + 32, ...: the
+  // running maximum and sum of l (each m kept for the weights), combined
+  // over the warp, then the weights 2^(m_i - m) of the lane's pieces; a
+  // poisoned piece (NaN m) makes the row's l NaN. Rows past the unit's live
+  // query rows are neither read nor stored.
+  {
+    const int lane = tid & 31;
+    for (int ri = tid >> 5; ri < nrs; ri += NT / 32) {
+      const int rr = rr0 + ri;
+      if ((rr % GRP) >= p.rows) continue;  // warp-uniform
+      float m = -INFINITY, l = 0.f;
+      bool bad = false;
+      constexpr int KB = 8;  // pieces whose loads are in flight together
+      for (int p0 = lane; p0 < np; p0 += 32 * KB) {
+        float mv[KB], lv[KB];
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          const int pi = p0 + 32 * u;
+          const float* rp = p.recs + (size_t)slot(h0 + (pi < np ? pi : 0)) * C::RS + rr * REC;
+          mv[u] = pi < np ? __ldcg(rp) : -INFINITY;
+          lv[u] = pi < np ? __ldcg(rp + 1) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+          const int pi = p0 + 32 * u;
+          if (pi >= np) break;
+          const float mi = mv[u];
+          wm[pi * nrs + ri] = mi;
+          bad |= mi != mi;
+          if (mi > m) {
+            l = (m == -INFINITY) ? 0.f : l * ex2(m - mi);
+            m = mi;
+          }
+          if (mi > -INFINITY) l = fmaf(ex2(mi - m), lv[u], l);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(kFull, m, o), l2 = __shfl_xor_sync(kFull, l, o);
+        const float mn = fmaxf(m, m2);
+        l = (m == -INFINITY ? 0.f : l * ex2(m - mn)) + (m2 == -INFINITY ? 0.f : l2 * ex2(m2 - mn));
+        m = mn;
+      }
+      bad = __any_sync(kFull, bad);
+      for (int pi = lane; pi < np; pi += 32) {
+        const float mi = wm[pi * nrs + ri];
+        wm[pi * nrs + ri] = (mi == -INFINITY) ? 0.f : ex2(mi - m);  // NaN for a poisoned piece
+      }
+      if (lane == 0) lr[ri] = bad ? __int_as_float(0x7fc00000) : l;
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  consumer_sync(NT);  // the weights, l and every thread's copies are in shared memory
+  // the weighted sums of 4-output vectors; with fewer vectors than threads,
+  // ng threads split the pieces of each vector
+  const int ng = (nev >= NT || nev <= 0) ? 1 : cmin(np, NT / nev);
+  const float nan = __int_as_float(0x7fc00000);
+  auto store = [&](int v, float4 o) {
+    const int r2 = 4 * v / D, c = 4 * v % D, hh = r2 / GRP, j = r2 % GRP;
+    const float inv = 1.f / lr[r2 - rr0];
+    store_out4(p.out, row_index(p, b, kvh0 + hh, j) * D + c, fail ? nan : o.x * inv, fail ? nan : o.y * inv,
+               fail ? nan : o.z * inv, fail ? nan : o.w * inv, p.out_dtype);
+  };
+  if (ng == 1) {
+    for (int v = v0 + tid; v < v1; v += NT) {
+      const int r2 = 4 * v / D;
+      if ((r2 % GRP) >= p.rows) continue;
+      const int x = off(v) - a0, wi = r2 - rr0;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int pi = 0; pi < np; ++pi)
+        o = fma4(wm[pi * nrs + wi], *reinterpret_cast<const float4*>(so + (size_t)pi * span + x), o);
+      store(v, o);
+    }
+  } else {
+    const int ei = tid % nev, jg = tid / nev;
+    const int v = v0 + ei, r2 = 4 * v / D;
+    const bool vlive = (r2 % GRP) < p.rows;
+    if (jg < ng && vlive) {
+      const int x = off(v) - a0, wi = r2 - rr0;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int pi = jg; pi < np; pi += ng)
+        o = fma4(wm[pi * nrs + wi], *reinterpret_cast<const float4*>(so + (size_t)pi * span + x), o);
+      part4[jg * nev + ei] = o;
+    }
+    consumer_sync(NT);
+    if (tid < nev && vlive) {
+      float4 o = part4[tid];
+      for (int k2 = 1; k2 < ng; ++k2) {
+        const float4 x = part4[k2 * nev + tid];
+        o = make_float4(o.x + x.x, o.y + x.y, o.z + x.z, o.w + x.w);
+      }
+      store(v, o);
+    }
+  }
+}
+
 template <int D, int T, int GRP, typename E, int HP>
 __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t* full, uint64_t* empty, uint64_t* stg,
                                         float* mrg, volatile int* abort_flag, uint32_t epoch) {
@@ -1173,9 +1360,16 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
       }
     }
     const bool poisoned = (*abort_flag != 0) || !ok;
+    // a piece of a unit whose merge every CTA ending on one of its pieces
+    // shares (merge_unit_shared, after the loop): every piece writes a
+    // record, the CTA's last segment in slot G + g
+    const bool split = kind == kHost || kind == kNonHost;
+    const bool shared =
+        split && merged_shared<C>(p, kind == kHost ? g : p.segs[(size_t)si * kDevSegWords + 11], peer);
 
-    if (kind == kNonHost || kind == kPartial) {
-      float* rec = p.recs + (size_t)g * C::RS;
+    if (kind == kNonHost || kind == kPartial || shared) {
+      const int slot = (shared && si == s_end - 1) ? p.G + g : g;
+      float* rec = p.recs + (size_t)slot * C::RS;
 #pragma unroll
       for (int i = 0; i < C::V4; ++i) {
         const int v = tid + i * C::NCT;
@@ -1187,9 +1381,12 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
             *reinterpret_cast<float4*>(r) = make_float4(poisoned ? __int_as_float(0x7fc00000) : M[i], Lsum[i], 0.f, 0.f);
         }
       }
-      __threadfence();
+      // the barrier orders every thread's record stores before thread 0's
+      // release store, which is cumulative at gpu scope: a CTA that
+      // acquires the flag sees the whole record (no fence per thread)
       consumer_sync(C::NCT);
-      if (kind == kNonHost && tid == 0 && g != p.skip_signal) st_release_gpu(&p.flags[g], ready);
+      if (kind != kPartial && tid == 0 && !(g == p.skip_signal && si == s_begin))
+        st_release_gpu(&p.flags[slot], ready);
     } else {
       bool fail = poisoned;
       if (kind == kHost) {
@@ -1267,6 +1464,16 @@ __device__ __forceinline__ void consume(const KParams& p, int g, E* kv, uint64_t
       }
     }
     consumer_sync(C::NCT);  // the merge area is rewritten by the next segment
+  }
+  // The CTA's last segment, when a piece of a unit merged shared: this CTA's
+  // share of the unit's outputs. Called here, after the segment loop, so
+  // that no state of the loop is live across the call.
+  if (s_end > s_begin) {
+    const int* w = p.segs + (size_t)(s_end - 1) * kDevSegWords;
+    const int kind = w[3], fin = w[4], host = w[11];
+    if ((kind == kHost || kind == kNonHost) && merged_shared<C>(p, host, fin))
+      merge_unit_shared<C>(p, g, host, fin, w[0] / groups, (w[0] % groups) * HP, reinterpret_cast<float*>(kv),
+                           abort_flag, ready);
   }
 }
 

@@ -53,9 +53,11 @@ struct Layout {
   size_t cu, cta_seg, segs, host, fin, total;
 };
 
-Layout layout_of(const la_schedule* s) {
+// shared: two record slots per CTA where the instance can merge split units
+// shared (la::record_slots); false: one, every unit merged at its host.
+Layout layout_of(const la_schedule* s, bool shared) {
   Layout L;
-  L.ws = la::workspace_layout(s->G, s->d, s->R * s->hp);  // header, flags and records as in a workspace
+  L.ws = la::workspace_layout(s->G, s->d, s->R * s->hp, shared);  // header, flags and records as in a workspace
   size_t off = la::align_up(L.ws.end, 256);
   auto table = [&off](size_t words) {
     const size_t at = off;
@@ -92,7 +94,14 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f) return LA_ERR_INVALID;
   const la_schedule* s = sc;
   if (s->hp != 1) return LA_ERR_UNSUPPORTED;  // units of several kv heads read token-major or paged caches
-  const Layout L = layout_of(s);
+  // Where the second record slot per CTA of a shared merge does not fit,
+  // the 16-row kernel merges every split unit at its host (one slot).
+  bool shared = true;
+  Layout L = layout_of(s, true);
+  if (L.total > kStaticScratchBytes && s->R < la::kWideInstanceRows) {
+    L = layout_of(s, false);
+    shared = false;
+  }
   if (L.total > kStaticScratchBytes) return LA_ERR_WORKSPACE;  // schedule too large for the fixed array
 
   if (s->kind == 0) {  // host CTAs wait on later CTAs: all of the grid must be resident
@@ -157,6 +166,7 @@ extern "C" la_status la_decode_static(const void* q, const void* k, const void* 
   p.rows = s->unit_grp() * s->nq;
   p.stages = s->stages > 0 ? s->stages
                            : (s->kind == 0 && s->R <= 16 ? la::stream_stages(s->d, s->T, s->hp, la::kKvSlab) : 0);
+  p.shared_pieces = shared ? la::shared_merge_pieces(s->R * s->hp) : 0;
   cudaError_t ce = la::launch_decode(s->d, s->T, s->R, 1, dtype, p, st);
   if (ce != cudaSuccess) return LA_ERR_CUDA;
   if (s->kind == 1 && s->splits > 1) {

@@ -16,8 +16,9 @@
  * over G CTAs, which may cross head and request boundaries; each CTA
  * produces partial results (m, l, unscaled O) that the unit's host CTA
  * merges with the rescaling reduction f and normalises, all in one launch
- * (for units of more than 16 query rows every CTA that ends on a piece of
- * the unit merges an equal share of its outputs instead).
+ * (for units of more than 16 query rows, and for units of 4-16 rows whose
+ * host would read at least 96 KiB of records, every CTA that ends on a
+ * piece of the unit merges an equal share of its outputs instead).
  *
  * Data layout (device memory, row-major, no padding):
  *   q    [batch, hq, d]                         fp16 or bf16
@@ -206,12 +207,14 @@ int la_schedule_grid(const la_schedule* s);
  * Bytes of device workspace la_decode needs for this schedule: a 256-byte
  * header, ready flags (padded to 256 bytes) and partial records, one flag
  * per record ("7.4 limitations": a small amount of global memory for
- * sharing partial results). The 16-row kernel has G records of rows rows of
+ * sharing partial results). The 16-row kernel has records of rows rows of
  * [m, l, 0, 0, O[d]] floats (rows = query rows per unit head -- a kv head
  * or one query block of one -- rounded up to 1, 2, 4, 8 or 16, times the kv
- * heads per unit); the tcgen05 kernel (128 rows) 2 G records of the same
- * triples column-major over the rows, rounded up to a multiple of 4 floats
- * (every piece of a split unit writes one, and a CTA can hold two). Zero it
+ * heads per unit): G of them below 4 rows, 2 G from 4 rows (a unit split
+ * into many pieces is then merged by every CTA that ends on one of them, so
+ * each piece writes a record and a CTA can hold two); the tcgen05 kernel
+ * (128 rows) 2 G records of the same triples column-major over the rows,
+ * rounded up to a multiple of 4 floats. Zero it
  * once (la_workspace_init) before its first use; after that it needs no
  * clearing between calls. One workspace must not be used by two launches
  * that can run at the same time.
@@ -354,6 +357,9 @@ la_status la_plan_kv(int batch, int hq, int hkv, int d, int nq, const int32_t* c
  *   - A schedule whose scratch does not fit in 4 MiB is rejected with
  *     LA_ERR_WORKSPACE before anything is enqueued (about 7,000 CTA records
  *     at d = 128 without query-head grouping; use la_decode for more).
+ *     Where the second record per CTA of the shared merge (see
+ *     la_workspace_size) does not fit but one does, every split unit is
+ *     merged at its host instead.
  *   - The first call on a device looks up the array's address on that
  *     device (cudaGetSymbolAddress) with the device current; make that
  *     first call before any stream capture.

@@ -174,8 +174,12 @@ def test_workspace_size_formula():
     # header 256 + flags (3 words padded to 256) + 3 records of 1 row of
     # [m, l, 0, 0, O[64]] (68 floats)
     assert la.la_workspace_size(s) == 256 + 256 + 3 * 68 * 4
+    # group 8: records of 8 rows, two slots per CTA (from 4 rows a split unit
+    # of enough pieces is merged by every CTA that ends on one of them)
     g = la.la_plan(2, 16, 2, 128, [0, 100, 300], 5)
-    assert la.la_workspace_size(g) == 256 + 256 + 5 * 8 * 132 * 4
+    assert la.la_workspace_size(g) == 256 + 256 + 2 * 5 * 8 * 132 * 4
+    two = la.la_plan(2, 4, 2, 128, [0, 100, 300], 5)  # group 2: one slot per CTA
+    assert la.la_workspace_size(two) == 256 + 256 + 5 * 2 * 132 * 4
 
 
 def test_export_size_and_short_buffer():
@@ -263,8 +267,9 @@ def test_spec_schedule_matches_the_decode_plan_and_sizes_its_records():
     s = la.la_plan_spec(3, 4, 2, 128, 3, cu_of(lengths), 11)
     assert s.nq == 3
     assert la.la_schedule_export(s) == P.export(P.plan_lean(3, 4, 2, 128, cu_of(lengths), 11))
-    # grp 2 x nq 3 = 6 query rows per unit: records of 8 rows (the instance's row count)
-    assert la.la_workspace_size(s) == 256 + 256 + 11 * 8 * 132 * 4
+    # grp 2 x nq 3 = 6 query rows per unit: records of 8 rows (the instance's
+    # row count), two slots per CTA
+    assert la.la_workspace_size(s) == 256 + 256 + 2 * 11 * 8 * 132 * 4
 
 
 @pytest.mark.parametrize("hq,hkv,nq,lengths,status", [
@@ -327,7 +332,7 @@ def test_two_head_records_hold_both_heads():
     # d 64, grp 4, nq 2: 8 query rows per kv head, two kv heads per unit
     s = la.la_plan_kv(2, 16, 4, 64, [0, 300, 700], nq=2, num_sms=9)
     assert s.heads_per_unit == 2
-    assert la.la_workspace_size(s) == 256 + 256 + 9 * 2 * 8 * 68 * 4
+    assert la.la_workspace_size(s) == 256 + 256 + 2 * 9 * 2 * 8 * 68 * 4  # 16 rows: two slots per CTA
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -378,10 +383,10 @@ def test_sixteen_query_rows_per_kv_head():
     # group 16 (and group x query tokens up to 16) plans like any other group
     s = la.la_plan(2, 32, 2, 128, [0, 900, 1000], 7)
     assert la.la_schedule_export(s) == P.export(P.plan_lean(2, 32, 2, 128, [0, 900, 1000], 7, 128))
-    # records hold 16 rows of (d + 2) floats
-    assert la.la_workspace_size(s) == 256 + 256 + 7 * 16 * 132 * 4
+    # records hold 16 rows of (d + 4) floats, two slots per CTA
+    assert la.la_workspace_size(s) == 256 + 256 + 2 * 7 * 16 * 132 * 4
     sp = la.la_plan_spec(2, 16, 2, 64, 2, [0, 900, 1000], 7)
-    assert la.la_workspace_size(sp) == 256 + 256 + 7 * 16 * 68 * 4
+    assert la.la_workspace_size(sp) == 256 + 256 + 2 * 7 * 16 * 68 * 4
     # caches: units of one kv head once a kv head has more than 8 rows
     assert la.la_plan_kv(1, 32, 2, 64, [0, 900], num_sms=7).heads_per_unit == 1
     assert la.la_plan_kv(1, 16, 2, 64, [0, 900], num_sms=7).heads_per_unit == 2
@@ -394,7 +399,8 @@ def test_groups_that_are_not_powers_of_two(grp):
     s = la.la_plan(3, 2 * grp, 2, 128, cu_of(lengths), 11)
     assert la.la_schedule_export(s) == P.export(P.plan_lean(3, 2 * grp, 2, 128, cu_of(lengths), 11, 128))
     R = 4 if grp <= 4 else 8 if grp <= 8 else 16
-    assert la.la_workspace_size(s) == 256 + 256 + 11 * R * 132 * 4
+    slots = 11 if R < 4 else 2 * 11
+    assert la.la_workspace_size(s) == 256 + 256 + slots * R * 132 * 4
 
 
 # ---- query blocks: more query rows per kv head than one unit holds
@@ -426,11 +432,11 @@ def test_query_blocks_are_units_of_their_own(d, grp, nq, qb, R):
     s = la.la_plan_spec(3, hkv * grp, hkv, d, nq, cu_of(lengths), G)
     assert s.query_blocks == qb and s.heads_per_unit == 1
     assert la.la_schedule_export(s) == P.export(P.plan_lean(3, hkv * grp, hkv * qb, d, cu_of(lengths), G, T))
-    # a record: R rows of [m, l, 0, 0, O[d]] on the 16-row kernel, one per
-    # CTA; on the tcgen05 kernel (R = 128) columns over the rows, padded to
-    # 16 bytes, two per CTA (with a ready flag each)
+    # a record: R rows of [m, l, 0, 0, O[d]] on the 16-row kernel; on the
+    # tcgen05 kernel (R = 128) columns over the rows, padded to 16 bytes;
+    # two per CTA (with a ready flag each) from 4 rows on
     rec = R * (d + 4) if R < 128 else -(-R * (d + 2) // 4) * 4
-    slots = G if R < 128 else 2 * G
+    slots = G if R < 4 else 2 * G
     assert la.la_workspace_size(s) == 256 + 256 + slots * rec * 4
     if nq == 1:
         assert la.la_schedule_export(la.la_plan(3, hkv * grp, hkv, d, cu_of(lengths), G)) \

@@ -105,6 +105,24 @@ def _decode_both(w, q, k, v, cu, sched):
 
 
 @pytest.mark.gpu
+def test_static_scratch_merges_at_the_host_when_two_record_slots_do_not_fit():
+    # d 256, group 16, every SM: two record slots per CTA (the shared merge
+    # of split units) need 5.1 MB, one slot fits; the call merges every
+    # split unit at its host instead and matches the oracle
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    w = workloads.custom(1, 32, 2, 256, "bf16", [20000])
+    q, k, v, _ = workloads.make_inputs(w, seed=17, device="cuda")
+    cu = torch.as_tensor(w.cu, dtype=torch.int32, device="cuda")
+    sched = la.la_plan(w.batch, w.hq, w.hkv, w.d, w.cu, 0)
+    assert la.la_workspace_size(sched) > 4 << 20
+    out, ref = _decode_both(w, q, k, v, cu, sched)
+    _close(out, ref)
+    compare(out.cpu(), reference(w, q, k, v))
+
+
+@pytest.mark.gpu
 def test_static_scratch_after_a_larger_schedule_and_back():
     # A stream-K schedule over every SM with many split units leaves flags,
     # records and tables in the array; a smaller, different schedule follows,
