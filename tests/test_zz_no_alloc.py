@@ -9,7 +9,9 @@ stops at the first failure has already run every other test. The GPU tests
 call the entry point through the C ABI and check it against la_decode and
 against the float64 oracle on two calls in a row (the array keeps the
 previous call's contents), after a larger schedule has left its flags,
-records and tables in the array, and when a bounded wait runs out."""
+records and tables in the array, where the second record slot per CTA of
+the shared merge does not fit (every split unit is then merged at its
+host), and when a bounded wait runs out."""
 import ctypes
 
 import numpy as np
