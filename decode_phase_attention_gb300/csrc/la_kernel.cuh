@@ -1146,7 +1146,7 @@ __device__ __noinline__ void merge_unit_shared(const KParams& p, int g, int h0, 
   const int nrs = nev > 0 ? 4 * (v1 - 1) / D - rr0 + 1 : 0;
   const int a0 = off(v0), span = nev > 0 ? off(v1 - 1) + 4 - a0 : 0;
   // shared memory (the idle ring and merge area)
-  float4* part4 = reinterpret_cast<float4*>(sm);  // [NT] partial sums of phase 2
+  float4* part4 = reinterpret_cast<float4*>(sm);  // [NT] partial weighted sums (threads splitting a vector's pieces)
   float* so = sm + 4 * NT;                        // [np][span]: every piece's part
   float* wm = so + (size_t)np * span;             // [np][nrs]: m of every piece, then its weight
   float* lr = wm + (size_t)np * nrs;              // [nrs]: the row sums l
